@@ -1,0 +1,180 @@
+"""Seeded synthetic inputs for prompt-lookup drafting.
+
+This module only draws token histories; it holds none of the drafting
+arithmetic, so both the CUDA path's tests and the CPU oracle take their inputs
+from here without sharing any of the method's code.
+
+A batch is a CSR pair: ``tokens`` (int32, the histories concatenated) and
+``offsets`` (int64, B+1 entries, request r is tokens[offsets[r]:offsets[r+1]]).
+
+The five named workloads stand in for the workloads of the pages, whose corpora
+are not available here: HyperQwen's 25k-token verbatim recitation and short
+chats, and list-like periodic text (HyperQwen lookup-drafting article,
+sections "先看效果" and "第1步").  Every random choice goes through numpy's
+PCG64 generator seeded with (seed, workload index).
+"""
+from __future__ import annotations
+
+import dataclasses
+import functools
+
+import numpy as np
+
+VOCAB_QWEN = 151936   # vocabulary size of the Qwen tokenizer the pages' models use
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    tokens: np.ndarray          # int32 [offsets[-1]]
+    offsets: np.ndarray         # int64 [B + 1]
+    min_m: int
+    max_m: int
+    K: int
+    seed: int
+    planted: dict               # request -> (source start s0, copy length c)
+
+    @property
+    def B(self) -> int:
+        return int(self.offsets.shape[0]) - 1
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.offsets[-1] - self.offsets[0])
+
+    @property
+    def history_bytes(self) -> int:
+        return 4 * self.total_tokens
+
+
+WORKLOADS = ("tiny", "recitation25k", "periodic", "ragged262k", "chats")
+DEFAULT_SEED = {"tiny": 1, "recitation25k": 2, "periodic": 3, "ragged262k": 4, "chats": 5}
+
+DESCRIPTION = {
+    "tiny": "B=8, L=4096, uniform vocab 32000; 4 requests end in a 64-token copy of a "
+            "span starting in [500,3000); min_m=4 max_m=12 K=15",
+    "recitation25k": "B=64, L=25000, Zipf(1.1) over vocab 151936 (permuted); 30% of requests "
+                     "end 1-2000 tokens into a copy of an earlier 2000-token span; "
+                     "min_m=4 max_m=12 K=15",
+    "periodic": "B=64, L=8192, runs of random periods 3-40 (run length 50-500), 5% uniform "
+                "mutations, vocab 151936; min_m=4 max_m=12 K=7",
+    "ragged262k": "B=256, L log-uniform in [512, 262144], Zipf(1.1); 20% end in a copy of an "
+                  "earlier 1-4k span; min_m=4 max_m=12 K=15",
+    "chats": "B=4096, L=2048, Zipf(1.2); 10% end in a 32-256-token copy of an earlier span; "
+             "min_m=4 max_m=12 K=7",
+}
+
+
+def rng_for(seed: int, stream: int = 0) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64([int(seed), int(stream)]))
+
+
+@functools.lru_cache(maxsize=8)
+def _zipf_cdf(vocab: int, s: float) -> np.ndarray:
+    ranks = np.arange(1, vocab + 1, dtype=np.float64)
+    w = ranks ** (-s)
+    cdf = np.cumsum(w)
+    cdf /= cdf[-1]
+    return cdf
+
+
+def zipf_tokens(rng: np.random.Generator, n: int, vocab: int, s: float,
+                perm: np.ndarray) -> np.ndarray:
+    """n tokens with P(rank k) proportional to k^-s, rank k mapped to token perm[k-1]."""
+    cdf = _zipf_cdf(vocab, s)
+    u = rng.random(n)
+    idx = np.searchsorted(cdf, u, side="right")
+    np.minimum(idx, vocab - 1, out=idx)
+    return perm[idx].astype(np.int32)
+
+
+def uniform_tokens(rng: np.random.Generator, n: int, vocab: int) -> np.ndarray:
+    return rng.integers(0, vocab, size=n, dtype=np.int64).astype(np.int32)
+
+
+def offsets_from_lengths(lengths) -> np.ndarray:
+    lengths = np.asarray(lengths, dtype=np.int64)
+    return np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+
+
+def plant_copy(hist: np.ndarray, s0: int, c: int) -> None:
+    """Make the history end in a verbatim copy of hist[s0 : s0 + c] (in place)."""
+    L = hist.shape[0]
+    assert 0 <= s0 and s0 + c <= L - c, (s0, c, L)
+    hist[L - c:] = hist[s0:s0 + c]
+
+
+def _choose(rng: np.random.Generator, B: int, frac: float) -> np.ndarray:
+    n = int(round(frac * B))
+    return np.sort(rng.permutation(B)[:n])
+
+
+def make_workload(name: str, seed: int | None = None) -> Workload:
+    if name not in WORKLOADS:
+        raise KeyError(f"unknown workload {name!r}; known: {WORKLOADS}")
+    seed = DEFAULT_SEED[name] if seed is None else int(seed)
+    rng = rng_for(seed, WORKLOADS.index(name))
+    planted: dict = {}
+
+    if name == "tiny":
+        B, L = 8, 4096
+        tokens = uniform_tokens(rng, B * L, 32000)
+        offsets = offsets_from_lengths([L] * B)
+        for r in _choose(rng, B, 0.5):
+            s0 = int(rng.integers(500, 3000))
+            plant_copy(tokens[r * L:(r + 1) * L], s0, 64)
+            planted[int(r)] = (s0, 64)
+        return Workload(name, tokens, offsets, 4, 12, 15, seed, planted)
+
+    if name == "periodic":
+        B, L = 64, 8192
+        rows = []
+        for _ in range(B):
+            parts, n = [], 0
+            while n < L:
+                d = int(rng.integers(3, 41))
+                run = int(rng.integers(50, 501))
+                pattern = uniform_tokens(rng, d, VOCAB_QWEN)
+                parts.append(np.resize(pattern, run))
+                n += run
+            h = np.concatenate(parts)[:L].copy()
+            flip = rng.random(L) < 0.05
+            h[flip] = uniform_tokens(rng, int(flip.sum()), VOCAB_QWEN)
+            rows.append(h)
+        tokens = np.concatenate(rows).astype(np.int32)
+        offsets = offsets_from_lengths([L] * B)
+        return Workload(name, tokens, offsets, 4, 12, 7, seed, planted)
+
+    perm = rng.permutation(VOCAB_QWEN).astype(np.int64)
+    if name == "recitation25k":
+        B, s, frac = 64, 1.1, 0.3
+        lengths = np.full(B, 25000, dtype=np.int64)
+        K = 15
+    elif name == "ragged262k":
+        B, s, frac = 256, 1.1, 0.2
+        lengths = np.floor(np.exp(rng.uniform(np.log(512), np.log(262144), size=B))).astype(np.int64)
+        K = 15
+    else:  # chats
+        B, s, frac = 4096, 1.2, 0.1
+        lengths = np.full(B, 2048, dtype=np.int64)
+        K = 7
+    offsets = offsets_from_lengths(lengths)
+    tokens = zipf_tokens(rng, int(offsets[-1]), VOCAB_QWEN, s, perm)
+    for r in _choose(rng, B, frac):
+        r = int(r)
+        L = int(lengths[r])
+        if name == "recitation25k":
+            span = 2000
+            c = int(rng.integers(1, 2001))
+            s0 = int(rng.integers(0, L - c - span + 1))
+        elif name == "ragged262k":
+            c = int(rng.integers(1024, 4097))
+            c = min(c, L // 2 - 1)
+            s0 = int(rng.integers(0, L - 2 * c + 1))
+        else:
+            c = int(rng.integers(32, 257))
+            s0 = int(rng.integers(0, L - 2 * c + 1))
+        h = tokens[offsets[r]:offsets[r + 1]]
+        plant_copy(h, s0, c)
+        planted[r] = (s0, c)
+    return Workload(name, tokens, offsets, 4, 12, K, seed, planted)

@@ -1,0 +1,106 @@
+"""The oracle's pins are strong enough to catch plausible mistakes.
+
+Each case below plants one mistake in a copy of the oracle's C source (a wrong
+loop direction, an off-by-one bound, a dropped comparison, a wrong sentinel ...),
+compiles the copy with gcc into a temporary library, and runs the pins of
+test_oracle_pins.py against it through the same ctypes wrapper.  Every mutant
+must fail at least one pin.  The mistakes are planted on the CPU only; the real
+oracle is never modified.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import gen
+import oracle
+from goldens import load_cases
+from invariants import check_small
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "lookup_oracle.c")
+
+MUTANTS = {
+    "oldest_first": ("for (int64_t p = L - m - 1; p >= 0; --p)",
+                     "for (int64_t p = 0; p <= L - m - 1; ++p)"),
+    "no_overlap": ("for (int64_t p = L - m - 1; p >= 0; --p)",
+                   "for (int64_t p = L - 2 * m; p >= 0; --p)"),
+    "suffix_counts_as_earlier": ("for (int64_t p = L - m - 1; p >= 0; --p)",
+                                 "for (int64_t p = L - m; p >= 0; --p)"),
+    "shortest_first": ("for (int64_t m = top; m >= (int64_t)min_m; --m)",
+                       "for (int64_t m = (int64_t)min_m; m <= top; ++m)"),
+    "min_m_excluded": ("for (int64_t m = top; m >= (int64_t)min_m; --m)",
+                       "for (int64_t m = top; m > (int64_t)min_m; --m)"),
+    "cap_too_low": ("top = L - 1;", "top = L - 2;"),
+    "max_m_ignored": ("int64_t top = (int64_t)max_m;", "int64_t top = L - 1 + 0 * max_m;"),
+    "first_token_skipped": ("if (t[a + i] != t[b + i])", "if (i > 0 && t[a + i] != t[b + i])"),
+    "last_token_skipped": ("for (int64_t i = 0; i < n; ++i)", "for (int64_t i = 0; i + 1 < n; ++i)"),
+    "no_self_extension": ("draft[j] = (src < L) ? t[src] : draft[src - L];",
+                          "draft[j] = (src < L) ? t[src] : t[L - 1];"),
+    "draft_off_by_one": ("int64_t src = p + m + j;", "int64_t src = p + m + j - 1;"),
+    "wrong_position": ("out_pos[r] = (int32_t)p;", "out_pos[r] = (int32_t)(p + m);"),
+    "wrong_sentinel": ("out_pos[r] = -1;", "out_pos[r] = 0;"),
+    "short_draft_length": ("out_len[r] = K;", "out_len[r] = K - 1;"),
+}
+
+
+def _pins_fail(lib) -> list[str]:
+    """Run the pins against a library; return the names of those that fail."""
+    failed = []
+
+    def run(tokens, offsets, min_m, max_m, K):
+        return oracle.lookup_draft(tokens, offsets, min_m, max_m, K, lib=lib)
+
+    for c in load_cases():
+        d, ln, p, m = run(c.tokens, c.offsets, c.min_m, c.max_m, c.K)
+        if not (np.array_equal(m, c.expect_m) and np.array_equal(p, c.expect_pos)
+                and np.array_equal(ln, c.expect_len) and np.array_equal(d, c.expect_draft)):
+            failed.append(f"golden:{c.name}")
+    w = gen.make_workload("tiny")
+    d, ln, p, m = run(w.tokens, w.offsets, w.min_m, w.max_m, w.K)
+    for r, (s0, c) in w.planted.items():
+        t = w.tokens[w.offsets[r]:w.offsets[r + 1]]
+        if (m[r], p[r], ln[r]) != (12, s0 + c - 12, 15) or \
+                not np.array_equal(d[r], t[s0 + c:s0 + c + 15]):
+            failed.append("planted")
+            break
+    for dd in (1, 3, 7):
+        a = np.arange(dd, dtype=np.int32) + 50
+        L = dd + 12 + 5
+        t = a[np.arange(L) % dd]
+        d, ln, p, m = run(t, np.array([0, L], np.int64), 4, 12, 15)
+        if (m[0], p[0]) != (12, L - 12 - dd) or \
+                not np.array_equal(d[0], a[(L + np.arange(15)) % dd]):
+            failed.append(f"periodic:{dd}")
+    import itertools
+    hists = [list(s) for L in range(0, 9) for s in itertools.product(range(2), repeat=L)]
+    tokens = np.array([x for h in hists for x in h], dtype=np.int32)
+    offsets = gen.offsets_from_lengths([len(h) for h in hists])
+    for (min_m, max_m, K) in [(1, 3, 5), (2, 4, 1)]:
+        d, ln, p, m = run(tokens, offsets, min_m, max_m, K)
+        for r, h in enumerate(hists):
+            if check_small(h, min_m, max_m, K, int(m[r]), int(p[r]), int(ln[r]), d[r]):
+                failed.append(f"exhaustive:{min_m},{max_m}")
+                break
+    return failed
+
+
+def test_unmutated_oracle_passes_the_pins():
+    assert _pins_fail(oracle.load()) == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC, encoding="utf-8").read()
+    assert src.count(old) >= 1, f"mutation target for {name} not found in the oracle"
+    mutated = src.replace(old, new, 1)
+    c_path = tmp_path / "mutant.c"
+    so_path = tmp_path / "libmutant.so"
+    c_path.write_text(mutated, encoding="utf-8")
+    subprocess.run(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", "-o", str(so_path),
+                    str(c_path)], check=True)
+    failed = _pins_fail(oracle.load(str(so_path)))
+    assert failed, f"mutant {name} passed every pin"
