@@ -1,0 +1,165 @@
+/*
+ * lookup_draft.h -- C ABI of the GB300 prompt-lookup (n-gram) drafting library.
+ *
+ * The operation (HyperQwen lookup-drafting article, kwkr.cn/news/564408, section
+ * "第1步"): before a decode step, every request of a batch scans its own token
+ * history for the most recent earlier occurrence of its longest current suffix,
+ * trying suffix lengths from max_m down to min_m (the article uses 12 .. 4); the
+ * occurrence may overlap the suffix, so periodic text (list items, indentation,
+ * code fences) matches its own period.  The K tokens that follow the occurrence
+ * are the draft.  The draft is read from the history extended by its own draft,
+ * e[L + j] = e[p + m + j], so a match that runs into the suffix continues the
+ * period.
+ *
+ * Precisely, for request r with history t[0..L):
+ *   (m, p) = the largest m in [min_m, min(max_m, L-1)], then the largest p, such
+ *            that p + m <= L - 1 and t[p .. p+m) == t[L-m .. L);
+ *   found:    out_len[r] = K, out_pos[r] = p, out_mlen[r] = m,
+ *             out_draft[r*K + j] = t[p + m + (j mod (L - p - m))] for j < K;
+ *   none:     out_len[r] = 0, out_pos[r] = -1, out_mlen[r] = 0,
+ *             out_draft[r*K + j] = -1.
+ * Tokens compare as raw int32 values; a match never leaves its own request.
+ *
+ * Batch layout (CSR): request r's history is tokens[offsets[r] .. offsets[r+1]).
+ * offsets has B+1 non-decreasing int64 entries, offsets[0] >= 0 (it need not be
+ * 0), and every history is shorter than 2^31 tokens.  These preconditions are
+ * not checked on the device pointers (the host never reads them); violating
+ * them gives undefined results.  tokens needs only int32 alignment.
+ *
+ * Execution: every call enqueues its work on `stream` (NULL = the legacy
+ * default stream) and returns without synchronising, except lookup_draft_host.
+ * Device pointers must be valid on the current device.  The library keeps no
+ * pointer to caller memory after a call returns.  Calls are thread-safe.
+ *
+ * Return codes: LOOKUP_DRAFT_OK, or a negative LOOKUP_DRAFT_E* code.  A call that
+ * returns an error may have enqueued nothing or part of its work; its outputs
+ * are then unspecified.  Work that fails on the device after a successful return
+ * is reported per request: out_len[r] = LOOKUP_DRAFT_LEN_FAILED.
+ */
+#ifndef LOOKUP_DRAFT_H
+#define LOOKUP_DRAFT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                     /* same type as cudaStream_t */
+
+#define LOOKUP_DRAFT_MAX_M 32           /* largest accepted max_m */
+#define LOOKUP_DRAFT_MAX_K 64           /* largest accepted K */
+
+#define LOOKUP_DRAFT_OK 0
+#define LOOKUP_DRAFT_EINVAL (-1)        /* arguments do not describe a valid step */
+#define LOOKUP_DRAFT_ECUDA (-2)         /* a CUDA call failed; see lookup_draft_last_cuda_error */
+
+#define LOOKUP_DRAFT_LEN_FAILED (-1)    /* out_len value: the scan for this request did not
+                                           complete (a bounded wait on the device ran out) */
+
+/*
+ * One batched draft step (HyperQwen lookup-drafting article, section "第1步").
+ *
+ * tokens     device, int32 [offsets[B]]   concatenated histories (read only)
+ * offsets    device, int64 [B + 1]        CSR boundaries (read only)
+ * B          number of requests, >= 0; B == 0 enqueues nothing and returns OK
+ * min_m      shortest suffix tried, 1 <= min_m <= max_m
+ * max_m      longest suffix tried, max_m <= LOOKUP_DRAFT_MAX_M
+ * K          draft tokens per request, 0 <= K <= LOOKUP_DRAFT_MAX_K
+ * out_draft  device, int32 [B * K], row-major (may be NULL when K == 0)
+ * out_len    device, int32 [B]: K on a match, 0 without, LOOKUP_DRAFT_LEN_FAILED
+ * out_pos    device, int32 [B]: start p of the occurrence in the request, or -1
+ * stream     CUDA stream all work is enqueued on
+ *
+ * Scratch: B + (number of scan CTAs) 64-bit words, taken from and returned to a
+ * library-owned, stream-ordered CUDA memory pool of the current device.
+ * Errors: LOOKUP_DRAFT_EINVAL for null pointers (with B > 0), bad m range, K out of
+ * range, or misaligned tokens/offsets; LOOKUP_DRAFT_ECUDA when an allocation or
+ * launch fails.
+ */
+int lookup_draft(const int32_t *tokens, const int64_t *offsets, int32_t B,
+                 int32_t min_m, int32_t max_m, int32_t K,
+                 int32_t *out_draft, int32_t *out_len, int32_t *out_pos,
+                 struct CUstream_st *stream);
+
+/*
+ * lookup_draft plus the match length: out_mlen (device, int32 [B], may be NULL)
+ * receives m, or 0 when there is no match.  The article's fusion rules (section
+ * "第2步") key on this length.
+ */
+int lookup_draft_ex(const int32_t *tokens, const int64_t *offsets, int32_t B,
+                    int32_t min_m, int32_t max_m, int32_t K,
+                    int32_t *out_draft, int32_t *out_len, int32_t *out_pos,
+                    int32_t *out_mlen, struct CUstream_st *stream);
+
+/*
+ * Bytes of caller-provided scratch that lookup_draft_scan / lookup_draft_fill need
+ * for a batch of B requests on the current device (a function of B and the
+ * device's SM count).  Returns 0 when B < 0 or the device cannot be queried.
+ */
+size_t lookup_draft_workspace_bytes(int32_t B);
+
+/*
+ * The two stages of lookup_draft with caller-owned scratch, for callers that
+ * manage their own memory or want to time the stages.  Run lookup_draft_scan,
+ * then lookup_draft_fill with the same tokens, offsets, B, min_m and workspace,
+ * on the same device and in stream order.
+ *
+ * lookup_draft_scan: the split-history scan.  Every history token is read once;
+ *   each candidate end position tests the last suffix token first and extends
+ *   survivors backwards; the best (m, p) per request and per scan CTA is left in
+ *   `workspace` (device, >= lookup_draft_workspace_bytes(B) bytes, 8-byte aligned;
+ *   needs no initialisation).
+ * lookup_draft_fill: reduces those partial results and writes out_draft, out_len,
+ *   out_pos and (if not NULL) out_mlen exactly as lookup_draft_ex does.
+ * Errors as for lookup_draft, plus LOOKUP_DRAFT_EINVAL when the workspace is NULL,
+ * misaligned or too small.
+ */
+int lookup_draft_scan(const int32_t *tokens, const int64_t *offsets, int32_t B,
+                      int32_t min_m, int32_t max_m,
+                      void *workspace, size_t workspace_bytes,
+                      struct CUstream_st *stream);
+
+int lookup_draft_fill(const int32_t *tokens, const int64_t *offsets, int32_t B,
+                      int32_t min_m, int32_t max_m, int32_t K,
+                      const void *workspace, size_t workspace_bytes,
+                      int32_t *out_draft, int32_t *out_len, int32_t *out_pos,
+                      int32_t *out_mlen, struct CUstream_st *stream);
+
+/*
+ * lookup_draft on HOST buffers: copies tokens[offsets[0] .. offsets[B]) and the
+ * offsets to the current device (stream-ordered scratch from the library pool),
+ * runs the step on `stream`, copies the outputs back into the host arrays and
+ * synchronises the stream before returning.  Pinned host memory gives the
+ * fastest copies; pageable memory works.  The host offsets are checked
+ * (non-decreasing, offsets[0] >= 0, every history < 2^31 tokens):
+ * LOOKUP_DRAFT_EINVAL if not.
+ */
+int lookup_draft_host(const int32_t *h_tokens, const int64_t *h_offsets, int32_t B,
+                      int32_t min_m, int32_t max_m, int32_t K,
+                      int32_t *h_out_draft, int32_t *h_out_len, int32_t *h_out_pos,
+                      struct CUstream_st *stream);
+
+/* Static description of a return code (never NULL). */
+const char *lookup_draft_strerror(int code);
+
+/* Message of the CUDA error behind the calling thread's last LOOKUP_DRAFT_ECUDA
+ * ("" if none).  Valid until that thread's next call into the library. */
+const char *lookup_draft_last_cuda_error(void);
+
+/*
+ * Diagnostics: the limit, in nanoseconds, on each bounded wait inside the scan
+ * kernel (default 1e9).  When a wait runs out, the kernel waits again (with the
+ * default limit) for its own copies in flight, marks its requests
+ * LOOKUP_DRAFT_LEN_FAILED and returns, leaving the context usable.  Setting a
+ * tiny limit forces that path, to test that the failure reaches the host.
+ * Process-wide; applies to launches made after the call.  0 restores the default.
+ */
+void lookup_draft_set_wait_limit_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOOKUP_DRAFT_H */

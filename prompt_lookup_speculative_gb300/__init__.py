@@ -1,0 +1,247 @@
+"""GB300 prompt-lookup (n-gram) speculative drafting.
+
+Python binding of the C ABI in ``include/lookup_draft.h`` (ctypes; argument
+marshalling only -- every step of the draft runs in the library's CUDA kernels).
+PyTorch tensors supply device memory and the current CUDA stream.
+
+    draft, length, pos = lookup_draft(tokens, offsets, min_m=4, max_m=12, K=15)
+
+``tokens`` is an int32 CUDA tensor of concatenated histories and ``offsets`` an
+int64 CUDA tensor of B+1 CSR boundaries.  For each request the result is the
+longest current suffix (max_m .. min_m tokens) with a most recent earlier
+occurrence in the request's own history, overlap allowed, and the K tokens
+following it read from the self-extended history (HyperQwen lookup-drafting
+article, section "第1步").  There is no CPU fallback: if the compiled library is
+missing, importing the binding's functions raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+__all__ = [
+    "LookupDraftError", "load_library", "lookup_draft", "lookup_draft_ex", "lookup_draft_host",
+    "lookup_draft_scan", "lookup_draft_fill", "workspace_bytes", "set_wait_limit_ns",
+    "MAX_M", "MAX_K", "LEN_FAILED",
+]
+
+MAX_M = 32
+MAX_K = 64
+LEN_FAILED = -1
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+class LookupDraftError(RuntimeError):
+    def __init__(self, code: int, lib):
+        msg = lib.lookup_draft_strerror(code).decode()
+        cuda = lib.lookup_draft_last_cuda_error().decode()
+        super().__init__(f"lookup_draft failed ({code}: {msg}){': ' + cuda if cuda else ''}")
+        self.code = code
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load the compiled library (building it first if nvcc is available and it is stale)."""
+    global _lib
+    with _lib_lock:
+        if _lib is not None and path is None:
+            return _lib
+        if path is None:
+            path = _build.LIB_PATH
+            if not _build.up_to_date():
+                try:
+                    _build.build()
+                except Exception as exc:  # no toolchain: fail loudly, never fall back
+                    if not os.path.exists(path):
+                        raise RuntimeError(
+                            f"the CUDA library {path} is missing and could not be built: {exc}") from exc
+        if not os.path.exists(path):
+            raise RuntimeError(f"the CUDA library {path} is missing; run build() first")
+        lib = ctypes.CDLL(path)
+        _declare(lib)
+        if path == _build.LIB_PATH:
+            _lib = lib
+        return lib
+
+
+def _declare(lib: ctypes.CDLL) -> None:
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    lib.lookup_draft.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
+    lib.lookup_draft.restype = ctypes.c_int
+    lib.lookup_draft_ex.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
+    lib.lookup_draft_ex.restype = ctypes.c_int
+    lib.lookup_draft_workspace_bytes.argtypes = [i32]
+    lib.lookup_draft_workspace_bytes.restype = sz
+    lib.lookup_draft_scan.argtypes = [vp, vp, i32, i32, i32, vp, sz, vp]
+    lib.lookup_draft_scan.restype = ctypes.c_int
+    lib.lookup_draft_fill.argtypes = [vp, vp, i32, i32, i32, i32, vp, sz, vp, vp, vp, vp, vp]
+    lib.lookup_draft_fill.restype = ctypes.c_int
+    lib.lookup_draft_host.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
+    lib.lookup_draft_host.restype = ctypes.c_int
+    lib.lookup_draft_strerror.argtypes = [ctypes.c_int]
+    lib.lookup_draft_strerror.restype = ctypes.c_char_p
+    lib.lookup_draft_last_cuda_error.argtypes = []
+    lib.lookup_draft_last_cuda_error.restype = ctypes.c_char_p
+    lib.lookup_draft_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.lookup_draft_set_wait_limit_ns.restype = None
+
+
+def _check(rc: int, lib) -> None:
+    if rc != 0:
+        raise LookupDraftError(rc, lib)
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _as_batch(tokens, offsets):
+    import torch
+    if not (isinstance(tokens, torch.Tensor) and isinstance(offsets, torch.Tensor)):
+        raise TypeError("tokens and offsets must be torch tensors")
+    if tokens.dtype != torch.int32 or offsets.dtype != torch.int64:
+        raise TypeError("tokens must be int32 and offsets int64")
+    if not (tokens.is_cuda and offsets.is_cuda) or tokens.device != offsets.device:
+        raise ValueError("tokens and offsets must be CUDA tensors on the same device")
+    if not (tokens.is_contiguous() and offsets.is_contiguous()) or offsets.dim() != 1:
+        raise ValueError("tokens and offsets must be contiguous; offsets one-dimensional")
+    if offsets.numel() < 1:
+        raise ValueError("offsets needs B + 1 >= 1 entries")
+    return offsets.numel() - 1
+
+
+def _outputs(B: int, K: int, device, out, with_mlen: bool):
+    import torch
+    if out is None:
+        draft = torch.empty((B, K), dtype=torch.int32, device=device)
+        length = torch.empty(B, dtype=torch.int32, device=device)
+        pos = torch.empty(B, dtype=torch.int32, device=device)
+        mlen = torch.empty(B, dtype=torch.int32, device=device) if with_mlen else None
+        return draft, length, pos, mlen
+    draft, length, pos = out[:3]
+    mlen = out[3] if len(out) > 3 else None
+    for t, shape in ((draft, (B, K)), (length, (B,)), (pos, (B,))):
+        if t.dtype != torch.int32 or tuple(t.shape) != shape or not t.is_contiguous() or t.device != device:
+            raise ValueError("output tensors must be contiguous int32 [B, K], [B], [B] on the input device")
+    return draft, length, pos, mlen
+
+
+def lookup_draft(tokens, offsets, min_m: int = 4, max_m: int = 12, K: int = 15,
+                 out=None, stream=None):
+    """One batched draft step on the current (or given) stream; returns (draft, length, pos)."""
+    import torch
+    lib = load_library()
+    B = _as_batch(tokens, offsets)
+    draft, length, pos, _ = _outputs(B, K, tokens.device, out, False)
+    with torch.cuda.device(tokens.device):
+        rc = lib.lookup_draft(tokens.data_ptr(), offsets.data_ptr(), B, min_m, max_m, K,
+                              draft.data_ptr(), length.data_ptr(), pos.data_ptr(),
+                              _stream_handle(stream))
+    _check(rc, lib)
+    return draft, length, pos
+
+
+def lookup_draft_ex(tokens, offsets, min_m: int = 4, max_m: int = 12, K: int = 15,
+                    out=None, stream=None):
+    """lookup_draft plus the match length; returns (draft, length, pos, mlen)."""
+    import torch
+    lib = load_library()
+    B = _as_batch(tokens, offsets)
+    draft, length, pos, mlen = _outputs(B, K, tokens.device, out, True)
+    with torch.cuda.device(tokens.device):
+        rc = lib.lookup_draft_ex(tokens.data_ptr(), offsets.data_ptr(), B, min_m, max_m, K,
+                                 draft.data_ptr(), length.data_ptr(), pos.data_ptr(),
+                                 mlen.data_ptr() if mlen is not None else None,
+                                 _stream_handle(stream))
+    _check(rc, lib)
+    return draft, length, pos, mlen
+
+
+def workspace_bytes(B: int, device=None) -> int:
+    """Scratch bytes the staged calls need for B requests on a device."""
+    import torch
+    lib = load_library()
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        n = lib.lookup_draft_workspace_bytes(B)
+    if n == 0 and B >= 0:
+        raise LookupDraftError(-2, lib)
+    return int(n)
+
+
+def lookup_draft_scan(tokens, offsets, min_m: int, max_m: int, workspace, stream=None) -> None:
+    """Stage 1 (the scan) into a caller-owned uint8/any CUDA workspace tensor."""
+    import torch
+    lib = load_library()
+    B = _as_batch(tokens, offsets)
+    with torch.cuda.device(tokens.device):
+        rc = lib.lookup_draft_scan(tokens.data_ptr(), offsets.data_ptr(), B, min_m, max_m,
+                                   workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                   _stream_handle(stream))
+    _check(rc, lib)
+
+
+def lookup_draft_fill(tokens, offsets, min_m: int, max_m: int, K: int, workspace,
+                      out=None, stream=None, with_mlen: bool = False):
+    """Stage 2 (reduce + draft fill) from a workspace written by lookup_draft_scan."""
+    import torch
+    lib = load_library()
+    B = _as_batch(tokens, offsets)
+    draft, length, pos, mlen = _outputs(B, K, tokens.device, out, with_mlen)
+    with torch.cuda.device(tokens.device):
+        rc = lib.lookup_draft_fill(tokens.data_ptr(), offsets.data_ptr(), B, min_m, max_m, K,
+                                   workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                   draft.data_ptr(), length.data_ptr(), pos.data_ptr(),
+                                   mlen.data_ptr() if mlen is not None else None,
+                                   _stream_handle(stream))
+    _check(rc, lib)
+    return (draft, length, pos, mlen) if with_mlen else (draft, length, pos)
+
+
+def lookup_draft_host(tokens, offsets, min_m: int = 4, max_m: int = 12, K: int = 15,
+                      out=None, stream=None, device=None):
+    """The step on host (numpy or CPU torch) buffers; copies in, runs, copies out, syncs.
+
+    Returns numpy arrays (draft [B, K], length [B], pos [B]) unless ``out`` gives
+    host arrays to fill.
+    """
+    import numpy as np
+    import torch
+    lib = load_library()
+    tok = np.ascontiguousarray(tokens.numpy() if isinstance(tokens, torch.Tensor) else tokens,
+                               dtype=np.int32)
+    off = np.ascontiguousarray(offsets.numpy() if isinstance(offsets, torch.Tensor) else offsets,
+                               dtype=np.int64)
+    B = off.shape[0] - 1
+    if out is None:
+        out = (np.empty((B, K), np.int32), np.empty(B, np.int32), np.empty(B, np.int32))
+    draft, length, pos = out
+    dev = device if device is not None else torch.cuda.current_device()
+    with torch.cuda.device(dev):
+        rc = lib.lookup_draft_host(tok.ctypes.data, off.ctypes.data, B, min_m, max_m, K,
+                                   _host_ptr(draft), _host_ptr(length), _host_ptr(pos),
+                                   _stream_handle(stream))
+    _check(rc, lib)
+    return draft, length, pos
+
+
+def _host_ptr(a) -> int:
+    import torch
+    if isinstance(a, torch.Tensor):
+        if a.is_cuda or not a.is_contiguous() or a.dtype != torch.int32:
+            raise ValueError("host outputs must be contiguous int32 CPU tensors or arrays")
+        return a.data_ptr()
+    if a.dtype.name != "int32" or not a.flags["C_CONTIGUOUS"]:
+        raise ValueError("host outputs must be contiguous int32 arrays")
+    return a.ctypes.data
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Diagnostics: limit on each bounded wait inside the scan kernel (0 = default 1 s)."""
+    load_library().lookup_draft_set_wait_limit_ns(int(ns))

@@ -1,0 +1,269 @@
+"""Parity of the CUDA path with the CPU oracle, through the C ABI.
+
+Every comparison is bit-exact on out_len, out_pos, the match length and all K
+draft slots (the sentinels included), on the same seeded inputs.  Covered:
+the five synthetic workloads at full size (default seeds and five more each),
+the hand-worked fixtures, and edge cases: empty batch, short and empty
+requests, K = 0 and the largest K, the widest m range, unaligned token
+pointers, offsets[0] > 0, fewer tokens than scan CTAs, more requests than the
+offsets the scan keeps in shared memory, all-equal and tiny-alphabet histories,
+long single requests spread over many CTAs, a match ending exactly at a tile or
+chunk boundary, the staged and host-buffer entry points, repeated calls and the
+failure path of the bounded waits.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import gen
+import oracle
+from goldens import load_cases
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU machines too
+    pytestmark = [pytest.mark.gpu, pytest.mark.skip(reason="needs a CUDA GPU")]
+
+import prompt_lookup_speculative_gb300 as pkg  # noqa: E402
+
+DEV = "cuda:0"
+
+
+def run_gpu(tokens: np.ndarray, offsets: np.ndarray, min_m, max_m, K, token_pad: int = 0):
+    """Run lookup_draft_ex; token_pad shifts the tokens pointer by that many int32."""
+    buf = torch.zeros(tokens.size + token_pad + 4, dtype=torch.int32, device=DEV)
+    buf[token_pad:token_pad + tokens.size] = torch.from_numpy(tokens).to(DEV)
+    t = buf[token_pad:token_pad + tokens.size] if tokens.size else buf[token_pad:token_pad]
+    o = torch.from_numpy(np.ascontiguousarray(offsets, np.int64)).to(DEV)
+    d, ln, p, m = pkg.lookup_draft_ex(t, o, min_m, max_m, K)
+    torch.cuda.synchronize()
+    return d.cpu().numpy(), ln.cpu().numpy(), p.cpu().numpy(), m.cpu().numpy()
+
+
+def assert_parity(tokens, offsets, min_m, max_m, K, token_pad=0, threads=8):
+    got = run_gpu(tokens, offsets, min_m, max_m, K, token_pad)
+    want = oracle.lookup_draft(tokens, offsets, min_m, max_m, K, threads=threads)
+    for name, g, w in zip(("draft", "len", "pos", "mlen"), got, want):
+        if not np.array_equal(g, w):
+            bad = np.nonzero((g != w).reshape(g.shape[0], -1).any(axis=1))[0] if g.ndim else []
+            raise AssertionError(f"{name} differs at requests {list(bad[:10])} "
+                                 f"(gpu {g[bad[:3]]}, oracle {w[bad[:3]]})")
+    return got
+
+
+@pytest.mark.parametrize("name", gen.WORKLOADS)
+def test_workload_default_seed(name):
+    w = gen.make_workload(name)
+    assert_parity(w.tokens, w.offsets, w.min_m, w.max_m, w.K)
+
+
+@pytest.mark.parametrize("seed", [6, 7, 8, 9, 10])
+@pytest.mark.parametrize("name", gen.WORKLOADS)
+def test_workload_more_seeds(name, seed):
+    w = gen.make_workload(name, seed)
+    assert_parity(w.tokens, w.offsets, w.min_m, w.max_m, w.K)
+
+
+@pytest.mark.parametrize("case", load_cases(), ids=lambda c: c.name)
+def test_hand_worked(case):
+    d, ln, p, m = run_gpu(case.tokens, case.offsets, case.min_m, case.max_m, case.K)
+    np.testing.assert_array_equal(m, case.expect_m)
+    np.testing.assert_array_equal(p, case.expect_pos)
+    np.testing.assert_array_equal(ln, case.expect_len)
+    np.testing.assert_array_equal(d, case.expect_draft)
+
+
+def test_empty_batch():
+    t = torch.zeros(0, dtype=torch.int32, device=DEV)
+    o = torch.zeros(1, dtype=torch.int64, device=DEV)
+    d, ln, p = pkg.lookup_draft(t, o, 4, 12, 15)
+    assert d.shape == (0, 15) and ln.numel() == 0
+
+
+@pytest.mark.parametrize("pad", [0, 1, 2, 3])
+def test_unaligned_tokens_pointer(pad):
+    w = gen.make_workload("periodic", 11)
+    assert_parity(w.tokens, w.offsets, w.min_m, w.max_m, w.K, token_pad=pad)
+
+
+@pytest.mark.parametrize("pad", [0, 1, 3])
+def test_short_requests_and_offset_base(pad):
+    """Lengths 0, 1, min_m, min_m + 1 and a few longer ones, all tokens equal, with
+    offsets[0] > 0 (tokens before it belong to no request)."""
+    rng = np.random.default_rng(pad)
+    lengths = [0, 1, 4, 5, 0, 13, 12, 3, 100, 0, 6, 1]
+    lead = 7
+    tokens = np.concatenate([rng.integers(0, 3, lead), np.full(sum(lengths), 5)]).astype(np.int32)
+    offsets = gen.offsets_from_lengths(lengths) + lead
+    assert_parity(tokens, offsets, 4, 12, 15, token_pad=pad)
+
+
+@pytest.mark.parametrize("K", [0, 1, 31, 32, 33, 64])
+def test_draft_lengths(K):
+    w = gen.make_workload("periodic", 12)
+    assert_parity(w.tokens, w.offsets, w.min_m, w.max_m, K)
+
+
+@pytest.mark.parametrize("min_m,max_m", [(1, 1), (1, 32), (32, 32), (4, 4), (2, 9), (12, 12)])
+def test_m_ranges(min_m, max_m):
+    rng = np.random.default_rng(min_m * 100 + max_m)
+    lengths = rng.integers(0, 3000, size=40)
+    tokens = rng.integers(0, 4, size=int(lengths.sum())).astype(np.int32)
+    assert_parity(tokens, gen.offsets_from_lengths(lengths), min_m, max_m, 9)
+
+
+def test_fewer_tokens_than_ctas():
+    """A handful of tokens: most scan CTAs get an empty chunk."""
+    tokens = np.array([1, 2, 3, 1, 2, 3, 1, 2, 9, 9, 9, 9, 9, 4, 4, 4, 4, 4, 4], dtype=np.int32)
+    offsets = np.array([0, 8, 8, 13, 19], dtype=np.int64)
+    for pad in range(4):
+        assert_parity(tokens, offsets, 2, 4, 5, token_pad=pad)
+        assert_parity(tokens, offsets, 1, 3, 3, token_pad=pad)
+
+
+@pytest.mark.parametrize("B", [4096, 4097, 10000])
+def test_many_requests(B):
+    """Around and above the number of offsets the scan keeps in shared memory."""
+    rng = np.random.default_rng(B)
+    lengths = rng.integers(0, 40, size=B)
+    tokens = rng.integers(0, 3, size=int(lengths.sum())).astype(np.int32)
+    assert_parity(tokens, gen.offsets_from_lengths(lengths), 2, 6, 5)
+
+
+def test_many_requests_long_chunks():
+    rng = np.random.default_rng(5)
+    lengths = rng.integers(0, 600, size=6000)
+    tokens = rng.integers(0, 50, size=int(lengths.sum())).astype(np.int32)
+    assert_parity(tokens, gen.offsets_from_lengths(lengths), 2, 12, 7)
+
+
+def test_all_equal_tokens():
+    lengths = [1, 17, 4096, 25000, 3]
+    tokens = np.full(sum(lengths), -7, dtype=np.int32)
+    assert_parity(tokens, gen.offsets_from_lengths(lengths), 4, 12, 15)
+
+
+@pytest.mark.parametrize("alphabet", [2, 3, 5])
+def test_tiny_alphabet_dense_matches(alphabet):
+    rng = np.random.default_rng(alphabet)
+    lengths = rng.integers(0, 20000, size=50)
+    tokens = rng.integers(0, alphabet, size=int(lengths.sum())).astype(np.int32)
+    assert_parity(tokens, gen.offsets_from_lengths(lengths), 4, 12, 15)
+
+
+def test_extreme_token_values():
+    rng = np.random.default_rng(3)
+    vals = np.array([np.iinfo(np.int32).min, np.iinfo(np.int32).max, -1, 0], dtype=np.int32)
+    lengths = rng.integers(1, 5000, size=30)
+    tokens = vals[rng.integers(0, 4, size=int(lengths.sum()))]
+    assert_parity(tokens, gen.offsets_from_lengths(lengths), 3, 10, 6)
+
+
+def test_long_single_request():
+    """One 3M-token history shared by every scan CTA; matches planted near its start."""
+    rng = np.random.default_rng(11)
+    L = 3_000_000
+    t = rng.integers(0, 1 << 30, size=L).astype(np.int32)
+    t[-20:] = t[100:120]          # the only 12-gram repeat: p = 108
+    got = assert_parity(t, np.array([0, L], np.int64), 4, 12, 15)
+    assert got[2][0] == 108 and got[3][0] == 12
+
+
+@pytest.mark.parametrize("where", range(0, 64, 5))
+def test_match_end_at_every_alignment(where):
+    """Move a planted match across quad, tile and chunk boundaries."""
+    rng = np.random.default_rng(where)
+    L = 200_000
+    t = rng.integers(0, 1 << 30, size=L).astype(np.int32)
+    src = 16384 * 3 + where - 12     # ends near a multiple of the 16 KB tile
+    t[-12:] = t[src:src + 12]
+    lengths = [L, 5000, 1 + where]
+    tokens = np.concatenate([t, rng.integers(0, 7, size=5001 + where).astype(np.int32)])
+    assert_parity(tokens, gen.offsets_from_lengths(lengths), 4, 12, 15, token_pad=where % 4)
+
+
+def test_cross_request_boundary():
+    rng = np.random.default_rng(7)
+    a = rng.integers(0, 1 << 20, size=3000).astype(np.int32)
+    b = rng.integers(0, 1 << 20, size=3000).astype(np.int32)
+    b[-12:] = a[-12:]
+    tokens = np.concatenate([a, b])
+    offsets = np.array([0, a.size, a.size + b.size], dtype=np.int64)
+    d, ln, p, m = assert_parity(tokens, offsets, 4, 12, 5)
+    assert ln[1] == 0
+
+
+def test_staged_entry_points_match_one_call():
+    w = gen.make_workload("recitation25k")
+    t = torch.from_numpy(w.tokens).to(DEV)
+    o = torch.from_numpy(w.offsets).to(DEV)
+    ws = torch.empty(pkg.workspace_bytes(w.B), dtype=torch.uint8, device=DEV)
+    ws.fill_(0xAB)                      # garbage: the scan must not need a clean workspace
+    pkg.lookup_draft_scan(t, o, w.min_m, w.max_m, ws)
+    d1, l1, p1, m1 = pkg.lookup_draft_fill(t, o, w.min_m, w.max_m, w.K, ws, with_mlen=True)
+    d2, l2, p2, m2 = pkg.lookup_draft_ex(t, o, w.min_m, w.max_m, w.K)
+    torch.cuda.synchronize()
+    for a, b in ((d1, d2), (l1, l2), (p1, p2), (m1, m2)):
+        assert torch.equal(a, b)
+
+
+def test_host_entry_point():
+    w = gen.make_workload("chats", 13)
+    d, ln, p = pkg.lookup_draft_host(w.tokens, w.offsets, w.min_m, w.max_m, w.K)
+    od, oln, op, _ = oracle.lookup_draft(w.tokens, w.offsets, w.min_m, w.max_m, w.K, threads=8)
+    np.testing.assert_array_equal(d, od)
+    np.testing.assert_array_equal(ln, oln)
+    np.testing.assert_array_equal(p, op)
+
+
+def test_host_entry_point_offset_base():
+    tokens = np.array([9, 9, 9, 1, 2, 3, 1, 2, 3, 1, 2], dtype=np.int32)
+    offsets = np.array([3, 3, 11], dtype=np.int64)
+    d, ln, p = pkg.lookup_draft_host(tokens, offsets, 2, 4, 4)
+    od, oln, op, _ = oracle.lookup_draft(tokens, offsets, 2, 4, 4)
+    np.testing.assert_array_equal(d, od)
+    np.testing.assert_array_equal(ln, oln)
+    np.testing.assert_array_equal(p, op)
+
+
+def test_repeated_calls_and_streams():
+    w = gen.make_workload("ragged262k", 14)
+    t = torch.from_numpy(w.tokens).to(DEV)
+    o = torch.from_numpy(w.offsets).to(DEV)
+    ref = pkg.lookup_draft(t, o, w.min_m, w.max_m, w.K)
+    s = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(s):
+        for _ in range(5):
+            outs.append(pkg.lookup_draft(t, o, w.min_m, w.max_m, w.K))
+    torch.cuda.synchronize()
+    for out in outs:
+        for a, b in zip(out, ref):
+            assert torch.equal(a, b)
+    want = oracle.lookup_draft(w.tokens, w.offsets, w.min_m, w.max_m, w.K, threads=8)
+    np.testing.assert_array_equal(ref[0].cpu().numpy(), want[0])
+
+
+def test_bounded_wait_failure_reaches_the_host():
+    """With a 1 ns wait limit the scan's first tile wait runs out; the kernel waits
+    for its copies with the default limit, marks its requests failed and returns.
+    The host sees LOOKUP_DRAFT_LEN_FAILED, and the next call is normal again."""
+    w = gen.make_workload("recitation25k")
+    t = torch.from_numpy(w.tokens).to(DEV)
+    o = torch.from_numpy(w.offsets).to(DEV)
+    want = oracle.lookup_draft(w.tokens, w.offsets, w.min_m, w.max_m, w.K, threads=8)
+    try:
+        pkg.set_wait_limit_ns(1)
+        d, ln, p = pkg.lookup_draft(t, o, w.min_m, w.max_m, w.K)
+        torch.cuda.synchronize()
+    finally:
+        pkg.set_wait_limit_ns(0)
+    ln = ln.cpu().numpy()
+    assert (ln == pkg.LEN_FAILED).any()
+    ok = ln != pkg.LEN_FAILED
+    np.testing.assert_array_equal(ln[ok], want[1][ok])
+    got = run_gpu(w.tokens, w.offsets, w.min_m, w.max_m, w.K)
+    np.testing.assert_array_equal(got[1], want[1])
+    np.testing.assert_array_equal(got[0], want[0])

@@ -1,0 +1,121 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library is compiled for sm_103a with the CUDA runtime linked statically, so
+it loads on a machine without a GPU.  These tests check that it exports every
+function include/lookup_draft.h declares, and that argument validation rejects
+bad calls before any CUDA call is made (so they run here, on the CPU).
+"""
+from __future__ import annotations
+
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+import prompt_lookup_speculative_gb300 as pkg
+from prompt_lookup_speculative_gb300 import build as lib_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    return pkg.load_library()
+
+
+def declared_functions() -> set[str]:
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h, encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(lookup_draft\w*)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("lookup_draft", "lookup_draft_ex", "lookup_draft_scan", "lookup_draft_fill",
+                 "lookup_draft_host", "lookup_draft_workspace_bytes", "lookup_draft_strerror",
+                 "lookup_draft_last_cuda_error", "lookup_draft_set_wait_limit_ns"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in sorted(declared_functions()):
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_exported_symbols_are_c_linkage(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_build.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    for name in declared_functions():
+        assert name in exported, f"{name} is not an unmangled dynamic symbol"
+
+
+def test_built_for_sm103a():
+    cmd = lib_build.compile_command("x.so")
+    assert "arch=compute_103a,code=sm_103a" in cmd
+
+
+def test_strerror(lib):
+    assert lib.lookup_draft_strerror(0) == b"ok"
+    assert lib.lookup_draft_strerror(-1) == b"invalid argument"
+    assert lib.lookup_draft_strerror(-2) == b"CUDA error"
+    assert lib.lookup_draft_strerror(12345)
+
+
+FAKE = 0x10000        # a non-null, aligned address; never dereferenced by the host checks
+
+
+@pytest.mark.parametrize("B,min_m,max_m,K", [
+    (-1, 4, 12, 15),        # negative batch
+    (4, 0, 12, 15),         # min_m < 1
+    (4, 5, 4, 15),          # min_m > max_m
+    (4, 4, 33, 15),         # max_m above LOOKUP_DRAFT_MAX_M
+    (4, 4, 12, -1),         # K < 0
+    (4, 4, 12, 65),         # K above LOOKUP_DRAFT_MAX_K
+])
+def test_rejects_bad_parameters(lib, B, min_m, max_m, K):
+    rc = lib.lookup_draft(FAKE, FAKE, B, min_m, max_m, K, FAKE, FAKE, FAKE, None)
+    assert rc == -1
+
+
+def test_rejects_null_and_misaligned_pointers(lib):
+    assert lib.lookup_draft(None, FAKE, 4, 4, 12, 15, FAKE, FAKE, FAKE, None) == -1
+    assert lib.lookup_draft(FAKE, None, 4, 4, 12, 15, FAKE, FAKE, FAKE, None) == -1
+    assert lib.lookup_draft(FAKE, FAKE, 4, 4, 12, 15, None, FAKE, FAKE, None) == -1
+    assert lib.lookup_draft(FAKE, FAKE, 4, 4, 12, 15, FAKE, None, FAKE, None) == -1
+    assert lib.lookup_draft(FAKE, FAKE, 4, 4, 12, 15, FAKE, FAKE, None, None) == -1
+    assert lib.lookup_draft(FAKE + 2, FAKE, 4, 4, 12, 15, FAKE, FAKE, FAKE, None) == -1
+    assert lib.lookup_draft(FAKE, FAKE + 4, 4, 4, 12, 15, FAKE, FAKE, FAKE, None) == -1
+    assert lib.lookup_draft_scan(FAKE, FAKE, 4, 4, 12, None, 1 << 20, None) == -1
+    assert lib.lookup_draft_scan(FAKE, FAKE, 4, 4, 12, FAKE + 4, 1 << 20, None) == -1
+    assert lib.lookup_draft_fill(FAKE, FAKE, 4, 4, 12, 15, None, 1 << 20, FAKE, FAKE, FAKE, None, None) == -1
+
+
+def test_empty_batch_is_a_no_op(lib):
+    # B == 0 enqueues nothing and needs no valid pointer or device.
+    assert lib.lookup_draft(None, None, 0, 4, 12, 15, None, None, None, None) == 0
+    assert lib.lookup_draft_ex(None, None, 0, 4, 12, 15, None, None, None, None, None) == 0
+    assert lib.lookup_draft_host(None, None, 0, 4, 12, 15, None, None, None, None) == 0
+
+
+def test_host_entry_checks_host_offsets(lib):
+    import numpy as np
+    tok = np.zeros(16, np.int32)
+    out_d, out_l, out_p = np.zeros(8, np.int32), np.zeros(2, np.int32), np.zeros(2, np.int32)
+    for bad in ([0, 5, 3], [-1, 4, 8], [0, 4, 4 + (1 << 31)]):
+        off = np.array(bad, np.int64)
+        rc = lib.lookup_draft_host(tok.ctypes.data, off.ctypes.data, 2, 4, 12, 4,
+                                   out_d.ctypes.data, out_l.ctypes.data, out_p.ctypes.data, None)
+        assert rc == -1, bad
+
+
+def test_package_fails_loudly_without_the_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        pkg.load_library(str(tmp_path / "missing.so"))
