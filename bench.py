@@ -1,0 +1,537 @@
+#!/usr/bin/env python
+"""Benchmark of one batched prompt-lookup draft step on GB300.
+
+A step is one call of the library's public entry point, lookup_draft: the
+split-history scan over every request's history plus the draft fill, for one
+batch of synthetic histories (default: the 25k-token recitation workload, B=64
+requests of 25,000 tokens, 6.4 MB of int32 history).  Prints one JSON line.
+
+  value         microseconds per step on the device, inputs resident in HBM.  The
+                K timed steps are public-API calls captured into CUDA graphs
+                (replayed back to back); consecutive steps read different copies
+                of the batch whose total size is over twice the L2 cache, so
+                every step reads its history from HBM.
+  eager_us_per_step
+                the same K steps as direct calls from Python (host launch cost
+                included), for reference.
+  roofline      the scan kernel alone: 4 bytes per history token (each read once)
+                divided by its mean duration per launch, from CUDA events around
+                back-to-back scan launches (captured in a CUDA graph, inputs
+                rotating as above) on their stream, against the measured HBM copy
+                bandwidth.  scan_us_isolated: events around single launches.
+  e2e           lookup_draft_host: pinned host buffers in, the step, outputs back
+                to the host, every step.
+  cpu_baseline  the CPU oracle (brute force, one thread per slice of requests) on
+                this machine's host cores, on the same batch.
+
+--impl reference times that oracle as the comparison arm on the same workload.
+Multi-GPU (torchrun, one rank per GPU): every rank drafts its own batch (weak
+scaling, no data exchange); the step time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "µs per batched draft step; history GB/s scanned vs GB300 HBM roofline"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+SCAN_SOURCE = os.path.join(ROOT, "prompt_lookup_speculative_gb300", "csrc", "lookup_draft.cu")
+SCAN_PROFILE = os.path.join(ROOT, "profiles", "scan_kernel_recitation25k.md")
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--workload", default="recitation25k")
+    ap.add_argument("--seed", type=int, default=None)
+    ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--cpu-budget-s", type=float, default=2.0,
+                    help="wall-clock budget of the CPU-baseline sample")
+    ap.add_argument("--reference-budget-s", type=float, default=90.0,
+                    help="wall-clock budget of the whole --impl reference run")
+    ap.add_argument("--settle-s", type=float, default=0.5,
+                    help="untimed graph replays before the timed region, so clocks settle")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------- ranks ----
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank drafts its own batch: same workload recipe, its own seed."""
+    return int(base_seed) + 1000 * int(rank)
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks ----
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms while the GPU work runs."""
+
+    def __init__(self, gpu_index: int, enabled: bool = True):
+        self.proc = None
+        self.rows = []
+        if not enabled:
+            return
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for ln in out.splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) >= 10:
+                self.rows.append(parts)
+
+    def summary(self) -> dict:
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in self.rows if num(r[1]) is not None]
+        util = [num(r[4]) or 0.0 for r in self.rows]
+        loaded = [num(r[1]) for r, u in zip(self.rows, util) if u > 0 and num(r[1]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in self.rows for n, v in zip(names, r[6:10]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(loaded or sm) if (loaded or sm) else None,
+                "sm_max_mhz": num(self.rows[0][2]),
+                "reasons": reasons,
+                "samples": len(self.rows),
+                "samples_under_load": len(loaded),
+                "power_w_max": max((num(r[3]) or 0.0) for r in self.rows)}
+
+
+# ------------------------------------------------------------- roofline ----
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def scan_source_hash() -> str:
+    with open(SCAN_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per scan launch from the committed ncu summary, if it was taken on
+    this exact kernel source and workload (else None)."""
+    try:
+        text = open(SCAN_PROFILE, encoding="utf-8").read()
+    except OSError:
+        return None
+    src = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    wl = re.search(r"workload:\s*(\S+)", text)
+    tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not (src and wl and tr) or src.group(1) != scan_source_hash() or wl.group(1) != workload:
+        return None
+    return int(tr.group(1))
+
+
+# ------------------------------------------------------------------ GPU ----
+def run_gpu(args, rank: int, world: int, local_rank: int):
+    import numpy as np
+    import torch
+
+    import gen
+    import prompt_lookup_speculative_gb300 as pkg
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (there is no CPU fallback)")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = dist_init(world, "nccl")
+    lib = pkg.load_library()
+
+    seed = rank_seed(gen.DEFAULT_SEED[args.workload] if args.seed is None else args.seed, rank)
+    w = gen.make_workload(args.workload, seed)
+    B, K, min_m, max_m = w.B, w.K, w.min_m, w.max_m
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2**20))
+    ncopy = max(3, math.ceil(2 * l2 / max(w.history_bytes, 1)) + 1)
+    stream = torch.cuda.Stream(dev)
+    h = int(stream.cuda_stream)
+
+    tok_host = torch.from_numpy(w.tokens)
+    off_host = torch.from_numpy(w.offsets)
+    toks = [tok_host.to(dev) for _ in range(ncopy)]
+    offs = [off_host.to(dev) for _ in range(ncopy)]
+    tok_p = [t.data_ptr() for t in toks]
+    off_p = [o.data_ptr() for o in offs]
+    draft = torch.empty((B, K), dtype=torch.int32, device=dev)
+    length = torch.empty(B, dtype=torch.int32, device=dev)
+    pos = torch.empty(B, dtype=torch.int32, device=dev)
+    dp, lp, pp = draft.data_ptr(), length.data_ptr(), pos.data_ptr()
+    ws_bytes = pkg.workspace_bytes(B, dev)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    wsp = ws.data_ptr()
+
+    def step(i: int, handle: int):
+        j = i % ncopy
+        rc = lib.lookup_draft(tok_p[j], off_p[j], B, min_m, max_m, K, dp, lp, pp, handle)
+        if rc != 0:
+            raise pkg.LookupDraftError(rc, lib)
+
+    clocks = ClockSampler(dev.index, enabled=not args.no_clocks)
+    torch.cuda.synchronize(dev)
+
+    # warm-up: eager steps, then graph capture (one graph per rotation of the copies)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i, h)
+    stream.synchronize()
+    full_reps, tail = divmod(args.steps, ncopy)
+    graphs = {}
+    for n in sorted({ncopy if full_reps else 0, tail} - {0}):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            hc = int(torch.cuda.current_stream().cuda_stream)
+            for i in range(n):
+                step(i, hc)
+        graphs[n] = g
+    with torch.cuda.stream(stream):
+        t_end = time.perf_counter() + args.settle_s  # untimed replays: clocks settle under load
+        while True:
+            for g in graphs.values():
+                g.replay()
+            stream.synchronize()
+            if time.perf_counter() >= t_end:
+                break
+
+    # timed region: exactly K steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(full_reps):
+            graphs[ncopy].replay()
+        if tail:
+            graphs[tail].replay()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
+    us_per_step = 1000.0 * ms_total / args.steps
+
+    # eager: the same K steps as direct calls
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i, h)
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    eager_us = 1000.0 * max_over_ranks(ev0.elapsed_time(ev1), dist, dev) / args.steps
+
+    # roofline: the scan kernel alone.  (a) back to back: ncopy scan launches over
+    # the rotating copies captured in one CUDA graph, replayed; CUDA events around
+    # the replays on the launching stream give the mean duration per launch.
+    # (b) isolated: events around each single launch (includes the event gaps).
+    def scan_call(j: int, handle: int):
+        rc = lib.lookup_draft_scan(tok_p[j], off_p[j], B, min_m, max_m, wsp, ws_bytes, handle)
+        if rc != 0:
+            raise pkg.LookupDraftError(rc, lib)
+
+    def fill_call(j: int, handle: int):
+        rc = lib.lookup_draft_fill(tok_p[j], off_p[j], B, min_m, max_m, K, wsp, ws_bytes,
+                                   dp, lp, pp, None, handle)
+        if rc != 0:
+            raise pkg.LookupDraftError(rc, lib)
+
+    def graph_of(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            hc = int(torch.cuda.current_stream().cuda_stream)
+            for j in range(ncopy):
+                fn(j, hc)
+        return g
+
+    def time_graph(g, reps: int) -> float:
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            ev0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        return 1000.0 * ev0.elapsed_time(ev1) / (reps * ncopy)
+
+    reps = max(10, min(200, args.steps // ncopy))
+    scan_us = max_over_ranks(time_graph(graph_of(scan_call), reps), dist, dev)
+    fill_us = max_over_ranks(time_graph(graph_of(fill_call), reps), dist, dev)
+    clock_hz = float(getattr(props, "clock_rate", 2_000_000)) * 1000.0
+    ea = [torch.cuda.Event(enable_timing=True) for _ in range(ncopy)]
+    eb = [torch.cuda.Event(enable_timing=True) for _ in range(ncopy)]
+    iso_ms = []
+    for rep in range(4):
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(2e-3 * clock_hz))   # host runs ahead: no gaps between launches
+            for j in range(ncopy):
+                ea[j].record(stream)
+                scan_call(j, h)
+                eb[j].record(stream)
+                fill_call(j, h)
+        stream.synchronize()
+        if rep:
+            iso_ms += [ea[j].elapsed_time(eb[j]) for j in range(ncopy)]
+    scan_iso_us = 1000.0 * max_over_ranks(statistics.fmean(iso_ms), dist, dev)
+
+    # e2e: host buffers through lookup_draft_host, copies inside every step
+    h_tok = tok_host.pin_memory()
+    h_off = off_host.pin_memory()
+    h_draft = torch.empty((B, K), dtype=torch.int32).pin_memory()
+    h_len = torch.empty(B, dtype=torch.int32).pin_memory()
+    h_pos = torch.empty(B, dtype=torch.int32).pin_memory()
+    args_host = (h_tok.data_ptr(), h_off.data_ptr(), B, min_m, max_m, K,
+                 h_draft.data_ptr(), h_len.data_ptr(), h_pos.data_ptr(), h)
+    for _ in range(3):
+        lib.lookup_draft_host(*args_host)
+    n_e2e = max(1, min(args.e2e_steps, args.steps))
+    barrier(dist, dev)
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        rc = lib.lookup_draft_host(*args_host)
+        if rc != 0:
+            raise pkg.LookupDraftError(rc, lib)
+    e2e_us = 1e6 * max_over_ranks(time.perf_counter() - t0, dist, dev) / n_e2e
+    clocks.stop()
+
+    # outputs must be the oracle's (checked on request 0..B of the last step's copy)
+    import oracle
+    o_draft, o_len, o_pos, _ = oracle.lookup_draft(w.tokens, w.offsets, min_m, max_m, K,
+                                                   threads=os.cpu_count() or 1)
+    parity = (np.array_equal(draft.cpu().numpy(), o_draft) and np.array_equal(length.cpu().numpy(), o_len)
+              and np.array_equal(pos.cpu().numpy(), o_pos)
+              and np.array_equal(h_draft.numpy(), o_draft) and np.array_equal(h_len.numpy(), o_len))
+
+    cpu = None
+    if rank == 0:
+        cpu = cpu_baseline(w, args.cpu_budget_s)
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+
+    hist_bytes = w.history_bytes
+    peak, peak_kind = measured_hbm_peak()
+    achieved = hist_bytes / (scan_us * 1e-6) / 1e9
+    traffic = recorded_traffic(args.workload)
+    line = {
+        "metric": METRIC,
+        "value": round(us_per_step, 3),
+        "unit": "us/step",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(us_per_step / 1000.0, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int32",
+        "data": "synthetic",
+        "config": {
+            "workload": args.workload,
+            "description": gen.DESCRIPTION[args.workload],
+            "B": B, "history_tokens": w.total_tokens, "history_bytes": hist_bytes,
+            "min_m": min_m, "max_m": max_m, "K": K, "seed": seed,
+            "l2": f"inputs rotate over {ncopy} device copies "
+                  f"({ncopy * hist_bytes / 2**20:.0f} MiB > 2x L2 of {l2 / 2**20:.0f} MiB)",
+            "launch": f"lookup_draft calls captured in CUDA graphs of {ncopy} steps",
+            "parallelism": f"replicas x{world} (one batch per GPU, no exchange)",
+        },
+        "history_gbs_per_step": round(world * hist_bytes / (us_per_step * 1e-6) / 1e9, 1),
+        "eager_us_per_step": round(eager_us, 3),
+        "scan_us": round(scan_us, 3),
+        "scan_us_isolated": round(scan_iso_us, 3),
+        "fill_us": round(fill_us, 3),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "scan_kernel",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "peak_kind": f"{peak_kind} copy bandwidth",
+            "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+            "algorithmic_bytes_per_launch": hist_bytes,
+            "traffic": traffic,
+        },
+        "e2e": {
+            "value": round(e2e_us, 3),
+            "unit": "us/step",
+            "h2d_bytes_per_step": int(w.tokens.nbytes + w.offsets.nbytes),
+            "d2h_bytes_per_step": int(4 * B * K + 8 * B),
+            "steps": n_e2e,
+        },
+        "cpu_baseline": cpu,
+        "gpu_launches": 2 * args.steps,
+        "parity_with_oracle": bool(parity),
+        "clocks": clocks.summary(),
+        "gpu": torch.cuda.get_device_name(dev),
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ CPU ----
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, budget_s: float) -> dict:
+    """The oracle, as it stands, on the host cores: whole batches until the budget."""
+    import oracle
+    cores = host_cores()
+    oracle.lookup_draft(w.tokens, w.offsets, w.min_m, w.max_m, w.K, threads=cores)   # warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.lookup_draft(w.tokens, w.offsets, w.min_m, w.max_m, w.K, threads=cores)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= 1000:
+            break
+    return {"value": round(1e6 * el / n, 1), "unit": "us/step", "cores": cores, "kind": "oracle",
+            "sample": f"the whole {w.name} batch ({w.B} requests, {w.total_tokens} tokens) "
+                      f"x {n} runs, {el:.1f} s wall"}
+
+
+def run_reference(args, rank: int, world: int):
+    """The oracle as the comparison arm: per step, a slice of the batch's requests
+    sized so that the whole run fits the budget; the time is scaled to the whole
+    batch by history tokens."""
+    if rank != 0:
+        return
+    import gen
+    import oracle
+    seed = gen.DEFAULT_SEED[args.workload] if args.seed is None else args.seed
+    w = gen.make_workload(args.workload, seed)
+    cores = host_cores()
+    lens = (w.offsets[1:] - w.offsets[:-1])
+    t0 = time.perf_counter()
+    oracle.lookup_draft(w.tokens, w.offsets, w.min_m, w.max_m, w.K, threads=cores)
+    full_s = time.perf_counter() - t0
+    total_steps = args.steps + args.warmup
+    per_step_budget = args.reference_budget_s / max(total_steps, 1)
+    frac = min(1.0, per_step_budget / max(full_s, 1e-9))
+    n_req = max(1, min(w.B, int(round(frac * w.B))))
+    timed_s, timed_tokens = 0.0, 0
+    for i in range(total_steps):
+        lo = (i * n_req) % w.B
+        hi = min(w.B, lo + n_req)
+        sub_off = w.offsets[lo:hi + 1]
+        t = time.perf_counter()
+        oracle.lookup_draft(w.tokens[sub_off[0]:sub_off[-1]], sub_off - sub_off[0],
+                            w.min_m, w.max_m, w.K, threads=cores)
+        dt = time.perf_counter() - t
+        if i >= args.warmup:
+            timed_s += dt
+            timed_tokens += int(lens[lo:hi].sum())
+    # time per history token over the timed steps, times the tokens of one whole batch
+    us_per_step = 1e6 * timed_s * w.total_tokens / max(timed_tokens, 1)
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(us_per_step, 1),
+        "unit": "us/step",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(us_per_step / 1000.0, 4),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "description": gen.DESCRIPTION[args.workload],
+                   "B": w.B, "history_tokens": w.total_tokens, "history_bytes": w.history_bytes,
+                   "min_m": w.min_m, "max_m": w.max_m, "K": w.K, "seed": seed},
+        "cpu_baseline": {"value": round(us_per_step, 1), "unit": "us/step", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"per step {n_req} of {w.B} requests of the {w.name} batch, "
+                                   f"time scaled to the whole batch by history tokens"},
+        "e2e": {"value": round(us_per_step, 1), "unit": "us/step",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -149,8 +149,9 @@ const char *lookup_draft_strerror(int code);
 const char *lookup_draft_last_cuda_error(void);
 
 /*
- * Diagnostics: the limit, in nanoseconds, on each bounded wait inside the scan
- * kernel (default 1e9).  When a wait runs out, the kernel waits again (with the
+ * Diagnostics: the time limit, in nanoseconds, on the scan kernel's bounded waits
+ * (default 1e9): every tile a scan CTA waits for must land within this time of
+ * the CTA's start.  When the limit runs out, the CTA waits again (with the
  * default limit) for its own copies in flight, marks its requests
  * LOOKUP_DRAFT_LEN_FAILED and returns, leaving the context usable.  Setting a
  * tiny limit forces that path, to test that the failure reaches the host.

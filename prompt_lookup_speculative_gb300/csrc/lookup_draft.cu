@@ -10,33 +10,38 @@
 // Two kernels, both on the caller's stream:
 //
 //  scan_kernel -- the split-history scan, HBM bound (4 bytes per history token,
-//    read once).  The whole batch is one array of 16-byte quads; the grid (a fixed
-//    number of CTAs per SM, independent of the data so the host never reads the
-//    offsets) splits it into equal contiguous chunks, so long requests are shared
-//    by many CTAs and short ones are packed into one.  Each CTA streams its chunk
-//    through shared memory in tiles moved by 1-D TMA bulk copies (cp.async.bulk,
-//    mbarrier completion, a ring of stages), each tile preceded by a halo of up to
-//    31 tokens of backward context.  A thread reads one quad (128-bit) at a time
-//    and compares its tokens with the last suffix token of their request; the rare
-//    survivors are extended backwards against the suffix kept in shared memory
-//    (the article's cheap rejection test, section "第1步").  A match of length k
-//    ending at local position q gives the key (k << 32) | (q - k + 1): its maximum
-//    is the longest match, then the most recent.  Each thread keeps its best key
-//    for its current request and folds it into a per-(request, CTA) slot with one
-//    red.max when it moves on.
+//    read once).  The whole batch is one array of 16-byte quads; the grid (one CTA
+//    per SM, independent of the data so the host never reads the offsets) splits
+//    it into equal contiguous chunks, so long requests are shared by many CTAs and
+//    short ones are packed into one.  The offsets arrive in shared memory with one
+//    TMA bulk copy.  Each warp then streams its own tiles of the chunk (tiles
+//    w, w+16, w+32, ... of the CTA's chunk) through a private ring of shared-memory
+//    buffers filled by 1-D TMA bulk copies (cp.async.bulk, mbarrier completion),
+//    each tile preceded by a halo of up to 31 tokens of backward context; no CTA
+//    barrier is needed in the main loop.  A tile is walked request by request.
+//    Within a request, every lane takes one 128-bit quad at a time and runs the
+//    article's cheap rejection test (section "第1步") branch-free: a token and the
+//    D - 1 tokens before it against the last D suffix tokens, D = min(min_m, 2).
+//    The rare survivors are extended backwards against the suffix kept in shared
+//    memory.  A match of length k ending at local position q gives the key
+//    (k << 32) | (q - k + 1): its maximum is the longest match, then the most
+//    recent.  A lane folds its best key per request into a per-(request, CTA)
+//    slot with one red.max.
 //
 //  fill_kernel -- one warp per request: max over the request's slots, then the
 //    draft tokens t[p + m + (j mod d)], d = L - p - m, and the length/position.
-//    Launched with programmatic dependent launch so its launch and its reads of
-//    the offsets overlap the scan's tail.
+//
+// Both kernels use programmatic dependent launch: each lets the next kernel on
+// the stream start its prologue early and waits for its predecessor's results
+// before reading them.
 //
 // Partial-result slots.  CTA c owns slot (r + c) for every request r that has a
 // token in its chunk.  Chunks and requests are both ordered and disjoint, so the
 // (c, r) pairs form a monotone staircase and r + c never repeats: no slot is shared
 // and none needs clearing before a call (each CTA zeroes its own before use).
 //
-// No spin-wait is unbounded: every mbarrier wait gives up after a time limit, and
-// a CTA that gives up waits (bounded) for its own copies, marks its requests as
+// No spin-wait is unbounded: every mbarrier wait gives up at a deadline, and a
+// CTA that gives up waits (bounded) for its own copies, marks its requests as
 // failed in their slots and exits, so the failure reaches the host as
 // out_len = LOOKUP_DRAFT_LEN_FAILED instead of a hang.
 
@@ -53,13 +58,14 @@
 namespace {
 
 // ---------------------------------------------------------------- tuning ----
-constexpr int kThreads = 256;          // scan CTA size
-constexpr int kTileQuads = 1024;       // 16 KB of history per tile
+constexpr int kWarps = 16;             // scan warps per CTA; each streams its own tiles
+constexpr int kThreads = kWarps * 32;
+constexpr int kBufs = 3;               // tiles in flight per warp
+constexpr int kTileQuadsMax = 192;     // 3 KB of history per tile at most
+constexpr int kTileQuadsMin = 32;
 constexpr int kHaloQuads = 8;          // room for (LOOKUP_DRAFT_MAX_M - 1) tokens of context
-constexpr int kStages = 4;             // tiles in flight per CTA
 constexpr int kSufCap = 64;            // requests per CTA whose suffix is kept in smem
 constexpr int kOffCap = 4097;          // offsets kept in smem when B + 1 <= kOffCap
-constexpr int kCtasPerSm = 2;
 constexpr int kFillWarps = 4;          // requests per fill CTA
 
 constexpr unsigned long long kKeyFailed = ~0ull;
@@ -67,7 +73,7 @@ constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 
 static_assert(4 * kHaloQuads >= LOOKUP_DRAFT_MAX_M - 1, "halo too small for LOOKUP_DRAFT_MAX_M");
 
-constexpr size_t kStageBytes = size_t(kTileQuads + kHaloQuads) * 16;
+constexpr size_t kBufBytes = size_t(kTileQuadsMax + kHaloQuads) * 16;
 
 struct ScanParams {
     const int32_t *tokens;
@@ -95,36 +101,39 @@ struct FillParams {
 
 // ------------------------------------------------------ partition helpers ----
 // The batch occupies aligned quads [q_lo, q_lo + nq) of the 16-byte-aligned view
-// of `tokens`; chunk c is quads [q_lo + c*nq/G, q_lo + (c+1)*nq/G).
+// of `tokens`.  Chunk c is quads [q_lo + c*S, q_lo + (c+1)*S) clipped to the batch,
+// with S = ceil(nq / G): every chunk but the last non-empty one holds S quads, and
+// the empty ones (if any) all come last.
 struct Partition {
     int64_t a_begin;    // first history token, index in the aligned view
     int64_t a_end;      // one past the last
     int64_t q_lo;
     int64_t nq;
+    int64_t S;          // quads per chunk
 };
 
 __host__ __device__ inline int tokens_shift(const int32_t *tokens) {
     return int((reinterpret_cast<uintptr_t>(tokens) & 15u) >> 2);
 }
 
-__device__ inline Partition make_partition(int64_t a_begin, int64_t a_end) {
+// x / y for y > 0, in 32-bit arithmetic whenever x allows it.
+__device__ inline int64_t div_u(int64_t x, int64_t y) {
+    if (((unsigned long long)x | (unsigned long long)y) < (1ull << 32)) return int64_t(uint32_t(x) / uint32_t(y));
+    return int64_t((unsigned long long)x / (unsigned long long)y);
+}
+
+__device__ inline Partition make_partition(int64_t a_begin, int64_t a_end, int G) {
     Partition P;
     P.a_begin = a_begin;
     P.a_end = a_end;
     P.q_lo = a_begin >> 2;
     P.nq = ((a_end + 3) >> 2) - P.q_lo;
+    P.S = div_u(P.nq + G - 1, G);
     return P;
 }
 
-__device__ inline int64_t chunk_start(const Partition &P, int64_t c, int G) {
-    return P.q_lo + int64_t((unsigned long long)c * (unsigned long long)P.nq / (unsigned long long)G);
-}
-
-// The chunk holding aligned quad x: the largest c with chunk_start(c) <= x.
-__device__ inline int64_t chunk_of_quad(const Partition &P, int64_t x, int G) {
-    unsigned long long rel = (unsigned long long)(x - P.q_lo);
-    return int64_t(((rel + 1) * (unsigned long long)G - 1) / (unsigned long long)P.nq);
-}
+// The chunk holding aligned quad x.
+__device__ inline int64_t chunk_of_quad(const Partition &P, int64_t x) { return div_u(x - P.q_lo, P.S); }
 
 // ----------------------------------------------------------- PTX wrappers ----
 __device__ inline uint32_t smem_addr(const void *p) {
@@ -148,12 +157,17 @@ __device__ inline void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                  : "memory");
 }
 
-// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
+// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.  Both
+// addresses and the size are multiples of 16 bytes.
 __device__ inline void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+__device__ inline void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 __device__ inline bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -174,13 +188,12 @@ __device__ inline uint64_t global_ns() {
     return t;
 }
 
-// Wait for phase `parity` of `bar` to complete; false if `limit_ns` ran out first.
-__device__ inline bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
+// Wait for phase `parity` of `bar` to complete; false once the global timer has
+// passed `deadline_ns` (checked before every try, so a past deadline fails at once).
+__device__ inline bool mbar_wait_until(uint32_t bar, uint32_t parity, uint64_t deadline_ns) {
     for (;;) {
+        if (global_ns() > deadline_ns) return false;
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > limit_ns) return false;
     }
 }
 
@@ -188,6 +201,8 @@ __device__ inline void red_max_u64(unsigned long long *p, unsigned long long v) 
     atomicMax(p, v);   // result unused: compiles to a fire-and-forget reduction
 }
 
+// Programmatic dependent launch: let the next kernel on the stream start its
+// prologue now / wait until the previous kernel's results are visible.
 __device__ inline void allow_dependent_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -197,95 +212,162 @@ __device__ inline void wait_for_prerequisite_grid() {
 }
 
 // ------------------------------------------------------------ scan kernel ----
+// Dynamic shared memory: the warps' tile rings, their mbarriers (plus one for the
+// offsets copy), the suffix rows, and the offsets.  The ring alone exceeds half
+// of an SM's shared memory, so exactly one scan CTA runs per SM.
 struct ScanSmemLayout {
-    size_t stages, bars, suf, offs, total;
+    size_t bufs, bars, suf, offs, total;
 };
 
 __host__ __device__ inline ScanSmemLayout scan_smem_layout(int32_t B, int32_t max_m) {
     ScanSmemLayout L;
-    L.stages = 0;
-    L.bars = L.stages + kStages * kStageBytes;
-    L.suf = L.bars + kStages * sizeof(unsigned long long);
-    L.offs = L.suf + ((size_t(kSufCap) * size_t(max_m) * 4 + 15) & ~size_t(15));
-    size_t n_off = (int64_t(B) + 1 <= kOffCap) ? size_t(B) + 1 : 2;
-    L.total = L.offs + n_off * 8;
+    L.bufs = 0;
+    L.bars = L.bufs + size_t(kWarps) * kBufs * kBufBytes;
+    L.suf = L.bars + (size_t(kWarps) * kBufs + 1) * sizeof(unsigned long long);
+    L.offs = (L.suf + size_t(kSufCap) * size_t(max_m) * 4 + 15) & ~size_t(15);
+    // offsets copied as the 16-byte-aligned span covering them
+    const size_t n_off = (int64_t(B) + 1 <= kOffCap) ? size_t(B) + 1 : 2;
+    L.total = L.offs + ((n_off * 8 + 16 + 15) & ~size_t(15));
     return L;
 }
 
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) scan_kernel(ScanParams prm) {
+// Rejection test on one quad: bit e is set when the token at element e of `cur`
+// (and, for D == 2, the token before it) equals the last suffix token s0 (and
+// the one before it, s1).  The token before cur.x is `prev`.
+template <int D>
+__device__ __forceinline__ unsigned quad_hits(int32_t prev, const int4 &cur, int32_t s0, int32_t s1) {
+    bool h0 = cur.x == s0, h1 = cur.y == s0, h2 = cur.z == s0, h3 = cur.w == s0;
+    if (D >= 2) {
+        h0 = h0 && prev == s1; h1 = h1 && cur.x == s1; h2 = h2 && cur.y == s1; h3 = h3 && cur.z == s1;
+    }
+    return unsigned(h0) | (unsigned(h1) << 1) | (unsigned(h2) << 2) | (unsigned(h3) << 3);
+}
+
+// D = min(min_m, 2): how many suffix tokens the branch-free rejection test checks
+// before a candidate is extended one token at a time.
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
     extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int sh_rlo, sh_rhi, sh_abort;
     const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
     const int c = blockIdx.x;
     const int G = prm.grid;
     const int B = prm.B;
     const int min_m = prm.min_m;
     const int max_m = prm.max_m;
 
+    // Every copy must land within wait_ns of this CTA's start.
+    const uint64_t deadline = global_ns() + prm.wait_ns;
     const ScanSmemLayout lay = scan_smem_layout(B, max_m);
     unsigned long long *bars = reinterpret_cast<unsigned long long *>(smem + lay.bars);
+    unsigned long long *offs_bar = bars + kWarps * kBufs;
     int32_t *suf_s = reinterpret_cast<int32_t *>(smem + lay.suf);
-    int64_t *offs_s = reinterpret_cast<int64_t *>(smem + lay.offs);
 
     const int shift = tokens_shift(prm.tokens);
     const int32_t *ta = reinterpret_cast<const int32_t *>(reinterpret_cast<uintptr_t>(prm.tokens) & ~uintptr_t(15));
     const bool offs_in_smem = int64_t(B) + 1 <= kOffCap;
+    const uintptr_t off_src = reinterpret_cast<uintptr_t>(prm.offsets) & ~uintptr_t(15);
+    const int64_t *offs_s =
+        reinterpret_cast<const int64_t *>(smem + lay.offs + (reinterpret_cast<uintptr_t>(prm.offsets) & 15u));
 
-    // 1. Offsets (shifted into the aligned view) -> shared memory, one burst.
-    if (offs_in_smem) {
-        for (int i = tid; i <= B; i += kThreads) offs_s[i] = __ldg(prm.offsets + i) + shift;
-    } else if (tid < 2) {
-        offs_s[tid] = __ldg(prm.offsets + (tid == 0 ? 0 : B)) + shift;
+    // 0. Barriers, and the offsets warmed into L2 while the previous kernel on
+    //    the stream finishes; then wait for it (it may have written the inputs).
+    if (offs_in_smem && tid * 16 <= B) prefetch_l2(prm.offsets + tid * 16);
+    if (tid == 0) {
+        for (int i = 0; i <= kWarps * kBufs; ++i) mbar_init(smem_addr(&bars[i]), 1);
+        fence_barrier_init();
+        sh_abort = 0;
     }
-    __syncthreads();
+    wait_for_prerequisite_grid();
+
+    // 1. Offsets -> shared memory: one bulk copy of the 16-byte span covering them.
+    //    Should the copy not land in time, the CTA reads the offsets from global
+    //    memory instead (and lets the copy land before it exits).
+    bool ok = true;
+    if (offs_in_smem && tid == 0) {
+        const uintptr_t end = (reinterpret_cast<uintptr_t>(prm.offsets + B + 1) + 15) & ~uintptr_t(15);
+        const uint32_t bytes = uint32_t(end - off_src);
+        mbar_expect_tx(smem_addr(offs_bar), bytes);
+        bulk_copy_g2s(smem_addr(smem + lay.offs), reinterpret_cast<const void *>(off_src), bytes,
+                      smem_addr(offs_bar));
+    }
+    __syncthreads();                                     // barrier init visible before waiting
+    if (offs_in_smem) ok = mbar_wait_until(smem_addr(offs_bar), 0, deadline);
+    const bool offs_smem = offs_in_smem && !__syncthreads_or(!ok);
+    const bool offs_pending = offs_in_smem && !offs_smem;
+    auto drain_offsets = [&]() {
+        if (offs_pending && tid == 0) (void)mbar_wait_until(smem_addr(offs_bar), 0, global_ns() + kDefaultWaitNs);
+    };
 
     auto off_a = [&](int i) -> int64_t {
-        return offs_in_smem ? offs_s[i] : __ldg(prm.offsets + i) + shift;
+        return (offs_smem ? offs_s[i] : __ldg(prm.offsets + i)) + shift;
     };
 
-    const int64_t a_begin = offs_s[0];
-    const int64_t a_end = offs_in_smem ? offs_s[B] : offs_s[1];
-    if (a_end <= a_begin) return;                       // no history tokens at all
-    const Partition P = make_partition(a_begin, a_end);
-    const int64_t qa = chunk_start(P, c, G);
-    const int64_t qb = chunk_start(P, c + 1, G);
-    if (qa >= qb) return;                               // empty chunk: owns no slot
+    const int64_t a_begin = off_a(0);
+    const int64_t a_end = off_a(B);
+    allow_dependent_launch();
+    if (a_end <= a_begin) {                             // no history tokens at all
+        drain_offsets();
+        return;
+    }
+    const Partition P = make_partition(a_begin, a_end, G);
+    const int64_t q_hi = P.q_lo + P.nq;
+    const int64_t qa = P.q_lo + int64_t(c) * P.S;
+    if (qa >= q_hi) {                                   // empty chunk: owns no slot
+        drain_offsets();
+        return;
+    }
+    const int64_t qb = (qa + P.S < q_hi) ? qa + P.S : q_hi;
 
-    // 2. Tile plan and the first copies (one elected thread).
+    // 2. Tiles: tile i of this chunk is quads [qa + i*tq, ...), streamed by warp
+    //    i % kWarps through its ring; each warp starts its first copies now.
     const int halo = (max_m - 1 + 3) >> 2;
-    const int ntiles = int((qb - qa + kTileQuads - 1) / kTileQuads);
-    auto issue_tile = [&](int i) {
-        const int s = i % kStages;
-        const int64_t t0 = qa + int64_t(i) * kTileQuads;
-        const int64_t t1 = (t0 + kTileQuads < qb) ? t0 + kTileQuads : qb;
+    const int64_t chunk_q = qb - qa;
+    int tq = int((chunk_q + 2 * kWarps - 1) / (2 * kWarps));
+    tq = tq < kTileQuadsMin ? kTileQuadsMin : (tq > kTileQuadsMax ? kTileQuadsMax : tq);
+    const int ntiles = int((chunk_q + tq - 1) / tq);
+    unsigned char *my_bufs = smem + lay.bufs + size_t(warp) * kBufs * kBufBytes;
+    unsigned long long *my_bars = bars + warp * kBufs;
+    auto issue_tile = [&](int i, int slot) {           // lane 0 only
+        const int64_t t0 = qa + int64_t(i) * tq;
+        const int64_t t1 = (t0 + tq < qb) ? t0 + tq : qb;
         const int64_t ls = (t0 - halo > P.q_lo) ? t0 - halo : P.q_lo;
         const uint32_t bytes = uint32_t(t1 - ls) * 16u;
-        unsigned char *stage = smem + lay.stages + size_t(s) * kStageBytes;
-        const uint32_t dst = smem_addr(stage + size_t(kHaloQuads - (t0 - ls)) * 16);
-        const uint32_t bar = smem_addr(&bars[s]);
+        unsigned char *buf = my_bufs + size_t(slot) * kBufBytes;
+        const uint32_t bar = smem_addr(&my_bars[slot]);
         mbar_expect_tx(bar, bytes);
-        bulk_copy_g2s(dst, ta + ls * 4, bytes, bar);
+        bulk_copy_g2s(smem_addr(buf + size_t(kHaloQuads - (t0 - ls)) * 16), ta + ls * 4, bytes, bar);
     };
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(smem_addr(&bars[s]), 1);
-        fence_barrier_init();
-        const int first = ntiles < kStages ? ntiles : kStages;
-        for (int i = 0; i < first; ++i) issue_tile(i);
+    // this warp's tiles: i = warp + kWarps * k, k = 0, 1, ...; tile k uses slot k % kBufs
+    const int my_tiles = (ntiles > warp) ? (ntiles - warp + kWarps - 1) / kWarps : 0;
+    if (lane == 0) {
+        const int first = my_tiles < kBufs ? my_tiles : kBufs;
+        for (int k = 0; k < first; ++k) issue_tile(warp + kWarps * k, k);
     }
-    allow_dependent_launch();
 
     // 3. Requests with a token in this chunk: [r_lo, r_hi].
     const int64_t e_first = (4 * qa > a_begin) ? 4 * qa : a_begin;
     const int64_t e_last = ((4 * qb < a_end) ? 4 * qb : a_end) - 1;
-    auto owner = [&](int64_t a) -> int {                // largest r with off_a(r) <= a
-        int lo = 0, hi = B;                             // off_a(0) <= a < off_a(B)
+    if (offs_smem) {
+        for (int i = tid; i < B; i += kThreads) {
+            const int64_t o0 = offs_s[i] + shift, o1 = offs_s[i + 1] + shift;
+            if (o0 <= e_first && e_first < o1) sh_rlo = i;
+            if (o0 <= e_last && e_last < o1) sh_rhi = i;
+        }
+    } else if (tid < 2) {
+        const int64_t e = tid == 0 ? e_first : e_last;
+        int lo = 0, hi = B;                              // largest r with off_a(r) <= e
         while (hi - lo > 1) {
             const int mid = lo + ((hi - lo) >> 1);
-            if (off_a(mid) <= a) lo = mid; else hi = mid;
+            if (off_a(mid) <= e) lo = mid; else hi = mid;
         }
-        return lo;
-    };
-    const int r_lo = owner(e_first);
-    const int r_hi = owner(e_last);
+        if (tid == 0) sh_rlo = lo; else sh_rhi = lo;
+    }
+    __syncthreads();
+    const int r_lo = sh_rlo;
+    const int r_hi = sh_rhi;
 
     // 4. Suffix rows (row[j] = t[L-1-j]) of the first kSufCap requests, and this
     //    CTA's slots cleared.
@@ -301,111 +383,127 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) scan_kernel(ScanParams p
     }
     __syncthreads();
 
-    auto suffix = [&](int r, int64_t nxt, int j) -> int32_t {
+    // Suffix token j of request r (t[L-1-j]); 0 past the start of the history.
+    auto suffix = [&](int r, int64_t o_r, int64_t nxt, int j) -> int32_t {
         const int row = r - r_lo;
-        return row < kSufCap ? suf_s[row * max_m + j] : ta[nxt - 1 - j];
+        if (row < kSufCap) return suf_s[row * max_m + j];
+        return (nxt - 1 - j >= o_r) ? ta[nxt - 1 - j] : 0;
     };
 
-    // Per-thread position in the batch: current request and its candidate range.
-    int r = r_lo;
-    int64_t nxt = off_a(r + 1);
-    int64_t lo = off_a(r) + (min_m - 1);    // first candidate end position
-    int64_t hi = nxt - 2;                    // last candidate end position (p + m <= L - 1)
-    int32_t last = suffix(r, nxt, 0);
-    int best_r = -1;
-    unsigned long long best_key = 0ull;
-
-    auto flush = [&]() {
-        if (best_key) red_max_u64(prm.slots + (int64_t(best_r) + c), best_key);
-    };
-    // Candidate end at aligned index a (its token equals `last`): extend backwards.
-    auto extend = [&](const int32_t *st, int64_t st_base, int64_t a) {
-        const int64_t q = a - off_a(r);                 // local end position
-        const int kmax = (int64_t(max_m) < q + 1) ? max_m : int(q + 1);
-        int k = 1;
-        while (k < kmax && st[a - k - st_base] == suffix(r, nxt, k)) ++k;
-        if (k >= min_m) {
-            const unsigned long long key =
-                (static_cast<unsigned long long>(k) << 32) | static_cast<uint32_t>(q - k + 1);
-            if (r != best_r) {
-                flush();
-                best_r = r;
-                best_key = key;
-            } else if (key > best_key) {
-                best_key = key;
-            }
-        }
-    };
-    auto advance_to = [&](int64_t a) {                 // make r the request holding a
-        if (a < nxt) return;
-        do {
-            ++r;
-            nxt = off_a(r + 1);
-        } while (a >= nxt);
-        lo = off_a(r) + (min_m - 1);
-        hi = nxt - 2;
-        last = suffix(r, nxt, 0);
-    };
-
-    // 5. Stream the tiles.
+    // 5. Stream this warp's tiles.
     bool failed = false;
-    int i = 0;
-    for (; i < ntiles; ++i) {
-        const int s = i % kStages;
-        const uint32_t parity = uint32_t(i / kStages) & 1u;
-        const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), parity, prm.wait_ns);
-        const int64_t t0 = qa + int64_t(i) * kTileQuads;
-        const int nq = int(((t0 + kTileQuads < qb) ? t0 + kTileQuads : qb) - t0);
-        if (ok) {
-            const unsigned char *stage = smem + lay.stages + size_t(s) * kStageBytes + kHaloQuads * 16;
-            const int4 *sq = reinterpret_cast<const int4 *>(stage);
-            const int32_t *st = reinterpret_cast<const int32_t *>(stage);
-            const int64_t st_base = 4 * t0;              // aligned index of st[0]
-            for (int j = tid; j < nq; j += kThreads) {
-                const int64_t a0 = st_base + 4 * int64_t(j);
-                const int4 v = sq[j];
-                if (a0 >= lo && a0 + 3 <= hi) {          // the whole quad is candidates of r
-                    if ((v.x == last) | (v.y == last) | (v.z == last) | (v.w == last)) {
-                        if (v.x == last) extend(st, st_base, a0);
-                        if (v.y == last) extend(st, st_base, a0 + 1);
-                        if (v.z == last) extend(st, st_base, a0 + 2);
-                        if (v.w == last) extend(st, st_base, a0 + 3);
-                    }
-                } else {
-                    const int32_t vals[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int64_t a = a0 + e;
-                        if (a < a_begin) continue;
-                        if (a >= a_end) break;
-                        advance_to(a);
-                        if (a >= lo && a <= hi && vals[e] == last) extend(st, st_base, a);
-                    }
-                }
-            }
-        }
-        if (__syncthreads_or(!ok)) {
+    int seg_r = r_lo;                                   // first request not yet finished
+    int k = 0;
+    for (; k < my_tiles; ++k) {
+        const int slot = k % kBufs;
+        const uint32_t bar = smem_addr(&my_bars[slot]);
+        if (!mbar_wait_until(bar, uint32_t(k / kBufs) & 1u, deadline) ||
+            *reinterpret_cast<volatile int *>(&sh_abort)) {
             failed = true;
+            sh_abort = 1;
             break;
         }
-        if (tid == 0 && i + kStages < ntiles) {
+        const int i = warp + kWarps * k;
+        const int64_t t0 = qa + int64_t(i) * tq;
+        const int nq = int(((t0 + tq < qb) ? t0 + tq : qb) - t0);
+        const unsigned char *buf = my_bufs + size_t(slot) * kBufBytes + kHaloQuads * 16;
+        const int4 *sq = reinterpret_cast<const int4 *>(buf);
+        const int32_t *st = reinterpret_cast<const int32_t *>(buf);
+        const int64_t base = 4 * t0;                     // aligned index of st[0]
+        const int64_t eb = base > a_begin ? base : a_begin;
+        const int64_t ee = (base + 4 * nq < a_end) ? base + 4 * nq : a_end;
+
+        // Requests overlapping this tile, in order (uniform across the warp).
+        while (seg_r < r_hi && off_a(seg_r + 1) <= eb) ++seg_r;
+        for (int r = seg_r; r <= r_hi; ++r) {
+            const int64_t o_r = off_a(r);
+            if (o_r >= ee) break;
+            const int64_t nxt = off_a(r + 1);
+            const int64_t lo = (o_r + (min_m - 1) > eb) ? o_r + (min_m - 1) : eb;   // candidate end range
+            const int64_t hi = (nxt - 2 < ee - 1) ? nxt - 2 : ee - 1;                // within this tile
+            if (lo > hi) continue;
+            const int lo_rel = int(lo - base), hi_rel = int(hi - base);
+            const int qoff = int(base - o_r);            // local position of st[0] in request r
+            const int32_t s0 = suffix(r, o_r, nxt, 0);
+            const int32_t s1 = D >= 2 ? suffix(r, o_r, nxt, 1) : 0;
+            unsigned long long best = 0ull;
+            // Candidate end at tile element e whose last k0 tokens already match:
+            // extend backwards, fold its key into `best`.
+            auto extend = [&](int e, int k0) {
+                const int q = qoff + e;                  // local end position in request r
+                const int kmax = max_m < q + 1 ? max_m : q + 1;
+                int kk = k0;
+                while (kk < kmax && st[e - kk] == suffix(r, o_r, nxt, kk)) ++kk;
+                if (kk >= min_m) {
+                    const unsigned long long key =
+                        (static_cast<unsigned long long>(kk) << 32) | static_cast<uint32_t>(q - kk + 1);
+                    best = key > best ? key : best;
+                }
+            };
+            // whole quads inside [lo_rel, hi_rel], then the partial quads at its ends
+            const int jq0 = (lo_rel + 3) >> 2;           // first quad fully inside
+            const int jq1 = ((hi_rel + 1) >> 2) - 1;     // last quad fully inside
+            // two quads per lane per iteration: independent loads and tests
+            int j = jq0 + lane;
+            for (; j + 32 <= jq1; j += 64) {
+                const int4 c0 = sq[j], c1 = sq[j + 32];
+                const int32_t p0 = D >= 2 ? st[4 * j - 1] : 0;          // the halo when j == 0
+                const int32_t p1 = D >= 2 ? st[4 * (j + 32) - 1] : 0;
+                unsigned h = quad_hits<D>(p0, c0, s0, s1) | (quad_hits<D>(p1, c1, s0, s1) << 4);
+                while (h) {
+                    const int b = __ffs(h) - 1;
+                    h &= h - 1;
+                    extend(4 * (j + (b >> 2) * 32) + (b & 3), D);
+                }
+            }
+            if (j <= jq1) {
+                const int4 c0 = sq[j];
+                const int32_t p0 = D >= 2 ? st[4 * j - 1] : 0;
+                unsigned h = quad_hits<D>(p0, c0, s0, s1);
+                while (h) {
+                    const int e = __ffs(h) - 1;
+                    h &= h - 1;
+                    extend(4 * j + e, D);
+                }
+            }
+            // elements of [lo_rel, hi_rel] outside whole quads: fewer than 8
+            {
+                const int head_end = 4 * jq0 < hi_rel + 1 ? 4 * jq0 : hi_rel + 1;   // [lo_rel, head_end)
+                const int tail_beg = 4 * (jq1 + 1) > lo_rel ? 4 * (jq1 + 1) : lo_rel;   // [tail_beg, hi_rel]
+                int e = -1;
+                if (lane < 4) e = lo_rel + lane < head_end ? lo_rel + lane : -1;
+                else if (lane < 8) e = tail_beg + (lane - 4) <= hi_rel && tail_beg + (lane - 4) >= head_end
+                                           ? tail_beg + (lane - 4) : -1;
+                if (e >= 0 && st[e] == s0) extend(e, 1);
+            }
+            if (__any_sync(0xffffffffu, best != 0ull)) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const unsigned long long v = __shfl_xor_sync(0xffffffffu, best, o);
+                    best = v > best ? v : best;
+                }
+                if (lane == 0) red_max_u64(prm.slots + (int64_t(r) + c), best);
+            }
+        }
+        // Refill this slot with the warp's tile k + kBufs.
+        __syncwarp();
+        if (lane == 0 && k + kBufs < my_tiles) {
             fence_proxy_async_smem();
-            issue_tile(i + kStages);
+            issue_tile(warp + kWarps * (k + kBufs), slot);
         }
     }
 
-    if (!failed) {
-        flush();
-        return;
-    }
-    // 6. A wait ran out: let this CTA's copies land (bounded), then mark every
-    //    request it owns as failed.  The stage of tile i is still outstanding, and
-    //    so are tiles i+1 .. min(i + kStages, ntiles) - 1.
-    if (tid == 0) {
-        const int stop = (i + kStages < ntiles) ? i + kStages : ntiles;
-        for (int k = i; k < stop; ++k)
-            (void)mbar_wait_bounded(smem_addr(&bars[k % kStages]), uint32_t(k / kStages) & 1u,
-                                    kDefaultWaitNs);
+    failed = __syncthreads_or(failed);
+    drain_offsets();
+    if (!failed) return;
+    // 6. A wait ran out: let this warp's copies land (bounded), then mark every
+    //    request the CTA owns as failed.  Copies k .. min(k + kBufs, my_tiles) - 1
+    //    may still be in flight for a warp that stopped at tile k.
+    if (lane == 0) {
+        const uint64_t drain_deadline = global_ns() + kDefaultWaitNs;
+        const int stop = (k + kBufs < my_tiles) ? k + kBufs : my_tiles;
+        for (int kk = k; kk < stop; ++kk)
+            (void)mbar_wait_until(smem_addr(&my_bars[kk % kBufs]), uint32_t(kk / kBufs) & 1u, drain_deadline);
     }
     __syncthreads();
     for (int rr = r_lo + tid; rr <= r_hi; rr += kThreads) red_max_u64(prm.slots + (int64_t(rr) + c), kKeyFailed);
@@ -415,27 +513,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) scan_kernel(ScanParams p
 __global__ void __launch_bounds__(kFillWarps * 32) fill_kernel(FillParams prm) {
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * kFillWarps + (threadIdx.x >> 5);
-    if (r >= prm.B) {
-        wait_for_prerequisite_grid();
-        return;
-    }
     // Inputs the scan does not write: read them before waiting for it.
-    const int64_t o0 = __ldg(prm.offsets + r);
-    const int64_t o1 = __ldg(prm.offsets + r + 1);
-    const int64_t first = __ldg(prm.offsets);
-    const int64_t end = __ldg(prm.offsets + prm.B);
+    int64_t o0 = 0, o1 = 0, first = 0, end = 0;
+    if (r < prm.B) {
+        o0 = __ldg(prm.offsets + r);
+        o1 = __ldg(prm.offsets + r + 1);
+        first = __ldg(prm.offsets);
+        end = __ldg(prm.offsets + prm.B);
+    }
     const int shift = tokens_shift(prm.tokens);
     const int64_t L = o1 - o0;
+    allow_dependent_launch();
     wait_for_prerequisite_grid();
+    if (r >= prm.B) return;
 
     unsigned long long key = 0ull;
     if (L > 0) {
-        const Partition P = make_partition(first + shift, end + shift);
-        const int64_t c0 = chunk_of_quad(P, (o0 + shift) >> 2, prm.grid);
-        const int64_t c1 = chunk_of_quad(P, (o1 - 1 + shift) >> 2, prm.grid);
+        const Partition P = make_partition(first + shift, end + shift, prm.grid);
+        const int64_t c0 = chunk_of_quad(P, (o0 + shift) >> 2);
+        const int64_t c1 = chunk_of_quad(P, (o1 - 1 + shift) >> 2);
         for (int64_t cc = c0 + lane; cc <= c1; cc += 32) {
-            // With fewer quads than CTAs some chunks are empty; their CTAs own no slot.
-            if (chunk_start(P, cc, prm.grid) == chunk_start(P, cc + 1, prm.grid)) continue;
             const unsigned long long v = prm.slots[int64_t(r) + cc];
             key = v > key ? v : key;
         }
@@ -499,7 +596,8 @@ int device_state(DeviceState **out) {
         int sms = 0;
         LD_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
         const ScanSmemLayout worst = scan_smem_layout(kOffCap - 1, LOOKUP_DRAFT_MAX_M);
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(worst.total)));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(worst.total)));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(worst.total)));
         cudaMemPoolProps props;
         std::memset(&props, 0, sizeof props);
         props.allocType = cudaMemAllocationTypePinned;
@@ -518,7 +616,8 @@ int device_state(DeviceState **out) {
     return LOOKUP_DRAFT_OK;
 }
 
-int grid_for(const DeviceState &st) { return st.sms * kCtasPerSm; }
+// One scan CTA per SM (its shared-memory ring admits no second one).
+int grid_for(const DeviceState &st) { return st.sms; }
 
 size_t workspace_bytes_for(int32_t B, int grid) { return (size_t(B) + size_t(grid)) * sizeof(unsigned long long); }
 
@@ -555,8 +654,19 @@ int launch_scan(const DeviceState &st, const int32_t *tokens, const int64_t *off
     prm.grid = grid_for(st);
     prm.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     const ScanSmemLayout lay = scan_smem_layout(B, max_m);
-    scan_kernel<<<prm.grid, kThreads, lay.total, stream>>>(prm);
-    LD_CUDA(cudaGetLastError());
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(unsigned(prm.grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = lay.total;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (min_m >= 2) LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<2>, prm));
+    else LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<1>, prm));
     return LOOKUP_DRAFT_OK;
 }
 

@@ -247,10 +247,11 @@ def test_repeated_calls_and_streams():
 
 
 def test_bounded_wait_failure_reaches_the_host():
-    """With a 1 ns wait limit the scan's first tile wait runs out; the kernel waits
-    for its copies with the default limit, marks its requests failed and returns.
-    The host sees LOOKUP_DRAFT_LEN_FAILED, and the next call is normal again."""
-    w = gen.make_workload("recitation25k")
+    """With a 1 ns wait limit the scan's tile waits run out (the limit counts from
+    each CTA's start); the kernel waits for its copies with the default limit,
+    marks its requests failed and returns.  The host sees
+    LOOKUP_DRAFT_LEN_FAILED, and the next call is normal again."""
+    w = gen.make_workload("ragged262k")
     t = torch.from_numpy(w.tokens).to(DEV)
     o = torch.from_numpy(w.offsets).to(DEV)
     want = oracle.lookup_draft(w.tokens, w.offsets, w.min_m, w.max_m, w.K, threads=8)
