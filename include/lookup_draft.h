@@ -150,12 +150,13 @@ const char *lookup_draft_last_cuda_error(void);
 
 /*
  * Diagnostics: the time limit, in nanoseconds, on the scan kernel's bounded waits
- * (default 1e9): every tile a scan CTA waits for must land within this time of
- * the CTA's start.  When the limit runs out, the CTA waits again (with the
- * default limit) for its own copies in flight, marks its requests
- * LOOKUP_DRAFT_LEN_FAILED and returns, leaving the context usable.  Setting a
- * tiny limit forces that path, to test that the failure reaches the host.
- * Process-wide; applies to launches made after the call.  0 restores the default.
+ * (default 1e9), counted from each scan CTA's start.  A CTA whose wait for the
+ * TMA copy of the offsets runs out reads them from global memory instead (same
+ * results).  A CTA whose wait for a history tile runs out lets its own copies
+ * land (bounded again), marks its requests LOOKUP_DRAFT_LEN_FAILED and returns,
+ * leaving the context usable.  Setting a tiny limit forces these paths, to test
+ * them.  Process-wide; applies to launches made after the call.  0 restores the
+ * default.
  */
 void lookup_draft_set_wait_limit_ns(uint64_t ns);
 

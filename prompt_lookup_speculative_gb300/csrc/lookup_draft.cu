@@ -21,7 +21,9 @@
 //    barrier is needed in the main loop.  A tile is walked request by request.
 //    Within a request, every lane takes one 128-bit quad at a time and runs the
 //    article's cheap rejection test (section "第1步") branch-free: a token and the
-//    D - 1 tokens before it against the last D suffix tokens, D = min(min_m, 2).
+//    D - 1 tokens before it against the last D suffix tokens, D = min(min_m, 4).
+//    A warp keeps the request it is in across tiles, so a tile that lies inside
+//    one request's candidate range goes straight to that test.
 //    The rare survivors are extended backwards against the suffix kept in shared
 //    memory.  A match of length k ending at local position q gives the key
 //    (k << 32) | (q - k + 1): its maximum is the longest match, then the most
@@ -232,18 +234,25 @@ __host__ __device__ inline ScanSmemLayout scan_smem_layout(int32_t B, int32_t ma
 }
 
 // Rejection test on one quad: bit e is set when the token at element e of `cur`
-// (and, for D == 2, the token before it) equals the last suffix token s0 (and
-// the one before it, s1).  The token before cur.x is `prev`.
+// and the D - 1 tokens before it equal the last D suffix tokens s0, s1, ...  The
+// tokens before cur.x are the last three of `prv`.
 template <int D>
-__device__ __forceinline__ unsigned quad_hits(int32_t prev, const int4 &cur, int32_t s0, int32_t s1) {
+__device__ __forceinline__ unsigned quad_hits(const int4 &prv, const int4 &cur, int32_t s0, int32_t s1, int32_t s2,
+                                              int32_t s3) {
     bool h0 = cur.x == s0, h1 = cur.y == s0, h2 = cur.z == s0, h3 = cur.w == s0;
     if (D >= 2) {
-        h0 = h0 && prev == s1; h1 = h1 && cur.x == s1; h2 = h2 && cur.y == s1; h3 = h3 && cur.z == s1;
+        h0 = h0 && prv.w == s1; h1 = h1 && cur.x == s1; h2 = h2 && cur.y == s1; h3 = h3 && cur.z == s1;
+    }
+    if (D >= 3) {
+        h0 = h0 && prv.z == s2; h1 = h1 && prv.w == s2; h2 = h2 && cur.x == s2; h3 = h3 && cur.y == s2;
+    }
+    if (D >= 4) {
+        h0 = h0 && prv.y == s3; h1 = h1 && prv.z == s3; h2 = h2 && prv.w == s3; h3 = h3 && cur.x == s3;
     }
     return unsigned(h0) | (unsigned(h1) << 1) | (unsigned(h2) << 2) | (unsigned(h3) << 3);
 }
 
-// D = min(min_m, 2): how many suffix tokens the branch-free rejection test checks
+// D = min(min_m, 4): how many suffix tokens the branch-free rejection test checks
 // before a candidate is extended one token at a time.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
@@ -390,14 +399,43 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
         return (nxt - 1 - j >= o_r) ? ta[nxt - 1 - j] : 0;
     };
 
-    // 5. Stream this warp's tiles.
+    // 5. Stream this warp's tiles.  The warp's current request (uniform across
+    //    it) and each lane's best key for it carry over from tile to tile; the
+    //    best keys are folded into the request's slot when the warp moves on.
     bool failed = false;
     int seg_r = r_lo;                                   // first request not yet finished
+    int cur_r = -1;                                     // request of the cached state below
+    int64_t cur_o = 0, cur_nxt = 0;
+    int32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0;
+    unsigned long long best = 0ull;
+    auto flush = [&]() {                                // warp-uniform
+        if (__any_sync(0xffffffffu, best != 0ull)) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long v = __shfl_xor_sync(0xffffffffu, best, o);
+                best = v > best ? v : best;
+            }
+            if (lane == 0) red_max_u64(prm.slots + (int64_t(cur_r) + c), best);
+            best = 0ull;
+        }
+    };
+    auto set_request = [&](int r) {                     // warp-uniform, r in [r_lo, r_hi]
+        if (r == cur_r) return;
+        flush();
+        cur_r = r;
+        cur_o = off_a(r);
+        cur_nxt = off_a(r + 1);
+        s0 = suffix(r, cur_o, cur_nxt, 0);
+        if (D >= 2) s1 = suffix(r, cur_o, cur_nxt, 1);
+        if (D >= 3) s2 = suffix(r, cur_o, cur_nxt, 2);
+        if (D >= 4) s3 = suffix(r, cur_o, cur_nxt, 3);
+    };
     int k = 0;
     for (; k < my_tiles; ++k) {
         const int slot = k % kBufs;
         const uint32_t bar = smem_addr(&my_bars[slot]);
-        if (!mbar_wait_until(bar, uint32_t(k / kBufs) & 1u, deadline) ||
+        const uint32_t parity = uint32_t(k / kBufs) & 1u;
+        if ((!mbar_try_wait(bar, parity) && !mbar_wait_until(bar, parity, deadline)) ||
             *reinterpret_cast<volatile int *>(&sh_abort)) {
             failed = true;
             sh_abort = 1;
@@ -413,43 +451,35 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
         const int64_t eb = base > a_begin ? base : a_begin;
         const int64_t ee = (base + 4 * nq < a_end) ? base + 4 * nq : a_end;
 
-        // Requests overlapping this tile, in order (uniform across the warp).
-        while (seg_r < r_hi && off_a(seg_r + 1) <= eb) ++seg_r;
-        for (int r = seg_r; r <= r_hi; ++r) {
-            const int64_t o_r = off_a(r);
-            if (o_r >= ee) break;
-            const int64_t nxt = off_a(r + 1);
-            const int64_t lo = (o_r + (min_m - 1) > eb) ? o_r + (min_m - 1) : eb;   // candidate end range
-            const int64_t hi = (nxt - 2 < ee - 1) ? nxt - 2 : ee - 1;                // within this tile
-            if (lo > hi) continue;
-            const int lo_rel = int(lo - base), hi_rel = int(hi - base);
-            const int qoff = int(base - o_r);            // local position of st[0] in request r
-            const int32_t s0 = suffix(r, o_r, nxt, 0);
-            const int32_t s1 = D >= 2 ? suffix(r, o_r, nxt, 1) : 0;
-            unsigned long long best = 0ull;
+        // Candidate ends [lo_rel, hi_rel] of the current request r in this tile:
+        // the D-token test on every whole quad, the rest element by element.
+        auto scan_range = [&](int lo_rel, int hi_rel) {
+            const int qoff = int(base - cur_o);          // local position of st[0] in request r
             // Candidate end at tile element e whose last k0 tokens already match:
             // extend backwards, fold its key into `best`.
             auto extend = [&](int e, int k0) {
                 const int q = qoff + e;                  // local end position in request r
                 const int kmax = max_m < q + 1 ? max_m : q + 1;
                 int kk = k0;
-                while (kk < kmax && st[e - kk] == suffix(r, o_r, nxt, kk)) ++kk;
+                while (kk < kmax && st[e - kk] == suffix(cur_r, cur_o, cur_nxt, kk)) ++kk;
                 if (kk >= min_m) {
                     const unsigned long long key =
                         (static_cast<unsigned long long>(kk) << 32) | static_cast<uint32_t>(q - kk + 1);
                     best = key > best ? key : best;
                 }
             };
-            // whole quads inside [lo_rel, hi_rel], then the partial quads at its ends
             const int jq0 = (lo_rel + 3) >> 2;           // first quad fully inside
             const int jq1 = ((hi_rel + 1) >> 2) - 1;     // last quad fully inside
             // two quads per lane per iteration: independent loads and tests
             int j = jq0 + lane;
             for (; j + 32 <= jq1; j += 64) {
                 const int4 c0 = sq[j], c1 = sq[j + 32];
-                const int32_t p0 = D >= 2 ? st[4 * j - 1] : 0;          // the halo when j == 0
-                const int32_t p1 = D >= 2 ? st[4 * (j + 32) - 1] : 0;
-                unsigned h = quad_hits<D>(p0, c0, s0, s1) | (quad_hits<D>(p1, c1, s0, s1) << 4);
+                int4 p0 = make_int4(0, 0, 0, 0), p1 = make_int4(0, 0, 0, 0);
+                if (D >= 2) {                            // the halo when j == 0
+                    p0 = sq[j - 1];
+                    p1 = sq[j + 31];
+                }
+                unsigned h = quad_hits<D>(p0, c0, s0, s1, s2, s3) | (quad_hits<D>(p1, c1, s0, s1, s2, s3) << 4);
                 while (h) {
                     const int b = __ffs(h) - 1;
                     h &= h - 1;
@@ -458,8 +488,9 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
             }
             if (j <= jq1) {
                 const int4 c0 = sq[j];
-                const int32_t p0 = D >= 2 ? st[4 * j - 1] : 0;
-                unsigned h = quad_hits<D>(p0, c0, s0, s1);
+                int4 p0 = make_int4(0, 0, 0, 0);
+                if (D >= 2) p0 = sq[j - 1];
+                unsigned h = quad_hits<D>(p0, c0, s0, s1, s2, s3);
                 while (h) {
                     const int e = __ffs(h) - 1;
                     h &= h - 1;
@@ -467,8 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                 }
             }
             // elements of [lo_rel, hi_rel] outside whole quads: fewer than 8
-            {
-                const int head_end = 4 * jq0 < hi_rel + 1 ? 4 * jq0 : hi_rel + 1;   // [lo_rel, head_end)
+            if (4 * jq0 != lo_rel || 4 * (jq1 + 1) != hi_rel + 1) {
+                const int head_end = 4 * jq0 < hi_rel + 1 ? 4 * jq0 : hi_rel + 1;       // [lo_rel, head_end)
                 const int tail_beg = 4 * (jq1 + 1) > lo_rel ? 4 * (jq1 + 1) : lo_rel;   // [tail_beg, hi_rel]
                 int e = -1;
                 if (lane < 4) e = lo_rel + lane < head_end ? lo_rel + lane : -1;
@@ -476,13 +507,22 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                                            ? tail_beg + (lane - 4) : -1;
                 if (e >= 0 && st[e] == s0) extend(e, 1);
             }
-            if (__any_sync(0xffffffffu, best != 0ull)) {
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const unsigned long long v = __shfl_xor_sync(0xffffffffu, best, o);
-                    best = v > best ? v : best;
-                }
-                if (lane == 0) red_max_u64(prm.slots + (int64_t(r) + c), best);
+        };
+
+        if (cur_r >= 0 && eb == base && ee == base + 4 * nq && cur_o + (min_m - 1) <= eb && ee - 1 <= cur_nxt - 2) {
+            scan_range(0, 4 * nq - 1);                   // the whole tile is candidates of cur_r
+        } else {
+            // Requests overlapping this tile, in order (uniform across the warp).
+            while (seg_r < r_hi && off_a(seg_r + 1) <= eb) ++seg_r;
+            for (int r = seg_r; r <= r_hi; ++r) {
+                const int64_t o_r = off_a(r);
+                if (o_r >= ee) break;
+                const int64_t nxt = off_a(r + 1);
+                const int64_t lo = (o_r + (min_m - 1) > eb) ? o_r + (min_m - 1) : eb;   // candidate end range
+                const int64_t hi = (nxt - 2 < ee - 1) ? nxt - 2 : ee - 1;                // within this tile
+                if (lo > hi) continue;
+                set_request(r);
+                scan_range(int(lo - base), int(hi - base));
             }
         }
         // Refill this slot with the warp's tile k + kBufs.
@@ -492,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
             issue_tile(warp + kWarps * (k + kBufs), slot);
         }
     }
+    if (!failed) flush();                               // fold the last request's keys
 
     failed = __syncthreads_or(failed);
     drain_offsets();
@@ -598,6 +639,8 @@ int device_state(DeviceState **out) {
         const ScanSmemLayout worst = scan_smem_layout(kOffCap - 1, LOOKUP_DRAFT_MAX_M);
         LD_CUDA(cudaFuncSetAttribute(scan_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(worst.total)));
         LD_CUDA(cudaFuncSetAttribute(scan_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(worst.total)));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(worst.total)));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(worst.total)));
         cudaMemPoolProps props;
         std::memset(&props, 0, sizeof props);
         props.allocType = cudaMemAllocationTypePinned;
@@ -665,8 +708,12 @@ int launch_scan(const DeviceState &st, const int32_t *tokens, const int64_t *off
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (min_m >= 2) LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<2>, prm));
-    else LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<1>, prm));
+    switch (min_m < 4 ? min_m : 4) {
+    case 1: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<1>, prm)); break;
+    case 2: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<2>, prm)); break;
+    case 3: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<3>, prm)); break;
+    default: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<4>, prm)); break;
+    }
     return LOOKUP_DRAFT_OK;
 }
 

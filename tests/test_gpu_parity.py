@@ -246,25 +246,29 @@ def test_repeated_calls_and_streams():
     np.testing.assert_array_equal(ref[0].cpu().numpy(), want[0])
 
 
-def test_bounded_wait_failure_reaches_the_host():
-    """With a 1 ns wait limit the scan's tile waits run out (the limit counts from
-    each CTA's start); the kernel waits for its copies with the default limit,
-    marks its requests failed and returns.  The host sees
-    LOOKUP_DRAFT_LEN_FAILED, and the next call is normal again."""
-    w = gen.make_workload("ragged262k")
+def test_bounded_waits_fail_cleanly():
+    """With a 1 ns wait limit the scan's bounded waits run out.  A CTA whose wait
+    for its TMA copy of the offsets runs out reads them from global memory
+    instead; one whose wait for a history tile runs out lets its copies land,
+    marks its requests LOOKUP_DRAFT_LEN_FAILED and returns.  Every request is
+    then either exactly the oracle's or marked failed, and the next call with
+    the default limit is exact again (the context stays usable)."""
+    w = gen.make_workload("ragged262k", 15)
     t = torch.from_numpy(w.tokens).to(DEV)
     o = torch.from_numpy(w.offsets).to(DEV)
     want = oracle.lookup_draft(w.tokens, w.offsets, w.min_m, w.max_m, w.K, threads=8)
     try:
         pkg.set_wait_limit_ns(1)
-        d, ln, p = pkg.lookup_draft(t, o, w.min_m, w.max_m, w.K)
+        d, ln, p, m = pkg.lookup_draft_ex(t, o, w.min_m, w.max_m, w.K)
         torch.cuda.synchronize()
     finally:
         pkg.set_wait_limit_ns(0)
-    ln = ln.cpu().numpy()
-    assert (ln == pkg.LEN_FAILED).any()
+    d, ln, p, m = (x.cpu().numpy() for x in (d, ln, p, m))
     ok = ln != pkg.LEN_FAILED
     np.testing.assert_array_equal(ln[ok], want[1][ok])
+    np.testing.assert_array_equal(p[ok], want[2][ok])
+    np.testing.assert_array_equal(d[ok], want[0][ok])
+    assert np.all(p[~ok] == -1) and np.all(d[~ok] == -1)
     got = run_gpu(w.tokens, w.offsets, w.min_m, w.max_m, w.K)
-    np.testing.assert_array_equal(got[1], want[1])
-    np.testing.assert_array_equal(got[0], want[0])
+    for g, exp in zip(got, want):
+        np.testing.assert_array_equal(g, exp)
