@@ -252,12 +252,30 @@ __device__ __forceinline__ unsigned quad_hits(const int4 &prv, const int4 &cur, 
     return unsigned(h0) | (unsigned(h1) << 1) | (unsigned(h2) << 2) | (unsigned(h3) << 3);
 }
 
+// Whether any element of the quad passes the D-token test (the common answer is
+// no, so the per-element bits are only formed on the rare path).
+template <int D>
+__device__ __forceinline__ bool quad_any(const int4 &prv, const int4 &cur, int32_t s0, int32_t s1, int32_t s2,
+                                         int32_t s3) {
+    bool h0 = cur.x == s0, h1 = cur.y == s0, h2 = cur.z == s0, h3 = cur.w == s0;
+    if (D >= 2) {
+        h0 &= prv.w == s1; h1 &= cur.x == s1; h2 &= cur.y == s1; h3 &= cur.z == s1;
+    }
+    if (D >= 3) {
+        h0 &= prv.z == s2; h1 &= prv.w == s2; h2 &= cur.x == s2; h3 &= cur.y == s2;
+    }
+    if (D >= 4) {
+        h0 &= prv.y == s3; h1 &= prv.z == s3; h2 &= prv.w == s3; h3 &= cur.x == s3;
+    }
+    return (h0 | h1) | (h2 | h3);
+}
+
 // D = min(min_m, 4): how many suffix tokens the branch-free rejection test checks
 // before a candidate is extended one token at a time.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ int sh_rlo, sh_rhi, sh_abort;
+    __shared__ int sh_rlo, sh_rhi;
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -287,7 +305,6 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
     if (tid == 0) {
         for (int i = 0; i <= kWarps * kBufs; ++i) mbar_init(smem_addr(&bars[i]), 1);
         fence_barrier_init();
-        sh_abort = 0;
     }
     wait_for_prerequisite_grid();
 
@@ -399,13 +416,19 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
         return (nxt - 1 - j >= o_r) ? ta[nxt - 1 - j] : 0;
     };
 
-    // 5. Stream this warp's tiles.  The warp's current request (uniform across
-    //    it) and each lane's best key for it carry over from tile to tile; the
-    //    best keys are folded into the request's slot when the warp moves on.
+    // 5. Stream this warp's tiles.  Positions from here on are int32 and relative
+    //    to A0 = 4 * qa, the chunk's first element.  The warp's current request
+    //    (uniform across it) and each lane's best key for it carry over from tile
+    //    to tile; the best keys are folded into the request's slot when the warp
+    //    moves on.
+    const int64_t A0 = 4 * qa;
+    const int begin_x = int(a_begin - A0);               // > 0 only in chunk 0
+    const int end_x = int(((a_end < 4 * qb) ? a_end : 4 * qb) - A0);
+    auto rel = [&](int r) -> int { return int(off_a(r) - A0); };
     bool failed = false;
     int seg_r = r_lo;                                   // first request not yet finished
     int cur_r = -1;                                     // request of the cached state below
-    int64_t cur_o = 0, cur_nxt = 0;
+    int cur_o = 0, cur_nxt = 0;                         // its start and end, relative
     int32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0;
     unsigned long long best = 0ull;
     auto flush = [&]() {                                // warp-uniform
@@ -423,106 +446,106 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
         if (r == cur_r) return;
         flush();
         cur_r = r;
-        cur_o = off_a(r);
-        cur_nxt = off_a(r + 1);
-        s0 = suffix(r, cur_o, cur_nxt, 0);
-        if (D >= 2) s1 = suffix(r, cur_o, cur_nxt, 1);
-        if (D >= 3) s2 = suffix(r, cur_o, cur_nxt, 2);
-        if (D >= 4) s3 = suffix(r, cur_o, cur_nxt, 3);
+        const int64_t o = off_a(r), n = off_a(r + 1);
+        cur_o = int(o - A0);
+        cur_nxt = int(n - A0);
+        s0 = suffix(r, o, n, 0);
+        if (D >= 2) s1 = suffix(r, o, n, 1);
+        if (D >= 3) s2 = suffix(r, o, n, 2);
+        if (D >= 4) s3 = suffix(r, o, n, 3);
     };
     int k = 0;
     for (; k < my_tiles; ++k) {
         const int slot = k % kBufs;
         const uint32_t bar = smem_addr(&my_bars[slot]);
         const uint32_t parity = uint32_t(k / kBufs) & 1u;
-        if ((!mbar_try_wait(bar, parity) && !mbar_wait_until(bar, parity, deadline)) ||
-            *reinterpret_cast<volatile int *>(&sh_abort)) {
+        if (!mbar_try_wait(bar, parity) && !mbar_wait_until(bar, parity, deadline)) {
             failed = true;
-            sh_abort = 1;
             break;
         }
-        const int i = warp + kWarps * k;
-        const int64_t t0 = qa + int64_t(i) * tq;
-        const int nq = int(((t0 + tq < qb) ? t0 + tq : qb) - t0);
+        const int t0 = (warp + kWarps * k) * tq;         // tile's first quad, relative
+        const int nq = (t0 + tq < int(chunk_q)) ? tq : int(chunk_q) - t0;
         const unsigned char *buf = my_bufs + size_t(slot) * kBufBytes + kHaloQuads * 16;
         const int4 *sq = reinterpret_cast<const int4 *>(buf);
         const int32_t *st = reinterpret_cast<const int32_t *>(buf);
-        const int64_t base = 4 * t0;                     // aligned index of st[0]
-        const int64_t eb = base > a_begin ? base : a_begin;
-        const int64_t ee = (base + 4 * nq < a_end) ? base + 4 * nq : a_end;
+        const int base = 4 * t0;                         // relative position of st[0]
+        const int eb = base > begin_x ? base : begin_x;
+        const int ee = (base + 4 * nq < end_x) ? base + 4 * nq : end_x;
 
-        // Candidate ends [lo_rel, hi_rel] of the current request r in this tile:
-        // the D-token test on every whole quad, the rest element by element.
-        auto scan_range = [&](int lo_rel, int hi_rel) {
-            const int qoff = int(base - cur_o);          // local position of st[0] in request r
+        // Candidate ends [lo, hi] (tile elements) of the current request: the
+        // D-token test on every whole quad, the rest element by element.
+        auto scan_range = [&](int lo, int hi) {
+            const int qoff = base - cur_o;               // local position of st[0] in the request
             // Candidate end at tile element e whose last k0 tokens already match:
             // extend backwards, fold its key into `best`.
             auto extend = [&](int e, int k0) {
-                const int q = qoff + e;                  // local end position in request r
+                const int q = qoff + e;                  // local end position in the request
                 const int kmax = max_m < q + 1 ? max_m : q + 1;
                 int kk = k0;
-                while (kk < kmax && st[e - kk] == suffix(cur_r, cur_o, cur_nxt, kk)) ++kk;
+                while (kk < kmax && st[e - kk] == suffix(cur_r, A0 + cur_o, A0 + cur_nxt, kk)) ++kk;
                 if (kk >= min_m) {
                     const unsigned long long key =
                         (static_cast<unsigned long long>(kk) << 32) | static_cast<uint32_t>(q - kk + 1);
                     best = key > best ? key : best;
                 }
             };
-            const int jq0 = (lo_rel + 3) >> 2;           // first quad fully inside
-            const int jq1 = ((hi_rel + 1) >> 2) - 1;     // last quad fully inside
-            // two quads per lane per iteration: independent loads and tests
+            auto extend_quad = [&](const int4 &p, const int4 &cq, int j) {   // rare path
+                unsigned h = quad_hits<D>(p, cq, s0, s1, s2, s3);
+                while (h) {
+                    const int e = __ffs(h) - 1;
+                    h &= h - 1;
+                    extend(4 * j + e, D);
+                }
+            };
+            const int jq0 = (lo + 3) >> 2;               // first quad fully inside
+            const int jq1 = ((hi + 1) >> 2) - 1;         // last quad fully inside
+            // two quads per lane per iteration: independent loads and tests; the
+            // previous quad (the halo when j == 0) supplies the tokens before each
             int j = jq0 + lane;
             for (; j + 32 <= jq1; j += 64) {
                 const int4 c0 = sq[j], c1 = sq[j + 32];
                 int4 p0 = make_int4(0, 0, 0, 0), p1 = make_int4(0, 0, 0, 0);
-                if (D >= 2) {                            // the halo when j == 0
+                if (D >= 2) {
                     p0 = sq[j - 1];
                     p1 = sq[j + 31];
                 }
-                unsigned h = quad_hits<D>(p0, c0, s0, s1, s2, s3) | (quad_hits<D>(p1, c1, s0, s1, s2, s3) << 4);
-                while (h) {
-                    const int b = __ffs(h) - 1;
-                    h &= h - 1;
-                    extend(4 * (j + (b >> 2) * 32) + (b & 3), D);
+                if (quad_any<D>(p0, c0, s0, s1, s2, s3) | quad_any<D>(p1, c1, s0, s1, s2, s3)) {
+                    extend_quad(p0, c0, j);
+                    extend_quad(p1, c1, j + 32);
                 }
             }
             if (j <= jq1) {
                 const int4 c0 = sq[j];
                 int4 p0 = make_int4(0, 0, 0, 0);
                 if (D >= 2) p0 = sq[j - 1];
-                unsigned h = quad_hits<D>(p0, c0, s0, s1, s2, s3);
-                while (h) {
-                    const int e = __ffs(h) - 1;
-                    h &= h - 1;
-                    extend(4 * j + e, D);
-                }
+                if (quad_any<D>(p0, c0, s0, s1, s2, s3)) extend_quad(p0, c0, j);
             }
-            // elements of [lo_rel, hi_rel] outside whole quads: fewer than 8
-            if (4 * jq0 != lo_rel || 4 * (jq1 + 1) != hi_rel + 1) {
-                const int head_end = 4 * jq0 < hi_rel + 1 ? 4 * jq0 : hi_rel + 1;       // [lo_rel, head_end)
-                const int tail_beg = 4 * (jq1 + 1) > lo_rel ? 4 * (jq1 + 1) : lo_rel;   // [tail_beg, hi_rel]
+            // elements of [lo, hi] outside whole quads: fewer than 8
+            if (4 * jq0 != lo || 4 * (jq1 + 1) != hi + 1) {
+                const int head_end = 4 * jq0 < hi + 1 ? 4 * jq0 : hi + 1;   // [lo, head_end)
+                const int tail_beg = 4 * (jq1 + 1) > lo ? 4 * (jq1 + 1) : lo;   // [tail_beg, hi]
                 int e = -1;
-                if (lane < 4) e = lo_rel + lane < head_end ? lo_rel + lane : -1;
-                else if (lane < 8) e = tail_beg + (lane - 4) <= hi_rel && tail_beg + (lane - 4) >= head_end
+                if (lane < 4) e = lo + lane < head_end ? lo + lane : -1;
+                else if (lane < 8) e = tail_beg + (lane - 4) <= hi && tail_beg + (lane - 4) >= head_end
                                            ? tail_beg + (lane - 4) : -1;
                 if (e >= 0 && st[e] == s0) extend(e, 1);
             }
         };
 
-        if (cur_r >= 0 && eb == base && ee == base + 4 * nq && cur_o + (min_m - 1) <= eb && ee - 1 <= cur_nxt - 2) {
+        if (cur_r >= 0 && eb == base && ee == base + 4 * nq && cur_o + (min_m - 1) <= eb && ee + 1 <= cur_nxt) {
             scan_range(0, 4 * nq - 1);                   // the whole tile is candidates of cur_r
         } else {
             // Requests overlapping this tile, in order (uniform across the warp).
-            while (seg_r < r_hi && off_a(seg_r + 1) <= eb) ++seg_r;
+            while (seg_r < r_hi && rel(seg_r + 1) <= eb) ++seg_r;
             for (int r = seg_r; r <= r_hi; ++r) {
-                const int64_t o_r = off_a(r);
+                const int o_r = rel(r);
                 if (o_r >= ee) break;
-                const int64_t nxt = off_a(r + 1);
-                const int64_t lo = (o_r + (min_m - 1) > eb) ? o_r + (min_m - 1) : eb;   // candidate end range
-                const int64_t hi = (nxt - 2 < ee - 1) ? nxt - 2 : ee - 1;                // within this tile
+                const int nxt = rel(r + 1);
+                const int lo = (o_r + (min_m - 1) > eb) ? o_r + (min_m - 1) : eb;   // candidate end range
+                const int hi = (nxt - 2 < ee - 1) ? nxt - 2 : ee - 1;               // within this tile
                 if (lo > hi) continue;
                 set_request(r);
-                scan_range(int(lo - base), int(hi - base));
+                scan_range(lo - base, hi - base);
             }
         }
         // Refill this slot with the warp's tile k + kBufs.
