@@ -12,23 +12,23 @@
 //  scan_kernel -- the split-history scan, HBM bound (4 bytes per history token,
 //    read once).  The whole batch is one array of 16-byte quads; the grid (one CTA
 //    per SM, independent of the data so the host never reads the offsets) splits
-//    it into equal contiguous chunks, so long requests are shared by many CTAs and
+//    it into equal contiguous chunks, and each CTA's chunk into 16 equal warp
+//    ranges ("virtual chunks"), so long requests are shared by many warps and
 //    short ones are packed into one.  The offsets arrive in shared memory with one
-//    TMA bulk copy.  Each warp then streams its own tiles of the chunk (tiles
-//    w, w+16, w+32, ... of the CTA's chunk) through a private ring of shared-memory
-//    buffers filled by 1-D TMA bulk copies (cp.async.bulk, mbarrier completion),
-//    each tile preceded by a halo of up to 31 tokens of backward context; no CTA
-//    barrier is needed in the main loop.  A tile is walked request by request.
-//    Within a request, every lane takes one 128-bit quad at a time and runs the
-//    article's cheap rejection test (section "第1步") branch-free: a token and the
-//    D - 1 tokens before it against the last D suffix tokens, D = min(min_m, 4).
-//    A warp keeps the request it is in across tiles, so a tile that lies inside
-//    one request's candidate range goes straight to that test.
-//    The rare survivors are extended backwards against the suffix kept in shared
-//    memory.  A match of length k ending at local position q gives the key
-//    (k << 32) | (q - k + 1): its maximum is the longest match, then the most
-//    recent.  A lane folds its best key per request into a per-(request, CTA)
-//    slot with one red.max.
+//    TMA bulk copy; from then on every warp works alone.  A warp first loads the
+//    suffix tokens of the requests in its range (ahead of its bulk history reads,
+//    so they are not queued behind them), then streams its range through a
+//    private ring of shared-memory buffers filled by 1-D TMA bulk copies
+//    (cp.async.bulk, mbarrier completion), each tile preceded by a halo of up to
+//    31 tokens of backward context.  A tile is walked request by request; within
+//    a request every lane takes 128-bit quads and runs the article's cheap
+//    rejection test (section "第1步") branch-free: a token and the D - 1 tokens
+//    before it against the last D suffix tokens, D = min(min_m, 4).  The rare
+//    survivors are extended backwards.  A match of length k ending at local
+//    position q gives the key (k << 32) | (q - k + 1): its maximum is the longest
+//    match, then the most recent.  A warp keeps its current request and its
+//    lanes' best keys across tiles and writes the warp's maximum into the
+//    (request, virtual chunk) slot when it moves on.
 //
 //  fill_kernel -- one warp per request: max over the request's slots, then the
 //    draft tokens t[p + m + (j mod d)], d = L - p - m, and the length/position.
@@ -37,14 +37,15 @@
 // the stream start its prologue early and waits for its predecessor's results
 // before reading them.
 //
-// Partial-result slots.  CTA c owns slot (r + c) for every request r that has a
-// token in its chunk.  Chunks and requests are both ordered and disjoint, so the
-// (c, r) pairs form a monotone staircase and r + c never repeats: no slot is shared
-// and none needs clearing before a call (each CTA zeroes its own before use).
+// Partial-result slots.  Virtual chunk v owns slot (r + v) for every non-empty
+// request r that has a token in its range.  Virtual chunks and requests are both
+// ordered and disjoint, so the (v, r) pairs form a monotone staircase and r + v
+// never repeats: every slot has one writer (one warp), needs no atomics, and no
+// clearing before a call (its warp zeroes it before use).
 //
-// No spin-wait is unbounded: every mbarrier wait gives up at a deadline, and a
-// CTA that gives up waits (bounded) for its own copies, marks its requests as
-// failed in their slots and exits, so the failure reaches the host as
+// No spin-wait is unbounded: every mbarrier wait gives up at a deadline.  A warp
+// that gives up lets its own copies land (bounded), marks its requests as failed
+// in their slots and stops, so the failure reaches the host as
 // out_len = LOOKUP_DRAFT_LEN_FAILED instead of a hang.
 
 #include "lookup_draft.h"
@@ -60,13 +61,14 @@
 namespace {
 
 // ---------------------------------------------------------------- tuning ----
-constexpr int kWarps = 16;             // scan warps per CTA; each streams its own tiles
+constexpr int kWarps = 16;             // scan warps per CTA; each owns a contiguous range
 constexpr int kThreads = kWarps * 32;
 constexpr int kBufs = 3;               // tiles in flight per warp
 constexpr int kTileQuadsMax = 192;     // 3 KB of history per tile at most
 constexpr int kTileQuadsMin = 32;
 constexpr int kHaloQuads = 8;          // room for (LOOKUP_DRAFT_MAX_M - 1) tokens of context
-constexpr int kSufCap = 64;            // requests per CTA whose suffix is kept in smem
+constexpr int kSufRows = 8;            // requests per warp whose suffix is kept in smem
+constexpr int kSufRegs = kSufRows * LOOKUP_DRAFT_MAX_M / 32;   // suffix loads per lane
 constexpr int kOffCap = 4097;          // offsets kept in smem when B + 1 <= kOffCap
 constexpr int kFillWarps = 4;          // requests per fill CTA
 
@@ -103,15 +105,15 @@ struct FillParams {
 
 // ------------------------------------------------------ partition helpers ----
 // The batch occupies aligned quads [q_lo, q_lo + nq) of the 16-byte-aligned view
-// of `tokens`.  Chunk c is quads [q_lo + c*S, q_lo + (c+1)*S) clipped to the batch,
-// with S = ceil(nq / G): every chunk but the last non-empty one holds S quads, and
-// the empty ones (if any) all come last.
+// of `tokens`.  Chunk c (CTA c) is quads [c*S, (c+1)*S) of that range, clipped,
+// with S = ceil(nq / G); warp w of chunk c takes quads [c*S + w*Sw, c*S + (w+1)*Sw)
+// of it, clipped to the chunk, with Sw = ceil(S / kWarps).  Virtual chunk
+// v = c*kWarps + w.  Empty chunks and empty warp ranges come last in their order.
 struct Partition {
-    int64_t a_begin;    // first history token, index in the aligned view
-    int64_t a_end;      // one past the last
     int64_t q_lo;
     int64_t nq;
     int64_t S;          // quads per chunk
+    int64_t Sw;         // quads per warp range
 };
 
 __host__ __device__ inline int tokens_shift(const int32_t *tokens) {
@@ -126,16 +128,27 @@ __device__ inline int64_t div_u(int64_t x, int64_t y) {
 
 __device__ inline Partition make_partition(int64_t a_begin, int64_t a_end, int G) {
     Partition P;
-    P.a_begin = a_begin;
-    P.a_end = a_end;
     P.q_lo = a_begin >> 2;
     P.nq = ((a_end + 3) >> 2) - P.q_lo;
     P.S = div_u(P.nq + G - 1, G);
+    P.Sw = div_u(P.S + kWarps - 1, kWarps);
     return P;
 }
 
-// The chunk holding aligned quad x.
-__device__ inline int64_t chunk_of_quad(const Partition &P, int64_t x) { return div_u(x - P.q_lo, P.S); }
+// Quads [lo, hi) of virtual chunk v, relative to q_lo (empty when lo >= hi).
+__device__ inline void vchunk_range(const Partition &P, int64_t v, int64_t &lo, int64_t &hi) {
+    const int64_t c = v / kWarps, w = v - c * kWarps;
+    const int64_t c0 = c * P.S;
+    const int64_t c1 = (c0 + P.S < P.nq) ? c0 + P.S : P.nq;
+    lo = c0 + w * P.Sw;
+    hi = (lo + P.Sw < c1) ? lo + P.Sw : c1;
+}
+
+// The virtual chunk holding quad x (relative to q_lo, 0 <= x < nq).
+__device__ inline int64_t vchunk_of_quad(const Partition &P, int64_t x) {
+    const int64_t c = div_u(x, P.S);
+    return c * kWarps + div_u(x - c * P.S, P.Sw);
+}
 
 // ----------------------------------------------------------- PTX wrappers ----
 __device__ inline uint32_t smem_addr(const void *p) {
@@ -199,10 +212,6 @@ __device__ inline bool mbar_wait_until(uint32_t bar, uint32_t parity, uint64_t d
     }
 }
 
-__device__ inline void red_max_u64(unsigned long long *p, unsigned long long v) {
-    atomicMax(p, v);   // result unused: compiles to a fire-and-forget reduction
-}
-
 // Programmatic dependent launch: let the next kernel on the stream start its
 // prologue now / wait until the previous kernel's results are visible.
 __device__ inline void allow_dependent_launch() {
@@ -215,8 +224,8 @@ __device__ inline void wait_for_prerequisite_grid() {
 
 // ------------------------------------------------------------ scan kernel ----
 // Dynamic shared memory: the warps' tile rings, their mbarriers (plus one for the
-// offsets copy), the suffix rows, and the offsets.  The ring alone exceeds half
-// of an SM's shared memory, so exactly one scan CTA runs per SM.
+// offsets copy), the warps' suffix rows, and the offsets.  The rings alone exceed
+// half of an SM's shared memory, so exactly one scan CTA runs per SM.
 struct ScanSmemLayout {
     size_t bufs, bars, suf, offs, total;
 };
@@ -226,7 +235,7 @@ __host__ __device__ inline ScanSmemLayout scan_smem_layout(int32_t B, int32_t ma
     L.bufs = 0;
     L.bars = L.bufs + size_t(kWarps) * kBufs * kBufBytes;
     L.suf = L.bars + (size_t(kWarps) * kBufs + 1) * sizeof(unsigned long long);
-    L.offs = (L.suf + size_t(kSufCap) * size_t(max_m) * 4 + 15) & ~size_t(15);
+    L.offs = (L.suf + size_t(kWarps) * kSufRows * size_t(max_m) * 4 + 15) & ~size_t(15);
     // offsets copied as the 16-byte-aligned span covering them
     const size_t n_off = (int64_t(B) + 1 <= kOffCap) ? size_t(B) + 1 : 2;
     L.total = L.offs + ((n_off * 8 + 16 + 15) & ~size_t(15));
@@ -275,7 +284,6 @@ __device__ __forceinline__ bool quad_any(const int4 &prv, const int4 &cur, int32
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ int sh_rlo, sh_rhi;
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -290,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
     const ScanSmemLayout lay = scan_smem_layout(B, max_m);
     unsigned long long *bars = reinterpret_cast<unsigned long long *>(smem + lay.bars);
     unsigned long long *offs_bar = bars + kWarps * kBufs;
-    int32_t *suf_s = reinterpret_cast<int32_t *>(smem + lay.suf);
+    int32_t *suf_w = reinterpret_cast<int32_t *>(smem + lay.suf) + warp * kSufRows * max_m;
 
     const int shift = tokens_shift(prm.tokens);
     const int32_t *ta = reinterpret_cast<const int32_t *>(reinterpret_cast<uintptr_t>(prm.tokens) & ~uintptr_t(15));
@@ -323,254 +331,245 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
     if (offs_in_smem) ok = mbar_wait_until(smem_addr(offs_bar), 0, deadline);
     const bool offs_smem = offs_in_smem && !__syncthreads_or(!ok);
     const bool offs_pending = offs_in_smem && !offs_smem;
-    auto drain_offsets = [&]() {
-        if (offs_pending && tid == 0) (void)mbar_wait_until(smem_addr(offs_bar), 0, global_ns() + kDefaultWaitNs);
-    };
-
     auto off_a = [&](int i) -> int64_t {
         return (offs_smem ? offs_s[i] : __ldg(prm.offsets + i)) + shift;
+    };
+    // largest r in [lo, hi] with off_a(r) <= e (off_a(lo) <= e assumed)
+    auto owner = [&](int64_t e, int lo, int hi) -> int {
+        ++hi;
+        while (hi - lo > 1) {
+            const int mid = lo + ((hi - lo) >> 1);
+            if (off_a(mid) <= e) lo = mid; else hi = mid;
+        }
+        return lo;
     };
 
     const int64_t a_begin = off_a(0);
     const int64_t a_end = off_a(B);
     allow_dependent_launch();
-    if (a_end <= a_begin) {                             // no history tokens at all
-        drain_offsets();
-        return;
-    }
-    const Partition P = make_partition(a_begin, a_end, G);
-    const int64_t q_hi = P.q_lo + P.nq;
-    const int64_t qa = P.q_lo + int64_t(c) * P.S;
-    if (qa >= q_hi) {                                   // empty chunk: owns no slot
-        drain_offsets();
-        return;
-    }
-    const int64_t qb = (qa + P.S < q_hi) ? qa + P.S : q_hi;
-
-    // 2. Tiles: tile i of this chunk is quads [qa + i*tq, ...), streamed by warp
-    //    i % kWarps through its ring; each warp starts its first copies now.
-    const int halo = (max_m - 1 + 3) >> 2;
-    const int64_t chunk_q = qb - qa;
-    int tq = int((chunk_q + 2 * kWarps - 1) / (2 * kWarps));
-    tq = tq < kTileQuadsMin ? kTileQuadsMin : (tq > kTileQuadsMax ? kTileQuadsMax : tq);
-    const int ntiles = int((chunk_q + tq - 1) / tq);
-    unsigned char *my_bufs = smem + lay.bufs + size_t(warp) * kBufs * kBufBytes;
-    unsigned long long *my_bars = bars + warp * kBufs;
-    auto issue_tile = [&](int i, int slot) {           // lane 0 only
-        const int64_t t0 = qa + int64_t(i) * tq;
-        const int64_t t1 = (t0 + tq < qb) ? t0 + tq : qb;
-        const int64_t ls = (t0 - halo > P.q_lo) ? t0 - halo : P.q_lo;
-        const uint32_t bytes = uint32_t(t1 - ls) * 16u;
-        unsigned char *buf = my_bufs + size_t(slot) * kBufBytes;
-        const uint32_t bar = smem_addr(&my_bars[slot]);
-        mbar_expect_tx(bar, bytes);
-        bulk_copy_g2s(smem_addr(buf + size_t(kHaloQuads - (t0 - ls)) * 16), ta + ls * 4, bytes, bar);
-    };
-    // this warp's tiles: i = warp + kWarps * k, k = 0, 1, ...; tile k uses slot k % kBufs
-    const int my_tiles = (ntiles > warp) ? (ntiles - warp + kWarps - 1) / kWarps : 0;
-    if (lane == 0) {
-        const int first = my_tiles < kBufs ? my_tiles : kBufs;
-        for (int k = 0; k < first; ++k) issue_tile(warp + kWarps * k, k);
-    }
-
-    // 3. Requests with a token in this chunk: [r_lo, r_hi].
-    const int64_t e_first = (4 * qa > a_begin) ? 4 * qa : a_begin;
-    const int64_t e_last = ((4 * qb < a_end) ? 4 * qb : a_end) - 1;
-    if (offs_smem) {
-        for (int i = tid; i < B; i += kThreads) {
-            const int64_t o0 = offs_s[i] + shift, o1 = offs_s[i + 1] + shift;
-            if (o0 <= e_first && e_first < o1) sh_rlo = i;
-            if (o0 <= e_last && e_last < o1) sh_rhi = i;
-        }
-    } else if (tid < 2) {
-        const int64_t e = tid == 0 ? e_first : e_last;
-        int lo = 0, hi = B;                              // largest r with off_a(r) <= e
-        while (hi - lo > 1) {
-            const int mid = lo + ((hi - lo) >> 1);
-            if (off_a(mid) <= e) lo = mid; else hi = mid;
-        }
-        if (tid == 0) sh_rlo = lo; else sh_rhi = lo;
-    }
-    __syncthreads();
-    const int r_lo = sh_rlo;
-    const int r_hi = sh_rhi;
-
-    // 4. Suffix rows (row[j] = t[L-1-j]) of the first kSufCap requests, and this
-    //    CTA's slots cleared.
-    {
-        const int nrows = (r_hi - r_lo + 1 < kSufCap) ? r_hi - r_lo + 1 : kSufCap;
-        for (int idx = tid; idx < nrows * max_m; idx += kThreads) {
-            const int row = idx / max_m, j = idx - row * max_m;
-            const int r = r_lo + row;
-            const int64_t src = off_a(r + 1) - 1 - j;
-            suf_s[idx] = (src >= off_a(r)) ? ta[src] : 0;
-        }
-        for (int r = r_lo + tid; r <= r_hi; r += kThreads) prm.slots[int64_t(r) + c] = 0ull;
-    }
-    __syncthreads();
-
-    // Suffix token j of request r (t[L-1-j]); 0 past the start of the history.
-    auto suffix = [&](int r, int64_t o_r, int64_t nxt, int j) -> int32_t {
-        const int row = r - r_lo;
-        if (row < kSufCap) return suf_s[row * max_m + j];
-        return (nxt - 1 - j >= o_r) ? ta[nxt - 1 - j] : 0;
-    };
-
-    // 5. Stream this warp's tiles.  Positions from here on are int32 and relative
-    //    to A0 = 4 * qa, the chunk's first element.  The warp's current request
-    //    (uniform across it) and each lane's best key for it carry over from tile
-    //    to tile; the best keys are folded into the request's slot when the warp
-    //    moves on.
-    const int64_t A0 = 4 * qa;
-    const int begin_x = int(a_begin - A0);               // > 0 only in chunk 0
-    const int end_x = int(((a_end < 4 * qb) ? a_end : 4 * qb) - A0);
-    auto rel = [&](int r) -> int { return int(off_a(r) - A0); };
     bool failed = false;
-    int seg_r = r_lo;                                   // first request not yet finished
-    int cur_r = -1;                                     // request of the cached state below
-    int cur_o = 0, cur_nxt = 0;                         // its start and end, relative
-    int32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0;
-    unsigned long long best = 0ull;
-    auto flush = [&]() {                                // warp-uniform
-        if (__any_sync(0xffffffffu, best != 0ull)) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const unsigned long long v = __shfl_xor_sync(0xffffffffu, best, o);
-                best = v > best ? v : best;
-            }
-            if (lane == 0) red_max_u64(prm.slots + (int64_t(cur_r) + c), best);
-            best = 0ull;
-        }
-    };
-    auto set_request = [&](int r) {                     // warp-uniform, r in [r_lo, r_hi]
-        if (r == cur_r) return;
-        flush();
-        cur_r = r;
-        const int64_t o = off_a(r), n = off_a(r + 1);
-        cur_o = int(o - A0);
-        cur_nxt = int(n - A0);
-        s0 = suffix(r, o, n, 0);
-        if (D >= 2) s1 = suffix(r, o, n, 1);
-        if (D >= 3) s2 = suffix(r, o, n, 2);
-        if (D >= 4) s3 = suffix(r, o, n, 3);
-    };
-    int k = 0;
-    for (; k < my_tiles; ++k) {
-        const int slot = k % kBufs;
-        const uint32_t bar = smem_addr(&my_bars[slot]);
-        const uint32_t parity = uint32_t(k / kBufs) & 1u;
-        if (!mbar_try_wait(bar, parity) && !mbar_wait_until(bar, parity, deadline)) {
-            failed = true;
-            break;
-        }
-        const int t0 = (warp + kWarps * k) * tq;         // tile's first quad, relative
-        const int nq = (t0 + tq < int(chunk_q)) ? tq : int(chunk_q) - t0;
-        const unsigned char *buf = my_bufs + size_t(slot) * kBufBytes + kHaloQuads * 16;
-        const int4 *sq = reinterpret_cast<const int4 *>(buf);
-        const int32_t *st = reinterpret_cast<const int32_t *>(buf);
-        const int base = 4 * t0;                         // relative position of st[0]
-        const int eb = base > begin_x ? base : begin_x;
-        const int ee = (base + 4 * nq < end_x) ? base + 4 * nq : end_x;
+    const Partition P = make_partition(a_begin, a_end, G);
+    int64_t wq0 = 0, wq1 = 0;
+    if (a_end > a_begin) vchunk_range(P, int64_t(c) * kWarps + warp, wq0, wq1);
 
-        // Candidate ends [lo, hi] (tile elements) of the current request: the
-        // D-token test on every whole quad, the rest element by element.
-        auto scan_range = [&](int lo, int hi) {
-            const int qoff = base - cur_o;               // local position of st[0] in the request
-            // Candidate end at tile element e whose last k0 tokens already match:
-            // extend backwards, fold its key into `best`.
-            auto extend = [&](int e, int k0) {
-                const int q = qoff + e;                  // local end position in the request
-                const int kmax = max_m < q + 1 ? max_m : q + 1;
-                int kk = k0;
-                while (kk < kmax && st[e - kk] == suffix(cur_r, A0 + cur_o, A0 + cur_nxt, kk)) ++kk;
-                if (kk >= min_m) {
-                    const unsigned long long key =
-                        (static_cast<unsigned long long>(kk) << 32) | static_cast<uint32_t>(q - kk + 1);
-                    best = key > best ? key : best;
-                }
-            };
-            auto extend_quad = [&](const int4 &p, const int4 &cq, int j) {   // rare path
-                unsigned h = quad_hits<D>(p, cq, s0, s1, s2, s3);
-                while (h) {
-                    const int e = __ffs(h) - 1;
-                    h &= h - 1;
-                    extend(4 * j + e, D);
-                }
-            };
-            const int jq0 = (lo + 3) >> 2;               // first quad fully inside
-            const int jq1 = ((hi + 1) >> 2) - 1;         // last quad fully inside
-            // two quads per lane per iteration: independent loads and tests; the
-            // previous quad (the halo when j == 0) supplies the tokens before each
-            int j = jq0 + lane;
-            for (; j + 32 <= jq1; j += 64) {
-                const int4 c0 = sq[j], c1 = sq[j + 32];
-                int4 p0 = make_int4(0, 0, 0, 0), p1 = make_int4(0, 0, 0, 0);
-                if (D >= 2) {
-                    p0 = sq[j - 1];
-                    p1 = sq[j + 31];
-                }
-                if (quad_any<D>(p0, c0, s0, s1, s2, s3) | quad_any<D>(p1, c1, s0, s1, s2, s3)) {
-                    extend_quad(p0, c0, j);
-                    extend_quad(p1, c1, j + 32);
-                }
+    if (wq0 < wq1) {                                     // warp-uniform: this warp has a range
+        // 2. The warp's range: elements [WA + wbeg, WA + wend) of the aligned view;
+        //    positions below are int32 relative to WA.
+        const int64_t v = int64_t(c) * kWarps + warp;    // virtual chunk: slot column
+        unsigned long long *slots = prm.slots + v;       // slot of request r: slots[r]
+        const int64_t WA = 4 * (P.q_lo + wq0);
+        const int wn = int(wq1 - wq0);
+        const int wbeg = int(((WA > a_begin) ? WA : a_begin) - WA);
+        const int wend = int(((4 * (P.q_lo + wq1) < a_end) ? 4 * (P.q_lo + wq1) : a_end) - WA);
+        const int rw_lo = owner(WA + wbeg, 0, B - 1);
+        const int rw_hi = owner(WA + wend - 1, rw_lo, B - 1);
+        const int nrows = (rw_hi - rw_lo + 1 < kSufRows) ? rw_hi - rw_lo + 1 : kSufRows;
+
+        // 3. Suffix tokens (row[j] = t[L-1-j]) of the warp's first kSufRows requests:
+        //    loads issued first, so they are not queued behind the bulk reads.
+        int32_t sreg[kSufRegs];
+#pragma unroll
+        for (int t = 0; t < kSufRegs; ++t) {
+            const int idx = lane + 32 * t;
+            const int row = idx / max_m, j = idx - row * max_m;
+            sreg[t] = 0;
+            if (row < nrows) {
+                const int64_t n = off_a(rw_lo + row + 1);
+                if (n - 1 - j >= off_a(rw_lo + row)) sreg[t] = __ldg(ta + n - 1 - j);
             }
-            if (j <= jq1) {
-                const int4 c0 = sq[j];
-                int4 p0 = make_int4(0, 0, 0, 0);
-                if (D >= 2) p0 = sq[j - 1];
-                if (quad_any<D>(p0, c0, s0, s1, s2, s3)) extend_quad(p0, c0, j);
-            }
-            // elements of [lo, hi] outside whole quads: fewer than 8
-            if (4 * jq0 != lo || 4 * (jq1 + 1) != hi + 1) {
-                const int head_end = 4 * jq0 < hi + 1 ? 4 * jq0 : hi + 1;   // [lo, head_end)
-                const int tail_beg = 4 * (jq1 + 1) > lo ? 4 * (jq1 + 1) : lo;   // [tail_beg, hi]
-                int e = -1;
-                if (lane < 4) e = lo + lane < head_end ? lo + lane : -1;
-                else if (lane < 8) e = tail_beg + (lane - 4) <= hi && tail_beg + (lane - 4) >= head_end
-                                           ? tail_beg + (lane - 4) : -1;
-                if (e >= 0 && st[e] == s0) extend(e, 1);
-            }
+        }
+
+        // 4. Tiles: tile k is quads [k*tq, min((k+1)*tq, wn)) of the range; the
+        //    ring holds kBufs of them, tile k in buffer k % kBufs.
+        const int halo = (max_m - 1 + 3) >> 2;
+        int tq = (wn + 1) / 2;
+        tq = tq < kTileQuadsMin ? kTileQuadsMin : (tq > kTileQuadsMax ? kTileQuadsMax : tq);
+        const int ntiles = (wn + tq - 1) / tq;
+        unsigned char *my_bufs = smem + lay.bufs + size_t(warp) * kBufs * kBufBytes;
+        unsigned long long *my_bars = bars + warp * kBufs;
+        auto issue_tile = [&](int k, int slot) {           // lane 0 only
+            const int64_t t0 = P.q_lo + wq0 + int64_t(k) * tq;
+            const int64_t t1 = (t0 + tq < P.q_lo + wq1) ? t0 + tq : P.q_lo + wq1;
+            const int64_t ls = (t0 - halo > P.q_lo) ? t0 - halo : P.q_lo;
+            const uint32_t bytes = uint32_t(t1 - ls) * 16u;
+            unsigned char *buf = my_bufs + size_t(slot) * kBufBytes;
+            const uint32_t bar = smem_addr(&my_bars[slot]);
+            mbar_expect_tx(bar, bytes);
+            bulk_copy_g2s(smem_addr(buf + size_t(kHaloQuads - (t0 - ls)) * 16), ta + ls * 4, bytes, bar);
+        };
+        if (lane == 0) {
+            const int first = ntiles < kBufs ? ntiles : kBufs;
+            for (int k = 0; k < first; ++k) issue_tile(k, k);
+        }
+#pragma unroll
+        for (int t = 0; t < kSufRegs; ++t) {
+            const int idx = lane + 32 * t;
+            if (idx < nrows * max_m) suf_w[idx] = sreg[t];
+        }
+        // this warp's slots: cleared before the warp writes its results into them
+        for (int r = rw_lo + lane; r <= rw_hi; r += 32)
+            if (off_a(r + 1) > off_a(r)) slots[r] = 0ull;
+        __syncwarp();
+
+        // Suffix token j of request r (t[L-1-j]); 0 past the start of the history.
+        auto suffix = [&](int r, int64_t o, int64_t n, int j) -> int32_t {
+            const int row = r - rw_lo;
+            if (row < kSufRows) return suf_w[row * max_m + j];
+            return (n - 1 - j >= o) ? __ldg(ta + n - 1 - j) : 0;
         };
 
-        if (cur_r >= 0 && eb == base && ee == base + 4 * nq && cur_o + (min_m - 1) <= eb && ee + 1 <= cur_nxt) {
-            scan_range(0, 4 * nq - 1);                   // the whole tile is candidates of cur_r
-        } else {
-            // Requests overlapping this tile, in order (uniform across the warp).
-            while (seg_r < r_hi && rel(seg_r + 1) <= eb) ++seg_r;
-            for (int r = seg_r; r <= r_hi; ++r) {
-                const int o_r = rel(r);
-                if (o_r >= ee) break;
-                const int nxt = rel(r + 1);
-                const int lo = (o_r + (min_m - 1) > eb) ? o_r + (min_m - 1) : eb;   // candidate end range
-                const int hi = (nxt - 2 < ee - 1) ? nxt - 2 : ee - 1;               // within this tile
-                if (lo > hi) continue;
-                set_request(r);
-                scan_range(lo - base, hi - base);
+        // 5. Stream the tiles.  The warp's current request (uniform across it) and
+        //    each lane's best key for it carry over from tile to tile; the warp's
+        //    maximum goes into the request's slot when the warp moves on.
+        int seg_r = rw_lo;                               // first request not yet finished
+        int cur_r = -1;                                  // request of the cached state below
+        int cur_o = 0, cur_nxt = 0;                      // its start and end, relative to WA
+        int32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0;
+        unsigned long long best = 0ull;
+        auto flush = [&]() {                             // warp-uniform
+            if (__any_sync(0xffffffffu, best != 0ull)) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const unsigned long long x = __shfl_xor_sync(0xffffffffu, best, o);
+                    best = x > best ? x : best;
+                }
+                if (lane == 0) slots[cur_r] = best;
+                best = 0ull;
+            }
+        };
+        auto set_request = [&](int r) {                  // warp-uniform, r in [rw_lo, rw_hi]
+            if (r == cur_r) return;
+            flush();
+            cur_r = r;
+            const int64_t o = off_a(r), n = off_a(r + 1);
+            cur_o = int(o - WA);
+            cur_nxt = int(n - WA);
+            s0 = suffix(r, o, n, 0);
+            if (D >= 2) s1 = suffix(r, o, n, 1);
+            if (D >= 3) s2 = suffix(r, o, n, 2);
+            if (D >= 4) s3 = suffix(r, o, n, 3);
+        };
+        int k = 0;
+        for (; k < ntiles; ++k) {
+            const int slot = k % kBufs;
+            const uint32_t bar = smem_addr(&my_bars[slot]);
+            const uint32_t parity = uint32_t(k / kBufs) & 1u;
+            if (!mbar_try_wait(bar, parity) && !mbar_wait_until(bar, parity, deadline)) {
+                failed = true;
+                break;
+            }
+            const int t0 = k * tq;                       // tile's first quad, relative
+            const int nq = (t0 + tq < wn) ? tq : wn - t0;
+            const unsigned char *buf = my_bufs + size_t(slot) * kBufBytes + kHaloQuads * 16;
+            const int4 *sq = reinterpret_cast<const int4 *>(buf);
+            const int32_t *st = reinterpret_cast<const int32_t *>(buf);
+            const int base = 4 * t0;                     // relative position of st[0]
+            const int eb = base > wbeg ? base : wbeg;
+            const int ee = (base + 4 * nq < wend) ? base + 4 * nq : wend;
+
+            // Candidate ends [lo, hi] (tile elements) of the current request: the
+            // D-token test on every whole quad, the rest element by element.
+            auto scan_range = [&](int lo, int hi) {
+                const int qoff = base - cur_o;           // local position of st[0] in the request
+                // Candidate end at tile element e whose last k0 tokens already
+                // match: extend backwards, fold its key into `best`.
+                auto extend = [&](int e, int k0) {
+                    const int q = qoff + e;              // local end position in the request
+                    const int kmax = max_m < q + 1 ? max_m : q + 1;
+                    int kk = k0;
+                    while (kk < kmax && st[e - kk] == suffix(cur_r, WA + cur_o, WA + cur_nxt, kk)) ++kk;
+                    if (kk >= min_m) {
+                        const unsigned long long key =
+                            (static_cast<unsigned long long>(kk) << 32) | static_cast<uint32_t>(q - kk + 1);
+                        best = key > best ? key : best;
+                    }
+                };
+                auto extend_quad = [&](const int4 &p, const int4 &cq, int j) {   // rare path
+                    unsigned h = quad_hits<D>(p, cq, s0, s1, s2, s3);
+                    while (h) {
+                        const int e = __ffs(h) - 1;
+                        h &= h - 1;
+                        extend(4 * j + e, D);
+                    }
+                };
+                const int jq0 = (lo + 3) >> 2;           // first quad fully inside
+                const int jq1 = ((hi + 1) >> 2) - 1;     // last quad fully inside
+                // two quads per lane per iteration: independent loads and tests; the
+                // previous quad (the halo when j == 0) supplies the tokens before each
+                int j = jq0 + lane;
+                for (; j + 32 <= jq1; j += 64) {
+                    const int4 c0 = sq[j], c1 = sq[j + 32];
+                    int4 p0 = make_int4(0, 0, 0, 0), p1 = make_int4(0, 0, 0, 0);
+                    if (D >= 2) {
+                        p0 = sq[j - 1];
+                        p1 = sq[j + 31];
+                    }
+                    if (quad_any<D>(p0, c0, s0, s1, s2, s3) | quad_any<D>(p1, c1, s0, s1, s2, s3)) {
+                        extend_quad(p0, c0, j);
+                        extend_quad(p1, c1, j + 32);
+                    }
+                }
+                if (j <= jq1) {
+                    const int4 c0 = sq[j];
+                    int4 p0 = make_int4(0, 0, 0, 0);
+                    if (D >= 2) p0 = sq[j - 1];
+                    if (quad_any<D>(p0, c0, s0, s1, s2, s3)) extend_quad(p0, c0, j);
+                }
+                // elements of [lo, hi] outside whole quads: fewer than 8
+                if (4 * jq0 != lo || 4 * (jq1 + 1) != hi + 1) {
+                    const int head_end = 4 * jq0 < hi + 1 ? 4 * jq0 : hi + 1;       // [lo, head_end)
+                    const int tail_beg = 4 * (jq1 + 1) > lo ? 4 * (jq1 + 1) : lo;   // [tail_beg, hi]
+                    int e = -1;
+                    if (lane < 4) e = lo + lane < head_end ? lo + lane : -1;
+                    else if (lane < 8) e = tail_beg + (lane - 4) <= hi && tail_beg + (lane - 4) >= head_end
+                                               ? tail_beg + (lane - 4) : -1;
+                    if (e >= 0 && st[e] == s0) extend(e, 1);
+                }
+            };
+
+            if (cur_r >= 0 && eb == base && ee == base + 4 * nq && cur_o + (min_m - 1) <= eb &&
+                ee + 1 <= cur_nxt) {
+                scan_range(0, 4 * nq - 1);               // the whole tile is candidates of cur_r
+            } else {
+                // Requests overlapping this tile, in order (uniform across the warp).
+                while (seg_r < rw_hi && off_a(seg_r + 1) - WA <= eb) ++seg_r;
+                for (int r = seg_r; r <= rw_hi; ++r) {
+                    const int o_r = int(off_a(r) - WA);
+                    if (o_r >= ee) break;
+                    const int nxt = int(off_a(r + 1) - WA);
+                    const int lo = (o_r + (min_m - 1) > eb) ? o_r + (min_m - 1) : eb;   // candidate end range
+                    const int hi = (nxt - 2 < ee - 1) ? nxt - 2 : ee - 1;               // within this tile
+                    if (lo > hi) continue;
+                    set_request(r);
+                    scan_range(lo - base, hi - base);
+                }
+            }
+            // Refill this buffer with the warp's tile k + kBufs.
+            __syncwarp();
+            if (lane == 0 && k + kBufs < ntiles) {
+                fence_proxy_async_smem();
+                issue_tile(k + kBufs, slot);
             }
         }
-        // Refill this slot with the warp's tile k + kBufs.
-        __syncwarp();
-        if (lane == 0 && k + kBufs < my_tiles) {
-            fence_proxy_async_smem();
-            issue_tile(warp + kWarps * (k + kBufs), slot);
+        if (!failed) {
+            flush();                                     // the last request's result
+        } else {
+            // 6. A wait ran out: let this warp's copies land (bounded), then mark
+            //    its requests as failed.  Copies k .. min(k + kBufs, ntiles) - 1 may
+            //    still be in flight.
+            if (lane == 0) {
+                const uint64_t drain_deadline = global_ns() + kDefaultWaitNs;
+                const int stop = (k + kBufs < ntiles) ? k + kBufs : ntiles;
+                for (int kk = k; kk < stop; ++kk)
+                    (void)mbar_wait_until(smem_addr(&my_bars[kk % kBufs]), uint32_t(kk / kBufs) & 1u,
+                                          drain_deadline);
+            }
+            __syncwarp();
+            for (int r = rw_lo + lane; r <= rw_hi; r += 32)
+                if (off_a(r + 1) > off_a(r)) slots[r] = kKeyFailed;
         }
     }
-    if (!failed) flush();                               // fold the last request's keys
-
-    failed = __syncthreads_or(failed);
-    drain_offsets();
-    if (!failed) return;
-    // 6. A wait ran out: let this warp's copies land (bounded), then mark every
-    //    request the CTA owns as failed.  Copies k .. min(k + kBufs, my_tiles) - 1
-    //    may still be in flight for a warp that stopped at tile k.
-    if (lane == 0) {
-        const uint64_t drain_deadline = global_ns() + kDefaultWaitNs;
-        const int stop = (k + kBufs < my_tiles) ? k + kBufs : my_tiles;
-        for (int kk = k; kk < stop; ++kk)
-            (void)mbar_wait_until(smem_addr(&my_bars[kk % kBufs]), uint32_t(kk / kBufs) & 1u, drain_deadline);
-    }
-    __syncthreads();
-    for (int rr = r_lo + tid; rr <= r_hi; rr += kThreads) red_max_u64(prm.slots + (int64_t(rr) + c), kKeyFailed);
+    if (offs_pending && tid == 0) (void)mbar_wait_until(smem_addr(offs_bar), 0, global_ns() + kDefaultWaitNs);
 }
 
 // ------------------------------------------------------------ fill kernel ----
@@ -594,16 +593,19 @@ __global__ void __launch_bounds__(kFillWarps * 32) fill_kernel(FillParams prm) {
     unsigned long long key = 0ull;
     if (L > 0) {
         const Partition P = make_partition(first + shift, end + shift, prm.grid);
-        const int64_t c0 = chunk_of_quad(P, (o0 + shift) >> 2);
-        const int64_t c1 = chunk_of_quad(P, (o1 - 1 + shift) >> 2);
-        for (int64_t cc = c0 + lane; cc <= c1; cc += 32) {
-            const unsigned long long v = prm.slots[int64_t(r) + cc];
-            key = v > key ? v : key;
+        const int64_t v0 = vchunk_of_quad(P, ((o0 + shift) >> 2) - P.q_lo);
+        const int64_t v1 = vchunk_of_quad(P, ((o1 - 1 + shift) >> 2) - P.q_lo);
+        for (int64_t v = v0 + lane; v <= v1; v += 32) {
+            int64_t lo, hi;
+            vchunk_range(P, v, lo, hi);
+            if (lo >= hi) continue;                      // an empty warp range owns no slot
+            const unsigned long long x = prm.slots[int64_t(r) + v];
+            key = x > key ? x : key;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            const unsigned long long v = __shfl_xor_sync(0xffffffffu, key, o);
-            key = v > key ? v : key;
+            const unsigned long long x = __shfl_xor_sync(0xffffffffu, key, o);
+            key = x > key ? x : key;
         }
     }
     // A key that does not describe an admissible match (1 <= m, p + m <= L - 1) can
@@ -682,10 +684,14 @@ int device_state(DeviceState **out) {
     return LOOKUP_DRAFT_OK;
 }
 
-// One scan CTA per SM (its shared-memory ring admits no second one).
+// One scan CTA per SM (its shared-memory rings admit no second one).
 int grid_for(const DeviceState &st) { return st.sms; }
 
-size_t workspace_bytes_for(int32_t B, int grid) { return (size_t(B) + size_t(grid)) * sizeof(unsigned long long); }
+// One 64-bit slot per (request, virtual chunk) pair on the staircase: at most
+// B + (number of virtual chunks) of them.
+size_t workspace_bytes_for(int32_t B, int grid) {
+    return (size_t(B) + size_t(grid) * kWarps) * sizeof(unsigned long long);
+}
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
