@@ -68,7 +68,6 @@ constexpr int kTileQuadsMax = 192;     // 3 KB of history per tile at most
 constexpr int kTileQuadsMin = 32;
 constexpr int kHaloQuads = 8;          // room for (LOOKUP_DRAFT_MAX_M - 1) tokens of context
 constexpr int kSufRows = 8;            // requests per warp whose suffix is kept in smem
-constexpr int kSufRegs = kSufRows * LOOKUP_DRAFT_MAX_M / 32;   // suffix loads per lane
 constexpr int kOffCap = 4097;          // offsets kept in smem when B + 1 <= kOffCap
 constexpr int kFillWarps = 4;          // requests per fill CTA
 
@@ -280,10 +279,12 @@ __device__ __forceinline__ bool quad_any(const int4 &prv, const int4 &cur, int32
 }
 
 // D = min(min_m, 4): how many suffix tokens the branch-free rejection test checks
-// before a candidate is extended one token at a time.
-template <int D>
+// before a candidate is extended one token at a time.  OFFS_SMEM: B + 1 <= kOffCap,
+// the offsets are copied into shared memory (otherwise read from global memory).
+template <int D, bool OFFS_SMEM>
 __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
     extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ unsigned long long sh_deadline;
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -293,8 +294,6 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
     const int min_m = prm.min_m;
     const int max_m = prm.max_m;
 
-    // Every copy must land within wait_ns of this CTA's start.
-    const uint64_t deadline = global_ns() + prm.wait_ns;
     const ScanSmemLayout lay = scan_smem_layout(B, max_m);
     unsigned long long *bars = reinterpret_cast<unsigned long long *>(smem + lay.bars);
     unsigned long long *offs_bar = bars + kWarps * kBufs;
@@ -302,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
 
     const int shift = tokens_shift(prm.tokens);
     const int32_t *ta = reinterpret_cast<const int32_t *>(reinterpret_cast<uintptr_t>(prm.tokens) & ~uintptr_t(15));
-    const bool offs_in_smem = int64_t(B) + 1 <= kOffCap;
+    constexpr bool offs_in_smem = OFFS_SMEM;
     const uintptr_t off_src = reinterpret_cast<uintptr_t>(prm.offsets) & ~uintptr_t(15);
     const int64_t *offs_s =
         reinterpret_cast<const int64_t *>(smem + lay.offs + (reinterpret_cast<uintptr_t>(prm.offsets) & 15u));
@@ -311,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
     //    the stream finishes; then wait for it (it may have written the inputs).
     if (offs_in_smem && tid * 16 <= B) prefetch_l2(prm.offsets + tid * 16);
     if (tid == 0) {
+        sh_deadline = global_ns() + prm.wait_ns;         // every copy must land by then
         for (int i = 0; i <= kWarps * kBufs; ++i) mbar_init(smem_addr(&bars[i]), 1);
         fence_barrier_init();
     }
@@ -328,18 +328,25 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                       smem_addr(offs_bar));
     }
     __syncthreads();                                     // barrier init visible before waiting
-    if (offs_in_smem) ok = mbar_wait_until(smem_addr(offs_bar), 0, deadline);
+    const uint64_t deadline = sh_deadline;
+    if (offs_in_smem) ok = mbar_try_wait(smem_addr(offs_bar), 0) || mbar_wait_until(smem_addr(offs_bar), 0, deadline);
     const bool offs_smem = offs_in_smem && !__syncthreads_or(!ok);
     const bool offs_pending = offs_in_smem && !offs_smem;
     auto off_a = [&](int i) -> int64_t {
-        return (offs_smem ? offs_s[i] : __ldg(prm.offsets + i)) + shift;
+        if (OFFS_SMEM && offs_smem) return offs_s[i] + shift;
+        return __ldg(prm.offsets + i) + shift;
     };
-    // largest r in [lo, hi] with off_a(r) <= e (off_a(lo) <= e assumed)
+    // Largest r in [lo, hi] with off_a(r) <= e, given off_a(lo) <= e: a 32-way
+    // search, each lane testing one probe per round (warp-uniform result).
     auto owner = [&](int64_t e, int lo, int hi) -> int {
-        ++hi;
-        while (hi - lo > 1) {
-            const int mid = lo + ((hi - lo) >> 1);
-            if (off_a(mid) <= e) lo = mid; else hi = mid;
+        while (hi > lo) {
+            const int step = (hi - lo + 31) >> 5;
+            const int probe = (lo + (lane + 1) * step < hi) ? lo + (lane + 1) * step : hi;
+            const int cnt = __popc(__ballot_sync(0xffffffffu, off_a(probe) <= e));   // a prefix of lanes
+            const int nlo = cnt == 0 ? lo : ((lo + cnt * step < hi) ? lo + cnt * step : hi);
+            const int nhi = cnt == 32 ? hi : ((lo + (cnt + 1) * step < hi) ? lo + (cnt + 1) * step : hi) - 1;
+            lo = nlo;
+            hi = nhi;
         }
         return lo;
     };
@@ -362,21 +369,19 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
         const int wbeg = int(((WA > a_begin) ? WA : a_begin) - WA);
         const int wend = int(((4 * (P.q_lo + wq1) < a_end) ? 4 * (P.q_lo + wq1) : a_end) - WA);
         const int rw_lo = owner(WA + wbeg, 0, B - 1);
-        const int rw_hi = owner(WA + wend - 1, rw_lo, B - 1);
-        const int nrows = (rw_hi - rw_lo + 1 < kSufRows) ? rw_hi - rw_lo + 1 : kSufRows;
 
-        // 3. Suffix tokens (row[j] = t[L-1-j]) of the warp's first kSufRows requests:
-        //    loads issued first, so they are not queued behind the bulk reads.
-        int32_t sreg[kSufRegs];
+        // 3. Suffix tokens (row[j] = t[L-1-j], lane j) of requests rw_lo, rw_lo + 1,
+        //    ...: loads issued before the bulk reads, so they are not queued behind
+        //    them.
+        int64_t bound[kSufRows + 1];
 #pragma unroll
-        for (int t = 0; t < kSufRegs; ++t) {
-            const int idx = lane + 32 * t;
-            const int row = idx / max_m, j = idx - row * max_m;
-            sreg[t] = 0;
-            if (row < nrows) {
-                const int64_t n = off_a(rw_lo + row + 1);
-                if (n - 1 - j >= off_a(rw_lo + row)) sreg[t] = __ldg(ta + n - 1 - j);
-            }
+        for (int row = 0; row <= kSufRows; ++row) bound[row] = off_a(rw_lo + row <= B ? rw_lo + row : B);
+        int32_t sreg[kSufRows];
+#pragma unroll
+        for (int row = 0; row < kSufRows; ++row) {
+            const int64_t src = bound[row + 1] - 1 - lane;
+            const bool ld = rw_lo + row < B && lane < max_m && src >= bound[row];
+            sreg[row] = ld ? __ldg(ta + src) : 0;
         }
 
         // 4. Tiles: tile k is quads [k*tq, min((k+1)*tq, wn)) of the range; the
@@ -401,11 +406,11 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
             const int first = ntiles < kBufs ? ntiles : kBufs;
             for (int k = 0; k < first; ++k) issue_tile(k, k);
         }
+        const int rw_hi = owner(WA + wend - 1, rw_lo, B - 1);
+        const int nrows = (rw_hi - rw_lo + 1 < kSufRows) ? rw_hi - rw_lo + 1 : kSufRows;
 #pragma unroll
-        for (int t = 0; t < kSufRegs; ++t) {
-            const int idx = lane + 32 * t;
-            if (idx < nrows * max_m) suf_w[idx] = sreg[t];
-        }
+        for (int row = 0; row < kSufRows; ++row)
+            if (row < nrows && lane < max_m) suf_w[row * max_m + lane] = sreg[row];
         // this warp's slots: cleared before the warp writes its results into them
         for (int r = rw_lo + lane; r <= rw_hi; r += 32)
             if (off_a(r + 1) > off_a(r)) slots[r] = 0ull;
@@ -449,6 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
             if (D >= 3) s2 = suffix(r, o, n, 2);
             if (D >= 4) s3 = suffix(r, o, n, 3);
         };
+        set_request(rw_lo);
         int k = 0;
         for (; k < ntiles; ++k) {
             const int slot = k % kBufs;
@@ -662,10 +668,15 @@ int device_state(DeviceState **out) {
         int sms = 0;
         LD_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
         const ScanSmemLayout worst = scan_smem_layout(kOffCap - 1, LOOKUP_DRAFT_MAX_M);
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(worst.total)));
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(worst.total)));
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(worst.total)));
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(worst.total)));
+        const int smem_max = int(worst.total);
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<3, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<3, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
         cudaMemPoolProps props;
         std::memset(&props, 0, sizeof props);
         props.allocType = cudaMemAllocationTypePinned;
@@ -737,11 +748,16 @@ int launch_scan(const DeviceState &st, const int32_t *tokens, const int64_t *off
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    switch (min_m < 4 ? min_m : 4) {
-    case 1: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<1>, prm)); break;
-    case 2: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<2>, prm)); break;
-    case 3: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<3>, prm)); break;
-    default: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<4>, prm)); break;
+    const bool offs_smem = int64_t(B) + 1 <= kOffCap;
+    switch ((min_m < 4 ? min_m : 4) * 2 + (offs_smem ? 1 : 0)) {
+    case 2: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<1, false>, prm)); break;
+    case 3: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<1, true>, prm)); break;
+    case 4: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<2, false>, prm)); break;
+    case 5: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<2, true>, prm)); break;
+    case 6: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<3, false>, prm)); break;
+    case 7: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<3, true>, prm)); break;
+    case 8: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<4, false>, prm)); break;
+    default: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<4, true>, prm)); break;
     }
     return LOOKUP_DRAFT_OK;
 }
