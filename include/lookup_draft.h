@@ -54,6 +54,7 @@ struct CUstream_st;                     /* same type as cudaStream_t */
 #define LOOKUP_DRAFT_OK 0
 #define LOOKUP_DRAFT_EINVAL (-1)        /* arguments do not describe a valid step */
 #define LOOKUP_DRAFT_ECUDA (-2)         /* a CUDA call failed; see lookup_draft_last_cuda_error */
+#define LOOKUP_DRAFT_ERANGE (-3)        /* batch too large for lookup_draft_noalloc's fixed scratch */
 
 #define LOOKUP_DRAFT_LEN_FAILED (-1)    /* out_len value: the scan for this request did not
                                            complete (a bounded wait on the device ran out) */
@@ -140,6 +141,37 @@ int lookup_draft_host(const int32_t *h_tokens, const int64_t *h_offsets, int32_t
                       int32_t min_m, int32_t max_m, int32_t K,
                       int32_t *h_out_draft, int32_t *h_out_len, int32_t *h_out_pos,
                       struct CUstream_st *stream);
+
+/*
+ * lookup_draft without any allocation.  (The source article has no counterpart to
+ * this entry point; it is a property of this library.)
+ *
+ * Some callers must not allocate device memory during a step: a serving loop whose
+ * GPU memory is entirely handed out by another framework's allocator, a process
+ * that runs under a fixed device-memory budget, or code that must not make the
+ * driver calls an allocation implies while it is on a latency-critical path.  This
+ * call computes exactly what lookup_draft computes, with the same arguments and
+ * outputs, but it keeps the scan's scratch (one 64-bit slot per (request, warp
+ * range) pair) in a fixed array of 65,536 slots (512 KiB) in device memory that is
+ * part of the library: every GPU that loads the library holds that array until the
+ * process exits.  It calls no cudaMalloc, cudaFree, memory-pool or other allocating
+ * routine.
+ *
+ * Limit: B + 16 * (number of SMs) <= 65,536 (B <= 63,104 on a 152-SM GB300);
+ * larger batches return LOOKUP_DRAFT_ERANGE and enqueue nothing.
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address and sets kernel attributes; make that first call before
+ * any stream capture on that device.
+ * Sharing: every call on a device uses the same array and leaves its contents
+ * behind.  Nothing in it needs clearing between calls (each scan writes every slot
+ * it later reads), but calls whose GPU work overlaps in time race on the array and
+ * give undefined results: issue them on one stream, or order them with events.
+ * Errors as for lookup_draft, plus LOOKUP_DRAFT_ERANGE.
+ */
+int lookup_draft_noalloc(const int32_t *tokens, const int64_t *offsets, int32_t B,
+                         int32_t min_m, int32_t max_m, int32_t K,
+                         int32_t *out_draft, int32_t *out_len, int32_t *out_pos,
+                         struct CUstream_st *stream);
 
 /* Static description of a return code (never NULL). */
 const char *lookup_draft_strerror(int code);

@@ -24,7 +24,8 @@ from . import build as _build
 
 __all__ = [
     "LookupDraftError", "load_library", "lookup_draft", "lookup_draft_ex", "lookup_draft_host",
-    "lookup_draft_scan", "lookup_draft_fill", "workspace_bytes", "set_wait_limit_ns",
+    "lookup_draft_scan", "lookup_draft_fill", "lookup_draft_noalloc", "workspace_bytes",
+    "set_wait_limit_ns",
     "MAX_M", "MAX_K", "LEN_FAILED",
 ]
 
@@ -82,6 +83,8 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.lookup_draft_fill.restype = ctypes.c_int
     lib.lookup_draft_host.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
     lib.lookup_draft_host.restype = ctypes.c_int
+    lib.lookup_draft_noalloc.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
+    lib.lookup_draft_noalloc.restype = ctypes.c_int
     lib.lookup_draft_strerror.argtypes = [ctypes.c_int]
     lib.lookup_draft_strerror.restype = ctypes.c_char_p
     lib.lookup_draft_last_cuda_error.argtypes = []
@@ -162,6 +165,28 @@ def lookup_draft_ex(tokens, offsets, min_m: int = 4, max_m: int = 12, K: int = 1
                                  _stream_handle(stream))
     _check(rc, lib)
     return draft, length, pos, mlen
+
+
+def lookup_draft_noalloc(tokens, offsets, min_m: int = 4, max_m: int = 12, K: int = 15,
+                         out=None, stream=None):
+    """lookup_draft for callers that must not allocate device memory during a step.
+
+    Same results as lookup_draft; the scan's scratch lives in a fixed array inside
+    the library (B + 16 * SMs <= 65,536), so the call allocates nothing.  Pass
+    preallocated ``out`` tensors to keep the whole call allocation-free on the
+    Python side too.  Calls whose GPU work overlaps in time share that array and
+    race: keep them on one stream.
+    """
+    import torch
+    lib = load_library()
+    B = _as_batch(tokens, offsets)
+    draft, length, pos, _ = _outputs(B, K, tokens.device, out, False)
+    with torch.cuda.device(tokens.device):
+        rc = lib.lookup_draft_noalloc(tokens.data_ptr(), offsets.data_ptr(), B, min_m, max_m, K,
+                                      draft.data_ptr(), length.data_ptr(), pos.data_ptr(),
+                                      _stream_handle(stream))
+    _check(rc, lib)
+    return draft, length, pos
 
 
 def workspace_bytes(B: int, device=None) -> int:

@@ -807,6 +807,60 @@ int run_step(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t m
     return rc;
 }
 
+// ------------------------------------------------- no-allocation entry point ----
+// lookup_draft_noalloc keeps the scan's result slots in one fixed array in device
+// memory instead of taking them from a pool, so a call makes no allocation at
+// all.  The host needs the array's device address, which it takes once per device
+// (with that device current) from cudaGetSymbolAddress; the array's name in host
+// code is only a host-side stand-in and must never be handed to a kernel.
+constexpr size_t kStaticSlots = size_t(1) << 16;   // 64-bit slots: 512 KiB per device
+
+struct StaticState {
+    bool ready = false;
+    int sms = 0;
+    unsigned long long *slots = nullptr;                // device address of the array
+};
+StaticState g_static[kMaxDevices];
+std::mutex g_static_mu;
+
+}  // namespace
+
+// Fixed scratch of lookup_draft_noalloc (file scope; every GPU that loads the
+// library holds it until the process exits).
+static __device__ __align__(256) unsigned long long g_static_slots[kStaticSlots];
+
+namespace {
+
+// Per-device set-up of lookup_draft_noalloc, once: SM count, the scan kernels'
+// shared-memory opt-in, and the device address of g_static_slots.  No allocation.
+int static_state(StaticState **out) {
+    int dev = 0;
+    LD_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice, "device index");
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    StaticState &st = g_static[dev];
+    if (!st.ready) {
+        int sms = 0;
+        LD_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+        const int smem_max = int(scan_smem_layout(kOffCap - 1, LOOKUP_DRAFT_MAX_M).total);
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<3, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<3, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+        LD_CUDA(cudaFuncSetAttribute(scan_kernel<4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+        void *ptr = nullptr;
+        LD_CUDA(cudaGetSymbolAddress(&ptr, g_static_slots));
+        st.sms = sms;
+        st.slots = static_cast<unsigned long long *>(ptr);
+        st.ready = true;
+    }
+    *out = &st;
+    return LOOKUP_DRAFT_OK;
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ C ABI ----
@@ -927,11 +981,32 @@ int lookup_draft_host(const int32_t *h_tokens, const int64_t *h_offsets, int32_t
     return rc;
 }
 
+int lookup_draft_noalloc(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t min_m, int32_t max_m,
+                         int32_t K, int32_t *out_draft, int32_t *out_len, int32_t *out_pos,
+                         struct CUstream_st *stream) {
+    g_cuda_msg[0] = '\0';
+    int rc = check_common(tokens, offsets, B, min_m, max_m, K);
+    if (rc == LOOKUP_DRAFT_OK) rc = check_outputs(B, K, out_draft, out_len, out_pos, nullptr);
+    if (rc != LOOKUP_DRAFT_OK || B == 0) return rc;
+    StaticState *st = nullptr;
+    rc = static_state(&st);
+    if (rc != LOOKUP_DRAFT_OK) return rc;
+    DeviceState ds;                                     // SM count only: no pool is made or used
+    ds.sms = st->sms;
+    ds.ready = true;
+    if (size_t(B) + size_t(grid_for(ds)) * kWarps > kStaticSlots) return LOOKUP_DRAFT_ERANGE;
+    rc = launch_scan(ds, tokens, offsets, B, min_m, max_m, st->slots, stream);
+    if (rc == LOOKUP_DRAFT_OK)
+        rc = launch_fill(ds, tokens, offsets, B, K, st->slots, out_draft, out_len, out_pos, nullptr, stream);
+    return rc;
+}
+
 const char *lookup_draft_strerror(int code) {
     switch (code) {
     case LOOKUP_DRAFT_OK: return "ok";
     case LOOKUP_DRAFT_EINVAL: return "invalid argument";
     case LOOKUP_DRAFT_ECUDA: return "CUDA error";
+    case LOOKUP_DRAFT_ERANGE: return "batch too large for the fixed scratch of lookup_draft_noalloc";
     default: return "unknown lookup_draft status";
     }
 }
