@@ -368,24 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
         const int wn = int(wq1 - wq0);
         const int wbeg = int(((WA > a_begin) ? WA : a_begin) - WA);
         const int wend = int(((4 * (P.q_lo + wq1) < a_end) ? 4 * (P.q_lo + wq1) : a_end) - WA);
-        const int rw_lo = owner(WA + wbeg, 0, B - 1);
-
-        // 3. Suffix tokens (row[j] = t[L-1-j], lane j) of requests rw_lo, rw_lo + 1,
-        //    ...: loads issued before the bulk reads, so they are not queued behind
-        //    them.
-        int64_t bound[kSufRows + 1];
-#pragma unroll
-        for (int row = 0; row <= kSufRows; ++row) bound[row] = off_a(rw_lo + row <= B ? rw_lo + row : B);
-        int32_t sreg[kSufRows];
-#pragma unroll
-        for (int row = 0; row < kSufRows; ++row) {
-            const int64_t src = bound[row + 1] - 1 - lane;
-            const bool ld = rw_lo + row < B && lane < max_m && src >= bound[row];
-            sreg[row] = ld ? __ldg(ta + src) : 0;
-        }
-
-        // 4. Tiles: tile k is quads [k*tq, min((k+1)*tq, wn)) of the range; the
-        //    ring holds kBufs of them, tile k in buffer k % kBufs.
+        // 3. Tiles: tile k is quads [k*tq, min((k+1)*tq, wn)) of the range; the ring
+        //    holds kBufs of them, tile k in buffer k % kBufs.  The first one is
+        //    issued at once, the rest after the suffix loads below, so that only
+        //    one tile per warp is queued ahead of those latency-critical loads.
         const int halo = (max_m - 1 + 3) >> 2;
         int tq = (wn + 1) / 2;
         tq = tq < kTileQuadsMin ? kTileQuadsMin : (tq > kTileQuadsMax ? kTileQuadsMax : tq);
@@ -402,9 +388,23 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
             mbar_expect_tx(bar, bytes);
             bulk_copy_g2s(smem_addr(buf + size_t(kHaloQuads - (t0 - ls)) * 16), ta + ls * 4, bytes, bar);
         };
+        if (lane == 0) issue_tile(0, 0);
+        const int rw_lo = owner(WA + wbeg, 0, B - 1);
+
+        // 4. Suffix tokens (row[j] = t[L-1-j], lane j) of requests rw_lo, rw_lo + 1, ...
+        int64_t bound[kSufRows + 1];
+#pragma unroll
+        for (int row = 0; row <= kSufRows; ++row) bound[row] = off_a(rw_lo + row <= B ? rw_lo + row : B);
+        int32_t sreg[kSufRows];
+#pragma unroll
+        for (int row = 0; row < kSufRows; ++row) {
+            const int64_t src = bound[row + 1] - 1 - lane;
+            const bool ld = rw_lo + row < B && lane < max_m && src >= bound[row];
+            sreg[row] = ld ? __ldg(ta + src) : 0;
+        }
         if (lane == 0) {
             const int first = ntiles < kBufs ? ntiles : kBufs;
-            for (int k = 0; k < first; ++k) issue_tile(k, k);
+            for (int k = 1; k < first; ++k) issue_tile(k, k);
         }
         const int rw_hi = owner(WA + wend - 1, rw_lo, B - 1);
         const int nrows = (rw_hi - rw_lo + 1 < kSufRows) ? rw_hi - rw_lo + 1 : kSufRows;
