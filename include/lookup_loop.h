@@ -1,0 +1,141 @@
+/*
+ * lookup_loop.h -- the decode-loop steps around prompt-lookup drafting, on GB300.
+ *
+ * Source: HyperQwen lookup-drafting article, kwkr.cn/news/564408.
+ *  - "第2步" (fusion): the lookup draft is merged with the draft model's proposals,
+ *    not written over them.  In the head (the positions the draft model proposes,
+ *    7 in the article) a lookup match of >= 8 tokens replaces the proposals; a
+ *    shorter match of >= 6 is adopted only when the draft model independently
+ *    proposed the same first 2 tokens.  In the tail (8 further positions nobody
+ *    proposed) a match of >= 4 tokens is enough.
+ *  - "第3步" (scheduling): the long verify block (head + tail) is used only while
+ *    the request is copying.  It is entered when the lookup match can fill the
+ *    tail and the previous step's output was a nearly full block, on two
+ *    consecutive steps; once entered it is kept for 3 more steps after the
+ *    condition drops (sticky exit).
+ *  - "第3步" (losslessness): greedy verification reads no proposal distribution;
+ *    for sampled requests every lookup-filled position is rewritten as a point
+ *    mass on the proposed token, a legal proposal for the rejection sampler.
+ *
+ * All arrays are device memory owned by the caller, row-major; every call
+ * enqueues its work on `stream` and returns without synchronising.  Return
+ * codes are those of lookup_draft.h (LOOKUP_DRAFT_OK, LOOKUP_DRAFT_EINVAL for
+ * arguments that describe no valid call, LOOKUP_DRAFT_ECUDA for a failed
+ * launch).  B == 0 enqueues nothing.
+ */
+#ifndef LOOKUP_LOOP_H
+#define LOOKUP_LOOP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+
+/*
+ * Fusion of the lookup draft with the draft model's proposals ("第2步").
+ *
+ * lookup_draft  int32 [B][K]: drafts from lookup_draft_ex (K >= H + T)
+ * lookup_mlen   int32 [B]: their match lengths (0 = no match)
+ * model_draft   int32 [B][H]: the draft model's proposals for the head
+ * long_block    int32 [B]: nonzero = this step verifies head + tail; NULL = all 0
+ * H, T          head and tail lengths (the article: 7 and 8); H >= 1, T >= 0
+ * replace_min   match length that replaces the head outright (8)
+ * agree_min     shorter match length adopted when the model agrees (6)
+ * agree_n       number of leading tokens that must agree (2), 0 <= agree_n <= H
+ * tail_min      match length that fills the tail (4)
+ * out_block     int32 [B][H + T]: the proposal block; unused tail slots -1
+ * out_len       int32 [B]: proposals in the block, H or H + T
+ * out_point_mass int32 [B][H + T]: 1 where the position holds a lookup token
+ *               (its proposal distribution is a point mass), else 0
+ *
+ * Per request, with m = lookup_mlen[r], L = lookup_draft[r], M = model_draft[r]:
+ *   head_lookup = m >= replace_min || (m >= agree_min && L[0..agree_n) == M[0..agree_n))
+ *   block[i] = head_lookup ? L[i] : M[i] for i < H          (point mass = head_lookup)
+ *   if long_block[r] and m >= tail_min: block[H + i] = L[H + i] for i < T, len = H + T
+ *   else: block[H + i] = -1, len = H
+ * The head and tail rules are applied independently, as the article states them.
+ */
+int lookup_fuse(const int32_t *lookup_draft, const int32_t *lookup_mlen, const int32_t *model_draft,
+                const int32_t *long_block, int32_t B, int32_t K, int32_t H, int32_t T,
+                int32_t replace_min, int32_t agree_min, int32_t agree_n, int32_t tail_min,
+                int32_t *out_block, int32_t *out_len, int32_t *out_point_mass,
+                struct CUstream_st *stream);
+
+/*
+ * Long-block scheduling ("第3步"), one update per request and step.
+ *
+ * lookup_mlen   int32 [B]: this step's lookup match length
+ * committed     int32 [B]: tokens the previous step committed (accepted + 1)
+ * state         int32 [B][3] in/out: {long, streak, hold}; all zero initially
+ * out_long      int32 [B]: 1 = verify the long block (head + tail) this step
+ * H, T          head and tail lengths; a step's full block commits H + 1 tokens
+ *               (short) or H + T + 1 (long)
+ * tail_min      match length that can fill the tail (4)
+ * slack         "nearly full": committed >= full - slack (1)
+ * enter_steps   consecutive steps the condition must hold to enter (2)
+ * sticky        steps the long block is kept after the condition drops (3)
+ *
+ * Per request: full = (long ? H + T : H) + 1 for the block the previous step used;
+ *   cond = m >= tail_min && committed >= full - slack;
+ *   streak = cond ? streak + 1 : 0;
+ *   if !long: if streak >= enter_steps: long = 1, hold = sticky
+ *   else if cond: hold = sticky
+ *   else if hold > 0: hold -= 1            (kept: sticky exit)
+ *   else: long = 0
+ *   out_long = long
+ */
+int lookup_schedule(const int32_t *lookup_mlen, const int32_t *committed, int32_t B,
+                    int32_t H, int32_t T, int32_t tail_min, int32_t slack, int32_t enter_steps,
+                    int32_t sticky, int32_t *state, int32_t *out_long, struct CUstream_st *stream);
+
+/*
+ * Verification of a proposal block of width P (= H + T), greedy or sampled.
+ *
+ * block         int32 [B][P], len int32 [B] (proposals used, 0 <= len <= P)
+ * Greedy (probs == NULL): target int32 [B][P + 1] holds the target model's
+ *   greedy token at each position given the block before it; accepted a is the
+ *   largest a <= len with block[i] == target[i] for all i < a, and the step
+ *   commits block[0..a) then target[a].
+ * Sampled (probs != NULL): probs float [B][P] holds the target probability of
+ *   each proposed token, qprobs float [B][P] the proposal probability of it (may
+ *   be NULL = 1), point_mass int32 [B][P] (may be NULL) marks lookup positions,
+ *   whose proposal probability is taken as exactly 1 (the point-mass rewrite),
+ *   u float [B][P] uniform [0, 1) draws, and target int32 [B][P + 1] the tokens
+ *   to commit at the first rejection (drawn by the caller from the residual
+ *   distribution) or after a full acceptance (the bonus token).  Position i is
+ *   accepted when u[i] * q[i] < p[i] (float32, as written); a is the first
+ *   position not accepted (or len), and the step commits block[0..a) then
+ *   target[a].
+ * out_accepted  int32 [B]: a
+ * out_commit    int32 [B][P + 1]: the committed tokens; slots past a + 1 are -1
+ * out_ncommit   int32 [B]: a + 1
+ */
+int lookup_verify(const int32_t *block, const int32_t *len, const int32_t *target, const float *probs,
+                  const float *qprobs, const int32_t *point_mass, const float *u, int32_t B, int32_t P,
+                  int32_t *out_accepted, int32_t *out_commit, int32_t *out_ncommit,
+                  struct CUstream_st *stream);
+
+/*
+ * The next step's histories: request r's history followed by its committed
+ * tokens, as a new CSR batch.
+ *
+ * tokens, offsets  the current CSR batch (offsets[0] may be > 0)
+ * commit           int32 [B][W], ncommit int32 [B] (0 <= ncommit <= W)
+ * out_offsets      int64 [B + 1]: new boundaries, out_offsets[0] = 0
+ * out_tokens       int32 [offsets[B] - offsets[0] + sum(ncommit)]
+ * The new history of r is tokens[offsets[r] .. offsets[r+1]) then
+ * commit[r][0 .. ncommit[r]).  Outputs must not overlap the inputs.
+ */
+int lookup_append(const int32_t *tokens, const int64_t *offsets, const int32_t *commit, const int32_t *ncommit,
+                  int32_t B, int32_t W, int32_t *out_tokens, int64_t *out_offsets,
+                  struct CUstream_st *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOOKUP_LOOP_H */

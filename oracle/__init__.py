@@ -27,7 +27,7 @@ from concurrent.futures import ThreadPoolExecutor
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "lookup_oracle.c")
+_SRCS = [os.path.join(_HERE, "lookup_oracle.c"), os.path.join(_HERE, "loop_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liblookup_oracle.so")
 
@@ -39,11 +39,11 @@ def build(force: bool = False) -> str:
     """Compile the oracle into a shared object next to its source; return its path."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB_PATH) >= os.path.getmtime(s) for s in _SRCS)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     subprocess.run(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-Wall", "-Wextra",
-                    "-o", tmp, _SRC], check=True)
+                    "-o", tmp, *_SRCS], check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -69,6 +69,15 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_find_match.restype = ctypes.c_int
     lib.oracle_fill_draft.argtypes = [p32, i64, i32, i64, i32, p32]
     lib.oracle_fill_draft.restype = None
+    vp = ctypes.c_void_p
+    lib.oracle_fuse.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+    lib.oracle_fuse.restype = ctypes.c_int
+    lib.oracle_schedule.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp]
+    lib.oracle_schedule.restype = ctypes.c_int
+    lib.oracle_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, vp]
+    lib.oracle_verify.restype = ctypes.c_int
+    lib.oracle_append.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp]
+    lib.oracle_append.restype = ctypes.c_int
     return lib
 
 
@@ -140,3 +149,85 @@ def fill_draft(history, m: int, p: int, K: int, lib: ctypes.CDLL | None = None):
     lib.oracle_fill_draft(_ptr(t, ctypes.c_int32), int(t.shape[0]), m, p, K,
                           _ptr(out, ctypes.c_int32))
     return out
+
+
+# ------------------------------------------------------------- loop steps ----
+def _arr(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data
+
+
+def fuse(lookup_draft, lookup_mlen, model_draft, long_block, H: int, T: int, replace_min: int = 8,
+         agree_min: int = 6, agree_n: int = 2, tail_min: int = 4, lib=None):
+    """Fusion of lookup drafts with draft-model proposals (HyperQwen article, "第2步").
+    Returns (block [B][H+T], len [B], point_mass [B][H+T])."""
+    lib = lib or load()
+    ld = _arr(lookup_draft, np.int32)
+    lm = _arr(lookup_mlen, np.int32)
+    md = _arr(model_draft, np.int32)
+    lg = _arr(long_block, np.int32)
+    B, K = ld.shape
+    block = np.empty((B, H + T), np.int32)
+    ln = np.empty(B, np.int32)
+    pm = np.empty((B, H + T), np.int32)
+    rc = lib.oracle_fuse(_p(ld), _p(lm), _p(md), _p(lg), B, K, H, T, replace_min, agree_min, agree_n,
+                         tail_min, _p(block), _p(ln), _p(pm))
+    if rc:
+        raise ValueError("oracle_fuse rejected the arguments")
+    return block, ln, pm
+
+
+def schedule(lookup_mlen, committed, state, H: int, T: int, tail_min: int = 4, slack: int = 1,
+             enter_steps: int = 2, sticky: int = 3, lib=None):
+    """One long-block scheduling update ("第3步"); `state` [B][3] is updated in place.
+    Returns out_long [B]."""
+    lib = lib or load()
+    lm = _arr(lookup_mlen, np.int32)
+    cm = _arr(committed, np.int32)
+    assert state.dtype == np.int32 and state.flags["C_CONTIGUOUS"]
+    B = lm.shape[0]
+    out = np.empty(B, np.int32)
+    rc = lib.oracle_schedule(_p(lm), _p(cm), B, H, T, tail_min, slack, enter_steps, sticky,
+                             _p(state), _p(out))
+    if rc:
+        raise ValueError("oracle_schedule rejected the arguments")
+    return out
+
+
+def verify(block, length, target, probs=None, qprobs=None, point_mass=None, u=None, lib=None):
+    """Greedy (probs None) or sampled verification of proposal blocks.
+    Returns (accepted [B], commit [B][P+1], ncommit [B])."""
+    lib = lib or load()
+    bl = _arr(block, np.int32)
+    ln = _arr(length, np.int32)
+    tg = _arr(target, np.int32)
+    pr, qp, pm, uu = _arr(probs, np.float32), _arr(qprobs, np.float32), _arr(point_mass, np.int32), _arr(u, np.float32)
+    B, P = bl.shape
+    acc = np.empty(B, np.int32)
+    commit = np.empty((B, P + 1), np.int32)
+    nc = np.empty(B, np.int32)
+    rc = lib.oracle_verify(_p(bl), _p(ln), _p(tg), _p(pr), _p(qp), _p(pm), _p(uu), B, P,
+                           _p(acc), _p(commit), _p(nc))
+    if rc:
+        raise ValueError("oracle_verify rejected the arguments")
+    return acc, commit, nc
+
+
+def append(tokens, offsets, commit, ncommit, lib=None):
+    """The next CSR batch: every history followed by its committed tokens."""
+    lib = lib or load()
+    tk = _arr(tokens, np.int32)
+    of = _arr(offsets, np.int64)
+    cm = _arr(commit, np.int32)
+    nc = _arr(ncommit, np.int32)
+    B, W = cm.shape
+    total = int(of[-1] - of[0]) + int(nc.sum())
+    out_t = np.empty(total, np.int32)
+    out_o = np.empty(B + 1, np.int64)
+    rc = lib.oracle_append(_p(tk), _p(of), _p(cm), _p(nc), B, W, _p(out_t), _p(out_o))
+    if rc:
+        raise ValueError("oracle_append rejected the arguments")
+    return out_t, out_o

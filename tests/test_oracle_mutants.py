@@ -21,6 +21,7 @@ from goldens import load_cases
 from invariants import check_small
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "lookup_oracle.c")
+LOOP_SRC = os.path.join(os.path.dirname(oracle.__file__), "loop_oracle.c")
 
 MUTANTS = {
     "oldest_first": ("for (int64_t p = L - m - 1; p >= 0; --p)",
@@ -101,6 +102,59 @@ def test_mutant_is_caught(name, tmp_path):
     so_path = tmp_path / "libmutant.so"
     c_path.write_text(mutated, encoding="utf-8")
     subprocess.run(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", "-o", str(so_path),
-                    str(c_path)], check=True)
+                    str(c_path), LOOP_SRC], check=True)
     failed = _pins_fail(oracle.load(str(so_path)))
     assert failed, f"mutant {name} passed every pin"
+
+
+# ------------------------------------------------------- loop-step oracle ----
+LOOP_MUTANTS = {
+    "replace_strict": ("if (m >= replace_min)", "if (m > replace_min)"),
+    "agree_ignored": ("else if (m >= agree_min && agree)", "else if (m >= agree_min)"),
+    "tail_threshold": ("int tail = is_long && m >= tail_min;", "int tail = is_long && m > tail_min;"),
+    "tail_not_long": ("int tail = is_long && m >= tail_min;", "int tail = m >= tail_min;"),
+    "no_sticky": ("st[2] -= 1;                              /* sticky exit: keep the long block */",
+                  "st[0] = 0;"),
+    "enter_at_once": ("if (st[1] >= enter_steps) {", "if (st[1] >= 1) {"),
+    "full_ignores_long": ("int32_t full = (st[0] ? H + T : H) + 1;", "int32_t full = H + 1;"),
+    "greedy_off_by_one": ("ok = block[a] == target[a];", "ok = block[a] == target[a + 1];"),
+    "point_mass_ignored": ("qa = 1.0f;                       /* point mass on the lookup token */", "qa = qa;"),
+    "no_bonus": ("commit[i] = i < a ? block[i] : (i == a ? target[a] : -1);",
+                 "commit[i] = i < a ? block[i] : -1;"),
+    "append_order": ("        for (int64_t i = offsets[r]; i < offsets[r + 1]; ++i)\n            out_tokens[pos++] = tokens[i];\n        for (int32_t j = 0; j < ncommit[r]; ++j)\n            out_tokens[pos++] = commit[(int64_t)r * W + j];",
+                     "        for (int32_t j = 0; j < ncommit[r]; ++j)\n            out_tokens[pos++] = commit[(int64_t)r * W + j];\n        for (int64_t i = offsets[r]; i < offsets[r + 1]; ++i)\n            out_tokens[pos++] = tokens[i];"),
+}
+
+
+def _loop_pins_fail(lib) -> list[str]:
+    import test_loop_oracle_pins as pins
+    failed = []
+    saved = oracle.load
+    oracle.load = lambda path=None: lib
+    try:
+        for name in dir(pins):
+            if name.startswith("test_"):
+                try:
+                    getattr(pins, name)()
+                except (AssertionError, ValueError, Exception):  # noqa: B014 - any failure counts
+                    failed.append(name)
+    finally:
+        oracle.load = saved
+    return failed
+
+
+def test_unmutated_loop_oracle_passes_its_pins():
+    assert _loop_pins_fail(oracle.load()) == []
+
+
+@pytest.mark.parametrize("name", sorted(LOOP_MUTANTS))
+def test_loop_mutant_is_caught(name, tmp_path):
+    old, new = LOOP_MUTANTS[name]
+    src = open(LOOP_SRC, encoding="utf-8").read()
+    assert src.count(old) >= 1, f"mutation target for {name} not found in the loop oracle"
+    c_path = tmp_path / "loop_mutant.c"
+    so_path = tmp_path / "libloopmutant.so"
+    c_path.write_text(src.replace(old, new, 1), encoding="utf-8")
+    subprocess.run(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", "-o", str(so_path), SRC, str(c_path)],
+                   check=True)
+    assert _loop_pins_fail(oracle.load(str(so_path))), f"mutant {name} passed every pin"
