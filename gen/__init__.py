@@ -178,3 +178,87 @@ def make_workload(name: str, seed: int | None = None) -> Workload:
         plant_copy(h, s0, c)
         planted[r] = (s0, c)
     return Workload(name, tokens, offsets, 4, 12, K, seed, planted)
+
+
+# ----------------------------------------------------------- loop-step inputs ----
+# Random inputs for the decode-loop steps (fusion, scheduling, verification,
+# append).  As above, only draws: no rule of the method is applied here.  Values
+# are concentrated where the rules have their thresholds (match lengths 3..8,
+# commit counts near a full short or long block, exact ties in the sampled
+# acceptance test) so that every branch is taken often.
+
+def loop_fuse_inputs(B: int, K: int, H: int, T: int, agree_n: int, seed: int, vocab: int = 50):
+    """(lookup_draft [B,K], lookup_mlen [B], model_draft [B,H], long_block [B])."""
+    rng = rng_for(seed, 101)
+    ld = rng.integers(0, vocab, size=(B, K), dtype=np.int64).astype(np.int32)
+    special = np.array([0, 3, 4, 5, 6, 7, 8, 9, 12], np.int32)
+    m = np.where(rng.random(B) < 0.7, special[rng.integers(0, special.size, size=B)],
+                 rng.integers(0, 17, size=B)).astype(np.int32)
+    md = rng.integers(0, vocab, size=(B, H), dtype=np.int64).astype(np.int32)
+    copy = rng.random(B) < 0.5                       # the model proposes the lookup's head ...
+    md[copy] = ld[copy, :H]
+    if agree_n > 0:                                  # ... sometimes with one agreement token changed
+        bump = copy & (rng.random(B) < 0.3)
+        col = rng.integers(0, agree_n, size=B)
+        md[bump, col[bump]] += 1
+    long_block = (rng.random(B) < 0.5).astype(np.int32)
+    return ld, m, md, long_block
+
+
+def loop_schedule_trace(B: int, steps: int, H: int, T: int, seed: int):
+    """(lookup_mlen [steps,B], committed [steps,B]): each request switches at random
+    between copying (long matches, nearly full commits) and free text."""
+    rng = rng_for(seed, 102)
+    copying = rng.random(B) < 0.5
+    mlen = np.empty((steps, B), np.int32)
+    committed = np.empty((steps, B), np.int32)
+    for s in range(steps):
+        flip = rng.random(B) < 0.15
+        copying = np.where(flip, ~copying, copying)
+        m_copy = rng.integers(3, 13, size=B)
+        m_free = np.where(rng.random(B) < 0.6, 0, rng.integers(0, 7, size=B))
+        mlen[s] = np.where(copying, m_copy, m_free)
+        near = np.array([H - 1, H, H + 1, H + T - 1, H + T, H + T + 1])
+        c_copy = near[rng.integers(0, near.size, size=B)]
+        c_free = rng.integers(1, H + T + 2, size=B)
+        committed[s] = np.maximum(np.where(copying, c_copy, c_free), 1)
+    return mlen, committed
+
+
+def loop_verify_inputs(B: int, P: int, seed: int, vocab: int = 50):
+    """(block [B,P], len [B], target [B,P+1], probs, qprobs, point_mass, u) with the
+    target agreeing with the block on a random prefix, and exact ties u*q == p."""
+    rng = rng_for(seed, 103)
+    block = rng.integers(0, vocab, size=(B, P), dtype=np.int64).astype(np.int32)
+    length = rng.integers(0, P + 1, size=B).astype(np.int32)
+    full = rng.random(B) < 0.3
+    length[full] = P
+    target = rng.integers(0, vocab, size=(B, P + 1), dtype=np.int64).astype(np.int32)
+    first_diff = rng.integers(0, P + 1, size=B)
+    first_diff[rng.random(B) < 0.3] = P
+    for r in range(B):
+        f = int(first_diff[r])
+        target[r, :f] = block[r, :f]
+        if f < P:
+            target[r, f] = block[r, f] + 1
+    probs = rng.random((B, P), dtype=np.float32)
+    qprobs = (1.0 - rng.random((B, P), dtype=np.float32)).astype(np.float32)   # (0, 1]
+    u = rng.random((B, P), dtype=np.float32)
+    tie = rng.random((B, P)) < 0.05                  # u * 1 == p exactly
+    qprobs[tie] = 1.0
+    probs[tie] = u[tie]
+    half = (~tie) & (rng.random((B, P)) < 0.05)      # u * 0.5 == p exactly
+    qprobs[half] = 0.5
+    probs[half] = u[half] * np.float32(0.5)
+    easy = rng.random(B) < 0.4                       # long accepted runs
+    probs[easy] = np.float32(0.999)
+    point_mass = (rng.random((B, P)) < 0.5).astype(np.int32)
+    return block, length, target, probs, qprobs, point_mass, u
+
+
+def loop_append_inputs(B: int, W: int, seed: int, vocab: int = VOCAB_QWEN):
+    """(commit [B,W], ncommit [B]) with counts in [0, W]."""
+    rng = rng_for(seed, 104)
+    commit = rng.integers(0, vocab, size=(B, W), dtype=np.int64).astype(np.int32)
+    ncommit = rng.integers(0, W + 1, size=B).astype(np.int32)
+    return commit, ncommit

@@ -21,7 +21,8 @@
  * enqueues its work on `stream` and returns without synchronising.  Return
  * codes are those of lookup_draft.h (LOOKUP_DRAFT_OK, LOOKUP_DRAFT_EINVAL for
  * arguments that describe no valid call, LOOKUP_DRAFT_ECUDA for a failed
- * launch).  B == 0 enqueues nothing.
+ * launch).  B == 0 enqueues nothing, except in lookup_append, which then
+ * writes out_offsets[0] = 0.
  */
 #ifndef LOOKUP_LOOP_H
 #define LOOKUP_LOOP_H
@@ -42,7 +43,8 @@ struct CUstream_st;
  * lookup_mlen   int32 [B]: their match lengths (0 = no match)
  * model_draft   int32 [B][H]: the draft model's proposals for the head
  * long_block    int32 [B]: nonzero = this step verifies head + tail; NULL = all 0
- * H, T          head and tail lengths (the article: 7 and 8); H >= 1, T >= 0
+ * H, T          head and tail lengths (the article: 7 and 8); H >= 1, T >= 0,
+ *               H + T <= 65536
  * replace_min   match length that replaces the head outright (8)
  * agree_min     shorter match length adopted when the model agrees (6)
  * agree_n       number of leading tokens that must agree (2), 0 <= agree_n <= H
@@ -95,7 +97,9 @@ int lookup_schedule(const int32_t *lookup_mlen, const int32_t *committed, int32_
 /*
  * Verification of a proposal block of width P (= H + T), greedy or sampled.
  *
- * block         int32 [B][P], len int32 [B] (proposals used, 0 <= len <= P)
+ * block         int32 [B][P] (P <= 65536), len int32 [B] (proposals used,
+ *               0 <= len <= P; a request with len outside that range gets the
+ *               error row accepted = -1, ncommit = 0, commit all -1)
  * Greedy (probs == NULL): target int32 [B][P + 1] holds the target model's
  *   greedy token at each position given the block before it; accepted a is the
  *   largest a <= len with block[i] == target[i] for all i < a, and the step
@@ -124,9 +128,12 @@ int lookup_verify(const int32_t *block, const int32_t *len, const int32_t *targe
  * tokens, as a new CSR batch.
  *
  * tokens, offsets  the current CSR batch (offsets[0] may be > 0)
- * commit           int32 [B][W], ncommit int32 [B] (0 <= ncommit <= W)
+ * commit           int32 [B][W], ncommit int32 [B] (0 <= ncommit <= W; a value
+ *                  outside is clamped to that range)
  * out_offsets      int64 [B + 1]: new boundaries, out_offsets[0] = 0
- * out_tokens       int32 [offsets[B] - offsets[0] + sum(ncommit)]
+ * out_tokens       int32 [offsets[B] - offsets[0] + sum(ncommit)]; a buffer of
+ *                  offsets[B] - offsets[0] + B * W tokens always suffices, so
+ *                  the caller need not read the counts back first
  * The new history of r is tokens[offsets[r] .. offsets[r+1]) then
  * commit[r][0 .. ncommit[r]).  Outputs must not overlap the inputs.
  */

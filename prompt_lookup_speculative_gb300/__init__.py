@@ -1,7 +1,8 @@
 """GB300 prompt-lookup (n-gram) speculative drafting.
 
-Python binding of the C ABI in ``include/lookup_draft.h`` (ctypes; argument
-marshalling only -- every step of the draft runs in the library's CUDA kernels).
+Python binding of the C ABI in ``include/lookup_draft.h`` and
+``include/lookup_loop.h`` (ctypes; argument marshalling only -- every step runs in
+the library's CUDA kernels).
 PyTorch tensors supply device memory and the current CUDA stream.
 
     draft, length, pos = lookup_draft(tokens, offsets, min_m=4, max_m=12, K=15)
@@ -25,7 +26,7 @@ from . import build as _build
 __all__ = [
     "LookupDraftError", "load_library", "lookup_draft", "lookup_draft_ex", "lookup_draft_host",
     "lookup_draft_scan", "lookup_draft_fill", "lookup_draft_noalloc", "workspace_bytes",
-    "set_wait_limit_ns",
+    "set_wait_limit_ns", "lookup_fuse", "lookup_schedule", "lookup_verify", "lookup_append",
     "MAX_M", "MAX_K", "LEN_FAILED",
 ]
 
@@ -91,6 +92,14 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.lookup_draft_last_cuda_error.restype = ctypes.c_char_p
     lib.lookup_draft_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.lookup_draft_set_wait_limit_ns.restype = None
+    lib.lookup_fuse.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp]
+    lib.lookup_fuse.restype = ctypes.c_int
+    lib.lookup_schedule.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+    lib.lookup_schedule.restype = ctypes.c_int
+    lib.lookup_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp]
+    lib.lookup_verify.restype = ctypes.c_int
+    lib.lookup_append.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp]
+    lib.lookup_append.restype = ctypes.c_int
 
 
 def _check(rc: int, lib) -> None:
@@ -270,3 +279,119 @@ def _host_ptr(a) -> int:
 def set_wait_limit_ns(ns: int) -> None:
     """Diagnostics: limit on each bounded wait inside the scan kernel (0 = default 1 s)."""
     load_library().lookup_draft_set_wait_limit_ns(int(ns))
+
+
+# ------------------------------------------------------------- loop steps ----
+def _dev(t, dtype, shape, device, name, optional=False):
+    """Check a device tensor argument; return its pointer (None for an absent optional)."""
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or t.device != device:
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} on {device}")
+    return t.data_ptr()
+
+
+def lookup_fuse(lookup_draft, lookup_mlen, model_draft, long_block=None, H: int = 7, T: int = 8,
+                replace_min: int = 8, agree_min: int = 6, agree_n: int = 2, tail_min: int = 4,
+                out=None, stream=None):
+    """Merge lookup drafts with the draft model's head proposals (HyperQwen
+    lookup-drafting article, section "第2步").  Returns (block [B, H+T], len [B],
+    point_mass [B, H+T]), int32 tensors on the inputs' device."""
+    import torch
+    lib = load_library()
+    dev = lookup_draft.device
+    B, K = lookup_draft.shape
+    args = (_dev(lookup_draft, torch.int32, (B, K), dev, "lookup_draft"),
+            _dev(lookup_mlen, torch.int32, (B,), dev, "lookup_mlen"),
+            _dev(model_draft, torch.int32, (B, H), dev, "model_draft"),
+            _dev(long_block, torch.int32, (B,), dev, "long_block", optional=True))
+    if out is None:
+        out = (torch.empty((B, H + T), dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev),
+               torch.empty((B, H + T), dtype=torch.int32, device=dev))
+    block, ln, pm = out
+    optr = (_dev(block, torch.int32, (B, H + T), dev, "block"), _dev(ln, torch.int32, (B,), dev, "len"),
+            _dev(pm, torch.int32, (B, H + T), dev, "point_mass"))
+    with torch.cuda.device(dev):
+        rc = lib.lookup_fuse(*args, B, K, H, T, replace_min, agree_min, agree_n, tail_min, *optr,
+                             _stream_handle(stream))
+    _check(rc, lib)
+    return block, ln, pm
+
+
+def lookup_schedule(lookup_mlen, committed, state, H: int = 7, T: int = 8, tail_min: int = 4, slack: int = 1,
+                    enter_steps: int = 2, sticky: int = 3, out=None, stream=None):
+    """One long-block scheduling update ("第3步"); ``state`` (int32 [B, 3], zeros at
+    the start) is updated in place.  Returns out_long [B]."""
+    import torch
+    lib = load_library()
+    dev = lookup_mlen.device
+    B = lookup_mlen.shape[0]
+    args = (_dev(lookup_mlen, torch.int32, (B,), dev, "lookup_mlen"),
+            _dev(committed, torch.int32, (B,), dev, "committed"))
+    sp = _dev(state, torch.int32, (B, 3), dev, "state")
+    if out is None:
+        out = torch.empty(B, dtype=torch.int32, device=dev)
+    op = _dev(out, torch.int32, (B,), dev, "out_long")
+    with torch.cuda.device(dev):
+        rc = lib.lookup_schedule(*args, B, H, T, tail_min, slack, enter_steps, sticky, sp, op,
+                                 _stream_handle(stream))
+    _check(rc, lib)
+    return out
+
+
+def lookup_verify(block, length, target, probs=None, qprobs=None, point_mass=None, u=None,
+                  out=None, stream=None):
+    """Greedy (``probs`` None) or sampled verification of proposal blocks
+    ("第3步").  Returns (accepted [B], commit [B, P+1], ncommit [B])."""
+    import torch
+    lib = load_library()
+    dev = block.device
+    B, P = block.shape
+    f32 = torch.float32
+    args = (_dev(block, torch.int32, (B, P), dev, "block"), _dev(length, torch.int32, (B,), dev, "len"),
+            _dev(target, torch.int32, (B, P + 1), dev, "target"),
+            _dev(probs, f32, (B, P), dev, "probs", optional=True),
+            _dev(qprobs, f32, (B, P), dev, "qprobs", optional=True),
+            _dev(point_mass, torch.int32, (B, P), dev, "point_mass", optional=True),
+            _dev(u, f32, (B, P), dev, "u", optional=probs is None))
+    if out is None:
+        out = (torch.empty(B, dtype=torch.int32, device=dev), torch.empty((B, P + 1), dtype=torch.int32, device=dev),
+               torch.empty(B, dtype=torch.int32, device=dev))
+    acc, commit, nc = out
+    optr = (_dev(acc, torch.int32, (B,), dev, "accepted"), _dev(commit, torch.int32, (B, P + 1), dev, "commit"),
+            _dev(nc, torch.int32, (B,), dev, "ncommit"))
+    with torch.cuda.device(dev):
+        rc = lib.lookup_verify(*args, B, P, *optr, _stream_handle(stream))
+    _check(rc, lib)
+    return acc, commit, nc
+
+
+def lookup_append(tokens, offsets, commit, ncommit, out=None, stream=None):
+    """The next step's CSR batch: every history followed by its committed tokens.
+
+    Returns (new_tokens, new_offsets).  Without ``out`` the token buffer holds
+    offsets[B] - offsets[0] + B * W tokens, enough for any counts, so the call
+    never reads the counts back to the host; the batch is
+    new_tokens[new_offsets[0] .. new_offsets[B]).
+    """
+    import torch
+    lib = load_library()
+    B = _as_batch(tokens, offsets)
+    dev = tokens.device
+    W = commit.shape[1]
+    cp = _dev(commit, torch.int32, (B, W), dev, "commit")
+    np_ = _dev(ncommit, torch.int32, (B,), dev, "ncommit")
+    if out is None:
+        out = (torch.empty(tokens.numel() + B * W, dtype=torch.int32, device=dev),
+               torch.empty(B + 1, dtype=torch.int64, device=dev))
+    out_t, out_o = out
+    if out_t.dtype != torch.int32 or not out_t.is_contiguous() or out_t.device != dev:
+        raise ValueError("out tokens must be a contiguous int32 tensor on the inputs' device")
+    op = _dev(out_o, torch.int64, (B + 1,), dev, "out_offsets")
+    with torch.cuda.device(dev):
+        rc = lib.lookup_append(tokens.data_ptr(), offsets.data_ptr(), cp, np_, B, W, out_t.data_ptr(), op,
+                               _stream_handle(stream))
+    _check(rc, lib)
+    return out_t, out_o

@@ -1,7 +1,8 @@
 """Compile the CUDA library in-tree for GB300 (sm_103a).
 
-The library is one translation unit, ``csrc/lookup_draft.cu``, built with nvcc
-into ``_build/liblookup_draft.so`` next to this file.  The CUDA runtime is linked
+The library is two translation units, ``csrc/lookup_draft.cu`` (the drafting
+step) and ``csrc/lookup_loop.cu`` (the decode-loop steps around it), built with
+nvcc into ``_build/liblookup_draft.so`` next to this file.  The CUDA runtime is linked
 statically, so the library loads on a machine without a GPU (its calls then
 fail with a CUDA error) and needs nothing from the Python environment.
 """
@@ -14,8 +15,8 @@ import subprocess
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 REPO_DIR = os.path.dirname(PKG_DIR)
 INCLUDE_DIR = os.path.join(REPO_DIR, "include")
-SOURCES = [os.path.join(PKG_DIR, "csrc", "lookup_draft.cu")]
-HEADERS = [os.path.join(INCLUDE_DIR, "lookup_draft.h")]
+SOURCES = [os.path.join(PKG_DIR, "csrc", "lookup_draft.cu"), os.path.join(PKG_DIR, "csrc", "lookup_loop.cu")]
+HEADERS = [os.path.join(INCLUDE_DIR, "lookup_draft.h"), os.path.join(INCLUDE_DIR, "lookup_loop.h")]
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "liblookup_draft.so")
 

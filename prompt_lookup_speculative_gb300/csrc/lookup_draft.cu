@@ -825,6 +825,12 @@ std::mutex g_static_mu;
 
 }  // namespace
 
+// The error record shared with the loop-step entry points of lookup_loop.cu
+// (same library; not exported from it).
+__attribute__((visibility("hidden"))) int lookup_record_cuda_error(cudaError_t e, const char *what) {
+    return cuda_fail(e, what);
+}
+
 // Fixed scratch of lookup_draft_noalloc (file scope; every GPU that loads the
 // library holds it until the process exits).
 static __device__ __align__(256) unsigned long long g_static_slots[kStaticSlots];

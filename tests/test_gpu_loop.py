@@ -1,0 +1,226 @@
+"""GPU parity of the decode-loop steps (include/lookup_loop.h) against the oracle.
+
+Every comparison is element by element and exact: the steps are integer work,
+and the one floating-point decision (the sampled acceptance test u * q < p) is
+taken in float32 on both sides, as the header states.  Inputs come from the
+seeded generators in gen/, at sizes the oracle finishes in well under a second,
+and at the full sizes of the drafting workloads for the append.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import gen
+import oracle
+
+torch = pytest.importorskip("torch")
+pkg = pytest.importorskip("prompt_lookup_speculative_gb300")
+
+pytestmark = pytest.mark.gpu
+
+
+def dev(a):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+# ------------------------------------------------------------------ fusion ----
+@pytest.mark.parametrize("B", [1, 7, 4096])
+@pytest.mark.parametrize("H,T,agree_n", [(7, 8, 2), (3, 2, 0), (3, 2, 3), (1, 0, 1), (7, 0, 2), (16, 48, 2)])
+@pytest.mark.parametrize("seed", [1, 2])
+def test_fuse_matches_oracle(B, H, T, agree_n, seed):
+    K = max(H + T, 15)
+    ld, m, md, lg = gen.loop_fuse_inputs(B, K, H, T, agree_n, seed)
+    want = oracle.fuse(ld, m, md, lg, H, T, agree_n=agree_n)
+    got = pkg.lookup_fuse(dev(ld), dev(m), dev(md), dev(lg), H, T, agree_n=agree_n)
+    for w, g in zip(want, got):
+        np.testing.assert_array_equal(host(g), w)
+
+
+@pytest.mark.parametrize("rm,am,tm", [(8, 6, 4), (4, 4, 4), (1, 20, 0), (13, 13, 13)])
+def test_fuse_thresholds_and_no_long_flags(rm, am, tm):
+    B, H, T = 2048, 7, 8
+    ld, m, md, lg = gen.loop_fuse_inputs(B, 15, H, T, 2, 7)
+    for long_block in (lg, None):
+        want = oracle.fuse(ld, m, md, long_block, H, T, replace_min=rm, agree_min=am, tail_min=tm)
+        got = pkg.lookup_fuse(dev(ld), dev(m), dev(md), dev(long_block), H, T, replace_min=rm,
+                              agree_min=am, tail_min=tm)
+        for w, g in zip(want, got):
+            np.testing.assert_array_equal(host(g), w)
+
+
+# -------------------------------------------------------------- scheduling ----
+@pytest.mark.parametrize("B,steps", [(1, 64), (33, 40), (4096, 24)])
+@pytest.mark.parametrize("params", [dict(), dict(slack=0, enter_steps=1, sticky=0),
+                                    dict(slack=3, enter_steps=3, sticky=5, tail_min=6)])
+def test_schedule_trace_matches_oracle(B, steps, params):
+    H, T = 7, 8
+    mlen, committed = gen.loop_schedule_trace(B, steps, H, T, seed=B + steps)
+    st_o = np.zeros((B, 3), np.int32)
+    st_g = torch.zeros((B, 3), dtype=torch.int32, device="cuda")
+    entered = 0
+    for s in range(steps):
+        want = oracle.schedule(mlen[s], committed[s], st_o, H, T, **params)
+        got = pkg.lookup_schedule(dev(mlen[s]), dev(committed[s]), st_g, H, T, **params)
+        np.testing.assert_array_equal(host(got), want, err_msg=f"step {s}")
+        np.testing.assert_array_equal(host(st_g), st_o, err_msg=f"state after step {s}")
+        entered += int(want.sum())
+    if B > 1:
+        assert 0 < entered < B * steps          # the trace really switches modes
+
+
+# ------------------------------------------------------------ verification ----
+@pytest.mark.parametrize("B", [1, 5, 4096])
+@pytest.mark.parametrize("P", [0, 1, 15, 31, 32, 33, 70])
+def test_verify_greedy_matches_oracle(B, P):
+    block, ln, target, *_ = gen.loop_verify_inputs(B, P, seed=P + 11)
+    want = oracle.verify(block, ln, target)
+    got = pkg.lookup_verify(dev(block), dev(ln), dev(target))
+    for w, g in zip(want, got):
+        np.testing.assert_array_equal(host(g), w)
+
+
+@pytest.mark.parametrize("B", [3, 4096])
+@pytest.mark.parametrize("P", [1, 15, 40])
+@pytest.mark.parametrize("with_q,with_pm", [(True, True), (True, False), (False, False), (False, True)])
+def test_verify_sampled_matches_oracle(B, P, with_q, with_pm):
+    block, ln, target, p, q, pm, u = gen.loop_verify_inputs(B, P, seed=P + 23)
+    q = q if with_q else None
+    pm = pm if with_pm else None
+    want = oracle.verify(block, ln, target, probs=p, qprobs=q, point_mass=pm, u=u)
+    got = pkg.lookup_verify(dev(block), dev(ln), dev(target), probs=dev(p), qprobs=dev(q),
+                            point_mass=dev(pm), u=dev(u))
+    for w, g in zip(want, got):
+        np.testing.assert_array_equal(host(g), w)
+    acc = want[0]
+    assert 0 < (acc < ln).sum() < B or B < 10         # both full and partial acceptances occur
+
+
+def test_verify_ties_reject():
+    # u * q == p exactly is a rejection on both sides (strict comparison).
+    P = 4
+    block = np.array([[1, 2, 3, 4]], np.int32)
+    target = np.array([[1, 2, 3, 4, 5]], np.int32)
+    u = np.array([[0.25, 0.5, 0.75, 0.125]], np.float32)
+    q = np.array([[1.0, 0.5, 1.0, 1.0]], np.float32)
+    p = np.array([[0.5, 0.25, 0.9, 0.9]], np.float32)     # 0.5*0.5 == 0.25: reject at 1
+    got = pkg.lookup_verify(dev(block), dev(np.array([P], np.int32)), dev(target), probs=dev(p),
+                            qprobs=dev(q), u=dev(u))
+    want = oracle.verify(block, [P], target, probs=p, qprobs=q, u=u)
+    assert int(want[0][0]) == 1
+    for w, g in zip(want, got):
+        np.testing.assert_array_equal(host(g), w)
+
+
+def test_verify_invalid_length_gives_error_row():
+    block = np.arange(12, dtype=np.int32).reshape(3, 4)
+    target = np.arange(15, dtype=np.int32).reshape(3, 5)
+    ln = np.array([4, 5, -1], np.int32)                   # rows 1 and 2 are invalid
+    acc, commit, nc = pkg.lookup_verify(dev(block), dev(ln), dev(target))
+    acc, commit, nc = host(acc), host(commit), host(nc)
+    assert list(acc[1:]) == [-1, -1] and list(nc[1:]) == [0, 0]
+    assert (commit[1:] == -1).all()
+    want = oracle.verify(block[:1], ln[:1], target[:1])  # the valid row is untouched by the others
+    assert acc[0] == want[0][0] and list(commit[0]) == list(want[1][0])
+
+
+# ------------------------------------------------------------------ append ----
+def _append_case(tokens, offsets, W, seed, lead=0, unaligned=False):
+    B = offsets.shape[0] - 1
+    commit, ncommit = gen.loop_append_inputs(B, W, seed)
+    if lead:
+        tokens = np.concatenate([np.full(lead, -7, np.int32), tokens])
+        offsets = offsets + lead
+    want_t, want_o = oracle.append(tokens, offsets, commit, ncommit)
+    t, o = dev(tokens), dev(offsets)
+    cap = tokens.shape[0] + B * W + 8
+    buf = torch.full((cap,), -99, dtype=torch.int32, device="cuda")
+    out_t = buf[1:] if unaligned else buf[:-1]
+    out_o = torch.empty(B + 1, dtype=torch.int64, device="cuda")
+    pkg.lookup_append(t, o, dev(commit), dev(ncommit), out=(out_t, out_o))
+    got_o = host(out_o)
+    np.testing.assert_array_equal(got_o, want_o)
+    got_t = host(out_t)
+    np.testing.assert_array_equal(got_t[:want_t.shape[0]], want_t)
+    assert (got_t[want_t.shape[0]:] == -99).all()          # nothing written past the batch
+
+
+@pytest.mark.parametrize("lengths", [[0], [1], [5, 0, 0, 3], [0] * 100, [3000, 1, 0, 7777, 31]])
+@pytest.mark.parametrize("W", [0, 1, 16])
+@pytest.mark.parametrize("unaligned", [False, True])
+def test_append_small_and_ragged(lengths, W, unaligned):
+    rng = gen.rng_for(len(lengths) * 31 + W, 9)
+    tokens = rng.integers(0, 1000, size=sum(lengths)).astype(np.int32)
+    _append_case(tokens, gen.offsets_from_lengths(lengths), W, seed=W + 1, lead=5, unaligned=unaligned)
+
+
+@pytest.mark.parametrize("name", gen.WORKLOADS)
+def test_append_full_workloads(name):
+    w = gen.make_workload(name)
+    _append_case(w.tokens, w.offsets, 16, seed=3)
+
+
+def test_append_empty_batch():
+    t = torch.zeros(4, dtype=torch.int32, device="cuda")
+    o = torch.zeros(1, dtype=torch.int64, device="cuda")
+    out_t, out_o = pkg.lookup_append(t, o, torch.zeros((0, 16), dtype=torch.int32, device="cuda"),
+                                     torch.zeros(0, dtype=torch.int32, device="cuda"))
+    assert list(host(out_o)) == [0]
+
+
+# ------------------------------------------------------------- whole loop ----
+@pytest.mark.parametrize("name", ["tiny", "chats"])
+def test_decode_loop_matches_oracle(name):
+    """Draft -> fuse -> verify -> append -> schedule, several steps, both sides.
+
+    The target model is synthetic: at each step the target tokens agree with
+    the (already compared) proposal block on a random prefix, drawn on the host
+    from the step's seed.  Every intermediate is compared exactly."""
+    w = gen.make_workload(name)
+    B, H, T = w.B, 7, 8
+    K = H + T
+    P = H + T
+    tokens_o, offsets_o = w.tokens, w.offsets
+    tokens_g, offsets_g = dev(w.tokens), dev(w.offsets)
+    st_o = np.zeros((B, 3), np.int32)
+    st_g = torch.zeros((B, 3), dtype=torch.int32, device="cuda")
+    long_o = np.zeros(B, np.int32)
+    long_g = torch.zeros(B, dtype=torch.int32, device="cuda")
+    committed = np.full(B, H + 1, np.int32)
+    for step in range(4):
+        d_o, l_o, p_o, m_o = oracle.lookup_draft(tokens_o, offsets_o, w.min_m, w.max_m, K, threads=8)
+        d_g, l_g, p_g, m_g = pkg.lookup_draft_ex(tokens_g, offsets_g, w.min_m, w.max_m, K)
+        np.testing.assert_array_equal(host(d_g), d_o)
+        np.testing.assert_array_equal(host(m_g), m_o)
+        # scheduling from this step's match and the previous step's commit count
+        lg_o = oracle.schedule(m_o, committed, st_o, H, T)
+        pkg.lookup_schedule(m_g, dev(committed), st_g, H, T, out=long_g)
+        np.testing.assert_array_equal(host(long_g), lg_o)
+        # a synthetic draft model: the lookup head for a third of the requests
+        rng = gen.rng_for(step, 77)
+        md = rng.integers(0, 50, size=(B, H), dtype=np.int64).astype(np.int32)
+        pick = rng.random(B) < 0.33
+        md[pick] = d_o[pick, :H]
+        blk_o, len_o, pm_o = oracle.fuse(d_o, m_o, md, lg_o, H, T)
+        blk_g, len_g, pm_g = pkg.lookup_fuse(d_g, m_g, dev(md), long_g, H, T)
+        for a, b in ((blk_o, blk_g), (len_o, len_g), (pm_o, pm_g)):
+            np.testing.assert_array_equal(host(b), a)
+        # synthetic target: agree with the block on a random prefix
+        target = rng.integers(0, 50, size=(B, P + 1), dtype=np.int64).astype(np.int32)
+        f = rng.integers(0, P + 1, size=B)
+        for r in range(B):
+            target[r, :f[r]] = blk_o[r, :f[r]]
+        acc_o, com_o, nc_o = oracle.verify(blk_o, len_o, target)
+        acc_g, com_g, nc_g = pkg.lookup_verify(blk_g, len_g, dev(target))
+        for a, b in ((acc_o, acc_g), (com_o, com_g), (nc_o, nc_g)):
+            np.testing.assert_array_equal(host(b), a)
+        tokens_o, offsets_o = oracle.append(tokens_o, offsets_o, com_o, nc_o)
+        tokens_g, offsets_g = pkg.lookup_append(tokens_g, offsets_g, com_g, nc_g)
+        np.testing.assert_array_equal(host(offsets_g), offsets_o)
+        np.testing.assert_array_equal(host(tokens_g)[:offsets_o[-1]], tokens_o)
+        committed = nc_o

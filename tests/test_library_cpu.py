@@ -2,7 +2,7 @@
 
 The library is compiled for sm_103a with the CUDA runtime linked statically, so
 it loads on a machine without a GPU.  These tests check that it exports every
-function include/lookup_draft.h declares, and that argument validation rejects
+function include/*.h declares, and that argument validation rejects
 bad calls before any CUDA call is made (so they run here, on the CPU).
 """
 from __future__ import annotations
@@ -31,7 +31,7 @@ def declared_functions() -> set[str]:
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
         text = open(h, encoding="utf-8").read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(lookup_draft\w*)\s*\(", text, flags=re.M):
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(lookup_\w*)\s*\(", text, flags=re.M):
             names.add(m.group(1))
     return names
 
@@ -40,7 +40,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for must in ("lookup_draft", "lookup_draft_ex", "lookup_draft_scan", "lookup_draft_fill",
                  "lookup_draft_host", "lookup_draft_workspace_bytes", "lookup_draft_strerror",
-                 "lookup_draft_last_cuda_error", "lookup_draft_set_wait_limit_ns"):
+                 "lookup_draft_last_cuda_error", "lookup_draft_set_wait_limit_ns", "lookup_draft_noalloc",
+                 "lookup_fuse", "lookup_schedule", "lookup_verify", "lookup_append"):
         assert must in names
 
 
@@ -119,3 +120,31 @@ def test_host_entry_checks_host_offsets(lib):
 def test_package_fails_loudly_without_the_library(tmp_path):
     with pytest.raises(RuntimeError):
         pkg.load_library(str(tmp_path / "missing.so"))
+
+
+def test_loop_steps_reject_bad_parameters(lib):
+    F = FAKE
+    # fuse: K < H + T, H < 1, agree_n > H, H + T above the limit, a null output
+    assert lib.lookup_fuse(F, F, F, None, 4, 14, 7, 8, 8, 6, 2, 4, F, F, F, None) == -1
+    assert lib.lookup_fuse(F, F, F, None, 4, 15, 0, 8, 8, 6, 0, 4, F, F, F, None) == -1
+    assert lib.lookup_fuse(F, F, F, None, 4, 15, 7, 8, 8, 6, 8, 4, F, F, F, None) == -1
+    assert lib.lookup_fuse(F, F, F, None, 4, 1 << 20, 1 << 16, 8, 8, 6, 2, 4, F, F, F, None) == -1
+    assert lib.lookup_fuse(F, F, F, None, 4, 15, 7, 8, 8, 6, 2, 4, F, None, F, None) == -1
+    # schedule: enter_steps < 1, sticky < 0, null state
+    assert lib.lookup_schedule(F, F, 4, 7, 8, 4, 1, 0, 3, F, F, None) == -1
+    assert lib.lookup_schedule(F, F, 4, 7, 8, 4, 1, 2, -1, F, F, None) == -1
+    assert lib.lookup_schedule(F, F, 4, 7, 8, 4, 1, 2, 3, None, F, None) == -1
+    # verify: negative P, P above the limit, probs without u
+    assert lib.lookup_verify(F, F, F, None, None, None, None, 4, -1, F, F, F, None) == -1
+    assert lib.lookup_verify(F, F, F, None, None, None, None, 4, 1 << 17, F, F, F, None) == -1
+    assert lib.lookup_verify(F, F, F, F, None, None, None, 4, 15, F, F, F, None) == -1
+    # append: negative W, null offsets
+    assert lib.lookup_append(F, F, F, F, 4, -1, F, F, None) == -1
+    assert lib.lookup_append(F, None, F, F, 4, 16, F, F, None) == -1
+
+
+def test_loop_steps_empty_batch(lib):
+    # B == 0: fuse, schedule and verify enqueue nothing and need no pointer.
+    assert lib.lookup_fuse(None, None, None, None, 0, 15, 7, 8, 8, 6, 2, 4, None, None, None, None) == 0
+    assert lib.lookup_schedule(None, None, 0, 7, 8, 4, 1, 2, 3, None, None, None) == 0
+    assert lib.lookup_verify(None, None, None, None, None, None, None, 0, 15, None, None, None, None) == 0
