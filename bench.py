@@ -23,6 +23,10 @@ requests of 25,000 tokens, 6.4 MB of int32 history).  Prints one JSON line.
                 to the host, every step.
   cpu_baseline  the CPU oracle (brute force, one thread per slice of requests) on
                 this machine's host cores, on the same batch.
+  loop_steps    microseconds per call of the decode-loop steps around the draft
+                (fusion, scheduling, greedy and sampled verification, append of
+                the committed tokens), the append's GB/s, and one whole
+                draft-to-append loop step, on the same batch.
 
 --impl reference times that oracle as the comparison arm on the same workload.
 Multi-GPU (torchrun, one rank per GPU): every rank drafts its own batch (weak
@@ -71,6 +75,10 @@ def parse_args(argv=None):
     ap.add_argument("--settle-s", type=float, default=0.5,
                     help="untimed graph replays before the timed region, so clocks settle")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-loop", action="store_true",
+                    help="skip the timing of the decode-loop steps (fusion, scheduling, verification, append)")
+    ap.add_argument("--loop-only", action="store_true",
+                    help="time only the decode-loop steps (replays = steps / copies of the batch)")
     return ap.parse_args(argv)
 
 
@@ -232,6 +240,19 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     wsp = ws.data_ptr()
 
+    if args.loop_only:
+        loop = measure_loop(lib, pkg, w, dev, stream, toks, offs, max(1, args.steps // ncopy))
+        if rank == 0:
+            print(json.dumps({"metric": "µs per decode-loop step (draft, schedule, fuse, verify, append)",
+                              "value": loop["loop_step_us"], "unit": "us/step", "n_gpus": world,
+                              "higher_is_better": False, "data": "synthetic",
+                              "config": {"workload": args.workload, "B": B, "history_tokens": w.total_tokens,
+                                         "seed": seed},
+                              "loop_steps": loop}), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
     def step(i: int, handle: int):
         j = i % ncopy
         rc = lib.lookup_draft(tok_p[j], off_p[j], B, min_m, max_m, K, dp, lp, pp, handle)
@@ -343,6 +364,10 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
             iso_ms += [ea[j].elapsed_time(eb[j]) for j in range(ncopy)]
     scan_iso_us = 1000.0 * max_over_ranks(statistics.fmean(iso_ms), dist, dev)
 
+    loop = None
+    if not args.no_loop:
+        loop = measure_loop(lib, pkg, w, dev, stream, toks, offs, reps)
+
     # e2e: host buffers through lookup_draft_host, copies inside every step
     h_tok = tok_host.pin_memory()
     h_off = off_host.pin_memory()
@@ -431,12 +456,153 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
             "steps": n_e2e,
         },
         "cpu_baseline": cpu,
+        "loop_steps": loop,
         "gpu_launches": 2 * args.steps,
         "parity_with_oracle": bool(parity),
         "clocks": clocks.summary(),
         "gpu": torch.cuda.get_device_name(dev),
     }
     print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------- decode loop ----
+LOOP_H, LOOP_T = 7, 8            # head and tail of the verify block (HyperQwen article, "第2步")
+
+
+def measure_loop(lib, pkg, w, dev, stream, toks, offs, reps: int) -> dict:
+    """Times of the decode-loop steps around the draft on the bench's batch.
+
+    Each entry point is captured ncopy times back to back in one CUDA graph
+    (inputs rotating over the device copies of the batch, so the append reads
+    every history from HBM) and replayed; CUDA events on the launching stream
+    give the mean time per call.  ``loop_step_us`` is one whole decode-loop
+    step: draft with mlen (K = H + T), scheduling, fusion, greedy verification
+    and the append of the committed tokens to every history."""
+    import numpy as np
+    import torch
+
+    import gen
+
+    H, T = LOOP_H, LOOP_T
+    P = H + T
+    K = H + T
+    B, ncopy = w.B, len(toks)
+    i32 = torch.int32
+    tok_p = [t.data_ptr() for t in toks]
+    off_p = [o.data_ptr() for o in offs]
+
+    def check(rc):
+        if rc != 0:
+            raise pkg.LookupDraftError(rc, lib)
+
+    # inputs: this batch's lookup drafts and match lengths, a synthetic draft model
+    # that proposes the lookup head for a third of the requests, a synthetic target
+    # that agrees with the block on a random prefix
+    draft, length, pos, mlen = pkg.lookup_draft_ex(toks[0], offs[0], w.min_m, w.max_m, K, stream=stream)
+    torch.cuda.synchronize(dev)
+    rng = gen.rng_for(w.seed, 500)
+    md_h = rng.integers(0, 50, size=(B, H), dtype=np.int64).astype(np.int32)
+    pick = rng.random(B) < 0.33
+    md_h[pick] = draft.cpu().numpy()[pick, :H]
+    model_draft = torch.from_numpy(md_h).to(dev)
+    state = torch.zeros((B, 3), dtype=i32, device=dev)
+    long_block = torch.zeros(B, dtype=i32, device=dev)
+    committed = torch.full((B,), H + T + 1, dtype=i32, device=dev)
+    block = torch.empty((B, P), dtype=i32, device=dev)
+    blen = torch.empty(B, dtype=i32, device=dev)
+    pm = torch.empty((B, P), dtype=i32, device=dev)
+    with torch.cuda.stream(stream):
+        pkg.lookup_fuse(draft, mlen, model_draft, None, H, T, out=(block, blen, pm), stream=stream)
+    torch.cuda.synchronize(dev)
+    blk_h = block.cpu().numpy()
+    tg_h = rng.integers(0, 50, size=(B, P + 1), dtype=np.int64).astype(np.int32)
+    f = rng.integers(0, P + 1, size=B)
+    for r in range(B):
+        tg_h[r, :f[r]] = blk_h[r, :f[r]]
+    target = torch.from_numpy(tg_h).to(dev)
+    _, _, _, p_h, q_h, pm_h, u_h = gen.loop_verify_inputs(B, P, w.seed)
+    probs, qprobs, u = (torch.from_numpy(a).to(dev) for a in (p_h, q_h, u_h))
+    accepted = torch.empty(B, dtype=i32, device=dev)
+    commit = torch.empty((B, P + 1), dtype=i32, device=dev)
+    ncommit = torch.empty(B, dtype=i32, device=dev)
+    cap = max(int(t.numel()) for t in toks) + B * (P + 1)
+    out_t = [torch.empty(cap, dtype=i32, device=dev) for _ in range(ncopy)]
+    out_o = [torch.empty(B + 1, dtype=torch.int64, device=dev) for _ in range(ncopy)]
+    dp, lp, pp, mp = draft.data_ptr(), length.data_ptr(), pos.data_ptr(), mlen.data_ptr()
+
+    def fuse(j, hs):
+        check(lib.lookup_fuse(dp, mp, model_draft.data_ptr(), long_block.data_ptr(), B, K, H, T, 8, 6, 2, 4,
+                              block.data_ptr(), blen.data_ptr(), pm.data_ptr(), hs))
+
+    def schedule(j, hs):
+        check(lib.lookup_schedule(mp, committed.data_ptr(), B, H, T, 4, 1, 2, 3, state.data_ptr(),
+                                  long_block.data_ptr(), hs))
+
+    def verify_greedy(j, hs):
+        check(lib.lookup_verify(block.data_ptr(), blen.data_ptr(), target.data_ptr(), None, None, None, None,
+                                B, P, accepted.data_ptr(), commit.data_ptr(), ncommit.data_ptr(), hs))
+
+    def verify_sampled(j, hs):
+        check(lib.lookup_verify(block.data_ptr(), blen.data_ptr(), target.data_ptr(), probs.data_ptr(),
+                                qprobs.data_ptr(), pm.data_ptr(), u.data_ptr(), B, P, accepted.data_ptr(),
+                                commit.data_ptr(), ncommit.data_ptr(), hs))
+
+    def append(j, hs):
+        check(lib.lookup_append(tok_p[j], off_p[j], commit.data_ptr(), ncommit.data_ptr(), B, P + 1,
+                                out_t[j].data_ptr(), out_o[j].data_ptr(), hs))
+
+    def draft_ex(j, hs):
+        check(lib.lookup_draft_ex(tok_p[j], off_p[j], B, w.min_m, w.max_m, K, dp, lp, pp, mp, hs))
+
+    def loop_step(j, hs):
+        draft_ex(j, hs)
+        schedule(j, hs)
+        fuse(j, hs)
+        verify_greedy(j, hs)
+        append(j, hs)
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn) -> float:
+        with torch.cuda.stream(stream):
+            for j in range(ncopy):                      # eager warm-up
+                fn(j, int(stream.cuda_stream))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            hc = int(torch.cuda.current_stream().cuda_stream)
+            for j in range(ncopy):
+                fn(j, hc)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            ev0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        return 1000.0 * ev0.elapsed_time(ev1) / (reps * ncopy)
+
+    verify_sampled(0, int(stream.cuda_stream))            # a valid commit/ncommit before the append
+    res = {
+        "H": H, "T": T,
+        "fuse_us": timed(fuse),
+        "schedule_us": timed(schedule),
+        "verify_greedy_us": timed(verify_greedy),
+        "verify_sampled_us": timed(verify_sampled),
+        "append_us": timed(append),
+        "loop_step_us": timed(loop_step),
+    }
+    # the append's algorithmic bytes: every history token read and written once,
+    # the committed tokens read and written, the counts and both offset arrays
+    committed_tokens = int(ncommit.sum().item())
+    append_bytes = 8 * w.total_tokens + 8 * committed_tokens + 4 * B + 16 * (B + 1)
+    res = {k: (round(v, 3) if isinstance(v, float) else v) for k, v in res.items()}
+    res["append_algorithmic_bytes"] = append_bytes
+    res["append_gbs"] = round(append_bytes / (res["append_us"] * 1e-6) / 1e9, 1)
+    res["loop_step_launches"] = 2 + 1 + 1 + 1 + 2
+    res["method"] = (f"each call captured {ncopy}x back to back in a CUDA graph over rotating input copies, "
+                     f"{reps} replays, CUDA events on the launching stream")
+    return res
 
 
 # ------------------------------------------------------------------ CPU ----

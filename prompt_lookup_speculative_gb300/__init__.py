@@ -390,8 +390,11 @@ def lookup_append(tokens, offsets, commit, ncommit, out=None, stream=None):
     if out_t.dtype != torch.int32 or not out_t.is_contiguous() or out_t.device != dev:
         raise ValueError("out tokens must be a contiguous int32 tensor on the inputs' device")
     op = _dev(out_o, torch.int64, (B + 1,), dev, "out_offsets")
+    # an empty tensor has no address; with no history token and nothing to write the
+    # kernel dereferences neither pointer, so any valid aligned address will do
+    tp = tokens.data_ptr() if tokens.numel() else offsets.data_ptr()
+    otp = out_t.data_ptr() if out_t.numel() else out_o.data_ptr()
     with torch.cuda.device(dev):
-        rc = lib.lookup_append(tokens.data_ptr(), offsets.data_ptr(), cp, np_, B, W, out_t.data_ptr(), op,
-                               _stream_handle(stream))
+        rc = lib.lookup_append(tp, offsets.data_ptr(), cp, np_, B, W, otp, op, _stream_handle(stream))
     _check(rc, lib)
     return out_t, out_o

@@ -33,9 +33,12 @@ namespace {
 
 constexpr int kMaxBlock = 1 << 16;        // H + T (a verify block) at most
 constexpr int kScanThreads = 1024;       // offsets_kernel
-constexpr int kCopyThreads = 512;        // append_kernel
-constexpr int kCopyCtasPerSm = 4;
-constexpr int kCopyUnroll = 2;
+constexpr int kCopyThreads = 256;        // append_kernel
+constexpr int kCopyCtasPerSm = 3;
+constexpr int kCopyUnroll = 2;           // windows in flight per warp
+constexpr int kSub = 4;                  // 128-token sub-windows per window (one int4 per lane each)
+constexpr int kWin = 128 * kSub;         // tokens per window
+constexpr int kCommitRegs = 1;           // committed tokens per lane held in registers
 
 __device__ inline void allow_dependent_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -197,108 +200,241 @@ struct AppendParams {
     int32_t B, W;
 };
 
+__device__ inline int64_t clamped_count(const AppendParams &p, int64_t r) {
+    return min(max(p.ncommit[r], 0), p.W);
+}
+
 // The new boundaries: out_offsets[r] = (offsets[r] - offsets[0]) + sum(ncommit[0..r)),
-// one CTA scanning the counts in blocks of kScanThreads.
+// one CTA: each thread sums a contiguous run of counts, a block-wide exclusive
+// scan of the run sums, then each thread writes its run's boundaries.
 __global__ void __launch_bounds__(kScanThreads) offsets_kernel(AppendParams p) {
     __shared__ int64_t warp_sums[kScanThreads / 32];
-    __shared__ int64_t carry_s;
     wait_for_prerequisite_grid();
     allow_dependent_launch();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t base = p.offsets[0];
-    if (tid == 0) carry_s = 0;
+    const int64_t per = (int64_t(p.B) + kScanThreads - 1) / kScanThreads;
+    const int64_t r0 = min(int64_t(tid) * per, int64_t(p.B)), r1 = min(r0 + per, int64_t(p.B));
+    int64_t own = 0;
+    for (int64_t r = r0; r < r1; ++r) own += clamped_count(p, r);
+    int64_t incl = own;                                  // inclusive scan within the warp
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += y;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
     __syncthreads();
-    for (int64_t r0 = 0; r0 < p.B; r0 += kScanThreads) {
-        const int64_t r = r0 + tid;
-        int64_t x = r < p.B ? int64_t(min(max(p.ncommit[r], 0), p.W)) : 0;   // clamped to [0, W]
-        int64_t incl = x;                                // inclusive scan within the warp
+    if (warp == 0) {
+        int64_t s = warp_sums[lane];
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
-            const int64_t y = __shfl_up_sync(0xffffffffu, incl, d);
-            if (lane >= d) incl += y;
+            const int64_t y = __shfl_up_sync(0xffffffffu, s, d);
+            if (lane >= d) s += y;
         }
-        if (lane == 31) warp_sums[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {
-            int64_t s = warp_sums[lane];
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const int64_t y = __shfl_up_sync(0xffffffffu, s, d);
-                if (lane >= d) s += y;
-            }
-            warp_sums[lane] = s;                         // inclusive over warps
-        }
-        __syncthreads();
-        const int64_t carry = carry_s;
-        const int64_t before = carry + (warp ? warp_sums[warp - 1] : 0) + incl - x;   // exclusive
-        if (r < p.B) p.out_offsets[r] = (p.offsets[r] - base) + before;
-        __syncthreads();
-        if (tid == kScanThreads - 1) carry_s = carry + warp_sums[kScanThreads / 32 - 1];
-        __syncthreads();
+        warp_sums[lane] = s;                             // inclusive over warps
     }
-    if (tid == 0) p.out_offsets[p.B] = (p.offsets[p.B] - base) + carry_s;
+    __syncthreads();
+    const int64_t base = p.offsets[0];
+    int64_t before = (warp ? warp_sums[warp - 1] : 0) + incl - own;
+    for (int64_t r = r0; r < r1; ++r) {
+        p.out_offsets[r] = (p.offsets[r] - base) + before;
+        before += clamped_count(p, r);
+    }
+    if (tid == kScanThreads - 1) p.out_offsets[p.B] = (p.offsets[p.B] - base) + warp_sums[kScanThreads / 32 - 1];
 }
 
-// Copy: CTA c writes the output quads [c*Sq, (c+1)*Sq) (4 tokens each).  Thread
-// t takes quads t, t + kCopyThreads, ... of its CTA's range, kCopyUnroll of them
-// per pass, so a warp reads and writes 512 contiguous bytes per quad step; the
-// request of each token comes from a monotone walk over the new boundaries.
-// Sources are read token by token (a history's shift into the new batch is the
-// running sum of earlier commits, so it has no fixed alignment); with kVec the
-// quad is written with one 16-byte store (out_tokens 16-byte aligned).
-template <bool kVec>
-__global__ void __launch_bounds__(kCopyThreads, kCopyCtasPerSm) append_kernel(AppendParams p) {
-    wait_for_prerequisite_grid();                        // out_offsets are ready
-    allow_dependent_launch();
-    const int64_t total = p.out_offsets[p.B];
-    const int64_t nquad = (total + 3) >> 2;
-    const int64_t Sq = (nquad + gridDim.x - 1) / gridDim.x;
-    const int64_t x0 = int64_t(blockIdx.x) * Sq * 4;
-    const int64_t x1 = (x0 + Sq * 4 < total) ? x0 + Sq * 4 : total;
-    if (x0 >= x1) return;
-    // the request holding x0: the largest r with out_offsets[r] <= x0
-    int lo = 0, hi = p.B;
-    while (hi - lo > 1) {
-        const int mid = lo + ((hi - lo) >> 1);
-        if (p.out_offsets[mid] <= x0) lo = mid; else hi = mid;
+// The output quad at an aligned position: out[j] is run position 4l + 4 - a + j
+// of the sub-window, i.e. cur[4 - a + j] for j < a, else nxt[j - a] (cur = this
+// lane's input quad, nxt = the next one in the run).
+__device__ inline int4 realign(int4 cur, int4 nxt, int a) {
+    switch (a) {
+    case 1: return make_int4(cur.w, nxt.x, nxt.y, nxt.z);
+    case 2: return make_int4(cur.z, cur.w, nxt.x, nxt.y);
+    default: return make_int4(cur.y, cur.z, cur.w, nxt.x);
     }
-    int r = lo;
-    int64_t nstart = p.out_offsets[r], nend = p.out_offsets[r + 1];
-    int64_t hist = p.offsets[r + 1] - p.offsets[r];
-    const int32_t *src = p.tokens + p.offsets[r];
-    const int32_t *crow = p.commit + int64_t(r) * p.W;
-    for (int64_t xb = x0 + 4 * threadIdx.x; xb < x1; xb += int64_t(4) * kCopyThreads * kCopyUnroll) {
-        int32_t v[kCopyUnroll][4];
+}
+
+__device__ inline int comp(int4 q, int k) { return k == 0 ? q.x : k == 1 ? q.y : k == 2 ? q.z : q.w; }
+
+__device__ inline int4 shfl_quad(int4 v, int src) {
+    return make_int4(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src),
+                     __shfl_sync(0xffffffffu, v.z, src), __shfl_sync(0xffffffffu, v.w, src));
+}
+
+__device__ inline int4 shfl_quad_down(int4 v) {
+    return make_int4(__shfl_down_sync(0xffffffffu, v.x, 1), __shfl_down_sync(0xffffffffu, v.y, 1),
+                     __shfl_down_sync(0xffffffffu, v.z, 1), __shfl_down_sync(0xffffffffu, v.w, 1));
+}
+
+// The copy.  The histories tokens[offsets[0] .. offsets[B]) are contiguous in
+// the input, and each request's run moves as a block to out_offsets[r].  The
+// input is cut into windows of kWin tokens aligned to 16 bytes; a window is
+// kSub sub-windows of 128 tokens, one int4 per lane each, and each warp takes
+// a contiguous range of windows, kCopyUnroll windows in flight.  A window inside
+// one request and inside the batch is one contiguous output run: when the run
+// is not 16-byte aligned, lanes pass their quads along the run (shuffles) and
+// store aligned int4s, with the two partial quads at the run's ends stored
+// token by token.  A window that holds a request boundary or an end of the
+// batch is written token by token, one request at a time.
+//
+// Request boundaries come from a per-warp cache: lane i holds the end and the
+// shift of request r_first + i, so walking to the next request is a shuffle
+// (past 32 requests it falls back to loads).  Everything that reads only the
+// inputs -- the window range, the first windows' loads, the request of the
+// warp's first window (a 32-way search over offsets), the cache's ends and the
+// warp's committed tokens -- is done before waiting for offsets_kernel; after
+// it, one load per lane completes the cache.  The committed tokens of request
+// r are written by warp r (grid-stride).
+__global__ void __launch_bounds__(kCopyThreads, kCopyCtasPerSm) append_kernel(AppendParams p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gwarp = (int64_t(blockIdx.x) * kCopyThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = int64_t(gridDim.x) * (kCopyThreads / 32);
+    const int B = p.B;
+    const int64_t A0 = p.offsets[0], A1 = p.offsets[B];
+    // e_base: the first window start, at or before A0, with tokens + e_base 16-byte aligned
+    const int64_t mis_in = int64_t((reinterpret_cast<uintptr_t>(p.tokens) >> 2) & 3);
+    const int64_t e_base = A0 - ((mis_in + A0) & 3);
+    const int64_t nwin = A1 > A0 ? (A1 - e_base + kWin - 1) / kWin : 0;
+    const int64_t per = nwin < (int64_t(1) << 32)      // windows per warp, rounded up
+                            ? int64_t((uint32_t(nwin) + uint32_t(nwarps) - 1) / uint32_t(nwarps))
+                            : (nwin + nwarps - 1) / nwarps;
+    const int64_t k0 = min(gwarp * per, nwin), k1 = min(k0 + per, nwin);
+    const int64_t mis_out = int64_t((reinterpret_cast<uintptr_t>(p.out_tokens) >> 2) & 3);
+
+    int4 q[kCopyUnroll][kSub];
+    auto load = [&](int64_t k, int u) {
 #pragma unroll
-        for (int u = 0; u < kCopyUnroll; ++u) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int64_t x = xb + int64_t(4) * kCopyThreads * u + k;
-                v[u][k] = 0;
-                if (x < x1) {
-                    while (x >= nend) {                  // into the next request
-                        ++r;
-                        nstart = nend;
-                        nend = p.out_offsets[r + 1];
-                        hist = p.offsets[r + 1] - p.offsets[r];
-                        src = p.tokens + p.offsets[r];
-                        crow = p.commit + int64_t(r) * p.W;
-                    }
-                    const int64_t i = x - nstart;        // position in the new history
-                    v[u][k] = i < hist ? __ldg(src + i) : __ldg(crow + (i - hist));
-                }
+        for (int s = 0; s < kSub; ++s) {
+            const int64_t e = e_base + k * kWin + 128 * s + 4 * lane;   // this lane's quad
+            if (e >= A0 && e + 4 <= A1) {
+                q[u][s] = __ldg(reinterpret_cast<const int4 *>(p.tokens + e));
+            } else {
+                q[u][s] = make_int4(e >= A0 && e < A1 ? p.tokens[e] : 0,
+                                    e + 1 >= A0 && e + 1 < A1 ? p.tokens[e + 1] : 0,
+                                    e + 2 >= A0 && e + 2 < A1 ? p.tokens[e + 2] : 0,
+                                    e + 3 >= A0 && e + 3 < A1 ? p.tokens[e + 3] : 0);
             }
         }
+    };
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u)                // first windows in flight before anything else
+        if (k0 + u < k1) load(k0 + u, u);
+
+    // this warp's committed tokens (request gwarp), into registers
+    const int64_t rc0 = gwarp;
+    int64_t nc0 = 0;
+    int32_t cv[kCommitRegs];
+    if (rc0 < B) {
+        nc0 = clamped_count(p, rc0);
+#pragma unroll
+        for (int c = 0; c < kCommitRegs; ++c)
+            cv[c] = lane + 32 * c < nc0 ? __ldg(p.commit + rc0 * p.W + lane + 32 * c) : 0;
+    }
+
+    // request holding the first valid token of window k0: largest r with offsets[r] <= e
+    int r_first = 0;
+    if (k0 < k1) {
+        const int64_t e = max(e_base + k0 * kWin, A0);
+        int lo = 0, hi = B;                              // offsets[lo] <= e < offsets[hi]
+        while (hi - lo > 1) {
+            const int step = (hi - lo + 31) / 32;
+            const int idx = min(lo + lane * step, hi - 1);
+            const unsigned le = __ballot_sync(0xffffffffu, p.offsets[idx] <= e);
+            const int last = 31 - __clz(le);             // lane 0 always qualifies (idx = lo)
+            const int nlo = min(lo + last * step, hi - 1);
+            hi = min(nlo + step, hi);
+            lo = nlo;
+        }
+        r_first = lo;
+    }
+    // the cache: lane i holds request r_first + i (its end, then its shift)
+    const int rc = r_first + lane;
+    const int64_t c_start = (k0 < k1 && rc < B) ? p.offsets[rc] : 0;
+    const int64_t c_end = (k0 < k1 && rc < B) ? p.offsets[rc + 1] : 0;
+
+    wait_for_prerequisite_grid();                        // out_offsets are ready
+    allow_dependent_launch();
+
+    int64_t c_shift = (k0 < k1 && rc < B) ? p.out_offsets[rc] - c_start : 0;
+    if (rc0 < B) {                                       // committed tokens after the history
+        const int64_t dst = p.out_offsets[rc0 + 1] - nc0;
+#pragma unroll
+        for (int c = 0; c < kCommitRegs; ++c)
+            if (lane + 32 * c < nc0) p.out_tokens[dst + lane + 32 * c] = cv[c];
+        for (int64_t j = lane + 32 * kCommitRegs; j < nc0; j += 32) p.out_tokens[dst + j] = __ldg(p.commit + rc0 * p.W + j);
+    }
+    for (int64_t rr = rc0 + nwarps; rr < B; rr += nwarps) {
+        const int64_t n = clamped_count(p, rr);
+        const int64_t dst = p.out_offsets[rr + 1] - n;
+        for (int64_t j = lane; j < n; j += 32) p.out_tokens[dst + j] = __ldg(p.commit + rr * p.W + j);
+    }
+    if (k0 >= k1) return;
+
+    // the current request r: tokens [.., r_end) move by shift (uniform across the warp)
+    int r = r_first;
+    int64_t r_end = __shfl_sync(0xffffffffu, c_end, 0);
+    int64_t shift = __shfl_sync(0xffffffffu, c_shift, 0);
+    auto next_request = [&]() {
+        ++r;
+        const int i = r - r_first;
+        if (i < 32) {
+            r_end = __shfl_sync(0xffffffffu, c_end, i);
+            shift = __shfl_sync(0xffffffffu, c_shift, i);
+        } else {
+            r_end = p.offsets[r + 1];
+            shift = p.out_offsets[r] - p.offsets[r];
+        }
+    };
+
+    for (int64_t kb = k0; kb < k1; kb += kCopyUnroll) {
 #pragma unroll
         for (int u = 0; u < kCopyUnroll; ++u) {
-            const int64_t x = xb + int64_t(4) * kCopyThreads * u;
-            if (kVec && x + 4 <= x1) {
-                *reinterpret_cast<int4 *>(p.out_tokens + x) = make_int4(v[u][0], v[u][1], v[u][2], v[u][3]);
-            } else {
+            const int64_t k = kb + u;
+            if (k >= k1) break;
+            const int64_t w0 = e_base + k * kWin;
+            const int64_t v0 = max(w0, A0), v1 = min(w0 + kWin, A1);
+            while (r_end <= v0) next_request();          // the request of the window's first token
+            if (w0 >= A0 && w0 + kWin <= A1 && r_end >= v1) {
+                // one request, whole window: output run [w0 + shift, w0 + shift + kWin)
+                int32_t *run = p.out_tokens + (w0 + shift);
+                const int a = int((mis_out + w0 + shift) & 3);
+                if (a == 0) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    if (x + k < x1) p.out_tokens[x + k] = v[u][k];
+                    for (int s = 0; s < kSub; ++s)
+                        *reinterpret_cast<int4 *>(run + 128 * s + 4 * lane) = q[u][s];
+                } else {
+#pragma unroll
+                    for (int s = 0; s < kSub; ++s) {
+                        const int4 down = shfl_quad_down(q[u][s]);
+                        const int4 wrap = shfl_quad(q[u][s + 1 < kSub ? s + 1 : s], 0);
+                        const int4 nxt = lane < 31 ? down : wrap;
+                        if (lane < 31 || s + 1 < kSub)
+                            *reinterpret_cast<int4 *>(run - a + 128 * s + 4 * (lane + 1)) = realign(q[u][s], nxt, a);
+                    }
+                    if (lane == 0)
+                        for (int j = 0; j < 4 - a; ++j) run[j] = comp(q[u][0], j);
+                    if (lane == 31)
+                        for (int j = 4 - a; j < 4; ++j) run[kWin - 4 + j] = comp(q[u][kSub - 1], j);
+                }
+            } else {
+                // token by token, one request at a time: [seg0, seg1) moves by shift
+                int64_t seg0 = v0;
+                while (true) {
+                    const int64_t seg1 = min(r_end, v1);
+#pragma unroll
+                    for (int s = 0; s < kSub; ++s) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int64_t e = w0 + 128 * s + 4 * lane + j;
+                            if (e >= seg0 && e < seg1) p.out_tokens[e + shift] = comp(q[u][s], j);
+                        }
+                    }
+                    if (r_end >= v1) break;
+                    seg0 = r_end;
+                    next_request();
+                }
             }
+            if (k + kCopyUnroll < k1) load(k + kCopyUnroll, u);   // the next pass's window
         }
     }
 }
@@ -375,9 +511,8 @@ int lookup_append(const int32_t *tokens, const int64_t *offsets, const int32_t *
     if (e != cudaSuccess) return cuda_fail(e, "device query");
     int rc = launch_pdl(offsets_kernel, dim3(1), dim3(kScanThreads), stream, p);
     if (rc != LOOKUP_DRAFT_OK || B == 0) return rc;      // B == 0: out_offsets = {0} only
-    const bool vec = (reinterpret_cast<uintptr_t>(out_tokens) & 15) == 0;
-    return launch_pdl(vec ? append_kernel<true> : append_kernel<false>, dim3(unsigned(sms * kCopyCtasPerSm)),
-                      dim3(kCopyThreads), stream, p);
+    if ((reinterpret_cast<uintptr_t>(tokens) | reinterpret_cast<uintptr_t>(out_tokens)) & 3) return LOOKUP_DRAFT_EINVAL;
+    return launch_pdl(append_kernel, dim3(unsigned(sms * kCopyCtasPerSm)), dim3(kCopyThreads), stream, p);
 }
 
 }  // extern "C"

@@ -150,13 +150,39 @@ def _append_case(tokens, offsets, W, seed, lead=0, unaligned=False):
     assert (got_t[want_t.shape[0]:] == -99).all()          # nothing written past the batch
 
 
-@pytest.mark.parametrize("lengths", [[0], [1], [5, 0, 0, 3], [0] * 100, [3000, 1, 0, 7777, 31]])
+@pytest.mark.parametrize("lengths", [[0], [1], [5, 0, 0, 3], [0] * 100, [3000, 1, 0, 7777, 31],
+                                     [127, 128, 129, 0, 256, 1, 1000], [511, 512, 513, 0, 1024, 2047, 1]])
 @pytest.mark.parametrize("W", [0, 1, 16])
-@pytest.mark.parametrize("unaligned", [False, True])
-def test_append_small_and_ragged(lengths, W, unaligned):
+@pytest.mark.parametrize("lead,unaligned", [(5, False), (5, True), (0, True), (1, False), (2, True), (3, False)])
+def test_append_small_and_ragged(lengths, W, lead, unaligned):
     rng = gen.rng_for(len(lengths) * 31 + W, 9)
     tokens = rng.integers(0, 1000, size=sum(lengths)).astype(np.int32)
-    _append_case(tokens, gen.offsets_from_lengths(lengths), W, seed=W + 1, lead=5, unaligned=unaligned)
+    _append_case(tokens, gen.offsets_from_lengths(lengths), W, seed=W + 1, lead=lead, unaligned=unaligned)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_append_random_batches(seed):
+    rng = gen.rng_for(seed, 19)
+    B = int(rng.integers(1, 3000))
+    lengths = np.where(rng.random(B) < 0.2, 0, rng.integers(1, 2000, size=B))
+    tokens = rng.integers(0, 1 << 30, size=int(lengths.sum())).astype(np.int32)
+    _append_case(tokens, gen.offsets_from_lengths(lengths), int(rng.integers(1, 40)), seed=seed,
+                 lead=int(rng.integers(0, 8)), unaligned=bool(seed % 2))
+
+
+def test_append_clamps_counts():
+    # counts outside [0, W] are clamped (the header's rule); the oracle takes the clamped counts
+    rng = gen.rng_for(5, 21)
+    lengths = [300, 0, 17, 129]
+    tokens = rng.integers(0, 1000, size=sum(lengths)).astype(np.int32)
+    offsets = gen.offsets_from_lengths(lengths)
+    W = 4
+    commit = rng.integers(0, 1000, size=(4, W)).astype(np.int32)
+    ncommit = np.array([-3, 9, 4, 0], np.int32)
+    want_t, want_o = oracle.append(tokens, offsets, commit, np.clip(ncommit, 0, W))
+    out_t, out_o = pkg.lookup_append(dev(tokens), dev(offsets), dev(commit), dev(ncommit))
+    np.testing.assert_array_equal(host(out_o), want_o)
+    np.testing.assert_array_equal(host(out_t)[:want_t.shape[0]], want_t)
 
 
 @pytest.mark.parametrize("name", gen.WORKLOADS)
