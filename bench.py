@@ -27,6 +27,9 @@ requests of 25,000 tokens, 6.4 MB of int32 history).  Prints one JSON line.
                 (fusion, scheduling, greedy and sampled verification, append of
                 the committed tokens), the append's GB/s, and one whole
                 draft-to-append loop step, on the same batch.
+  index         the incremental n-gram index on the same batch: build time and
+                size, the draft from the index (checked against the oracle), the
+                in-place append, and the decode-loop step on the index.
 
 --impl reference times that oracle as the comparison arm on the same workload.
 Multi-GPU (torchrun, one rank per GPU): every rank drafts its own batch (weak
@@ -77,6 +80,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-loop", action="store_true",
                     help="skip the timing of the decode-loop steps (fusion, scheduling, verification, append)")
+    ap.add_argument("--no-index", action="store_true",
+                    help="skip the timing of the incremental n-gram index")
     ap.add_argument("--loop-only", action="store_true",
                     help="time only the decode-loop steps (replays = steps / copies of the batch)")
     return ap.parse_args(argv)
@@ -242,13 +247,18 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
 
     if args.loop_only:
         loop = measure_loop(lib, pkg, w, dev, stream, toks, offs, max(1, args.steps // ncopy))
+        index = None
+        if not args.no_index:
+            import oracle
+            want = oracle.lookup_draft(w.tokens, w.offsets, min_m, max_m, K, threads=os.cpu_count() or 1)
+            index = measure_index(lib, pkg, w, dev, stream, want)
         if rank == 0:
             print(json.dumps({"metric": "µs per decode-loop step (draft, schedule, fuse, verify, append)",
                               "value": loop["loop_step_us"], "unit": "us/step", "n_gpus": world,
                               "higher_is_better": False, "data": "synthetic",
                               "config": {"workload": args.workload, "B": B, "history_tokens": w.total_tokens,
                                          "seed": seed},
-                              "loop_steps": loop}), flush=True)
+                              "loop_steps": loop, "index": index}), flush=True)
         if dist is not None:
             dist.destroy_process_group()
         return
@@ -367,6 +377,11 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     loop = None
     if not args.no_loop:
         loop = measure_loop(lib, pkg, w, dev, stream, toks, offs, reps)
+    index = None
+    if not args.no_index:
+        import oracle
+        want = oracle.lookup_draft(w.tokens, w.offsets, min_m, max_m, K, threads=os.cpu_count() or 1)
+        index = measure_index(lib, pkg, w, dev, stream, want)
 
     # e2e: host buffers through lookup_draft_host, copies inside every step
     h_tok = tok_host.pin_memory()
@@ -457,6 +472,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         },
         "cpu_baseline": cpu,
         "loop_steps": loop,
+        "index": index,
         "gpu_launches": 2 * args.steps,
         "parity_with_oracle": bool(parity),
         "clocks": clocks.summary(),
@@ -602,6 +618,146 @@ def measure_loop(lib, pkg, w, dev, stream, toks, offs, reps: int) -> dict:
     res["loop_step_launches"] = 2 + 1 + 1 + 1 + 2
     res["method"] = (f"each call captured {ncopy}x back to back in a CUDA graph over rotating input copies, "
                      f"{reps} replays, CUDA events on the launching stream")
+    return res
+
+
+# ------------------------------------------------------- n-gram index ----
+INDEX_SPARE = 2048               # tokens of room per request for the timed appends
+
+
+def measure_index(lib, pkg, w, dev, stream, want) -> dict:
+    """The incremental n-gram index on the bench's batch (histories laid out in
+    slabs with INDEX_SPARE tokens of room each): build time, index size, the
+    draft from the index (which must equal the oracle's `want`), the in-place
+    append of 8 committed tokens per request, and one whole decode-loop step on
+    the index (draft, schedule, fuse, greedy verify, append).  Each call is
+    captured back to back in a CUDA graph and timed with CUDA events on its
+    stream; the index is larger than L2 and its accesses are scattered."""
+    import numpy as np
+    import torch
+
+    import gen
+
+    H, T = LOOP_H, LOOP_T
+    P = H + T
+    B = w.B
+    i32 = torch.int32
+    st, base_h, len_h, cap_h = gen.slabs_from_batch(w.tokens, w.offsets, INDEX_SPARE, seed=w.seed)
+    tokens = torch.from_numpy(st).to(dev)
+    base = torch.from_numpy(base_h).to(dev)
+    length = torch.from_numpy(len_h).to(dev)
+    cap = torch.from_numpy(cap_h).to(dev)
+    idx = pkg.NgramIndex(st.shape[0], w.min_m, w.max_m, device=dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def check(rc):
+        if rc != 0:
+            raise pkg.LookupDraftError(rc, lib)
+
+    torch.cuda.synchronize(dev)
+    builds = []
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            idx.build(tokens, base, length, stream=stream)
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        builds.append(ev0.elapsed_time(ev1))
+
+    K = w.K
+    draft = torch.empty((B, max(K, P)), dtype=i32, device=dev)
+    dl, dp, dm = (torch.empty(B, dtype=i32, device=dev) for _ in range(3))
+    with torch.cuda.stream(stream):
+        out = pkg.lookup_index_draft(tokens, base, length, w.min_m, w.max_m, K, idx.memory, idx.slots,
+                                     out=(draft[:, :K].contiguous(), dl, dp, dm), with_fallback=True, stream=stream)
+    torch.cuda.synchronize(dev)
+    parity = (np.array_equal(out[0].cpu().numpy(), want[0]) and np.array_equal(dl.cpu().numpy(), want[1])
+              and np.array_equal(dp.cpu().numpy(), want[2]))
+    fallbacks = int(out[4].sum().item())
+
+    hs = int(stream.cuda_stream)
+    tp, bp, lp, cp = tokens.data_ptr(), base.data_ptr(), length.data_ptr(), cap.data_ptr()
+    mem = idx.memory.data_ptr()
+
+    def draft_call(h, k=K):
+        check(lib.lookup_index_draft(tp, bp, lp, B, w.min_m, w.max_m, k, mem, idx.slots, 64, draft.data_ptr(),
+                                     dl.data_ptr(), dp.data_ptr(), dm.data_ptr(), None, h))
+
+    def timed(fn, per_graph: int, reps: int) -> float:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            hc = int(torch.cuda.current_stream().cuda_stream)
+            for _ in range(per_graph):
+                fn(hc)
+        with torch.cuda.stream(stream):
+            g.replay()
+            ev0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        return 1000.0 * ev0.elapsed_time(ev1) / (reps * per_graph)
+
+    draft_us = timed(draft_call, 32, 20)
+
+    # in-place append: 8 committed tokens per request per call (64 calls: 512 tokens of room)
+    rng = gen.rng_for(w.seed, 501)
+    W8 = 8
+    commit8 = torch.from_numpy(rng.integers(0, 50, size=(B, W8)).astype(np.int32)).to(dev)
+    n8 = torch.full((B,), W8, dtype=i32, device=dev)
+    status = torch.empty(B, dtype=i32, device=dev)
+
+    def append_call(h):
+        check(lib.lookup_index_append(tp, bp, lp, cp, commit8.data_ptr(), n8.data_ptr(), B, W8, w.min_m, w.max_m,
+                                      mem, idx.slots, 64, status.data_ptr(), h))
+
+    append_us = timed(append_call, 16, 3)                 # 16 (capture is not run) + 16 + 48 calls
+
+    # the decode-loop step on the index: at most P + 1 = 16 tokens per request per step
+    model_draft = torch.from_numpy(rng.integers(0, 50, size=(B, H)).astype(np.int32)).to(dev)
+    state = torch.zeros((B, 3), dtype=i32, device=dev)
+    long_block = torch.zeros(B, dtype=i32, device=dev)
+    committed = torch.full((B,), H + 1, dtype=i32, device=dev)
+    block = torch.empty((B, P), dtype=i32, device=dev)
+    blen = torch.empty(B, dtype=i32, device=dev)
+    pm = torch.empty((B, P), dtype=i32, device=dev)
+    target = torch.from_numpy(rng.integers(0, 50, size=(B, P + 1)).astype(np.int32)).to(dev)
+    accepted = torch.empty(B, dtype=i32, device=dev)
+    commit = torch.empty((B, P + 1), dtype=i32, device=dev)
+    ncommit = torch.empty(B, dtype=i32, device=dev)
+
+    def loop_call(h):
+        draft_call(h, P)
+        check(lib.lookup_schedule(dm.data_ptr(), committed.data_ptr(), B, H, T, 4, 1, 2, 3, state.data_ptr(),
+                                  long_block.data_ptr(), h))
+        check(lib.lookup_fuse(draft.data_ptr(), dm.data_ptr(), model_draft.data_ptr(), long_block.data_ptr(), B,
+                              P, H, T, 8, 6, 2, 4, block.data_ptr(), blen.data_ptr(), pm.data_ptr(), h))
+        check(lib.lookup_verify(block.data_ptr(), blen.data_ptr(), target.data_ptr(), None, None, None, None, B, P,
+                                accepted.data_ptr(), commit.data_ptr(), ncommit.data_ptr(), h))
+        check(lib.lookup_index_append(tp, bp, lp, cp, commit.data_ptr(), ncommit.data_ptr(), B, P + 1, w.min_m,
+                                      w.max_m, mem, idx.slots, 64, status.data_ptr(), h))
+
+    loop_us = timed(loop_call, 16, 4)                     # 80 steps: at most 1280 tokens of room
+    torch.cuda.synchronize(dev)
+    room_ok = bool((status == 0).all().item())
+    total_tokens = int(st.shape[0])
+    res = {
+        "layout": f"slabs with {INDEX_SPARE} tokens of room per request",
+        "index_bytes": int(idx.memory.numel()),
+        "index_bytes_per_token": round(idx.memory.numel() / total_tokens, 1),
+        "slots": idx.slots,
+        "build_ms": round(statistics.median(builds), 3),
+        "draft_us": round(draft_us, 3),
+        "append8_us": round(append_us, 3),
+        "loop_step_us": round(loop_us, 3),
+        "loop_step_launches": 5,
+        "parity_with_oracle": bool(parity),
+        "fallback_requests": fallbacks,
+        "appends_fit": room_ok,
+        "method": "calls captured back to back in CUDA graphs (32 drafts, 16 appends, 16 loop steps per graph), "
+                  "CUDA events on the launching stream",
+    }
+    del idx
     return res
 
 

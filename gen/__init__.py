@@ -262,3 +262,34 @@ def loop_append_inputs(B: int, W: int, seed: int, vocab: int = VOCAB_QWEN):
     commit = rng.integers(0, vocab, size=(B, W), dtype=np.int64).astype(np.int32)
     ncommit = rng.integers(0, W + 1, size=B).astype(np.int32)
     return commit, ncommit
+
+
+# ------------------------------------------------------------- slab layout ----
+def slabs_from_batch(tokens: np.ndarray, offsets: np.ndarray, spare: int, seed: int, gap_max: int = 40,
+                     fill: int = -5):
+    """Lay a CSR batch out as capacity-padded slabs: request r's history at
+    slab_tokens[base[r] : base[r] + len[r]], room for `spare` more tokens after
+    it, then a random gap.  Everything outside the histories holds `fill`.
+    Returns (slab_tokens int32, base int64 [B], len int32 [B], cap int32 [B])."""
+    rng = rng_for(seed, 105)
+    B = int(offsets.shape[0]) - 1
+    lens = (offsets[1:] - offsets[:-1]).astype(np.int64)
+    caps = lens + int(spare)
+    gaps = rng.integers(0, gap_max + 1, size=B)
+    base = np.zeros(B, np.int64)
+    pos = int(rng.integers(0, gap_max + 1))
+    for r in range(B):
+        base[r] = pos
+        pos += int(caps[r] + gaps[r])
+    out = np.full(pos + 1, fill, np.int32)
+    for r in range(B):
+        out[base[r]:base[r] + lens[r]] = tokens[offsets[r]:offsets[r + 1]]
+    return out, base, lens.astype(np.int32), caps.astype(np.int32)
+
+
+def csr_of_slabs(slab_tokens: np.ndarray, base: np.ndarray, length: np.ndarray):
+    """The CSR batch (tokens, offsets) holding the slabs' histories."""
+    parts = [slab_tokens[int(b):int(b) + int(n)] for b, n in zip(base, length)]
+    offsets = offsets_from_lengths([int(n) for n in length])
+    tokens = np.concatenate(parts).astype(np.int32) if parts else np.zeros(0, np.int32)
+    return tokens, offsets

@@ -1,0 +1,106 @@
+/*
+ * lookup_index.h -- a device-resident, incrementally updated n-gram index for
+ * prompt-lookup drafting on GB300.
+ *
+ * Source: Strata engine article, gtnt.cn/news/124732, section 四 (the engine
+ * keeps an n-gram -> position index of the prompt and of the confirmed output in
+ * a fixed-size open-addressing hash table, a few tens of bytes per history token,
+ * with O(1) appends, and drafts from the longest match it finds).  The result
+ * returned here is not an approximation: lookup_index_draft returns exactly what
+ * lookup_draft (include/lookup_draft.h; HyperQwen lookup-drafting article,
+ * section "第1步") returns for the same histories -- the longest current suffix of
+ * min_m..max_m tokens with an earlier occurrence, its most recent occurrence, and
+ * the K tokens after it read from the self-extended history.
+ *
+ * What the index holds.  For every request r, every length n in [min_m, max_m]
+ * and every history position q >= n - 1, the n-gram ending at q is a key
+ * (r, n, t[q-n+1 .. q]).  Each key's slot holds the two largest positions at
+ * which it ends (top1 > top2).  The current suffix's own n-gram ends at L - 1,
+ * the newest position, so its top2 is the most recent earlier occurrence: the
+ * longest n whose top2 exists is the match length, top2 - n + 1 its position.
+ * Keys are 64-bit hashes; every candidate is checked against the history, and a
+ * request whose candidates do not check out (two keys sharing a slot, or a
+ * table that overflowed) is answered by a brute-force warp scan of its history,
+ * so the result is exact whatever the hash does.
+ *
+ * Layout (device memory, caller-owned):
+ *   tokens   int32 [N]: the slabs; request r's history is tokens[base[r] ..
+ *            base[r] + len[r]) and may grow in place up to base[r] + cap[r].
+ *            Positions are int32 indexes into tokens, so N < 2^31.
+ *   base     int64 [B], len int32 [B], cap int32 [B] (len <= cap; slabs must not
+ *            overlap)
+ *   index    lookup_index_bytes(slots) bytes, 16-byte aligned (128-byte aligned
+ *            for full speed): a 128-byte header then `slots` 16-byte slots
+ *            (slots a power of two >= 16) in buckets of 2 slots, one 32-byte
+ *            sector each; a key's bucket is read whole in one load round.
+ *   The index remembers min_m, max_m, slots and hash_bits from the last build;
+ *   a call with other values fails its requests (lookup_index_draft reports
+ *   LOOKUP_DRAFT_LEN_FAILED, lookup_index_append status 2) instead of reading
+ *   a table it did not build.
+ *
+ * Return codes are those of lookup_draft.h.  Every call enqueues its work on
+ * `stream` and returns without synchronising; B == 0 enqueues nothing.
+ */
+#ifndef LOOKUP_INDEX_H
+#define LOOKUP_INDEX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+
+/* Slots for an index over `capacity_tokens` history tokens: the smallest power
+ * of two >= 2 * (max_m - min_m + 1) * capacity_tokens (load factor <= 1/2).
+ * Returns 0 for invalid arguments. */
+int64_t lookup_index_slots_for(int64_t capacity_tokens, int32_t min_m, int32_t max_m);
+
+/* Bytes of an index with `slots` slots: 128 + 16 * slots (0 if slots is not a
+ * power of two >= 16). */
+size_t lookup_index_bytes(int64_t slots);
+
+/*
+ * Build the index of the current histories: clears the table, then inserts every
+ * n-gram (n in [min_m, max_m]) of every history.  The insertions run in
+ * parallel, in any order (the slot update keeps the two largest positions).
+ * hash_bits in [1, 64] masks the 64-bit keys (64 in normal use; fewer bits make
+ * keys share slots, which the exact fallback absorbs -- a test hook).
+ * Scratch for the build comes from the library's stream-ordered pool.
+ * 1 <= min_m <= max_m <= LOOKUP_DRAFT_MAX_M; returns LOOKUP_DRAFT_EINVAL otherwise.
+ */
+int lookup_index_build(const int32_t *tokens, const int64_t *base, const int32_t *len, int32_t B,
+                       int32_t min_m, int32_t max_m, void *index, int64_t slots, int32_t hash_bits,
+                       struct CUstream_st *stream);
+
+/*
+ * Append request r's committed tokens commit[r][0 .. n) (n = ncommit[r] clamped
+ * to [0, W]) at tokens[base[r] + len[r]], insert the n-grams that end at the new
+ * positions, and add n to len[r].  out_status[r] (may be NULL): 0 = appended,
+ * 1 = the slab is full (len + n > cap; nothing appended), 2 = the index was
+ * built with other parameters (nothing appended).  O(n * (max_m - min_m + 1))
+ * per request.
+ */
+int lookup_index_append(int32_t *tokens, const int64_t *base, int32_t *len, const int32_t *cap,
+                        const int32_t *commit, const int32_t *ncommit, int32_t B, int32_t W,
+                        int32_t min_m, int32_t max_m, void *index, int64_t slots, int32_t hash_bits,
+                        int32_t *out_status, struct CUstream_st *stream);
+
+/*
+ * The draft step from the index: out_draft [B][K], out_len, out_pos, out_mlen
+ * (may be NULL) exactly as lookup_draft_ex gives them for the histories
+ * tokens[base[r] .. base[r] + len[r]).  out_fallback [B] (may be NULL): 1 where
+ * the request was answered by the brute-force scan, else 0.  0 <= K <= 64.
+ */
+int lookup_index_draft(const int32_t *tokens, const int64_t *base, const int32_t *len, int32_t B,
+                       int32_t min_m, int32_t max_m, int32_t K, const void *index, int64_t slots,
+                       int32_t hash_bits, int32_t *out_draft, int32_t *out_len, int32_t *out_pos,
+                       int32_t *out_mlen, int32_t *out_fallback, struct CUstream_st *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOOKUP_INDEX_H */

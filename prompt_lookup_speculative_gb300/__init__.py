@@ -1,8 +1,8 @@
 """GB300 prompt-lookup (n-gram) speculative drafting.
 
-Python binding of the C ABI in ``include/lookup_draft.h`` and
-``include/lookup_loop.h`` (ctypes; argument marshalling only -- every step runs in
-the library's CUDA kernels).
+Python binding of the C ABI in ``include/lookup_draft.h``,
+``include/lookup_loop.h`` and ``include/lookup_index.h`` (ctypes; argument
+marshalling only -- every step runs in the library's CUDA kernels).
 PyTorch tensors supply device memory and the current CUDA stream.
 
     draft, length, pos = lookup_draft(tokens, offsets, min_m=4, max_m=12, K=15)
@@ -27,6 +27,8 @@ __all__ = [
     "LookupDraftError", "load_library", "lookup_draft", "lookup_draft_ex", "lookup_draft_host",
     "lookup_draft_scan", "lookup_draft_fill", "lookup_draft_noalloc", "workspace_bytes",
     "set_wait_limit_ns", "lookup_fuse", "lookup_schedule", "lookup_verify", "lookup_append",
+    "NgramIndex", "index_slots_for", "index_bytes", "lookup_index_build", "lookup_index_append",
+    "lookup_index_draft",
     "MAX_M", "MAX_K", "LEN_FAILED",
 ]
 
@@ -100,6 +102,17 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.lookup_verify.restype = ctypes.c_int
     lib.lookup_append.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp]
     lib.lookup_append.restype = ctypes.c_int
+    i64 = ctypes.c_int64
+    lib.lookup_index_slots_for.argtypes = [i64, i32, i32]
+    lib.lookup_index_slots_for.restype = i64
+    lib.lookup_index_bytes.argtypes = [i64]
+    lib.lookup_index_bytes.restype = sz
+    lib.lookup_index_build.argtypes = [vp, vp, vp, i32, i32, i32, vp, i64, i32, vp]
+    lib.lookup_index_build.restype = ctypes.c_int
+    lib.lookup_index_append.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, i64, i32, vp, vp]
+    lib.lookup_index_append.restype = ctypes.c_int
+    lib.lookup_index_draft.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, i64, i32, vp, vp, vp, vp, vp, vp]
+    lib.lookup_index_draft.restype = ctypes.c_int
 
 
 def _check(rc: int, lib) -> None:
@@ -398,3 +411,114 @@ def lookup_append(tokens, offsets, commit, ncommit, out=None, stream=None):
         rc = lib.lookup_append(tp, offsets.data_ptr(), cp, np_, B, W, otp, op, _stream_handle(stream))
     _check(rc, lib)
     return out_t, out_o
+
+
+# ----------------------------------------------------------- n-gram index ----
+def index_slots_for(capacity_tokens: int, min_m: int = 4, max_m: int = 12) -> int:
+    """Recommended slot count (a power of two, load factor <= 1/2)."""
+    n = load_library().lookup_index_slots_for(int(capacity_tokens), min_m, max_m)
+    if n <= 0:
+        raise ValueError("invalid index parameters")
+    return int(n)
+
+
+def index_bytes(slots: int) -> int:
+    n = load_library().lookup_index_bytes(int(slots))
+    if n == 0:
+        raise ValueError("slots must be a power of two >= 16")
+    return int(n)
+
+
+def _slab_args(tokens, base, length, cap=None):
+    import torch
+    dev = tokens.device
+    B = base.shape[0]
+    if tokens.dtype != torch.int32 or not tokens.is_contiguous() or not tokens.is_cuda:
+        raise ValueError("tokens must be a contiguous int32 CUDA tensor")
+    ptrs = (_dev(base, torch.int64, (B,), dev, "base"), _dev(length, torch.int32, (B,), dev, "len"))
+    if cap is not None:
+        ptrs += (_dev(cap, torch.int32, (B,), dev, "cap"),)
+    return dev, B, ptrs
+
+
+def lookup_index_build(tokens, base, length, min_m: int, max_m: int, index, slots: int, hash_bits: int = 64,
+                       stream=None) -> None:
+    """Build the n-gram index of the slab histories tokens[base[r] .. base[r] + len[r])."""
+    import torch
+    lib = load_library()
+    dev, B, (bp, lp) = _slab_args(tokens, base, length)
+    with torch.cuda.device(dev):
+        rc = lib.lookup_index_build(tokens.data_ptr(), bp, lp, B, min_m, max_m, index.data_ptr(), int(slots),
+                                    hash_bits, _stream_handle(stream))
+    _check(rc, lib)
+
+
+def lookup_index_append(tokens, base, length, cap, commit, ncommit, min_m: int, max_m: int, index, slots: int,
+                        hash_bits: int = 64, status=None, stream=None):
+    """Append each request's committed tokens in place, index them, grow len.
+    Returns the per-request status tensor (0 ok, 1 slab full, 2 index mismatch)."""
+    import torch
+    lib = load_library()
+    dev, B, (bp, lp, cp) = _slab_args(tokens, base, length, cap)
+    W = commit.shape[1]
+    cm = _dev(commit, torch.int32, (B, W), dev, "commit")
+    nc = _dev(ncommit, torch.int32, (B,), dev, "ncommit")
+    if status is None:
+        status = torch.empty(B, dtype=torch.int32, device=dev)
+    sp = _dev(status, torch.int32, (B,), dev, "status")
+    with torch.cuda.device(dev):
+        rc = lib.lookup_index_append(tokens.data_ptr(), bp, lp, cp, cm, nc, B, W, min_m, max_m, index.data_ptr(),
+                                     int(slots), hash_bits, sp, _stream_handle(stream))
+    _check(rc, lib)
+    return status
+
+
+def lookup_index_draft(tokens, base, length, min_m: int, max_m: int, K: int, index, slots: int,
+                       hash_bits: int = 64, out=None, with_fallback: bool = False, stream=None):
+    """The draft step from the index; exactly lookup_draft_ex's results for the slab
+    histories.  Returns (draft, len, pos, mlen) and, with with_fallback, the
+    per-request flag of the brute-force path."""
+    import torch
+    lib = load_library()
+    dev, B, (bp, lp) = _slab_args(tokens, base, length)
+    if out is None:
+        out = (torch.empty((B, K), dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev),
+               torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev))
+    draft, ln, pos, mlen = out
+    fb = torch.empty(B, dtype=torch.int32, device=dev) if with_fallback else None
+    optr = (_dev(draft, torch.int32, (B, K), dev, "draft"), _dev(ln, torch.int32, (B,), dev, "len"),
+            _dev(pos, torch.int32, (B,), dev, "pos"), _dev(mlen, torch.int32, (B,), dev, "mlen"),
+            _dev(fb, torch.int32, (B,), dev, "fallback", optional=True))
+    with torch.cuda.device(dev):
+        rc = lib.lookup_index_draft(tokens.data_ptr(), bp, lp, B, min_m, max_m, K, index.data_ptr(), int(slots),
+                                    hash_bits, *optr, _stream_handle(stream))
+    _check(rc, lib)
+    return (draft, ln, pos, mlen, fb) if with_fallback else (draft, ln, pos, mlen)
+
+
+class NgramIndex:
+    """A device-resident n-gram index over slab histories (include/lookup_index.h).
+
+    Holds the index memory and its parameters; every method is one library call.
+    """
+
+    def __init__(self, capacity_tokens: int, min_m: int = 4, max_m: int = 12, device=None,
+                 hash_bits: int = 64, slots: int | None = None):
+        import torch
+        self.min_m, self.max_m, self.hash_bits = min_m, max_m, hash_bits
+        self.slots = int(slots) if slots is not None else index_slots_for(capacity_tokens, min_m, max_m)
+        nbytes = index_bytes(self.slots)
+        self.memory = torch.empty(nbytes, dtype=torch.uint8,
+                                  device=device if device is not None else torch.cuda.current_device())
+
+    def build(self, tokens, base, length, stream=None) -> None:
+        lookup_index_build(tokens, base, length, self.min_m, self.max_m, self.memory, self.slots,
+                           self.hash_bits, stream)
+
+    def append(self, tokens, base, length, cap, commit, ncommit, status=None, stream=None):
+        return lookup_index_append(tokens, base, length, cap, commit, ncommit, self.min_m, self.max_m,
+                                   self.memory, self.slots, self.hash_bits, status, stream)
+
+    def draft(self, tokens, base, length, K: int = 15, out=None, with_fallback: bool = False, stream=None):
+        return lookup_index_draft(tokens, base, length, self.min_m, self.max_m, K, self.memory, self.slots,
+                                  self.hash_bits, out, with_fallback, stream)

@@ -1,8 +1,9 @@
 """Compile the CUDA library in-tree for GB300 (sm_103a).
 
-The library is two translation units, ``csrc/lookup_draft.cu`` (the drafting
-step) and ``csrc/lookup_loop.cu`` (the decode-loop steps around it), built with
-nvcc into ``_build/liblookup_draft.so`` next to this file.  The CUDA runtime is linked
+The library is three translation units, ``csrc/lookup_draft.cu`` (the drafting
+step), ``csrc/lookup_loop.cu`` (the decode-loop steps around it) and
+``csrc/lookup_index.cu`` (the incremental n-gram index), built with nvcc into
+``_build/liblookup_draft.so`` next to this file.  The CUDA runtime is linked
 statically, so the library loads on a machine without a GPU (its calls then
 fail with a CUDA error) and needs nothing from the Python environment.
 """
@@ -15,8 +16,8 @@ import subprocess
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 REPO_DIR = os.path.dirname(PKG_DIR)
 INCLUDE_DIR = os.path.join(REPO_DIR, "include")
-SOURCES = [os.path.join(PKG_DIR, "csrc", "lookup_draft.cu"), os.path.join(PKG_DIR, "csrc", "lookup_loop.cu")]
-HEADERS = [os.path.join(INCLUDE_DIR, "lookup_draft.h"), os.path.join(INCLUDE_DIR, "lookup_loop.h")]
+SOURCES = [os.path.join(PKG_DIR, "csrc", f) for f in ("lookup_draft.cu", "lookup_loop.cu", "lookup_index.cu")]
+HEADERS = [os.path.join(INCLUDE_DIR, f) for f in ("lookup_draft.h", "lookup_loop.h", "lookup_index.h")]
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "liblookup_draft.so")
 

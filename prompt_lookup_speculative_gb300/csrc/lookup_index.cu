@@ -1,0 +1,716 @@
+// lookup_index.cu -- device-resident n-gram index for exact prompt-lookup drafting.
+//
+// Source: Strata engine article, gtnt.cn/news/124732, section 四 (an n-gram ->
+// position index of the prompt and confirmed output, open addressing, O(1)
+// appends); the result is the exact draft of HyperQwen lookup-drafting article,
+// section "第1步".  The contract is in include/lookup_index.h.
+//
+// Table: a 128-byte header, then `slots` 16-byte slots {key, top1, top2} in
+// buckets of 2 (one 32-byte sector: one DRAM access per probe).  The key of the n-gram ending at q in
+// request r is a 64-bit hash of (r, n, t[q], t[q-1], ..., t[q-n+1]) (0 marks an
+// empty slot); top1 > top2 are the two largest end positions inserted under it.
+// The build claims a slot with a CAS on the key and keeps the top two with two
+// atomicMax: the
+// new position goes into top1, and whichever of it and the displaced top1 is
+// smaller goes into top2.  Every value except the overall maximum reaches top2
+// that way and the maximum never does, so top2 ends as the second largest in
+// any insertion order: the build runs all positions in parallel, and hot keys
+// (periodic text) cost one atomic each rather than CAS retries.  The append,
+// where few threads meet on a slot, updates a slot with one 128-bit CAS of the
+// whole slot instead (fewer dependent round trips); the two kinds of update
+// never run at the same time.
+//
+// Query (one warp per request): lane j probes the key of the suffix's n-gram
+// for n = min_m + j.  The suffix ends at L - 1, the newest position, so its own
+// slot has top1 = L - 1 and top2 = the most recent earlier occurrence.  The
+// candidates are checked against the history; the longest n with a checked
+// candidate is the match.  A slot whose top1 is not L - 1 or whose top2 does
+// not check out has been shared with another key, and the request is answered
+// by a warp brute-force scan instead, so the result never depends on the hash.
+
+#include "lookup_draft.h"
+#include "lookup_index.h"
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+int lookup_record_cuda_error(cudaError_t e, const char *what);
+
+namespace {
+
+constexpr uint32_t kMagic = 0x4c4b4958u;        // "LKIX"
+constexpr int kBucket = 2;                      // slots per bucket: one 32-byte sector
+constexpr int kMaxProbe = 2048;                 // buckets probed before the overflow flag
+constexpr int kBuildThreads = 256;
+constexpr int kWarpThreads = 128;               // draft kernel: 4 warps per CTA
+constexpr int kAppendThreads = 256;             // append kernels
+constexpr int kScanThreads = 1024;
+
+struct __align__(16) Header {
+    uint32_t magic;
+    int32_t min_m, max_m, hash_bits;
+    int64_t slots;
+    uint32_t overflow;                          // set when an insertion found no slot
+    uint32_t pad[25];
+};
+static_assert(sizeof(Header) == 128, "header is 128 bytes: the slots start on a 128-byte line");
+
+struct __align__(16) Slot {
+    unsigned long long key;
+    int top1, top2;
+};
+static_assert(sizeof(Slot) == 16, "slot is 16 bytes");
+
+__device__ inline void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ inline void wait_for_prerequisite_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// splitmix64's output mix (Steele, Lea and Flood, "Fast splittable pseudorandom
+// number generators", OOPSLA 2014).
+__device__ inline uint64_t mix64(uint64_t x) {
+    x ^= x >> 30;
+    x *= 0xbf58476d1ce4e5b9ull;
+    x ^= x >> 27;
+    x *= 0x94d049bb133111ebull;
+    x ^= x >> 31;
+    return x;
+}
+
+__device__ inline uint64_t seed_of(int r) { return mix64(uint64_t(uint32_t(r)) * 0x9e3779b97f4a7c15ull + 0x632be59bd9b4e019ull); }
+__device__ inline uint64_t step_hash(uint64_t h, int32_t tok) { return mix64(h ^ uint64_t(uint32_t(tok))); }
+__device__ inline unsigned long long key_of(uint64_t h, int n, int hash_bits) {
+    uint64_t k = mix64(h ^ (uint64_t(n) << 40));
+    if (hash_bits < 64) k &= (uint64_t(1) << hash_bits) - 1;
+    return k ? k : 1ull;
+}
+
+__device__ inline bool header_ok(const Header *hd, int min_m, int max_m, int hash_bits, int64_t slots) {
+    return hd->magic == kMagic && hd->min_m == min_m && hd->max_m == max_m && hd->hash_bits == hash_bits &&
+           hd->slots == slots;
+}
+
+// Buckets: a key's home is bucket (key & bmask), kBucket consecutive slots in
+// one 32-byte sector, read whole in one round of loads; a full bucket moves on
+// to the next.  Every insertion scans in that same order and slots never empty again,
+// so an empty slot seen during a scan means the key is not stored further on.
+__device__ inline void read_bucket(const Slot *tab, int64_t b, int4 (&v)[kBucket]) {
+    const int4 *p = reinterpret_cast<const int4 *>(tab + b * kBucket);
+#pragma unroll
+    for (int s = 0; s < kBucket; ++s) v[s] = __ldcg(p + s);
+}
+
+__device__ inline unsigned long long key_in(int4 v) {
+    return (unsigned long long)(uint32_t(v.x)) | ((unsigned long long)(uint32_t(v.y)) << 32);
+}
+
+// Insert position q under key (the build); false (and the overflow flag) if no
+// slot was found.
+__device__ inline bool insert(Slot *tab, int64_t bmask, unsigned long long key, int q, Header *hd) {
+    int64_t b = int64_t(key & uint64_t(bmask));
+    for (int probe = 0; probe < kMaxProbe; ++probe) {
+        int4 v[kBucket];
+        read_bucket(tab, b, v);
+#pragma unroll
+        for (int s = 0; s < kBucket; ++s) {
+            Slot *sl = tab + b * kBucket + s;
+            unsigned long long k = key_in(v[s]);
+            if (k == 0ull) {
+                k = atomicCAS(&sl->key, 0ull, key);
+                if (k == 0ull) k = key;                  // claimed
+            }
+            if (k == key) {
+                const int old1 = atomicMax(&sl->top1, q);
+                atomicMax(&sl->top2, q > old1 ? old1 : q);
+                return true;
+            }
+        }
+        b = (b + 1) & bmask;
+    }
+    atomicOr(&hd->overflow, 1u);
+    return false;
+}
+
+// 128-bit compare-and-swap of a whole slot (atom.cas.b128, sm_90 and later):
+// returns the slot's previous contents.
+__device__ inline void cas_slot(Slot *s, uint64_t cmp_lo, uint64_t cmp_hi, uint64_t new_lo, uint64_t new_hi,
+                                uint64_t &old_lo, uint64_t &old_hi) {
+    asm volatile(
+        "{\n\t.reg .b128 d, c, v;\n\t"
+        "mov.b128 c, {%2, %3};\n\t"
+        "mov.b128 v, {%4, %5};\n\t"
+        "atom.global.cas.b128 d, [%6], c, v;\n\t"
+        "mov.b128 {%0, %1}, d;\n\t}"
+        : "=l"(old_lo), "=l"(old_hi)
+        : "l"(cmp_lo), "l"(cmp_hi), "l"(new_lo), "l"(new_hi), "l"(s)
+        : "memory");
+}
+
+__device__ inline uint64_t pack_tops(int top1, int top2) { return uint64_t(uint32_t(top1)) | (uint64_t(uint32_t(top2)) << 32); }
+
+// Insert for the append, where few threads meet on a slot: every change of a
+// slot is one 128-bit CAS of {key, top1, top2}.  After the bucket read, a new
+// key is one CAS (claim with tops {q, -1}) and an existing key one CAS from the
+// value read to the updated top two (retried on a lost race; a position already
+// dominated by both tops needs no write).  Only this kernel's insertions touch
+// the table while it runs.
+constexpr int kMaxCasRetries = 256;
+
+__device__ inline bool update_tops(Slot *sl, unsigned long long key, uint64_t hi, int q) {
+    for (int retry = 0; retry < kMaxCasRetries; ++retry) {
+        const int t1 = int(uint32_t(hi)), t2 = int(uint32_t(hi >> 32));
+        if (q == t1 || q <= t2) return true;             // present, or below both tops
+        const uint64_t want = q > t1 ? pack_tops(q, t1) : pack_tops(t1, q);
+        uint64_t lo2, hi2;
+        cas_slot(sl, key, hi, key, want, lo2, hi2);
+        if (hi2 == hi) return true;
+        hi = hi2;                                        // lost a race: retry from the new value
+    }
+    return false;
+}
+
+__device__ inline bool insert_cas(Slot *tab, int64_t bmask, unsigned long long key, int q, Header *hd) {
+    const uint64_t empty_hi = pack_tops(-1, -1);
+    int64_t b = int64_t(key & uint64_t(bmask));
+    for (int probe = 0; probe < kMaxProbe; ++probe) {
+        int4 v[kBucket];
+        read_bucket(tab, b, v);
+#pragma unroll
+        for (int s = 0; s < kBucket; ++s) {
+            Slot *sl = tab + b * kBucket + s;
+            const unsigned long long k = key_in(v[s]);
+            uint64_t hi = uint64_t(uint32_t(v[s].z)) | (uint64_t(uint32_t(v[s].w)) << 32);
+            if (k == 0ull) {
+                uint64_t lo;
+                cas_slot(sl, 0ull, empty_hi, key, pack_tops(q, -1), lo, hi);
+                if (lo == 0ull) return true;             // claimed (an empty slot is always {0, -1, -1})
+                if (lo != key) continue;                 // taken by another key meanwhile
+            } else if (k != key) {
+                continue;
+            }
+            if (update_tops(sl, key, hi, q)) return true;
+            atomicOr(&hd->overflow, 1u);
+            return false;
+        }
+        b = (b + 1) & bmask;
+    }
+    atomicOr(&hd->overflow, 1u);
+    return false;
+}
+
+// The slot of key (its tops), from whole-bucket reads; false when an empty slot
+// or the probe limit is reached first.
+__device__ inline bool find(const Slot *tab, int64_t bmask, unsigned long long key, int &top1, int &top2) {
+    int64_t b = int64_t(key & uint64_t(bmask));
+    for (int probe = 0; probe < kMaxProbe; ++probe) {
+        int4 v[kBucket];
+        read_bucket(tab, b, v);
+#pragma unroll
+        for (int s = 0; s < kBucket; ++s) {
+            const unsigned long long k = key_in(v[s]);
+            if (k == key) {
+                top1 = v[s].z;
+                top2 = v[s].w;
+                return true;
+            }
+            if (k == 0ull) return false;
+        }
+        b = (b + 1) & bmask;
+    }
+    return false;
+}
+
+// Insert the n-grams (n in [min_m, max_m]) that end at position q = base + i.
+// The tokens are loaded first, all at once (the hash chain would otherwise wait
+// for each load in turn).
+__device__ inline void insert_position(const int32_t *tokens, int64_t base, int i, int r, int min_m, int max_m,
+                                       int hash_bits, Slot *tab, int64_t mask, Header *hd) {
+    const int64_t q = base + i;
+    const int top = min(max_m, i + 1);
+    int32_t v[LOOKUP_DRAFT_MAX_M];
+#pragma unroll
+    for (int k = 0; k < LOOKUP_DRAFT_MAX_M; ++k) v[k] = k < top ? tokens[q - k] : 0;
+    uint64_t h = seed_of(r);
+#pragma unroll
+    for (int k = 0; k < LOOKUP_DRAFT_MAX_M; ++k) {
+        if (k < top) {
+            h = step_hash(h, v[k]);
+            if (k + 1 >= min_m) insert(tab, mask, key_of(h, k + 1, hash_bits), int(q), hd);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ build ----
+struct BuildParams {
+    const int32_t *tokens;
+    const int64_t *base;
+    const int32_t *len;
+    int64_t *pref;                                       // [B + 1] scratch: prefix of len
+    Slot *tab;
+    Header *hd;
+    int64_t slots;
+    int32_t B, min_m, max_m, hash_bits;
+};
+
+__global__ void clear_kernel(BuildParams p) {
+    wait_for_prerequisite_grid();
+    allow_dependent_launch();
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < p.slots; i += stride) {
+        Slot s;
+        s.key = 0ull;
+        s.top1 = -1;
+        s.top2 = -1;
+        p.tab[i] = s;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        Header h;
+        memset(&h, 0, sizeof h);
+        h.magic = kMagic;
+        h.min_m = p.min_m;
+        h.max_m = p.max_m;
+        h.hash_bits = p.hash_bits;
+        h.slots = p.slots;
+        *p.hd = h;
+    }
+}
+
+// pref[r] = sum of len[0..r) (negative lengths count as 0), one CTA.
+__global__ void __launch_bounds__(kScanThreads) prefix_kernel(BuildParams p) {
+    __shared__ int64_t warp_sums[kScanThreads / 32];
+    wait_for_prerequisite_grid();
+    allow_dependent_launch();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t per = (int64_t(p.B) + kScanThreads - 1) / kScanThreads;
+    const int64_t r0 = min(int64_t(tid) * per, int64_t(p.B)), r1 = min(r0 + per, int64_t(p.B));
+    int64_t own = 0;
+    for (int64_t r = r0; r < r1; ++r) own += max(p.len[r], 0);
+    int64_t incl = own;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += y;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t s = warp_sums[lane];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, s, d);
+            if (lane >= d) s += y;
+        }
+        warp_sums[lane] = s;
+    }
+    __syncthreads();
+    int64_t before = (warp ? warp_sums[warp - 1] : 0) + incl - own;
+    for (int64_t r = r0; r < r1; ++r) {
+        p.pref[r] = before;
+        before += max(p.len[r], 0);
+    }
+    if (tid == kScanThreads - 1) p.pref[p.B] = warp_sums[kScanThreads / 32 - 1];
+}
+
+// Every history position, flattened: warp w takes a contiguous range of the
+// virtual positions [0, pref[B]); each lane walks its request forward.
+__global__ void __launch_bounds__(kBuildThreads) build_kernel(BuildParams p) {
+    wait_for_prerequisite_grid();
+    allow_dependent_launch();
+    const int lane = threadIdx.x & 31;
+    const int64_t gwarp = (int64_t(blockIdx.x) * kBuildThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = int64_t(gridDim.x) * (kBuildThreads / 32);
+    const int64_t total = p.pref[p.B];
+    const int64_t per = ((total + nwarps - 1) / nwarps + 31) & ~int64_t(31);
+    const int64_t v0 = min(gwarp * per, total), v1 = min(v0 + per, total);
+    if (v0 >= v1) return;
+    int lo = 0, hi = p.B;                                // pref[lo] <= v0 < pref[hi]
+    while (hi - lo > 1) {
+        const int step = (hi - lo + 31) / 32;
+        const int idx = min(lo + lane * step, hi - 1);
+        const unsigned le = __ballot_sync(0xffffffffu, p.pref[idx] <= v0);
+        const int last = 31 - __clz(le);
+        const int nlo = min(lo + last * step, hi - 1);
+        hi = min(nlo + step, hi);
+        lo = nlo;
+    }
+    int r = lo;
+    int64_t r_end = p.pref[r + 1], r_start = p.pref[r], base = p.base[r];
+    const int64_t mask = (p.slots / kBucket) - 1;       // bucket mask
+    for (int64_t v = v0 + lane; v < v1; v += 32) {
+        while (r_end <= v) {
+            ++r;
+            r_start = r_end;
+            r_end = p.pref[r + 1];
+            base = p.base[r];
+        }
+        insert_position(p.tokens, base, int(v - r_start), r, p.min_m, p.max_m, p.hash_bits, p.tab, mask, p.hd);
+    }
+}
+
+// ----------------------------------------------------------------- append ----
+struct AppendParams {
+    int32_t *tokens;
+    const int64_t *base;
+    int32_t *len;
+    const int32_t *cap;
+    const int32_t *commit;
+    const int32_t *ncommit;
+    Slot *tab;
+    Header *hd;
+    int32_t *status;
+    int64_t slots;
+    int32_t B, W, min_m, max_m, hash_bits;
+};
+
+__device__ inline int append_status(const AppendParams &p, bool ok, int r, int &L, int &n, int64_t &base) {
+    L = p.len[r];
+    n = min(max(p.ncommit[r], 0), p.W);
+    base = p.base[r];
+    return !ok ? 2 : (int64_t(L) + n > int64_t(p.cap[r]) ? 1 : 0);
+}
+
+// The writes and insertions: one thread per (request, new position, length)
+// task, grid-stride over B * W * (max_m - min_m + 1) tasks.  The tokens that
+// end at a new position come from the old history or straight from `commit`,
+// so no insertion waits for a write.  len is only read here.
+template <int kMaxLen>
+__global__ void __launch_bounds__(kAppendThreads) index_append_kernel(AppendParams p) {
+    wait_for_prerequisite_grid();
+    allow_dependent_launch();
+    const bool ok = header_ok(p.hd, p.min_m, p.max_m, p.hash_bits, p.slots);
+    const int64_t mask = (p.slots / kBucket) - 1;       // bucket mask
+    const int nl = p.max_m - p.min_m + 1;
+    const int64_t per_r = int64_t(p.W) * nl;
+    const int64_t total = int64_t(p.B) * per_r;
+    for (int64_t task = int64_t(blockIdx.x) * kAppendThreads + threadIdx.x; task < total;
+         task += int64_t(gridDim.x) * kAppendThreads) {
+        const int r = int(task / per_r);
+        const int rest = int(task - int64_t(r) * per_r);
+        const int j = rest / nl, len_n = p.min_m + rest % nl;   // new position L + j, length len_n
+        int L, n;
+        int64_t base;
+        if (append_status(p, ok, r, L, n, base) != 0 || j >= n) continue;
+        const int32_t *crow = p.commit + int64_t(r) * p.W;
+        if (len_n == p.min_m) p.tokens[base + L + j] = crow[j];  // one writer per new token
+        const int i = L + j;
+        if (i + 1 < len_n) continue;                         // no n-gram of that length ends here
+        // the len_n tokens ending at i, from the old history or from commit, loaded at once
+        int32_t v[kMaxLen];
+#pragma unroll
+        for (int k = 0; k < kMaxLen; ++k) {
+            const int src = i - k;
+            v[k] = k >= len_n ? 0 : (src >= L ? crow[src - L] : p.tokens[base + src]);
+        }
+        uint64_t h = seed_of(r);
+#pragma unroll
+        for (int k = 0; k < kMaxLen; ++k)
+            if (k < len_n) h = step_hash(h, v[k]);
+        insert_cas(p.tab, mask, key_of(h, len_n, p.hash_bits), int(base + i), p.hd);
+    }
+}
+
+// Then the lengths and the status, one thread per request (after every reader
+// of len in the kernel above).
+__global__ void __launch_bounds__(kAppendThreads) append_len_kernel(AppendParams p) {
+    wait_for_prerequisite_grid();
+    allow_dependent_launch();
+    const bool ok = header_ok(p.hd, p.min_m, p.max_m, p.hash_bits, p.slots);
+    for (int r = blockIdx.x * kAppendThreads + threadIdx.x; r < p.B; r += gridDim.x * kAppendThreads) {
+        int L, n;
+        int64_t base;
+        const int st = append_status(p, ok, r, L, n, base);
+        if (st == 0) p.len[r] = L + n;
+        if (p.status) p.status[r] = st;
+    }
+}
+
+// ------------------------------------------------------------------ draft ----
+struct DraftParams {
+    const int32_t *tokens;
+    const int64_t *base;
+    const int32_t *len;
+    const Slot *tab;
+    const Header *hd;
+    int32_t *out_draft;
+    int32_t *out_len;
+    int32_t *out_pos;
+    int32_t *out_mlen;
+    int32_t *out_fallback;
+    int64_t slots;
+    int32_t B, min_m, max_m, K, hash_bits;
+};
+
+// The exact answer by brute force: candidate ends q = L-2, L-3, ... in batches of
+// 32 (one per lane), each extended backwards up to max_m tokens; the largest key
+// (m << 32 | p) wins, and a batch holding a max_m match ends the search.
+__device__ unsigned long long brute_force(const int32_t *t, int L, int tok, int min_m, int max_m, int lane) {
+    unsigned long long best = 0ull;
+    for (int qe = L - 2; qe >= min_m - 1; qe -= 32) {
+        const int q = qe - lane;
+        int k = 0;
+        bool alive = q >= min_m - 1;
+        for (int i = 0; i < max_m; ++i) {
+            const int s = __shfl_sync(0xffffffffu, tok, i);    // suffix token i (from the end)
+            alive = alive && q - i >= 0 && t[q - i] == s;
+            k += alive;
+        }
+        unsigned long long key = 0ull;
+        if (k >= min_m) key = (uint64_t(uint32_t(k)) << 32) | uint32_t(q - k + 1);
+#pragma unroll
+        for (int d = 16; d; d >>= 1) {
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, d);
+            key = o > key ? o : key;
+        }
+        best = key > best ? key : best;
+        if (int(best >> 32) == max_m) break;
+    }
+    return best;
+}
+
+__global__ void __launch_bounds__(kWarpThreads) index_draft_kernel(DraftParams p) {
+    wait_for_prerequisite_grid();
+    allow_dependent_launch();
+    const int lane = threadIdx.x & 31;
+    const int nwarps = gridDim.x * (kWarpThreads / 32);
+    const bool hd_ok = header_ok(p.hd, p.min_m, p.max_m, p.hash_bits, p.slots);
+    const bool overflow = hd_ok && p.hd->overflow != 0u;
+    const int64_t mask = (p.slots / kBucket) - 1;       // bucket mask
+    const int nl = p.max_m - p.min_m + 1;
+    for (int r = (blockIdx.x * kWarpThreads + threadIdx.x) >> 5; r < p.B; r += nwarps) {
+        const int L = max(p.len[r], 0);
+        const int64_t base = p.base[r];
+        const int32_t *t = p.tokens + base;
+        // suffix token i (counted from the end) in lane i
+        const int tok = (lane < p.max_m && lane < L) ? t[L - 1 - lane] : 0;
+        int32_t *row = p.out_draft + int64_t(r) * p.K;
+        unsigned long long best = 0ull;
+        bool fallback = overflow, drafted = false;
+        if (hd_ok && !overflow && L >= p.min_m + 1) {
+            // keys: lane j hashes the n-gram of length n = min_m + j
+            const int n = p.min_m + lane;
+            unsigned long long key = 0ull;
+            uint64_t h = seed_of(r);
+            const int top = min(p.max_m, L);
+            for (int k = 0; k < top; ++k) {
+                h = step_hash(h, __shfl_sync(0xffffffffu, tok, k));
+                if (k + 1 == n) key = key_of(h, n, p.hash_bits);
+            }
+            // 0 none, 1 candidate, 2 inconsistent (the slot is shared or missing)
+            int state = 0, cand = -1;
+            if (lane < nl && n <= L - 1) {
+                int top1 = -1, top2 = -1;
+                if (!find(p.tab, mask, key, top1, top2)) {
+                    state = 2;
+                } else if (int64_t(top1) != base + L - 1) {
+                    state = 2;
+                } else if (top2 >= 0) {
+                    const int64_t c = int64_t(top2) - base;      // relative end position
+                    if (c < n - 1 || c > L - 2) state = 2;
+                    else { state = 1; cand = int(c); }
+                }
+            }
+            const unsigned cmask = __ballot_sync(0xffffffffu, state == 1);
+            const unsigned incons = __ballot_sync(0xffffffffu, state == 2);
+            const int jbest = cmask ? 31 - __clz(cmask) : -1;
+            // a longer length whose slot is inconsistent may hide the true match
+            const unsigned above = jbest >= 0 ? (jbest < 31 ? ~((2u << jbest) - 1) : 0u) : 0xffffffffu;
+            if (incons & above) {
+                fallback = true;
+            } else if (jbest >= 0) {
+                // check the candidate and gather its draft in the same round of loads
+                const int m = p.min_m + jbest;
+                const int c = __shfl_sync(0xffffffffu, cand, jbest);
+                const int d = L - 1 - c;                         // L - pos - m
+                const bool bad = lane < m && t[c - lane] != tok;
+                const int32_t d0 = lane < p.K ? t[c + 1 + lane % d] : 0;
+                const int32_t d1 = lane + 32 < p.K ? t[c + 1 + (lane + 32) % d] : 0;
+                if (__ballot_sync(0xffffffffu, bad)) {
+                    fallback = true;                             // the slot was shared with another key
+                } else {
+                    best = (uint64_t(uint32_t(m)) << 32) | uint32_t(c - m + 1);
+                    if (lane < p.K) row[lane] = d0;
+                    if (lane + 32 < p.K) row[lane + 32] = d1;
+                    drafted = true;
+                }
+            }
+        }
+        if (fallback && hd_ok) best = brute_force(t, L, tok, p.min_m, p.max_m, lane);
+        const int m = int(best >> 32);
+        const int pos = int(uint32_t(best));
+        const bool found = hd_ok && m > 0;
+        if (!drafted) {                                         // the draft from the self-extended history
+            const int d = L - pos - m;
+            for (int j = lane; j < p.K; j += 32) row[j] = found ? t[pos + m + (j % d)] : -1;
+        }
+        if (lane == 0) {
+            p.out_len[r] = !hd_ok ? LOOKUP_DRAFT_LEN_FAILED : (found ? p.K : 0);
+            p.out_pos[r] = found ? pos : -1;
+            if (p.out_mlen) p.out_mlen[r] = found ? m : 0;
+            if (p.out_fallback) p.out_fallback[r] = fallback ? 1 : 0;
+        }
+    }
+}
+
+// ------------------------------------------------------------------- host ----
+template <typename Params>
+int launch_pdl(void (*kernel)(Params), unsigned grid, unsigned block, cudaStream_t stream, const Params &prm) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
+    return e == cudaSuccess ? LOOKUP_DRAFT_OK : lookup_record_cuda_error(e, "kernel launch");
+}
+
+int sm_count(int *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
+    return e == cudaSuccess ? LOOKUP_DRAFT_OK : lookup_record_cuda_error(e, "device query");
+}
+
+bool pow2(int64_t x) { return x >= 16 && (x & (x - 1)) == 0; }
+
+bool params_ok(int32_t min_m, int32_t max_m, int32_t hash_bits, int64_t slots) {
+    return min_m >= 1 && min_m <= max_m && max_m <= LOOKUP_DRAFT_MAX_M && hash_bits >= 1 && hash_bits <= 64 &&
+           pow2(slots);
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+unsigned warp_grid(int B, int sms) {
+    const int64_t need = (int64_t(B) + kWarpThreads / 32 - 1) / (kWarpThreads / 32);
+    return unsigned(need < int64_t(sms) * 16 ? need : int64_t(sms) * 16);
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t lookup_index_slots_for(int64_t capacity_tokens, int32_t min_m, int32_t max_m) {
+    if (capacity_tokens < 0 || min_m < 1 || min_m > max_m || max_m > LOOKUP_DRAFT_MAX_M) return 0;
+    const int64_t want = 2 * int64_t(max_m - min_m + 1) * capacity_tokens;
+    int64_t s = 16;
+    while (s < want) {
+        if (s > (int64_t(1) << 40)) return 0;
+        s <<= 1;
+    }
+    return s;
+}
+
+size_t lookup_index_bytes(int64_t slots) {
+    if (!pow2(slots) || slots > (int64_t(1) << 40)) return 0;
+    return sizeof(Header) + sizeof(Slot) * size_t(slots);
+}
+
+int lookup_index_build(const int32_t *tokens, const int64_t *base, const int32_t *len, int32_t B, int32_t min_m,
+                       int32_t max_m, void *index, int64_t slots, int32_t hash_bits, struct CUstream_st *stream) {
+    if (B < 0 || !params_ok(min_m, max_m, hash_bits, slots) || !index || !aligned16(index)) return LOOKUP_DRAFT_EINVAL;
+    if (B > 0 && (!tokens || !base || !len)) return LOOKUP_DRAFT_EINVAL;
+    int sms = 0;
+    int rc = sm_count(&sms);
+    if (rc != LOOKUP_DRAFT_OK) return rc;
+    cudaStream_t st = stream;
+    BuildParams p{};
+    p.tokens = tokens;
+    p.base = base;
+    p.len = len;
+    p.hd = static_cast<Header *>(index);
+    p.tab = reinterpret_cast<Slot *>(static_cast<char *>(index) + sizeof(Header));
+    p.slots = slots;
+    p.B = B;
+    p.min_m = min_m;
+    p.max_m = max_m;
+    p.hash_bits = hash_bits;
+    void *pref = nullptr;
+    if (B > 0) {                                         // scratch first: the kernels then follow one another
+        const cudaError_t e = cudaMallocAsync(&pref, sizeof(int64_t) * (size_t(B) + 1), st);
+        if (e != cudaSuccess) return lookup_record_cuda_error(e, "build scratch");
+    }
+    p.pref = static_cast<int64_t *>(pref);
+    rc = launch_pdl(clear_kernel, unsigned(sms * 8), 256u, st, p);
+    if (B == 0) return rc;
+    if (rc == LOOKUP_DRAFT_OK) rc = launch_pdl(prefix_kernel, 1u, unsigned(kScanThreads), st, p);
+    if (rc == LOOKUP_DRAFT_OK) rc = launch_pdl(build_kernel, unsigned(sms * 8), unsigned(kBuildThreads), st, p);
+    const cudaError_t e = cudaFreeAsync(pref, st);
+    if (rc == LOOKUP_DRAFT_OK && e != cudaSuccess) rc = lookup_record_cuda_error(e, "build scratch");
+    return rc;
+}
+
+int lookup_index_append(int32_t *tokens, const int64_t *base, int32_t *len, const int32_t *cap, const int32_t *commit,
+                        const int32_t *ncommit, int32_t B, int32_t W, int32_t min_m, int32_t max_m, void *index,
+                        int64_t slots, int32_t hash_bits, int32_t *out_status, struct CUstream_st *stream) {
+    if (B < 0 || W < 0 || !params_ok(min_m, max_m, hash_bits, slots)) return LOOKUP_DRAFT_EINVAL;
+    if (B == 0) return LOOKUP_DRAFT_OK;
+    if (!tokens || !base || !len || !cap || !ncommit || (W > 0 && !commit) || !index || !aligned16(index))
+        return LOOKUP_DRAFT_EINVAL;
+    int sms = 0;
+    int rc = sm_count(&sms);
+    if (rc != LOOKUP_DRAFT_OK) return rc;
+    AppendParams p{};
+    p.tokens = tokens;
+    p.base = base;
+    p.len = len;
+    p.cap = cap;
+    p.commit = commit;
+    p.ncommit = ncommit;
+    p.hd = static_cast<Header *>(index);
+    p.tab = reinterpret_cast<Slot *>(static_cast<char *>(index) + sizeof(Header));
+    p.status = out_status;
+    p.slots = slots;
+    p.B = B;
+    p.W = W;
+    p.min_m = min_m;
+    p.max_m = max_m;
+    p.hash_bits = hash_bits;
+    const int64_t tasks = int64_t(B) * W * (max_m - min_m + 1);
+    const int64_t want = (tasks + kAppendThreads - 1) / kAppendThreads;
+    const unsigned grid = unsigned(want < int64_t(sms) * 8 ? (want > 0 ? want : 1) : int64_t(sms) * 8);
+    // the token window in registers: 16 entries when max_m allows, else 32
+    rc = launch_pdl(max_m <= 16 ? index_append_kernel<16> : index_append_kernel<LOOKUP_DRAFT_MAX_M>, grid,
+                    unsigned(kAppendThreads), stream, p);
+    if (rc != LOOKUP_DRAFT_OK) return rc;
+    const unsigned grid2 = unsigned((int64_t(B) + kAppendThreads - 1) / kAppendThreads);
+    return launch_pdl(append_len_kernel, grid2 < unsigned(sms * 4) ? grid2 : unsigned(sms * 4), unsigned(kAppendThreads),
+                      stream, p);
+}
+
+int lookup_index_draft(const int32_t *tokens, const int64_t *base, const int32_t *len, int32_t B, int32_t min_m,
+                       int32_t max_m, int32_t K, const void *index, int64_t slots, int32_t hash_bits,
+                       int32_t *out_draft, int32_t *out_len, int32_t *out_pos, int32_t *out_mlen,
+                       int32_t *out_fallback, struct CUstream_st *stream) {
+    if (B < 0 || K < 0 || K > LOOKUP_DRAFT_MAX_K || !params_ok(min_m, max_m, hash_bits, slots))
+        return LOOKUP_DRAFT_EINVAL;
+    if (B == 0) return LOOKUP_DRAFT_OK;
+    if (!tokens || !base || !len || !index || !aligned16(index) || (K > 0 && !out_draft) || !out_len || !out_pos)
+        return LOOKUP_DRAFT_EINVAL;
+    int sms = 0;
+    int rc = sm_count(&sms);
+    if (rc != LOOKUP_DRAFT_OK) return rc;
+    DraftParams p{};
+    p.tokens = tokens;
+    p.base = base;
+    p.len = len;
+    p.hd = static_cast<const Header *>(index);
+    p.tab = reinterpret_cast<const Slot *>(static_cast<const char *>(index) + sizeof(Header));
+    p.out_draft = out_draft;
+    p.out_len = out_len;
+    p.out_pos = out_pos;
+    p.out_mlen = out_mlen;
+    p.out_fallback = out_fallback;
+    p.slots = slots;
+    p.B = B;
+    p.min_m = min_m;
+    p.max_m = max_m;
+    p.K = K;
+    p.hash_bits = hash_bits;
+    return launch_pdl(index_draft_kernel, warp_grid(B, sms), unsigned(kWarpThreads), stream, p);
+}
+
+}  // extern "C"

@@ -1,0 +1,183 @@
+"""GPU parity of the incremental n-gram index (include/lookup_index.h).
+
+The index must return exactly the oracle's draft (the definition of the draft
+step) for the histories it holds: after a build, after every append of a
+multi-step decode loop, with keys forced to share slots (the exact fallback),
+and with a table too small to hold them.  Histories sit in capacity-padded
+slabs with gaps (gen.slabs_from_batch); the oracle reads the same histories
+as a CSR batch.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import gen
+import oracle
+
+torch = pytest.importorskip("torch")
+pkg = pytest.importorskip("prompt_lookup_speculative_gb300")
+
+pytestmark = pytest.mark.gpu
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def oracle_draft(slab_t, base, length, min_m, max_m, K):
+    t, o = gen.csr_of_slabs(slab_t, base, length)
+    return oracle.lookup_draft(t, o, min_m, max_m, K, threads=16)
+
+
+def check_draft(got, want):
+    d, ln, pos, m = (host(x) for x in got[:4])
+    wd, wl, wp, wm = want
+    np.testing.assert_array_equal(m, wm)
+    np.testing.assert_array_equal(pos, wp)
+    np.testing.assert_array_equal(ln, wl)
+    np.testing.assert_array_equal(d, wd)
+
+
+def built(slab_t, base, length, min_m, max_m, hash_bits=64, slots=None):
+    t, b, n = dev(slab_t), dev(base), dev(length)
+    idx = pkg.NgramIndex(slab_t.shape[0], min_m, max_m, hash_bits=hash_bits, slots=slots)
+    idx.build(t, b, n)
+    return idx, t, b, n
+
+
+@pytest.mark.parametrize("name", gen.WORKLOADS)
+def test_index_draft_matches_oracle(name):
+    w = gen.make_workload(name)
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, 32, seed=w.seed)
+    idx, t, b, n = built(st, base, length, w.min_m, w.max_m)
+    got = idx.draft(t, b, n, w.K, with_fallback=True)
+    check_draft(got, oracle_draft(st, base, length, w.min_m, w.max_m, w.K))
+    assert host(got[4]).sum() == 0                      # 64-bit keys: no request needed the fallback
+
+
+@pytest.mark.parametrize("min_m,max_m,K", [(1, 3, 5), (2, 8, 0), (4, 4, 64), (3, 32, 7), (1, 1, 1)])
+def test_index_parameters_and_short_histories(min_m, max_m, K):
+    rng = gen.rng_for(min_m * 100 + max_m, 31)
+    lengths = [0, 1, 2, 3, 4, 5, 6, 7, 8, 12, 13, 33, 100, 700]
+    hist = [rng.integers(0, 3, size=L).astype(np.int32) for L in lengths]
+    tokens = np.concatenate(hist)
+    offsets = gen.offsets_from_lengths(lengths)
+    st, base, length, cap = gen.slabs_from_batch(tokens, offsets, 16, seed=3)
+    idx, t, b, n = built(st, base, length, min_m, max_m)
+    check_draft(idx.draft(t, b, n, K), oracle_draft(st, base, length, min_m, max_m, K))
+
+
+@pytest.mark.parametrize("hash_bits", [1, 3, 8, 14])
+@pytest.mark.parametrize("name", ["tiny", "periodic"])
+def test_shared_slots_fall_back_exactly(hash_bits, name):
+    """With few key bits most keys share slots; the candidates that do not check
+    out send their requests to the brute-force scan, and the result stays exact."""
+    w = gen.make_workload(name)
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, 0, seed=5)
+    idx, t, b, n = built(st, base, length, w.min_m, w.max_m, hash_bits=hash_bits)
+    got = idx.draft(t, b, n, w.K, with_fallback=True)
+    check_draft(got, oracle_draft(st, base, length, w.min_m, w.max_m, w.K))
+    if hash_bits <= 8:
+        assert host(got[4]).sum() > 0
+
+
+def test_overflowing_table_falls_back_exactly():
+    w = gen.make_workload("tiny")
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, 0, seed=6)
+    idx, t, b, n = built(st, base, length, w.min_m, w.max_m, slots=1024)   # far too small
+    got = idx.draft(t, b, n, w.K, with_fallback=True)
+    check_draft(got, oracle_draft(st, base, length, w.min_m, w.max_m, w.K))
+    assert host(got[4]).all()
+
+
+@pytest.mark.parametrize("name", ["tiny", "recitation25k", "periodic", "chats"])
+def test_index_decode_loop(name):
+    """Draft from the index, commit a synthetic continuation (an accepted prefix
+    of the draft and one more token), append it in place, and compare both the
+    histories and the next draft with the oracle, for several steps."""
+    w = gen.make_workload(name)
+    W = 16
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, 6 * W, seed=w.seed)
+    idx, t, b, n = built(st, base, length, w.min_m, w.max_m)
+    capd = dev(cap)
+    B = w.B
+    cur_t, cur_o = w.tokens, w.offsets
+    rng = gen.rng_for(w.seed, 41)
+    for step in range(6):
+        got = idx.draft(t, b, n, w.K, with_fallback=True)
+        want = oracle.lookup_draft(cur_t, cur_o, w.min_m, w.max_m, w.K, threads=16)
+        check_draft(got, want)
+        # commit: an accepted prefix of the draft (or of random tokens), then one more token
+        acc = rng.integers(0, W, size=B)
+        commit = rng.integers(0, 50, size=(B, W)).astype(np.int32)
+        d = want[0]
+        for r in range(B):
+            k = min(int(acc[r]), w.K) if want[1][r] > 0 else 0
+            commit[r, :k] = d[r, :k]
+        ncommit = (np.minimum(acc, w.K) + 1).astype(np.int32)
+        status = idx.append(t, b, n, capd, dev(commit), dev(ncommit))
+        assert (host(status) == 0).all()
+        cur_t, cur_o = oracle.append(cur_t, cur_o, commit, ncommit)
+        got_t, got_o = gen.csr_of_slabs(host(t), base, host(n))
+        np.testing.assert_array_equal(got_o, cur_o)
+        np.testing.assert_array_equal(got_t, cur_t)
+
+
+def test_append_status_full_slab_and_mismatch():
+    w = gen.make_workload("tiny")
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, 4, seed=8)
+    idx, t, b, n = built(st, base, length, w.min_m, w.max_m)
+    commit = np.arange(8 * 6, dtype=np.int32).reshape(8, 6)
+    ncommit = np.array([0, 4, 5, 6, 1, 2, 3, 4], np.int32)          # 5 and 6 do not fit in 4 spare slots
+    status = host(idx.append(t, b, n, dev(cap), dev(commit), dev(ncommit)))
+    assert list(status) == [0, 0, 1, 1, 0, 0, 0, 0]
+    assert list(host(n)) == list(length + np.where(status == 0, ncommit, 0))
+    # the index was built for min_m = 4: other parameters fail their requests
+    status = host(pkg.lookup_index_append(t, b, n, dev(cap), dev(commit), dev(np.zeros(8, np.int32)), 3, 12,
+                                          idx.memory, idx.slots))
+    assert (status == 2).all()
+    d, ln, pos, m = pkg.lookup_index_draft(t, b, n, 3, 12, 15, idx.memory, idx.slots)
+    assert (host(ln) == pkg.LEN_FAILED).all()
+    # and the right parameters still work on the appended histories
+    t2, o2 = gen.csr_of_slabs(host(t), base, host(n))
+    check_draft(idx.draft(t, b, n, 15), oracle.lookup_draft(t2, o2, 4, 12, 15))
+
+
+def test_index_agrees_with_the_scan():
+    """The index and the scan kernel give the same drafts on the same histories."""
+    w = gen.make_workload("ragged262k")
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, 0, seed=9)
+    idx, t, b, n = built(st, base, length, w.min_m, w.max_m)
+    a = idx.draft(t, b, n, w.K)
+    s = pkg.lookup_draft_ex(dev(w.tokens), dev(w.offsets), w.min_m, w.max_m, w.K)
+    for x, y in zip(a, s):
+        np.testing.assert_array_equal(host(x), host(y))
+
+
+@pytest.mark.parametrize("period", [1, 2, 3, 5])
+def test_append_repeated_ngrams_in_one_call(period):
+    """Commits that repeat their own n-grams: several threads of one append
+    update the same slots at once (the contended path of the slot update)."""
+    rng = gen.rng_for(period, 51)
+    B, W = 24, 32
+    lengths = rng.integers(0, 300, size=B)
+    tokens = rng.integers(0, 20, size=int(lengths.sum())).astype(np.int32)
+    offsets = gen.offsets_from_lengths(lengths)
+    st, base, length, cap = gen.slabs_from_batch(tokens, offsets, 4 * W, seed=period)
+    idx, t, b, n = built(st, base, length, 4, 12)
+    cur_t, cur_o = tokens, offsets
+    for step in range(3):
+        pattern = rng.integers(0, 20, size=(B, period)).astype(np.int32)
+        commit = np.tile(pattern, (1, W // period + 1))[:, :W].astype(np.int32)
+        ncommit = rng.integers(W // 2, W + 1, size=B).astype(np.int32)
+        assert (host(idx.append(t, b, n, dev(cap), dev(commit), dev(ncommit))) == 0).all()
+        cur_t, cur_o = oracle.append(cur_t, cur_o, commit, ncommit)
+        got = idx.draft(t, b, n, 15, with_fallback=True)
+        check_draft(got, oracle.lookup_draft(cur_t, cur_o, 4, 12, 15))
+        assert host(got[4]).sum() == 0

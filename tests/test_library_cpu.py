@@ -41,7 +41,8 @@ def test_header_declares_the_entry_points():
     for must in ("lookup_draft", "lookup_draft_ex", "lookup_draft_scan", "lookup_draft_fill",
                  "lookup_draft_host", "lookup_draft_workspace_bytes", "lookup_draft_strerror",
                  "lookup_draft_last_cuda_error", "lookup_draft_set_wait_limit_ns", "lookup_draft_noalloc",
-                 "lookup_fuse", "lookup_schedule", "lookup_verify", "lookup_append"):
+                 "lookup_fuse", "lookup_schedule", "lookup_verify", "lookup_append", "lookup_index_slots_for",
+                 "lookup_index_bytes", "lookup_index_build", "lookup_index_append", "lookup_index_draft"):
         assert must in names
 
 
@@ -148,3 +149,32 @@ def test_loop_steps_empty_batch(lib):
     assert lib.lookup_fuse(None, None, None, None, 0, 15, 7, 8, 8, 6, 2, 4, None, None, None, None) == 0
     assert lib.lookup_schedule(None, None, 0, 7, 8, 4, 1, 2, 3, None, None, None) == 0
     assert lib.lookup_verify(None, None, None, None, None, None, None, 0, 15, None, None, None, None) == 0
+
+
+def test_index_sizes(lib):
+    # 2 * (12 - 4 + 1) * 1000 = 18000 -> 32768 slots; 128 + 16 * slots bytes
+    assert lib.lookup_index_slots_for(1000, 4, 12) == 32768
+    assert lib.lookup_index_slots_for(0, 4, 12) == 16
+    assert lib.lookup_index_slots_for(1000, 5, 4) == 0
+    assert lib.lookup_index_slots_for(1000, 4, 33) == 0
+    assert lib.lookup_index_bytes(32768) == 128 + 16 * 32768
+    assert lib.lookup_index_bytes(1000) == 0 and lib.lookup_index_bytes(8) == 0
+
+
+def test_index_rejects_bad_parameters(lib):
+    F = FAKE
+    # build: min_m > max_m, hash_bits 0, slots not a power of two, misaligned index
+    assert lib.lookup_index_build(F, F, F, 4, 5, 4, F, 1024, 64, None) == -1
+    assert lib.lookup_index_build(F, F, F, 4, 4, 12, F, 1024, 0, None) == -1
+    assert lib.lookup_index_build(F, F, F, 4, 4, 12, F, 1000, 64, None) == -1
+    assert lib.lookup_index_build(F, F, F, 4, 4, 12, F + 8, 1024, 64, None) == -1
+    # append: negative W, null cap
+    assert lib.lookup_index_append(F, F, F, F, F, F, 4, -1, 4, 12, F, 1024, 64, None, None) == -1
+    assert lib.lookup_index_append(F, F, F, None, F, F, 4, 16, 4, 12, F, 1024, 64, None, None) == -1
+    # draft: K above the limit, null index
+    assert lib.lookup_index_draft(F, F, F, 4, 4, 12, 65, F, 1024, 64, F, F, F, None, None, None) == -1
+    assert lib.lookup_index_draft(F, F, F, 4, 4, 12, 15, None, 1024, 64, F, F, F, None, None, None) == -1
+    # B == 0: append and draft enqueue nothing
+    assert lib.lookup_index_append(None, None, None, None, None, None, 0, 16, 4, 12, None, 1024, 64, None, None) == 0
+    assert lib.lookup_index_draft(None, None, None, 0, 4, 12, 15, None, 1024, 64, None, None, None, None, None,
+                                  None) == 0
