@@ -1,10 +1,13 @@
 """CPU oracle for prompt-lookup drafting -- TEST INFRASTRUCTURE ONLY.
 
-The oracle is ``lookup_oracle.c`` in this directory: a plain brute-force
-statement of one batched draft step (HyperQwen lookup-drafting article,
-section "第1步": longest current suffix of min_m..max_m tokens, its most recent
-earlier occurrence, overlap with the suffix allowed, the following tokens as
-the draft).  This module compiles it with gcc and calls it through ctypes.
+The oracle is plain C in this directory, compiled with gcc and called through
+ctypes:
+  lookup_oracle.c  one batched draft step, brute force (HyperQwen lookup-drafting
+                   article, section "第1步": longest current suffix of min_m..max_m
+                   tokens, its most recent earlier occurrence, overlap with the
+                   suffix allowed, the following tokens as the draft);
+  loop_oracle.c    the decode-loop steps around it ("第2步", "第3步");
+  ctx_oracle.c     context-cache drafting (llama.cpp prompt-lookup article).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
 legs of ``bench.py`` may import this package.  The CUDA library never does, and
@@ -27,7 +30,7 @@ from concurrent.futures import ThreadPoolExecutor
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRCS = [os.path.join(_HERE, "lookup_oracle.c"), os.path.join(_HERE, "loop_oracle.c")]
+_SRCS = [os.path.join(_HERE, f) for f in ("lookup_oracle.c", "loop_oracle.c", "ctx_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liblookup_oracle.so")
 
@@ -78,6 +81,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_verify.restype = ctypes.c_int
     lib.oracle_append.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp]
     lib.oracle_append.restype = ctypes.c_int
+    if hasattr(lib, "oracle_ctx_draft"):
+        lib.oracle_ctx_draft.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]
+        lib.oracle_ctx_draft.restype = ctypes.c_int
     return lib
 
 
@@ -231,3 +237,38 @@ def append(tokens, offsets, commit, ncommit, lib=None):
     if rc:
         raise ValueError("oracle_append rejected the arguments")
     return out_t, out_o
+
+
+# ----------------------------------------------------------- context cache ----
+def ctx_draft(tokens, offsets, K: int, n_min: int = 1, n_max: int = 4, min_count=(1, 1, 1, 1),
+              share=((1, 2), (1, 2), (1, 2), (1, 2)), threads: int = 1, lib=None):
+    """Context-cache drafting (llama.cpp prompt-lookup article): for each request,
+    up to K tokens, each the most frequent next token of the longest n-gram
+    (n_max .. n_min) of the context that passes the thresholds (count >=
+    min_count[n-1], share of the top next token >= share[n-1] = (num, den)).
+    Returns (draft [B, K] int32 (-1 past the end), len [B] int32)."""
+    lib = lib or load()
+    tk = np.ascontiguousarray(tokens, dtype=np.int32)
+    of = np.ascontiguousarray(offsets, dtype=np.int64)
+    B = int(of.shape[0]) - 1
+    mc = np.ascontiguousarray(min_count, dtype=np.int32)
+    num = np.ascontiguousarray([s[0] for s in share], dtype=np.int32)
+    den = np.ascontiguousarray([s[1] for s in share], dtype=np.int32)
+    draft = np.empty((max(B, 0), K), np.int32)
+    length = np.empty(max(B, 0), np.int32)
+    if B <= 0:
+        return draft, length
+
+    def run(lo, hi):
+        return lib.oracle_ctx_draft(_p(tk), _p(of), lo, hi, n_min, n_max, K, _p(mc), _p(num), _p(den),
+                                    _p(draft), _p(length))
+
+    if threads <= 1 or B == 1:
+        rcs = [run(0, B)]
+    else:
+        cuts = np.linspace(0, B, min(B, threads * 4) + 1).astype(int)
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            rcs = list(ex.map(lambda ab: run(int(ab[0]), int(ab[1])), zip(cuts[:-1], cuts[1:])))
+    if any(rcs):
+        raise ValueError("oracle_ctx_draft rejected the arguments")
+    return draft, length

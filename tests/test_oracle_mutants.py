@@ -22,6 +22,7 @@ from invariants import check_small
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "lookup_oracle.c")
 LOOP_SRC = os.path.join(os.path.dirname(oracle.__file__), "loop_oracle.c")
+CTX_SRC = os.path.join(os.path.dirname(oracle.__file__), "ctx_oracle.c")
 
 MUTANTS = {
     "oldest_first": ("for (int64_t p = L - m - 1; p >= 0; --p)",
@@ -102,7 +103,7 @@ def test_mutant_is_caught(name, tmp_path):
     so_path = tmp_path / "libmutant.so"
     c_path.write_text(mutated, encoding="utf-8")
     subprocess.run(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", "-o", str(so_path),
-                    str(c_path), LOOP_SRC], check=True)
+                    str(c_path), LOOP_SRC, CTX_SRC], check=True)
     failed = _pins_fail(oracle.load(str(so_path)))
     assert failed, f"mutant {name} passed every pin"
 
@@ -155,6 +156,66 @@ def test_loop_mutant_is_caught(name, tmp_path):
     c_path = tmp_path / "loop_mutant.c"
     so_path = tmp_path / "libloopmutant.so"
     c_path.write_text(src.replace(old, new, 1), encoding="utf-8")
-    subprocess.run(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", "-o", str(so_path), SRC, str(c_path)],
+    subprocess.run(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", "-o", str(so_path), SRC, str(c_path), CTX_SRC],
                    check=True)
     assert _loop_pins_fail(oracle.load(str(so_path))), f"mutant {name} passed every pin"
+
+
+# -------------------------------------------------- context-cache oracle ----
+
+CTX_MUTANTS = {
+    "tie_to_larger": ("if (b - a > best_c) {", "if (b - a >= best_c) {"),
+    "share_strict": ("if (best_c * (int64_t)den[n - 1] >= (int64_t)num[n - 1] * total) {",
+                     "if (best_c * (int64_t)den[n - 1] > (int64_t)num[n - 1] * total) {"),
+    "last_occurrence_dropped": ("for (int64_t i = 0; i + n <= L - 1; ++i) {",
+                                "for (int64_t i = 0; i + n <= L - 2; ++i) {"),
+    "shortest_first": ("for (int32_t n = n_max; n >= n_min && !accepted; --n) {",
+                       "for (int32_t n = n_min; n <= n_max && !accepted; ++n) {"),
+    "drafts_not_in_context": ("g[k] = c < L ? t[c] : draft[c - L];", "g[k] = t[c < L ? c : L - 1];"),
+    "min_count_ignored": ("if (total == 0 || total < min_count[n - 1])", "if (total == 0)"),
+    "share_ignored": ("if (best_c * (int64_t)den[n - 1] >= (int64_t)num[n - 1] * total) {", "if (1) {"),
+    "wrong_sentinel": ("draft[k] = -1;", "draft[k] = 0;"),
+    "successor_off_by_one": ("succ[total++] = t[i + n];", "succ[total++] = t[i + n - 1];"),
+}
+
+
+def _ctx_pins_fail(lib) -> list[str]:
+    import test_ctx_oracle_pins as pins
+    failed = []
+    saved = oracle.load
+    oracle.load = lambda path=None: lib
+    try:
+        for name in dir(pins):
+            if name.startswith("test_"):
+                fn = getattr(pins, name)
+                params = getattr(fn, "pytestmark", [])
+                cases = [{}]
+                for mark in params:
+                    if mark.name == "parametrize":
+                        argname, values = mark.args
+                        cases = [{argname: v} for v in values]
+                for kw in cases:
+                    try:
+                        fn(**kw)
+                    except (AssertionError, ValueError, Exception):  # noqa: B014 - any failure counts
+                        failed.append(f"{name}{kw}")
+    finally:
+        oracle.load = saved
+    return failed
+
+
+def test_unmutated_ctx_oracle_passes_its_pins():
+    assert _ctx_pins_fail(oracle.load()) == []
+
+
+@pytest.mark.parametrize("name", sorted(CTX_MUTANTS))
+def test_ctx_mutant_is_caught(name, tmp_path):
+    old, new = CTX_MUTANTS[name]
+    src = open(CTX_SRC, encoding="utf-8").read()
+    assert src.count(old) >= 1, f"mutation target for {name} not found in the context-cache oracle"
+    c_path = tmp_path / "ctx_mutant.c"
+    so_path = tmp_path / "libctxmutant.so"
+    c_path.write_text(src.replace(old, new, 1), encoding="utf-8")
+    subprocess.run(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", "-o", str(so_path), SRC, LOOP_SRC, str(c_path)],
+                   check=True)
+    assert _ctx_pins_fail(oracle.load(str(so_path))), f"mutant {name} passed every pin"
