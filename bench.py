@@ -30,6 +30,9 @@ requests of 25,000 tokens, 6.4 MB of int32 history).  Prints one JSON line.
   index         the incremental n-gram index on the same batch: build time and
                 size, the draft from the index (checked against the oracle), the
                 in-place append, and the decode-loop step on the index.
+  context_cache context-cache drafting (llama.cpp's rule) on the same batch:
+                build time and size, the draft (checked against the oracle) and
+                the in-place append.
 
 --impl reference times that oracle as the comparison arm on the same workload.
 Multi-GPU (torchrun, one rank per GPU): every rank drafts its own batch (weak
@@ -82,6 +85,7 @@ def parse_args(argv=None):
                     help="skip the timing of the decode-loop steps (fusion, scheduling, verification, append)")
     ap.add_argument("--no-index", action="store_true",
                     help="skip the timing of the incremental n-gram index")
+    ap.add_argument("--no-ctx", action="store_true", help="skip the timing of context-cache drafting")
     ap.add_argument("--loop-only", action="store_true",
                     help="time only the decode-loop steps (replays = steps / copies of the batch)")
     return ap.parse_args(argv)
@@ -252,13 +256,14 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
             import oracle
             want = oracle.lookup_draft(w.tokens, w.offsets, min_m, max_m, K, threads=os.cpu_count() or 1)
             index = measure_index(lib, pkg, w, dev, stream, want)
+        ctx = None if args.no_ctx else measure_ctx(lib, pkg, w, dev, stream)
         if rank == 0:
             print(json.dumps({"metric": "µs per decode-loop step (draft, schedule, fuse, verify, append)",
                               "value": loop["loop_step_us"], "unit": "us/step", "n_gpus": world,
                               "higher_is_better": False, "data": "synthetic",
                               "config": {"workload": args.workload, "B": B, "history_tokens": w.total_tokens,
                                          "seed": seed},
-                              "loop_steps": loop, "index": index}), flush=True)
+                              "loop_steps": loop, "index": index, "context_cache": ctx}), flush=True)
         if dist is not None:
             dist.destroy_process_group()
         return
@@ -382,6 +387,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         import oracle
         want = oracle.lookup_draft(w.tokens, w.offsets, min_m, max_m, K, threads=os.cpu_count() or 1)
         index = measure_index(lib, pkg, w, dev, stream, want)
+    ctx = None if args.no_ctx else measure_ctx(lib, pkg, w, dev, stream)
 
     # e2e: host buffers through lookup_draft_host, copies inside every step
     h_tok = tok_host.pin_memory()
@@ -473,6 +479,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         "cpu_baseline": cpu,
         "loop_steps": loop,
         "index": index,
+        "context_cache": ctx,
         "gpu_launches": 2 * args.steps,
         "parity_with_oracle": bool(parity),
         "clocks": clocks.summary(),
@@ -758,6 +765,84 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
                   "CUDA events on the launching stream",
     }
     del idx
+    return res
+
+
+# -------------------------------------------------------- context cache ----
+CTX_K = 8                        # context-cache drafts per request
+
+
+def measure_ctx(lib, pkg, w, dev, stream) -> dict:
+    """Context-cache drafting on the bench's batch (slabs with INDEX_SPARE tokens
+    of room): build time, size, the draft of up to CTX_K tokens (checked against
+    the oracle), and the in-place append of 8 committed tokens per request."""
+    import numpy as np
+    import torch
+
+    import gen
+    import oracle
+
+    B = w.B
+    i32 = torch.int32
+    st, base_h, len_h, cap_h = gen.slabs_from_batch(w.tokens, w.offsets, INDEX_SPARE, seed=w.seed)
+    tokens = torch.from_numpy(st).to(dev)
+    base = torch.from_numpy(base_h).to(dev)
+    length = torch.from_numpy(len_h).to(dev)
+    cap = torch.from_numpy(cap_h).to(dev)
+    cc = pkg.ContextCache(st.shape[0], 1, 4, device=dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    builds = []
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            cc.build(tokens, base, length, stream=stream)
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        builds.append(ev0.elapsed_time(ev1))
+    draft = torch.empty((B, CTX_K), dtype=i32, device=dev)
+    dlen = torch.empty(B, dtype=i32, device=dev)
+    with torch.cuda.stream(stream):
+        cc.draft(tokens, base, length, CTX_K, out=(draft, dlen), stream=stream)
+    torch.cuda.synchronize(dev)
+    wd, wl = oracle.ctx_draft(w.tokens, w.offsets, CTX_K, threads=os.cpu_count() or 1)
+    parity = bool(np.array_equal(draft.cpu().numpy(), wd) and np.array_equal(dlen.cpu().numpy(), wl))
+
+    def timed(fn, per_graph: int, reps: int) -> float:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(per_graph):
+                fn()
+        with torch.cuda.stream(stream):
+            g.replay()
+            ev0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        return 1000.0 * ev0.elapsed_time(ev1) / (reps * per_graph)
+
+    draft_us = timed(lambda: cc.draft(tokens, base, length, CTX_K, out=(draft, dlen), stream=stream), 32, 20)
+    rng = gen.rng_for(w.seed, 502)
+    commit = torch.from_numpy(rng.integers(0, 50, size=(B, 8)).astype(np.int32)).to(dev)
+    n8 = torch.full((B,), 8, dtype=i32, device=dev)
+    status = torch.empty(B, dtype=i32, device=dev)
+    append_us = timed(lambda: cc.append(tokens, base, length, cap, commit, n8, status=status, stream=stream), 16, 3)
+    torch.cuda.synchronize(dev)
+    res = {
+        "n_range": [1, 4], "K": CTX_K, "thresholds": "count >= 1, top next token >= 1/2, every n",
+        "cache_bytes": int(cc.memory.numel()),
+        "cache_bytes_per_token": round(cc.memory.numel() / st.shape[0], 1),
+        "build_ms": round(statistics.median(builds), 3),
+        "draft_us": round(draft_us, 3),
+        "mean_draft_len": round(float(wl.mean()), 3),
+        "append8_us": round(append_us, 3),
+        "parity_with_oracle": parity,
+        "appends_fit": bool((status == 0).all().item()),
+        "method": "calls captured back to back in CUDA graphs (32 drafts, 16 appends per graph), "
+                  "CUDA events on the launching stream",
+    }
+    del cc
     return res
 
 

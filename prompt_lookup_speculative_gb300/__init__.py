@@ -1,8 +1,9 @@
 """GB300 prompt-lookup (n-gram) speculative drafting.
 
 Python binding of the C ABI in ``include/lookup_draft.h``,
-``include/lookup_loop.h`` and ``include/lookup_index.h`` (ctypes; argument
-marshalling only -- every step runs in the library's CUDA kernels).
+``include/lookup_loop.h``, ``include/lookup_index.h`` and
+``include/lookup_ctxcache.h`` (ctypes; argument marshalling only -- every step
+runs in the library's CUDA kernels).
 PyTorch tensors supply device memory and the current CUDA stream.
 
     draft, length, pos = lookup_draft(tokens, offsets, min_m=4, max_m=12, K=15)
@@ -28,7 +29,7 @@ __all__ = [
     "lookup_draft_scan", "lookup_draft_fill", "lookup_draft_noalloc", "workspace_bytes",
     "set_wait_limit_ns", "lookup_fuse", "lookup_schedule", "lookup_verify", "lookup_append",
     "NgramIndex", "index_slots_for", "index_bytes", "lookup_index_build", "lookup_index_append",
-    "lookup_index_draft",
+    "lookup_index_draft", "ContextCache",
     "MAX_M", "MAX_K", "LEN_FAILED",
 ]
 
@@ -113,6 +114,16 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.lookup_index_append.restype = ctypes.c_int
     lib.lookup_index_draft.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, i64, i32, vp, vp, vp, vp, vp, vp]
     lib.lookup_index_draft.restype = ctypes.c_int
+    lib.lookup_ctx_slots_for.argtypes = [i64, i32, i32]
+    lib.lookup_ctx_slots_for.restype = i64
+    lib.lookup_ctx_bytes.argtypes = [i64]
+    lib.lookup_ctx_bytes.restype = sz
+    lib.lookup_ctx_build.argtypes = [vp, vp, vp, i32, i32, i32, vp, i64, vp]
+    lib.lookup_ctx_build.restype = ctypes.c_int
+    lib.lookup_ctx_append.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, i64, vp, vp]
+    lib.lookup_ctx_append.restype = ctypes.c_int
+    lib.lookup_ctx_draft.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, i64, vp, vp, vp]
+    lib.lookup_ctx_draft.restype = ctypes.c_int
 
 
 def _check(rc: int, lib) -> None:
@@ -522,3 +533,78 @@ class NgramIndex:
     def draft(self, tokens, base, length, K: int = 15, out=None, with_fallback: bool = False, stream=None):
         return lookup_index_draft(tokens, base, length, self.min_m, self.max_m, K, self.memory, self.slots,
                                   self.hash_bits, out, with_fallback, stream)
+
+
+# ---------------------------------------------------------- context cache ----
+class ContextCache:
+    """Context-cache drafting (include/lookup_ctxcache.h): n-gram statistics of
+    the slab histories, n in [n_min, n_max] (1..4), on the device.
+
+    min_count and share ((num, den) per n, index n - 1) are the acceptance
+    thresholds; the defaults take the llama.cpp article's 4-gram example (seen at
+    least once, the top next token at least half of the time) for every n.
+    """
+
+    def __init__(self, capacity_tokens: int, n_min: int = 1, n_max: int = 4, device=None, slots: int | None = None,
+                 min_count=(1, 1, 1, 1), share=((1, 2), (1, 2), (1, 2), (1, 2))):
+        import torch
+        lib = load_library()
+        self.n_min, self.n_max = n_min, n_max
+        self.slots = int(slots) if slots is not None else int(lib.lookup_ctx_slots_for(int(capacity_tokens), n_min,
+                                                                                      n_max))
+        nbytes = int(lib.lookup_ctx_bytes(self.slots))
+        if nbytes == 0:
+            raise ValueError("invalid context-cache parameters")
+        self.memory = torch.empty(nbytes, dtype=torch.uint8,
+                                  device=device if device is not None else torch.cuda.current_device())
+        self.set_thresholds(min_count, share)
+
+    def set_thresholds(self, min_count, share) -> None:
+        import numpy as np
+        self._mc = np.ascontiguousarray(min_count, dtype=np.int32)
+        self._num = np.ascontiguousarray([s[0] for s in share], dtype=np.int32)
+        self._den = np.ascontiguousarray([s[1] for s in share], dtype=np.int32)
+        if self._mc.shape != (4,) or self._num.shape != (4,) or self._den.shape != (4,):
+            raise ValueError("min_count and share need 4 entries (n = 1..4)")
+
+    def build(self, tokens, base, length, stream=None) -> None:
+        import torch
+        lib = load_library()
+        dev, B, (bp, lp) = _slab_args(tokens, base, length)
+        with torch.cuda.device(dev):
+            rc = lib.lookup_ctx_build(tokens.data_ptr(), bp, lp, B, self.n_min, self.n_max, self.memory.data_ptr(),
+                                      self.slots, _stream_handle(stream))
+        _check(rc, lib)
+
+    def append(self, tokens, base, length, cap, commit, ncommit, status=None, stream=None):
+        import torch
+        lib = load_library()
+        dev, B, (bp, lp, cp) = _slab_args(tokens, base, length, cap)
+        W = commit.shape[1]
+        cm = _dev(commit, torch.int32, (B, W), dev, "commit")
+        nc = _dev(ncommit, torch.int32, (B,), dev, "ncommit")
+        if status is None:
+            status = torch.empty(B, dtype=torch.int32, device=dev)
+        sp = _dev(status, torch.int32, (B,), dev, "status")
+        with torch.cuda.device(dev):
+            rc = lib.lookup_ctx_append(tokens.data_ptr(), bp, lp, cp, cm, nc, B, W, self.n_min, self.n_max,
+                                       self.memory.data_ptr(), self.slots, sp, _stream_handle(stream))
+        _check(rc, lib)
+        return status
+
+    def draft(self, tokens, base, length, K: int = 8, out=None, stream=None):
+        """Returns (draft [B, K] int32, -1 past the end; len [B] int32)."""
+        import torch
+        lib = load_library()
+        dev, B, (bp, lp) = _slab_args(tokens, base, length)
+        if out is None:
+            out = (torch.empty((B, K), dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev))
+        d, ln = out
+        dp = _dev(d, torch.int32, (B, K), dev, "draft")
+        lnp = _dev(ln, torch.int32, (B,), dev, "len")
+        with torch.cuda.device(dev):
+            rc = lib.lookup_ctx_draft(tokens.data_ptr(), bp, lp, B, self.n_min, self.n_max, K, self._mc.ctypes.data,
+                                      self._num.ctypes.data, self._den.ctypes.data, self.memory.data_ptr(),
+                                      self.slots, dp, lnp, _stream_handle(stream))
+        _check(rc, lib)
+        return d, ln

@@ -1,0 +1,79 @@
+// common.cuh -- device and host helpers shared by the library's kernels (private).
+#pragma once
+
+#include "lookup_draft.h"
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+// Records a CUDA failure for lookup_draft_last_cuda_error (lookup_draft.cu);
+// returns LOOKUP_DRAFT_ECUDA.
+int lookup_record_cuda_error(cudaError_t e, const char *what);
+
+namespace lkd {
+
+// Programmatic dependent launch: wait for the previous kernel on the stream
+// (its writes visible), and let the next one start launching.
+__device__ inline void wait_for_prerequisite_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ inline void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// splitmix64's output mix (Steele, Lea and Flood, "Fast splittable pseudorandom
+// number generators", OOPSLA 2014).
+__device__ inline uint64_t mix64(uint64_t x) {
+    x ^= x >> 30;
+    x *= 0xbf58476d1ce4e5b9ull;
+    x ^= x >> 27;
+    x *= 0x94d049bb133111ebull;
+    x ^= x >> 31;
+    return x;
+}
+
+// 128-bit compare-and-swap at a 16-byte aligned global address (atom.cas.b128,
+// sm_90 and later); returns the previous 128 bits.
+__device__ inline void cas128(void *addr, uint64_t cmp_lo, uint64_t cmp_hi, uint64_t new_lo, uint64_t new_hi,
+                              uint64_t &old_lo, uint64_t &old_hi) {
+    asm volatile(
+        "{\n\t.reg .b128 d, c, v;\n\t"
+        "mov.b128 c, {%2, %3};\n\t"
+        "mov.b128 v, {%4, %5};\n\t"
+        "atom.global.cas.b128 d, [%6], c, v;\n\t"
+        "mov.b128 {%0, %1}, d;\n\t}"
+        : "=l"(old_lo), "=l"(old_hi)
+        : "l"(cmp_lo), "l"(cmp_hi), "l"(new_lo), "l"(new_hi), "l"(addr)
+        : "memory");
+}
+
+// Host: launch with programmatic stream serialization allowed.
+template <typename Params>
+inline int launch_pdl(void (*kernel)(Params), unsigned grid, unsigned block, cudaStream_t stream, const Params &prm) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
+    return e == cudaSuccess ? LOOKUP_DRAFT_OK : lookup_record_cuda_error(e, "kernel launch");
+}
+
+inline int sm_count(int *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
+    return e == cudaSuccess ? LOOKUP_DRAFT_OK : lookup_record_cuda_error(e, "device query");
+}
+
+inline bool pow2_at_least(int64_t x, int64_t lo) { return x >= lo && (x & (x - 1)) == 0; }
+
+inline unsigned capped_grid(int64_t want, int64_t cap) {
+    if (want < 1) want = 1;
+    return unsigned(want < cap ? want : cap);
+}
+
+}  // namespace lkd

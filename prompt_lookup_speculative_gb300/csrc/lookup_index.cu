@@ -28,17 +28,18 @@
 // not check out has been shared with another key, and the request is answered
 // by a warp brute-force scan instead, so the result never depends on the hash.
 
-#include "lookup_draft.h"
 #include "lookup_index.h"
 
-#include <cuda_runtime.h>
-
-#include <cstdint>
-#include <cstring>
-
-int lookup_record_cuda_error(cudaError_t e, const char *what);
+#include "common.cuh"
 
 namespace {
+
+using lkd::allow_dependent_launch;
+using lkd::cas128;
+using lkd::launch_pdl;
+using lkd::mix64;
+using lkd::sm_count;
+using lkd::wait_for_prerequisite_grid;
 
 constexpr uint32_t kMagic = 0x4c4b4958u;        // "LKIX"
 constexpr int kBucket = 2;                      // slots per bucket: one 32-byte sector
@@ -62,20 +63,6 @@ struct __align__(16) Slot {
     int top1, top2;
 };
 static_assert(sizeof(Slot) == 16, "slot is 16 bytes");
-
-__device__ inline void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ inline void wait_for_prerequisite_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// splitmix64's output mix (Steele, Lea and Flood, "Fast splittable pseudorandom
-// number generators", OOPSLA 2014).
-__device__ inline uint64_t mix64(uint64_t x) {
-    x ^= x >> 30;
-    x *= 0xbf58476d1ce4e5b9ull;
-    x ^= x >> 27;
-    x *= 0x94d049bb133111ebull;
-    x ^= x >> 31;
-    return x;
-}
 
 __device__ inline uint64_t seed_of(int r) { return mix64(uint64_t(uint32_t(r)) * 0x9e3779b97f4a7c15ull + 0x632be59bd9b4e019ull); }
 __device__ inline uint64_t step_hash(uint64_t h, int32_t tok) { return mix64(h ^ uint64_t(uint32_t(tok))); }
@@ -131,19 +118,10 @@ __device__ inline bool insert(Slot *tab, int64_t bmask, unsigned long long key, 
     return false;
 }
 
-// 128-bit compare-and-swap of a whole slot (atom.cas.b128, sm_90 and later):
-// returns the slot's previous contents.
+// 128-bit compare-and-swap of a whole slot: returns its previous contents.
 __device__ inline void cas_slot(Slot *s, uint64_t cmp_lo, uint64_t cmp_hi, uint64_t new_lo, uint64_t new_hi,
                                 uint64_t &old_lo, uint64_t &old_hi) {
-    asm volatile(
-        "{\n\t.reg .b128 d, c, v;\n\t"
-        "mov.b128 c, {%2, %3};\n\t"
-        "mov.b128 v, {%4, %5};\n\t"
-        "atom.global.cas.b128 d, [%6], c, v;\n\t"
-        "mov.b128 {%0, %1}, d;\n\t}"
-        : "=l"(old_lo), "=l"(old_hi)
-        : "l"(cmp_lo), "l"(cmp_hi), "l"(new_lo), "l"(new_hi), "l"(s)
-        : "memory");
+    cas128(s, cmp_lo, cmp_hi, new_lo, new_hi, old_lo, old_hi);
 }
 
 __device__ inline uint64_t pack_tops(int top1, int top2) { return uint64_t(uint32_t(top1)) | (uint64_t(uint32_t(top2)) << 32); }
@@ -552,29 +530,6 @@ __global__ void __launch_bounds__(kWarpThreads) index_draft_kernel(DraftParams p
 }
 
 // ------------------------------------------------------------------- host ----
-template <typename Params>
-int launch_pdl(void (*kernel)(Params), unsigned grid, unsigned block, cudaStream_t stream, const Params &prm) {
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(block);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
-    return e == cudaSuccess ? LOOKUP_DRAFT_OK : lookup_record_cuda_error(e, "kernel launch");
-}
-
-int sm_count(int *out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
-    return e == cudaSuccess ? LOOKUP_DRAFT_OK : lookup_record_cuda_error(e, "device query");
-}
-
 bool pow2(int64_t x) { return x >= 16 && (x & (x - 1)) == 0; }
 
 bool params_ok(int32_t min_m, int32_t max_m, int32_t hash_bits, int64_t slots) {

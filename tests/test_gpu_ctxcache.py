@@ -1,0 +1,139 @@
+"""GPU parity of context-cache drafting (include/lookup_ctxcache.h) with the oracle.
+
+Exact comparison of every draft token and length, after a build and after every
+append of a decode loop, for several thresholds and n ranges, on the workloads
+and on small-alphabet streams where ties and thresholds decide often.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import gen
+import oracle
+
+torch = pytest.importorskip("torch")
+pkg = pytest.importorskip("prompt_lookup_speculative_gb300")
+
+pytestmark = pytest.mark.gpu
+
+SHARE_HALF = ((1, 2),) * 4
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def setup(tokens, offsets, spare, seed, n_min=1, n_max=4, **kw):
+    st, base, length, cap = gen.slabs_from_batch(tokens, offsets, spare, seed=seed)
+    t, b, n = dev(st), dev(base), dev(length)
+    cc = pkg.ContextCache(st.shape[0], n_min, n_max, **kw)
+    cc.build(t, b, n)
+    return cc, st, base, length, cap, t, b, n
+
+
+def check(cc, t, b, n, tokens, offsets, K, n_min=1, n_max=4, min_count=(1, 1, 1, 1), share=SHARE_HALF):
+    d, ln = cc.draft(t, b, n, K)
+    wd, wl = oracle.ctx_draft(tokens, offsets, K, n_min=n_min, n_max=n_max, min_count=min_count, share=share,
+                              threads=16)
+    np.testing.assert_array_equal(host(ln), wl)
+    np.testing.assert_array_equal(host(d), wd)
+    return wl
+
+
+@pytest.mark.parametrize("name", gen.WORKLOADS)
+def test_ctx_draft_matches_oracle(name):
+    w = gen.make_workload(name)
+    cc, st, base, length, cap, t, b, n = setup(w.tokens, w.offsets, 16, w.seed)
+    lens = check(cc, t, b, n, w.tokens, w.offsets, 8)
+    if name in ("tiny", "recitation25k", "periodic"):
+        assert lens.sum() > 0
+
+
+def small_alphabet_batch(seed, B=200, vocab=6, Lmax=400):
+    rng = gen.rng_for(seed, 61)
+    lengths = rng.integers(0, Lmax, size=B)
+    tokens = rng.integers(0, vocab, size=int(lengths.sum())).astype(np.int32)
+    return tokens, gen.offsets_from_lengths(lengths)
+
+
+@pytest.mark.parametrize("params", [
+    dict(),
+    dict(min_count=(2, 2, 2, 2)),
+    dict(min_count=(5, 3, 2, 1), share=((2, 3), (3, 5), (1, 2), (1, 1))),
+    dict(share=((0, 1),) * 4),
+    dict(n_min=2, n_max=3),
+    dict(n_min=4, n_max=4),
+    dict(n_min=1, n_max=1),
+])
+@pytest.mark.parametrize("vocab", [2, 6, 40])
+def test_ctx_thresholds_and_ranges(params, vocab):
+    tokens, offsets = small_alphabet_batch(vocab, vocab=vocab)
+    n_min, n_max = params.get("n_min", 1), params.get("n_max", 4)
+    mc = params.get("min_count", (1, 1, 1, 1))
+    share = params.get("share", SHARE_HALF)
+    cc, st, base, length, cap, t, b, n = setup(tokens, offsets, 0, 2, n_min, n_max, min_count=mc, share=share)
+    check(cc, t, b, n, tokens, offsets, 12, n_min, n_max, mc, share)
+
+
+@pytest.mark.parametrize("K", [0, 1, 64])
+def test_ctx_draft_lengths(K):
+    tokens, offsets = small_alphabet_batch(7, vocab=3)
+    cc, st, base, length, cap, t, b, n = setup(tokens, offsets, 0, 3)
+    check(cc, t, b, n, tokens, offsets, K)
+
+
+@pytest.mark.parametrize("name,vocab", [("tiny", None), ("chats", None), ("small", 4)])
+def test_ctx_decode_loop(name, vocab):
+    """Draft, commit a synthetic continuation (an accepted prefix of the draft,
+    then one more token), append in place, compare with the oracle each step."""
+    if name == "small":
+        tokens, offsets = small_alphabet_batch(11, B=300, vocab=vocab)
+    else:
+        w = gen.make_workload(name)
+        tokens, offsets = w.tokens, w.offsets
+    B = offsets.shape[0] - 1
+    W, K = 9, 8
+    cc, st, base, length, cap, t, b, n = setup(tokens, offsets, 6 * W, 4)
+    capd = dev(cap)
+    rng = gen.rng_for(B, 62)
+    cur_t, cur_o = tokens, offsets
+    for step in range(5):
+        d, ln = cc.draft(t, b, n, K)
+        wd, wl = oracle.ctx_draft(cur_t, cur_o, K, threads=16)
+        np.testing.assert_array_equal(host(ln), wl)
+        np.testing.assert_array_equal(host(d), wd)
+        acc = np.minimum(rng.integers(0, K + 1, size=B), wl)
+        commit = rng.integers(0, vocab or 50, size=(B, W)).astype(np.int32)
+        for r in range(B):
+            commit[r, :acc[r]] = wd[r, :acc[r]]
+        ncommit = (acc + 1).astype(np.int32)
+        assert (host(cc.append(t, b, n, capd, dev(commit), dev(ncommit))) == 0).all()
+        cur_t, cur_o = oracle.append(cur_t, cur_o, commit, ncommit)
+        got_t, got_o = gen.csr_of_slabs(host(t), base, host(n))
+        np.testing.assert_array_equal(got_o, cur_o)
+        np.testing.assert_array_equal(got_t, cur_t)
+
+
+def test_ctx_status_mismatch_and_overflow():
+    tokens, offsets = small_alphabet_batch(13, B=20, vocab=5)
+    cc, st, base, length, cap, t, b, n = setup(tokens, offsets, 3, 5)
+    commit = np.arange(20 * 5, dtype=np.int32).reshape(20, 5) % 5
+    ncommit = np.array([4, 3] * 10, np.int32)                      # 4 does not fit in 3 spare slots
+    status = host(cc.append(t, b, n, dev(cap), dev(commit), dev(ncommit)))
+    assert list(status) == [1, 0] * 10
+    # a cache queried with other lengths fails its requests
+    other = pkg.ContextCache(10, 2, 4, slots=cc.slots)
+    other.memory = cc.memory
+    d, ln = other.draft(t, b, n, 4)
+    assert (host(ln) == pkg.LEN_FAILED).all()
+    # a table far too small overflows: every request reports the failure
+    small = pkg.ContextCache(st.shape[0], 1, 4, slots=64)
+    small.build(t, b, n)
+    d, ln = small.draft(t, b, n, 4)
+    assert (host(ln) == pkg.LEN_FAILED).all()

@@ -42,7 +42,9 @@ def test_header_declares_the_entry_points():
                  "lookup_draft_host", "lookup_draft_workspace_bytes", "lookup_draft_strerror",
                  "lookup_draft_last_cuda_error", "lookup_draft_set_wait_limit_ns", "lookup_draft_noalloc",
                  "lookup_fuse", "lookup_schedule", "lookup_verify", "lookup_append", "lookup_index_slots_for",
-                 "lookup_index_bytes", "lookup_index_build", "lookup_index_append", "lookup_index_draft"):
+                 "lookup_index_bytes", "lookup_index_build", "lookup_index_append", "lookup_index_draft",
+                 "lookup_ctx_slots_for", "lookup_ctx_bytes", "lookup_ctx_build", "lookup_ctx_append",
+                 "lookup_ctx_draft"):
         assert must in names
 
 
@@ -178,3 +180,23 @@ def test_index_rejects_bad_parameters(lib):
     assert lib.lookup_index_append(None, None, None, None, None, None, 0, 16, 4, 12, None, 1024, 64, None, None) == 0
     assert lib.lookup_index_draft(None, None, None, 0, 4, 12, 15, None, 1024, 64, None, None, None, None, None,
                                   None) == 0
+
+
+def test_ctx_sizes_and_argument_checks(lib):
+    import numpy as np
+    assert lib.lookup_ctx_slots_for(1000, 1, 4) == 16384          # 4 * 4 * 1000 = 16000 -> 16384
+    assert lib.lookup_ctx_slots_for(1000, 0, 4) == 0 and lib.lookup_ctx_slots_for(1000, 1, 5) == 0
+    assert lib.lookup_ctx_bytes(16384) == 128 + 32 * 16384 and lib.lookup_ctx_bytes(100) == 0
+    F = FAKE
+    mc = np.ones(4, np.int32)
+    num = np.ones(4, np.int32)
+    den = np.full(4, 2, np.int32)
+    bad_den = np.zeros(4, np.int32)
+    args = (mc.ctypes.data, num.ctypes.data)
+    assert lib.lookup_ctx_build(F, F, F, 4, 2, 1, F, 1024, None) == -1                 # n_min > n_max
+    assert lib.lookup_ctx_build(F, F, F, 70000, 1, 4, F, 1024, None) == -1             # B above 65536
+    assert lib.lookup_ctx_draft(F, F, F, 4, 1, 4, 8, *args, bad_den.ctypes.data, F, 1024, F, F, None) == -1
+    assert lib.lookup_ctx_draft(F, F, F, 4, 1, 4, 65, *args, den.ctypes.data, F, 1024, F, F, None) == -1
+    assert lib.lookup_ctx_draft(None, None, None, 0, 1, 4, 8, *args, den.ctypes.data, None, 1024, None, None,
+                                None) == 0
+    assert lib.lookup_ctx_append(F, F, F, F, F, F, 4, -1, 1, 4, F, 1024, None, None) == -1
