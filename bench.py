@@ -757,7 +757,7 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
         "draft_us": round(draft_us, 3),
         "append8_us": round(append_us, 3),
         "loop_step_us": round(loop_us, 3),
-        "loop_step_launches": 5,
+        "loop_step_launches": 6,
         "parity_with_oracle": bool(parity),
         "fallback_requests": fallbacks,
         "appends_fit": room_ok,
