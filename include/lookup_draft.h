@@ -131,9 +131,11 @@ int lookup_draft_fill(const int32_t *tokens, const int64_t *offsets, int32_t B,
 /*
  * lookup_draft on HOST buffers: copies tokens[offsets[0] .. offsets[B]) and the
  * offsets to the current device (stream-ordered scratch from the library pool),
- * runs the step on `stream`, copies the outputs back into the host arrays and
- * synchronises the stream before returning.  Pinned host memory gives the
- * fastest copies; pageable memory works.  The host offsets are checked
+ * runs the step on `stream`, delivers the outputs into the host arrays and
+ * synchronises the stream before returning.  Page-locked output arrays that the
+ * device can address (cudaHostAlloc / cudaHostRegister memory) are written by
+ * the draft-fill kernel directly; other host memory receives the outputs by
+ * copies.  Pinned host memory gives the fastest copies; pageable memory works.  The host offsets are checked
  * (non-decreasing, offsets[0] >= 0, every history < 2^31 tokens):
  * LOOKUP_DRAFT_EINVAL if not.
  */

@@ -648,6 +648,19 @@ int cuda_fail(cudaError_t e, const char *what) {
 
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 
+// The device address of page-locked host memory the device can write, else
+// nullptr (pageable or unknown memory).
+int32_t *mapped_host(int32_t *p) {
+    if (!p) return nullptr;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();                              // clear the error state of the query
+        return nullptr;
+    }
+    if (a.type != cudaMemoryTypeHost || !a.devicePointer) return nullptr;
+    return static_cast<int32_t *>(a.devicePointer);
+}
+
 struct DeviceState {
     bool ready = false;
     int sms = 0;
@@ -958,6 +971,15 @@ int lookup_draft_host(const int32_t *h_tokens, const int64_t *h_offsets, int32_t
     int32_t *d_draft = d_out;
     int32_t *d_len = d_out + size_t(B) * size_t(K);
     int32_t *d_pos = d_len + B;
+    // Page-locked, device-mapped output buffers are written by the fill kernel
+    // directly (no copies back); any other host memory gets them by copies.
+    int32_t *m_draft = mapped_host(h_out_draft), *m_len = mapped_host(h_out_len), *m_pos = mapped_host(h_out_pos);
+    const bool direct = m_len && m_pos && (K == 0 || m_draft);
+    if (direct) {
+        d_draft = K > 0 ? m_draft : d_draft;
+        d_len = m_len;
+        d_pos = m_pos;
+    }
     // The device copy holds tokens[first .. end); index it with the caller's offsets
     // through a base pointer moved back by `first` elements (never dereferenced there).
     const int32_t *d_tok_base =
@@ -973,11 +995,11 @@ int lookup_draft_host(const int32_t *h_tokens, const int64_t *h_offsets, int32_t
     } else {
         rc = cuda_fail(e, "cudaMemcpyAsync (host to device)");
     }
-    if (rc == LOOKUP_DRAFT_OK && K > 0)
+    if (rc == LOOKUP_DRAFT_OK && !direct && K > 0)
         e = cudaMemcpyAsync(h_out_draft, d_draft, size_t(B) * size_t(K) * 4, cudaMemcpyDeviceToHost, stream);
-    if (rc == LOOKUP_DRAFT_OK && e == cudaSuccess)
+    if (rc == LOOKUP_DRAFT_OK && !direct && e == cudaSuccess)
         e = cudaMemcpyAsync(h_out_len, d_len, size_t(B) * 4, cudaMemcpyDeviceToHost, stream);
-    if (rc == LOOKUP_DRAFT_OK && e == cudaSuccess)
+    if (rc == LOOKUP_DRAFT_OK && !direct && e == cudaSuccess)
         e = cudaMemcpyAsync(h_out_pos, d_pos, size_t(B) * 4, cudaMemcpyDeviceToHost, stream);
     if (rc == LOOKUP_DRAFT_OK && e != cudaSuccess) rc = cuda_fail(e, "cudaMemcpyAsync (device to host)");
     cudaError_t fe = cudaFreeAsync(buf, stream);

@@ -218,6 +218,25 @@ def test_host_entry_point():
     np.testing.assert_array_equal(p, op)
 
 
+@pytest.mark.parametrize("pinned", ["all", "some", "none"])
+def test_host_entry_point_pinned_outputs(pinned):
+    """Page-locked outputs are written by the fill kernel directly; mixed or
+    pageable outputs go through copies.  Same results either way."""
+    w = gen.make_workload("recitation25k", 15)
+    B, K = w.B, w.K
+    def buf(shape, pin):
+        t = torch.full(shape, -77, dtype=torch.int32)
+        return t.pin_memory() if pin else t
+    out = (buf((B, K), pinned != "none"), buf((B,), pinned == "all"), buf((B,), pinned != "none"))
+    tok = torch.from_numpy(w.tokens).pin_memory()
+    off = torch.from_numpy(w.offsets).pin_memory()
+    d, ln, p = pkg.lookup_draft_host(tok, off, w.min_m, w.max_m, K, out=out)
+    od, oln, op, _ = oracle.lookup_draft(w.tokens, w.offsets, w.min_m, w.max_m, K, threads=8)
+    np.testing.assert_array_equal(d.numpy(), od)
+    np.testing.assert_array_equal(ln.numpy(), oln)
+    np.testing.assert_array_equal(p.numpy(), op)
+
+
 def test_host_entry_point_offset_base():
     tokens = np.array([9, 9, 9, 1, 2, 3, 1, 2, 3, 1, 2], dtype=np.int32)
     offsets = np.array([3, 3, 11], dtype=np.int64)
