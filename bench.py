@@ -191,9 +191,16 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+HOST_SIDE_MARKER = b"// ------------------------------------------------------------- host side ----"
+
+
 def scan_source_hash() -> str:
+    """sha256 (16 hex) of the device code of csrc/lookup_draft.cu: the file up to
+    its host-side marker, so host-only edits keep a kernel capture valid."""
     with open(SCAN_SOURCE, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+        src = f.read()
+    cut = src.find(HOST_SIDE_MARKER)
+    return hashlib.sha256(src if cut < 0 else src[:cut]).hexdigest()[:16]
 
 
 def recorded_traffic(workload: str):
