@@ -473,8 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
             const int eb = base > wbeg ? base : wbeg;
             const int ee = (base + 4 * nq < wend) ? base + 4 * nq : wend;
 
-            // Candidate ends [lo, hi] (tile elements) of the current request: the
-            // D-token test on every whole quad, the rest element by element.
+            // Candidate ends [lo, hi] (tile elements, whole quads: lo and hi + 1 are
+            // multiples of 4) of the current request: the D-token test on every quad.
             auto scan_range = [&](int lo, int hi) {
                 const int qoff = base - cur_o;           // local position of st[0] in the request
                 // Candidate end at tile element e whose last k0 tokens already
@@ -521,15 +521,54 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                     if (D >= 2) p0 = sq[j - 1];
                     if (quad_any<D>(p0, c0, s0, s1, s2, s3)) extend_quad(p0, c0, j);
                 }
-                // elements of [lo, hi] outside whole quads: fewer than 8
-                if (4 * jq0 != lo || 4 * (jq1 + 1) != hi + 1) {
-                    const int head_end = 4 * jq0 < hi + 1 ? 4 * jq0 : hi + 1;       // [lo, head_end)
-                    const int tail_beg = 4 * (jq1 + 1) > lo ? 4 * (jq1 + 1) : lo;   // [tail_beg, hi]
-                    int e = -1;
-                    if (lane < 4) e = lo + lane < head_end ? lo + lane : -1;
-                    else if (lane < 8) e = tail_beg + (lane - 4) <= hi && tail_beg + (lane - 4) >= head_end
-                                               ? tail_beg + (lane - 4) : -1;
-                    if (e >= 0 && st[e] == s0) extend(e, 1);
+            };
+
+            // Candidate ends [lo, hi] (tile elements) of the current request that cover
+            // quads only in part (a tile shared by requests): one pass over every quad
+            // the range touches, two per lane, the D-token test masked to the range.
+            auto scan_partial = [&](int lo, int hi) {
+                const int qoff = base - cur_o;           // local position of st[0] in the request
+                const int row = cur_r - rw_lo;
+                const int32_t *suf = row < kSufRows ? suf_w + row * max_m : nullptr;
+                const int32_t *hist_last = ta + (WA + cur_nxt) - 1;
+                auto extend = [&](int e) {               // the D tokens ending at e match
+                    const int q = qoff + e;
+                    const int kmax = max_m < q + 1 ? max_m : q + 1;
+                    int kk = D;
+                    while (kk < kmax && st[e - kk] == (suf ? suf[kk] : __ldg(hist_last - kk))) ++kk;
+                    if (kk >= min_m) {
+                        const unsigned long long key =
+                            (static_cast<unsigned long long>(kk) << 32) | static_cast<uint32_t>(q - kk + 1);
+                        best = key > best ? key : best;
+                    }
+                };
+                const int ja = lo >> 2, jb = hi >> 2;
+                const unsigned head = (0xFu << (lo & 3)) & 0xFu;   // elements >= lo in quad ja
+                const unsigned tail = 0xFu >> (3 - (hi & 3));      // elements <= hi in quad jb
+                for (int j = ja + lane; j <= jb; j += 64) {
+                    const int j2 = j + 32;
+                    const bool has2 = j2 <= jb;
+                    const int jj2 = has2 ? j2 : jb;
+                    const int4 c0 = sq[j], c1 = sq[jj2];
+                    int4 p0 = make_int4(0, 0, 0, 0), p1 = make_int4(0, 0, 0, 0);
+                    if (D >= 2) {
+                        p0 = sq[j - 1];
+                        p1 = sq[jj2 - 1];
+                    }
+                    const unsigned m0 = (j == ja ? head : 0xFu) & (j == jb ? tail : 0xFu);
+                    const unsigned m1 = has2 ? (j2 == jb ? tail : 0xFu) : 0u;
+                    unsigned h0 = quad_hits<D>(p0, c0, s0, s1, s2, s3) & m0;
+                    unsigned h1 = quad_hits<D>(p1, c1, s0, s1, s2, s3) & m1;
+                    while (h0) {
+                        const int e = __ffs(h0) - 1;
+                        h0 &= h0 - 1;
+                        extend(4 * j + e);
+                    }
+                    while (h1) {
+                        const int e = __ffs(h1) - 1;
+                        h1 &= h1 - 1;
+                        extend(4 * j2 + e);
+                    }
                 }
             };
 
@@ -547,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                     const int hi = (nxt - 2 < ee - 1) ? nxt - 2 : ee - 1;               // within this tile
                     if (lo > hi) continue;
                     set_request(r);
-                    scan_range(lo - base, hi - base);
+                    scan_partial(lo - base, hi - base);
                 }
             }
             // Refill this buffer with the warp's tile k + kBufs.
