@@ -424,23 +424,19 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
         };
 
         // 5. Stream the tiles.  The warp's current request (uniform across it) and
-        //    each lane's best key for it carry over from tile to tile; the warp's
-        //    maximum goes into the request's slot when the warp moves on.
+        //    each lane's best key for it carry over from tile to tile; the lanes'
+        //    keys go into the request's slot when the warp moves on.
         int seg_r = rw_lo;                               // first request not yet finished
         int cur_r = -1;                                  // request of the cached state below
         int cur_o = 0, cur_nxt = 0;                      // its start and end, relative to WA
         int32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0;
         unsigned long long best = 0ull;
-        auto flush = [&]() {                             // warp-uniform
-            if (__any_sync(0xffffffffu, best != 0ull)) {
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const unsigned long long x = __shfl_xor_sync(0xffffffffu, best, o);
-                    best = x > best ? x : best;
-                }
-                if (lane == 0) slots[cur_r] = best;
-                best = 0ull;
-            }
+        // A lane's best key goes into the request's slot with an atomic max (no
+        // value returned, so nothing waits for it): the slot was zeroed above and
+        // only this warp's lanes write it.
+        auto flush = [&]() {
+            if (best != 0ull) atomicMax(&slots[cur_r], best);
+            best = 0ull;
         };
         auto set_request = [&](int r) {                  // warp-uniform, r in [rw_lo, rw_hi]
             if (r == cur_r) return;
