@@ -278,6 +278,15 @@ __device__ __forceinline__ bool quad_any(const int4 &prv, const int4 &cur, int32
     return (h0 | h1) | (h2 | h3);
 }
 
+// Bit e set when element x4 + e lies in [lo, hi] (e = 0..3).
+__device__ __forceinline__ unsigned range_mask(int x4, int lo, int hi) {
+    const int a = lo - x4, b = hi - x4;
+    if (b < 0 || a > 3) return 0u;
+    const unsigned ma = a <= 0 ? 0xFu : (0xFu << a) & 0xFu;
+    const unsigned mb = b >= 3 ? 0xFu : 0xFu >> (3 - b);
+    return ma & mb;
+}
+
 // D = min(min_m, 4): how many suffix tokens the branch-free rejection test checks
 // before a candidate is extended one token at a time.  OFFS_SMEM: B + 1 <= kOffCap,
 // the offsets are copied into shared memory (otherwise read from global memory).
@@ -574,7 +583,111 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
             } else {
                 // Requests overlapping this tile, in order (uniform across the warp).
                 while (seg_r < rw_hi && off_a(seg_r + 1) - WA <= eb) ++seg_r;
-                for (int r = seg_r; r <= rw_hi; ++r) {
+                // The common shared tile: request A = seg_r ends in it and B = seg_r + 1
+                // reaches past its end.  With D >= 3, A's last candidate end and B's
+                // first are more than 4 elements apart, so no quad holds candidates of
+                // both: one pass over the whole quads of both ranges, each tested with
+                // its own request's suffix, then the few quads the ranges cover in part.
+                const int rA = seg_r, rB = seg_r + 1;
+                const int oA = int(off_a(rA) - WA), nA = int(off_a(rA + 1) - WA);
+                const int nB = rB <= rw_hi ? int(off_a(rB + 1) - WA) : nA;
+                if (D >= 3 && rB <= rw_hi && nA < ee && nB >= ee && nB > nA) {
+                    flush();                             // the keys pending for cur_r
+                    const int oB = nA;
+                    const int loA = ((oA + (min_m - 1) > eb) ? oA + (min_m - 1) : eb) - base;
+                    const int hiA = ((nA - 2 < ee - 1) ? nA - 2 : ee - 1) - base;
+                    const int loB = ((oB + (min_m - 1) > eb) ? oB + (min_m - 1) : eb) - base;
+                    const int hiB = ((nB - 2 < ee - 1) ? nB - 2 : ee - 1) - base;
+                    const int32_t a0 = suffix(rA, WA + oA, WA + nA, 0), a1 = suffix(rA, WA + oA, WA + nA, 1),
+                                  a2 = suffix(rA, WA + oA, WA + nA, 2);
+                    const int32_t a3 = D >= 4 ? suffix(rA, WA + oA, WA + nA, 3) : 0;
+                    const int32_t b0 = suffix(rB, WA + oB, WA + nB, 0), b1 = suffix(rB, WA + oB, WA + nB, 1),
+                                  b2 = suffix(rB, WA + oB, WA + nB, 2);
+                    const int32_t b3 = D >= 4 ? suffix(rB, WA + oB, WA + nB, 3) : 0;
+                    // candidate end at tile element e of A or B whose last D tokens match
+                    unsigned long long bestA = 0ull, bestB = 0ull;
+                    auto extend2 = [&](int e, bool inB) {
+                        const int r = inB ? rB : rA;
+                        const int q = base + e - (inB ? oB : oA);      // local end position
+                        const int kmax = max_m < q + 1 ? max_m : q + 1;
+                        const int64_t o_abs = WA + (inB ? oB : oA), n_abs = WA + (inB ? nB : nA);
+                        int kk = D;
+                        while (kk < kmax && st[e - kk] == suffix(r, o_abs, n_abs, kk)) ++kk;
+                        if (kk >= min_m) {
+                            const unsigned long long key =
+                                (static_cast<unsigned long long>(kk) << 32) | static_cast<uint32_t>(q - kk + 1);
+                            if (inB) bestB = key > bestB ? key : bestB;
+                            else bestA = key > bestA ? key : bestA;
+                        }
+                    };
+                    // the whole quads of A's range, then B's, as one index space: the
+                    // unmasked test, the request's suffix chosen per quad
+                    const bool hasA = loA <= hiA, hasB = loB <= hiB;
+                    const int jA0 = (loA + 3) >> 2, jA1 = ((hiA + 1) >> 2) - 1;
+                    const int jB0 = (loB + 3) >> 2, jB1 = ((hiB + 1) >> 2) - 1;
+                    const int nfa = hasA && jA1 >= jA0 ? jA1 - jA0 + 1 : 0;
+                    const int nf = nfa + (hasB && jB1 >= jB0 ? jB1 - jB0 + 1 : 0);
+                    for (int t = lane; t < nf; t += 64) {
+                        const bool has2 = t + 32 < nf;
+                        const int t2 = has2 ? t + 32 : t;
+                        const bool inB0 = t >= nfa, inB1 = t2 >= nfa;
+                        const int j = inB0 ? jB0 + (t - nfa) : jA0 + t;
+                        const int j2 = inB1 ? jB0 + (t2 - nfa) : jA0 + t2;
+                        const int4 c0 = sq[j], c1 = sq[j2], p0 = sq[j - 1], p1 = sq[j2 - 1];
+                        const bool any0 = quad_any<D>(p0, c0, inB0 ? b0 : a0, inB0 ? b1 : a1, inB0 ? b2 : a2,
+                                                      inB0 ? b3 : a3);
+                        const bool any1 = has2 && quad_any<D>(p1, c1, inB1 ? b0 : a0, inB1 ? b1 : a1,
+                                                              inB1 ? b2 : a2, inB1 ? b3 : a3);
+                        if (any0 | any1) {
+                            unsigned h0 = any0 ? quad_hits<D>(p0, c0, inB0 ? b0 : a0, inB0 ? b1 : a1,
+                                                              inB0 ? b2 : a2, inB0 ? b3 : a3) : 0u;
+                            unsigned h1 = any1 ? quad_hits<D>(p1, c1, inB1 ? b0 : a0, inB1 ? b1 : a1,
+                                                              inB1 ? b2 : a2, inB1 ? b3 : a3) : 0u;
+                            while (h0) {
+                                const int e = __ffs(h0) - 1;
+                                h0 &= h0 - 1;
+                                extend2(4 * j + e, inB0);
+                            }
+                            while (h1) {
+                                const int e = __ffs(h1) - 1;
+                                h1 &= h1 - 1;
+                                extend2(4 * j2 + e, inB1);
+                            }
+                        }
+                    }
+                    // the quads each range covers only in part, at most four: lanes 0 and 1
+                    // A's first and last, lanes 2 and 3 B's (a range inside one quad once)
+                    {
+                        const bool forB = lane >= 2;
+                        const bool has = forB ? hasB : hasA;
+                        const int lo = forB ? loB : loA, hi = forB ? hiB : hiA;
+                        int jp = -1;
+                        if (has && (lane & 1) == 0 && (lo & 3) != 0) jp = lo >> 2;
+                        else if (has && (lane & 1) == 1 && (hi & 3) != 3 &&
+                                 !((lo & 3) != 0 && (hi >> 2) == (lo >> 2)))
+                            jp = hi >> 2;
+                        if (lane < 4 && jp >= 0) {
+                            unsigned h = quad_hits<D>(sq[jp - 1], sq[jp], forB ? b0 : a0, forB ? b1 : a1,
+                                                      forB ? b2 : a2, forB ? b3 : a3) &
+                                         range_mask(4 * jp, lo, hi);
+                            while (h) {
+                                const int e = __ffs(h) - 1;
+                                h &= h - 1;
+                                extend2(4 * jp + e, forB);
+                            }
+                        }
+                    }
+                    // A ends here; B continues into the next tile with its keys pending
+                    if (bestA != 0ull) atomicMax(&slots[rA], bestA);
+                    cur_r = rB;
+                    cur_o = oB;
+                    cur_nxt = nB;
+                    s0 = b0;
+                    s1 = b1;
+                    s2 = b2;
+                    s3 = b3;
+                    best = bestB;
+                } else for (int r = seg_r; r <= rw_hi; ++r) {
                     const int o_r = int(off_a(r) - WA);
                     if (o_r >= ee) break;
                     const int nxt = int(off_a(r + 1) - WA);
