@@ -70,6 +70,11 @@ constexpr int kHaloQuads = 8;          // room for (LOOKUP_DRAFT_MAX_M - 1) toke
 constexpr int kSufRows = 8;            // requests per warp whose suffix is kept in smem
 constexpr int kOffCap = 4097;          // offsets kept in smem when B + 1 <= kOffCap
 constexpr int kFillWarps = 4;          // requests per fill CTA
+constexpr int kFillUnroll = 4;         // slot loads in flight per fill lane
+constexpr int kFillMinBlocks = 12;     // fill CTAs that fit beside a scan CTA on one SM
+constexpr int kLaneFillThreads = 128;  // requests per CTA of the lane-per-request fill
+constexpr int kLaneCover = 4;          // scan warps a lane folds by itself
+constexpr int kLaneFillMinB = 1024;    // batches from this size use the lane-per-request fill
 
 constexpr unsigned long long kKeyFailed = ~0ull;
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
@@ -727,7 +732,34 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
 }
 
 // ------------------------------------------------------------ fill kernel ----
-__global__ void __launch_bounds__(kFillWarps * 32) fill_kernel(FillParams prm) {
+// The outputs of request r (history start o0, length L) from its reduced key.  A
+// key that does not describe an admissible match (1 <= m, p + m <= L - 1) can only
+// come from a failed scan; it is reported as such and never dereferenced.  Draft
+// token j is t[p + m + (j mod d)], d = L - p - m >= 1: the history extended by
+// its own draft.  Lanes first, first + step, ... of the row are written here.
+__device__ inline void write_draft(const FillParams &prm, int r, int64_t o0, int64_t L, unsigned long long key,
+                                   int first, int step, bool head) {
+    const int64_t km = int64_t(key >> 32), kp = int64_t(uint32_t(key));
+    const bool failed = key != 0ull && (key == kKeyFailed || km < 1 || kp + km > L - 1);
+    const bool found = key != 0ull && !failed;
+    const int32_t m = found ? int32_t(km) : 0;
+    const int64_t p = found ? kp : -1;
+    const int d = found ? int(L - p - m) : 1;            // L < 2^31
+    const int K = prm.K;
+    int32_t *row = prm.out_draft + int64_t(r) * K;
+    const int32_t *src = prm.tokens + o0 + p + m;
+    for (int j = first; j < K; j += step) row[j] = found ? __ldg(src + (j < d ? j : j % d)) : -1;
+    if (head) {
+        prm.out_len[r] = found ? K : (failed ? LOOKUP_DRAFT_LEN_FAILED : 0);
+        prm.out_pos[r] = int32_t(p);
+        if (prm.out_mlen) prm.out_mlen[r] = m;
+    }
+}
+
+// One warp per request, for small batches: the request's slots lie in the scan
+// warps v0 .. v1 holding its first and last quads, and the lanes load them in
+// parallel.
+__global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_kernel(FillParams prm) {
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * kFillWarps + (threadIdx.x >> 5);
     // Inputs the scan does not write: read them before waiting for it.
@@ -749,12 +781,19 @@ __global__ void __launch_bounds__(kFillWarps * 32) fill_kernel(FillParams prm) {
         const Partition P = make_partition(first + shift, end + shift, prm.grid);
         const int64_t v0 = vchunk_of_quad(P, ((o0 + shift) >> 2) - P.q_lo);
         const int64_t v1 = vchunk_of_quad(P, ((o1 - 1 + shift) >> 2) - P.q_lo);
-        for (int64_t v = v0 + lane; v <= v1; v += 32) {
-            int64_t lo, hi;
-            vchunk_range(P, v, lo, hi);
-            if (lo >= hi) continue;                      // an empty warp range owns no slot
-            const unsigned long long x = prm.slots[int64_t(r) + v];
-            key = x > key ? x : key;
+        // Lane i folds the slots of warps v0 + i, v0 + i + 32, ...: kFillUnroll
+        // independent loads at a time, none for an empty warp range (it owns no slot).
+        for (int64_t vb = v0 + lane; vb <= v1; vb += kFillUnroll * 32) {
+            unsigned long long x[kFillUnroll];
+#pragma unroll
+            for (int u = 0; u < kFillUnroll; ++u) {
+                const int64_t v = vb + u * 32;
+                int64_t lo, hi;
+                vchunk_range(P, v, lo, hi);
+                x[u] = (v <= v1 && lo < hi) ? prm.slots[int64_t(r) + v] : 0ull;
+            }
+#pragma unroll
+            for (int u = 0; u < kFillUnroll; ++u) key = x[u] > key ? x[u] : key;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -762,22 +801,70 @@ __global__ void __launch_bounds__(kFillWarps * 32) fill_kernel(FillParams prm) {
             key = x > key ? x : key;
         }
     }
-    // A key that does not describe an admissible match (1 <= m, p + m <= L - 1) can
-    // only come from a failed scan; it is reported as such and never dereferenced.
-    const int64_t km = int64_t(key >> 32), kp = int64_t(uint32_t(key));
-    const bool failed = key != 0ull && (key == kKeyFailed || km < 1 || kp + km > L - 1);
-    const bool found = key != 0ull && !failed;
-    const int32_t m = found ? int32_t(km) : 0;
-    const int64_t p = found ? kp : -1;
-    const int64_t d = found ? L - p - m : 1;
-    const int K = prm.K;
-    int32_t *row = prm.out_draft + int64_t(r) * K;
-    for (int j = lane; j < K; j += 32) row[j] = found ? __ldg(prm.tokens + o0 + p + m + (j % d)) : -1;
-    if (lane == 0) {
-        prm.out_len[r] = found ? K : (failed ? LOOKUP_DRAFT_LEN_FAILED : 0);
-        prm.out_pos[r] = int32_t(p);
-        if (prm.out_mlen) prm.out_mlen[r] = m;
+    write_draft(prm, r, o0, L, key, lane, 32, lane == 0);
+}
+
+// One request per lane, for large batches: there most requests' slots lie in one
+// or two scan warps, and a warp per request would spend its issue slots on idle
+// lanes.  A lane folds up to kLaneCover slots itself; the few requests whose
+// slots span more scan warps are folded by the whole warp, one at a time.
+__global__ void __launch_bounds__(kLaneFillThreads) fill_lanes_kernel(FillParams prm) {
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * kLaneFillThreads + threadIdx.x;
+    const bool live = r < prm.B;
+    int64_t o0 = 0, o1 = 0;
+    if (live) {
+        o0 = __ldg(prm.offsets + r);
+        o1 = __ldg(prm.offsets + r + 1);
     }
+    const int64_t first = __ldg(prm.offsets);
+    const int64_t end = __ldg(prm.offsets + prm.B);
+    const int shift = tokens_shift(prm.tokens);
+    const int64_t L = o1 - o0;
+    allow_dependent_launch();
+    wait_for_prerequisite_grid();
+    if (__all_sync(0xffffffffu, !live)) return;          // warp-uniform
+
+    const Partition P = make_partition(first + shift, end + shift, prm.grid);
+    int64_t v0 = 0, v1 = -1;                             // no slots: empty request or no request
+    if (L > 0) {
+        v0 = vchunk_of_quad(P, ((o0 + shift) >> 2) - P.q_lo);
+        v1 = vchunk_of_quad(P, ((o1 - 1 + shift) >> 2) - P.q_lo);
+    }
+    unsigned long long key = 0ull;
+    const bool own = v1 - v0 < kLaneCover;
+    if (own) {
+        unsigned long long x[kLaneCover];
+#pragma unroll
+        for (int u = 0; u < kLaneCover; ++u) {
+            const int64_t v = v0 + u;
+            int64_t lo, hi;
+            vchunk_range(P, v, lo, hi);
+            x[u] = (v <= v1 && lo < hi) ? prm.slots[int64_t(r) + v] : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < kLaneCover; ++u) key = x[u] > key ? x[u] : key;
+    }
+    for (unsigned wide = __ballot_sync(0xffffffffu, !own); wide != 0u; wide &= wide - 1) {
+        const int src = __ffs(int(wide)) - 1;
+        const int64_t a = __shfl_sync(0xffffffffu, v0, src);
+        const int64_t b = __shfl_sync(0xffffffffu, v1, src);
+        const int rs = __shfl_sync(0xffffffffu, r, src);
+        unsigned long long kw = 0ull;
+        for (int64_t v = a + lane; v <= b; v += 32) {
+            int64_t lo, hi;
+            vchunk_range(P, v, lo, hi);
+            const unsigned long long x = lo < hi ? prm.slots[int64_t(rs) + v] : 0ull;
+            kw = x > kw ? x : kw;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long x = __shfl_xor_sync(0xffffffffu, kw, o);
+            kw = x > kw ? x : kw;
+        }
+        if (lane == src) key = kw;
+    }
+    if (live) write_draft(prm, r, o0, L, key, 0, 1, true);
 }
 
 // ------------------------------------------------------------- host side ----
@@ -937,10 +1024,12 @@ int launch_fill(const DeviceState &st, const int32_t *tokens, const int64_t *off
     prm.B = B;
     prm.K = K;
     prm.grid = grid_for(st);
+    const bool lanes = B >= kLaneFillMinB;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(unsigned((int64_t(B) + kFillWarps - 1) / kFillWarps));
-    cfg.blockDim = dim3(kFillWarps * 32);
+    cfg.gridDim = lanes ? dim3(unsigned((int64_t(B) + kLaneFillThreads - 1) / kLaneFillThreads))
+                        : dim3(unsigned((int64_t(B) + kFillWarps - 1) / kFillWarps));
+    cfg.blockDim = dim3(lanes ? kLaneFillThreads : kFillWarps * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -948,7 +1037,10 @@ int launch_fill(const DeviceState &st, const int32_t *tokens, const int64_t *off
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    LD_CUDA(cudaLaunchKernelEx(&cfg, fill_kernel, prm));
+    if (lanes)
+        LD_CUDA(cudaLaunchKernelEx(&cfg, fill_lanes_kernel, prm));
+    else
+        LD_CUDA(cudaLaunchKernelEx(&cfg, fill_kernel, prm));
     return LOOKUP_DRAFT_OK;
 }
 

@@ -8,8 +8,10 @@ requests, K = 0 and the largest K, the widest m range, unaligned token
 pointers, offsets[0] > 0, fewer tokens than scan CTAs, more requests than the
 offsets the scan keeps in shared memory, all-equal and tiny-alphabet histories,
 long single requests spread over many CTAs, a match ending exactly at a tile or
-chunk boundary, the staged and host-buffer entry points, repeated calls and the
-failure path of the bounded waits.
+chunk boundary, clusters of dozens of requests starting inside one quad, batch
+sizes on both sides of the switch to the lane-per-request fill (with requests
+spanning hundreds of scan warps), the staged and host-buffer entry points,
+repeated calls and the failure path of the bounded waits.
 """
 from __future__ import annotations
 
@@ -137,6 +139,52 @@ def test_many_requests_long_chunks():
     lengths = rng.integers(0, 600, size=6000)
     tokens = rng.integers(0, 50, size=int(lengths.sum())).astype(np.int32)
     assert_parity(tokens, gen.offsets_from_lengths(lengths), 2, 12, 7)
+
+
+def clustered_lengths(rng, B, cluster):
+    """Long requests separated by runs of `cluster` empty or 1-3 token requests, so
+    that dozens of requests start inside one 4-token quad."""
+    lengths = []
+    while len(lengths) < B:
+        lengths.append(int(rng.integers(200, 6000)))
+        lengths.extend(int(x) for x in rng.choice([0, 0, 0, 1, 2, 3], size=cluster))
+    return np.array(lengths[:B])
+
+
+@pytest.mark.parametrize("cluster", [1, 5, 40, 70])
+@pytest.mark.parametrize("pad", [0, 1, 2, 3])
+def test_clustered_short_requests(cluster, pad):
+    """Long requests separated by up to 70 requests that start inside one quad, in
+    batches for either fill."""
+    rng = np.random.default_rng(cluster * 10 + pad)
+    lengths = clustered_lengths(rng, 400 if pad % 2 == 0 else 1500, cluster)
+    tokens = rng.integers(0, 3, size=int(lengths.sum())).astype(np.int32)
+    offsets = gen.offsets_from_lengths(lengths) + int(rng.integers(0, 4))
+    tokens = np.concatenate([np.full(int(offsets[0]), 1, np.int32), tokens])
+    assert_parity(tokens, offsets, 1, 12, 5, token_pad=pad)
+    assert_parity(tokens, offsets, 4, 12, 7, token_pad=pad)
+
+
+@pytest.mark.parametrize("B", [2, 9, 300, 1023, 1024, 1025, 2432])
+def test_log_uniform_lengths(B):
+    """Log-uniform lengths (a few long requests, many boundaries), on both sides of
+    the batch size from which the fill takes one request per lane."""
+    rng = np.random.default_rng(B)
+    lengths = np.exp(rng.uniform(0, np.log(40000), size=B)).astype(np.int64)
+    tokens = rng.integers(0, 6, size=int(lengths.sum())).astype(np.int32)
+    assert_parity(tokens, gen.offsets_from_lengths(lengths), 4, 12, 9, token_pad=B % 4)
+
+
+@pytest.mark.parametrize("B", [1023, 1024, 3000])
+def test_large_batch_with_long_requests(B):
+    """Around the batch size from which the fill takes one request per lane, with
+    a few requests long enough to span hundreds of scan warps (those are folded
+    by the whole warp)."""
+    rng = np.random.default_rng(B + 77)
+    lengths = rng.integers(0, 300, size=B)
+    lengths[rng.choice(B, size=5, replace=False)] = rng.integers(100_000, 600_000, size=5)
+    tokens = rng.integers(0, 3, size=int(lengths.sum())).astype(np.int32)
+    assert_parity(tokens, gen.offsets_from_lengths(lengths), 4, 12, 9, token_pad=B % 4)
 
 
 def test_all_equal_tokens():
