@@ -91,6 +91,8 @@ struct ScanParams {
     int32_t min_m;
     int32_t max_m;
     int32_t grid;
+    uint32_t grid_magic;   // floor(n / grid) = umulhi(n, grid_magic) >> grid_shift for n < 2^31
+    int32_t grid_shift;    // -1: grid == 1
     uint64_t wait_ns;
 };
 
@@ -369,9 +371,29 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
     const int64_t a_end = off_a(B);
     allow_dependent_launch();
     bool failed = false;
-    const Partition P = make_partition(a_begin, a_end, G);
+    // The warp's range, in 32-bit arithmetic whenever the batch allows it: this
+    // integer chain lies on the path to the warp's first copy.
+    Partition P;
     int64_t wq0 = 0, wq1 = 0;
-    if (a_end > a_begin) vchunk_range(P, int64_t(c) * kWarps + warp, wq0, wq1);
+    P.q_lo = a_begin >> 2;
+    P.nq = ((a_end + 3) >> 2) - P.q_lo;
+    if (P.nq < (int64_t(1) << 31) - G) {
+        const uint32_t nq = uint32_t(P.nq), n = nq + uint32_t(G - 1);
+        const uint32_t S = prm.grid_shift < 0 ? n : __umulhi(n, prm.grid_magic) >> prm.grid_shift;
+        const uint32_t Sw = (S + kWarps - 1) / kWarps;
+        P.S = S;
+        P.Sw = Sw;
+        const uint32_t c0 = uint32_t(c) * S;
+        const uint32_t c1 = (c0 + S < nq) ? c0 + S : nq;
+        const uint32_t lo = c0 + uint32_t(warp) * Sw;
+        if (a_end > a_begin) {
+            wq0 = lo;
+            wq1 = (lo + Sw < c1) ? lo + Sw : c1;
+        }
+    } else {
+        P = make_partition(a_begin, a_end, G);
+        if (a_end > a_begin) vchunk_range(P, int64_t(c) * kWarps + warp, wq0, wq1);
+    }
 
     if (wq0 < wq1) {                                     // warp-uniform: this warp has a range
         // 2. The warp's range: elements [WA + wbeg, WA + wend) of the aligned view;
@@ -389,7 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
         const int halo = (max_m - 1 + 3) >> 2;
         int tq = (wn + 1) / 2;
         tq = tq < kTileQuadsMin ? kTileQuadsMin : (tq > kTileQuadsMax ? kTileQuadsMax : tq);
-        const int ntiles = (wn + tq - 1) / tq;
+        // ceil(wn / tq): at most 2 unless tq is at its cap
+        const int ntiles = tq == kTileQuadsMax ? (wn + kTileQuadsMax - 1) / kTileQuadsMax : (wn > tq ? 2 : 1);
         unsigned char *my_bufs = smem + lay.bufs + size_t(warp) * kBufs * kBufBytes;
         unsigned long long *my_bars = bars + warp * kBufs;
         auto issue_tile = [&](int k, int slot) {           // lane 0 only
@@ -946,6 +969,23 @@ int device_state(DeviceState **out) {
 // One scan CTA per SM (its shared-memory rings admit no second one).
 int grid_for(const DeviceState &st) { return st.sms; }
 
+// Division of n < 2^31 by the grid size G >= 2 as a multiply-high and a shift:
+// magic = ceil(2^k / G) with k = 31 + ceil(log2 G), so that magic < 2^32 and
+// n * magic / 2^k = n / G + n * err / (G * 2^k), err < G, stays below the next
+// integer whenever n * G <= 2^k (the method of division by invariant integers).
+void grid_divider(int G, uint32_t &magic, int32_t &shift) {
+    if (G <= 1) {
+        magic = 0;
+        shift = -1;
+        return;
+    }
+    int l = 0;
+    while ((int64_t(1) << l) < G) ++l;
+    const int k = 31 + l;
+    magic = uint32_t(((uint64_t(1) << k) + uint64_t(G) - 1) / uint64_t(G));
+    shift = k - 32;
+}
+
 // One 64-bit slot per (request, virtual chunk) pair on the staircase: at most
 // B + (number of virtual chunks) of them.
 size_t workspace_bytes_for(int32_t B, int grid) {
@@ -983,6 +1023,7 @@ int launch_scan(const DeviceState &st, const int32_t *tokens, const int64_t *off
     prm.min_m = min_m;
     prm.max_m = max_m;
     prm.grid = grid_for(st);
+    grid_divider(prm.grid, prm.grid_magic, prm.grid_shift);
     prm.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     const ScanSmemLayout lay = scan_smem_layout(B, max_m);
     cudaLaunchConfig_t cfg;
