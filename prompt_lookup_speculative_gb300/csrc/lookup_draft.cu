@@ -322,20 +322,28 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
     const int64_t *offs_s =
         reinterpret_cast<const int64_t *>(smem + lay.offs + (reinterpret_cast<uintptr_t>(prm.offsets) & 15u));
 
-    // 0. Barriers, and the offsets warmed into L2 while the previous kernel on
-    //    the stream finishes; then wait for it (it may have written the inputs).
+    // 0. Barriers (the offsets' by thread 0, each warp's ring by its lane 0), and
+    //    the offsets warmed into L2 while the previous kernel on the stream
+    //    finishes; then wait for it (it may have written the inputs).
     if (offs_in_smem && tid * 16 <= B) prefetch_l2(prm.offsets + tid * 16);
+    unsigned long long *my_bars = bars + warp * kBufs;
     if (tid == 0) {
         sh_deadline = global_ns() + prm.wait_ns;         // every copy must land by then
-        for (int i = 0; i <= kWarps * kBufs; ++i) mbar_init(smem_addr(&bars[i]), 1);
+        mbar_init(smem_addr(offs_bar), 1);
+        fence_barrier_init();
+    }
+    if (lane == 0) {
+        for (int i = 0; i < kBufs; ++i) mbar_init(smem_addr(&my_bars[i]), 1);
         fence_barrier_init();
     }
     wait_for_prerequisite_grid();
 
-    // 1. Offsets -> shared memory: one bulk copy of the 16-byte span covering them.
-    //    Should the copy not land in time, the CTA reads the offsets from global
-    //    memory instead (and lets the copy land before it exits).
-    bool ok = true;
+    // 1. Offsets -> shared memory: one bulk copy of the 16-byte span covering them,
+    //    for the request searches.  Should the copy not land in time, the CTA reads
+    //    the offsets from global memory instead (and lets the copy land before it
+    //    exits).  The batch's two ends, all that the first copy of history needs,
+    //    are read straight from memory meanwhile, through L1, which merges the
+    //    CTA's 16 warps' requests for the same two lines.
     if (offs_in_smem && tid == 0) {
         const uintptr_t end = (reinterpret_cast<uintptr_t>(prm.offsets + B + 1) + 15) & ~uintptr_t(15);
         const uint32_t bytes = uint32_t(end - off_src);
@@ -343,36 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
         bulk_copy_g2s(smem_addr(smem + lay.offs), reinterpret_cast<const void *>(off_src), bytes,
                       smem_addr(offs_bar));
     }
-    __syncthreads();                                     // barrier init visible before waiting
-    const uint64_t deadline = sh_deadline;
-    if (offs_in_smem) ok = mbar_try_wait(smem_addr(offs_bar), 0) || mbar_wait_until(smem_addr(offs_bar), 0, deadline);
-    const bool offs_smem = offs_in_smem && !__syncthreads_or(!ok);
-    const bool offs_pending = offs_in_smem && !offs_smem;
-    auto off_a = [&](int i) -> int64_t {
-        if (OFFS_SMEM && offs_smem) return offs_s[i] + shift;
-        return __ldg(prm.offsets + i) + shift;
-    };
-    // Largest r in [lo, hi] with off_a(r) <= e, given off_a(lo) <= e: a 32-way
-    // search, each lane testing one probe per round (warp-uniform result).
-    auto owner = [&](int64_t e, int lo, int hi) -> int {
-        while (hi > lo) {
-            const int step = (hi - lo + 31) >> 5;
-            const int probe = (lo + (lane + 1) * step < hi) ? lo + (lane + 1) * step : hi;
-            const int cnt = __popc(__ballot_sync(0xffffffffu, off_a(probe) <= e));   // a prefix of lanes
-            const int nlo = cnt == 0 ? lo : ((lo + cnt * step < hi) ? lo + cnt * step : hi);
-            const int nhi = cnt == 32 ? hi : ((lo + (cnt + 1) * step < hi) ? lo + (cnt + 1) * step : hi) - 1;
-            lo = nlo;
-            hi = nhi;
-        }
-        return lo;
-    };
-
-    const int64_t a_begin = off_a(0);
-    const int64_t a_end = off_a(B);
+    int64_t ends = 0;
+    if (lane < 2) ends = __ldca(prm.offsets + (lane == 0 ? 0 : B));
+    const int64_t a_begin = __shfl_sync(0xffffffffu, ends, 0) + shift;
+    const int64_t a_end = __shfl_sync(0xffffffffu, ends, 1) + shift;
     allow_dependent_launch();
     bool failed = false;
-    // The warp's range, in 32-bit arithmetic whenever the batch allows it: this
-    // integer chain lies on the path to the warp's first copy.
+    // 2. The warp's range, in 32-bit arithmetic whenever the batch allows it: this
+    //    integer chain lies on the path to the warp's first copy.
     Partition P;
     int64_t wq0 = 0, wq1 = 0;
     P.q_lo = a_begin >> 2;
@@ -395,37 +381,66 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
         if (a_end > a_begin) vchunk_range(P, int64_t(c) * kWarps + warp, wq0, wq1);
     }
 
-    if (wq0 < wq1) {                                     // warp-uniform: this warp has a range
-        // 2. The warp's range: elements [WA + wbeg, WA + wend) of the aligned view;
-        //    positions below are int32 relative to WA.
+    // 3. Tiles: tile k is quads [k*tq, min((k+1)*tq, wn)) of the range (one tile
+    //    when the range fits in one); the ring holds kBufs of them, tile k in buffer
+    //    k % kBufs.  The first one is issued at once, the rest after the suffix
+    //    loads below, so that only one tile per warp is queued ahead of those
+    //    latency-critical loads.  Quads are counted from the range's first, and the
+    //    halo reaches back at most `lead` quads (not before the batch).
+    const int wn = wq0 < wq1 ? int(wq1 - wq0) : 0;
+    const int halo = (max_m - 1 + 3) >> 2;
+    int tq = wn <= kTileQuadsMax ? wn : (wn + 1) / 2;
+    tq = tq < kTileQuadsMin ? kTileQuadsMin : (tq > kTileQuadsMax ? kTileQuadsMax : tq);
+    // ceil(wn / tq): at most 2 unless tq is at its cap
+    const int ntiles = tq == kTileQuadsMax ? (wn + kTileQuadsMax - 1) / kTileQuadsMax : (wn > tq ? 2 : 1);
+    unsigned char *my_bufs = smem + lay.bufs + size_t(warp) * kBufs * kBufBytes;
+    const int lead = wq0 < halo ? int(wq0) : halo;
+    const int32_t *wsrc = ta + 4 * (P.q_lo + wq0);
+    auto issue_tile = [&](int k, int slot) {             // lane 0 only
+        const int t0 = k * tq;
+        const int t1 = (t0 + tq < wn) ? t0 + tq : wn;
+        const int ls = (t0 - halo > -lead) ? t0 - halo : -lead;
+        const uint32_t bytes = uint32_t(t1 - ls) * 16u;
+        unsigned char *buf = my_bufs + size_t(slot) * kBufBytes;
+        const uint32_t bar = smem_addr(&my_bars[slot]);
+        mbar_expect_tx(bar, bytes);
+        bulk_copy_g2s(smem_addr(buf + (kHaloQuads - (t0 - ls)) * 16), wsrc + ls * 4, bytes, bar);
+    };
+    if (wn > 0 && lane == 0) issue_tile(0, 0);
+
+    __syncthreads();                                     // the offsets' barrier initialised before waiting
+    const uint64_t deadline = sh_deadline;
+    bool ok = true;
+    if (offs_in_smem) ok = mbar_try_wait(smem_addr(offs_bar), 0) || mbar_wait_until(smem_addr(offs_bar), 0, deadline);
+    const bool offs_smem = offs_in_smem && !__syncthreads_or(!ok);
+    const bool offs_pending = offs_in_smem && !offs_smem;
+    auto off_a = [&](int i) -> int64_t {
+        if (OFFS_SMEM && offs_smem) return offs_s[i] + shift;
+        return __ldg(prm.offsets + i) + shift;
+    };
+    // Largest r in [lo, hi] with off_a(r) <= e, given off_a(lo) <= e: a 32-way
+    // search, each lane testing one probe per round (warp-uniform result).
+    auto owner = [&](int64_t e, int lo, int hi) -> int {
+        while (hi > lo) {
+            const int step = (hi - lo + 31) >> 5;
+            const int probe = (lo + (lane + 1) * step < hi) ? lo + (lane + 1) * step : hi;
+            const int cnt = __popc(__ballot_sync(0xffffffffu, off_a(probe) <= e));   // a prefix of lanes
+            const int nlo = cnt == 0 ? lo : ((lo + cnt * step < hi) ? lo + cnt * step : hi);
+            const int nhi = cnt == 32 ? hi : ((lo + (cnt + 1) * step < hi) ? lo + (cnt + 1) * step : hi) - 1;
+            lo = nlo;
+            hi = nhi;
+        }
+        return lo;
+    };
+
+    if (wn > 0) {                                        // warp-uniform: this warp has a range
+        // The warp's range: elements [WA + wbeg, WA + wend) of the aligned view;
+        // positions below are int32 relative to WA.
         const int64_t v = int64_t(c) * kWarps + warp;    // virtual chunk: slot column
         unsigned long long *slots = prm.slots + v;       // slot of request r: slots[r]
         const int64_t WA = 4 * (P.q_lo + wq0);
-        const int wn = int(wq1 - wq0);
         const int wbeg = int(((WA > a_begin) ? WA : a_begin) - WA);
         const int wend = int(((4 * (P.q_lo + wq1) < a_end) ? 4 * (P.q_lo + wq1) : a_end) - WA);
-        // 3. Tiles: tile k is quads [k*tq, min((k+1)*tq, wn)) of the range; the ring
-        //    holds kBufs of them, tile k in buffer k % kBufs.  The first one is
-        //    issued at once, the rest after the suffix loads below, so that only
-        //    one tile per warp is queued ahead of those latency-critical loads.
-        const int halo = (max_m - 1 + 3) >> 2;
-        int tq = (wn + 1) / 2;
-        tq = tq < kTileQuadsMin ? kTileQuadsMin : (tq > kTileQuadsMax ? kTileQuadsMax : tq);
-        // ceil(wn / tq): at most 2 unless tq is at its cap
-        const int ntiles = tq == kTileQuadsMax ? (wn + kTileQuadsMax - 1) / kTileQuadsMax : (wn > tq ? 2 : 1);
-        unsigned char *my_bufs = smem + lay.bufs + size_t(warp) * kBufs * kBufBytes;
-        unsigned long long *my_bars = bars + warp * kBufs;
-        auto issue_tile = [&](int k, int slot) {           // lane 0 only
-            const int64_t t0 = P.q_lo + wq0 + int64_t(k) * tq;
-            const int64_t t1 = (t0 + tq < P.q_lo + wq1) ? t0 + tq : P.q_lo + wq1;
-            const int64_t ls = (t0 - halo > P.q_lo) ? t0 - halo : P.q_lo;
-            const uint32_t bytes = uint32_t(t1 - ls) * 16u;
-            unsigned char *buf = my_bufs + size_t(slot) * kBufBytes;
-            const uint32_t bar = smem_addr(&my_bars[slot]);
-            mbar_expect_tx(bar, bytes);
-            bulk_copy_g2s(smem_addr(buf + size_t(kHaloQuads - (t0 - ls)) * 16), ta + ls * 4, bytes, bar);
-        };
-        if (lane == 0) issue_tile(0, 0);
         const int rw_lo = owner(WA + wbeg, 0, B - 1);
 
         // 4. Suffix tokens (row[j] = t[L-1-j], lane j) of requests rw_lo, rw_lo + 1, ...
