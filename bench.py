@@ -59,7 +59,7 @@ METRIC = "µs per batched draft step; history GB/s scanned vs GB300 HBM roofline
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 SCAN_SOURCE = os.path.join(ROOT, "prompt_lookup_speculative_gb300", "csrc", "lookup_draft.cu")
-SCAN_PROFILE = os.path.join(ROOT, "profiles", "scan_kernel_recitation25k.md")
+PROFILES = os.path.join(ROOT, "profiles")
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -204,10 +204,11 @@ def scan_source_hash() -> str:
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per scan launch from the committed ncu summary, if it was taken on
-    this exact kernel source and workload (else None)."""
+    """DRAM bytes per scan launch from the committed ncu summary of this workload
+    (profiles/scan_kernel_<workload>.md), if it was taken on this exact kernel
+    source (else None)."""
     try:
-        text = open(SCAN_PROFILE, encoding="utf-8").read()
+        text = open(os.path.join(PROFILES, f"scan_kernel_{workload}.md"), encoding="utf-8").read()
     except OSError:
         return None
     src = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
