@@ -663,29 +663,34 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                             else bestA = key > bestA ? key : bestA;
                         }
                     };
-                    // the whole quads of A's range, then B's, as one index space: the
-                    // unmasked test, the request's suffix chosen per quad
+                    // every quad the two ranges touch, once: a quad holds candidate ends of
+                    // A or of B, never of both (D >= 3 leaves 3 elements between A's last
+                    // and B's first), so it is tested with that request's suffix and its
+                    // rare hits are masked to that request's range
                     const bool hasA = loA <= hiA, hasB = loB <= hiB;
-                    const int jA0 = (loA + 3) >> 2, jA1 = ((hiA + 1) >> 2) - 1;
-                    const int jB0 = (loB + 3) >> 2, jB1 = ((hiB + 1) >> 2) - 1;
-                    const int nfa = hasA && jA1 >= jA0 ? jA1 - jA0 + 1 : 0;
-                    const int nf = nfa + (hasB && jB1 >= jB0 ? jB1 - jB0 + 1 : 0);
-                    for (int t = lane; t < nf; t += 64) {
-                        const bool has2 = t + 32 < nf;
-                        const int t2 = has2 ? t + 32 : t;
-                        const bool inB0 = t >= nfa, inB1 = t2 >= nfa;
-                        const int j = inB0 ? jB0 + (t - nfa) : jA0 + t;
-                        const int j2 = inB1 ? jB0 + (t2 - nfa) : jA0 + t2;
-                        const int4 c0 = sq[j], c1 = sq[j2], p0 = sq[j - 1], p1 = sq[j2 - 1];
-                        const bool any0 = quad_any<D>(p0, c0, inB0 ? b0 : a0, inB0 ? b1 : a1, inB0 ? b2 : a2,
-                                                      inB0 ? b3 : a3);
-                        const bool any1 = has2 && quad_any<D>(p1, c1, inB1 ? b0 : a0, inB1 ? b1 : a1,
-                                                              inB1 ? b2 : a2, inB1 ? b3 : a3);
+                    const int jlo = (hasA ? loA : loB) >> 2, jhi = (hasB ? hiB : hiA) >> 2;
+                    for (int j = jlo + lane; j <= jhi; j += 64) {
+                        const int j2 = j + 32;
+                        const bool has2 = j2 <= jhi;
+                        const int jj2 = has2 ? j2 : j;
+                        const int4 c0 = sq[j], c1 = sq[jj2], p0 = sq[j - 1], p1 = sq[jj2 - 1];
+                        const bool inA0 = hasA && 4 * j + 3 >= loA && 4 * j <= hiA;
+                        const bool inB0 = hasB && 4 * j + 3 >= loB && 4 * j <= hiB;
+                        const bool inA1 = has2 && hasA && 4 * j2 + 3 >= loA && 4 * j2 <= hiA;
+                        const bool inB1 = has2 && hasB && 4 * j2 + 3 >= loB && 4 * j2 <= hiB;
+                        const bool any0 = (inA0 | inB0) && quad_any<D>(p0, c0, inB0 ? b0 : a0, inB0 ? b1 : a1,
+                                                                     inB0 ? b2 : a2, inB0 ? b3 : a3);
+                        const bool any1 = (inA1 | inB1) && quad_any<D>(p1, c1, inB1 ? b0 : a0, inB1 ? b1 : a1,
+                                                                     inB1 ? b2 : a2, inB1 ? b3 : a3);
                         if (any0 | any1) {
-                            unsigned h0 = any0 ? quad_hits<D>(p0, c0, inB0 ? b0 : a0, inB0 ? b1 : a1,
-                                                              inB0 ? b2 : a2, inB0 ? b3 : a3) : 0u;
-                            unsigned h1 = any1 ? quad_hits<D>(p1, c1, inB1 ? b0 : a0, inB1 ? b1 : a1,
-                                                              inB1 ? b2 : a2, inB1 ? b3 : a3) : 0u;
+                            unsigned h0 = any0 ? quad_hits<D>(p0, c0, inB0 ? b0 : a0, inB0 ? b1 : a1, inB0 ? b2 : a2,
+                                                              inB0 ? b3 : a3) &
+                                                     range_mask(4 * j, inB0 ? loB : loA, inB0 ? hiB : hiA)
+                                               : 0u;
+                            unsigned h1 = any1 ? quad_hits<D>(p1, c1, inB1 ? b0 : a0, inB1 ? b1 : a1, inB1 ? b2 : a2,
+                                                              inB1 ? b3 : a3) &
+                                                     range_mask(4 * j2, inB1 ? loB : loA, inB1 ? hiB : hiA)
+                                               : 0u;
                             while (h0) {
                                 const int e = __ffs(h0) - 1;
                                 h0 &= h0 - 1;
@@ -695,28 +700,6 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                                 const int e = __ffs(h1) - 1;
                                 h1 &= h1 - 1;
                                 extend2(4 * j2 + e, inB1);
-                            }
-                        }
-                    }
-                    // the quads each range covers only in part, at most four: lanes 0 and 1
-                    // A's first and last, lanes 2 and 3 B's (a range inside one quad once)
-                    {
-                        const bool forB = lane >= 2;
-                        const bool has = forB ? hasB : hasA;
-                        const int lo = forB ? loB : loA, hi = forB ? hiB : hiA;
-                        int jp = -1;
-                        if (has && (lane & 1) == 0 && (lo & 3) != 0) jp = lo >> 2;
-                        else if (has && (lane & 1) == 1 && (hi & 3) != 3 &&
-                                 !((lo & 3) != 0 && (hi >> 2) == (lo >> 2)))
-                            jp = hi >> 2;
-                        if (lane < 4 && jp >= 0) {
-                            unsigned h = quad_hits<D>(sq[jp - 1], sq[jp], forB ? b0 : a0, forB ? b1 : a1,
-                                                      forB ? b2 : a2, forB ? b3 : a3) &
-                                         range_mask(4 * jp, lo, hi);
-                            while (h) {
-                                const int e = __ffs(h) - 1;
-                                h &= h - 1;
-                                extend2(4 * jp + e, forB);
                             }
                         }
                     }
