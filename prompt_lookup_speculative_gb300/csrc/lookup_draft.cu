@@ -793,19 +793,38 @@ __global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_kernel(F
     }
     const int shift = tokens_shift(prm.tokens);
     const int64_t L = o1 - o0;
+    // The request's slots are those of warps v0 .. v1, the ones holding its first
+    // and last quads (empty warp ranges own none).  All of that follows from the
+    // offsets, so it is worked out before the wait, with the first round of loads.
+    Partition P{};
+    int64_t v0 = 0, v1 = -1;
+    if (r < prm.B && L > 0) {
+        P = make_partition(first + shift, end + shift, prm.grid);
+        v0 = vchunk_of_quad(P, ((o0 + shift) >> 2) - P.q_lo);
+        v1 = vchunk_of_quad(P, ((o1 - 1 + shift) >> 2) - P.q_lo);
+    }
+    bool take[kFillUnroll];
+#pragma unroll
+    for (int u = 0; u < kFillUnroll; ++u) {
+        const int64_t v = v0 + lane + u * 32;
+        int64_t lo = 0, hi = 0;
+        if (v <= v1) vchunk_range(P, v, lo, hi);
+        take[u] = v <= v1 && lo < hi;
+    }
     allow_dependent_launch();
     wait_for_prerequisite_grid();
     if (r >= prm.B) return;
 
     unsigned long long key = 0ull;
     if (L > 0) {
-        const Partition P = make_partition(first + shift, end + shift, prm.grid);
-        const int64_t v0 = vchunk_of_quad(P, ((o0 + shift) >> 2) - P.q_lo);
-        const int64_t v1 = vchunk_of_quad(P, ((o1 - 1 + shift) >> 2) - P.q_lo);
         // Lane i folds the slots of warps v0 + i, v0 + i + 32, ...: kFillUnroll
-        // independent loads at a time, none for an empty warp range (it owns no slot).
-        for (int64_t vb = v0 + lane; vb <= v1; vb += kFillUnroll * 32) {
-            unsigned long long x[kFillUnroll];
+        // independent loads at a time.
+        unsigned long long x[kFillUnroll];
+#pragma unroll
+        for (int u = 0; u < kFillUnroll; ++u) x[u] = take[u] ? prm.slots[int64_t(r) + v0 + lane + u * 32] : 0ull;
+#pragma unroll
+        for (int u = 0; u < kFillUnroll; ++u) key = x[u] > key ? x[u] : key;
+        for (int64_t vb = v0 + lane + kFillUnroll * 32; vb <= v1; vb += kFillUnroll * 32) {   // long requests
 #pragma unroll
             for (int u = 0; u < kFillUnroll; ++u) {
                 const int64_t v = vb + u * 32;
@@ -842,27 +861,32 @@ __global__ void __launch_bounds__(kLaneFillThreads) fill_lanes_kernel(FillParams
     const int64_t end = __ldg(prm.offsets + prm.B);
     const int shift = tokens_shift(prm.tokens);
     const int64_t L = o1 - o0;
-    allow_dependent_launch();
-    wait_for_prerequisite_grid();
-    if (__all_sync(0xffffffffu, !live)) return;          // warp-uniform
-
+    // The request's scan warps and which of them own a slot follow from the
+    // offsets alone: worked out before the wait.
     const Partition P = make_partition(first + shift, end + shift, prm.grid);
     int64_t v0 = 0, v1 = -1;                             // no slots: empty request or no request
     if (L > 0) {
         v0 = vchunk_of_quad(P, ((o0 + shift) >> 2) - P.q_lo);
         v1 = vchunk_of_quad(P, ((o1 - 1 + shift) >> 2) - P.q_lo);
     }
-    unsigned long long key = 0ull;
     const bool own = v1 - v0 < kLaneCover;
+    bool take[kLaneCover];
+#pragma unroll
+    for (int u = 0; u < kLaneCover; ++u) {
+        const int64_t v = v0 + u;
+        int64_t lo = 0, hi = 0;
+        if (own && v <= v1) vchunk_range(P, v, lo, hi);
+        take[u] = own && v <= v1 && lo < hi;
+    }
+    allow_dependent_launch();
+    wait_for_prerequisite_grid();
+    if (__all_sync(0xffffffffu, !live)) return;          // warp-uniform
+
+    unsigned long long key = 0ull;
     if (own) {
         unsigned long long x[kLaneCover];
 #pragma unroll
-        for (int u = 0; u < kLaneCover; ++u) {
-            const int64_t v = v0 + u;
-            int64_t lo, hi;
-            vchunk_range(P, v, lo, hi);
-            x[u] = (v <= v1 && lo < hi) ? prm.slots[int64_t(r) + v] : 0ull;
-        }
+        for (int u = 0; u < kLaneCover; ++u) x[u] = take[u] ? prm.slots[int64_t(r) + v0 + u] : 0ull;
 #pragma unroll
         for (int u = 0; u < kLaneCover; ++u) key = x[u] > key ? x[u] : key;
     }
