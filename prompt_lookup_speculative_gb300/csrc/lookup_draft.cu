@@ -629,8 +629,8 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                 // The common shared tile: request A = seg_r ends in it and B = seg_r + 1
                 // reaches past its end.  With D >= 3, A's last candidate end and B's
                 // first are more than 4 elements apart, so no quad holds candidates of
-                // both: one pass over the whole quads of both ranges, each tested with
-                // its own request's suffix, then the few quads the ranges cover in part.
+                // both: one pass over every quad of both ranges, each tested with its
+                // own request's suffix.
                 const int rA = seg_r, rB = seg_r + 1;
                 const int oA = int(off_a(rA) - WA), nA = int(off_a(rA + 1) - WA);
                 const int nB = rB <= rw_hi ? int(off_a(rB + 1) - WA) : nA;
