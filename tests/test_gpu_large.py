@@ -1,4 +1,5 @@
-"""Batches larger than 2^31 tokens: the 64-bit offset arithmetic end to end.
+"""Batches larger than 2^31 tokens, and larger than 2^31 quads: the 64-bit offset
+arithmetic end to end, and the scan's and the fill's 64-bit partition path.
 
 A history of 2^31 - 1000 tokens, built as x_i = (i * a) mod P for a prime P, so
 its only repeated 12-grams are exactly P apart; a short request with a planted
@@ -91,3 +92,43 @@ def test_append_beyond_2_31_tokens(batch):
     want = np.where(in_hist, tokens[np.minimum(offsets[r] + i, offsets[-1] - 1)],
                     commit[r, np.clip(i - lens[r], 0, W - 1)])
     np.testing.assert_array_equal(got, want)
+
+
+def test_draft_beyond_2_31_quads():
+    """A batch of more than 2^31 quads (about 36 GB of int32 history), which takes
+    the scan's and the fill's 64-bit partition arithmetic.  Five requests of about
+    1.8e9 tokens, request i built as x_j = (j * A_i) mod P_i on the device: its
+    only repeated 12-grams are exactly P_i apart, so its most recent 12-token match
+    is at p = L - 12 - P_i and the draft continues the period."""
+    props = torch.cuda.get_device_properties(0)
+    Ls = [1_800_000_000 + 7 * i for i in range(5)]
+    total = sum(Ls)
+    need = total * 4 + (2 << 30)
+    free, _ = torch.cuda.mem_get_info()
+    if free < need:
+        pytest.skip(f"needs {need / 2**30:.0f} GiB free on {props.name}")
+    assert total // 4 >= (1 << 31)
+    primes = [999_983, 1_000_003, 1_000_033, 999_979, 1_000_037]
+    t = torch.empty(total, dtype=torch.int32, device="cuda")
+    step = 1 << 27
+    base = 0
+    for L, P in zip(Ls, primes):
+        A = 2_654_435_761 % P
+        for s in range(0, L, step):
+            e = min(s + step, L)
+            t[base + s:base + e] = (torch.arange(s, e, dtype=torch.int64, device="cuda") * A % P).to(torch.int32)
+        base += L
+    offsets = np.concatenate([[0], np.cumsum(Ls)]).astype(np.int64)
+    o = torch.from_numpy(offsets).cuda()
+    K = 15
+    d, ln, pos, m = pkg.lookup_draft_ex(t, o, 4, 12, K)
+    torch.cuda.synchronize()
+    d, ln, pos, m = d.cpu().numpy(), ln.cpu().numpy(), pos.cpu().numpy(), m.cpu().numpy()
+    del t
+    torch.cuda.empty_cache()
+    for i, (L, P) in enumerate(zip(Ls, primes)):
+        A = 2_654_435_761 % P
+        p = L - 12 - P
+        assert (int(ln[i]), int(m[i]), int(pos[i])) == (K, 12, p), i
+        want = [((p + 12 + j) * A) % P for j in range(K)]      # t[p + m + j], inside the history
+        np.testing.assert_array_equal(d[i], np.array(want, dtype=np.int32))
