@@ -39,6 +39,8 @@ constexpr int kCopyUnroll = 2;           // windows in flight per warp
 constexpr int kSub = 4;                  // 128-token sub-windows per window (one int4 per lane each)
 constexpr int kWin = 128 * kSub;         // tokens per window
 constexpr int kCommitRegs = 1;           // committed tokens per lane held in registers
+constexpr int kFusedLoads = 4;           // counts per thread in the fused append's prefix
+constexpr int kFusedMaxB = kCopyThreads * kFusedLoads;   // batches up to this size: offsets inside append_kernel
 
 __device__ inline void allow_dependent_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -266,7 +268,12 @@ __device__ inline int4 shfl_quad_down(int4 v) {
                      __shfl_down_sync(0xffffffffu, v.z, 1), __shfl_down_sync(0xffffffffu, v.w, 1));
 }
 
-// The copy.  The histories tokens[offsets[0] .. offsets[B]) are contiguous in
+// The copy.  With FUSED (B <= kFusedMaxB = 1024 and sum(ncommit) < 2^31), every CTA
+// first forms the exclusive prefix of the clamped counts in shared memory --
+// what offsets_kernel computes -- and CTA 0 writes out_offsets from it; the
+// shifts below then come from shared memory instead of a second kernel.
+//
+// The histories tokens[offsets[0] .. offsets[B]) are contiguous in
 // the input, and each request's run moves as a block to out_offsets[r].  The
 // input is cut into windows of kWin tokens aligned to 16 bytes; a window is
 // kSub sub-windows of 128 tokens, one int4 per lane each, and each warp takes
@@ -282,11 +289,21 @@ __device__ inline int4 shfl_quad_down(int4 v) {
 // (past 32 requests it falls back to loads).  Everything that reads only the
 // inputs -- the window range, the first windows' loads, the request of the
 // warp's first window (a 32-way search over offsets), the cache's ends and the
-// warp's committed tokens -- is done before waiting for offsets_kernel; after
-// it, one load per lane completes the cache.  The committed tokens of request
-// r are written by warp r (grid-stride).
+// warp's committed tokens -- is done before waiting for offsets_kernel (FUSED:
+// after the previous kernel, since there is no offsets_kernel in between); after
+// the wait, one load per lane completes the cache.  The committed tokens of
+// request r are written by warp r (grid-stride).
+template <bool FUSED>
 __global__ void __launch_bounds__(kCopyThreads, kCopyCtasPerSm) append_kernel(AppendParams p) {
+    extern __shared__ int32_t pre[];                     // FUSED: [B + 1] exclusive prefix of the counts
+    __shared__ int32_t warp_tot[kCopyThreads / 32];
+    const int tid = threadIdx.x;
     const int lane = threadIdx.x & 31;
+    // FUSED: the previous kernel may still be writing any input (the verify step
+    // lets its dependents launch before it writes the counts), so nothing is
+    // read before it completes.  Unfused, the previous kernel is offsets_kernel,
+    // which waited for the inputs' producer before letting this one launch.
+    if (FUSED) wait_for_prerequisite_grid();
     const int64_t gwarp = (int64_t(blockIdx.x) * kCopyThreads + threadIdx.x) >> 5;
     const int64_t nwarps = int64_t(gridDim.x) * (kCopyThreads / 32);
     const int B = p.B;
@@ -324,6 +341,7 @@ __global__ void __launch_bounds__(kCopyThreads, kCopyCtasPerSm) append_kernel(Ap
     const int64_t rc0 = gwarp;
     int64_t nc0 = 0;
     int32_t cv[kCommitRegs];
+    const int64_t rc0_end = (FUSED && rc0 < B) ? p.offsets[rc0 + 1] : 0;
     if (rc0 < B) {
         nc0 = clamped_count(p, rc0);
 #pragma unroll
@@ -352,12 +370,59 @@ __global__ void __launch_bounds__(kCopyThreads, kCopyCtasPerSm) append_kernel(Ap
     const int64_t c_start = (k0 < k1 && rc < B) ? p.offsets[rc] : 0;
     const int64_t c_end = (k0 < k1 && rc < B) ? p.offsets[rc + 1] : 0;
 
-    wait_for_prerequisite_grid();                        // out_offsets are ready
+    wait_for_prerequisite_grid();                        // FUSED: the counts; else: out_offsets
     allow_dependent_launch();
 
-    int64_t c_shift = (k0 < k1 && rc < B) ? p.out_offsets[rc] - c_start : 0;
+    // out_offsets[r] - offsets[r] (FUSED: from the shared prefix)
+    auto shift_of = [&](int64_t r, int64_t off_r) -> int64_t {
+        if (FUSED) return int64_t(pre[r]) - A0;
+        return p.out_offsets[r] - off_r;
+    };
+    if (FUSED) {
+        // counts into shared memory (coalesced), each thread's run summed, a block
+        // scan of the run sums, then the runs rewritten as exclusive prefixes
+        int32_t cnt_r[kFusedLoads];                      // independent loads, then the stores
+#pragma unroll
+        for (int u = 0; u < kFusedLoads; ++u) {
+            const int i = tid + u * kCopyThreads;
+            cnt_r[u] = i < B ? int32_t(clamped_count(p, i)) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kFusedLoads; ++u)
+            if (tid + u * kCopyThreads < B) pre[tid + u * kCopyThreads] = cnt_r[u];
+        __syncthreads();
+        const int per = (B + kCopyThreads - 1) / kCopyThreads;
+        const int i0 = min(tid * per, B), i1 = min(i0 + per, B);
+        int own = 0;
+        for (int i = i0; i < i1; ++i) own += pre[i];
+        int incl = own;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += y;
+        }
+        if (lane == 31) warp_tot[tid >> 5] = incl;
+        __syncthreads();
+        int before = incl - own, total = 0;
+#pragma unroll
+        for (int w = 0; w < kCopyThreads / 32; ++w) {
+            before += w < (tid >> 5) ? warp_tot[w] : 0;
+            total += warp_tot[w];
+        }
+        for (int i = i0; i < i1; ++i) {
+            const int cnt = pre[i];
+            pre[i] = before;
+            before += cnt;
+        }
+        if (tid == 0) pre[B] = total;
+        __syncthreads();
+        if (blockIdx.x == 0)
+            for (int i = tid; i <= B; i += kCopyThreads) p.out_offsets[i] = (p.offsets[i] - A0) + pre[i];
+    }
+
+    int64_t c_shift = (k0 < k1 && rc < B) ? shift_of(rc, c_start) : 0;
     if (rc0 < B) {                                       // committed tokens after the history
-        const int64_t dst = p.out_offsets[rc0 + 1] - nc0;
+        const int64_t dst = (FUSED ? (rc0_end - A0) + pre[rc0 + 1] : p.out_offsets[rc0 + 1]) - nc0;
 #pragma unroll
         for (int c = 0; c < kCommitRegs; ++c)
             if (lane + 32 * c < nc0) p.out_tokens[dst + lane + 32 * c] = cv[c];
@@ -365,7 +430,7 @@ __global__ void __launch_bounds__(kCopyThreads, kCopyCtasPerSm) append_kernel(Ap
     }
     for (int64_t rr = rc0 + nwarps; rr < B; rr += nwarps) {
         const int64_t n = clamped_count(p, rr);
-        const int64_t dst = p.out_offsets[rr + 1] - n;
+        const int64_t dst = (FUSED ? (p.offsets[rr + 1] - A0) + pre[rr + 1] : p.out_offsets[rr + 1]) - n;
         for (int64_t j = lane; j < n; j += 32) p.out_tokens[dst + j] = __ldg(p.commit + rr * p.W + j);
     }
     if (k0 >= k1) return;
@@ -382,7 +447,7 @@ __global__ void __launch_bounds__(kCopyThreads, kCopyCtasPerSm) append_kernel(Ap
             shift = __shfl_sync(0xffffffffu, c_shift, i);
         } else {
             r_end = p.offsets[r + 1];
-            shift = p.out_offsets[r] - p.offsets[r];
+            shift = shift_of(r, p.offsets[r]);
         }
     };
 
@@ -443,11 +508,13 @@ __global__ void __launch_bounds__(kCopyThreads, kCopyCtasPerSm) append_kernel(Ap
 int cuda_fail(cudaError_t e, const char *what) { return lookup_record_cuda_error(e, what); }
 
 template <typename Params>
-int launch_pdl(void (*kernel)(Params), dim3 grid, dim3 block, cudaStream_t stream, const Params &prm) {
+int launch_pdl(void (*kernel)(Params), dim3 grid, dim3 block, cudaStream_t stream, const Params &prm,
+               size_t smem = 0) {
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = grid;
     cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -509,10 +576,14 @@ int lookup_append(const int32_t *tokens, const int64_t *offsets, const int32_t *
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "device query");
+    if (B > 0 && ((reinterpret_cast<uintptr_t>(tokens) | reinterpret_cast<uintptr_t>(out_tokens)) & 3))
+        return LOOKUP_DRAFT_EINVAL;
+    const dim3 grid(unsigned(sms * kCopyCtasPerSm));
+    if (B > 0 && B <= kFusedMaxB && int64_t(B) * W < (int64_t(1) << 31))
+        return launch_pdl(append_kernel<true>, grid, dim3(kCopyThreads), stream, p, size_t(B + 1) * sizeof(int32_t));
     int rc = launch_pdl(offsets_kernel, dim3(1), dim3(kScanThreads), stream, p);
     if (rc != LOOKUP_DRAFT_OK || B == 0) return rc;      // B == 0: out_offsets = {0} only
-    if ((reinterpret_cast<uintptr_t>(tokens) | reinterpret_cast<uintptr_t>(out_tokens)) & 3) return LOOKUP_DRAFT_EINVAL;
-    return launch_pdl(append_kernel, dim3(unsigned(sms * kCopyCtasPerSm)), dim3(kCopyThreads), stream, p);
+    return launch_pdl(append_kernel<false>, grid, dim3(kCopyThreads), stream, p);
 }
 
 }  // extern "C"

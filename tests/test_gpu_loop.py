@@ -250,3 +250,66 @@ def test_decode_loop_matches_oracle(name):
         np.testing.assert_array_equal(host(offsets_g), offsets_o)
         np.testing.assert_array_equal(host(tokens_g)[:offsets_o[-1]], tokens_o)
         committed = nc_o
+
+
+@pytest.mark.parametrize("name,B_sub", [("tiny", None), ("chats", 1000), ("chats", None)])
+def test_decode_loop_back_to_back(name, B_sub):
+    """The same loop with no host synchronisation inside it: every kernel runs
+    behind the previous one on the stream (programmatic dependent launch), the
+    synthetic model and target are formed on the device with torch, and only the
+    final histories and the last draft are compared with the oracle's loop.
+    Batches of at most 1024 requests take the append that forms the new offsets
+    itself, right behind the verify step that writes the counts."""
+    w = gen.make_workload(name)
+    tokens, offsets = w.tokens, w.offsets
+    if B_sub is not None:
+        offsets = offsets[:B_sub + 1]
+        tokens = tokens[:offsets[-1]]
+    B, H, T = offsets.shape[0] - 1, 7, 8
+    K = P = H + T
+    steps = 4
+    rng = gen.rng_for(B, 78)
+    md_rand = rng.integers(0, 50, size=(steps, B, H), dtype=np.int64).astype(np.int32)
+    pick = rng.random((steps, B)) < 0.33
+    tgt_rand = rng.integers(0, 50, size=(steps, B, P + 1), dtype=np.int64).astype(np.int32)
+    f = rng.integers(0, P + 1, size=(steps, B))
+    # the oracle's loop
+    t_o, o_o = tokens, offsets
+    st_o = np.zeros((B, 3), np.int32)
+    committed = np.full(B, H + 1, np.int32)
+    for s in range(steps):
+        d_o, l_o, p_o, m_o = oracle.lookup_draft(t_o, o_o, w.min_m, w.max_m, K, threads=8)
+        lg_o = oracle.schedule(m_o, committed, st_o, H, T)
+        md = md_rand[s].copy()
+        md[pick[s]] = d_o[pick[s], :H]
+        blk_o, len_o, pm_o = oracle.fuse(d_o, m_o, md, lg_o, H, T)
+        target = tgt_rand[s].copy()
+        for r in range(B):
+            target[r, :f[s, r]] = blk_o[r, :f[s, r]]
+        acc_o, com_o, nc_o = oracle.verify(blk_o, len_o, target)
+        t_o, o_o = oracle.append(t_o, o_o, com_o, nc_o)
+        committed = nc_o
+    d_last, _, _, m_last = oracle.lookup_draft(t_o, o_o, w.min_m, w.max_m, K, threads=8)
+    # the device's loop, all inputs uploaded first
+    md_g, pick_g, tgt_g, f_g = dev(md_rand), dev(pick), dev(tgt_rand), dev(f)
+    cols = torch.arange(P + 1, device="cuda")
+    t_g, o_g = dev(tokens), dev(offsets)
+    st_g = torch.zeros((B, 3), dtype=torch.int32, device="cuda")
+    long_g = torch.zeros(B, dtype=torch.int32, device="cuda")
+    com_g = torch.full((B,), H + 1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    for s in range(steps):
+        d_g, l_g, p_g, m_g = pkg.lookup_draft_ex(t_g, o_g, w.min_m, w.max_m, K)
+        pkg.lookup_schedule(m_g, com_g, st_g, H, T, out=long_g)
+        mdl = torch.where(pick_g[s][:, None], d_g[:, :H], md_g[s])
+        blk_g, len_g, pm_g = pkg.lookup_fuse(d_g, m_g, mdl, long_g, H, T)
+        prefix = cols[None, :] < f_g[s][:, None]
+        target_g = tgt_g[s].clone()
+        target_g[:, :P] = torch.where(prefix[:, :P], blk_g, target_g[:, :P])
+        acc_g, commit_g, com_g = pkg.lookup_verify(blk_g, len_g, target_g)
+        t_g, o_g = pkg.lookup_append(t_g, o_g, commit_g, com_g)
+    d_g, l_g, p_g, m_g = pkg.lookup_draft_ex(t_g, o_g, w.min_m, w.max_m, K)
+    np.testing.assert_array_equal(host(o_g), o_o)
+    np.testing.assert_array_equal(host(t_g)[:o_o[-1]], t_o)
+    np.testing.assert_array_equal(host(m_g), m_last)
+    np.testing.assert_array_equal(host(d_g), d_last)
