@@ -8,6 +8,8 @@
 #include <cstdint>
 #include <cstring>
 
+#include <nvtx3/nvToolsExt.h>
+
 // Records a CUDA failure for lookup_draft_last_cuda_error (lookup_draft.cu);
 // returns LOOKUP_DRAFT_ECUDA.
 int lookup_record_cuda_error(cudaError_t e, const char *what);
@@ -75,5 +77,14 @@ inline unsigned capped_grid(int64_t want, int64_t cap) {
     if (want < 1) want = 1;
     return unsigned(want < cap ? want : cap);
 }
+
+// An NVTX range over one library call: a span per call in a timeline tool,
+// nearly free when no tool is attached (header-only NVTX).
+struct TraceRange {
+    explicit TraceRange(const char *name) { nvtxRangePushA(name); }
+    ~TraceRange() { nvtxRangePop(); }
+    TraceRange(const TraceRange &) = delete;
+    TraceRange &operator=(const TraceRange &) = delete;
+};
 
 }  // namespace lkd

@@ -434,6 +434,7 @@ size_t lookup_ctx_bytes(int64_t slots) {
 
 int lookup_ctx_build(const int32_t *tokens, const int64_t *base, const int32_t *len, int32_t B, int32_t n_min,
                      int32_t n_max, void *cache, int64_t slots, struct CUstream_st *stream) {
+    lkd::TraceRange trace_("lookup_ctx_build");
     if (B < 0 || B > 65536 || !params_ok(n_min, n_max, slots) || !cache || !aligned16(cache))
         return LOOKUP_DRAFT_EINVAL;
     if (B > 0 && (!tokens || !base || !len)) return LOOKUP_DRAFT_EINVAL;
@@ -468,6 +469,7 @@ int lookup_ctx_build(const int32_t *tokens, const int64_t *base, const int32_t *
 int lookup_ctx_append(int32_t *tokens, const int64_t *base, int32_t *len, const int32_t *cap, const int32_t *commit,
                       const int32_t *ncommit, int32_t B, int32_t W, int32_t n_min, int32_t n_max, void *cache,
                       int64_t slots, int32_t *out_status, struct CUstream_st *stream) {
+    lkd::TraceRange trace_("lookup_ctx_append");
     if (B < 0 || B > 65536 || W < 0 || !params_ok(n_min, n_max, slots)) return LOOKUP_DRAFT_EINVAL;
     if (B == 0) return LOOKUP_DRAFT_OK;
     if (!tokens || !base || !len || !cap || !ncommit || (W > 0 && !commit) || !cache || !aligned16(cache))
@@ -502,6 +504,7 @@ int lookup_ctx_draft(const int32_t *tokens, const int64_t *base, const int32_t *
                      int32_t n_max, int32_t K, const int32_t *min_count, const int32_t *share_num,
                      const int32_t *share_den, const void *cache, int64_t slots, int32_t *out_draft,
                      int32_t *out_len, struct CUstream_st *stream) {
+    lkd::TraceRange trace_("lookup_ctx_draft");
     if (B < 0 || B > 65536 || K < 0 || K > LOOKUP_DRAFT_MAX_K || !params_ok(n_min, n_max, slots))
         return LOOKUP_DRAFT_EINVAL;
     if (!min_count || !share_num || !share_den) return LOOKUP_DRAFT_EINVAL;

@@ -58,6 +58,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 namespace {
 
 // ---------------------------------------------------------------- tuning ----
@@ -913,6 +915,15 @@ __global__ void __launch_bounds__(kLaneFillThreads) fill_lanes_kernel(FillParams
 }
 
 // ------------------------------------------------------------- host side ----
+// An NVTX range over one library call: a span per call in a timeline tool,
+// nearly free when no tool is attached (header-only NVTX).
+struct TraceRange {
+    explicit TraceRange(const char *name) { nvtxRangePushA(name); }
+    ~TraceRange() { nvtxRangePop(); }
+    TraceRange(const TraceRange &) = delete;
+    TraceRange &operator=(const TraceRange &) = delete;
+};
+
 thread_local char g_cuda_msg[256] = "";
 
 int cuda_fail(cudaError_t e, const char *what) {
@@ -1191,6 +1202,7 @@ extern "C" {
 int lookup_draft_ex(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t min_m, int32_t max_m,
                     int32_t K, int32_t *out_draft, int32_t *out_len, int32_t *out_pos, int32_t *out_mlen,
                     struct CUstream_st *stream) {
+    TraceRange trace_("lookup_draft_ex");
     g_cuda_msg[0] = '\0';
     int rc = check_common(tokens, offsets, B, min_m, max_m, K);
     if (rc == LOOKUP_DRAFT_OK) rc = check_outputs(B, K, out_draft, out_len, out_pos, out_mlen);
@@ -1200,6 +1212,7 @@ int lookup_draft_ex(const int32_t *tokens, const int64_t *offsets, int32_t B, in
 
 int lookup_draft(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t min_m, int32_t max_m, int32_t K,
                  int32_t *out_draft, int32_t *out_len, int32_t *out_pos, struct CUstream_st *stream) {
+    TraceRange trace_("lookup_draft");
     return lookup_draft_ex(tokens, offsets, B, min_m, max_m, K, out_draft, out_len, out_pos, nullptr, stream);
 }
 
@@ -1213,6 +1226,7 @@ size_t lookup_draft_workspace_bytes(int32_t B) {
 
 int lookup_draft_scan(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t min_m, int32_t max_m,
                       void *workspace, size_t workspace_bytes, struct CUstream_st *stream) {
+    TraceRange trace_("lookup_draft_scan");
     g_cuda_msg[0] = '\0';
     int rc = check_common(tokens, offsets, B, min_m, max_m, 0);
     if (rc != LOOKUP_DRAFT_OK || B == 0) return rc;
@@ -1227,6 +1241,7 @@ int lookup_draft_scan(const int32_t *tokens, const int64_t *offsets, int32_t B, 
 int lookup_draft_fill(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t min_m, int32_t max_m,
                       int32_t K, const void *workspace, size_t workspace_bytes, int32_t *out_draft, int32_t *out_len,
                       int32_t *out_pos, int32_t *out_mlen, struct CUstream_st *stream) {
+    TraceRange trace_("lookup_draft_fill");
     g_cuda_msg[0] = '\0';
     int rc = check_common(tokens, offsets, B, min_m, max_m, K);
     if (rc == LOOKUP_DRAFT_OK) rc = check_outputs(B, K, out_draft, out_len, out_pos, out_mlen);
@@ -1243,6 +1258,7 @@ int lookup_draft_fill(const int32_t *tokens, const int64_t *offsets, int32_t B, 
 int lookup_draft_host(const int32_t *h_tokens, const int64_t *h_offsets, int32_t B, int32_t min_m, int32_t max_m,
                       int32_t K, int32_t *h_out_draft, int32_t *h_out_len, int32_t *h_out_pos,
                       struct CUstream_st *stream) {
+    TraceRange trace_("lookup_draft_host");
     g_cuda_msg[0] = '\0';
     int rc = check_common(h_tokens, h_offsets, B, min_m, max_m, K);
     if (rc == LOOKUP_DRAFT_OK) rc = check_outputs(B, K, h_out_draft, h_out_len, h_out_pos, nullptr);
@@ -1315,6 +1331,7 @@ int lookup_draft_host(const int32_t *h_tokens, const int64_t *h_offsets, int32_t
 int lookup_draft_noalloc(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t min_m, int32_t max_m,
                          int32_t K, int32_t *out_draft, int32_t *out_len, int32_t *out_pos,
                          struct CUstream_st *stream) {
+    TraceRange trace_("lookup_draft_noalloc");
     g_cuda_msg[0] = '\0';
     int rc = check_common(tokens, offsets, B, min_m, max_m, K);
     if (rc == LOOKUP_DRAFT_OK) rc = check_outputs(B, K, out_draft, out_len, out_pos, nullptr);

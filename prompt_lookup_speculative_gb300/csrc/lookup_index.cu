@@ -566,6 +566,7 @@ size_t lookup_index_bytes(int64_t slots) {
 
 int lookup_index_build(const int32_t *tokens, const int64_t *base, const int32_t *len, int32_t B, int32_t min_m,
                        int32_t max_m, void *index, int64_t slots, int32_t hash_bits, struct CUstream_st *stream) {
+    lkd::TraceRange trace_("lookup_index_build");
     if (B < 0 || !params_ok(min_m, max_m, hash_bits, slots) || !index || !aligned16(index)) return LOOKUP_DRAFT_EINVAL;
     if (B > 0 && (!tokens || !base || !len)) return LOOKUP_DRAFT_EINVAL;
     int sms = 0;
@@ -601,6 +602,7 @@ int lookup_index_build(const int32_t *tokens, const int64_t *base, const int32_t
 int lookup_index_append(int32_t *tokens, const int64_t *base, int32_t *len, const int32_t *cap, const int32_t *commit,
                         const int32_t *ncommit, int32_t B, int32_t W, int32_t min_m, int32_t max_m, void *index,
                         int64_t slots, int32_t hash_bits, int32_t *out_status, struct CUstream_st *stream) {
+    lkd::TraceRange trace_("lookup_index_append");
     if (B < 0 || W < 0 || !params_ok(min_m, max_m, hash_bits, slots)) return LOOKUP_DRAFT_EINVAL;
     if (B == 0) return LOOKUP_DRAFT_OK;
     if (!tokens || !base || !len || !cap || !ncommit || (W > 0 && !commit) || !index || !aligned16(index))
@@ -640,6 +642,7 @@ int lookup_index_draft(const int32_t *tokens, const int64_t *base, const int32_t
                        int32_t max_m, int32_t K, const void *index, int64_t slots, int32_t hash_bits,
                        int32_t *out_draft, int32_t *out_len, int32_t *out_pos, int32_t *out_mlen,
                        int32_t *out_fallback, struct CUstream_st *stream) {
+    lkd::TraceRange trace_("lookup_index_draft");
     if (B < 0 || K < 0 || K > LOOKUP_DRAFT_MAX_K || !params_ok(min_m, max_m, hash_bits, slots))
         return LOOKUP_DRAFT_EINVAL;
     if (B == 0) return LOOKUP_DRAFT_OK;

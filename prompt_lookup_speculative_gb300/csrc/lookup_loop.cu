@@ -19,6 +19,7 @@
 
 #include "lookup_draft.h"
 #include "lookup_loop.h"
+#include "common.cuh"
 
 #include <cuda_runtime.h>
 
@@ -535,6 +536,7 @@ int lookup_fuse(const int32_t *lookup_draft, const int32_t *lookup_mlen, const i
                 const int32_t *long_block, int32_t B, int32_t K, int32_t H, int32_t T, int32_t replace_min,
                 int32_t agree_min, int32_t agree_n, int32_t tail_min, int32_t *out_block, int32_t *out_len,
                 int32_t *out_point_mass, struct CUstream_st *stream) {
+    lkd::TraceRange trace_("lookup_fuse");
     if (B < 0 || H < 1 || T < 0 || int64_t(H) + T > kMaxBlock || K < H + T || agree_n < 0 || agree_n > H)
         return LOOKUP_DRAFT_EINVAL;
     if (B == 0) return LOOKUP_DRAFT_OK;
@@ -548,6 +550,7 @@ int lookup_fuse(const int32_t *lookup_draft, const int32_t *lookup_mlen, const i
 int lookup_schedule(const int32_t *lookup_mlen, const int32_t *committed, int32_t B, int32_t H, int32_t T,
                     int32_t tail_min, int32_t slack, int32_t enter_steps, int32_t sticky, int32_t *state,
                     int32_t *out_long, struct CUstream_st *stream) {
+    lkd::TraceRange trace_("lookup_schedule");
     if (B < 0 || H < 1 || T < 0 || enter_steps < 1 || sticky < 0 || slack < 0) return LOOKUP_DRAFT_EINVAL;
     if (B == 0) return LOOKUP_DRAFT_OK;
     if (!lookup_mlen || !committed || !state || !out_long) return LOOKUP_DRAFT_EINVAL;
@@ -558,6 +561,7 @@ int lookup_schedule(const int32_t *lookup_mlen, const int32_t *committed, int32_
 int lookup_verify(const int32_t *block, const int32_t *len, const int32_t *target, const float *probs,
                   const float *qprobs, const int32_t *point_mass, const float *u, int32_t B, int32_t P,
                   int32_t *out_accepted, int32_t *out_commit, int32_t *out_ncommit, struct CUstream_st *stream) {
+    lkd::TraceRange trace_("lookup_verify");
     if (B < 0 || P < 0 || P > kMaxBlock) return LOOKUP_DRAFT_EINVAL;
     if (B == 0) return LOOKUP_DRAFT_OK;
     if ((P > 0 && !block) || !len || !target || (probs && !u) || !out_accepted || !out_commit || !out_ncommit)
@@ -568,6 +572,7 @@ int lookup_verify(const int32_t *block, const int32_t *len, const int32_t *targe
 
 int lookup_append(const int32_t *tokens, const int64_t *offsets, const int32_t *commit, const int32_t *ncommit,
                   int32_t B, int32_t W, int32_t *out_tokens, int64_t *out_offsets, struct CUstream_st *stream) {
+    lkd::TraceRange trace_("lookup_append");
     if (B < 0 || W < 0) return LOOKUP_DRAFT_EINVAL;
     if (!offsets || !out_offsets || (B > 0 && (!tokens || !ncommit || (W > 0 && !commit) || !out_tokens)))
         return LOOKUP_DRAFT_EINVAL;
