@@ -671,38 +671,33 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                     // rare hits are masked to that request's range
                     const bool hasA = loA <= hiA, hasB = loB <= hiB;
                     const int jlo = (hasA ? loA : loB) >> 2, jhi = (hasB ? hiB : hiA) >> 2;
+                    // a quad is B's when it reaches B's first candidate (the gap before it
+                    // is at least 3 elements), else A's; the range masks apply on the rare
+                    // path only, so a gap or edge quad costs nothing extra
+                    auto test2 = [&](int j, const int4 &p, const int4 &c) {
+                        const bool inB = hasB && 4 * j + 3 >= loB;
+                        unsigned h = quad_hits<D>(p, c, inB ? b0 : a0, inB ? b1 : a1, inB ? b2 : a2, inB ? b3 : a3) &
+                                     range_mask(4 * j, inB ? loB : loA, inB ? hiB : hiA);
+                        if (!inB && !hasA) h = 0u;
+                        while (h) {
+                            const int e = __ffs(h) - 1;
+                            h &= h - 1;
+                            extend2(4 * j + e, inB);
+                        }
+                    };
                     for (int j = jlo + lane; j <= jhi; j += 64) {
                         const int j2 = j + 32;
                         const bool has2 = j2 <= jhi;
                         const int jj2 = has2 ? j2 : j;
                         const int4 c0 = sq[j], c1 = sq[jj2], p0 = sq[j - 1], p1 = sq[jj2 - 1];
-                        const bool inA0 = hasA && 4 * j + 3 >= loA && 4 * j <= hiA;
-                        const bool inB0 = hasB && 4 * j + 3 >= loB && 4 * j <= hiB;
-                        const bool inA1 = has2 && hasA && 4 * j2 + 3 >= loA && 4 * j2 <= hiA;
-                        const bool inB1 = has2 && hasB && 4 * j2 + 3 >= loB && 4 * j2 <= hiB;
-                        const bool any0 = (inA0 | inB0) && quad_any<D>(p0, c0, inB0 ? b0 : a0, inB0 ? b1 : a1,
-                                                                     inB0 ? b2 : a2, inB0 ? b3 : a3);
-                        const bool any1 = (inA1 | inB1) && quad_any<D>(p1, c1, inB1 ? b0 : a0, inB1 ? b1 : a1,
-                                                                     inB1 ? b2 : a2, inB1 ? b3 : a3);
+                        const bool b0q = hasB && 4 * j + 3 >= loB, b1q = hasB && 4 * j2 + 3 >= loB;
+                        const bool any0 =
+                            quad_any<D>(p0, c0, b0q ? b0 : a0, b0q ? b1 : a1, b0q ? b2 : a2, b0q ? b3 : a3);
+                        const bool any1 =
+                            has2 && quad_any<D>(p1, c1, b1q ? b0 : a0, b1q ? b1 : a1, b1q ? b2 : a2, b1q ? b3 : a3);
                         if (any0 | any1) {
-                            unsigned h0 = any0 ? quad_hits<D>(p0, c0, inB0 ? b0 : a0, inB0 ? b1 : a1, inB0 ? b2 : a2,
-                                                              inB0 ? b3 : a3) &
-                                                     range_mask(4 * j, inB0 ? loB : loA, inB0 ? hiB : hiA)
-                                               : 0u;
-                            unsigned h1 = any1 ? quad_hits<D>(p1, c1, inB1 ? b0 : a0, inB1 ? b1 : a1, inB1 ? b2 : a2,
-                                                              inB1 ? b3 : a3) &
-                                                     range_mask(4 * j2, inB1 ? loB : loA, inB1 ? hiB : hiA)
-                                               : 0u;
-                            while (h0) {
-                                const int e = __ffs(h0) - 1;
-                                h0 &= h0 - 1;
-                                extend2(4 * j + e, inB0);
-                            }
-                            while (h1) {
-                                const int e = __ffs(h1) - 1;
-                                h1 &= h1 - 1;
-                                extend2(4 * j2 + e, inB1);
-                            }
+                            if (any0) test2(j, p0, c0);
+                            if (any1) test2(j2, p1, c1);
                         }
                     }
                     // A ends here; B continues into the next tile with its keys pending
