@@ -693,8 +693,8 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                         const bool b0q = hasB && 4 * j + 3 >= loB, b1q = hasB && 4 * j2 + 3 >= loB;
                         const bool any0 =
                             quad_any<D>(p0, c0, b0q ? b0 : a0, b0q ? b1 : a1, b0q ? b2 : a2, b0q ? b3 : a3);
-                        const bool any1 =
-                            has2 && quad_any<D>(p1, c1, b1q ? b0 : a0, b1q ? b1 : a1, b1q ? b2 : a2, b1q ? b3 : a3);
+                        const bool any1 =   // the test runs either way: no branch on has2
+                            quad_any<D>(p1, c1, b1q ? b0 : a0, b1q ? b1 : a1, b1q ? b2 : a2, b1q ? b3 : a3) & has2;
                         if (any0 | any1) {
                             if (any0) test2(j, p0, c0);
                             if (any1) test2(j2, p1, c1);
