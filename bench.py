@@ -196,11 +196,16 @@ HOST_SIDE_MARKER = b"// --------------------------------------------------------
 
 def scan_source_hash() -> str:
     """sha256 (16 hex) of the device code of csrc/lookup_draft.cu: the file up to
-    its host-side marker, so host-only edits keep a kernel capture valid."""
+    its host-side marker, with comments and layout removed, so host-only and
+    comment-only edits keep a kernel capture valid."""
     with open(SCAN_SOURCE, "rb") as f:
         src = f.read()
     cut = src.find(HOST_SIDE_MARKER)
-    return hashlib.sha256(src if cut < 0 else src[:cut]).hexdigest()[:16]
+    code = (src if cut < 0 else src[:cut]).decode("utf-8")
+    code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)          # block comments
+    code = re.sub(r"//[^\n]*", " ", code)                         # line comments
+    code = " ".join(code.split())                                  # layout
+    return hashlib.sha256(code.encode("utf-8")).hexdigest()[:16]
 
 
 def recorded_traffic(workload: str):

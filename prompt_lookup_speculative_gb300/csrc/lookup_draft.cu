@@ -792,7 +792,8 @@ __global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_kernel(F
     const int64_t L = o1 - o0;
     // The request's slots are those of warps v0 .. v1, the ones holding its first
     // and last quads (empty warp ranges own none).  All of that follows from the
-    // offsets, so it is worked out before the wait, with the first round of loads.
+    // offsets, so it is worked out before the wait, with which of the first round's
+    // loads to make.
     Partition P{};
     int64_t v0 = 0, v1 = -1;
     if (r < prm.B && L > 0) {
