@@ -33,6 +33,10 @@ requests of 25,000 tokens, 6.4 MB of int32 history).  Prints one JSON line.
   context_cache context-cache drafting (llama.cpp's rule) on the same batch:
                 build time and size, the draft (checked against the oracle) and
                 the in-place append.
+  workloads     the step and the scan on each of the five workloads (tiny,
+                recitation25k, periodic, ragged262k, chats), timed as above, with
+                the scan's GB/s and fraction of the measured copy bandwidth and a
+                whole-batch check of the outputs against the oracle.
 
 --impl reference times that oracle as the comparison arm on the same workload.
 Multi-GPU (torchrun, one rank per GPU): every rank drafts its own batch (weak
@@ -86,6 +90,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-index", action="store_true",
                     help="skip the timing of the incremental n-gram index")
     ap.add_argument("--no-ctx", action="store_true", help="skip the timing of context-cache drafting")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the step and scan timings of every workload")
     ap.add_argument("--loop-only", action="store_true",
                     help="time only the decode-loop steps (replays = steps / copies of the batch)")
     return ap.parse_args(argv)
@@ -401,6 +407,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         want = oracle.lookup_draft(w.tokens, w.offsets, min_m, max_m, K, threads=os.cpu_count() or 1)
         index = measure_index(lib, pkg, w, dev, stream, want)
     ctx = None if args.no_ctx else measure_ctx(lib, pkg, w, dev, stream)
+    workloads = None
+    if not args.no_workloads:
+        workloads = measure_workloads(lib, pkg, dev, stream, list(gen.DEFAULT_SEED), 1000 * rank, reps)
 
     # e2e: host buffers through lookup_draft_host, copies inside every step
     h_tok = tok_host.pin_memory()
@@ -493,6 +502,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         "loop_steps": loop,
         "index": index,
         "context_cache": ctx,
+        "workloads": workloads,
         "gpu_launches": 2 * args.steps,
         "parity_with_oracle": bool(parity),
         "clocks": clocks.summary(),
@@ -857,6 +867,85 @@ def measure_ctx(lib, pkg, w, dev, stream) -> dict:
     }
     del cc
     return res
+
+
+# ------------------------------------------------------------ workloads ----
+def measure_workloads(lib, pkg, dev, stream, names, seed_offset: int, reps_cap: int) -> dict:
+    """The draft step and the scan on each named workload, timed the way the main
+    line times its own: ncopy calls over rotating device copies (> 2x L2 in total)
+    captured in one CUDA graph, replayed back to back, CUDA events on the launching
+    stream.  Per workload: step and scan microseconds, the scan's GB/s (4 bytes per
+    history token) against the measured copy bandwidth, and whether the step's
+    outputs equal the oracle's on the whole batch."""
+    import numpy as np
+    import torch
+
+    import gen
+    import oracle
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2**20))
+    peak, peak_kind = measured_hbm_peak()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    out = {}
+    for name in names:
+        w = gen.make_workload(name, gen.DEFAULT_SEED[name] + seed_offset)
+        B, K = w.B, w.K
+        ncopy = max(3, math.ceil(2 * l2 / max(w.history_bytes, 1)) + 1)
+        tok_host, off_host = torch.from_numpy(w.tokens), torch.from_numpy(w.offsets)
+        toks = [tok_host.to(dev) for _ in range(ncopy)]
+        offs = [off_host.to(dev) for _ in range(ncopy)]
+        draft = torch.empty((B, K), dtype=torch.int32, device=dev)
+        length = torch.empty(B, dtype=torch.int32, device=dev)
+        pos = torch.empty(B, dtype=torch.int32, device=dev)
+        ws_bytes = pkg.workspace_bytes(B, dev)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
+        def step(j, hc):
+            rc = lib.lookup_draft(toks[j].data_ptr(), offs[j].data_ptr(), B, w.min_m, w.max_m, K,
+                                  draft.data_ptr(), length.data_ptr(), pos.data_ptr(), hc)
+            if rc != 0:
+                raise pkg.LookupDraftError(rc, lib)
+
+        def scan(j, hc):
+            rc = lib.lookup_draft_scan(toks[j].data_ptr(), offs[j].data_ptr(), B, w.min_m, w.max_m,
+                                       ws.data_ptr(), ws_bytes, hc)
+            if rc != 0:
+                raise pkg.LookupDraftError(rc, lib)
+
+        def timed(fn) -> float:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                hc = int(torch.cuda.current_stream().cuda_stream)
+                for j in range(ncopy):
+                    fn(j, hc)
+            reps = max(10, min(reps_cap, 20000 // ncopy))
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    g.replay()
+                ev0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                ev1.record(stream)
+            torch.cuda.synchronize(dev)
+            return 1000.0 * ev0.elapsed_time(ev1) / (reps * ncopy)
+
+        step_us = timed(step)
+        got = (draft.cpu().numpy(), length.cpu().numpy(), pos.cpu().numpy())
+        scan_us = timed(scan)
+        want = oracle.lookup_draft(w.tokens, w.offsets, w.min_m, w.max_m, K, threads=os.cpu_count() or 1)
+        parity = all(np.array_equal(a, b) for a, b in zip(got, want[:3]))
+        gbs = w.history_bytes / (scan_us * 1e-6) / 1e9
+        out[name] = {"B": B, "history_bytes": int(w.history_bytes), "seed": int(w.seed),
+                     "step_us": round(step_us, 3), "scan_us": round(scan_us, 3),
+                     "scan_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                     "copies": ncopy, "parity_with_oracle": bool(parity)}
+        del toks, offs, ws
+        torch.cuda.synchronize(dev)
+    return {"peak_gbs": peak, "peak_kind": f"{peak_kind} copy bandwidth",
+            "method": "per workload: calls over rotating device copies (> 2x L2) captured in one CUDA graph, "
+                      "replayed back to back; CUDA events on the launching stream",
+            "workloads": out}
 
 
 # ------------------------------------------------------------------ CPU ----
