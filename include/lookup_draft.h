@@ -73,8 +73,9 @@ struct CUstream_st;                     /* same type as cudaStream_t */
  * out_pos    device, int32 [B]: start p of the occurrence in the request, or -1
  * stream     CUDA stream all work is enqueued on
  *
- * Scratch: B + (number of scan CTAs) 64-bit words, taken from and returned to a
- * library-owned, stream-ordered CUDA memory pool of the current device.
+ * Scratch: B + 16 * (number of scan CTAs, one per SM) 64-bit words, taken from
+ * and returned to a library-owned, stream-ordered CUDA memory pool of the
+ * current device.
  * Errors: LOOKUP_DRAFT_EINVAL for null pointers (with B > 0), bad m range, K out of
  * range, or misaligned tokens/offsets; LOOKUP_DRAFT_ECUDA when an allocation or
  * launch fails.
@@ -109,7 +110,8 @@ size_t lookup_draft_workspace_bytes(int32_t B);
  *
  * lookup_draft_scan: the split-history scan.  Every history token is read once;
  *   each candidate end position tests the last suffix token first and extends
- *   survivors backwards; the best (m, p) per request and per scan CTA is left in
+ *   survivors backwards; the best (m, p) per request and per scan warp range (16
+ *   contiguous ranges per scan CTA) is left in
  *   `workspace` (device, >= lookup_draft_workspace_bytes(B) bytes, 8-byte aligned;
  *   needs no initialisation).
  * lookup_draft_fill: reduces those partial results and writes out_draft, out_len,
