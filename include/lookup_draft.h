@@ -137,7 +137,10 @@ int lookup_draft_fill(const int32_t *tokens, const int64_t *offsets, int32_t B,
  * synchronises the stream before returning.  Page-locked output arrays that the
  * device can address (cudaHostAlloc / cudaHostRegister memory) are written by
  * the draft-fill kernel directly; other host memory receives the outputs by
- * copies.  Pinned host memory gives the fastest copies; pageable memory works.  The host offsets are checked
+ * copies.  Page-locked input arrays that the device can address are read by the
+ * device itself over the host link (a copy kernel, with the scan launched behind
+ * it); other input memory goes through copy-engine transfers.  Pinned host
+ * memory is fastest; pageable memory works.  The host offsets are checked
  * (non-decreasing, offsets[0] >= 0, every history < 2^31 tokens):
  * LOOKUP_DRAFT_EINVAL if not.
  */

@@ -910,6 +910,42 @@ __global__ void __launch_bounds__(kLaneFillThreads) fill_lanes_kernel(FillParams
     if (live) write_draft(prm, r, o0, L, key, 0, 1, true);
 }
 
+// ------------------------------------------------------ host-input copy ----
+// lookup_draft_host with page-locked inputs: the device reads the batch straight
+// from host memory over the host link, with 16-byte loads, kCopyUnroll of them in
+// flight per thread, and writes the device copies the scan reads.  A kernel starts
+// sooner than a copy-engine transfer, and the scan behind it is launched while it
+// runs (programmatic dependent launch) and only waits for its results.
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;
+constexpr int kCopyCtasPerSm = 2;      // fit beside a scan CTA (its registers leave room for two)
+
+struct CopyParams {
+    const int4 *src;                   // host memory the device can address, 16-byte units
+    int4 *dst;                         // device
+    int64_t n16;
+    const int64_t *src_off;            // host offsets (B + 1 of them), device-addressable
+    int64_t *dst_off;
+    int32_t n_off;
+};
+
+__global__ void __launch_bounds__(kCopyThreads) host_copy_kernel(CopyParams prm) {
+    allow_dependent_launch();
+    wait_for_prerequisite_grid();      // the destination is stream-ordered scratch
+    const int64_t stride = int64_t(gridDim.x) * kCopyThreads;
+    const int64_t t = int64_t(blockIdx.x) * kCopyThreads + threadIdx.x;
+    for (int64_t i = t; i < prm.n_off; i += stride) prm.dst_off[i] = prm.src_off[i];
+    int64_t i = t;
+    for (; i + (kCopyUnroll - 1) * stride < prm.n16; i += kCopyUnroll * stride) {
+        int4 v[kCopyUnroll];
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) v[u] = prm.src[i + u * stride];
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) prm.dst[i + u * stride] = v[u];
+    }
+    for (; i < prm.n16; i += stride) prm.dst[i] = prm.src[i];
+}
+
 // ------------------------------------------------------------- host side ----
 // An NVTX range over one library call: a span per call in a timeline tool,
 // nearly free when no tool is attached (header-only NVTX).
@@ -935,9 +971,9 @@ int cuda_fail(cudaError_t e, const char *what) {
 
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 
-// The device address of page-locked host memory the device can write, else
+// The device address of page-locked host memory the device can address, else
 // nullptr (pageable or unknown memory).
-int32_t *mapped_host(int32_t *p) {
+const void *mapped_host_const(const void *p) {
     if (!p) return nullptr;
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
@@ -945,8 +981,10 @@ int32_t *mapped_host(int32_t *p) {
         return nullptr;
     }
     if (a.type != cudaMemoryTypeHost || !a.devicePointer) return nullptr;
-    return static_cast<int32_t *>(a.devicePointer);
+    return a.devicePointer;
 }
+
+int32_t *mapped_host(int32_t *p) { return static_cast<int32_t *>(const_cast<void *>(mapped_host_const(p))); }
 
 struct DeviceState {
     bool ready = false;
@@ -1114,6 +1152,23 @@ int launch_fill(const DeviceState &st, const int32_t *tokens, const int64_t *off
     return LOOKUP_DRAFT_OK;
 }
 
+cudaError_t launch_host_copy(const DeviceState &st, const CopyParams &cp, cudaStream_t stream) {
+    const int64_t want = (cp.n16 + kCopyThreads - 1) / kCopyThreads;
+    const int64_t cap = int64_t(st.sms) * kCopyCtasPerSm;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(unsigned(want < 1 ? 1 : (want < cap ? want : cap)));
+    cfg.blockDim = dim3(kCopyThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, host_copy_kernel, cp);
+}
+
 int run_step(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t min_m, int32_t max_m, int32_t K,
              int32_t *out_draft, int32_t *out_len, int32_t *out_pos, int32_t *out_mlen, cudaStream_t stream) {
     DeviceState *st = nullptr;
@@ -1270,7 +1325,18 @@ int lookup_draft_host(const int32_t *h_tokens, const int64_t *h_offsets, int32_t
 
     const int64_t first = h_offsets[0];
     const size_t n_tok = size_t(h_offsets[B] - first);
-    const size_t tok_bytes = (n_tok * 4 + 15) & ~size_t(15);
+    // Page-locked inputs the device can address are read by host_copy_kernel: the
+    // whole 16-byte units of their device-side address range (never past the
+    // pages that hold the tokens), so the device copy keeps the tokens' 16-byte
+    // phase.  Other host memory goes through copy-engine transfers.
+    const void *m_tok = n_tok ? mapped_host_const(h_tokens + first) : nullptr;
+    const void *m_off = mapped_host_const(h_offsets);
+    const bool kernel_copy = m_off && (n_tok == 0 || m_tok);
+    const uintptr_t src_t = kernel_copy && n_tok ? reinterpret_cast<uintptr_t>(m_tok) : 0;
+    const uintptr_t src_lo = src_t & ~uintptr_t(15);
+    const uintptr_t src_hi = (src_t + n_tok * 4 + 15) & ~uintptr_t(15);
+    const size_t phase = size_t(src_t - src_lo);
+    const size_t tok_bytes = kernel_copy ? size_t(src_hi - src_lo) : ((n_tok * 4 + 15) & ~size_t(15));
     const size_t off_bytes = (size_t(B) + 1) * 8;
     const size_t out_words = size_t(B) * size_t(K) + 2 * size_t(B);
     const size_t ws_bytes = workspace_bytes_for(B, grid_for(*st));
@@ -1278,7 +1344,7 @@ int lookup_draft_host(const int32_t *h_tokens, const int64_t *h_offsets, int32_t
     void *buf = nullptr;
     LD_CUDA(cudaMallocFromPoolAsync(&buf, total, st->pool, stream));
     unsigned char *base = static_cast<unsigned char *>(buf);
-    int32_t *d_tok = reinterpret_cast<int32_t *>(base);
+    int32_t *d_tok = reinterpret_cast<int32_t *>(base + phase);
     int64_t *d_off = reinterpret_cast<int64_t *>(base + tok_bytes);
     int32_t *d_out = reinterpret_cast<int32_t *>(base + tok_bytes + ((off_bytes + 15) & ~size_t(15)));
     auto *d_ws = reinterpret_cast<unsigned long long *>(reinterpret_cast<unsigned char *>(d_out) +
@@ -1301,14 +1367,25 @@ int lookup_draft_host(const int32_t *h_tokens, const int64_t *h_offsets, int32_t
         reinterpret_cast<const int32_t *>(reinterpret_cast<uintptr_t>(d_tok) - uintptr_t(first) * 4u);
 
     cudaError_t e = cudaSuccess;
-    if (n_tok) e = cudaMemcpyAsync(d_tok, h_tokens + first, n_tok * 4, cudaMemcpyHostToDevice, stream);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(d_off, h_offsets, off_bytes, cudaMemcpyHostToDevice, stream);
+    if (kernel_copy) {
+        CopyParams cp;
+        cp.src = reinterpret_cast<const int4 *>(src_lo);
+        cp.dst = reinterpret_cast<int4 *>(base);
+        cp.n16 = int64_t(tok_bytes / 16);
+        cp.src_off = static_cast<const int64_t *>(m_off);
+        cp.dst_off = d_off;
+        cp.n_off = B + 1;
+        e = launch_host_copy(*st, cp, stream);
+    } else {
+        if (n_tok) e = cudaMemcpyAsync(d_tok, h_tokens + first, n_tok * 4, cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(d_off, h_offsets, off_bytes, cudaMemcpyHostToDevice, stream);
+    }
     if (e == cudaSuccess) {
         rc = launch_scan(*st, d_tok_base, d_off, B, min_m, max_m, d_ws, stream);
         if (rc == LOOKUP_DRAFT_OK)
             rc = launch_fill(*st, d_tok_base, d_off, B, K, d_ws, d_draft, d_len, d_pos, nullptr, stream);
     } else {
-        rc = cuda_fail(e, "cudaMemcpyAsync (host to device)");
+        rc = cuda_fail(e, kernel_copy ? "host_copy_kernel launch" : "cudaMemcpyAsync (host to device)");
     }
     if (rc == LOOKUP_DRAFT_OK && !direct && K > 0)
         e = cudaMemcpyAsync(h_out_draft, d_draft, size_t(B) * size_t(K) * 4, cudaMemcpyDeviceToHost, stream);

@@ -295,6 +295,49 @@ def test_host_entry_point_offset_base():
     np.testing.assert_array_equal(p, op)
 
 
+@pytest.mark.parametrize("first", [0, 5])
+@pytest.mark.parametrize("shift", [0, 1, 2, 3])
+def test_host_entry_point_pinned_inputs_any_phase(shift, first):
+    """Page-locked inputs are read by the device straight from host memory, in
+    whole 16-byte units of their address range: tokens starting at any 4-byte
+    phase, and offsets[0] > 0, give the oracle's results."""
+    w = gen.make_workload("periodic", 16 + shift)
+    n = w.tokens.shape[0]
+    big = torch.full((shift + first + n + 8,), 7, dtype=torch.int32).pin_memory()
+    tok = big[shift: shift + first + n]
+    tok[first:] = torch.from_numpy(w.tokens)
+    off = torch.from_numpy(w.offsets + first).pin_memory()
+    d, ln, p = pkg.lookup_draft_host(tok, off, w.min_m, w.max_m, w.K)
+    od, oln, op, _ = oracle.lookup_draft(tok.numpy(), off.numpy(), w.min_m, w.max_m, w.K, threads=8)
+    np.testing.assert_array_equal(d, od)
+    np.testing.assert_array_equal(ln, oln)
+    np.testing.assert_array_equal(p, op)
+
+
+@pytest.mark.parametrize("pin", ["tokens", "offsets"])
+def test_host_entry_point_mixed_inputs(pin):
+    """One input page-locked and the other pageable: both go through copies."""
+    w = gen.make_workload("ragged262k", 17)
+    tok = torch.from_numpy(w.tokens)
+    off = torch.from_numpy(w.offsets)
+    tok = tok.pin_memory() if pin == "tokens" else tok
+    off = off.pin_memory() if pin == "offsets" else off
+    d, ln, p = pkg.lookup_draft_host(tok, off, w.min_m, w.max_m, w.K)
+    od, oln, op, _ = oracle.lookup_draft(w.tokens, w.offsets, w.min_m, w.max_m, w.K, threads=8)
+    np.testing.assert_array_equal(d, od)
+    np.testing.assert_array_equal(ln, oln)
+    np.testing.assert_array_equal(p, op)
+
+
+def test_host_entry_point_pinned_empty_histories():
+    tok = torch.arange(5, dtype=torch.int32).pin_memory()
+    off = torch.tensor([3, 3, 3], dtype=torch.int64).pin_memory()
+    d, ln, p = pkg.lookup_draft_host(tok, off, 4, 12, 3)
+    np.testing.assert_array_equal(ln, [0, 0])
+    np.testing.assert_array_equal(p, [-1, -1])
+    np.testing.assert_array_equal(d, np.full((2, 3), -1, np.int32))
+
+
 def test_repeated_calls_and_streams():
     w = gen.make_workload("ragged262k", 14)
     t = torch.from_numpy(w.tokens).to(DEV)
