@@ -19,6 +19,8 @@ requests of 25,000 tokens, 6.4 MB of int32 history).  Prints one JSON line.
                 back-to-back scan launches (captured in a CUDA graph, inputs
                 rotating as above) on their stream, against the measured HBM copy
                 bandwidth.  scan_us_isolated: events around single launches.
+                read_floor: a launch that only streams the same bytes, timed the
+                same way: what one launch reading them once reaches here.
   e2e           lookup_draft_host: pinned host buffers in, the step, outputs back
                 to the host, every step.
   cpu_baseline  the CPU oracle (brute force, one thread per slice of requests) on
@@ -381,6 +383,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
 
     reps = max(10, min(200, args.steps // ncopy))
     scan_us = max_over_ranks(time_graph(graph_of(scan_call), reps), dist, dev)
+    floor = time_read_floor(lib, pkg, toks, w.history_bytes, dev, stream, reps)
+    floor_us = max_over_ranks(floor["us"], dist, dev)
     fill_us = max_over_ranks(time_graph(graph_of(fill_call), reps), dist, dev)
     clock_hz = float(getattr(props, "clock_rate", 2_000_000)) * 1000.0
     ea = [torch.cuda.Event(enable_timing=True) for _ in range(ncopy)]
@@ -491,6 +495,17 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
             "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
             "algorithmic_bytes_per_launch": hist_bytes,
             "traffic": traffic,
+            "read_floor": {
+                "kernel": "read_floor_kernel",
+                "us": round(floor_us, 3),
+                "achieved": round(hist_bytes / (floor_us * 1e-6) / 1e9, 1),
+                "frac": round(hist_bytes / (floor_us * 1e-6) / 1e9 / peak, 4),
+                "shape": floor["shape"],
+                "scan_vs_read_floor": round(floor_us / scan_us, 3),
+                "what": "one launch that only streams the same bytes (16-byte loads, best of "
+                        "CTAs-per-SM x threads in " + ", ".join(f"{a}x{b}" for a, b in FLOOR_SHAPES) +
+                        "), timed like the scan",
+            },
         },
         "e2e": {
             "value": round(e2e_us, 3),
@@ -870,6 +885,43 @@ def measure_ctx(lib, pkg, w, dev, stream) -> dict:
     return res
 
 
+# ----------------------------------------------------------- read floor ----
+FLOOR_SHAPES = ((2, 512), (4, 256), (8, 256))   # CTAs per SM x threads
+
+
+def time_read_floor(lib, pkg, toks, nbytes: int, dev, stream, reps: int) -> dict:
+    """The plain streaming read of the same bytes, timed the way the scan is
+    (ncopy launches over the rotating copies captured in one CUDA graph, replayed
+    back to back, CUDA events on the launching stream): the best over a few launch
+    shapes."""
+    import torch
+    out = torch.zeros(1, dtype=torch.int32, device=dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ncopy = len(toks)
+    best = None
+    for cps, thr in FLOOR_SHAPES:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            hc = int(torch.cuda.current_stream().cuda_stream)
+            for j in range(ncopy):
+                rc = lib.lookup_draft_read_floor(toks[j].data_ptr(), nbytes, cps, thr, out.data_ptr(), hc)
+                if rc != 0:
+                    raise pkg.LookupDraftError(rc, lib)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            ev0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = 1000.0 * ev0.elapsed_time(ev1) / (reps * ncopy)
+        if best is None or us < best[0]:
+            best = (us, f"{cps}x{thr}")
+        del g
+    return {"us": best[0], "shape": best[1]}
+
+
 # ------------------------------------------------------------ workloads ----
 def measure_workloads(lib, pkg, dev, stream, names, seed_offset: int, reps_cap: int) -> dict:
     """The draft step and the scan on each named workload, timed the way the main
@@ -934,12 +986,16 @@ def measure_workloads(lib, pkg, dev, stream, names, seed_offset: int, reps_cap: 
         step_us = timed(step)
         got = (draft.cpu().numpy(), length.cpu().numpy(), pos.cpu().numpy())
         scan_us = timed(scan)
+        floor = time_read_floor(lib, pkg, toks, w.history_bytes, dev, stream, max(10, min(reps_cap, 20000 // ncopy)))
         want = oracle.lookup_draft(w.tokens, w.offsets, w.min_m, w.max_m, K, threads=os.cpu_count() or 1)
         parity = all(np.array_equal(a, b) for a, b in zip(got, want[:3]))
         gbs = w.history_bytes / (scan_us * 1e-6) / 1e9
         out[name] = {"B": B, "history_bytes": int(w.history_bytes), "seed": int(w.seed),
                      "step_us": round(step_us, 3), "scan_us": round(scan_us, 3),
                      "scan_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                     "read_floor_us": round(floor["us"], 3),
+                     "read_floor_frac": round(w.history_bytes / (floor["us"] * 1e-6) / 1e9 / peak, 4),
+                     "scan_vs_read_floor": round(floor["us"] / scan_us, 3),
                      "copies": ncopy, "parity_with_oracle": bool(parity)}
         del toks, offs, ws
         torch.cuda.synchronize(dev)

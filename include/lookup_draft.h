@@ -199,6 +199,29 @@ const char *lookup_draft_last_cuda_error(void);
  */
 void lookup_draft_set_wait_limit_ns(uint64_t ns);
 
+/*
+ * Measurement aid (the source article has no counterpart; it is part of this
+ * library's measurement): one launch that streams `bytes` of device memory at
+ * `data` and does nothing else with them.  The bytes are read once, with 16-byte
+ * loads, each CTA a contiguous chunk, in a grid of ctas_per_sm CTAs per SM of
+ * `threads` threads, launched like the draft step's kernels (programmatic
+ * dependent launch).  Timed the way the scan is timed over the same bytes, it is
+ * the floor that any kernel reading them once reaches in a launch here, so the
+ * scan's time can be read against it as well as against the copy bandwidth.
+ *
+ * data         device, 16-byte aligned, `bytes` readable bytes (read only)
+ * bytes        a multiple of 16; 0 enqueues nothing and returns OK
+ * ctas_per_sm  1 .. 32;  threads: a multiple of 32 in 32 .. 1024
+ * out_word     device, 4-byte aligned: receives a fold of the data only in the
+ *              rare case that it equals a fixed pattern (so the loads cannot be
+ *              optimised away); otherwise untouched
+ * Errors: LOOKUP_DRAFT_EINVAL for a null or misaligned pointer, bytes not a
+ * multiple of 16, or a launch shape out of range; LOOKUP_DRAFT_ECUDA when the
+ * launch fails.
+ */
+int lookup_draft_read_floor(const void *data, size_t bytes, int32_t ctas_per_sm, int32_t threads,
+                            uint32_t *out_word, struct CUstream_st *stream);
+
 #ifdef __cplusplus
 }
 #endif

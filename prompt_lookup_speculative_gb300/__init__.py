@@ -95,6 +95,8 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.lookup_draft_last_cuda_error.restype = ctypes.c_char_p
     lib.lookup_draft_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.lookup_draft_set_wait_limit_ns.restype = None
+    lib.lookup_draft_read_floor.argtypes = [vp, sz, i32, i32, vp, vp]
+    lib.lookup_draft_read_floor.restype = ctypes.c_int
     lib.lookup_fuse.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp]
     lib.lookup_fuse.restype = ctypes.c_int
     lib.lookup_schedule.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp]
@@ -298,6 +300,22 @@ def _host_ptr(a) -> int:
     if a.dtype.name != "int32" or not a.flags["C_CONTIGUOUS"]:
         raise ValueError("host outputs must be contiguous int32 arrays")
     return a.ctypes.data
+
+
+def read_floor(data, ctas_per_sm: int = 4, threads: int = 256, out=None, stream=None) -> None:
+    """Measurement aid: one launch that only streams ``data`` (a CUDA tensor whose
+    byte size is a multiple of 16, 16-byte aligned) on the stream.  ``out`` is a
+    one-element int32 CUDA tensor the kernel may write (a fold of the data, in the
+    rare case it equals a fixed pattern)."""
+    import torch
+    lib = load_library()
+    if not (isinstance(data, torch.Tensor) and data.is_cuda and data.is_contiguous()):
+        raise ValueError("data must be a contiguous CUDA tensor")
+    if out is None:
+        out = torch.zeros(1, dtype=torch.int32, device=data.device)
+    nbytes = data.numel() * data.element_size()
+    _check(lib.lookup_draft_read_floor(data.data_ptr(), nbytes, ctas_per_sm, threads, out.data_ptr(),
+                                       _stream_handle(stream)), lib)
 
 
 def set_wait_limit_ns(ns: int) -> None:

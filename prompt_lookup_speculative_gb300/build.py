@@ -1,9 +1,10 @@
 """Compile the CUDA library in-tree for GB300 (sm_103a).
 
-The library is four translation units, ``csrc/lookup_draft.cu`` (the drafting
+The library is five translation units, ``csrc/lookup_draft.cu`` (the drafting
 step), ``csrc/lookup_loop.cu`` (the decode-loop steps around it),
-``csrc/lookup_index.cu`` (the incremental n-gram index) and
-``csrc/lookup_ctxcache.cu`` (context-cache drafting), built with nvcc into
+``csrc/lookup_index.cu`` (the incremental n-gram index),
+``csrc/lookup_ctxcache.cu`` (context-cache drafting) and ``csrc/read_floor.cu``
+(a measurement aid: a plain streaming read), built with nvcc into
 ``_build/liblookup_draft.so`` next to this file.  The CUDA runtime is linked
 statically, so the library loads on a machine without a GPU (its calls then
 fail with a CUDA error) and needs nothing from the Python environment.
@@ -18,7 +19,8 @@ PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 REPO_DIR = os.path.dirname(PKG_DIR)
 INCLUDE_DIR = os.path.join(REPO_DIR, "include")
 SOURCES = [os.path.join(PKG_DIR, "csrc", f)
-           for f in ("lookup_draft.cu", "lookup_loop.cu", "lookup_index.cu", "lookup_ctxcache.cu")]
+           for f in ("lookup_draft.cu", "lookup_loop.cu", "lookup_index.cu", "lookup_ctxcache.cu",
+                     "read_floor.cu")]
 HEADERS = [os.path.join(INCLUDE_DIR, f)
            for f in ("lookup_draft.h", "lookup_loop.h", "lookup_index.h", "lookup_ctxcache.h")] + \
           [os.path.join(PKG_DIR, "csrc", "common.cuh")]

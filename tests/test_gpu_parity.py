@@ -10,8 +10,10 @@ offsets the scan keeps in shared memory, all-equal and tiny-alphabet histories,
 long single requests spread over many CTAs, a match ending exactly at a tile or
 chunk boundary, clusters of dozens of requests starting inside one quad, batch
 sizes on both sides of the switch to the lane-per-request fill (with requests
-spanning hundreds of scan warps), the staged and host-buffer entry points,
-repeated calls and the failure path of the bounded waits.
+spanning hundreds of scan warps), the staged and host-buffer entry points
+(page-locked inputs at every 4-byte phase, mixed and pageable inputs), the
+read-floor measurement aid, repeated calls and the failure path of the bounded
+waits.
 """
 from __future__ import annotations
 
@@ -336,6 +338,18 @@ def test_host_entry_point_pinned_empty_histories():
     np.testing.assert_array_equal(ln, [0, 0])
     np.testing.assert_array_equal(p, [-1, -1])
     np.testing.assert_array_equal(d, np.full((2, 3), -1, np.int32))
+
+
+@pytest.mark.parametrize("shape", [(1, 32), (2, 512), (4, 256), (8, 256)])
+def test_read_floor_streams_without_writing(shape):
+    """The measurement aid reads its bytes and leaves the output word alone unless
+    their fold hits its fixed pattern (the XOR of 0 .. 2^20 - 1 is 0)."""
+    x = torch.arange(1 << 20, dtype=torch.int32, device=DEV)
+    out = torch.full((1,), 123, dtype=torch.int32, device=DEV)
+    pkg.read_floor(x, *shape, out=out)
+    pkg.read_floor(x[:4], *shape, out=out)                   # fewer 16-byte units than threads
+    torch.cuda.synchronize()
+    assert out.item() == 123
 
 
 def test_repeated_calls_and_streams():

@@ -44,7 +44,7 @@ def test_header_declares_the_entry_points():
                  "lookup_fuse", "lookup_schedule", "lookup_verify", "lookup_append", "lookup_index_slots_for",
                  "lookup_index_bytes", "lookup_index_build", "lookup_index_append", "lookup_index_draft",
                  "lookup_ctx_slots_for", "lookup_ctx_bytes", "lookup_ctx_build", "lookup_ctx_append",
-                 "lookup_ctx_draft"):
+                 "lookup_ctx_draft", "lookup_draft_read_floor"):
         assert must in names
 
 
@@ -100,6 +100,19 @@ def test_rejects_null_and_misaligned_pointers(lib):
     assert lib.lookup_draft_scan(FAKE, FAKE, 4, 4, 12, None, 1 << 20, None) == -1
     assert lib.lookup_draft_scan(FAKE, FAKE, 4, 4, 12, FAKE + 4, 1 << 20, None) == -1
     assert lib.lookup_draft_fill(FAKE, FAKE, 4, 4, 12, 15, None, 1 << 20, FAKE, FAKE, FAKE, None, None) == -1
+
+
+def test_read_floor_checks_its_arguments(lib):
+    assert lib.lookup_draft_read_floor(FAKE, 1 << 20, 4, 256, None, None) == -1
+    assert lib.lookup_draft_read_floor(FAKE, 1 << 20, 4, 256, FAKE + 2, None) == -1
+    assert lib.lookup_draft_read_floor(None, 1 << 20, 4, 256, FAKE, None) == -1
+    assert lib.lookup_draft_read_floor(FAKE + 4, 1 << 20, 4, 256, FAKE, None) == -1
+    assert lib.lookup_draft_read_floor(FAKE, (1 << 20) + 4, 4, 256, FAKE, None) == -1
+    assert lib.lookup_draft_read_floor(FAKE, 1 << 20, 0, 256, FAKE, None) == -1
+    assert lib.lookup_draft_read_floor(FAKE, 1 << 20, 33, 256, FAKE, None) == -1
+    assert lib.lookup_draft_read_floor(FAKE, 1 << 20, 4, 100, FAKE, None) == -1
+    assert lib.lookup_draft_read_floor(FAKE, 1 << 20, 4, 2048, FAKE, None) == -1
+    assert lib.lookup_draft_read_floor(None, 0, 4, 256, FAKE, None) == 0     # nothing to read
 
 
 def test_empty_batch_is_a_no_op(lib):
