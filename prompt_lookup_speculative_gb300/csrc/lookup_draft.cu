@@ -189,6 +189,20 @@ __device__ inline void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t byt
         : "memory");
 }
 
+// The same copy with an L2 evict-first policy: for history tiles, each read once.
+// Streaming them at normal priority pushed this kernel's code, the slots and the
+// offsets out of L2 between launches; the rare path then fetched its instructions
+// from DRAM.
+__device__ inline void bulk_copy_g2s_stream(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 __device__ inline void prefetch_l2(const void *p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
@@ -406,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
         unsigned char *buf = my_bufs + size_t(slot) * kBufBytes;
         const uint32_t bar = smem_addr(&my_bars[slot]);
         mbar_expect_tx(bar, bytes);
-        bulk_copy_g2s(smem_addr(buf + (kHaloQuads - (t0 - ls)) * 16), wsrc + ls * 4, bytes, bar);
+        bulk_copy_g2s_stream(smem_addr(buf + (kHaloQuads - (t0 - ls)) * 16), wsrc + ls * 4, bytes, bar);
     };
     if (wn > 0 && lane == 0) issue_tile(0, 0);
 

@@ -19,6 +19,16 @@ using lkd::wait_for_prerequisite_grid;
 constexpr int kUnroll = 4;                       // 16-byte loads in flight per thread
 constexpr uint32_t kNeverWritten = 0x5eed1e55u;  // the result is stored only if it equals this
 
+// A 16-byte read-only load with an L2 evict-first policy, the policy the scan's
+// history copies use.
+__device__ __forceinline__ int4 load_stream(const int4 *p, uint64_t policy) {
+    int4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.s32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
+}
+
 struct FloorParams {
     const int4 *p;
     int64_t n16;
@@ -26,7 +36,7 @@ struct FloorParams {
 };
 
 // Contiguous chunk per CTA, kUnroll independent 16-byte loads per thread per
-// iteration, all folded by XOR.  The fold is stored only when it equals a fixed
+// iteration (L2 evict-first, as the scan's copies), all folded by XOR.  The fold is stored only when it equals a fixed
 // pattern, so the loads cannot be dropped and almost no launch writes anything.
 __global__ void read_floor_kernel(FloorParams prm) {
     wait_for_prerequisite_grid();
@@ -37,17 +47,19 @@ __global__ void read_floor_kernel(FloorParams prm) {
     const int64_t b = int64_t(blockIdx.x) * per;
     const int64_t e = b + per < n16 ? b + per : n16;
     const int64_t step = blockDim.x;
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
     uint32_t acc = 0;
     int64_t i = b + threadIdx.x;
     for (; i + (kUnroll - 1) * step < e; i += kUnroll * step) {
         int4 v[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) v[u] = __ldg(p + i + u * step);
+        for (int u = 0; u < kUnroll; ++u) v[u] = load_stream(p + i + u * step, policy);
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) acc ^= uint32_t(v[u].x ^ v[u].y ^ v[u].z ^ v[u].w);
     }
     for (; i < e; i += step) {
-        const int4 v = __ldg(p + i);
+        const int4 v = load_stream(p + i, policy);
         acc ^= uint32_t(v.x ^ v.y ^ v.z ^ v.w);
     }
     acc = __reduce_xor_sync(0xffffffffu, acc);
