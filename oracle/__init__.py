@@ -36,6 +36,17 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "liblookup_oracle.so")
 
 _lib = None
 _lock = threading.Lock()
+_pools: dict[int, ThreadPoolExecutor] = {}
+
+
+def _pool(threads: int) -> ThreadPoolExecutor:
+    """A thread pool of `threads` workers kept for the life of the process (making
+    one per call cost milliseconds, more than a whole batch on many cores)."""
+    with _lock:
+        ex = _pools.get(threads)
+        if ex is None:
+            ex = _pools[threads] = ThreadPoolExecutor(max_workers=threads)
+        return ex
 
 
 def build(force: bool = False) -> str:
@@ -122,15 +133,16 @@ def lookup_draft(tokens, offsets, min_m: int, max_m: int, K: int,
         if rc != 0:
             raise ValueError(f"oracle rejected the arguments (rc={rc})")
         return draft, length, pos, mlen
-    # Balance by history length: cut the request range at equal token counts.
+    # Balance by history length: cut the request range at equal token counts, one
+    # piece per thread (each piece is one C call; many short calls queue on the
+    # interpreter lock as they return).
     work = (offsets[1:] - offsets[:-1]).astype(np.float64) + 64.0
     cum = np.concatenate([[0.0], np.cumsum(work)])
-    pieces = min(B, threads * 8)
+    pieces = min(B, threads)
     cuts = np.searchsorted(cum, np.linspace(0.0, cum[-1], pieces + 1), side="left")
     cuts[0], cuts[-1] = 0, B
     cuts = np.unique(np.clip(cuts, 0, B))
-    with ThreadPoolExecutor(max_workers=threads) as ex:
-        rcs = list(ex.map(lambda ab: run(int(ab[0]), int(ab[1])), zip(cuts[:-1], cuts[1:])))
+    rcs = list(_pool(threads).map(lambda ab: run(int(ab[0]), int(ab[1])), zip(cuts[:-1], cuts[1:])))
     if any(rc != 0 for rc in rcs):
         raise ValueError("oracle rejected the arguments")
     return draft, length, pos, mlen
@@ -266,9 +278,8 @@ def ctx_draft(tokens, offsets, K: int, n_min: int = 1, n_max: int = 4, min_count
     if threads <= 1 or B == 1:
         rcs = [run(0, B)]
     else:
-        cuts = np.linspace(0, B, min(B, threads * 4) + 1).astype(int)
-        with ThreadPoolExecutor(max_workers=threads) as ex:
-            rcs = list(ex.map(lambda ab: run(int(ab[0]), int(ab[1])), zip(cuts[:-1], cuts[1:])))
+        cuts = np.linspace(0, B, min(B, threads) + 1).astype(int)
+        rcs = list(_pool(threads).map(lambda ab: run(int(ab[0]), int(ab[1])), zip(cuts[:-1], cuts[1:])))
     if any(rcs):
         raise ValueError("oracle_ctx_draft rejected the arguments")
     return draft, length
