@@ -36,8 +36,9 @@ struct FloorParams {
 };
 
 // Contiguous chunk per CTA, kUnroll independent 16-byte loads per thread per
-// iteration (L2 evict-first, as the scan's copies), all folded by XOR.  The fold is stored only when it equals a fixed
-// pattern, so the loads cannot be dropped and almost no launch writes anything.
+// iteration (L2 evict-first, as the scan's copies), all folded by XOR.  The fold
+// is stored only when it equals a fixed pattern, so the loads cannot be dropped
+// and almost no launch writes anything.
 __global__ void read_floor_kernel(FloorParams prm) {
     wait_for_prerequisite_grid();
     allow_dependent_launch();
