@@ -24,7 +24,8 @@
 //    a request every lane takes 128-bit quads and runs the article's cheap
 //    rejection test (section "第1步") branch-free: a token and the D - 1 tokens
 //    before it against the last D suffix tokens, D = min(min_m, 4).  The rare
-//    survivors are extended backwards.  A match of length k ending at local
+//    survivors are extended backwards, eight positions compared per round with
+//    their shared-memory loads issued together.  A match of length k ending at local
 //    position q gives the key (k << 32) | (q - k + 1): its maximum is the longest
 //    match, then the most recent.  A warp keeps its current request and its
 //    lanes' best keys across tiles and writes the warp's maximum into the
@@ -301,6 +302,28 @@ __device__ __forceinline__ bool quad_any(const int4 &prv, const int4 &cur, int32
     return (h0 | h1) | (h2 | h3);
 }
 
+// Length of the match ending at tile element e whose last k0 tokens already
+// match: the largest k <= kmax with st[e - i] == suf[i] for every i < k.  Eight
+// positions are compared per round, their loads issued together, so a full
+// match of max_m = 12 costs one round of shared-memory latency instead of eight.
+// st[e - k] stays inside the buffer (the halo holds 32 tokens and k < 32).
+__device__ __forceinline__ int match_len(const int32_t *st, int e, const int32_t *suf, int k0, int kmax) {
+    int kk = k0;
+    while (kk < kmax) {
+        unsigned ne = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int k = kk + i;
+            if (k < kmax && st[e - k] != suf[k]) ne |= 1u << i;
+        }
+        const int left = kmax - kk;
+        const unsigned stop = ne | (left < 8 ? (~0u << left) : 0u);
+        if (stop) return kk + __ffs(int(stop)) - 1;
+        kk += 8;
+    }
+    return kmax;
+}
+
 // Bit e set when element x4 + e lies in [lo, hi] (e = 0..3).
 __device__ __forceinline__ unsigned range_mask(int x4, int lo, int hi) {
     const int a = lo - x4, b = hi - x4;
@@ -311,7 +334,7 @@ __device__ __forceinline__ unsigned range_mask(int x4, int lo, int hi) {
 }
 
 // D = min(min_m, 4): how many suffix tokens the branch-free rejection test checks
-// before a candidate is extended one token at a time.  OFFS_SMEM: B + 1 <= kOffCap,
+// before a candidate is extended, eight positions per round.  OFFS_SMEM: B + 1 <= kOffCap,
 // the offsets are copied into shared memory (otherwise read from global memory).
 template <int D, bool OFFS_SMEM>
 __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
@@ -546,8 +569,12 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                 auto extend = [&](int e, int k0) {
                     const int q = qoff + e;              // local end position in the request
                     const int kmax = max_m < q + 1 ? max_m : q + 1;
+                    const int row = cur_r - rw_lo;
                     int kk = k0;
-                    while (kk < kmax && st[e - kk] == suffix(cur_r, WA + cur_o, WA + cur_nxt, kk)) ++kk;
+                    if (row < kSufRows)
+                        kk = match_len(st, e, suf_w + row * max_m, k0, kmax);
+                    else
+                        while (kk < kmax && st[e - kk] == suffix(cur_r, WA + cur_o, WA + cur_nxt, kk)) ++kk;
                     if (kk >= min_m) {
                         const unsigned long long key =
                             (static_cast<unsigned long long>(kk) << 32) | static_cast<uint32_t>(q - kk + 1);
@@ -599,7 +626,10 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                     const int q = qoff + e;
                     const int kmax = max_m < q + 1 ? max_m : q + 1;
                     int kk = D;
-                    while (kk < kmax && st[e - kk] == (suf ? suf[kk] : __ldg(hist_last - kk))) ++kk;
+                    if (suf)
+                        kk = match_len(st, e, suf, D, kmax);
+                    else
+                        while (kk < kmax && st[e - kk] == __ldg(hist_last - kk)) ++kk;
                     if (kk >= min_m) {
                         const unsigned long long key =
                             (static_cast<unsigned long long>(kk) << 32) | static_cast<uint32_t>(q - kk + 1);
@@ -671,7 +701,10 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                         const int kmax = max_m < q + 1 ? max_m : q + 1;
                         const int64_t o_abs = WA + (inB ? oB : oA), n_abs = WA + (inB ? nB : nA);
                         int kk = D;
-                        while (kk < kmax && st[e - kk] == suffix(r, o_abs, n_abs, kk)) ++kk;
+                        if (r - rw_lo < kSufRows)
+                            kk = match_len(st, e, suf_w + (r - rw_lo) * max_m, D, kmax);
+                        else
+                            while (kk < kmax && st[e - kk] == suffix(r, o_abs, n_abs, kk)) ++kk;
                         if (kk >= min_m) {
                             const unsigned long long key =
                                 (static_cast<unsigned long long>(kk) << 32) | static_cast<uint32_t>(q - kk + 1);
