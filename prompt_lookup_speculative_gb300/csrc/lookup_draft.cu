@@ -1033,6 +1033,21 @@ const void *mapped_host_const(const void *p) {
 
 int32_t *mapped_host(int32_t *p) { return static_cast<int32_t *>(const_cast<void *>(mapped_host_const(p))); }
 
+// Every scan instantiation may use the shared memory of the largest batch the
+// offsets copy serves and the largest max_m (more than the 48 KB default).
+int scan_attributes() {
+    const int smem_max = int(scan_smem_layout(kOffCap - 1, LOOKUP_DRAFT_MAX_M).total);
+    LD_CUDA(cudaFuncSetAttribute(scan_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+    LD_CUDA(cudaFuncSetAttribute(scan_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+    LD_CUDA(cudaFuncSetAttribute(scan_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+    LD_CUDA(cudaFuncSetAttribute(scan_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+    LD_CUDA(cudaFuncSetAttribute(scan_kernel<3, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+    LD_CUDA(cudaFuncSetAttribute(scan_kernel<3, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+    LD_CUDA(cudaFuncSetAttribute(scan_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+    LD_CUDA(cudaFuncSetAttribute(scan_kernel<4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+    return LOOKUP_DRAFT_OK;
+}
+
 struct DeviceState {
     bool ready = false;
     int sms = 0;
@@ -1052,16 +1067,8 @@ int device_state(DeviceState **out) {
     if (!st.ready) {
         int sms = 0;
         LD_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-        const ScanSmemLayout worst = scan_smem_layout(kOffCap - 1, LOOKUP_DRAFT_MAX_M);
-        const int smem_max = int(worst.total);
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<3, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<3, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+        const int rc_attr = scan_attributes();
+        if (rc_attr != LOOKUP_DRAFT_OK) return rc_attr;
         cudaMemPoolProps props;
         std::memset(&props, 0, sizeof props);
         props.allocType = cudaMemAllocationTypePinned;
@@ -1273,15 +1280,8 @@ int static_state(StaticState **out) {
     if (!st.ready) {
         int sms = 0;
         LD_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-        const int smem_max = int(scan_smem_layout(kOffCap - 1, LOOKUP_DRAFT_MAX_M).total);
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<3, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<3, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
-        LD_CUDA(cudaFuncSetAttribute(scan_kernel<4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max));
+        const int rc_attr = scan_attributes();
+        if (rc_attr != LOOKUP_DRAFT_OK) return rc_attr;
         void *ptr = nullptr;
         LD_CUDA(cudaGetSymbolAddress(&ptr, g_static_slots));
         st.sms = sms;
