@@ -347,12 +347,62 @@ __device__ inline int append_status(const AppendParams &p, bool ok, int r, int &
     return !ok ? 2 : (int64_t(L) + n > int64_t(p.cap[r]) ? 1 : 0);
 }
 
-// The writes and insertions: one thread per (request, new position, length)
-// task, grid-stride over B * W * (max_m - min_m + 1) tasks.  The tokens that
+// Batches that fit in one wave: one CTA per request at a time (grid-stride over
+// requests), the CTA's threads
+// take the request's (new position, length) tasks, writing the new tokens and
+// inserting the n-grams that end at them.  The tokens that end at a new position
+// come from the old history or straight from `commit`, so no insertion waits for
+// a write.  Every thread reads the request's old length first; after a barrier
+// (no thread reads it any more) one thread writes the new length and the status,
+// so the append is one launch.
+template <int kMaxLen>
+__global__ void __launch_bounds__(kAppendThreads) index_append_request_kernel(AppendParams p) {
+    wait_for_prerequisite_grid();
+    allow_dependent_launch();
+    const bool ok = header_ok(p.hd, p.min_m, p.max_m, p.hash_bits, p.slots);
+    const int64_t mask = (p.slots / kBucket) - 1;       // bucket mask
+    const int nl = p.max_m - p.min_m + 1;
+    const int64_t per_r = int64_t(p.W) * nl;
+    for (int r = blockIdx.x; r < p.B; r += gridDim.x) {
+        int L, n;
+        int64_t base;
+        const int st = append_status(p, ok, r, L, n, base);
+        const int32_t *crow = p.commit + int64_t(r) * p.W;
+        for (int64_t t = threadIdx.x; st == 0 && t < per_r; t += blockDim.x) {
+            const int j = int(t / nl), len_n = p.min_m + int(t % nl);   // new position L + j, length len_n
+            if (j >= n) break;                                   // tasks are ordered by j
+            if (len_n == p.min_m) p.tokens[base + L + j] = crow[j];  // one writer per new token
+            const int i = L + j;
+            if (i + 1 < len_n) continue;                         // no n-gram of that length ends here
+            // the len_n tokens ending at i, from the old history or from commit, loaded at once
+            int32_t v[kMaxLen];
+#pragma unroll
+            for (int k = 0; k < kMaxLen; ++k) {
+                const int src = i - k;
+                v[k] = k >= len_n ? 0 : (src >= L ? crow[src - L] : p.tokens[base + src]);
+            }
+            uint64_t h = seed_of(r);
+#pragma unroll
+            for (int k = 0; k < kMaxLen; ++k)
+                if (k < len_n) h = step_hash(h, v[k]);
+            insert_cas(p.tab, mask, key_of(h, len_n, p.hash_bits), int(base + i), p.hd);
+        }
+        __syncthreads();                                     // every reader of len[r] is done
+        if (threadIdx.x == 0) {
+            if (st == 0) p.len[r] = L + n;
+            if (p.status) p.status[r] = st;
+        }
+    }
+}
+
+// Large batches (more requests than one wave of per-request CTAs): the writes
+// and insertions with one thread per (request, new position, length) task,
+// grid-stride over B * W * (max_m - min_m + 1) tasks, then the lengths in a
+// second kernel.  The tokens that
 // end at a new position come from the old history or straight from `commit`,
 // so no insertion waits for a write.  len is only read here.
 template <int kMaxLen>
-__global__ void __launch_bounds__(kAppendThreads) index_append_kernel(AppendParams p) {
+__global__ void __launch_bounds__(kAppendThreads) index_append_dense_kernel(AppendParams p) {
     wait_for_prerequisite_grid();
     allow_dependent_launch();
     const bool ok = header_ok(p.hd, p.min_m, p.max_m, p.hash_bits, p.slots);
@@ -626,11 +676,22 @@ int lookup_index_append(int32_t *tokens, const int64_t *base, int32_t *len, cons
     p.min_m = min_m;
     p.max_m = max_m;
     p.hash_bits = hash_bits;
-    const int64_t tasks = int64_t(B) * W * (max_m - min_m + 1);
+    // A CTA per request, sized to its tasks (a warp at least, kAppendThreads at
+    // most), when every request gets one in a single wave: one launch.  Larger
+    // batches spread the tasks densely over the threads and set the lengths in a
+    // second launch (one CTA per request would take several waves).
+    const int64_t per_r = int64_t(W) * (max_m - min_m + 1);
+    const int64_t block = per_r < 32 ? 32 : (per_r >= kAppendThreads ? kAppendThreads : (per_r + 31) / 32 * 32);
+    const int64_t wave = int64_t(sms) * (2048 / block);
+    // the token window in registers: 16 entries when max_m allows, else 32
+    if (B <= wave)
+        return launch_pdl(max_m <= 16 ? index_append_request_kernel<16>
+                                      : index_append_request_kernel<LOOKUP_DRAFT_MAX_M>,
+                          unsigned(B), unsigned(block), stream, p);
+    const int64_t tasks = int64_t(B) * per_r;
     const int64_t want = (tasks + kAppendThreads - 1) / kAppendThreads;
     const unsigned grid = unsigned(want < int64_t(sms) * 8 ? (want > 0 ? want : 1) : int64_t(sms) * 8);
-    // the token window in registers: 16 entries when max_m allows, else 32
-    rc = launch_pdl(max_m <= 16 ? index_append_kernel<16> : index_append_kernel<LOOKUP_DRAFT_MAX_M>, grid,
+    rc = launch_pdl(max_m <= 16 ? index_append_dense_kernel<16> : index_append_dense_kernel<LOOKUP_DRAFT_MAX_M>, grid,
                     unsigned(kAppendThreads), stream, p);
     if (rc != LOOKUP_DRAFT_OK) return rc;
     const unsigned grid2 = unsigned((int64_t(B) + kAppendThreads - 1) / kAppendThreads);

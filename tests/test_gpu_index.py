@@ -149,6 +149,31 @@ def test_append_status_full_slab_and_mismatch():
     check_draft(idx.draft(t, b, n, 15), oracle.lookup_draft(t2, o2, 4, 12, 15))
 
 
+@pytest.mark.parametrize("B", [300, 12000])
+def test_append_both_launch_shapes(B):
+    """The append runs one CTA per request when the batch fits in one wave of
+    them, else dense tasks then a length pass.  Both must write the same tokens,
+    lengths and statuses, and leave an index that drafts exactly."""
+    rng = np.random.default_rng(B)
+    lengths = rng.integers(0, 60, size=B)
+    tokens = rng.integers(0, 6, size=int(lengths.sum())).astype(np.int32)
+    offsets = gen.offsets_from_lengths(lengths)
+    st, base, length, cap = gen.slabs_from_batch(tokens, offsets, 4, seed=B)
+    idx, t, b, n = built(st, base, length, 4, 12)
+    W = 6
+    commit = rng.integers(0, 6, size=(B, W)).astype(np.int32)
+    ncommit = rng.integers(0, W + 1, size=B).astype(np.int32)       # 5 and 6 do not fit in 4 spare slots
+    status = host(idx.append(t, b, n, dev(cap), dev(commit), dev(ncommit)))
+    fits = ncommit <= 4
+    np.testing.assert_array_equal(status, np.where(fits, 0, 1))
+    np.testing.assert_array_equal(host(n), length + np.where(fits, ncommit, 0))
+    want_t, want_o = oracle.append(tokens, offsets, commit, np.where(fits, ncommit, 0).astype(np.int32))
+    got_t, got_o = gen.csr_of_slabs(host(t), base, host(n))
+    np.testing.assert_array_equal(got_o, want_o)
+    np.testing.assert_array_equal(got_t, want_t)
+    check_draft(idx.draft(t, b, n, 7), oracle.lookup_draft(want_t, want_o, 4, 12, 7, threads=16))
+
+
 def test_index_agrees_with_the_scan():
     """The index and the scan kernel give the same drafts on the same histories."""
     w = gen.make_workload("ragged262k")
