@@ -324,6 +324,49 @@ __global__ void __launch_bounds__(kThreads) ctx_append_kernel(AppendParams p) {
     }
 }
 
+// Batches that fit in one wave: one CTA per request at a time (grid-stride over
+// requests) takes that request's tasks as above; every thread reads the old
+// length first, and after a barrier one thread writes the new length and the
+// status, so the append is one launch.  (Larger batches use the kernel above and
+// then the length pass below.)
+__global__ void __launch_bounds__(kThreads) ctx_append_request_kernel(AppendParams p) {
+    wait_for_prerequisite_grid();
+    allow_dependent_launch();
+    const bool ok = header_ok(p.hd, p.n_min, p.n_max, p.slots);
+    const int64_t bmask = p.slots / kBucket - 1;
+    const int nl = p.n_max - p.n_min + 1;
+    const int64_t per_r = int64_t(p.W) * nl;
+    for (int r = blockIdx.x; r < p.B; r += gridDim.x) {
+        int L, cnt;
+        int64_t base;
+        const int st = append_status(p, ok, r, L, cnt, base);
+        const int32_t *crow = p.commit + int64_t(r) * p.W;
+        for (int64_t t = threadIdx.x; st == 0 && t < per_r; t += blockDim.x) {
+            const int j = int(t / nl), n = p.n_min + int(t % nl);
+            if (j >= cnt) break;                                 // tasks are ordered by j
+            const int32_t x = crow[j];
+            if (n == p.n_min) p.tokens[base + L + j] = x;      // one writer per new token
+            const int i = L + j;                                 // x's position
+            if (i < n || !in_range(x)) continue;
+            int32_t g[kMaxN] = {0, 0, 0, 0};
+            bool okg = true;
+#pragma unroll
+            for (int k = 0; k < kMaxN; ++k)
+                if (k < n) {
+                    const int src = i - n + k;
+                    g[k] = src >= L ? crow[src - L] : p.tokens[base + src];
+                    okg = okg && in_range(g[k]);
+                }
+            if (okg) count_pair(p.tab, bmask, p.hd, r, n, g, x);
+        }
+        __syncthreads();                                     // every reader of len[r] is done
+        if (threadIdx.x == 0) {
+            if (st == 0) p.len[r] = L + cnt;
+            if (p.status) p.status[r] = st;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads) append_len_kernel(AppendParams p) {
     wait_for_prerequisite_grid();
     allow_dependent_launch();
@@ -492,7 +535,13 @@ int lookup_ctx_append(int32_t *tokens, const int64_t *base, int32_t *len, const 
     p.W = W;
     p.n_min = n_min;
     p.n_max = n_max;
-    const int64_t tasks = int64_t(B) * W * (n_max - n_min + 1);
+    // a CTA per request (sized to its tasks) when the batch fits in one wave of
+    // them: one launch; else dense tasks, then the lengths
+    const int64_t per_r = int64_t(W) * (n_max - n_min + 1);
+    const int64_t block = per_r < 32 ? 32 : (per_r >= kThreads ? kThreads : (per_r + 31) / 32 * 32);
+    const int64_t wave = int64_t(sms) * (2048 / block < 32 ? 2048 / block : 32);   // resident CTAs
+    if (B <= wave) return launch_pdl(ctx_append_request_kernel, unsigned(B), unsigned(block), stream, p);
+    const int64_t tasks = int64_t(B) * per_r;
     rc = launch_pdl(ctx_append_kernel, lkd::capped_grid((tasks + kThreads - 1) / kThreads, int64_t(sms) * 8),
                     unsigned(kThreads), stream, p);
     if (rc != LOOKUP_DRAFT_OK) return rc;

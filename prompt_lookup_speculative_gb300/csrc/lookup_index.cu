@@ -682,7 +682,7 @@ int lookup_index_append(int32_t *tokens, const int64_t *base, int32_t *len, cons
     // second launch (one CTA per request would take several waves).
     const int64_t per_r = int64_t(W) * (max_m - min_m + 1);
     const int64_t block = per_r < 32 ? 32 : (per_r >= kAppendThreads ? kAppendThreads : (per_r + 31) / 32 * 32);
-    const int64_t wave = int64_t(sms) * (2048 / block);
+    const int64_t wave = int64_t(sms) * (2048 / block < 32 ? 2048 / block : 32);   // resident CTAs
     // the token window in registers: 16 entries when max_m allows, else 32
     if (B <= wave)
         return launch_pdl(max_m <= 16 ? index_append_request_kernel<16>

@@ -137,3 +137,33 @@ def test_ctx_status_mismatch_and_overflow():
     small.build(t, b, n)
     d, ln = small.draft(t, b, n, 4)
     assert (host(ln) == pkg.LEN_FAILED).all()
+
+
+@pytest.mark.parametrize("B", [300, 12000])
+def test_ctx_append_both_launch_shapes(B):
+    """The append runs one CTA per request when the batch fits in one wave of
+    them, else dense tasks then a length pass: same tokens, lengths, statuses and
+    next drafts either way."""
+    rng = np.random.default_rng(B + 7)
+    lengths = rng.integers(0, 60, size=B)
+    tokens = rng.integers(0, 6, size=int(lengths.sum())).astype(np.int32)
+    offsets = gen.offsets_from_lengths(lengths)
+    st, base, length, cap = gen.slabs_from_batch(tokens, offsets, 4, seed=B)
+    t, b, n = dev(st), dev(base), dev(length)
+    cc = pkg.ContextCache(st.shape[0], 1, 4)
+    cc.build(t, b, n)
+    W = 6
+    commit = rng.integers(0, 6, size=(B, W)).astype(np.int32)
+    ncommit = rng.integers(0, W + 1, size=B).astype(np.int32)      # 5 and 6 do not fit in 4 spare slots
+    status = host(cc.append(t, b, n, dev(cap), dev(commit), dev(ncommit)))
+    fits = ncommit <= 4
+    np.testing.assert_array_equal(status, np.where(fits, 0, 1))
+    np.testing.assert_array_equal(host(n), length + np.where(fits, ncommit, 0))
+    want_t, want_o = oracle.append(tokens, offsets, commit, np.where(fits, ncommit, 0).astype(np.int32))
+    got_t, got_o = gen.csr_of_slabs(host(t), base, host(n))
+    np.testing.assert_array_equal(got_o, want_o)
+    np.testing.assert_array_equal(got_t, want_t)
+    d, ln = cc.draft(t, b, n, 5)
+    wd, wl = oracle.ctx_draft(want_t, want_o, 5, threads=16)
+    np.testing.assert_array_equal(host(ln), wl)
+    np.testing.assert_array_equal(host(d), wd)
