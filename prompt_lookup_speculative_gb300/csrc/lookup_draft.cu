@@ -25,8 +25,8 @@
 //    rejection test (section "第1步") branch-free: a token and the D - 1 tokens
 //    before it against the last D suffix tokens, D = min(min_m, 4).  The rare
 //    survivors are extended backwards, eight positions compared per round with
-//    their shared-memory loads issued together.  A match of length k ending at local
-//    position q gives the key (k << 32) | (q - k + 1): its maximum is the longest
+//    their shared-memory loads issued together.  A match of length k ending at
+//    local position q gives the key (k << 32) | (q - k + 1): its maximum is the longest
 //    match, then the most recent.  A warp keeps its current request and its
 //    lanes' best keys across tiles and writes the warp's maximum into the
 //    (request, virtual chunk) slot when it moves on.
@@ -190,10 +190,9 @@ __device__ inline void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t byt
         : "memory");
 }
 
-// The same copy with an L2 evict-first policy: for history tiles, each read once.
-// Streaming them at normal priority pushed this kernel's code, the slots and the
-// offsets out of L2 between launches; the rare path then fetched its instructions
-// from DRAM.
+// The same copy with an L2 evict-first policy, for history tiles: each is read
+// once, so the lines that are used again across launches (the kernels' code, the
+// slots, the offsets) are the ones kept in L2.
 __device__ inline void bulk_copy_g2s_stream(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
     uint64_t policy;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
