@@ -65,6 +65,8 @@ namespace {
 
 // ---------------------------------------------------------------- tuning ----
 constexpr int kWarps = 16;             // scan warps per CTA; each owns a contiguous range
+constexpr int kChunkSmall = 512;       // quads per CTA chunk below which it has 8 warp ranges
+constexpr int kChunkMid = 2048;        // ... and below which 12 (else kWarps)
 constexpr int kThreads = kWarps * 32;
 constexpr int kBufs = 3;               // tiles in flight per warp
 constexpr int kTileQuadsMax = 192;     // 3 KB of history per tile at most
@@ -116,8 +118,19 @@ struct FillParams {
 // The batch occupies aligned quads [q_lo, q_lo + nq) of the 16-byte-aligned view
 // of `tokens`.  Chunk c (CTA c) is quads [c*S, (c+1)*S) of that range, clipped,
 // with S = ceil(nq / G); warp w of chunk c takes quads [c*S + w*Sw, c*S + (w+1)*Sw)
-// of it, clipped to the chunk, with Sw = ceil(S / kWarps).  Virtual chunk
+// of it, clipped to the chunk, with Sw = warp_span32(S) (ceil(S / kWarps) unless
+// the chunk is small).  Virtual chunk
 // v = c*kWarps + w.  Empty chunks and empty warp ranges come last in their order.
+// Quads per warp range for a CTA chunk of S quads.  Small chunks get fewer and
+// longer ranges (8, or 12, of the kWarps; the other warps' ranges are empty), so
+// a small batch starts fewer warps' request searches and suffix loads and leaves
+// fewer slots to the fill.
+__host__ __device__ __forceinline__ uint32_t warp_span32(uint32_t S) {
+    if (S < uint32_t(kChunkSmall)) return (S + 7u) >> 3;
+    if (S < uint32_t(kChunkMid)) return (S + 11u) / 12u;
+    return (S + uint32_t(kWarps) - 1u) / uint32_t(kWarps);
+}
+
 struct Partition {
     int64_t q_lo;
     int64_t nq;
@@ -140,7 +153,7 @@ __device__ inline Partition make_partition(int64_t a_begin, int64_t a_end, int G
     P.q_lo = a_begin >> 2;
     P.nq = ((a_end + 3) >> 2) - P.q_lo;
     P.S = div_u(P.nq + G - 1, G);
-    P.Sw = div_u(P.S + kWarps - 1, kWarps);
+    P.Sw = P.S < kChunkMid ? int64_t(warp_span32(uint32_t(P.S))) : div_u(P.S + kWarps - 1, kWarps);
     return P;
 }
 
@@ -404,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
     if (P.nq < (int64_t(1) << 31) - G) {
         const uint32_t nq = uint32_t(P.nq), n = nq + uint32_t(G - 1);
         const uint32_t S = prm.grid_shift < 0 ? n : __umulhi(n, prm.grid_magic) >> prm.grid_shift;
-        const uint32_t Sw = (S + kWarps - 1) / kWarps;
+        const uint32_t Sw = warp_span32(S);
         P.S = S;
         P.Sw = Sw;
         const uint32_t c0 = uint32_t(c) * S;

@@ -37,6 +37,8 @@ def _const(name, text=SRC):
 
 
 K_WARPS = _const("kWarps")
+CHUNK_SMALL = _const("kChunkSmall")
+CHUNK_MID = _const("kChunkMid")
 K_BUFS = _const("kBufs")
 TQ_MAX = _const("kTileQuadsMax")
 TQ_MIN = _const("kTileQuadsMin")
@@ -72,11 +74,18 @@ def test_grid_division_is_exact(G):
         assert div_grid(n, magic, shift) == n // G, (G, n)
 
 
+def warp_span(S):
+    """Quads per warp range of a chunk of S quads: 8 ranges below CHUNK_SMALL,
+    12 below CHUNK_MID, else K_WARPS (the kernel's warp_span32)."""
+    w = 8 if S < CHUNK_SMALL else (12 if S < CHUNK_MID else K_WARPS)
+    return (S + w - 1) // w
+
+
 def warp_ranges(nq, G):
     """[lo, hi) per virtual chunk v = c * K_WARPS + w, quads relative to q_lo."""
     magic, shift = grid_divider(G)
     S = div_grid(nq + G - 1, magic, shift)
-    Sw = (S + K_WARPS - 1) // K_WARPS
+    Sw = warp_span(S)
     out = []
     for c in range(G):
         c0 = c * S
