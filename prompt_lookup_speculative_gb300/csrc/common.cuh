@@ -47,13 +47,16 @@ __device__ inline void cas128(void *addr, uint64_t cmp_lo, uint64_t cmp_hi, uint
         : "memory");
 }
 
-// Host: launch with programmatic stream serialization allowed.
+// Host: launch with programmatic stream serialization allowed (and `smem` bytes
+// of dynamic shared memory).
 template <typename Params>
-inline int launch_pdl(void (*kernel)(Params), unsigned grid, unsigned block, cudaStream_t stream, const Params &prm) {
+inline int launch_pdl(void (*kernel)(Params), unsigned grid, unsigned block, cudaStream_t stream, const Params &prm,
+                      size_t smem = 0) {
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -51,7 +51,7 @@
 
 #include "lookup_draft.h"
 
-#include <cuda_runtime.h>
+#include "common.cuh"
 
 #include <atomic>
 #include <cstdint>
@@ -59,9 +59,12 @@
 #include <cstring>
 #include <mutex>
 
-#include <nvtx3/nvToolsExt.h>
-
 namespace {
+
+using lkd::allow_dependent_launch;
+using lkd::launch_pdl;
+using lkd::TraceRange;
+using lkd::wait_for_prerequisite_grid;
 
 // ---------------------------------------------------------------- tuning ----
 constexpr int kWarps = 16;             // scan warps per CTA; each owns a contiguous range
@@ -245,16 +248,6 @@ __device__ inline bool mbar_wait_until(uint32_t bar, uint32_t parity, uint64_t d
         if (global_ns() > deadline_ns) return false;
         if (mbar_try_wait(bar, parity)) return true;
     }
-}
-
-// Programmatic dependent launch: let the next kernel on the stream start its
-// prologue now / wait until the previous kernel's results are visible.
-__device__ inline void allow_dependent_launch() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-__device__ inline void wait_for_prerequisite_grid() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------------------------------------ scan kernel ----
@@ -1006,15 +999,6 @@ __global__ void __launch_bounds__(kCopyThreads) host_copy_kernel(CopyParams prm)
 }
 
 // ------------------------------------------------------------- host side ----
-// An NVTX range over one library call: a span per call in a timeline tool,
-// nearly free when no tool is attached (header-only NVTX).
-struct TraceRange {
-    explicit TraceRange(const char *name) { nvtxRangePushA(name); }
-    ~TraceRange() { nvtxRangePop(); }
-    TraceRange(const TraceRange &) = delete;
-    TraceRange &operator=(const TraceRange &) = delete;
-};
-
 thread_local char g_cuda_msg[256] = "";
 
 int cuda_fail(cudaError_t e, const char *what) {
@@ -1061,7 +1045,7 @@ int scan_attributes() {
 }
 
 struct DeviceState {
-    bool ready = false;
+    std::atomic<bool> ready{false};     // set (release) once the fields below are final
     int sms = 0;
     cudaMemPool_t pool = nullptr;
 };
@@ -1069,14 +1053,19 @@ constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
-// Per-device set-up, once: SM count, shared-memory opt-in, scratch pool.
+// Per-device set-up, once: SM count, shared-memory opt-in, scratch pool.  After
+// it, a call only reads the ready flag; the lock is taken for the set-up alone.
 int device_state(DeviceState **out) {
     int dev = 0;
     LD_CUDA(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice, "device index");
-    std::lock_guard<std::mutex> lock(g_dev_mu);
     DeviceState &st = g_dev[dev];
-    if (!st.ready) {
+    if (st.ready.load(std::memory_order_acquire)) {
+        *out = &st;
+        return LOOKUP_DRAFT_OK;
+    }
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (!st.ready.load(std::memory_order_relaxed)) {
         int sms = 0;
         LD_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
         const int rc_attr = scan_attributes();
@@ -1093,7 +1082,7 @@ int device_state(DeviceState **out) {
         LD_CUDA(cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep));
         st.sms = sms;
         st.pool = pool;
-        st.ready = true;
+        st.ready.store(true, std::memory_order_release);
     }
     *out = &st;
     return LOOKUP_DRAFT_OK;
@@ -1159,29 +1148,19 @@ int launch_scan(const DeviceState &st, const int32_t *tokens, const int64_t *off
     grid_divider(prm.grid, prm.grid_magic, prm.grid_shift);
     prm.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     const ScanSmemLayout lay = scan_smem_layout(B, max_m);
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(unsigned(prm.grid));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = lay.total;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     const bool offs_smem = int64_t(B) + 1 <= kOffCap;
+    void (*kernel)(ScanParams) = nullptr;
     switch ((min_m < 4 ? min_m : 4) * 2 + (offs_smem ? 1 : 0)) {
-    case 2: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<1, false>, prm)); break;
-    case 3: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<1, true>, prm)); break;
-    case 4: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<2, false>, prm)); break;
-    case 5: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<2, true>, prm)); break;
-    case 6: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<3, false>, prm)); break;
-    case 7: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<3, true>, prm)); break;
-    case 8: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<4, false>, prm)); break;
-    default: LD_CUDA(cudaLaunchKernelEx(&cfg, scan_kernel<4, true>, prm)); break;
+    case 2: kernel = scan_kernel<1, false>; break;
+    case 3: kernel = scan_kernel<1, true>; break;
+    case 4: kernel = scan_kernel<2, false>; break;
+    case 5: kernel = scan_kernel<2, true>; break;
+    case 6: kernel = scan_kernel<3, false>; break;
+    case 7: kernel = scan_kernel<3, true>; break;
+    case 8: kernel = scan_kernel<4, false>; break;
+    default: kernel = scan_kernel<4, true>; break;
     }
-    return LOOKUP_DRAFT_OK;
+    return launch_pdl(kernel, unsigned(prm.grid), unsigned(kThreads), stream, prm, lay.total);
 }
 
 int launch_fill(const DeviceState &st, const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t K,
@@ -1198,41 +1177,18 @@ int launch_fill(const DeviceState &st, const int32_t *tokens, const int64_t *off
     prm.B = B;
     prm.K = K;
     prm.grid = grid_for(st);
-    const bool lanes = B >= kLaneFillMinB;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = lanes ? dim3(unsigned((int64_t(B) + kLaneFillThreads - 1) / kLaneFillThreads))
-                        : dim3(unsigned((int64_t(B) + kFillWarps - 1) / kFillWarps));
-    cfg.blockDim = dim3(lanes ? kLaneFillThreads : kFillWarps * 32);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (lanes)
-        LD_CUDA(cudaLaunchKernelEx(&cfg, fill_lanes_kernel, prm));
-    else
-        LD_CUDA(cudaLaunchKernelEx(&cfg, fill_kernel, prm));
-    return LOOKUP_DRAFT_OK;
+    if (B >= kLaneFillMinB)
+        return launch_pdl(fill_lanes_kernel, unsigned((int64_t(B) + kLaneFillThreads - 1) / kLaneFillThreads),
+                          unsigned(kLaneFillThreads), stream, prm);
+    return launch_pdl(fill_kernel, unsigned((int64_t(B) + kFillWarps - 1) / kFillWarps), unsigned(kFillWarps * 32),
+                      stream, prm);
 }
 
-cudaError_t launch_host_copy(const DeviceState &st, const CopyParams &cp, cudaStream_t stream) {
+int launch_host_copy(const DeviceState &st, const CopyParams &cp, cudaStream_t stream) {
     const int64_t want = (cp.n16 + kCopyThreads - 1) / kCopyThreads;
     const int64_t cap = int64_t(st.sms) * kCopyCtasPerSm;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(unsigned(want < 1 ? 1 : (want < cap ? want : cap)));
-    cfg.blockDim = dim3(kCopyThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, host_copy_kernel, cp);
+    return launch_pdl(host_copy_kernel, unsigned(want < 1 ? 1 : (want < cap ? want : cap)), unsigned(kCopyThreads),
+                      stream, cp);
 }
 
 int run_step(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t min_m, int32_t max_m, int32_t K,
@@ -1260,7 +1216,7 @@ int run_step(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t m
 constexpr size_t kStaticSlots = size_t(1) << 16;   // 64-bit slots: 512 KiB per device
 
 struct StaticState {
-    bool ready = false;
+    std::atomic<bool> ready{false};                     // set (release) once the fields below are final
     int sms = 0;
     unsigned long long *slots = nullptr;                // device address of the array
 };
@@ -1283,13 +1239,18 @@ namespace {
 
 // Per-device set-up of lookup_draft_noalloc, once: SM count, the scan kernels'
 // shared-memory opt-in, and the device address of g_static_slots.  No allocation.
+// After it, a call only reads the ready flag; the lock is taken for the set-up alone.
 int static_state(StaticState **out) {
     int dev = 0;
     LD_CUDA(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice, "device index");
-    std::lock_guard<std::mutex> lock(g_static_mu);
     StaticState &st = g_static[dev];
-    if (!st.ready) {
+    if (st.ready.load(std::memory_order_acquire)) {
+        *out = &st;
+        return LOOKUP_DRAFT_OK;
+    }
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!st.ready.load(std::memory_order_relaxed)) {
         int sms = 0;
         LD_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
         const int rc_attr = scan_attributes();
@@ -1298,7 +1259,7 @@ int static_state(StaticState **out) {
         LD_CUDA(cudaGetSymbolAddress(&ptr, g_static_slots));
         st.sms = sms;
         st.slots = static_cast<unsigned long long *>(ptr);
-        st.ready = true;
+        st.ready.store(true, std::memory_order_release);
     }
     *out = &st;
     return LOOKUP_DRAFT_OK;
@@ -1434,17 +1395,16 @@ int lookup_draft_host(const int32_t *h_tokens, const int64_t *h_offsets, int32_t
         cp.src_off = static_cast<const int64_t *>(m_off);
         cp.dst_off = d_off;
         cp.n_off = B + 1;
-        e = launch_host_copy(*st, cp, stream);
+        rc = launch_host_copy(*st, cp, stream);
     } else {
         if (n_tok) e = cudaMemcpyAsync(d_tok, h_tokens + first, n_tok * 4, cudaMemcpyHostToDevice, stream);
         if (e == cudaSuccess) e = cudaMemcpyAsync(d_off, h_offsets, off_bytes, cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) rc = cuda_fail(e, "cudaMemcpyAsync (host to device)");
     }
-    if (e == cudaSuccess) {
+    if (rc == LOOKUP_DRAFT_OK) {
         rc = launch_scan(*st, d_tok_base, d_off, B, min_m, max_m, d_ws, stream);
         if (rc == LOOKUP_DRAFT_OK)
             rc = launch_fill(*st, d_tok_base, d_off, B, K, d_ws, d_draft, d_len, d_pos, nullptr, stream);
-    } else {
-        rc = cuda_fail(e, kernel_copy ? "host_copy_kernel launch" : "cudaMemcpyAsync (host to device)");
     }
     if (rc == LOOKUP_DRAFT_OK && !direct && K > 0)
         e = cudaMemcpyAsync(h_out_draft, d_draft, size_t(B) * size_t(K) * 4, cudaMemcpyDeviceToHost, stream);
@@ -1473,7 +1433,6 @@ int lookup_draft_noalloc(const int32_t *tokens, const int64_t *offsets, int32_t 
     if (rc != LOOKUP_DRAFT_OK) return rc;
     DeviceState ds;                                     // SM count only: no pool is made or used
     ds.sms = st->sms;
-    ds.ready = true;
     if (size_t(B) + size_t(grid_for(ds)) * kWarps > kStaticSlots) return LOOKUP_DRAFT_ERANGE;
     rc = launch_scan(ds, tokens, offsets, B, min_m, max_m, st->slots, stream);
     if (rc == LOOKUP_DRAFT_OK)

@@ -189,6 +189,26 @@ def test_large_batch_with_long_requests(B):
     assert_parity(tokens, gen.offsets_from_lengths(lengths), 4, 12, 9, token_pad=B % 4)
 
 
+@pytest.mark.parametrize("S", [511, 512, 2047, 2048])
+def test_chunk_size_at_range_count_switch(S):
+    """Batches whose scan CTA chunk is exactly S quads on this GPU's SM count: 511 /
+    512 quads (8 or 12 warp ranges per CTA) and 2047 / 2048 (12 or 16), where the
+    scan's multiply-high split and the fill's division must agree."""
+    G = torch.cuda.get_device_properties(0).multi_processor_count
+    rng = np.random.default_rng(S)
+    for nq in ((S - 1) * G + 1, S * G):
+        cuts = np.sort(rng.integers(0, 4 * nq - 1, size=int(rng.integers(20, 90))))
+        offsets = np.concatenate([[0], cuts, [4 * nq - 1]]).astype(np.int64)
+        tokens = rng.integers(0, 40, size=4 * nq - 1).astype(np.int32)
+        for r in range(0, offsets.size - 1, 3):              # planted copies of earlier spans
+            o, n = int(offsets[r]), int(offsets[r + 1])
+            if n - o > 64:
+                c = int(rng.integers(13, min(60, (n - o) // 2)))
+                s0 = int(rng.integers(o, n - 2 * c))
+                tokens[n - c:n] = tokens[s0:s0 + c]
+        assert_parity(tokens, offsets, 4, 12, 15)
+
+
 def test_all_equal_tokens():
     lengths = [1, 17, 4096, 25000, 3]
     tokens = np.full(sum(lengths), -7, dtype=np.int32)

@@ -96,6 +96,14 @@ def warp_ranges(nq, G):
     return S, Sw, out
 
 
+def fill_partition(nq, G):
+    """(S, Sw) as the fill kernel forms them (make_partition: plain divisions, the
+    wide-chunk rule written separately), to be held against the scan's."""
+    S = (nq + G - 1) // G
+    Sw = warp_span(S) if S < CHUNK_MID else (S + K_WARPS - 1) // K_WARPS
+    return S, Sw
+
+
 def tiles(wn):
     tq = wn if wn <= TQ_MAX else (wn + 1) // 2
     tq = min(max(tq, TQ_MIN), TQ_MAX)
@@ -118,6 +126,7 @@ def emulate(offsets, shift, G, min_m, max_m):
     q_lo = a_begin >> 2
     nq = ((a_end + 3) >> 2) - q_lo
     S, Sw, ranges = warp_ranges(nq, G)
+    assert (S, Sw) == fill_partition(nq, G)              # scan and fill agree on the split
     halo = (max_m - 1 + 3) >> 2
     assert halo <= HALO_QUADS
     covered = np.zeros(nq, np.int32)
@@ -198,3 +207,34 @@ def test_workload_sized_batches():
                     np.exp(np.random.default_rng(4).uniform(np.log(512), np.log(262_144), size=256)).astype(np.int64)):
         offsets = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
         emulate(offsets, 0, 152, 4, 12)
+
+
+def batch_with_chunk(S, G, rng, shift=0, lead=0):
+    """Offsets of a batch whose CTA chunk is exactly S quads on G CTAs: its quads
+    run from (S - 1) * G + 1 to S * G (both ends are drawn), cut into requests of
+    random lengths (some empty, some shorter than a quad)."""
+    nq = int(rng.choice([(S - 1) * G + 1, S * G, int(rng.integers((S - 1) * G + 1, S * G + 1))]))
+    a0 = 4 * ((lead + shift) >> 2)
+    total = 4 * nq - ((lead + shift) - a0) - int(rng.integers(0, 4))
+    cuts = np.sort(rng.integers(0, total + 1, size=int(rng.integers(0, 60))))
+    bounds = np.concatenate([[0], cuts, [total]])
+    return (lead + bounds).astype(np.int64)
+
+
+@pytest.mark.parametrize("S", [CHUNK_SMALL - 1, CHUNK_SMALL, CHUNK_MID - 1, CHUNK_MID])
+@pytest.mark.parametrize("G", [152, 148, 7])
+def test_chunk_sizes_at_the_range_count_switches(S, G):
+    """A CTA chunk of 511 / 512 quads (8 or 12 warp ranges) and of 2047 / 2048 (12 or
+    16): the scan's multiply-high path and the fill's division give the same split,
+    and the ranges still tile the batch with an exact cover per request."""
+    rng = np.random.default_rng(S * 1000 + G)
+    for _ in range(6):
+        shift = int(rng.integers(0, 4))
+        lead = int(rng.integers(0, 9))
+        offsets = batch_with_chunk(S, G, rng, shift, lead)
+        offa = offsets + shift
+        q_lo = int(offa[0]) >> 2
+        nq = ((int(offa[-1]) + 3) >> 2) - q_lo
+        assert warp_ranges(nq, G)[0] == S
+        emulate(offsets, shift, G, 4, 12)
+        emulate(offsets, shift, G, 1, MAX_M)
