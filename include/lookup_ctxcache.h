@@ -20,14 +20,22 @@
  *   draft ends.  Counts come from the history only.
  * out_len[r] is the number of tokens drafted (0..K); out_draft[r][len..K) = -1.
  *
+ * Tokens compare as raw int32 values, as in lookup_draft.h: negative and
+ * out-of-vocabulary values are counted and matched like any other.
+ *
  * The cache holds, for every request r, n in [n_min, n_max] and history n-gram
  * g: the number of its occurrences with a next token, and the best (count, next
  * token) pair; and for every (g, next token) its count.  Keys are the exact
  * (r, n, g, x) packed into 128 bits -- no hashing of the identity, so no two
- * n-grams ever share counts -- which bounds the domain:
- *   token ids in [0, 2^20) (the pages' Qwen vocabulary is 151,936), B <= 65,536,
- *   1 <= n_min <= n_max <= 4.
- * An n-gram with a token outside [0, 2^20) is not counted and never matches.
+ * n-grams ever share counts.  A token enters a key as a 21-bit code: a value in
+ * [0, 2^20) (the pages' Qwen vocabulary is 151,936) is its own code; any other
+ * int32 value is given a code by a dictionary kept in the same table (2^20
+ * codes; a value takes the first free code of a probe sequence of its own, so
+ * up to about a million distinct such values per cache, its build and appends
+ * together).  Limits: B <= 65,536, 1 <= n_min <= n_max <= 4.  A cache in which
+ * some value found no code, or some key found no slot, fails every request of
+ * its drafts (out_len LOOKUP_DRAFT_LEN_FAILED) instead of drafting from
+ * incomplete counts.
  *
  * Layout (device memory, caller-owned): the slabs of include/lookup_index.h --
  * tokens int32 [N], base int64 [B], len int32 [B], cap int32 [B]; request r's
@@ -54,7 +62,8 @@ struct CUstream_st;
 
 /* Slots for `capacity_tokens` history tokens: the smallest power of two >=
  * 4 * (n_max - n_min + 1) * capacity_tokens (two keys per position and length,
- * load factor <= 1/2).  0 for invalid arguments. */
+ * load factor <= 1/2; dictionary keys, at most one per distinct token value
+ * outside [0, 2^20), keep it <= 3/4).  0 for invalid arguments. */
 int64_t lookup_ctx_slots_for(int64_t capacity_tokens, int32_t n_min, int32_t n_max);
 
 /* 128 + 32 * slots (0 unless slots is a power of two >= 16). */

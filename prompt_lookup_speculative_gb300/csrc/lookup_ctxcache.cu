@@ -6,21 +6,30 @@
 // include/lookup_ctxcache.h.
 //
 // Table: a 128-byte header, then 32-byte slots {key (two 64-bit words), v0, v1}
-// in buckets of 2.  A key is the exact (r, n, g, x) packed into 128 bits (20-bit
-// tokens), so two n-grams never share a slot; only the bucket is hashed.  Two
-// kinds of key:
+// in buckets of 2.  A key is the exact (r, n, g, x) packed into 128 bits, so two
+// n-grams never share a slot; only the bucket is hashed.  Tokens enter keys as
+// 21-bit codes: a token in [0, 2^20) is its own code, and any other int32 value
+// gets a code in [2^20, 2^21) from a dictionary kept in the same table, so the
+// statistics are exact on every int32 value.  Three kinds of key:
 //   COUNT (r, n, g, x): v0 = how many occurrences of g are followed by x;
 //   CTX   (r, n, g):    v0 = occurrences of g that have a next token,
-//                       v1 = max over x of (count(g, x) << 32 | (2^32 - 1 - x)).
+//                       v1 = max over x of (count(g, x) << 32 | order(x)),
+//                       order(x) = 2^32 - 1 - (x + 2^31) as unsigned, so the
+//                       maximum is the smallest signed token with the count;
+//   CODE  (c):          v0 = 2^32 | the token value that owns dictionary code c.
 // Counting an occurrence of g followed by x is an atomicAdd on COUNT (giving the
-// new count c), an atomicAdd on CTX.v0 and an atomicMax of (c << 32 | ~x) on
-// CTX.v1.  Counts only grow, so v1 ends as (the largest count, the smallest
+// new count c), an atomicAdd on CTX.v0 and an atomicMax of (c << 32 | order(x))
+// on CTX.v1.  Counts only grow, so v1 ends as (the largest count, the smallest
 // token with that count) in any order of updates: the build counts every
 // position of every history in parallel.  A slot is claimed with one 128-bit CAS
-// of its key.  The draft is one warp per request, one token per round: lane l
-// reads the CTX slot of the context's last (n_max - l) tokens, the longest
-// length that passes the thresholds gives the token, and the context window
-// (four tokens, one per lane) shifts by a shuffle.
+// of its key.  A value outside [0, 2^20) owns the first code of its probe
+// sequence (a hash of the value, then the following codes) that was free when it
+// asked or already is its own; a code is taken with one CAS of its CODE slot's
+// value, so racing claimants of one value agree and no code is wasted.  The draft is one
+// warp per request, one token per round: lane l reads the CTX slot of the
+// context's last (n_max - l) tokens, the longest length that passes the
+// thresholds gives the token, and the context window (four tokens and their
+// codes, one per lane) shifts by a shuffle.
 
 #include "lookup_ctxcache.h"
 
@@ -38,8 +47,10 @@ using lkd::wait_for_prerequisite_grid;
 constexpr uint32_t kMagic = 0x4c4b4358u;        // "LKCX"
 constexpr int kBucket = 2;                      // slots per bucket: one 64-byte pair of sectors
 constexpr int kMaxProbe = 2048;                 // buckets probed before the overflow flag
-constexpr int kTokBits = 20;
-constexpr int32_t kTokLimit = 1 << kTokBits;
+constexpr int kCodeBits = 21;                   // token code width in a key
+constexpr int32_t kDirect = 1 << 20;            // tokens in [0, kDirect) are their own code
+constexpr uint32_t kMaxCodes = 1u << 20;        // dictionary codes: kDirect + [0, kMaxCodes)
+constexpr int kCodeProbe = 4096;                // codes tried per value before the overflow flag
 constexpr int kThreads = 256;
 constexpr int kDraftThreads = 128;              // 4 warps per CTA, one request each
 constexpr int kScanThreads = 1024;
@@ -49,7 +60,7 @@ struct __align__(16) Header {
     uint32_t magic;
     int32_t n_min, n_max, pad0;
     int64_t slots;
-    uint32_t overflow;
+    uint32_t overflow;                          // a key found no slot, or a value found no code
     uint32_t pad[25];
 };
 static_assert(sizeof(Header) == 128, "header is 128 bytes");
@@ -61,16 +72,28 @@ static_assert(sizeof(Slot) == 32, "slot is 32 bytes");
 
 enum Kind { kCount = 0, kCtx = 1 };
 
-__device__ inline bool in_range(int32_t t) { return t >= 0 && t < kTokLimit; }
-
-// g: the n tokens oldest first (unused entries 0).
+// g: the codes of the n tokens, oldest first (unused entries 0); x: a code.  Bits:
+// lo = g0 | g1 << 21 | g2 << 42 | kind << 63, hi = g3 | x << 21 | n << 42 | r << 45.
+// n >= 1 keeps every such key non-zero and apart from the dictionary's CODE keys (n = 0).
 __device__ inline void make_key(int r, int n, const int32_t (&g)[kMaxN], int kind, int32_t x, uint64_t &lo,
                                 uint64_t &hi) {
-    lo = uint64_t(uint32_t(g[0])) | (uint64_t(uint32_t(g[1])) << 20) | (uint64_t(uint32_t(g[2])) << 40) |
-         (uint64_t(kind) << 60);
-    hi = uint64_t(uint32_t(g[3])) | (uint64_t(uint32_t(x)) << 20) | (uint64_t(n) << 40) |
-         (uint64_t(uint32_t(r)) << 43);
+    lo = uint64_t(uint32_t(g[0])) | (uint64_t(uint32_t(g[1])) << kCodeBits) |
+         (uint64_t(uint32_t(g[2])) << (2 * kCodeBits)) | (uint64_t(kind) << 63);
+    hi = uint64_t(uint32_t(g[3])) | (uint64_t(uint32_t(x)) << kCodeBits) | (uint64_t(n) << (2 * kCodeBits)) |
+         (uint64_t(uint32_t(r)) << (2 * kCodeBits + 3));
 }
+
+// The key of dictionary code c (bit 61 of hi; n = 0), and the mark of its owner v.
+__device__ inline void code_key(uint32_t c, uint64_t &lo, uint64_t &hi) {
+    lo = c;
+    hi = 1ull << 61;
+}
+__device__ inline unsigned long long owner_mark(int32_t v) { return (1ull << 32) | uint32_t(v); }
+__device__ inline uint32_t first_code(int32_t v) { return uint32_t(mix64(uint32_t(v))) & (kMaxCodes - 1u); }
+
+// Order of a token among equal counts: larger for smaller signed values.
+__device__ inline uint64_t tie_order(int32_t x) { return 0xffffffffull - uint64_t(uint32_t(x) ^ 0x80000000u); }
+__device__ inline int32_t from_tie_order(uint64_t low) { return int32_t(uint32_t(0xffffffffull - low) ^ 0x80000000u); }
 
 __device__ inline int64_t bucket_of(uint64_t lo, uint64_t hi, int64_t bmask) {
     return int64_t(mix64(lo ^ mix64(hi)) & uint64_t(bmask));
@@ -128,18 +151,60 @@ __device__ inline bool find(const Slot *tab, int64_t bmask, uint64_t lo, uint64_
     return false;
 }
 
-// One occurrence of g (length n) followed by x.
+// The code of token v if it has one (read only); -1 when v owns no code, so no
+// counted n-gram holds it.  A free code met before v's means v never asked for
+// one: codes are never released, so v would have taken it.
+__device__ inline int32_t encode_find(const Slot *tab, int64_t bmask, int32_t v) {
+    if (v >= 0 && v < kDirect) return v;
+    const unsigned long long mark = owner_mark(v);
+    uint32_t c = first_code(v);
+    for (int probe = 0; probe < kCodeProbe; ++probe) {
+        uint64_t lo, hi;
+        code_key(c, lo, hi);
+        unsigned long long owner = 0ull, unused = 0ull;
+        if (!find(tab, bmask, lo, hi, owner, unused) || owner == 0ull) return -1;
+        if (owner == mark) return kDirect + int32_t(c);
+        c = (c + 1u) & (kMaxCodes - 1u);
+    }
+    return -1;
+}
+
+// The code of token v, taking a dictionary code when v is outside [0, kDirect);
+// -1 (with the overflow flag) when the table ran out of slots or no code of v's
+// probe sequence could be had.
+__device__ inline int32_t encode_claim(Slot *tab, int64_t bmask, Header *hd, int32_t v) {
+    if (v >= 0 && v < kDirect) return v;
+    const unsigned long long mark = owner_mark(v);
+    uint32_t c = first_code(v);
+    for (int probe = 0; probe < kCodeProbe; ++probe) {
+        uint64_t lo, hi;
+        code_key(c, lo, hi);
+        Slot *sl = claim(tab, bmask, lo, hi, hd);
+        if (!sl) return -1;
+        unsigned long long owner = __ldcg(&sl->v0);
+        if (owner == 0ull) {
+            owner = atomicCAS(&sl->v0, 0ull, mark);
+            if (owner == 0ull) owner = mark;                 // taken now
+        }
+        if (owner == mark) return kDirect + int32_t(c);
+        c = (c + 1u) & (kMaxCodes - 1u);
+    }
+    atomicOr(&hd->overflow, 1u);
+    return -1;
+}
+
+// One occurrence of g (codes, length n) followed by the token x (code cx).
 __device__ inline void count_pair(Slot *tab, int64_t bmask, Header *hd, int r, int n, const int32_t (&g)[kMaxN],
-                                  int32_t x) {
+                                  int32_t x, int32_t cx) {
     uint64_t lo, hi;
-    make_key(r, n, g, kCount, x, lo, hi);
+    make_key(r, n, g, kCount, cx, lo, hi);
     Slot *c_slot = claim(tab, bmask, lo, hi, hd);
     make_key(r, n, g, kCtx, 0, lo, hi);
     Slot *g_slot = claim(tab, bmask, lo, hi, hd);
     if (!c_slot || !g_slot) return;
     const unsigned long long c = atomicAdd(&c_slot->v0, 1ull) + 1ull;
     atomicAdd(&g_slot->v0, 1ull);
-    atomicMax(&g_slot->v1, (c << 32) | (0xffffffffull - uint64_t(uint32_t(x))));
+    atomicMax(&g_slot->v1, (c << 32) | tie_order(x));
 }
 
 // ------------------------------------------------------------------ build ----
@@ -247,20 +312,25 @@ __global__ void __launch_bounds__(kThreads) build_kernel(BuildParams p) {
         if (i < 1) continue;
         const int32_t *t = p.tokens + base;
         const int32_t x = t[i];
+        const int span = i < p.n_max ? i : p.n_max;      // tokens before x that an n-gram uses
         int32_t w[kMaxN];                                // w[k] = t[i - 1 - k]
 #pragma unroll
-        for (int k = 0; k < kMaxN; ++k) w[k] = k < i ? t[i - 1 - k] : -1;
-        if (!in_range(x)) continue;
-        for (int n = p.n_min; n <= p.n_max && n <= i; ++n) {
+        for (int k = 0; k < kMaxN; ++k) w[k] = k < span ? t[i - 1 - k] : 0;
+        const int32_t cx = encode_claim(p.tab, bmask, p.hd, x);
+        if (cx < 0) continue;                            // out of room: flagged, every draft fails
+        int32_t cw[kMaxN];                               // their codes
+#pragma unroll
+        for (int k = 0; k < kMaxN; ++k) cw[k] = k < span ? encode_claim(p.tab, bmask, p.hd, w[k]) : 0;
+        for (int n = p.n_min; n <= span; ++n) {
             int32_t g[kMaxN] = {0, 0, 0, 0};
             bool ok = true;
 #pragma unroll
             for (int k = 0; k < kMaxN; ++k)
                 if (k < n) {
-                    g[k] = w[n - 1 - k];                 // oldest first
-                    ok = ok && in_range(g[k]);
+                    g[k] = cw[n - 1 - k];                // oldest first
+                    ok = ok && g[k] >= 0;
                 }
-            if (ok) count_pair(p.tab, bmask, p.hd, r, n, g, x);
+            if (ok) count_pair(p.tab, bmask, p.hd, r, n, g, x, cx);
         }
     }
 }
@@ -310,17 +380,19 @@ __global__ void __launch_bounds__(kThreads) ctx_append_kernel(AppendParams p) {
         const int32_t x = crow[j];
         if (n == p.n_min) p.tokens[base + L + j] = x;      // one writer per new token
         const int i = L + j;                                 // x's position
-        if (i < n || !in_range(x)) continue;
+        if (i < n) continue;
+        const int32_t cx = encode_claim(p.tab, bmask, p.hd, x);
+        if (cx < 0) continue;                                // out of room: flagged
         int32_t g[kMaxN] = {0, 0, 0, 0};
         bool okg = true;
 #pragma unroll
         for (int k = 0; k < kMaxN; ++k)
             if (k < n) {
                 const int src = i - n + k;
-                g[k] = src >= L ? crow[src - L] : p.tokens[base + src];
-                okg = okg && in_range(g[k]);
+                g[k] = encode_claim(p.tab, bmask, p.hd, src >= L ? crow[src - L] : p.tokens[base + src]);
+                okg = okg && g[k] >= 0;
             }
-        if (okg) count_pair(p.tab, bmask, p.hd, r, n, g, x);
+        if (okg) count_pair(p.tab, bmask, p.hd, r, n, g, x, cx);
     }
 }
 
@@ -347,17 +419,19 @@ __global__ void __launch_bounds__(kThreads) ctx_append_request_kernel(AppendPara
             const int32_t x = crow[j];
             if (n == p.n_min) p.tokens[base + L + j] = x;      // one writer per new token
             const int i = L + j;                                 // x's position
-            if (i < n || !in_range(x)) continue;
+            if (i < n) continue;
+            const int32_t cx = encode_claim(p.tab, bmask, p.hd, x);
+            if (cx < 0) continue;                                // out of room: flagged
             int32_t g[kMaxN] = {0, 0, 0, 0};
             bool okg = true;
 #pragma unroll
             for (int k = 0; k < kMaxN; ++k)
                 if (k < n) {
                     const int src = i - n + k;
-                    g[k] = src >= L ? crow[src - L] : p.tokens[base + src];
-                    okg = okg && in_range(g[k]);
+                    g[k] = encode_claim(p.tab, bmask, p.hd, src >= L ? crow[src - L] : p.tokens[base + src]);
+                    okg = okg && g[k] >= 0;
                 }
-            if (okg) count_pair(p.tab, bmask, p.hd, r, n, g, x);
+            if (okg) count_pair(p.tab, bmask, p.hd, r, n, g, x, cx);
         }
         __syncthreads();                                     // every reader of len[r] is done
         if (threadIdx.x == 0) {
@@ -406,8 +480,10 @@ __global__ void __launch_bounds__(kDraftThreads) ctx_draft_kernel(DraftParams p)
         const int L = max(p.len[r], 0);
         const int32_t *t = p.tokens + p.base[r];
         int32_t *row = p.out_draft + int64_t(r) * p.K;
-        // the context window: lane k < 4 holds the k-th token from the end
-        int32_t c = (lane < kMaxN && lane < L) ? t[L - 1 - lane] : -1;
+        // the context window: lane k < 4 holds the code of the k-th token from the
+        // end (-1: a value that no counted n-gram holds)
+        int32_t c = -1;
+        if (ok && lane < kMaxN && lane < L) c = encode_find(p.tab, bmask, t[L - 1 - lane]);
         int j = 0;
         while (ok && j < p.K) {
             const int n = p.n_max - lane;                // lane 0: the longest length
@@ -419,7 +495,7 @@ __global__ void __launch_bounds__(kDraftThreads) ctx_draft_kernel(DraftParams p)
                 const int32_t v = __shfl_sync(0xffffffffu, c, src);
                 if (k < n) {
                     g[k] = v;
-                    okg = okg && in_range(v);
+                    okg = okg && v >= 0;
                 }
             }
             bool pass = false;
@@ -438,10 +514,10 @@ __global__ void __launch_bounds__(kDraftThreads) ctx_draft_kernel(DraftParams p)
             if (!ballot) break;
             const int src = __ffs(ballot) - 1;           // the longest passing length
             const unsigned long long b = __shfl_sync(0xffffffffu, best, src);
-            const int32_t x = int32_t(0xffffffffu - uint32_t(b & 0xffffffffull));
+            const int32_t x = from_tie_order(b & 0xffffffffull);
             if (lane == 0) row[j] = x;
             const int32_t up = __shfl_up_sync(0xffffffffu, c, 1);
-            c = lane == 0 ? x : up;
+            c = lane == 0 ? encode_find(p.tab, bmask, x) : up;   // x was counted, so it has a code
             ++j;
         }
         for (int k = j + lane; k < p.K; k += 32) row[k] = -1;
