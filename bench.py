@@ -305,39 +305,71 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         for i in range(max(args.warmup, 3)):
             step(i, h)
     stream.synchronize()
+    # graphs: one whole rotation (steps over copies 0 .. ncopy-1) and, for K not a
+    # multiple of ncopy, the first K mod ncopy steps of one.  The untimed replays
+    # run whole rotations only, so the timed region starts at copy 0, the least
+    # recently read: every timed step reads a copy last read ncopy steps earlier,
+    # with (ncopy - 1) other copies (> 2x L2) read in between.
     full_reps, tail = divmod(args.steps, ncopy)
-    graphs = {}
-    for n in sorted({ncopy if full_reps else 0, tail} - {0}):
+
+    def capture(n):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             hc = int(torch.cuda.current_stream().cuda_stream)
             for i in range(n):
                 step(i, hc)
-        graphs[n] = g
+        return g
+
+    g_full = capture(ncopy)
+    g_tail = capture(tail) if tail else None
+    clock_hz = float(getattr(torch.cuda.get_device_properties(dev), "clock_rate", 2_000_000)) * 1000.0
     with torch.cuda.stream(stream):
+        for _ in range(3):                           # first launches upload the graphs
+            for g in (g_tail, g_full):
+                if g is not None:
+                    g.replay()
         t_end = time.perf_counter() + args.settle_s  # untimed replays: clocks settle under load
         while True:
-            for g in graphs.values():
-                g.replay()
+            g_full.replay()
             stream.synchronize()
             if time.perf_counter() >= t_end:
                 break
 
-    # timed region: exactly K steps
+    # timed region: exactly K steps.  A short device-side sleep ahead of the start
+    # event lets the host enqueue the replays first, so the events time the steps
+    # on the device, not the host's graph submission.
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(200e-6 * clock_hz))
         ev0.record(stream)
         for _ in range(full_reps):
-            graphs[ncopy].replay()
-        if tail:
-            graphs[tail].replay()
+            g_full.replay()
+        if g_tail is not None:
+            g_tail.replay()
         ev1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(dist, dev)
     ms_total = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
     us_per_step = 1000.0 * ms_total / args.steps
+
+    # spread: whole rotations replayed one by one, each between its own events
+    n_spread = 40
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_spread)]
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(200e-6 * clock_hz))
+        for a, b in evs:
+            a.record(stream)
+            g_full.replay()
+            b.record(stream)
+    torch.cuda.synchronize(dev)
+    per_rep = sorted(1000.0 * a.elapsed_time(b) / ncopy for a, b in evs)
+    spread = {q: round(max_over_ranks(float(np.percentile(per_rep, v)), dist, dev), 3)
+              for q, v in (("p10", 10), ("p50", 50), ("p90", 90))}
+    spread.update({"replays": n_spread, "steps_per_replay": ncopy,
+                   "what": "us per step of single whole-rotation graph replays, each between its own CUDA events"})
+    del g_full, g_tail
 
     # eager: the same K steps as direct calls
     with torch.cuda.stream(stream):
@@ -387,7 +419,6 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     floor = time_read_floor(lib, pkg, toks, w.history_bytes, dev, stream, reps)
     floor_us = max_over_ranks(floor["us"], dist, dev)
     fill_us = max_over_ranks(time_graph(graph_of(fill_call), reps), dist, dev)
-    clock_hz = float(getattr(props, "clock_rate", 2_000_000)) * 1000.0
     ea = [torch.cuda.Event(enable_timing=True) for _ in range(ncopy)]
     eb = [torch.cuda.Event(enable_timing=True) for _ in range(ncopy)]
     iso_ms = []
@@ -475,12 +506,17 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
             "description": gen.DESCRIPTION[args.workload],
             "B": B, "history_tokens": w.total_tokens, "history_bytes": hist_bytes,
             "min_m": min_m, "max_m": max_m, "K": K, "seed": seed,
-            "l2": f"inputs rotate over {ncopy} device copies "
-                  f"({ncopy * hist_bytes / 2**20:.0f} MiB > 2x L2 of {l2 / 2**20:.0f} MiB)",
-            "launch": f"lookup_draft calls captured in CUDA graphs of {ncopy} steps",
+            "l2": f"inputs larger than L2 in rotation: the {args.steps} timed steps read device copies "
+                  f"0, 1, ... (mod {ncopy}) of the batch, each last read {ncopy} steps earlier with "
+                  f"{(ncopy - 1) * hist_bytes / 2**20:.0f} MiB of other copies read in between "
+                  f"(> 2x L2 of {l2 / 2**20:.0f} MiB); {ncopy} copies, "
+                  f"{ncopy * hist_bytes / 2**20:.0f} MiB in all",
+            "launch": (f"lookup_draft calls captured in a CUDA graph of {ncopy} steps (one rotation), "
+                       f"replayed {full_reps}x" + (f", then a graph of the first {tail}" if tail else "")),
             "parallelism": f"replicas x{world} (one batch per GPU, no exchange)",
         },
         "history_gbs_per_step": round(world * hist_bytes / (us_per_step * 1e-6) / 1e9, 1),
+        "step_us_spread": spread,
         "eager_us_per_step": round(eager_us, 3),
         "scan_us": round(scan_us, 3),
         "scan_us_isolated": round(scan_iso_us, 3),
@@ -924,86 +960,114 @@ def time_read_floor(lib, pkg, toks, nbytes: int, dev, stream, reps: int) -> dict
 
 
 # ------------------------------------------------------------ workloads ----
-def measure_workloads(lib, pkg, dev, stream, names, seed_offset: int, reps_cap: int) -> dict:
-    """The draft step and the scan on each named workload, timed the way the main
-    line times its own: ncopy calls over rotating device copies (> 2x L2 in total)
+SPREAD_SEEDS = (6, 7, 8, 9, 10)
+
+
+def time_workload(lib, pkg, w, dev, stream, l2: int, reps_cap: int, with_floor: bool) -> dict:
+    """The draft step and the scan on one workload, timed the way the main line
+    times its own: ncopy calls over rotating device copies (> 2x L2 in total)
     captured in one CUDA graph, replayed back to back, CUDA events on the launching
-    stream.  Per workload: step and scan microseconds, the scan's GB/s (4 bytes per
-    history token) against the measured copy bandwidth, and whether the step's
-    outputs equal the oracle's on the whole batch."""
+    stream; the step's outputs against the oracle's on the whole batch."""
     import numpy as np
     import torch
 
-    import gen
     import oracle
+
+    peak, _ = measured_hbm_peak()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    B, K = w.B, w.K
+    ncopy = max(3, math.ceil(2 * l2 / max(w.history_bytes, 1)) + 1)
+    tok_host, off_host = torch.from_numpy(w.tokens), torch.from_numpy(w.offsets)
+    toks = [tok_host.to(dev) for _ in range(ncopy)]
+    offs = [off_host.to(dev) for _ in range(ncopy)]
+    draft = torch.empty((B, K), dtype=torch.int32, device=dev)
+    length = torch.empty(B, dtype=torch.int32, device=dev)
+    pos = torch.empty(B, dtype=torch.int32, device=dev)
+    ws_bytes = pkg.workspace_bytes(B, dev)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    reps = max(10, min(reps_cap, 20000 // ncopy))
+
+    def step(j, hc):
+        rc = lib.lookup_draft(toks[j].data_ptr(), offs[j].data_ptr(), B, w.min_m, w.max_m, K,
+                              draft.data_ptr(), length.data_ptr(), pos.data_ptr(), hc)
+        if rc != 0:
+            raise pkg.LookupDraftError(rc, lib)
+
+    def scan(j, hc):
+        rc = lib.lookup_draft_scan(toks[j].data_ptr(), offs[j].data_ptr(), B, w.min_m, w.max_m,
+                                   ws.data_ptr(), ws_bytes, hc)
+        if rc != 0:
+            raise pkg.LookupDraftError(rc, lib)
+
+    def timed(fn) -> float:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            hc = int(torch.cuda.current_stream().cuda_stream)
+            for j in range(ncopy):
+                fn(j, hc)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            ev0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        return 1000.0 * ev0.elapsed_time(ev1) / (reps * ncopy)
+
+    step_us = timed(step)
+    got = (draft.cpu().numpy(), length.cpu().numpy(), pos.cpu().numpy())
+    scan_us = timed(scan)
+    want = oracle.lookup_draft(w.tokens, w.offsets, w.min_m, w.max_m, K, threads=os.cpu_count() or 1)
+    parity = all(np.array_equal(a, b) for a, b in zip(got, want[:3]))
+    gbs = w.history_bytes / (scan_us * 1e-6) / 1e9
+    res = {"B": B, "history_bytes": int(w.history_bytes), "seed": int(w.seed),
+           "step_us": round(step_us, 3), "scan_us": round(scan_us, 3),
+           "scan_gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    if with_floor:
+        floor = time_read_floor(lib, pkg, toks, w.history_bytes, dev, stream, reps)
+        res.update({"read_floor_us": round(floor["us"], 3),
+                    "read_floor_frac": round(w.history_bytes / (floor["us"] * 1e-6) / 1e9 / peak, 4),
+                    "scan_vs_read_floor": round(floor["us"] / scan_us, 3)})
+    res.update({"copies": ncopy, "parity_with_oracle": bool(parity)})
+    del toks, offs, ws
+    torch.cuda.synchronize(dev)
+    return res
+
+
+def measure_workloads(lib, pkg, dev, stream, names, seed_offset: int, reps_cap: int) -> dict:
+    """Per workload: the step and the scan on its default seed (with the read floor
+    of the same bytes), then on seeds 6-10 (step, scan, parity), each timed by
+    time_workload; the scan's GB/s (4 bytes per history token) against the
+    measured copy bandwidth."""
+    import torch
+
+    import gen
 
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2**20))
     peak, peak_kind = measured_hbm_peak()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    out = {}
+    out, seeds = {}, {}
     for name in names:
         w = gen.make_workload(name, gen.DEFAULT_SEED[name] + seed_offset)
-        B, K = w.B, w.K
-        ncopy = max(3, math.ceil(2 * l2 / max(w.history_bytes, 1)) + 1)
-        tok_host, off_host = torch.from_numpy(w.tokens), torch.from_numpy(w.offsets)
-        toks = [tok_host.to(dev) for _ in range(ncopy)]
-        offs = [off_host.to(dev) for _ in range(ncopy)]
-        draft = torch.empty((B, K), dtype=torch.int32, device=dev)
-        length = torch.empty(B, dtype=torch.int32, device=dev)
-        pos = torch.empty(B, dtype=torch.int32, device=dev)
-        ws_bytes = pkg.workspace_bytes(B, dev)
-        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-
-        def step(j, hc):
-            rc = lib.lookup_draft(toks[j].data_ptr(), offs[j].data_ptr(), B, w.min_m, w.max_m, K,
-                                  draft.data_ptr(), length.data_ptr(), pos.data_ptr(), hc)
-            if rc != 0:
-                raise pkg.LookupDraftError(rc, lib)
-
-        def scan(j, hc):
-            rc = lib.lookup_draft_scan(toks[j].data_ptr(), offs[j].data_ptr(), B, w.min_m, w.max_m,
-                                       ws.data_ptr(), ws_bytes, hc)
-            if rc != 0:
-                raise pkg.LookupDraftError(rc, lib)
-
-        def timed(fn) -> float:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                hc = int(torch.cuda.current_stream().cuda_stream)
-                for j in range(ncopy):
-                    fn(j, hc)
-            reps = max(10, min(reps_cap, 20000 // ncopy))
-            with torch.cuda.stream(stream):
-                for _ in range(3):
-                    g.replay()
-                ev0.record(stream)
-                for _ in range(reps):
-                    g.replay()
-                ev1.record(stream)
-            torch.cuda.synchronize(dev)
-            return 1000.0 * ev0.elapsed_time(ev1) / (reps * ncopy)
-
-        step_us = timed(step)
-        got = (draft.cpu().numpy(), length.cpu().numpy(), pos.cpu().numpy())
-        scan_us = timed(scan)
-        floor = time_read_floor(lib, pkg, toks, w.history_bytes, dev, stream, max(10, min(reps_cap, 20000 // ncopy)))
-        want = oracle.lookup_draft(w.tokens, w.offsets, w.min_m, w.max_m, K, threads=os.cpu_count() or 1)
-        parity = all(np.array_equal(a, b) for a, b in zip(got, want[:3]))
-        gbs = w.history_bytes / (scan_us * 1e-6) / 1e9
-        out[name] = {"B": B, "history_bytes": int(w.history_bytes), "seed": int(w.seed),
-                     "step_us": round(step_us, 3), "scan_us": round(scan_us, 3),
-                     "scan_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
-                     "read_floor_us": round(floor["us"], 3),
-                     "read_floor_frac": round(w.history_bytes / (floor["us"] * 1e-6) / 1e9 / peak, 4),
-                     "scan_vs_read_floor": round(floor["us"] / scan_us, 3),
-                     "copies": ncopy, "parity_with_oracle": bool(parity)}
-        del toks, offs, ws
-        torch.cuda.synchronize(dev)
+        out[name] = time_workload(lib, pkg, w, dev, stream, l2, reps_cap, True)
+        rows = []
+        for sd in SPREAD_SEEDS:
+            r = time_workload(lib, pkg, gen.make_workload(name, sd + seed_offset), dev, stream, l2, reps_cap, False)
+            rows.append({k: r[k] for k in ("seed", "history_bytes", "step_us", "scan_us", "frac",
+                                           "parity_with_oracle")})
+        steps = sorted(r["step_us"] for r in rows)
+        scans = sorted(r["scan_us"] for r in rows)
+        seeds[name] = {"per_seed": rows,
+                       "step_us_median": steps[len(steps) // 2], "step_us_min": steps[0], "step_us_max": steps[-1],
+                       "scan_us_median": scans[len(scans) // 2], "scan_us_min": scans[0], "scan_us_max": scans[-1],
+                       "parity_with_oracle": all(r["parity_with_oracle"] for r in rows)}
     return {"peak_gbs": peak, "peak_kind": f"{peak_kind} copy bandwidth",
             "method": "per workload: calls over rotating device copies (> 2x L2) captured in one CUDA graph, "
                       "replayed back to back; CUDA events on the launching stream",
-            "workloads": out}
+            "workloads": out,
+            "seeds": seeds,
+            "seeds_what": f"the same timings on seeds {', '.join(map(str, SPREAD_SEEDS))} of each workload"}
 
 
 # ------------------------------------------------------------------ CPU ----
