@@ -13,15 +13,16 @@
  * the K tokens after it read from the self-extended history.
  *
  * What the index holds.  For every request r, every length n in [min_m, max_m]
- * and every history position q >= n - 1, the n-gram ending at q is a key
- * (r, n, t[q-n+1 .. q]).  Each key's slot holds the two largest positions at
- * which it ends (top1 > top2).  The current suffix's own n-gram ends at L - 1,
- * the newest position, so its top2 is the most recent earlier occurrence: the
- * longest n whose top2 exists is the match length, top2 - n + 1 its position.
- * Keys are 64-bit hashes; every candidate is checked against the history, and a
- * request whose candidates do not check out (two keys sharing a slot, or a
- * table that overflowed) is answered by a brute-force warp scan of its history,
- * so the result is exact whatever the hash does.
+ * and every history position q with n - 1 <= q <= L - 2 (every position but the
+ * last), the n-gram ending at q is a key (r, n, t[q-n+1 .. q]).  Each key's slot
+ * holds the largest such q.  The current suffix's own n-gram ends at L - 1, the
+ * unindexed last position, so its slot gives the most recent earlier
+ * occurrence: the longest n with a slot is the match length, q - n + 1 its
+ * position.  Keys are 64-bit hashes of which a slot keeps a 32-bit fingerprint;
+ * every candidate is checked against the history, and a request whose candidate
+ * does not check out (two keys sharing a slot, or a table that overflowed) is
+ * answered by a brute-force warp scan of its history, so the result is exact
+ * whatever the hash does.
  *
  * Layout (device memory, caller-owned):
  *   tokens   int32 [N]: the slabs; request r's history is tokens[base[r] ..
@@ -30,8 +31,8 @@
  *   base     int64 [B], len int32 [B], cap int32 [B] (len <= cap; slabs must not
  *            overlap)
  *   index    lookup_index_bytes(slots) bytes, 16-byte aligned (128-byte aligned
- *            for full speed): a 128-byte header then `slots` 16-byte slots
- *            (slots a power of two >= 16) in buckets of 2 slots, one 32-byte
+ *            for full speed): a 128-byte header then `slots` 8-byte slots
+ *            (slots a power of two >= 16) in buckets of 4 slots, one 32-byte
  *            sector each; a key's bucket is read whole in one load round.
  *   The index remembers min_m, max_m, slots and hash_bits from the last build;
  *   a call with other values fails its requests (lookup_index_draft reports
@@ -58,14 +59,15 @@ struct CUstream_st;
  * Returns 0 for invalid arguments. */
 int64_t lookup_index_slots_for(int64_t capacity_tokens, int32_t min_m, int32_t max_m);
 
-/* Bytes of an index with `slots` slots: 128 + 16 * slots (0 if slots is not a
+/* Bytes of an index with `slots` slots: 128 + 8 * slots (0 if slots is not a
  * power of two >= 16). */
 size_t lookup_index_bytes(int64_t slots);
 
 /*
  * Build the index of the current histories: clears the table, then inserts every
- * n-gram (n in [min_m, max_m]) of every history.  The insertions run in
- * parallel, in any order (the slot update keeps the two largest positions).
+ * n-gram (n in [min_m, max_m]) that ends before the last position of its
+ * history.  The insertions run in parallel, in any order (a slot keeps the
+ * largest position).
  * hash_bits in [1, 64] masks the 64-bit keys (64 in normal use; fewer bits make
  * keys share slots, which the exact fallback absorbs -- a test hook).
  * Scratch for the build comes from the library's stream-ordered pool.
@@ -77,11 +79,11 @@ int lookup_index_build(const int32_t *tokens, const int64_t *base, const int32_t
 
 /*
  * Append request r's committed tokens commit[r][0 .. n) (n = ncommit[r] clamped
- * to [0, W]) at tokens[base[r] + len[r]], insert the n-grams that end at the new
- * positions, and add n to len[r].  out_status[r] (may be NULL): 0 = appended,
- * 1 = the slab is full (len + n > cap; nothing appended), 2 = the index was
- * built with other parameters (nothing appended).  O(n * (max_m - min_m + 1))
- * per request.
+ * to [0, W]) at tokens[base[r] + len[r]], insert the n-grams that end at the old
+ * last position and at every new position but the new last, and add n to
+ * len[r].  out_status[r] (may be NULL): 0 = appended, 1 = the slab is full
+ * (len + n > cap; nothing appended), 2 = the index was built with other
+ * parameters (nothing appended).  O(n * (max_m - min_m + 1)) per request.
  */
 int lookup_index_append(int32_t *tokens, const int64_t *base, int32_t *len, const int32_t *cap,
                         const int32_t *commit, const int32_t *ncommit, int32_t B, int32_t W,

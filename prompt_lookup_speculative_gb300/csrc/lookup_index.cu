@@ -5,28 +5,24 @@
 // appends); the result is the exact draft of HyperQwen lookup-drafting article,
 // section "第1步".  The contract is in include/lookup_index.h.
 //
-// Table: a 128-byte header, then `slots` 16-byte slots {key, top1, top2} in
-// buckets of 2 (one 32-byte sector: one DRAM access per probe).  The key of the n-gram ending at q in
-// request r is a 64-bit hash of (r, n, t[q], t[q-1], ..., t[q-n+1]) (0 marks an
-// empty slot); top1 > top2 are the two largest end positions inserted under it.
-// The build claims a slot with a CAS on the key and keeps the top two with two
-// atomicMax: the
-// new position goes into top1, and whichever of it and the displaced top1 is
-// smaller goes into top2.  Every value except the overall maximum reaches top2
-// that way and the maximum never does, so top2 ends as the second largest in
-// any insertion order: the build runs all positions in parallel, and hot keys
-// (periodic text) cost one atomic each rather than CAS retries.  The append,
-// where few threads meet on a slot, updates a slot with one 128-bit CAS of the
-// whole slot instead (fewer dependent round trips); the two kinds of update
-// never run at the same time.
+// Table: a 128-byte header, then `slots` 8-byte slots in buckets of 4 (one
+// 32-byte sector: one DRAM access per probe).  The key of the n-gram ending at q
+// in request r is a 64-bit hash of (r, n, t[q], t[q-1], ..., t[q-n+1]); its home
+// bucket comes from the key's low bits, and its slot holds the key's high half
+// as a fingerprint (low bit set, so a used slot is never 0) above the largest
+// end position inserted under it.  Only positions before each request's last
+// are indexed, so that largest position is the most recent EARLIER occurrence
+// the query asks for.  An insertion claims an empty slot with a 64-bit CAS, and
+// a slot holding its fingerprint takes the position with one 64-bit atomicMax
+// (equal high halves: the maximum keeps the larger position), in any order.
 //
 // Query (one warp per request): lane j probes the key of the suffix's n-gram
-// for n = min_m + j.  The suffix ends at L - 1, the newest position, so its own
-// slot has top1 = L - 1 and top2 = the most recent earlier occurrence.  The
-// candidates are checked against the history; the longest n with a checked
-// candidate is the match.  A slot whose top1 is not L - 1 or whose top2 does
-// not check out has been shared with another key, and the request is answered
-// by a warp brute-force scan instead, so the result never depends on the hash.
+// for n = min_m + j and gets the latest earlier end of that n-gram, if any; the
+// longest n with a position is the match, checked against the history.  Keys
+// that share a fingerprint and a probe sequence merge their positions, so a
+// candidate that does not check out (or a table that overflowed) sends the
+// request to a warp brute-force scan instead: the result never depends on the
+// hash.
 
 #include "lookup_index.h"
 
@@ -35,14 +31,13 @@
 namespace {
 
 using lkd::allow_dependent_launch;
-using lkd::cas128;
 using lkd::launch_pdl;
 using lkd::mix64;
 using lkd::sm_count;
 using lkd::wait_for_prerequisite_grid;
 
-constexpr uint32_t kMagic = 0x4c4b4958u;        // "LKIX"
-constexpr int kBucket = 2;                      // slots per bucket: one 32-byte sector
+constexpr uint32_t kMagic = 0x4c4b4959u;        // "LKIY": 8-byte slots
+constexpr int kBucket = 4;                      // slots per bucket: one 32-byte sector
 constexpr int kMaxProbe = 2048;                 // buckets probed before the overflow flag
 constexpr int kBuildThreads = 256;
 constexpr int kWarpThreads = 128;               // draft kernel: 4 warps per CTA
@@ -58,19 +53,16 @@ struct __align__(16) Header {
 };
 static_assert(sizeof(Header) == 128, "header is 128 bytes: the slots start on a 128-byte line");
 
-struct __align__(16) Slot {
-    unsigned long long key;
-    int top1, top2;
-};
-static_assert(sizeof(Slot) == 16, "slot is 16 bytes");
+using Slot = unsigned long long;                // fingerprint << 32 | latest end position; 0 = empty
 
 __device__ inline uint64_t seed_of(int r) { return mix64(uint64_t(uint32_t(r)) * 0x9e3779b97f4a7c15ull + 0x632be59bd9b4e019ull); }
 __device__ inline uint64_t step_hash(uint64_t h, int32_t tok) { return mix64(h ^ uint64_t(uint32_t(tok))); }
 __device__ inline unsigned long long key_of(uint64_t h, int n, int hash_bits) {
     uint64_t k = mix64(h ^ (uint64_t(n) << 40));
     if (hash_bits < 64) k &= (uint64_t(1) << hash_bits) - 1;
-    return k ? k : 1ull;
+    return k;
 }
+__device__ inline uint32_t fingerprint(unsigned long long key) { return uint32_t(key >> 32) | 1u; }
 
 __device__ inline bool header_ok(const Header *hd, int min_m, int max_m, int hash_bits, int64_t slots) {
     return hd->magic == kMagic && hd->min_m == min_m && hd->max_m == max_m && hd->hash_bits == hash_bits &&
@@ -81,34 +73,34 @@ __device__ inline bool header_ok(const Header *hd, int min_m, int max_m, int has
 // one 32-byte sector, read whole in one round of loads; a full bucket moves on
 // to the next.  Every insertion scans in that same order and slots never empty again,
 // so an empty slot seen during a scan means the key is not stored further on.
-__device__ inline void read_bucket(const Slot *tab, int64_t b, int4 (&v)[kBucket]) {
-    const int4 *p = reinterpret_cast<const int4 *>(tab + b * kBucket);
-#pragma unroll
-    for (int s = 0; s < kBucket; ++s) v[s] = __ldcg(p + s);
+__device__ inline void read_bucket(const Slot *tab, int64_t b, Slot (&v)[kBucket]) {
+    const ulonglong2 *p = reinterpret_cast<const ulonglong2 *>(tab + b * kBucket);
+    const ulonglong2 a = __ldcg(p), c = __ldcg(p + 1);
+    v[0] = a.x;
+    v[1] = a.y;
+    v[2] = c.x;
+    v[3] = c.y;
 }
 
-__device__ inline unsigned long long key_in(int4 v) {
-    return (unsigned long long)(uint32_t(v.x)) | ((unsigned long long)(uint32_t(v.y)) << 32);
-}
-
-// Insert position q under key (the build); false (and the overflow flag) if no
-// slot was found.
+// Insert end position q under key; false (and the overflow flag) if no slot was
+// found.  Any order of insertions leaves each slot at its largest position.
 __device__ inline bool insert(Slot *tab, int64_t bmask, unsigned long long key, int q, Header *hd) {
+    const unsigned long long fp = (unsigned long long)fingerprint(key) << 32;
+    const unsigned long long word = fp | uint32_t(q);
     int64_t b = int64_t(key & uint64_t(bmask));
     for (int probe = 0; probe < kMaxProbe; ++probe) {
-        int4 v[kBucket];
+        Slot v[kBucket];
         read_bucket(tab, b, v);
 #pragma unroll
         for (int s = 0; s < kBucket; ++s) {
             Slot *sl = tab + b * kBucket + s;
-            unsigned long long k = key_in(v[s]);
+            unsigned long long k = v[s];
             if (k == 0ull) {
-                k = atomicCAS(&sl->key, 0ull, key);
-                if (k == 0ull) k = key;                  // claimed
+                k = atomicCAS(sl, 0ull, word);
+                if (k == 0ull) return true;              // claimed with q
             }
-            if (k == key) {
-                const int old1 = atomicMax(&sl->top1, q);
-                atomicMax(&sl->top2, q > old1 ? old1 : q);
+            if ((k & 0xffffffff00000000ull) == fp) {
+                if (uint32_t(k) < uint32_t(q)) atomicMax(sl, word);
                 return true;
             }
         }
@@ -118,80 +110,21 @@ __device__ inline bool insert(Slot *tab, int64_t bmask, unsigned long long key, 
     return false;
 }
 
-// 128-bit compare-and-swap of a whole slot: returns its previous contents.
-__device__ inline void cas_slot(Slot *s, uint64_t cmp_lo, uint64_t cmp_hi, uint64_t new_lo, uint64_t new_hi,
-                                uint64_t &old_lo, uint64_t &old_hi) {
-    cas128(s, cmp_lo, cmp_hi, new_lo, new_hi, old_lo, old_hi);
-}
-
-__device__ inline uint64_t pack_tops(int top1, int top2) { return uint64_t(uint32_t(top1)) | (uint64_t(uint32_t(top2)) << 32); }
-
-// Insert for the append, where few threads meet on a slot: every change of a
-// slot is one 128-bit CAS of {key, top1, top2}.  After the bucket read, a new
-// key is one CAS (claim with tops {q, -1}) and an existing key one CAS from the
-// value read to the updated top two (retried on a lost race; a position already
-// dominated by both tops needs no write).  Only this kernel's insertions touch
-// the table while it runs.
-constexpr int kMaxCasRetries = 256;
-
-__device__ inline bool update_tops(Slot *sl, unsigned long long key, uint64_t hi, int q) {
-    for (int retry = 0; retry < kMaxCasRetries; ++retry) {
-        const int t1 = int(uint32_t(hi)), t2 = int(uint32_t(hi >> 32));
-        if (q == t1 || q <= t2) return true;             // present, or below both tops
-        const uint64_t want = q > t1 ? pack_tops(q, t1) : pack_tops(t1, q);
-        uint64_t lo2, hi2;
-        cas_slot(sl, key, hi, key, want, lo2, hi2);
-        if (hi2 == hi) return true;
-        hi = hi2;                                        // lost a race: retry from the new value
-    }
-    return false;
-}
-
-__device__ inline bool insert_cas(Slot *tab, int64_t bmask, unsigned long long key, int q, Header *hd) {
-    const uint64_t empty_hi = pack_tops(-1, -1);
+// The latest end position stored under key; false when an empty slot or the
+// probe limit is reached first.
+__device__ inline bool find(const Slot *tab, int64_t bmask, unsigned long long key, int &pos) {
+    const unsigned long long fp = (unsigned long long)fingerprint(key) << 32;
     int64_t b = int64_t(key & uint64_t(bmask));
     for (int probe = 0; probe < kMaxProbe; ++probe) {
-        int4 v[kBucket];
+        Slot v[kBucket];
         read_bucket(tab, b, v);
 #pragma unroll
         for (int s = 0; s < kBucket; ++s) {
-            Slot *sl = tab + b * kBucket + s;
-            const unsigned long long k = key_in(v[s]);
-            uint64_t hi = uint64_t(uint32_t(v[s].z)) | (uint64_t(uint32_t(v[s].w)) << 32);
-            if (k == 0ull) {
-                uint64_t lo;
-                cas_slot(sl, 0ull, empty_hi, key, pack_tops(q, -1), lo, hi);
-                if (lo == 0ull) return true;             // claimed (an empty slot is always {0, -1, -1})
-                if (lo != key) continue;                 // taken by another key meanwhile
-            } else if (k != key) {
-                continue;
-            }
-            if (update_tops(sl, key, hi, q)) return true;
-            atomicOr(&hd->overflow, 1u);
-            return false;
-        }
-        b = (b + 1) & bmask;
-    }
-    atomicOr(&hd->overflow, 1u);
-    return false;
-}
-
-// The slot of key (its tops), from whole-bucket reads; false when an empty slot
-// or the probe limit is reached first.
-__device__ inline bool find(const Slot *tab, int64_t bmask, unsigned long long key, int &top1, int &top2) {
-    int64_t b = int64_t(key & uint64_t(bmask));
-    for (int probe = 0; probe < kMaxProbe; ++probe) {
-        int4 v[kBucket];
-        read_bucket(tab, b, v);
-#pragma unroll
-        for (int s = 0; s < kBucket; ++s) {
-            const unsigned long long k = key_in(v[s]);
-            if (k == key) {
-                top1 = v[s].z;
-                top2 = v[s].w;
+            if ((v[s] & 0xffffffff00000000ull) == fp) {
+                pos = int(uint32_t(v[s]));
                 return true;
             }
-            if (k == 0ull) return false;
+            if (v[s] == 0ull) return false;
         }
         b = (b + 1) & bmask;
     }
@@ -234,13 +167,7 @@ __global__ void clear_kernel(BuildParams p) {
     wait_for_prerequisite_grid();
     allow_dependent_launch();
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < p.slots; i += stride) {
-        Slot s;
-        s.key = 0ull;
-        s.top1 = -1;
-        s.top2 = -1;
-        p.tab[i] = s;
-    }
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < p.slots; i += stride) p.tab[i] = 0ull;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         Header h;
         memset(&h, 0, sizeof h);
@@ -289,8 +216,9 @@ __global__ void __launch_bounds__(kScanThreads) prefix_kernel(BuildParams p) {
     if (tid == kScanThreads - 1) p.pref[p.B] = warp_sums[kScanThreads / 32 - 1];
 }
 
-// Every history position, flattened: warp w takes a contiguous range of the
-// virtual positions [0, pref[B]); each lane walks its request forward.
+// Every history position but each request's last, flattened: warp w takes a
+// contiguous range of the virtual positions [0, pref[B]); each lane walks its
+// request forward.
 __global__ void __launch_bounds__(kBuildThreads) build_kernel(BuildParams p) {
     wait_for_prerequisite_grid();
     allow_dependent_launch();
@@ -321,6 +249,7 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(BuildParams p) {
             r_end = p.pref[r + 1];
             base = p.base[r];
         }
+        if (v + 1 == r_end) continue;                    // the last position: not indexed
         insert_position(p.tokens, base, int(v - r_start), r, p.min_m, p.max_m, p.hash_bits, p.tab, mask, p.hd);
     }
 }
@@ -348,13 +277,14 @@ __device__ inline int append_status(const AppendParams &p, bool ok, int r, int &
 }
 
 // Batches that fit in one wave: one CTA per request at a time (grid-stride over
-// requests), the CTA's threads
-// take the request's (new position, length) tasks, writing the new tokens and
-// inserting the n-grams that end at them.  The tokens that end at a new position
-// come from the old history or straight from `commit`, so no insertion waits for
-// a write.  Every thread reads the request's old length first; after a barrier
-// (no thread reads it any more) one thread writes the new length and the status,
-// so the append is one launch.
+// requests), the CTA's threads take the request's (new token j, length) tasks:
+// write token j at position L + j and insert the n-gram that ends one position
+// earlier, at L - 1 + j (the old last position first; the new last position is
+// indexed by the next append).  The tokens of an n-gram come from the old
+// history or straight from `commit`, so no insertion waits for a write.  Every
+// thread reads the request's old length first; after a barrier (no thread reads
+// it any more) one thread writes the new length and the status, so the append
+// is one launch.
 template <int kMaxLen>
 __global__ void __launch_bounds__(kAppendThreads) index_append_request_kernel(AppendParams p) {
     wait_for_prerequisite_grid();
@@ -369,10 +299,10 @@ __global__ void __launch_bounds__(kAppendThreads) index_append_request_kernel(Ap
         const int st = append_status(p, ok, r, L, n, base);
         const int32_t *crow = p.commit + int64_t(r) * p.W;
         for (int64_t t = threadIdx.x; st == 0 && t < per_r; t += blockDim.x) {
-            const int j = int(t / nl), len_n = p.min_m + int(t % nl);   // new position L + j, length len_n
+            const int j = int(t / nl), len_n = p.min_m + int(t % nl);   // new token j, length len_n
             if (j >= n) break;                                   // tasks are ordered by j
             if (len_n == p.min_m) p.tokens[base + L + j] = crow[j];  // one writer per new token
-            const int i = L + j;
+            const int i = L - 1 + j;                             // the n-gram's end: one before the new token
             if (i + 1 < len_n) continue;                         // no n-gram of that length ends here
             // the len_n tokens ending at i, from the old history or from commit, loaded at once
             int32_t v[kMaxLen];
@@ -385,7 +315,7 @@ __global__ void __launch_bounds__(kAppendThreads) index_append_request_kernel(Ap
 #pragma unroll
             for (int k = 0; k < kMaxLen; ++k)
                 if (k < len_n) h = step_hash(h, v[k]);
-            insert_cas(p.tab, mask, key_of(h, len_n, p.hash_bits), int(base + i), p.hd);
+            insert(p.tab, mask, key_of(h, len_n, p.hash_bits), int(base + i), p.hd);
         }
         __syncthreads();                                     // every reader of len[r] is done
         if (threadIdx.x == 0) {
@@ -396,7 +326,7 @@ __global__ void __launch_bounds__(kAppendThreads) index_append_request_kernel(Ap
 }
 
 // Large batches (more requests than one wave of per-request CTAs): the writes
-// and insertions with one thread per (request, new position, length) task,
+// and insertions with one thread per (request, new token, length) task,
 // grid-stride over B * W * (max_m - min_m + 1) tasks, then the lengths in a
 // second kernel.  The tokens that
 // end at a new position come from the old history or straight from `commit`,
@@ -414,13 +344,13 @@ __global__ void __launch_bounds__(kAppendThreads) index_append_dense_kernel(Appe
          task += int64_t(gridDim.x) * kAppendThreads) {
         const int r = int(task / per_r);
         const int rest = int(task - int64_t(r) * per_r);
-        const int j = rest / nl, len_n = p.min_m + rest % nl;   // new position L + j, length len_n
+        const int j = rest / nl, len_n = p.min_m + rest % nl;   // new token j, length len_n
         int L, n;
         int64_t base;
         if (append_status(p, ok, r, L, n, base) != 0 || j >= n) continue;
         const int32_t *crow = p.commit + int64_t(r) * p.W;
         if (len_n == p.min_m) p.tokens[base + L + j] = crow[j];  // one writer per new token
-        const int i = L + j;
+        const int i = L - 1 + j;                             // the n-gram's end: one before the new token
         if (i + 1 < len_n) continue;                         // no n-gram of that length ends here
         // the len_n tokens ending at i, from the old history or from commit, loaded at once
         int32_t v[kMaxLen];
@@ -433,7 +363,7 @@ __global__ void __launch_bounds__(kAppendThreads) index_append_dense_kernel(Appe
 #pragma unroll
         for (int k = 0; k < kMaxLen; ++k)
             if (k < len_n) h = step_hash(h, v[k]);
-        insert_cas(p.tab, mask, key_of(h, len_n, p.hash_bits), int(base + i), p.hd);
+        insert(p.tab, mask, key_of(h, len_n, p.hash_bits), int(base + i), p.hd);
     }
 }
 
@@ -523,16 +453,13 @@ __global__ void __launch_bounds__(kWarpThreads) index_draft_kernel(DraftParams p
                 h = step_hash(h, __shfl_sync(0xffffffffu, tok, k));
                 if (k + 1 == n) key = key_of(h, n, p.hash_bits);
             }
-            // 0 none, 1 candidate, 2 inconsistent (the slot is shared or missing)
+            // 0 none, 1 candidate, 2 inconsistent (a position outside the request:
+            // the slot is shared with another key)
             int state = 0, cand = -1;
             if (lane < nl && n <= L - 1) {
-                int top1 = -1, top2 = -1;
-                if (!find(p.tab, mask, key, top1, top2)) {
-                    state = 2;
-                } else if (int64_t(top1) != base + L - 1) {
-                    state = 2;
-                } else if (top2 >= 0) {
-                    const int64_t c = int64_t(top2) - base;      // relative end position
+                int pos = -1;
+                if (find(p.tab, mask, key, pos)) {
+                    const int64_t c = int64_t(pos) - base;       // relative end position
                     if (c < n - 1 || c > L - 2) state = 2;
                     else { state = 1; cand = int(c); }
                 }

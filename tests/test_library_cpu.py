@@ -167,12 +167,12 @@ def test_loop_steps_empty_batch(lib):
 
 
 def test_index_sizes(lib):
-    # 2 * (12 - 4 + 1) * 1000 = 18000 -> 32768 slots; 128 + 16 * slots bytes
+    # 2 * (12 - 4 + 1) * 1000 = 18000 -> 32768 slots; 128 + 8 * slots bytes
     assert lib.lookup_index_slots_for(1000, 4, 12) == 32768
     assert lib.lookup_index_slots_for(0, 4, 12) == 16
     assert lib.lookup_index_slots_for(1000, 5, 4) == 0
     assert lib.lookup_index_slots_for(1000, 4, 33) == 0
-    assert lib.lookup_index_bytes(32768) == 128 + 16 * 32768
+    assert lib.lookup_index_bytes(32768) == 128 + 8 * 32768
     assert lib.lookup_index_bytes(1000) == 0 and lib.lookup_index_bytes(8) == 0
 
 
