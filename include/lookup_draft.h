@@ -222,6 +222,47 @@ void lookup_draft_set_wait_limit_ns(uint64_t ns);
 int lookup_draft_read_floor(const void *data, size_t bytes, int32_t ctas_per_sm, int32_t threads,
                             uint32_t *out_word, struct CUstream_st *stream);
 
+/*
+ * Checked build (a debugging aid; the source article has no counterpart).  The
+ * drafting step's source also compiles with LOOKUP_DRAFT_CHECKED=1 into a second
+ * library with the same entry points.  There, the scan and fill kernels check
+ * the CSR offsets before they read any token through them, and check every
+ * index they compute.  A failed check sets a bit in a per-device check word and
+ * skips the access: no assert, no trap, no access out of bounds.  That covers
+ * tile, suffix-table, token, scratch-slot, bulk-copy, offsets and output
+ * indices.
+ *
+ * Invalid offsets: offsets[0] < 0, a decreasing pair, or a history of 2^31 tokens
+ * or more.  Every CTA of the scan then returns before its first copy, and every
+ * request of the call reports out_len = LOOKUP_DRAFT_LEN_FAILED, out_pos = -1,
+ * out_draft = -1 (and out_mlen = 0).  An offsets[B] past the end of the tokens
+ * buffer cannot be seen from the device and stays the caller's precondition.
+ * In the regular build no check is compiled.
+ *
+ * The word is one per device, shared by all calls and streams, and it keeps
+ * its bits until cleared.
+ */
+#define LOOKUP_DRAFT_CHECK_OFFSETS 0x01u  /* offsets are not a valid CSR (see above) */
+#define LOOKUP_DRAFT_CHECK_TILE    0x02u  /* a read of a shared-memory tile outside the bytes copied into it */
+#define LOOKUP_DRAFT_CHECK_SUFFIX  0x04u  /* a suffix-table index outside its rows or columns */
+#define LOOKUP_DRAFT_CHECK_TOKENS  0x08u  /* a token read outside the batch or outside its request */
+#define LOOKUP_DRAFT_CHECK_SLOTS   0x10u  /* a scratch-slot index outside the scratch */
+#define LOOKUP_DRAFT_CHECK_COPY    0x20u  /* a bulk copy from outside the batch or into outside its ring buffer */
+#define LOOKUP_DRAFT_CHECK_INDEX   0x40u  /* an offsets index outside [0, B] */
+#define LOOKUP_DRAFT_CHECK_OUTPUT  0x80u  /* an output index outside the B x K outputs */
+
+/* 1 in the checked build, 0 in the regular one. */
+int lookup_draft_checked_build(void);
+
+/*
+ * Reads the check word of the current device into *out (device memory is
+ * synchronised first: the word covers every call whose work has finished) and
+ * clears it when `clear` is non-zero.  In the regular build *out = 0.
+ * Errors: LOOKUP_DRAFT_EINVAL when out is NULL; LOOKUP_DRAFT_ECUDA when the copy
+ * fails.
+ */
+int lookup_draft_check_word(uint32_t *out, int32_t clear);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,15 +29,19 @@ __all__ = [
     "lookup_draft_scan", "lookup_draft_fill", "lookup_draft_noalloc", "workspace_bytes",
     "set_wait_limit_ns", "lookup_fuse", "lookup_schedule", "lookup_verify", "lookup_append",
     "NgramIndex", "index_slots_for", "index_bytes", "lookup_index_build", "lookup_index_append",
-    "lookup_index_draft", "ContextCache",
-    "MAX_M", "MAX_K", "LEN_FAILED",
+    "lookup_index_draft", "ContextCache", "load_checked_library", "check_word",
+    "MAX_M", "MAX_K", "LEN_FAILED", "CHECK_BITS",
 ]
 
 MAX_M = 32
 MAX_K = 64
 LEN_FAILED = -1
+# bits of the checked build's check word (LOOKUP_DRAFT_CHECK_* in include/lookup_draft.h)
+CHECK_BITS = {"offsets": 0x01, "tile": 0x02, "suffix": 0x04, "tokens": 0x08, "slots": 0x10,
+              "copy": 0x20, "index": 0x40, "output": 0x80}
 
 _lib = None
+_checked_lib = None
 _lib_lock = threading.Lock()
 
 
@@ -73,7 +77,38 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         return lib
 
 
+def load_checked_library() -> ctypes.CDLL:
+    """The checked build of the drafting step (include/lookup_draft.h, "Checked
+    build"): the entry points of lookup_draft.h with device-side index checks.
+    It is built beside the regular library; a debugging aid, not the product path."""
+    global _checked_lib
+    load_library()                       # builds both libraries when stale
+    with _lib_lock:
+        if _checked_lib is None:
+            path = _build.CHECKED_LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(f"the checked CUDA library {path} is missing; run build() first")
+            lib = ctypes.CDLL(path)
+            _declare_draft(lib)
+            _checked_lib = lib
+        return _checked_lib
+
+
+def check_word(lib: ctypes.CDLL, clear: bool = False) -> int:
+    """The current device's check word of `lib` (0 in the regular build); device
+    memory is synchronised first.  clear=True clears it after reading."""
+    out = ctypes.c_uint32(0)
+    _check(lib.lookup_draft_check_word(ctypes.byref(out), 1 if clear else 0), lib)
+    return int(out.value)
+
+
 def _declare(lib: ctypes.CDLL) -> None:
+    _declare_draft(lib)
+    _declare_loop(lib)
+
+
+def _declare_draft(lib: ctypes.CDLL) -> None:
+    """Argument types of the entry points in include/lookup_draft.h."""
     vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
     lib.lookup_draft.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
     lib.lookup_draft.restype = ctypes.c_int
@@ -97,6 +132,16 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.lookup_draft_set_wait_limit_ns.restype = None
     lib.lookup_draft_read_floor.argtypes = [vp, sz, i32, i32, vp, vp]
     lib.lookup_draft_read_floor.restype = ctypes.c_int
+    lib.lookup_draft_checked_build.argtypes = []
+    lib.lookup_draft_checked_build.restype = ctypes.c_int
+    lib.lookup_draft_check_word.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+    lib.lookup_draft_check_word.restype = ctypes.c_int
+
+
+def _declare_loop(lib: ctypes.CDLL) -> None:
+    """Argument types of the entry points in include/lookup_loop.h,
+    include/lookup_index.h and include/lookup_ctxcache.h."""
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
     lib.lookup_fuse.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp]
     lib.lookup_fuse.restype = ctypes.c_int
     lib.lookup_schedule.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp]

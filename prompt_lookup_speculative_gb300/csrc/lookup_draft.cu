@@ -89,6 +89,25 @@ constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 
 static_assert(4 * kHaloQuads >= LOOKUP_DRAFT_MAX_M - 1, "halo too small for LOOKUP_DRAFT_MAX_M");
 
+// ---------------------------------------------------------- checked build ----
+// Compiled with LOOKUP_DRAFT_CHECKED=1, every index the kernels compute is checked
+// before use: a failed check sets its LOOKUP_DRAFT_CHECK_* bit in the device's
+// check word and the access is skipped.  In the regular build LKD_OK(cond, bit)
+// is the constant true and no check is compiled.
+#ifndef LOOKUP_DRAFT_CHECKED
+#define LOOKUP_DRAFT_CHECKED 0
+#endif
+#if LOOKUP_DRAFT_CHECKED
+__device__ unsigned g_check_word;
+__device__ __forceinline__ bool check_ok(bool ok, unsigned bit) {
+    if (!ok) atomicOr(&g_check_word, bit);
+    return ok;
+}
+#define LKD_OK(cond, bit) check_ok((cond), (bit))
+#else
+#define LKD_OK(cond, bit) true
+#endif
+
 constexpr size_t kBufBytes = size_t(kTileQuadsMax + kHaloQuads) * 16;
 
 struct ScanParams {
@@ -102,6 +121,9 @@ struct ScanParams {
     uint32_t grid_magic;   // floor(n / grid) = umulhi(n, grid_magic) >> grid_shift for n < 2^31
     int32_t grid_shift;    // -1: grid == 1
     uint64_t wait_ns;
+#if LOOKUP_DRAFT_CHECKED
+    int64_t nslots;        // slots in the scratch
+#endif
 };
 
 struct FillParams {
@@ -115,6 +137,9 @@ struct FillParams {
     int32_t B;
     int32_t K;
     int32_t grid;
+#if LOOKUP_DRAFT_CHECKED
+    int64_t nslots;        // slots in the scratch
+#endif
 };
 
 // ------------------------------------------------------ partition helpers ----
@@ -381,6 +406,26 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
         fence_barrier_init();
     }
     wait_for_prerequisite_grid();
+#if LOOKUP_DRAFT_CHECKED
+    // The CSR offsets, before anything reads tokens through them: offsets[0] >= 0,
+    // non-decreasing, every history shorter than 2^31 tokens.  Otherwise the CTA
+    // returns before its first copy (the fill then fails every request).
+    {
+        bool bad = false;
+        for (int i = tid; i <= B; i += kThreads) {
+            const int64_t a = prm.offsets[i];
+            bad |= i == 0 && a < 0;
+            if (i < B) {
+                const int64_t b = prm.offsets[i + 1];
+                bad |= b < a || b - a >= (int64_t(1) << 31);
+            }
+        }
+        if (__syncthreads_or(bad)) {
+            if (tid == 0) atomicOr(&g_check_word, LOOKUP_DRAFT_CHECK_OFFSETS);
+            return;
+        }
+    }
+#endif
 
     // 1. Offsets -> shared memory: one bulk copy of the 16-byte span covering them,
     //    for the request searches.  Should the copy not land in time, the CTA reads
@@ -447,8 +492,14 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
         const uint32_t bytes = uint32_t(t1 - ls) * 16u;
         unsigned char *buf = my_bufs + size_t(slot) * kBufBytes;
         const uint32_t bar = smem_addr(&my_bars[slot]);
+        const int dq = kHaloQuads - (t0 - ls);           // first quad written in the buffer
+        if (!LKD_OK(wq0 + ls >= 0 && wq0 + t1 <= P.nq && dq >= 0 && dq + (t1 - ls) <= kHaloQuads + kTileQuadsMax,
+                    LOOKUP_DRAFT_CHECK_COPY)) {
+            mbar_expect_tx(bar, 0u);                     // the phase completes with nothing copied
+            return;
+        }
         mbar_expect_tx(bar, bytes);
-        bulk_copy_g2s_stream(smem_addr(buf + (kHaloQuads - (t0 - ls)) * 16), wsrc + ls * 4, bytes, bar);
+        bulk_copy_g2s_stream(smem_addr(buf + dq * 16), wsrc + ls * 4, bytes, bar);
     };
     if (wn > 0 && lane == 0) issue_tile(0, 0);
 
@@ -459,6 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
     const bool offs_smem = offs_in_smem && !__syncthreads_or(!ok);
     const bool offs_pending = offs_in_smem && !offs_smem;
     auto off_a = [&](int i) -> int64_t {
+        if (!LKD_OK(i >= 0 && i <= B, LOOKUP_DRAFT_CHECK_INDEX)) i = 0;
         if (OFFS_SMEM && offs_smem) return offs_s[i] + shift;
         return __ldg(prm.offsets + i) + shift;
     };
@@ -495,7 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
 #pragma unroll
         for (int row = 0; row < kSufRows; ++row) {
             const int64_t src = bound[row + 1] - 1 - lane;
-            const bool ld = rw_lo + row < B && lane < max_m && src >= bound[row];
+            const bool ld = rw_lo + row < B && lane < max_m && src >= bound[row] &&
+                            LKD_OK(src >= a_begin && src < a_end, LOOKUP_DRAFT_CHECK_TOKENS);
             sreg[row] = ld ? __ldg(ta + src) : 0;
         }
         if (lane == 0) {
@@ -507,16 +560,24 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
 #pragma unroll
         for (int row = 0; row < kSufRows; ++row)
             if (row < nrows && lane < max_m) suf_w[row * max_m + lane] = sreg[row];
+        // The slot of request r exists (checked build; the staircase keeps r + v below
+        // B + the number of warp ranges).
+        auto slot_ok = [&](int r) -> bool {
+            return LKD_OK(r >= 0 && v + r < prm.nslots, LOOKUP_DRAFT_CHECK_SLOTS);
+        };
         // this warp's slots: cleared before the warp writes its results into them
         for (int r = rw_lo + lane; r <= rw_hi; r += 32)
-            if (off_a(r + 1) > off_a(r)) slots[r] = 0ull;
+            if (off_a(r + 1) > off_a(r) && slot_ok(r)) slots[r] = 0ull;
         __syncwarp();
 
         // Suffix token j of request r (t[L-1-j]); 0 past the start of the history.
         auto suffix = [&](int r, int64_t o, int64_t n, int j) -> int32_t {
             const int row = r - rw_lo;
+            if (!LKD_OK(row >= 0 && j >= 0 && j < max_m, LOOKUP_DRAFT_CHECK_SUFFIX)) return 0;
             if (row < kSufRows) return suf_w[row * max_m + j];
-            return (n - 1 - j >= o) ? __ldg(ta + n - 1 - j) : 0;
+            return (n - 1 - j >= o && LKD_OK(n - 1 - j >= a_begin && n - 1 - j < a_end, LOOKUP_DRAFT_CHECK_TOKENS))
+                       ? __ldg(ta + n - 1 - j)
+                       : 0;
         };
 
         // 5. Stream the tiles.  The warp's current request (uniform across it) and
@@ -531,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
         // value returned, so nothing waits for it): the slot was zeroed above and
         // only this warp's lanes write it.
         auto flush = [&]() {
-            if (best != 0ull) atomicMax(&slots[cur_r], best);
+            if (best != 0ull && slot_ok(cur_r)) atomicMax(&slots[cur_r], best);
             best = 0ull;
         };
         auto set_request = [&](int r) {                  // warp-uniform, r in [rw_lo, rw_hi]
@@ -564,6 +625,20 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
             const int base = 4 * t0;                     // relative position of st[0]
             const int eb = base > wbeg ? base : wbeg;
             const int ee = (base + 4 * nq < wend) ? base + 4 * nq : wend;
+#if LOOKUP_DRAFT_CHECKED
+            const int qv = ((t0 - halo > -lead) ? t0 - halo : -lead) - t0;   // quads [qv, nq) were copied
+#endif
+            // Checked build: the tokens that the tests of candidate ends [lo, hi] depend
+            // on (lo - D + 1 .. hi; the loops also load the rest of the quad before
+            // lo's, whose masked values never count) lie in the tile's copied bytes;
+            // a match ending at element e can be extended up to kmax tokens in them.
+            auto tile_ok = [&](int lo, int hi) -> bool {
+                return LKD_OK(((lo - (D - 1)) >> 2) >= qv && (hi >> 2) < nq, LOOKUP_DRAFT_CHECK_TILE);
+            };
+            auto elem_ok = [&](int e, int kmax) -> bool {
+                return LKD_OK(kmax <= max_m, LOOKUP_DRAFT_CHECK_SUFFIX) &&
+                       LKD_OK(e < 4 * nq && e - (kmax - 1) >= 4 * qv, LOOKUP_DRAFT_CHECK_TILE);
+            };
 
             // Candidate ends [lo, hi] (tile elements, whole quads: lo and hi + 1 are
             // multiples of 4) of the current request: the D-token test on every quad.
@@ -575,6 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                     const int q = qoff + e;              // local end position in the request
                     const int kmax = max_m < q + 1 ? max_m : q + 1;
                     const int row = cur_r - rw_lo;
+                    if (!elem_ok(e, kmax)) return;
                     int kk = k0;
                     if (row < kSufRows)
                         kk = match_len(st, e, suf_w + row * max_m, k0, kmax);
@@ -596,6 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                 };
                 const int jq0 = (lo + 3) >> 2;           // first quad fully inside
                 const int jq1 = ((hi + 1) >> 2) - 1;     // last quad fully inside
+                if (jq0 <= jq1 && !tile_ok(4 * jq0, 4 * jq1 + 3)) return;
                 // two quads per lane per iteration: independent loads and tests; the
                 // previous quad (the halo when j == 0) supplies the tokens before each
                 int j = jq0 + lane;
@@ -630,11 +707,16 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                 auto extend = [&](int e) {               // the D tokens ending at e match
                     const int q = qoff + e;
                     const int kmax = max_m < q + 1 ? max_m : q + 1;
+                    if (!elem_ok(e, kmax)) return;
                     int kk = D;
                     if (suf)
                         kk = match_len(st, e, suf, D, kmax);
                     else
-                        while (kk < kmax && st[e - kk] == __ldg(hist_last - kk)) ++kk;
+                        while (kk < kmax &&
+                               LKD_OK(cur_nxt - 1 - kk >= cur_o && WA + cur_nxt - 1 - kk < a_end,
+                                      LOOKUP_DRAFT_CHECK_TOKENS) &&
+                               st[e - kk] == __ldg(hist_last - kk))
+                            ++kk;
                     if (kk >= min_m) {
                         const unsigned long long key =
                             (static_cast<unsigned long long>(kk) << 32) | static_cast<uint32_t>(q - kk + 1);
@@ -642,6 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                     }
                 };
                 const int ja = lo >> 2, jb = hi >> 2;
+                if (lo <= hi && !tile_ok(lo, hi)) return;
                 const unsigned head = (0xFu << (lo & 3)) & 0xFu;   // elements >= lo in quad ja
                 const unsigned tail = 0xFu >> (3 - (hi & 3));      // elements <= hi in quad jb
                 for (int j = ja + lane; j <= jb; j += 64) {
@@ -705,6 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                         const int q = base + e - (inB ? oB : oA);      // local end position
                         const int kmax = max_m < q + 1 ? max_m : q + 1;
                         const int64_t o_abs = WA + (inB ? oB : oA), n_abs = WA + (inB ? nB : nA);
+                        if (!elem_ok(e, kmax)) return;
                         int kk = D;
                         if (r - rw_lo < kSufRows)
                             kk = match_len(st, e, suf_w + (r - rw_lo) * max_m, D, kmax);
@@ -723,6 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                     // rare hits are masked to that request's range
                     const bool hasA = loA <= hiA, hasB = loB <= hiB;
                     const int jlo = (hasA ? loA : loB) >> 2, jhi = (hasB ? hiB : hiA) >> 2;
+                    const bool pass_ok = (!hasA && !hasB) || tile_ok(hasA ? loA : loB, hasB ? hiB : hiA);
                     // a quad is B's when it reaches B's first candidate (the gap before it
                     // is at least 3 elements), else A's; the range masks apply on the rare
                     // path only, so a gap or edge quad costs nothing extra
@@ -737,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                             extend2(4 * j + e, inB);
                         }
                     };
-                    for (int j = jlo + lane; j <= jhi; j += 64) {
+                    for (int j = jlo + lane; pass_ok && j <= jhi; j += 64) {
                         const int j2 = j + 32;
                         const bool has2 = j2 <= jhi;
                         const int jj2 = has2 ? j2 : j;
@@ -753,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
                         }
                     }
                     // A ends here; B continues into the next tile with its keys pending
-                    if (bestA != 0ull) atomicMax(&slots[rA], bestA);
+                    if (bestA != 0ull && slot_ok(rA)) atomicMax(&slots[rA], bestA);
                     cur_r = rB;
                     cur_o = oB;
                     cur_nxt = nB;
@@ -795,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
             }
             __syncwarp();
             for (int r = rw_lo + lane; r <= rw_hi; r += 32)
-                if (off_a(r + 1) > off_a(r)) slots[r] = kKeyFailed;
+                if (off_a(r + 1) > off_a(r) && slot_ok(r)) slots[r] = kKeyFailed;
         }
     }
     if (offs_pending && tid == 0) (void)mbar_wait_until(smem_addr(offs_bar), 0, global_ns() + kDefaultWaitNs);
@@ -809,6 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
 // its own draft.  Lanes first, first + step, ... of the row are written here.
 __device__ inline void write_draft(const FillParams &prm, int r, int64_t o0, int64_t L, unsigned long long key,
                                    int first, int step, bool head) {
+    if (!LKD_OK(r >= 0 && r < prm.B, LOOKUP_DRAFT_CHECK_OUTPUT)) return;
     const int64_t km = int64_t(key >> 32), kp = int64_t(uint32_t(key));
     const bool failed = key != 0ull && (key == kKeyFailed || km < 1 || kp + km > L - 1);
     const bool found = key != 0ull && !failed;
@@ -818,7 +904,10 @@ __device__ inline void write_draft(const FillParams &prm, int r, int64_t o0, int
     const int K = prm.K;
     int32_t *row = prm.out_draft + int64_t(r) * K;
     const int32_t *src = prm.tokens + o0 + p + m;
-    for (int j = first; j < K; j += step) row[j] = found ? __ldg(src + (j < d ? j : j % d)) : -1;
+    for (int j = first; j < K; j += step)
+        row[j] = found && LKD_OK(p + m + (j < d ? j : j % d) < L, LOOKUP_DRAFT_CHECK_TOKENS)
+                     ? __ldg(src + (j < d ? j : j % d))
+                     : -1;
     if (head) {
         prm.out_len[r] = found ? K : (failed ? LOOKUP_DRAFT_LEN_FAILED : 0);
         prm.out_pos[r] = int32_t(p);
@@ -826,15 +915,51 @@ __device__ inline void write_draft(const FillParams &prm, int r, int64_t o0, int
     }
 }
 
+#if LOOKUP_DRAFT_CHECKED
+// Checked build: whether the offsets are not a valid CSR (offsets[0] < 0, a
+// decreasing pair, a history of 2^31 tokens or more).  Every thread of the CTA
+// takes part; the answer is the CTA's.
+__device__ bool offsets_invalid(const int64_t *offsets, int B) {
+    bool bad = false;
+    for (int i = threadIdx.x; i <= B; i += blockDim.x) {
+        const int64_t a = offsets[i];
+        bad |= i == 0 && a < 0;
+        if (i < B) {
+            const int64_t b = offsets[i + 1];
+            bad |= b < a || b - a >= (int64_t(1) << 31);
+        }
+    }
+    bad = __syncthreads_or(bad) != 0;
+    if (bad && threadIdx.x == 0) atomicOr(&g_check_word, LOOKUP_DRAFT_CHECK_OFFSETS);
+    return bad;
+}
+
+// The outputs of request r when the batch's offsets are invalid.
+__device__ void write_failed(const FillParams &prm, int r, int first, int step, bool head) {
+    int32_t *row = prm.out_draft + int64_t(r) * prm.K;
+    for (int j = first; j < prm.K; j += step) row[j] = -1;
+    if (head) {
+        prm.out_len[r] = LOOKUP_DRAFT_LEN_FAILED;
+        prm.out_pos[r] = -1;
+        if (prm.out_mlen) prm.out_mlen[r] = 0;
+    }
+}
+#endif
+
 // One warp per request, for small batches: the request's slots lie in the scan
 // warps v0 .. v1 holding its first and last quads, and the lanes load them in
 // parallel.
 __global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_kernel(FillParams prm) {
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * kFillWarps + (threadIdx.x >> 5);
+#if LOOKUP_DRAFT_CHECKED
+    const bool csr_bad = offsets_invalid(prm.offsets, prm.B);
+#else
+    constexpr bool csr_bad = false;
+#endif
     // Inputs the scan does not write: read them before waiting for it.
     int64_t o0 = 0, o1 = 0, first = 0, end = 0;
-    if (r < prm.B) {
+    if (r < prm.B && !csr_bad) {
         o0 = __ldg(prm.offsets + r);
         o1 = __ldg(prm.offsets + r + 1);
         first = __ldg(prm.offsets);
@@ -859,11 +984,17 @@ __global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_kernel(F
         const int64_t v = v0 + lane + u * 32;
         int64_t lo = 0, hi = 0;
         if (v <= v1) vchunk_range(P, v, lo, hi);
-        take[u] = v <= v1 && lo < hi;
+        take[u] = v <= v1 && lo < hi && LKD_OK(int64_t(r) + v < prm.nslots, LOOKUP_DRAFT_CHECK_SLOTS);
     }
     allow_dependent_launch();
     wait_for_prerequisite_grid();
     if (r >= prm.B) return;
+#if LOOKUP_DRAFT_CHECKED
+    if (csr_bad) {
+        write_failed(prm, r, lane, 32, lane == 0);
+        return;
+    }
+#endif
 
     unsigned long long key = 0ull;
     if (L > 0) {
@@ -880,7 +1011,9 @@ __global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_kernel(F
                 const int64_t v = vb + u * 32;
                 int64_t lo, hi;
                 vchunk_range(P, v, lo, hi);
-                x[u] = (v <= v1 && lo < hi) ? prm.slots[int64_t(r) + v] : 0ull;
+                x[u] = (v <= v1 && lo < hi && LKD_OK(int64_t(r) + v < prm.nslots, LOOKUP_DRAFT_CHECK_SLOTS))
+                           ? prm.slots[int64_t(r) + v]
+                           : 0ull;
             }
 #pragma unroll
             for (int u = 0; u < kFillUnroll; ++u) key = x[u] > key ? x[u] : key;
@@ -901,9 +1034,14 @@ __global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_kernel(F
 __global__ void __launch_bounds__(kLaneFillThreads) fill_lanes_kernel(FillParams prm) {
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * kLaneFillThreads + threadIdx.x;
+#if LOOKUP_DRAFT_CHECKED
+    const bool csr_bad = offsets_invalid(prm.offsets, prm.B);
+#else
+    constexpr bool csr_bad = false;
+#endif
     const bool live = r < prm.B;
     int64_t o0 = 0, o1 = 0;
-    if (live) {
+    if (live && !csr_bad) {
         o0 = __ldg(prm.offsets + r);
         o1 = __ldg(prm.offsets + r + 1);
     }
@@ -915,7 +1053,7 @@ __global__ void __launch_bounds__(kLaneFillThreads) fill_lanes_kernel(FillParams
     // offsets alone: worked out before the wait.
     const Partition P = make_partition(first + shift, end + shift, prm.grid);
     int64_t v0 = 0, v1 = -1;                             // no slots: empty request or no request
-    if (L > 0) {
+    if (L > 0 && !csr_bad) {
         v0 = vchunk_of_quad(P, ((o0 + shift) >> 2) - P.q_lo);
         v1 = vchunk_of_quad(P, ((o1 - 1 + shift) >> 2) - P.q_lo);
     }
@@ -926,10 +1064,16 @@ __global__ void __launch_bounds__(kLaneFillThreads) fill_lanes_kernel(FillParams
         const int64_t v = v0 + u;
         int64_t lo = 0, hi = 0;
         if (own && v <= v1) vchunk_range(P, v, lo, hi);
-        take[u] = own && v <= v1 && lo < hi;
+        take[u] = own && v <= v1 && lo < hi && LKD_OK(int64_t(r) + v < prm.nslots, LOOKUP_DRAFT_CHECK_SLOTS);
     }
     allow_dependent_launch();
     wait_for_prerequisite_grid();
+#if LOOKUP_DRAFT_CHECKED
+    if (csr_bad) {
+        if (live) write_failed(prm, r, 0, 1, true);
+        return;
+    }
+#endif
     if (__all_sync(0xffffffffu, !live)) return;          // warp-uniform
 
     unsigned long long key = 0ull;
@@ -949,7 +1093,9 @@ __global__ void __launch_bounds__(kLaneFillThreads) fill_lanes_kernel(FillParams
         for (int64_t v = a + lane; v <= b; v += 32) {
             int64_t lo, hi;
             vchunk_range(P, v, lo, hi);
-            const unsigned long long x = lo < hi ? prm.slots[int64_t(rs) + v] : 0ull;
+            const unsigned long long x =
+                (lo < hi && LKD_OK(int64_t(rs) + v < prm.nslots, LOOKUP_DRAFT_CHECK_SLOTS)) ? prm.slots[int64_t(rs) + v]
+                                                                                           : 0ull;
             kw = x > kw ? x : kw;
         }
 #pragma unroll
@@ -1147,6 +1293,9 @@ int launch_scan(const DeviceState &st, const int32_t *tokens, const int64_t *off
     prm.grid = grid_for(st);
     grid_divider(prm.grid, prm.grid_magic, prm.grid_shift);
     prm.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+#if LOOKUP_DRAFT_CHECKED
+    prm.nslots = int64_t(B) + int64_t(prm.grid) * kWarps;
+#endif
     const ScanSmemLayout lay = scan_smem_layout(B, max_m);
     const bool offs_smem = int64_t(B) + 1 <= kOffCap;
     void (*kernel)(ScanParams) = nullptr;
@@ -1177,6 +1326,9 @@ int launch_fill(const DeviceState &st, const int32_t *tokens, const int64_t *off
     prm.B = B;
     prm.K = K;
     prm.grid = grid_for(st);
+#if LOOKUP_DRAFT_CHECKED
+    prm.nslots = int64_t(B) + int64_t(prm.grid) * kWarps;
+#endif
     if (B >= kLaneFillMinB)
         return launch_pdl(fill_lanes_kernel, unsigned((int64_t(B) + kLaneFillThreads - 1) / kLaneFillThreads),
                           unsigned(kLaneFillThreads), stream, prm);
@@ -1453,5 +1605,26 @@ const char *lookup_draft_strerror(int code) {
 const char *lookup_draft_last_cuda_error(void) { return g_cuda_msg; }
 
 void lookup_draft_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns ? ns : kDefaultWaitNs); }
+
+int lookup_draft_checked_build(void) { return LOOKUP_DRAFT_CHECKED ? 1 : 0; }
+
+int lookup_draft_check_word(uint32_t *out, int32_t clear) {
+    g_cuda_msg[0] = '\0';
+    if (!out) return LOOKUP_DRAFT_EINVAL;
+#if LOOKUP_DRAFT_CHECKED
+    LD_CUDA(cudaDeviceSynchronize());
+    unsigned w = 0;
+    LD_CUDA(cudaMemcpyFromSymbol(&w, g_check_word, sizeof w));
+    if (clear) {
+        const unsigned zero = 0;
+        LD_CUDA(cudaMemcpyToSymbol(g_check_word, &zero, sizeof zero));
+    }
+    *out = w;
+#else
+    (void)clear;
+    *out = 0;
+#endif
+    return LOOKUP_DRAFT_OK;
+}
 
 }  // extern "C"

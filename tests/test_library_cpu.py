@@ -213,3 +213,45 @@ def test_ctx_sizes_and_argument_checks(lib):
     assert lib.lookup_ctx_draft(None, None, None, 0, 1, 4, 8, *args, den.ctypes.data, None, 1024, None, None,
                                 None) == 0
     assert lib.lookup_ctx_append(F, F, F, F, F, F, 4, -1, 1, 4, F, 1024, None, None) == -1
+
+
+# ------------------------------------------------------------ checked build ----
+def declared_in(header: str) -> set[str]:
+    text = open(os.path.join(ROOT, "include", header), encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return {m.group(1) for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(lookup_\w*)\s*\(", text, flags=re.M)}
+
+
+@pytest.fixture(scope="module")
+def checked_lib():
+    lib_build.build()
+    return pkg.load_checked_library()
+
+
+def test_checked_library_exports_the_drafting_entry_points(checked_lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_build.CHECKED_LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    names = declared_in("lookup_draft.h")
+    assert {"lookup_draft", "lookup_draft_check_word", "lookup_draft_checked_build"} <= names
+    for name in names:
+        assert name in exported, f"{name} missing from the checked library"
+
+
+def test_checked_build_flag_and_word_without_a_gpu(lib, checked_lib):
+    import ctypes
+    assert lib.lookup_draft_checked_build() == 0
+    assert checked_lib.lookup_draft_checked_build() == 1
+    out = ctypes.c_uint32(99)
+    assert lib.lookup_draft_check_word(ctypes.byref(out), 1) == 0 and out.value == 0   # no device call
+    assert lib.lookup_draft_check_word(None, 0) == -1
+    assert checked_lib.lookup_draft_check_word(None, 0) == -1
+    # the checked library validates its arguments like the regular one
+    assert checked_lib.lookup_draft(FAKE, FAKE, 4, 5, 4, 15, FAKE, FAKE, FAKE, None) == -1
+    assert checked_lib.lookup_draft(None, None, 0, 4, 12, 15, None, None, None, None) == 0
+
+
+def test_checked_build_command():
+    cmd = lib_build.compile_command("x.so", checked=True)
+    assert "-DLOOKUP_DRAFT_CHECKED=1" in cmd and "arch=compute_103a,code=sm_103a" in cmd
+    assert "-DLOOKUP_DRAFT_CHECKED=1" not in lib_build.compile_command("x.so")
