@@ -73,9 +73,20 @@ struct CUstream_st;                     /* same type as cudaStream_t */
  * out_pos    device, int32 [B]: start p of the occurrence in the request, or -1
  * stream     CUDA stream all work is enqueued on
  *
- * Scratch: B + 16 * (number of scan CTAs, one per SM) 64-bit words, taken from
- * and returned to a library-owned, stream-ordered CUDA memory pool of the
- * current device.
+ * Scratch: B + 16 * (number of scan CTAs, one per SM) 64-bit words, kept per
+ * stream.  The first call on a stream, outside stream capture, allocates them
+ * (cudaMalloc, rounded up to 64 KiB) and later calls on that stream reuse them,
+ * so a run of calls has no allocation between its kernels.  A call with a larger
+ * batch makes a buffer twice as large or more.  The library frees none of these
+ * buffers before the process exits: a CUDA graph captured earlier may still use
+ * an old one.  A call inside stream capture on a stream whose buffer is missing
+ * or too small takes its scratch from a library-owned, stream-ordered memory
+ * pool instead (memory nodes in the graph).
+ * A graph captured from calls on a stream uses that stream's buffer, as it uses
+ * its fixed output buffers: replays of it must not overlap in time with other
+ * calls on that stream.
+ * Set-up: the first call on a device sets up per-device state.  Make it outside
+ * stream capture.
  * Errors: LOOKUP_DRAFT_EINVAL for null pointers (with B > 0), bad m range, K out of
  * range, or misaligned tokens/offsets; LOOKUP_DRAFT_ECUDA when an allocation or
  * launch fails.

@@ -1145,6 +1145,12 @@ __global__ void __launch_bounds__(kCopyThreads) host_copy_kernel(CopyParams prm)
 }
 
 // ------------------------------------------------------------- host side ----
+}  // namespace
+
+#include <unordered_map>                       // per-stream scratch (host code only)
+
+namespace {
+
 thread_local char g_cuda_msg[256] = "";
 
 int cuda_fail(cudaError_t e, const char *what) {
@@ -1343,14 +1349,67 @@ int launch_host_copy(const DeviceState &st, const CopyParams &cp, cudaStream_t s
                       stream, cp);
 }
 
+// Scratch kept per stream.  A call takes the result slots from its stream's
+// buffer, so consecutive calls in a CUDA graph have no memory nodes between them
+// and the next call's scan launches early behind the previous fill (a pool
+// allocation and free per call, captured as memory nodes, cost ~0.4 us per step).
+// Buffers are keyed by the stream handle and made outside stream capture only
+// (a hit makes no CUDA call; the capture check is legal during capture, a stream
+// id query is not).  They grow geometrically and are never freed before exit: a
+// captured graph may still refer to a buffer that a larger batch later replaced.
+// Calls on one stream are ordered, so they never overlap on its buffer.
+struct StreamScratch {
+    unsigned long long *slots = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_scratch_mu;
+std::unordered_map<uintptr_t, StreamScratch> g_scratch[kMaxDevices];
+
+// The scratch of `stream` on device `dev`, holding at least `need` bytes; nullptr
+// (no error) when it has none and cannot make one now: the stream is capturing.
+int stream_scratch(int dev, cudaStream_t stream, size_t need, unsigned long long **out) {
+    *out = nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    StreamScratch &sc = g_scratch[dev][reinterpret_cast<uintptr_t>(stream)];
+    if (sc.bytes >= need) {
+        *out = sc.slots;
+        return LOOKUP_DRAFT_OK;
+    }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    LD_CUDA(cudaStreamIsCapturing(stream, &cs));
+    if (cs != cudaStreamCaptureStatusNone) return LOOKUP_DRAFT_OK;
+    size_t bytes = sc.bytes * 2 > need ? sc.bytes * 2 : need;
+    bytes = (bytes + 65535) & ~size_t(65535);
+    void *p = nullptr;
+    LD_CUDA(cudaMalloc(&p, bytes));                     // valid on every stream at once
+    sc.slots = static_cast<unsigned long long *>(p);    // the old buffer, if any, stays allocated
+    sc.bytes = bytes;
+    *out = sc.slots;
+    return LOOKUP_DRAFT_OK;
+}
+
 int run_step(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t min_m, int32_t max_m, int32_t K,
              int32_t *out_draft, int32_t *out_len, int32_t *out_pos, int32_t *out_mlen, cudaStream_t stream) {
     DeviceState *st = nullptr;
     int rc = device_state(&st);
     if (rc != LOOKUP_DRAFT_OK) return rc;
+    int dev = 0;
+    LD_CUDA(cudaGetDevice(&dev));
+    const size_t need = workspace_bytes_for(B, grid_for(*st));
+    unsigned long long *slots = nullptr;
+    rc = stream_scratch(dev, stream, need, &slots);
+    if (rc != LOOKUP_DRAFT_OK) return rc;
+    if (slots) {
+        rc = launch_scan(*st, tokens, offsets, B, min_m, max_m, slots, stream);
+        if (rc == LOOKUP_DRAFT_OK)
+            rc = launch_fill(*st, tokens, offsets, B, K, slots, out_draft, out_len, out_pos, out_mlen, stream);
+        return rc;
+    }
+    // No stream scratch (a capture on a stream without one): stream-ordered scratch
+    // from the library pool for this call.
     void *ws = nullptr;
-    LD_CUDA(cudaMallocFromPoolAsync(&ws, workspace_bytes_for(B, grid_for(*st)), st->pool, stream));
-    auto *slots = static_cast<unsigned long long *>(ws);
+    LD_CUDA(cudaMallocFromPoolAsync(&ws, need, st->pool, stream));
+    slots = static_cast<unsigned long long *>(ws);
     rc = launch_scan(*st, tokens, offsets, B, min_m, max_m, slots, stream);
     if (rc == LOOKUP_DRAFT_OK)
         rc = launch_fill(*st, tokens, offsets, B, K, slots, out_draft, out_len, out_pos, out_mlen, stream);

@@ -1,0 +1,160 @@
+"""lookup_draft's per-stream scratch, against the oracle.
+
+lookup_draft keeps the scan's result slots in one buffer per stream, made on the
+first call outside stream capture and grown when a larger batch comes. Inside a
+capture on a stream without a big-enough buffer, a call takes its scratch from
+the library pool (graph memory nodes) instead.
+
+Checked here:
+- interleaved calls on two streams with different batches;
+- a batch larger than the stream's buffer, then smaller ones again;
+- a graph captured on a fresh stream (the pool path), and one captured after an
+  eager call (the stream's buffer), each replayed several times;
+- a graph replayed after a later, larger call replaced its stream's buffer (the
+  old buffer stays allocated).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import gen
+import oracle
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU machines too
+    pytestmark = [pytest.mark.gpu, pytest.mark.skip(reason="needs a CUDA GPU")]
+
+import prompt_lookup_speculative_gb300 as pkg  # noqa: E402
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device_set_up():
+    """The library's per-device set-up happens on its first call, which must come
+    before any stream capture: one eager call on the default stream."""
+    w = gen.make_workload("tiny")
+    pkg.lookup_draft(torch.from_numpy(w.tokens).to(DEV), torch.from_numpy(w.offsets).to(DEV), 4, 12, 15)
+    torch.cuda.synchronize()
+
+
+def many_requests(B: int, seed: int):
+    """B short requests over a 4-letter alphabet: more slots than a stream's first
+    buffer (64 KiB, 8,192 slots) holds, so a call with it grows the buffer."""
+    rng = np.random.default_rng(seed)
+    lengths = rng.integers(0, 60, size=B)
+    tokens = rng.integers(0, 4, size=int(lengths.sum())).astype(np.int32)
+    return gen.Workload(name=f"many{B}", tokens=tokens, offsets=gen.offsets_from_lengths(lengths), min_m=4,
+                        max_m=12, K=7, seed=seed, planted={})
+
+
+class Batch:
+    def __init__(self, name: str, seed: int):
+        self.w = many_requests(12000, seed) if name == "many" else gen.make_workload(name, seed)
+        self.t = torch.from_numpy(self.w.tokens).to(DEV)
+        self.o = torch.from_numpy(self.w.offsets).to(DEV)
+        self.want = oracle.lookup_draft(self.w.tokens, self.w.offsets, self.w.min_m, self.w.max_m, self.w.K,
+                                        threads=8)
+
+    def outputs(self):
+        w = self.w
+        return (torch.full((w.B, w.K), 7, dtype=torch.int32, device=DEV),
+                torch.full((w.B,), 7, dtype=torch.int32, device=DEV),
+                torch.full((w.B,), 7, dtype=torch.int32, device=DEV))
+
+    def call(self, lib, out, stream):
+        w = self.w
+        d, ln, p = out
+        rc = lib.lookup_draft(self.t.data_ptr(), self.o.data_ptr(), w.B, w.min_m, w.max_m, w.K, d.data_ptr(),
+                              ln.data_ptr(), p.data_ptr(), stream.cuda_stream)
+        assert rc == 0, (lib.lookup_draft_strerror(rc), lib.lookup_draft_last_cuda_error())
+
+    def check(self, out, what: str):
+        for name, g, e in zip(("draft", "len", "pos"), out, self.want[:3]):
+            np.testing.assert_array_equal(g.cpu().numpy(), e, err_msg=f"{what}: {name}")
+
+
+def test_two_streams_interleaved_with_growth():
+    lib = pkg.load_library()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    small, big, other = Batch("tiny", 41), Batch("many", 42), Batch("recitation25k", 43)
+    plan = [(small, s1), (other, s2), (big, s1), (small, s2), (other, s1), (big, s2), (small, s1)]
+    outs = [(b, s, b.outputs()) for b, s in plan]
+    torch.cuda.synchronize()                            # inputs and outputs made on the default stream
+    for b, s, out in outs:
+        with torch.cuda.stream(s):
+            b.call(lib, out, s)
+    torch.cuda.synchronize()
+    for i, (b, _, out) in enumerate(outs):
+        b.check(out, f"call {i}")
+
+
+def test_growth_then_smaller_batches_on_one_stream():
+    lib = pkg.load_library()
+    s = torch.cuda.Stream()
+    batches = [Batch("tiny", 44), Batch("ragged262k", 45), Batch("many", 46), Batch("chats", 47)]
+    torch.cuda.synchronize()
+    results = []
+    with torch.cuda.stream(s):
+        for b in batches + batches[::-1]:
+            out = b.outputs()
+            b.call(lib, out, s)
+            results.append((b, out))
+    torch.cuda.synchronize()
+    for i, (b, out) in enumerate(results):
+        b.check(out, f"call {i}")
+
+
+@pytest.mark.parametrize("warm", [False, True])
+def test_graph_on_fresh_and_warm_streams(warm):
+    """warm=False: the capture finds no buffer for the stream and takes scratch from
+    the pool; warm=True: an eager call first, so the graph uses the stream's buffer."""
+    lib = pkg.load_library()
+    s = torch.cuda.Stream()
+    b1, b2 = Batch("recitation25k", 48), Batch("chats", 49)
+    o1, o2 = b1.outputs(), b2.outputs()
+    torch.cuda.synchronize()
+    if warm:
+        with torch.cuda.stream(s):
+            b2.call(lib, o2, s)
+        torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        cs = torch.cuda.current_stream()
+        for _ in range(3):
+            b1.call(lib, o1, cs)
+            b2.call(lib, o2, cs)
+    for rep in range(3):
+        for x in o1 + o2:
+            x.fill_(7)
+        g.replay()
+        torch.cuda.synchronize()
+        b1.check(o1, f"replay {rep}, first batch")
+        b2.check(o2, f"replay {rep}, second batch")
+
+
+def test_graph_replayed_after_its_buffer_was_replaced():
+    lib = pkg.load_library()
+    s = torch.cuda.Stream()
+    small, big = Batch("tiny", 50), Batch("many", 51)
+    o_small, o_big = small.outputs(), big.outputs()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        small.call(lib, o_small, s)                     # the stream's buffer, sized for the small batch
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        small.call(lib, o_small, torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        big.call(lib, o_big, s)                         # grows: a new buffer for this stream
+    torch.cuda.synchronize()
+    big.check(o_big, "larger batch")
+    for x in o_small:
+        x.fill_(7)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        g.replay()                                      # still uses the first buffer, still allocated
+    torch.cuda.synchronize()
+    small.check(o_small, "graph replay after growth")
