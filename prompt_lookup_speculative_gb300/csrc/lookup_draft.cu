@@ -1353,10 +1353,11 @@ int launch_host_copy(const DeviceState &st, const CopyParams &cp, cudaStream_t s
 // buffer, so consecutive calls in a CUDA graph have no memory nodes between them
 // and the next call's scan launches early behind the previous fill (a pool
 // allocation and free per call, captured as memory nodes, cost ~0.4 us per step).
-// Buffers are keyed by the stream handle and made outside stream capture only
-// (a hit makes no CUDA call; the capture check is legal during capture, a stream
-// id query is not).  They grow geometrically and are never freed before exit: a
-// captured graph may still refer to a buffer that a larger batch later replaced.
+// Buffers are keyed by the stream handle and made outside stream capture only (a
+// hit makes no CUDA call at all, so it is safe inside a capture; a miss asks
+// cudaStreamIsCapturing, which capture allows).  They grow geometrically and are
+// never freed before exit: a captured graph may still refer to a buffer that a
+// larger batch later replaced.
 // Calls on one stream are ordered, so they never overlap on its buffer.
 struct StreamScratch {
     unsigned long long *slots = nullptr;
