@@ -26,11 +26,11 @@
 #include <cstdint>
 #include <cstring>
 
-// Records a CUDA failure for lookup_draft_last_cuda_error (lookup_draft.cu);
-// returns LOOKUP_DRAFT_ECUDA.
-int lookup_record_cuda_error(cudaError_t e, const char *what);
-
 namespace {
+
+using lkd::allow_dependent_launch;
+using lkd::launch_pdl;
+using lkd::wait_for_prerequisite_grid;
 
 constexpr int kMaxBlock = 1 << 16;        // H + T (a verify block) at most
 constexpr int kScanThreads = 1024;       // offsets_kernel
@@ -42,14 +42,6 @@ constexpr int kWin = 128 * kSub;         // tokens per window
 constexpr int kCommitRegs = 1;           // committed tokens per lane held in registers
 constexpr int kFusedLoads = 4;           // counts per thread in the fused append's prefix
 constexpr int kFusedMaxB = kCopyThreads * kFusedLoads;   // batches up to this size: offsets inside append_kernel
-
-__device__ inline void allow_dependent_launch() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-__device__ inline void wait_for_prerequisite_grid() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
 
 // ------------------------------------------------------------------ fusion ----
 struct FuseParams {
@@ -508,24 +500,6 @@ __global__ void __launch_bounds__(kCopyThreads, kCopyCtasPerSm) append_kernel(Ap
 // ------------------------------------------------------------------- host ----
 int cuda_fail(cudaError_t e, const char *what) { return lookup_record_cuda_error(e, what); }
 
-template <typename Params>
-int launch_pdl(void (*kernel)(Params), dim3 grid, dim3 block, cudaStream_t stream, const Params &prm,
-               size_t smem = 0) {
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
-    return e == cudaSuccess ? LOOKUP_DRAFT_OK : cuda_fail(e, "kernel launch");
-}
-
 unsigned blocks_for(int64_t n, int per) { return unsigned((n + per - 1) / per); }
 
 }  // namespace
@@ -544,7 +518,7 @@ int lookup_fuse(const int32_t *lookup_draft, const int32_t *lookup_mlen, const i
         return LOOKUP_DRAFT_EINVAL;
     FuseParams p{lookup_draft, lookup_mlen, model_draft, long_block, out_block, out_len, out_point_mass,
                  B, K, H, T, replace_min, agree_min, agree_n, tail_min};
-    return launch_pdl(fuse_kernel, dim3(blocks_for(int64_t(B) * (H + T), 256)), dim3(256), stream, p);
+    return launch_pdl(fuse_kernel, blocks_for(int64_t(B) * (H + T), 256), 256u, stream, p);
 }
 
 int lookup_schedule(const int32_t *lookup_mlen, const int32_t *committed, int32_t B, int32_t H, int32_t T,
@@ -555,7 +529,7 @@ int lookup_schedule(const int32_t *lookup_mlen, const int32_t *committed, int32_
     if (B == 0) return LOOKUP_DRAFT_OK;
     if (!lookup_mlen || !committed || !state || !out_long) return LOOKUP_DRAFT_EINVAL;
     ScheduleParams p{lookup_mlen, committed, state, out_long, B, H, T, tail_min, slack, enter_steps, sticky};
-    return launch_pdl(schedule_kernel, dim3(blocks_for(B, 256)), dim3(256), stream, p);
+    return launch_pdl(schedule_kernel, blocks_for(B, 256), 256u, stream, p);
 }
 
 int lookup_verify(const int32_t *block, const int32_t *len, const int32_t *target, const float *probs,
@@ -567,7 +541,7 @@ int lookup_verify(const int32_t *block, const int32_t *len, const int32_t *targe
     if ((P > 0 && !block) || !len || !target || (probs && !u) || !out_accepted || !out_commit || !out_ncommit)
         return LOOKUP_DRAFT_EINVAL;
     VerifyParams p{block, len, target, probs, qprobs, point_mass, u, out_accepted, out_commit, out_ncommit, B, P};
-    return launch_pdl(verify_kernel, dim3(blocks_for(B, kVerifyWarps)), dim3(kVerifyWarps * 32), stream, p);
+    return launch_pdl(verify_kernel, blocks_for(B, kVerifyWarps), unsigned(kVerifyWarps * 32), stream, p);
 }
 
 int lookup_append(const int32_t *tokens, const int64_t *offsets, const int32_t *commit, const int32_t *ncommit,
@@ -583,12 +557,12 @@ int lookup_append(const int32_t *tokens, const int64_t *offsets, const int32_t *
     if (e != cudaSuccess) return cuda_fail(e, "device query");
     if (B > 0 && ((reinterpret_cast<uintptr_t>(tokens) | reinterpret_cast<uintptr_t>(out_tokens)) & 3))
         return LOOKUP_DRAFT_EINVAL;
-    const dim3 grid(unsigned(sms * kCopyCtasPerSm));
+    const unsigned grid = unsigned(sms * kCopyCtasPerSm);
     if (B > 0 && B <= kFusedMaxB && int64_t(B) * W < (int64_t(1) << 31))
-        return launch_pdl(append_kernel<true>, grid, dim3(kCopyThreads), stream, p, size_t(B + 1) * sizeof(int32_t));
-    int rc = launch_pdl(offsets_kernel, dim3(1), dim3(kScanThreads), stream, p);
+        return launch_pdl(append_kernel<true>, grid, unsigned(kCopyThreads), stream, p, size_t(B + 1) * sizeof(int32_t));
+    int rc = launch_pdl(offsets_kernel, 1u, unsigned(kScanThreads), stream, p);
     if (rc != LOOKUP_DRAFT_OK || B == 0) return rc;      // B == 0: out_offsets = {0} only
-    return launch_pdl(append_kernel<false>, grid, dim3(kCopyThreads), stream, p);
+    return launch_pdl(append_kernel<false>, grid, unsigned(kCopyThreads), stream, p);
 }
 
 }  // extern "C"
