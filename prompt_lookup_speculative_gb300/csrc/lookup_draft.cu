@@ -12,7 +12,7 @@
 //  scan_kernel -- the split-history scan, HBM bound (4 bytes per history token,
 //    read once).  The whole batch is one array of 16-byte quads; the grid (one CTA
 //    per SM, independent of the data so the host never reads the offsets) splits
-//    it into equal contiguous chunks, and each CTA's chunk into 16 equal warp
+//    it into equal contiguous chunks of at least 256 quads, and each CTA's chunk into 16 equal warp
 //    ranges ("virtual chunks"), so long requests are shared by many warps and
 //    short ones are packed into one.  The offsets arrive in shared memory with one
 //    TMA bulk copy; from then on every warp works alone.  A warp first loads the
@@ -68,6 +68,7 @@ using lkd::wait_for_prerequisite_grid;
 
 // ---------------------------------------------------------------- tuning ----
 constexpr int kWarps = 16;             // scan warps per CTA; each owns a contiguous range
+constexpr int kChunkMin = 256;         // quads per CTA chunk at least (small batches use fewer CTAs)
 constexpr int kChunkSmall = 512;       // quads per CTA chunk below which it has 8 warp ranges
 constexpr int kChunkMid = 2048;        // ... and below which 12 (else kWarps)
 constexpr int kThreads = kWarps * 32;
@@ -145,7 +146,9 @@ struct FillParams {
 // ------------------------------------------------------ partition helpers ----
 // The batch occupies aligned quads [q_lo, q_lo + nq) of the 16-byte-aligned view
 // of `tokens`.  Chunk c (CTA c) is quads [c*S, (c+1)*S) of that range, clipped,
-// with S = ceil(nq / G); warp w of chunk c takes quads [c*S + w*Sw, c*S + (w+1)*Sw)
+// with S = max(ceil(nq / G), kChunkMin): a small batch fills fewer CTAs, so its
+// requests span fewer warp ranges (fewer slots for the fill to fold) and fewer
+// warps repeat the per-warp prologue.  Warp w of chunk c takes quads [c*S + w*Sw, c*S + (w+1)*Sw)
 // of it, clipped to the chunk, with Sw = warp_span32(S) (ceil(S / kWarps) unless
 // the chunk is small).  Virtual chunk
 // v = c*kWarps + w.  Empty chunks and empty warp ranges come last in their order.
@@ -181,6 +184,7 @@ __device__ inline Partition make_partition(int64_t a_begin, int64_t a_end, int G
     P.q_lo = a_begin >> 2;
     P.nq = ((a_end + 3) >> 2) - P.q_lo;
     P.S = div_u(P.nq + G - 1, G);
+    P.S = P.S < kChunkMin ? kChunkMin : P.S;
     P.Sw = P.S < kChunkMid ? int64_t(warp_span32(uint32_t(P.S))) : div_u(P.S + kWarps - 1, kWarps);
     return P;
 }
@@ -454,7 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(ScanParams prm) {
     P.nq = ((a_end + 3) >> 2) - P.q_lo;
     if (P.nq < (int64_t(1) << 31) - G) {
         const uint32_t nq = uint32_t(P.nq), n = nq + uint32_t(G - 1);
-        const uint32_t S = prm.grid_shift < 0 ? n : __umulhi(n, prm.grid_magic) >> prm.grid_shift;
+        uint32_t S = prm.grid_shift < 0 ? n : __umulhi(n, prm.grid_magic) >> prm.grid_shift;
+        S = S < uint32_t(kChunkMin) ? uint32_t(kChunkMin) : S;
         const uint32_t Sw = warp_span32(S);
         P.S = S;
         P.Sw = Sw;

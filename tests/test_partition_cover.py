@@ -9,6 +9,8 @@ integer arithmetic in Python, with the kernel's constants read from its source,
 and checks on random batches that
 
 - the division by the grid size is exact for every value the kernel divides;
+- a chunk is never shorter than kChunkMin quads, so a small batch leaves the
+  last CTAs empty;
 - the warp ranges tile the batch's quads, so every candidate end of every
   request (positions min_m - 1 .. L - 2) is examined by exactly one warp;
 - every tile's halo reaches max_m - 1 tokens before the tile (or the batch
@@ -37,6 +39,7 @@ def _const(name, text=SRC):
 
 
 K_WARPS = _const("kWarps")
+CHUNK_MIN = _const("kChunkMin")
 CHUNK_SMALL = _const("kChunkSmall")
 CHUNK_MID = _const("kChunkMid")
 K_BUFS = _const("kBufs")
@@ -84,7 +87,7 @@ def warp_span(S):
 def warp_ranges(nq, G):
     """[lo, hi) per virtual chunk v = c * K_WARPS + w, quads relative to q_lo."""
     magic, shift = grid_divider(G)
-    S = div_grid(nq + G - 1, magic, shift)
+    S = max(div_grid(nq + G - 1, magic, shift), CHUNK_MIN)
     Sw = warp_span(S)
     out = []
     for c in range(G):
@@ -99,7 +102,7 @@ def warp_ranges(nq, G):
 def fill_partition(nq, G):
     """(S, Sw) as the fill kernel forms them (make_partition: plain divisions, the
     wide-chunk rule written separately), to be held against the scan's."""
-    S = (nq + G - 1) // G
+    S = max((nq + G - 1) // G, CHUNK_MIN)
     Sw = warp_span(S) if S < CHUNK_MID else (S + K_WARPS - 1) // K_WARPS
     return S, Sw
 
@@ -238,3 +241,20 @@ def test_chunk_sizes_at_the_range_count_switches(S, G):
         assert warp_ranges(nq, G)[0] == S
         emulate(offsets, shift, G, 4, 12)
         emulate(offsets, shift, G, 1, MAX_M)
+
+
+@pytest.mark.parametrize("G", [152, 7])
+def test_small_batches_use_whole_minimum_chunks(G):
+    """Batches smaller than G * kChunkMin quads: chunks of exactly kChunkMin quads,
+    the CTAs past the batch empty, and the cover still exact."""
+    rng = np.random.default_rng(G + 5)
+    for nq in (1, CHUNK_MIN - 1, CHUNK_MIN, CHUNK_MIN + 1, 3 * CHUNK_MIN, (G - 1) * CHUNK_MIN + 7):
+        S, Sw, ranges = warp_ranges(nq, G)
+        assert S == CHUNK_MIN
+        live = [v for v, (lo, hi) in enumerate(ranges) if lo < hi]
+        assert max(live) // K_WARPS == (nq - 1) // CHUNK_MIN          # the last CTA with work
+        total = 4 * nq - int(rng.integers(0, 4))
+        cuts = np.sort(rng.integers(0, total + 1, size=int(rng.integers(0, 40))))
+        offsets = np.concatenate([[0], cuts, [total]]).astype(np.int64)
+        emulate(offsets, 0, G, 4, 12)
+        emulate(offsets, 0, G, 1, MAX_M)
