@@ -576,7 +576,9 @@ def measure_loop(lib, pkg, w, dev, stream, toks, offs, reps: int) -> dict:
     every history from HBM) and replayed; CUDA events on the launching stream
     give the mean time per call.  ``loop_step_us`` is one whole decode-loop
     step: draft with mlen (K = H + T), scheduling, fusion, greedy verification
-    and the append of the committed tokens to every history."""
+    and the append of the committed tokens to every history;
+    ``loop_step_plan_us`` the same step with scheduling and fusion in one launch
+    (lookup_plan)."""
     import numpy as np
     import torch
 
@@ -637,6 +639,11 @@ def measure_loop(lib, pkg, w, dev, stream, toks, offs, reps: int) -> dict:
         check(lib.lookup_schedule(mp, committed.data_ptr(), B, H, T, 4, 1, 2, 3, state.data_ptr(),
                                   long_block.data_ptr(), hs))
 
+    def plan(j, hs):
+        check(lib.lookup_plan(dp, mp, model_draft.data_ptr(), committed.data_ptr(), B, K, H, T, 8, 6, 2, 4, 1, 2, 3,
+                              state.data_ptr(), long_block.data_ptr(), block.data_ptr(), blen.data_ptr(),
+                              pm.data_ptr(), hs))
+
     def verify_greedy(j, hs):
         check(lib.lookup_verify(block.data_ptr(), blen.data_ptr(), target.data_ptr(), None, None, None, None,
                                 B, P, accepted.data_ptr(), commit.data_ptr(), ncommit.data_ptr(), hs))
@@ -657,6 +664,12 @@ def measure_loop(lib, pkg, w, dev, stream, toks, offs, reps: int) -> dict:
         draft_ex(j, hs)
         schedule(j, hs)
         fuse(j, hs)
+        verify_greedy(j, hs)
+        append(j, hs)
+
+    def loop_step_plan(j, hs):                          # scheduling and fusion in one launch
+        draft_ex(j, hs)
+        plan(j, hs)
         verify_greedy(j, hs)
         append(j, hs)
 
@@ -686,10 +699,12 @@ def measure_loop(lib, pkg, w, dev, stream, toks, offs, reps: int) -> dict:
         "H": H, "T": T,
         "fuse_us": timed(fuse),
         "schedule_us": timed(schedule),
+        "plan_us": timed(plan),
         "verify_greedy_us": timed(verify_greedy),
         "verify_sampled_us": timed(verify_sampled),
         "append_us": timed(append),
         "loop_step_us": timed(loop_step),
+        "loop_step_plan_us": timed(loop_step_plan),
     }
     # the append's algorithmic bytes: every history token read and written once,
     # the committed tokens read and written, the counts and both offset arrays
@@ -699,6 +714,7 @@ def measure_loop(lib, pkg, w, dev, stream, toks, offs, reps: int) -> dict:
     res["append_algorithmic_bytes"] = append_bytes
     res["append_gbs"] = round(append_bytes / (res["append_us"] * 1e-6) / 1e9, 1)
     res["loop_step_launches"] = 2 + 1 + 1 + 1 + 2
+    res["loop_step_plan_launches"] = 2 + 1 + 1 + 2
     res["method"] = (f"each call captured {ncopy}x back to back in a CUDA graph over rotating input copies, "
                      f"{reps} replays, CUDA events on the launching stream")
     return res

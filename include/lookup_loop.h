@@ -95,6 +95,23 @@ int lookup_schedule(const int32_t *lookup_mlen, const int32_t *committed, int32_
                     int32_t sticky, int32_t *state, int32_t *out_long, struct CUstream_st *stream);
 
 /*
+ * lookup_schedule, then lookup_fuse with long_block = the new out_long, in one
+ * launch (HyperQwen lookup-drafting article, sections "第3步" and "第2步"): the
+ * per-request scheduling update and the block it selects, without a kernel
+ * boundary between them.  Arguments, layouts and rules are those of the two
+ * calls; tail_min serves both (the tail and the scheduling condition use the same
+ * match length, m >= 4 in the article).  state is updated in place; out_long,
+ * out_block, out_len and out_point_mass are exactly what lookup_schedule followed
+ * by lookup_fuse write.  Errors: the union of the two calls' checks.
+ */
+int lookup_plan(const int32_t *lookup_draft, const int32_t *lookup_mlen, const int32_t *model_draft,
+                const int32_t *committed, int32_t B, int32_t K, int32_t H, int32_t T,
+                int32_t replace_min, int32_t agree_min, int32_t agree_n, int32_t tail_min,
+                int32_t slack, int32_t enter_steps, int32_t sticky, int32_t *state,
+                int32_t *out_long, int32_t *out_block, int32_t *out_len, int32_t *out_point_mass,
+                struct CUstream_st *stream);
+
+/*
  * Verification of a proposal block of width P (= H + T), greedy or sampled.
  *
  * block         int32 [B][P] (P <= 65536), len int32 [B] (proposals used,

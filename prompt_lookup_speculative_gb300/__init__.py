@@ -27,7 +27,7 @@ from . import build as _build
 __all__ = [
     "LookupDraftError", "load_library", "lookup_draft", "lookup_draft_ex", "lookup_draft_host",
     "lookup_draft_scan", "lookup_draft_fill", "lookup_draft_noalloc", "workspace_bytes",
-    "set_wait_limit_ns", "lookup_fuse", "lookup_schedule", "lookup_verify", "lookup_append",
+    "set_wait_limit_ns", "lookup_fuse", "lookup_schedule", "lookup_plan", "lookup_verify", "lookup_append",
     "NgramIndex", "index_slots_for", "index_bytes", "lookup_index_build", "lookup_index_append",
     "lookup_index_draft", "ContextCache", "load_checked_library", "check_word",
     "MAX_M", "MAX_K", "LEN_FAILED", "CHECK_BITS",
@@ -146,6 +146,9 @@ def _declare_loop(lib: ctypes.CDLL) -> None:
     lib.lookup_fuse.restype = ctypes.c_int
     lib.lookup_schedule.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp]
     lib.lookup_schedule.restype = ctypes.c_int
+    lib.lookup_plan.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp,
+                                vp, vp, vp]
+    lib.lookup_plan.restype = ctypes.c_int
     lib.lookup_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp]
     lib.lookup_verify.restype = ctypes.c_int
     lib.lookup_append.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp]
@@ -426,6 +429,34 @@ def lookup_schedule(lookup_mlen, committed, state, H: int = 7, T: int = 8, tail_
                                  _stream_handle(stream))
     _check(rc, lib)
     return out
+
+
+def lookup_plan(lookup_draft, lookup_mlen, model_draft, committed, state, H: int = 7, T: int = 8,
+                replace_min: int = 8, agree_min: int = 6, agree_n: int = 2, tail_min: int = 4, slack: int = 1,
+                enter_steps: int = 2, sticky: int = 3, out=None, stream=None):
+    """lookup_schedule, then lookup_fuse with the new long flags, in one launch
+    ("第3步", "第2步").  ``state`` (int32 [B, 3]) is updated in place.  Returns
+    (long [B], block [B, H+T], len [B], point_mass [B, H+T])."""
+    import torch
+    lib = load_library()
+    dev = lookup_draft.device
+    B, K = lookup_draft.shape
+    args = (_dev(lookup_draft, torch.int32, (B, K), dev, "lookup_draft"),
+            _dev(lookup_mlen, torch.int32, (B,), dev, "lookup_mlen"),
+            _dev(model_draft, torch.int32, (B, H), dev, "model_draft"),
+            _dev(committed, torch.int32, (B,), dev, "committed"))
+    sp = _dev(state, torch.int32, (B, 3), dev, "state")
+    if out is None:
+        out = (torch.empty(B, dtype=torch.int32, device=dev), torch.empty((B, H + T), dtype=torch.int32, device=dev),
+               torch.empty(B, dtype=torch.int32, device=dev), torch.empty((B, H + T), dtype=torch.int32, device=dev))
+    lng, block, ln, pm = out
+    optr = (_dev(lng, torch.int32, (B,), dev, "long"), _dev(block, torch.int32, (B, H + T), dev, "block"),
+            _dev(ln, torch.int32, (B,), dev, "len"), _dev(pm, torch.int32, (B, H + T), dev, "point_mass"))
+    with torch.cuda.device(dev):
+        rc = lib.lookup_plan(*args, B, K, H, T, replace_min, agree_min, agree_n, tail_min, slack, enter_steps, sticky,
+                             sp, *optr, _stream_handle(stream))
+    _check(rc, lib)
+    return lng, block, ln, pm
 
 
 def lookup_verify(block, length, target, probs=None, qprobs=None, point_mass=None, u=None,

@@ -67,6 +67,24 @@ inline int launch_pdl(void (*kernel)(Params), unsigned grid, unsigned block, cud
     return e == cudaSuccess ? LOOKUP_DRAFT_OK : lookup_record_cuda_error(e, "kernel launch");
 }
 
+// The same for a kernel of two parameter structs.
+template <typename P1, typename P2>
+inline int launch_pdl2(void (*kernel)(P1, P2), unsigned grid, unsigned block, cudaStream_t stream, const P1 &a,
+                       const P2 &b) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, b);
+    return e == cudaSuccess ? LOOKUP_DRAFT_OK : lookup_record_cuda_error(e, "kernel launch");
+}
+
 inline int sm_count(int *out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -55,21 +55,21 @@ struct FuseParams {
     int32_t B, K, H, T, replace_min, agree_min, agree_n, tail_min;
 };
 
-// One thread per (request, block position).
-__global__ void fuse_kernel(FuseParams p) {
-    wait_for_prerequisite_grid();
-    allow_dependent_launch();
-    const int W = p.H + p.T;
-    const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (idx >= int64_t(p.B) * W) return;
-    const int r = int(idx / W), i = int(idx - int64_t(r) * W);
+// The head rule of request r: its first H proposals come from the lookup draft
+// (a long match, or a medium one whose first agree_n tokens the model agrees with).
+__device__ inline bool head_from_lookup(const FuseParams &p, int r, int32_t m) {
     const int32_t *ld = p.lookup_draft + int64_t(r) * p.K;
     const int32_t *md = p.model_draft + int64_t(r) * p.H;
-    const int32_t m = p.lookup_mlen[r];
     bool agree = true;
     for (int j = 0; j < p.agree_n; ++j) agree = agree && ld[j] == md[j];
-    const bool head_lookup = m >= p.replace_min || (m >= p.agree_min && agree);
-    const bool tail = p.long_block != nullptr && p.long_block[r] != 0 && m >= p.tail_min;
+    return m >= p.replace_min || (m >= p.agree_min && agree);
+}
+
+// Block position i of request r: the proposal and its point-mass flag.
+__device__ inline void fuse_position(const FuseParams &p, int r, int i, bool head_lookup, bool tail) {
+    const int W = p.H + p.T;
+    const int32_t *ld = p.lookup_draft + int64_t(r) * p.K;
+    const int32_t *md = p.model_draft + int64_t(r) * p.H;
     int32_t v, pm;
     if (i < p.H) {
         v = head_lookup ? ld[i] : md[i];
@@ -78,8 +78,22 @@ __global__ void fuse_kernel(FuseParams p) {
         v = tail ? ld[i] : -1;
         pm = tail;
     }
-    p.out_block[idx] = v;
-    p.out_pm[idx] = pm;
+    p.out_block[int64_t(r) * W + i] = v;
+    p.out_pm[int64_t(r) * W + i] = pm;
+}
+
+// One thread per (request, block position).
+__global__ void fuse_kernel(FuseParams p) {
+    wait_for_prerequisite_grid();
+    allow_dependent_launch();
+    const int W = p.H + p.T;
+    const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= int64_t(p.B) * W) return;
+    const int r = int(idx / W), i = int(idx - int64_t(r) * W);
+    const int32_t m = p.lookup_mlen[r];
+    const bool head_lookup = head_from_lookup(p, r, m);
+    const bool tail = p.long_block != nullptr && p.long_block[r] != 0 && m >= p.tail_min;
+    fuse_position(p, r, i, head_lookup, tail);
     if (i == 0) p.out_len[r] = tail ? W : p.H;
 }
 
@@ -92,16 +106,12 @@ struct ScheduleParams {
     int32_t B, H, T, tail_min, slack, enter_steps, sticky;
 };
 
-// One thread per request: {long, streak, hold} updated in place.
-__global__ void schedule_kernel(ScheduleParams p) {
-    wait_for_prerequisite_grid();
-    allow_dependent_launch();
-    const int r = blockIdx.x * blockDim.x + threadIdx.x;
-    if (r >= p.B) return;
-    int32_t *st = p.state + 3 * int64_t(r);
-    int32_t lng = st[0], streak = st[1], hold = st[2];
+// One scheduling update of a request's {long, streak, hold} from this step's
+// match length m and the previous step's commit count.
+__device__ inline void schedule_rule(const ScheduleParams &p, int32_t m, int32_t committed, int32_t &lng,
+                                     int32_t &streak, int32_t &hold) {
     const int32_t full = (lng ? p.H + p.T : p.H) + 1;
-    const bool cond = p.lookup_mlen[r] >= p.tail_min && p.committed[r] >= full - p.slack;
+    const bool cond = m >= p.tail_min && committed >= full - p.slack;
     streak = cond ? streak + 1 : 0;
     if (!lng) {
         if (streak >= p.enter_steps) {
@@ -115,10 +125,52 @@ __global__ void schedule_kernel(ScheduleParams p) {
     } else {
         lng = 0;
     }
+}
+
+// One thread per request: {long, streak, hold} updated in place.
+__global__ void schedule_kernel(ScheduleParams p) {
+    wait_for_prerequisite_grid();
+    allow_dependent_launch();
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= p.B) return;
+    int32_t *st = p.state + 3 * int64_t(r);
+    int32_t lng = st[0], streak = st[1], hold = st[2];
+    schedule_rule(p, p.lookup_mlen[r], p.committed[r], lng, streak, hold);
     st[0] = lng;
     st[1] = streak;
     st[2] = hold;
     p.out_long[r] = lng;
+}
+
+// ---------------------------------------------------- schedule, then fuse ----
+constexpr int kPlanWarps = 4;                   // requests per CTA
+
+// One warp per request: every lane reads the old state and applies the
+// scheduling rule (same values), the warp synchronises, lane 0 writes the new
+// state and the long flag, and the lanes fuse the block's positions with that
+// flag: lookup_schedule then lookup_fuse, in one launch.
+__global__ void plan_kernel(ScheduleParams sp, FuseParams fp) {
+    wait_for_prerequisite_grid();
+    allow_dependent_launch();
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * kPlanWarps + (threadIdx.x >> 5);
+    if (r >= sp.B) return;                       // warp-uniform
+    int32_t *st = sp.state + 3 * int64_t(r);
+    int32_t lng = st[0], streak = st[1], hold = st[2];
+    const int32_t m = sp.lookup_mlen[r];
+    schedule_rule(sp, m, sp.committed[r], lng, streak, hold);
+    __syncwarp();                                // every lane has read the old state
+    if (lane == 0) {
+        st[0] = lng;
+        st[1] = streak;
+        st[2] = hold;
+        sp.out_long[r] = lng;
+    }
+    const bool head_lookup = head_from_lookup(fp, r, m);
+    const bool tail = lng != 0 && m >= fp.tail_min;
+    const int W = fp.H + fp.T;
+    for (int i = lane; i < W; i += 32) fuse_position(fp, r, i, head_lookup, tail);
+    if (lane == 0) fp.out_len[r] = tail ? W : fp.H;
 }
 
 // ------------------------------------------------------------ verification ----
@@ -530,6 +582,25 @@ int lookup_schedule(const int32_t *lookup_mlen, const int32_t *committed, int32_
     if (!lookup_mlen || !committed || !state || !out_long) return LOOKUP_DRAFT_EINVAL;
     ScheduleParams p{lookup_mlen, committed, state, out_long, B, H, T, tail_min, slack, enter_steps, sticky};
     return launch_pdl(schedule_kernel, blocks_for(B, 256), 256u, stream, p);
+}
+
+int lookup_plan(const int32_t *lookup_draft, const int32_t *lookup_mlen, const int32_t *model_draft,
+                const int32_t *committed, int32_t B, int32_t K, int32_t H, int32_t T, int32_t replace_min,
+                int32_t agree_min, int32_t agree_n, int32_t tail_min, int32_t slack, int32_t enter_steps,
+                int32_t sticky, int32_t *state, int32_t *out_long, int32_t *out_block, int32_t *out_len,
+                int32_t *out_point_mass, struct CUstream_st *stream) {
+    lkd::TraceRange trace_("lookup_plan");
+    if (B < 0 || H < 1 || T < 0 || int64_t(H) + T > kMaxBlock || K < H + T || agree_n < 0 || agree_n > H ||
+        enter_steps < 1 || sticky < 0 || slack < 0)
+        return LOOKUP_DRAFT_EINVAL;
+    if (B == 0) return LOOKUP_DRAFT_OK;
+    if (!lookup_draft || !lookup_mlen || !model_draft || !committed || !state || !out_long || !out_block ||
+        !out_len || !out_point_mass)
+        return LOOKUP_DRAFT_EINVAL;
+    ScheduleParams sp{lookup_mlen, committed, state, out_long, B, H, T, tail_min, slack, enter_steps, sticky};
+    FuseParams fp{lookup_draft, lookup_mlen, model_draft, out_long, out_block, out_len, out_point_mass,
+                  B, K, H, T, replace_min, agree_min, agree_n, tail_min};
+    return lkd::launch_pdl2(plan_kernel, blocks_for(B, kPlanWarps), unsigned(kPlanWarps * 32), stream, sp, fp);
 }
 
 int lookup_verify(const int32_t *block, const int32_t *len, const int32_t *target, const float *probs,

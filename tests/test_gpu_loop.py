@@ -313,3 +313,72 @@ def test_decode_loop_back_to_back(name, B_sub):
     np.testing.assert_array_equal(host(t_g)[:o_o[-1]], t_o)
     np.testing.assert_array_equal(host(m_g), m_last)
     np.testing.assert_array_equal(host(d_g), d_last)
+
+
+# ------------------------------------------------------- schedule, then fuse ----
+@pytest.mark.parametrize("B,steps", [(1, 40), (33, 30), (4096, 12)])
+@pytest.mark.parametrize("H,T,agree_n", [(7, 8, 2), (3, 2, 0), (16, 48, 3)])
+@pytest.mark.parametrize("params", [dict(), dict(slack=0, enter_steps=1, sticky=0),
+                                    dict(slack=3, enter_steps=3, sticky=5, tail_min=6)])
+def test_plan_is_schedule_then_fuse(B, steps, H, T, agree_n, params):
+    """lookup_plan over a scheduling trace against the oracle's schedule followed
+    by its fuse with the new long flags: the long flags, the state, the block, its
+    length and the point-mass flags, every step."""
+    K = H + T + 2
+    mlen, committed = gen.loop_schedule_trace(B, steps, H, T, seed=B + steps + H)
+    st_o = np.zeros((B, 3), np.int32)
+    st_g = torch.zeros((B, 3), dtype=torch.int32, device="cuda")
+    tail_min = params.get("tail_min", 4)
+    entered = 0
+    for s in range(steps):
+        ld, _, md, _ = gen.loop_fuse_inputs(B, K, H, T, agree_n, seed=100 * s + B)
+        lg_o = oracle.schedule(mlen[s], committed[s], st_o, H, T, **params)
+        want = oracle.fuse(ld, mlen[s], md, lg_o, H, T, agree_n=agree_n, tail_min=tail_min)
+        lg_g, blk, ln, pm = pkg.lookup_plan(dev(ld), dev(mlen[s]), dev(md), dev(committed[s]), st_g, H, T,
+                                            agree_n=agree_n, **params)
+        np.testing.assert_array_equal(host(lg_g), lg_o, err_msg=f"long, step {s}")
+        np.testing.assert_array_equal(host(st_g), st_o, err_msg=f"state, step {s}")
+        for name, g, w in zip(("block", "len", "point mass"), (blk, ln, pm), want):
+            np.testing.assert_array_equal(host(g), w, err_msg=f"{name}, step {s}")
+        entered += int(lg_o.sum())
+    if B > 1:
+        assert 0 < entered < B * steps
+
+
+@pytest.mark.parametrize("name", ["tiny", "chats"])
+def test_decode_loop_with_plan_matches_oracle(name):
+    """Draft -> plan (schedule + fuse) -> verify -> append, four steps, against the
+    oracle's draft -> schedule -> fuse -> verify -> append."""
+    w = gen.make_workload(name)
+    B, H, T = w.B, 7, 8
+    K = P = H + T
+    tokens_o, offsets_o = w.tokens, w.offsets
+    tokens_g, offsets_g = dev(w.tokens), dev(w.offsets)
+    st_o = np.zeros((B, 3), np.int32)
+    st_g = torch.zeros((B, 3), dtype=torch.int32, device="cuda")
+    committed = np.full(B, H + 1, np.int32)
+    com_g = dev(committed)
+    for step in range(4):
+        d_o, l_o, p_o, m_o = oracle.lookup_draft(tokens_o, offsets_o, w.min_m, w.max_m, K, threads=8)
+        d_g, l_g, p_g, m_g = pkg.lookup_draft_ex(tokens_g, offsets_g, w.min_m, w.max_m, K)
+        rng = gen.rng_for(step, 79)
+        md = rng.integers(0, 50, size=(B, H), dtype=np.int64).astype(np.int32)
+        pick = rng.random(B) < 0.33
+        md[pick] = d_o[pick, :H]
+        lg_o = oracle.schedule(m_o, committed, st_o, H, T)
+        blk_o, len_o, pm_o = oracle.fuse(d_o, m_o, md, lg_o, H, T)
+        lg_g, blk_g, len_g, pm_g = pkg.lookup_plan(d_g, m_g, dev(md), com_g, st_g, H, T)
+        for a, b in ((lg_o, lg_g), (blk_o, blk_g), (len_o, len_g), (pm_o, pm_g), (st_o, st_g)):
+            np.testing.assert_array_equal(host(b), a)
+        target = rng.integers(0, 50, size=(B, P + 1), dtype=np.int64).astype(np.int32)
+        f = rng.integers(0, P + 1, size=B)
+        for r in range(B):
+            target[r, :f[r]] = blk_o[r, :f[r]]
+        acc_o, com_o, nc_o = oracle.verify(blk_o, len_o, target)
+        acc_g, com_t, nc_g = pkg.lookup_verify(blk_g, len_g, dev(target))
+        np.testing.assert_array_equal(host(nc_g), nc_o)
+        tokens_o, offsets_o = oracle.append(tokens_o, offsets_o, com_o, nc_o)
+        tokens_g, offsets_g = pkg.lookup_append(tokens_g, offsets_g, com_t, nc_g)
+        np.testing.assert_array_equal(host(offsets_g), offsets_o)
+        np.testing.assert_array_equal(host(tokens_g)[:offsets_o[-1]], tokens_o)
+        committed, com_g = nc_o, nc_g

@@ -255,3 +255,18 @@ def test_checked_build_command():
     cmd = lib_build.compile_command("x.so", checked=True)
     assert "-DLOOKUP_DRAFT_CHECKED=1" in cmd and "arch=compute_103a,code=sm_103a" in cmd
     assert "-DLOOKUP_DRAFT_CHECKED=1" not in lib_build.compile_command("x.so")
+
+
+def test_plan_rejects_bad_parameters(lib):
+    F = FAKE
+    # K < H + T, agree_n > H, enter_steps < 1, sticky < 0, slack < 0, a null state or output
+    assert lib.lookup_plan(F, F, F, F, 4, 14, 7, 8, 8, 6, 2, 4, 1, 2, 3, F, F, F, F, F, None) == -1
+    assert lib.lookup_plan(F, F, F, F, 4, 15, 7, 8, 8, 6, 8, 4, 1, 2, 3, F, F, F, F, F, None) == -1
+    assert lib.lookup_plan(F, F, F, F, 4, 15, 7, 8, 8, 6, 2, 4, 1, 0, 3, F, F, F, F, F, None) == -1
+    assert lib.lookup_plan(F, F, F, F, 4, 15, 7, 8, 8, 6, 2, 4, 1, 2, -1, F, F, F, F, F, None) == -1
+    assert lib.lookup_plan(F, F, F, F, 4, 15, 7, 8, 8, 6, 2, 4, -1, 2, 3, F, F, F, F, F, None) == -1
+    assert lib.lookup_plan(F, F, F, F, 4, 15, 7, 8, 8, 6, 2, 4, 1, 2, 3, None, F, F, F, F, None) == -1
+    assert lib.lookup_plan(F, F, F, F, 4, 15, 7, 8, 8, 6, 2, 4, 1, 2, 3, F, F, F, F, None, None) == -1
+    # B == 0 enqueues nothing
+    assert lib.lookup_plan(None, None, None, None, 0, 15, 7, 8, 8, 6, 2, 4, 1, 2, 3, None, None, None, None, None,
+                           None) == 0
