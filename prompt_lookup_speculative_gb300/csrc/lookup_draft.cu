@@ -1371,14 +1371,33 @@ struct StreamScratch {
 std::mutex g_scratch_mu;
 std::unordered_map<uintptr_t, StreamScratch> g_scratch[kMaxDevices];
 
+// The calling thread's last stream and its buffer: a repeat call on that stream
+// takes no lock.  A buffer is never freed, so this copy stays valid even after
+// another thread has given the stream a larger one (calls on one stream are
+// ordered whichever buffer each uses).
+struct LastScratch {
+    int dev = -1;
+    uintptr_t stream = 0;
+    StreamScratch sc;
+};
+thread_local LastScratch t_last;
+
 // The scratch of `stream` on device `dev`, holding at least `need` bytes; nullptr
 // (no error) when it has none and cannot make one now: the stream is capturing.
 int stream_scratch(int dev, cudaStream_t stream, size_t need, unsigned long long **out) {
+    const uintptr_t key = reinterpret_cast<uintptr_t>(stream);
+    if (t_last.dev == dev && t_last.stream == key && t_last.sc.bytes >= need) {
+        *out = t_last.sc.slots;
+        return LOOKUP_DRAFT_OK;
+    }
     *out = nullptr;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    StreamScratch &sc = g_scratch[dev][reinterpret_cast<uintptr_t>(stream)];
+    StreamScratch &sc = g_scratch[dev][key];
     if (sc.bytes >= need) {
         *out = sc.slots;
+        t_last.dev = dev;
+        t_last.stream = key;
+        t_last.sc = sc;
         return LOOKUP_DRAFT_OK;
     }
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -1391,6 +1410,9 @@ int stream_scratch(int dev, cudaStream_t stream, size_t need, unsigned long long
     sc.slots = static_cast<unsigned long long *>(p);    // the old buffer, if any, stays allocated
     sc.bytes = bytes;
     *out = sc.slots;
+    t_last.dev = dev;
+    t_last.stream = key;
+    t_last.sc = sc;
     return LOOKUP_DRAFT_OK;
 }
 

@@ -158,3 +158,37 @@ def test_graph_replayed_after_its_buffer_was_replaced():
         g.replay()                                      # still uses the first buffer, still allocated
     torch.cuda.synchronize()
     small.check(o_small, "graph replay after growth")
+
+
+def test_threads_calling_on_their_own_and_shared_streams():
+    """Four host threads (ctypes releases the GIL, so the library's host code runs
+    concurrently): two on streams of their own, two sharing a third stream. Each
+    call's outputs are its own, so every result can be checked afterwards."""
+    import threading
+
+    lib = pkg.load_library()
+    own1, own2, shared = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    batches = [Batch("tiny", 60), Batch("many", 61), Batch("recitation25k", 62), Batch("chats", 63)]
+    plan = [(own1, batches[0], batches[1]), (own2, batches[2], batches[3]),
+            (shared, batches[0], batches[2]), (shared, batches[1], batches[3])]
+    work = [[(b, b.outputs()) for _ in range(6) for b in (b1, b2)] for _, b1, b2 in plan]
+    torch.cuda.synchronize()
+    errors = []
+
+    def run(stream, calls):
+        try:
+            for b, out in calls:
+                b.call(lib, out, stream)
+        except Exception as exc:  # surfaced below
+            errors.append(exc)
+
+    threads = [threading.Thread(target=run, args=(s, calls)) for (s, _, _), calls in zip(plan, work)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for i, calls in enumerate(work):
+        for j, (b, out) in enumerate(calls):
+            b.check(out, f"thread {i}, call {j}")
