@@ -578,7 +578,8 @@ def measure_loop(lib, pkg, w, dev, stream, toks, offs, reps: int) -> dict:
     step: draft with mlen (K = H + T), scheduling, fusion, greedy verification
     and the append of the committed tokens to every history;
     ``loop_step_plan_us`` the same step with scheduling and fusion in one launch
-    (lookup_plan)."""
+    (lookup_plan), ``loop_step_draft_plan_us`` with the draft, scheduling and
+    fusion in two (lookup_draft_plan)."""
     import numpy as np
     import torch
 
@@ -673,6 +674,17 @@ def measure_loop(lib, pkg, w, dev, stream, toks, offs, reps: int) -> dict:
         verify_greedy(j, hs)
         append(j, hs)
 
+    def draft_plan(j, hs):                              # draft, scheduling and fusion in two launches
+        check(lib.lookup_draft_plan(tok_p[j], off_p[j], B, w.min_m, w.max_m, model_draft.data_ptr(),
+                                    committed.data_ptr(), H, T, 8, 6, 2, 4, 1, 2, 3, state.data_ptr(),
+                                    long_block.data_ptr(), block.data_ptr(), blen.data_ptr(), pm.data_ptr(), mp,
+                                    None, hs))
+
+    def loop_step_draft_plan(j, hs):
+        draft_plan(j, hs)
+        verify_greedy(j, hs)
+        append(j, hs)
+
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def timed(fn) -> float:
@@ -705,6 +717,8 @@ def measure_loop(lib, pkg, w, dev, stream, toks, offs, reps: int) -> dict:
         "append_us": timed(append),
         "loop_step_us": timed(loop_step),
         "loop_step_plan_us": timed(loop_step_plan),
+        "draft_plan_us": timed(draft_plan),
+        "loop_step_draft_plan_us": timed(loop_step_draft_plan),
     }
     # the append's algorithmic bytes: every history token read and written once,
     # the committed tokens read and written, the counts and both offset arrays
@@ -715,6 +729,7 @@ def measure_loop(lib, pkg, w, dev, stream, toks, offs, reps: int) -> dict:
     res["append_gbs"] = round(append_bytes / (res["append_us"] * 1e-6) / 1e9, 1)
     res["loop_step_launches"] = 2 + 1 + 1 + 1 + 2
     res["loop_step_plan_launches"] = 2 + 1 + 1 + 2
+    res["loop_step_draft_plan_launches"] = 2 + 1 + 2
     res["method"] = (f"each call captured {ncopy}x back to back in a CUDA graph over rotating input copies, "
                      f"{reps} replays, CUDA events on the launching stream")
     return res

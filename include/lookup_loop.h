@@ -112,6 +112,34 @@ int lookup_plan(const int32_t *lookup_draft, const int32_t *lookup_mlen, const i
                 struct CUstream_st *stream);
 
 /*
+ * A draft step followed by lookup_plan, in two launches instead of four
+ * (HyperQwen lookup-drafting article, sections "第1步", "第3步", "第2步").  The
+ * scan is lookup_draft's; the second kernel reduces each request's scan results
+ * to its match (m, p), reads the draft tokens that lookup_draft_ex would write
+ * with K = H + T, and applies lookup_plan's scheduling and fusion to them in the
+ * same warp.  The draft itself is not written out.
+ *
+ * tokens, offsets, B, min_m, max_m   as for lookup_draft (device pointers)
+ * model_draft, committed, H, T, replace_min, agree_min, agree_n, tail_min,
+ * slack, enter_steps, sticky, state, out_long, out_block, out_len,
+ * out_point_mass                     as for lookup_plan; H + T <= LOOKUP_DRAFT_MAX_K
+ * out_mlen        int32 [B] or NULL: m, as lookup_draft_ex writes it
+ * out_draft_len   int32 [B] or NULL: what lookup_draft's out_len would be (H + T,
+ *                 0, or LOOKUP_DRAFT_LEN_FAILED); a failed request is planned as
+ *                 one without a match
+ * Scratch as for lookup_draft (the stream's buffer).  Errors: those of
+ * lookup_draft and lookup_plan, and LOOKUP_DRAFT_EINVAL for a misaligned pointer.
+ * Every output equals lookup_draft_ex (K = H + T) followed by lookup_plan.
+ */
+int lookup_draft_plan(const int32_t *tokens, const int64_t *offsets, int32_t B,
+                      int32_t min_m, int32_t max_m,
+                      const int32_t *model_draft, const int32_t *committed, int32_t H, int32_t T,
+                      int32_t replace_min, int32_t agree_min, int32_t agree_n, int32_t tail_min,
+                      int32_t slack, int32_t enter_steps, int32_t sticky, int32_t *state,
+                      int32_t *out_long, int32_t *out_block, int32_t *out_len, int32_t *out_point_mass,
+                      int32_t *out_mlen, int32_t *out_draft_len, struct CUstream_st *stream);
+
+/*
  * Verification of a proposal block of width P (= H + T), greedy or sampled.
  *
  * block         int32 [B][P] (P <= 65536), len int32 [B] (proposals used,

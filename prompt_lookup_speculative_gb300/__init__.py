@@ -27,7 +27,8 @@ from . import build as _build
 __all__ = [
     "LookupDraftError", "load_library", "lookup_draft", "lookup_draft_ex", "lookup_draft_host",
     "lookup_draft_scan", "lookup_draft_fill", "lookup_draft_noalloc", "workspace_bytes",
-    "set_wait_limit_ns", "lookup_fuse", "lookup_schedule", "lookup_plan", "lookup_verify", "lookup_append",
+    "set_wait_limit_ns", "lookup_fuse", "lookup_schedule", "lookup_plan", "lookup_draft_plan", "lookup_verify",
+    "lookup_append",
     "NgramIndex", "index_slots_for", "index_bytes", "lookup_index_build", "lookup_index_append",
     "lookup_index_draft", "ContextCache", "load_checked_library", "check_word",
     "MAX_M", "MAX_K", "LEN_FAILED", "CHECK_BITS",
@@ -149,6 +150,9 @@ def _declare_loop(lib: ctypes.CDLL) -> None:
     lib.lookup_plan.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp,
                                 vp, vp, vp]
     lib.lookup_plan.restype = ctypes.c_int
+    lib.lookup_draft_plan.argtypes = [vp, vp, i32, i32, i32, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                      vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.lookup_draft_plan.restype = ctypes.c_int
     lib.lookup_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp]
     lib.lookup_verify.restype = ctypes.c_int
     lib.lookup_append.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp]
@@ -457,6 +461,36 @@ def lookup_plan(lookup_draft, lookup_mlen, model_draft, committed, state, H: int
                              sp, *optr, _stream_handle(stream))
     _check(rc, lib)
     return lng, block, ln, pm
+
+
+def lookup_draft_plan(tokens, offsets, model_draft, committed, state, min_m: int = 4, max_m: int = 12, H: int = 7,
+                      T: int = 8, replace_min: int = 8, agree_min: int = 6, agree_n: int = 2, tail_min: int = 4,
+                      slack: int = 1, enter_steps: int = 2, sticky: int = 3, out=None, stream=None):
+    """A draft step followed by lookup_plan, in two launches ("第1步", "第3步",
+    "第2步"); ``state`` (int32 [B, 3]) is updated in place.  Returns (long [B],
+    block [B, H+T], len [B], point_mass [B, H+T], mlen [B], draft_len [B])."""
+    import torch
+    lib = load_library()
+    B = _as_batch(tokens, offsets)
+    t, o = tokens, offsets
+    dev = t.device
+    args = (_dev(model_draft, torch.int32, (B, H), dev, "model_draft"),
+            _dev(committed, torch.int32, (B,), dev, "committed"))
+    sp = _dev(state, torch.int32, (B, 3), dev, "state")
+    W = H + T
+    if out is None:
+        out = (torch.empty(B, dtype=torch.int32, device=dev), torch.empty((B, W), dtype=torch.int32, device=dev),
+               torch.empty(B, dtype=torch.int32, device=dev), torch.empty((B, W), dtype=torch.int32, device=dev),
+               torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev))
+    lng, block, ln, pm, ml, dl = out
+    optr = (_dev(lng, torch.int32, (B,), dev, "long"), _dev(block, torch.int32, (B, W), dev, "block"),
+            _dev(ln, torch.int32, (B,), dev, "len"), _dev(pm, torch.int32, (B, W), dev, "point_mass"),
+            _dev(ml, torch.int32, (B,), dev, "mlen"), _dev(dl, torch.int32, (B,), dev, "draft_len"))
+    with torch.cuda.device(dev):
+        rc = lib.lookup_draft_plan(t.data_ptr(), o.data_ptr(), B, min_m, max_m, *args, H, T, replace_min, agree_min,
+                                   agree_n, tail_min, slack, enter_steps, sticky, sp, *optr, _stream_handle(stream))
+    _check(rc, lib)
+    return lng, block, ln, pm, ml, dl
 
 
 def lookup_verify(block, length, target, probs=None, qprobs=None, point_mass=None, u=None,

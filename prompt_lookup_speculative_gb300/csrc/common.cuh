@@ -21,6 +21,46 @@ namespace lkd {
 __device__ inline void wait_for_prerequisite_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ inline void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Long-block scheduling (HyperQwen lookup-drafting article, section "第3步"): one
+// update of a request's {long, streak, hold} from this step's match length m and
+// the previous step's commit count.  full = the tokens a fully accepted block of
+// the previous step commits; the condition is a usable match and a nearly full
+// commit; `enter_steps` consecutive steps enter the long block, and it is kept for
+// `sticky` steps after the condition first fails.
+__device__ inline void schedule_update(int32_t m, int32_t committed, int32_t H, int32_t T, int32_t tail_min,
+                                       int32_t slack, int32_t enter_steps, int32_t sticky, int32_t &lng,
+                                       int32_t &streak, int32_t &hold) {
+    const int32_t full = (lng ? H + T : H) + 1;
+    const bool cond = m >= tail_min && committed >= full - slack;
+    streak = cond ? streak + 1 : 0;
+    if (!lng) {
+        if (streak >= enter_steps) {
+            lng = 1;
+            hold = sticky;
+        }
+    } else if (cond) {
+        hold = sticky;
+    } else if (hold > 0) {
+        --hold;                                          // sticky exit: the long block is kept
+    } else {
+        lng = 0;
+    }
+}
+
+// Fusion ("第2步"), block position i: the head (i < H) takes the lookup token when
+// the head rule holds, else the model's; the tail takes the lookup token when the
+// tail rule holds, else -1.  A lookup token is a point mass.
+__device__ inline void fuse_choice(int32_t i, int32_t H, bool head_lookup, bool tail, int32_t lookup_tok,
+                                   int32_t model_tok, int32_t &v, int32_t &pm) {
+    if (i < H) {
+        v = head_lookup ? lookup_tok : model_tok;
+        pm = head_lookup;
+    } else {
+        v = tail ? lookup_tok : -1;
+        pm = tail;
+    }
+}
+
 // splitmix64's output mix (Steele, Lea and Flood, "Fast splittable pseudorandom
 // number generators", OOPSLA 2014).
 __device__ inline uint64_t mix64(uint64_t x) {

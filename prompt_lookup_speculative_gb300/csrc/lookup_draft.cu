@@ -50,6 +50,7 @@
 // out_len = LOOKUP_DRAFT_LEN_FAILED instead of a hang.
 
 #include "lookup_draft.h"
+#include "lookup_loop.h"
 
 #include "common.cuh"
 
@@ -939,22 +940,15 @@ __device__ bool offsets_invalid(const int64_t *offsets, int B) {
     return bad;
 }
 
-// The outputs of request r when the batch's offsets are invalid.
-__device__ void write_failed(const FillParams &prm, int r, int first, int step, bool head) {
-    int32_t *row = prm.out_draft + int64_t(r) * prm.K;
-    for (int j = first; j < prm.K; j += step) row[j] = -1;
-    if (head) {
-        prm.out_len[r] = LOOKUP_DRAFT_LEN_FAILED;
-        prm.out_pos[r] = -1;
-        if (prm.out_mlen) prm.out_mlen[r] = 0;
-    }
-}
 #endif
 
 // One warp per request, for small batches: the request's slots lie in the scan
 // warps v0 .. v1 holding its first and last quads, and the lanes load them in
-// parallel.
-__global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_kernel(FillParams prm) {
+// parallel.  The reduced key (in every lane) goes to tail(r, lane, o0, L, key),
+// which writes the request's outputs; invalid offsets (checked build) arrive as a
+// failed key.
+template <class Tail>
+__device__ __forceinline__ void fold_request(const FillParams &prm, Tail &&tail) {
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * kFillWarps + (threadIdx.x >> 5);
 #if LOOKUP_DRAFT_CHECKED
@@ -996,7 +990,7 @@ __global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_kernel(F
     if (r >= prm.B) return;
 #if LOOKUP_DRAFT_CHECKED
     if (csr_bad) {
-        write_failed(prm, r, lane, 32, lane == 0);
+        tail(r, lane, int64_t(0), int64_t(0), kKeyFailed);
         return;
     }
 #endif
@@ -1029,7 +1023,87 @@ __global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_kernel(F
             key = x > key ? x : key;
         }
     }
-    write_draft(prm, r, o0, L, key, lane, 32, lane == 0);
+    tail(r, lane, o0, L, key);
+}
+
+__global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_kernel(FillParams prm) {
+    fold_request(prm, [&](int r, int lane, int64_t o0, int64_t L, unsigned long long key) {
+        write_draft(prm, r, o0, L, key, lane, 32, lane == 0);
+    });
+}
+
+// ------------------------------------------------- draft, then schedule and fuse ----
+// The decode loop's next two steps on the fill's result, in the fill's warp:
+// long-block scheduling and fusion with the draft model's head (HyperQwen
+// lookup-drafting article, sections "第3步" and "第2步"), the rules lookup_plan
+// applies, on the draft lookup_draft_ex would write (K = H + T <= 64).
+struct PlanArgs {
+    const int32_t *model_draft;   // [B][H]
+    const int32_t *committed;     // [B]
+    int32_t *state;               // [B][3] in/out
+    int32_t *out_long;
+    int32_t *out_block;           // [B][H + T]
+    int32_t *out_len;
+    int32_t *out_pm;              // [B][H + T]
+    int32_t *out_mlen;            // may be null
+    int32_t *out_draft_len;       // may be null
+    int32_t H, T, replace_min, agree_min, agree_n, tail_min, slack, enter_steps, sticky;
+};
+
+__global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_plan_kernel(FillParams prm, PlanArgs pa) {
+    fold_request(prm, [&](int r, int lane, int64_t o0, int64_t L, unsigned long long key) {
+        const int64_t km = int64_t(key >> 32), kp = int64_t(uint32_t(key));
+        const bool failed = key != 0ull && (key == kKeyFailed || km < 1 || kp + km > L - 1);
+        const bool found = key != 0ull && !failed;
+        const int32_t m = found ? int32_t(km) : 0;
+        const int64_t p = found ? kp : 0;
+        const int d = found ? int(L - p - m) : 1;
+        const int W = pa.H + pa.T;
+        // Draft tokens lane and lane + 32 (-1 without a match), as write_draft forms them.
+        const int32_t *src = prm.tokens + o0 + p + m;
+        const int j1 = lane + 32;
+        const int32_t tok0 = (found && lane < W && LKD_OK(p + m + (lane < d ? lane : lane % d) < L,
+                                                          LOOKUP_DRAFT_CHECK_TOKENS))
+                                 ? __ldg(src + (lane < d ? lane : lane % d))
+                                 : -1;
+        const int32_t tok1 = (found && j1 < W && LKD_OK(p + m + (j1 < d ? j1 : j1 % d) < L, LOOKUP_DRAFT_CHECK_TOKENS))
+                                 ? __ldg(src + (j1 < d ? j1 : j1 % d))
+                                 : -1;
+        // Head rule: the model agrees with the draft's first agree_n tokens.
+        const int32_t *md = pa.model_draft + int64_t(r) * pa.H;
+        const int32_t md0 = lane < pa.H ? md[lane] : -1, md1 = j1 < pa.H ? md[j1] : -1;
+        const bool ne = (lane < pa.agree_n && tok0 != md0) || (j1 < pa.agree_n && tok1 != md1);
+        const bool agree = __all_sync(0xffffffffu, !ne);
+        const bool head = m >= pa.replace_min || (m >= pa.agree_min && agree);
+        // Scheduling: every lane reads the old state, then lane 0 writes the new one.
+        int32_t *st = pa.state + 3 * int64_t(r);
+        int32_t lng = st[0], streak = st[1], hold = st[2];
+        lkd::schedule_update(m, pa.committed[r], pa.H, pa.T, pa.tail_min, pa.slack, pa.enter_steps, pa.sticky,
+                             lng, streak, hold);
+        __syncwarp();
+        const bool tail = lng != 0 && m >= pa.tail_min;
+        if (lane == 0) {
+            st[0] = lng;
+            st[1] = streak;
+            st[2] = hold;
+            pa.out_long[r] = lng;
+            pa.out_len[r] = tail ? W : pa.H;
+            if (pa.out_mlen) pa.out_mlen[r] = m;
+            if (pa.out_draft_len) pa.out_draft_len[r] = found ? W : (failed ? LOOKUP_DRAFT_LEN_FAILED : 0);
+        }
+        // Fusion of the block's positions.
+        int32_t v, pm;
+        if (lane < W) {
+            lkd::fuse_choice(lane, pa.H, head, tail, tok0, md0, v, pm);
+            pa.out_block[int64_t(r) * W + lane] = v;
+            pa.out_pm[int64_t(r) * W + lane] = pm;
+        }
+        if (j1 < W) {
+            lkd::fuse_choice(j1, pa.H, head, tail, tok1, md1, v, pm);
+            pa.out_block[int64_t(r) * W + j1] = v;
+            pa.out_pm[int64_t(r) * W + j1] = pm;
+        }
+    });
 }
 
 // One request per lane, for large batches: there most requests' slots lie in one
@@ -1075,7 +1149,7 @@ __global__ void __launch_bounds__(kLaneFillThreads) fill_lanes_kernel(FillParams
     wait_for_prerequisite_grid();
 #if LOOKUP_DRAFT_CHECKED
     if (csr_bad) {
-        if (live) write_failed(prm, r, 0, 1, true);
+        if (live) write_draft(prm, r, 0, 0, kKeyFailed, 0, 1, true);   // every output marked failed
         return;
     }
 #endif
@@ -1446,6 +1520,45 @@ int run_step(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t m
     return rc;
 }
 
+// The scan, then the fill with scheduling and fusion, on the stream's scratch (the
+// pool's when a capture finds none), as run_step does.
+int run_plan(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t min_m, int32_t max_m,
+             const PlanArgs &pa, cudaStream_t stream) {
+    DeviceState *st = nullptr;
+    int rc = device_state(&st);
+    if (rc != LOOKUP_DRAFT_OK) return rc;
+    int dev = 0;
+    LD_CUDA(cudaGetDevice(&dev));
+    const size_t need = workspace_bytes_for(B, grid_for(*st));
+    unsigned long long *slots = nullptr;
+    rc = stream_scratch(dev, stream, need, &slots);
+    if (rc != LOOKUP_DRAFT_OK) return rc;
+    void *ws = nullptr;
+    if (!slots) {
+        LD_CUDA(cudaMallocFromPoolAsync(&ws, need, st->pool, stream));
+        slots = static_cast<unsigned long long *>(ws);
+    }
+    FillParams fp{};
+    fp.tokens = tokens;
+    fp.offsets = offsets;
+    fp.slots = slots;
+    fp.B = B;
+    fp.K = pa.H + pa.T;
+    fp.grid = grid_for(*st);
+#if LOOKUP_DRAFT_CHECKED
+    fp.nslots = int64_t(B) + int64_t(fp.grid) * kWarps;
+#endif
+    rc = launch_scan(*st, tokens, offsets, B, min_m, max_m, slots, stream);
+    if (rc == LOOKUP_DRAFT_OK)
+        rc = lkd::launch_pdl2(fill_plan_kernel, unsigned((int64_t(B) + kFillWarps - 1) / kFillWarps),
+                              unsigned(kFillWarps * 32), stream, fp, pa);
+    if (ws) {
+        cudaError_t fe = cudaFreeAsync(ws, stream);
+        if (rc == LOOKUP_DRAFT_OK && fe != cudaSuccess) return cuda_fail(fe, "cudaFreeAsync");
+    }
+    return rc;
+}
+
 // ------------------------------------------------- no-allocation entry point ----
 // lookup_draft_noalloc keeps the scan's result slots in one fixed array in device
 // memory instead of taking them from a pool, so a call makes no allocation at
@@ -1692,6 +1805,30 @@ const char *lookup_draft_strerror(int code) {
 const char *lookup_draft_last_cuda_error(void) { return g_cuda_msg; }
 
 void lookup_draft_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns ? ns : kDefaultWaitNs); }
+
+int lookup_draft_plan(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t min_m, int32_t max_m,
+                      const int32_t *model_draft, const int32_t *committed, int32_t H, int32_t T,
+                      int32_t replace_min, int32_t agree_min, int32_t agree_n, int32_t tail_min, int32_t slack,
+                      int32_t enter_steps, int32_t sticky, int32_t *state, int32_t *out_long, int32_t *out_block,
+                      int32_t *out_len, int32_t *out_point_mass, int32_t *out_mlen, int32_t *out_draft_len,
+                      struct CUstream_st *stream) {
+    TraceRange trace_("lookup_draft_plan");
+    g_cuda_msg[0] = '\0';
+    if (H < 1 || T < 0 || int64_t(H) + T > LOOKUP_DRAFT_MAX_K || agree_n < 0 || agree_n > H || enter_steps < 1 ||
+        sticky < 0 || slack < 0)
+        return LOOKUP_DRAFT_EINVAL;
+    int rc = check_common(tokens, offsets, B, min_m, max_m, H + T);
+    if (rc != LOOKUP_DRAFT_OK || B == 0) return rc;
+    if (!model_draft || !committed || !state || !out_long || !out_block || !out_len || !out_point_mass)
+        return LOOKUP_DRAFT_EINVAL;
+    const int32_t *ptrs[] = {model_draft, committed, state, out_long, out_block, out_len, out_point_mass, out_mlen,
+                             out_draft_len};
+    for (const int32_t *q : ptrs)
+        if (q && !aligned(q, 4)) return LOOKUP_DRAFT_EINVAL;
+    PlanArgs pa{model_draft, committed, state, out_long, out_block, out_len, out_point_mass, out_mlen,
+                out_draft_len, H, T, replace_min, agree_min, agree_n, tail_min, slack, enter_steps, sticky};
+    return run_plan(tokens, offsets, B, min_m, max_m, pa, stream);
+}
 
 int lookup_draft_checked_build(void) { return LOOKUP_DRAFT_CHECKED ? 1 : 0; }
 

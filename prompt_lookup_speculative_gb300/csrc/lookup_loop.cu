@@ -71,13 +71,7 @@ __device__ inline void fuse_position(const FuseParams &p, int r, int i, bool hea
     const int32_t *ld = p.lookup_draft + int64_t(r) * p.K;
     const int32_t *md = p.model_draft + int64_t(r) * p.H;
     int32_t v, pm;
-    if (i < p.H) {
-        v = head_lookup ? ld[i] : md[i];
-        pm = head_lookup;
-    } else {
-        v = tail ? ld[i] : -1;
-        pm = tail;
-    }
+    lkd::fuse_choice(i, p.H, head_lookup, tail, ld[i], i < p.H ? md[i] : -1, v, pm);
     p.out_block[int64_t(r) * W + i] = v;
     p.out_pm[int64_t(r) * W + i] = pm;
 }
@@ -110,21 +104,7 @@ struct ScheduleParams {
 // match length m and the previous step's commit count.
 __device__ inline void schedule_rule(const ScheduleParams &p, int32_t m, int32_t committed, int32_t &lng,
                                      int32_t &streak, int32_t &hold) {
-    const int32_t full = (lng ? p.H + p.T : p.H) + 1;
-    const bool cond = m >= p.tail_min && committed >= full - p.slack;
-    streak = cond ? streak + 1 : 0;
-    if (!lng) {
-        if (streak >= p.enter_steps) {
-            lng = 1;
-            hold = p.sticky;
-        }
-    } else if (cond) {
-        hold = p.sticky;
-    } else if (hold > 0) {
-        --hold;                                          // sticky exit: the long block is kept
-    } else {
-        lng = 0;
-    }
+    lkd::schedule_update(m, committed, p.H, p.T, p.tail_min, p.slack, p.enter_steps, p.sticky, lng, streak, hold);
 }
 
 // One thread per request: {long, streak, hold} updated in place.

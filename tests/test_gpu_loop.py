@@ -382,3 +382,61 @@ def test_decode_loop_with_plan_matches_oracle(name):
         np.testing.assert_array_equal(host(offsets_g), offsets_o)
         np.testing.assert_array_equal(host(tokens_g)[:offsets_o[-1]], tokens_o)
         committed, com_g = nc_o, nc_g
+
+
+# ------------------------------------------------- draft, then plan (two launches) ----
+@pytest.mark.parametrize("name", ["tiny", "recitation25k", "periodic", "chats"])
+def test_draft_plan_is_draft_then_plan(name):
+    """lookup_draft_plan over a 4-step scheduling trace on a workload's histories,
+    against the oracle's draft (K = H + T) -> schedule -> fuse: long flags, state,
+    block, length, point masses, m and the draft length, every step."""
+    w = gen.make_workload(name)
+    B, H, T = w.B, 7, 8
+    K = H + T
+    t, o = dev(w.tokens), dev(w.offsets)
+    d_o, l_o, p_o, m_o = oracle.lookup_draft(w.tokens, w.offsets, w.min_m, w.max_m, K, threads=8)
+    _, committed = gen.loop_schedule_trace(B, 4, H, T, seed=B + 5)
+    st_o = np.zeros((B, 3), np.int32)
+    st_g = torch.zeros((B, 3), dtype=torch.int32, device="cuda")
+    for s in range(4):
+        rng = gen.rng_for(s, 81)
+        md = rng.integers(0, 50, size=(B, H), dtype=np.int64).astype(np.int32)
+        pick = rng.random(B) < 0.4
+        md[pick] = d_o[pick, :H]
+        bump = pick & (rng.random(B) < 0.3)
+        md[bump, 1] += 1                                 # agreement broken on the second token
+        lg_o = oracle.schedule(m_o, committed[s], st_o, H, T)
+        blk_o, len_o, pm_o = oracle.fuse(d_o, m_o, md, lg_o, H, T)
+        lg, blk, ln, pm, ml, dl = pkg.lookup_draft_plan(t, o, dev(md), dev(committed[s]), st_g, w.min_m, w.max_m,
+                                                        H, T)
+        for nm, g, e in (("long", lg, lg_o), ("state", st_g, st_o), ("block", blk, blk_o), ("len", ln, len_o),
+                         ("point mass", pm, pm_o), ("mlen", ml, m_o), ("draft len", dl, l_o)):
+            np.testing.assert_array_equal(host(g), e, err_msg=f"{nm}, step {s}")
+
+
+@pytest.mark.parametrize("H,T,agree_n", [(3, 2, 3), (1, 0, 1), (16, 48, 2), (40, 24, 36)])
+def test_draft_plan_block_shapes(H, T, agree_n):
+    """Blocks of 5 to 64 positions (two tokens per lane past 32), agreement over
+    up to 36 head tokens, min_m = 1 (dense matches) and histories of every short
+    length with offsets[0] > 0."""
+    rng = np.random.default_rng(H * 100 + T)
+    lengths = rng.integers(0, 400, size=300)
+    lengths[:20] = np.arange(20)
+    lead = 3
+    tokens = np.concatenate([rng.integers(0, 3, lead), rng.integers(0, 4, int(lengths.sum()))]).astype(np.int32)
+    offsets = gen.offsets_from_lengths(lengths) + lead
+    B, K = lengths.size, H + T
+    d_o, l_o, p_o, m_o = oracle.lookup_draft(tokens, offsets, 1, 12, K, threads=8)
+    md = rng.integers(0, 4, size=(B, H), dtype=np.int64).astype(np.int32)
+    take = rng.random(B) < 0.5
+    md[take] = np.where(d_o[take, :H] >= 0, d_o[take, :H], md[take])
+    committed = rng.integers(1, H + T + 2, size=B).astype(np.int32)
+    st_o = rng.integers(0, 2, size=(B, 3)).astype(np.int32)
+    st_g = dev(st_o.copy())
+    lg_o = oracle.schedule(m_o, committed, st_o, H, T)
+    blk_o, len_o, pm_o = oracle.fuse(d_o, m_o, md, lg_o, H, T, agree_n=agree_n)
+    lg, blk, ln, pm, ml, dl = pkg.lookup_draft_plan(dev(tokens), dev(offsets), dev(md), dev(committed), st_g, 1, 12,
+                                                    H, T, agree_n=agree_n)
+    for nm, g, e in (("long", lg, lg_o), ("state", st_g, st_o), ("block", blk, blk_o), ("len", ln, len_o),
+                     ("point mass", pm, pm_o), ("mlen", ml, m_o), ("draft len", dl, l_o)):
+        np.testing.assert_array_equal(host(g), e, err_msg=nm)

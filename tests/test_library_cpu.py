@@ -270,3 +270,30 @@ def test_plan_rejects_bad_parameters(lib):
     # B == 0 enqueues nothing
     assert lib.lookup_plan(None, None, None, None, 0, 15, 7, 8, 8, 6, 2, 4, 1, 2, 3, None, None, None, None, None,
                            None) == 0
+
+
+def test_draft_plan_rejects_bad_parameters(lib):
+    F = FAKE
+    ok = [F, F, 4, 4, 12, F, F, 7, 8, 8, 6, 2, 4, 1, 2, 3, F, F, F, F, F, None, None, None]
+    assert len(ok) == 24
+
+    def call(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return lib.lookup_draft_plan(*a)
+
+    assert call(a7=0) == -1                 # H < 1
+    assert call(a8=-1) == -1                # T < 0
+    assert call(a7=40, a8=25) == -1         # H + T above LOOKUP_DRAFT_MAX_K
+    assert call(a11=8) == -1                # agree_n > H
+    assert call(a14=0) == -1                # enter_steps < 1
+    assert call(a15=-1) == -1               # sticky < 0
+    assert call(a13=-1) == -1               # slack < 0
+    assert call(a3=5, a4=4) == -1           # min_m > max_m
+    assert call(a5=None) == -1              # no model draft
+    assert call(a16=None) == -1             # no state
+    assert call(a16=F + 2) == -1            # misaligned state
+    assert call(a0=F + 2) == -1             # misaligned tokens
+    assert lib.lookup_draft_plan(None, None, 0, 4, 12, None, None, 7, 8, 8, 6, 2, 4, 1, 2, 3, None, None, None, None,
+                                 None, None, None, None) == 0
