@@ -416,3 +416,29 @@ def test_bounded_waits_fail_cleanly():
     got = run_gpu(w.tokens, w.offsets, w.min_m, w.max_m, w.K)
     for g, exp in zip(got, want):
         np.testing.assert_array_equal(g, exp)
+
+
+def test_cuda_error_inside_capture_is_reported_and_the_context_stays_usable():
+    """lookup_draft_host called inside a stream capture: its copy from pageable host
+    memory and its stream synchronisation are not allowed there, so the call
+    returns LOOKUP_DRAFT_ECUDA with the failing call named, and the capture ends
+    in an error.  Nothing was executed on the device; the next call is exact."""
+    lib = pkg.load_library()
+    w = gen.make_workload("tiny", 18)
+    assert_parity(w.tokens, w.offsets, w.min_m, w.max_m, w.K)       # device set up outside the capture
+    out_d = np.zeros(w.B * w.K, np.int32)
+    out_l, out_p = np.zeros(w.B, np.int32), np.zeros(w.B, np.int32)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    seen = []
+    with pytest.raises(Exception):
+        with torch.cuda.graph(g, stream=s):
+            rc = lib.lookup_draft_host(w.tokens.ctypes.data, w.offsets.ctypes.data, w.B, w.min_m, w.max_m, w.K,
+                                       out_d.ctypes.data, out_l.ctypes.data, out_p.ctypes.data,
+                                       torch.cuda.current_stream().cuda_stream)
+            seen.append((rc, lib.lookup_draft_last_cuda_error().decode()))
+    assert seen and seen[0][0] == -2, seen
+    assert "cuda" in seen[0][1], seen
+    del g
+    torch.cuda.synchronize()
+    assert_parity(w.tokens, w.offsets, w.min_m, w.max_m, w.K)

@@ -297,3 +297,24 @@ def test_draft_plan_rejects_bad_parameters(lib):
     assert call(a0=F + 2) == -1             # misaligned tokens
     assert lib.lookup_draft_plan(None, None, 0, 4, 12, None, None, 7, 8, 8, 6, 2, 4, 1, 2, 3, None, None, None, None,
                                  None, None, None, None) == 0
+
+
+def _gpu_present() -> bool:
+    try:
+        import torch
+        return bool(torch.cuda.is_available())
+    except Exception:  # pragma: no cover
+        return False
+
+
+@pytest.mark.skipif(_gpu_present(), reason="with a GPU the fake pointers would be launched on")
+def test_cuda_failure_is_reported_without_a_gpu(lib):
+    """With no usable device the first CUDA call of a valid-looking step fails: the
+    entry point returns LOOKUP_DRAFT_ECUDA and lookup_draft_last_cuda_error names
+    the call and the CUDA error."""
+    rc = lib.lookup_draft(FAKE, FAKE, 4, 4, 12, 15, FAKE, FAKE, FAKE, None)
+    assert rc == -2
+    msg = lib.lookup_draft_last_cuda_error().decode()
+    assert msg and "cuda" in msg.lower()
+    assert lib.lookup_draft_strerror(rc) == b"CUDA error"
+    assert lib.lookup_draft_noalloc(FAKE, FAKE, 4, 4, 12, 15, FAKE, FAKE, FAKE, None) == -2
