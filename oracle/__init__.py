@@ -7,7 +7,8 @@ ctypes:
                    tokens, its most recent earlier occurrence, overlap with the
                    suffix allowed, the following tokens as the draft);
   loop_oracle.c    the decode-loop steps around it ("第2步", "第3步");
-  ctx_oracle.c     context-cache drafting (llama.cpp prompt-lookup article).
+  ctx_oracle.c     context-cache drafting (llama.cpp prompt-lookup article);
+  policy_oracle.c  the draft-source controller (Strata engine article, section 五).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
 legs of ``bench.py`` may import this package.  The CUDA library never does, and
@@ -30,7 +31,7 @@ from concurrent.futures import ThreadPoolExecutor
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRCS = [os.path.join(_HERE, f) for f in ("lookup_oracle.c", "loop_oracle.c", "ctx_oracle.c")]
+_SRCS = [os.path.join(_HERE, f) for f in ("lookup_oracle.c", "loop_oracle.c", "ctx_oracle.c", "policy_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liblookup_oracle.so")
 
@@ -95,6 +96,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     if hasattr(lib, "oracle_ctx_draft"):
         lib.oracle_ctx_draft.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]
         lib.oracle_ctx_draft.restype = ctypes.c_int
+    if hasattr(lib, "oracle_policy"):
+        f32 = ctypes.c_float
+        lib.oracle_policy.argtypes = [vp, vp, i32, i32, i32, f32, f32, f32, f32, f32, i32, i32, i32, vp, vp, vp]
+        lib.oracle_policy.restype = ctypes.c_int
     return lib
 
 
@@ -212,6 +217,25 @@ def schedule(lookup_mlen, committed, state, H: int, T: int, tail_min: int = 4, s
                              _p(state), _p(out))
     if rc:
         raise ValueError("oracle_schedule rejected the arguments")
+    return out
+
+
+def policy(lookup_mlen, accepted, acc, prev, n_lookup: int, n_model: int, t_lookup: float, t_model: float,
+           t_plain: float, alpha: float = 0.125, margin: float = 0.05, edges=(6, 8, 12), lib=None):
+    """One step of the draft-source controller (Strata engine article, section 五);
+    ``acc`` float32 [B][5] and ``prev`` int32 [B][3] are updated in place.  Returns
+    the choice per request: 0 plain decoding, 1 the draft model, 2 the lookup draft."""
+    lib = lib or load()
+    lm = _arr(lookup_mlen, np.int32)
+    ac = _arr(accepted, np.int32)
+    assert acc.dtype == np.float32 and acc.flags["C_CONTIGUOUS"] and acc.shape == (lm.shape[0], 5)
+    assert prev.dtype == np.int32 and prev.flags["C_CONTIGUOUS"] and prev.shape == (lm.shape[0], 3)
+    B = lm.shape[0]
+    out = np.empty(B, np.int32)
+    rc = lib.oracle_policy(_p(lm), _p(ac), B, n_lookup, n_model, t_lookup, t_model, t_plain, alpha, margin,
+                           int(edges[0]), int(edges[1]), int(edges[2]), _p(acc), _p(prev), _p(out))
+    if rc:
+        raise ValueError("oracle_policy rejected the arguments")
     return out
 
 

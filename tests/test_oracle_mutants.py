@@ -219,3 +219,57 @@ def test_ctx_mutant_is_caught(name, tmp_path):
     subprocess.run(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", "-o", str(so_path), SRC, LOOP_SRC, str(c_path)],
                    check=True)
     assert _ctx_pins_fail(oracle.load(str(so_path))), f"mutant {name} passed every pin"
+
+
+# ------------------------------------------------------ controller oracle ----
+POLICY_SRC = os.path.join(os.path.dirname(oracle.__file__), "policy_oracle.c")
+
+POLICY_MUTANTS = {
+    "edge_strict": ("if (m >= edge[i])", "if (m > edge[i])"),
+    "margin_ignored": ("benefit_lookup > (1.0f + margin) * benefit_model", "benefit_lookup > benefit_model"),
+    "tie_goes_to_lookup": ("benefit_lookup > (1.0f + margin) * benefit_model",
+                           "benefit_lookup >= (1.0f + margin) * benefit_model"),
+    "no_bonus_token": ("float sum = 1.0f;", "float sum = 0.0f;"),
+    "weights_swapped": ("const float kept = (1.0f - alpha) * acc[slot];", "const float kept = alpha * acc[slot];"),
+    "update_wrong_bucket": ("const int32_t slot = last == 2 ? prev[1] : 4;",
+                            "const int32_t slot = last == 2 ? bucket_of(m, edge) : 4;"),
+    "model_update_to_lookup": ("const int32_t slot = last == 2 ? prev[1] : 4;",
+                               "const int32_t slot = last == 2 ? prev[1] : 0;"),
+    "no_plain_fallback": ("if (!(best > benefit_plain))", "if (0)"),
+    "no_clamp": ("if (a > n)\n            a = n;", ""),
+    "lookup_without_match": ("const int lookup_available = m > 0;", "const int lookup_available = 1;"),
+}
+
+
+def _policy_pins_fail(lib) -> list[str]:
+    import test_policy_oracle_pins as pins
+    failed = []
+    saved = oracle.load
+    oracle.load = lambda path=None: lib
+    try:
+        for name in dir(pins):
+            if name.startswith("test_"):
+                try:
+                    getattr(pins, name)()
+                except (AssertionError, ValueError, Exception):  # noqa: B014 - any failure counts
+                    failed.append(name)
+    finally:
+        oracle.load = saved
+    return failed
+
+
+def test_unmutated_policy_oracle_passes_its_pins():
+    assert _policy_pins_fail(oracle.load()) == []
+
+
+@pytest.mark.parametrize("name", sorted(POLICY_MUTANTS))
+def test_policy_mutant_is_caught(name, tmp_path):
+    old, new = POLICY_MUTANTS[name]
+    src = open(POLICY_SRC, encoding="utf-8").read()
+    assert src.count(old) >= 1, f"mutation target for {name} not found in the controller oracle"
+    c_path = tmp_path / "policy_mutant.c"
+    so_path = tmp_path / "libpolicymutant.so"
+    c_path.write_text(src.replace(old, new, 1), encoding="utf-8")
+    subprocess.run(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", "-o", str(so_path), SRC, LOOP_SRC, CTX_SRC,
+                    str(c_path)], check=True)
+    assert _policy_pins_fail(oracle.load(str(so_path))), f"mutant {name} passed every pin"
