@@ -645,6 +645,14 @@ def measure_loop(lib, pkg, w, dev, stream, toks, offs, reps: int) -> dict:
                               state.data_ptr(), long_block.data_ptr(), block.data_ptr(), blen.data_ptr(),
                               pm.data_ptr(), hs))
 
+    acc = torch.full((B, 5), 0.5, dtype=torch.float32, device=dev)
+    prev = torch.zeros((B, 3), dtype=i32, device=dev)
+    choice = torch.empty(B, dtype=i32, device=dev)
+
+    def policy(j, hs):                                   # the draft-source controller
+        check(lib.lookup_policy(mp, blen.data_ptr(), B, H, 3, 1.3, 1.1, 0.8, 0.125, 0.05, 6, 8, 12, acc.data_ptr(),
+                                prev.data_ptr(), choice.data_ptr(), hs))
+
     def verify_greedy(j, hs):
         check(lib.lookup_verify(block.data_ptr(), blen.data_ptr(), target.data_ptr(), None, None, None, None,
                                 B, P, accepted.data_ptr(), commit.data_ptr(), ncommit.data_ptr(), hs))
@@ -712,6 +720,7 @@ def measure_loop(lib, pkg, w, dev, stream, toks, offs, reps: int) -> dict:
         "fuse_us": timed(fuse),
         "schedule_us": timed(schedule),
         "plan_us": timed(plan),
+        "policy_us": timed(policy),
         "verify_greedy_us": timed(verify_greedy),
         "verify_sampled_us": timed(verify_sampled),
         "append_us": timed(append),

@@ -112,6 +112,47 @@ int lookup_plan(const int32_t *lookup_draft, const int32_t *lookup_mlen, const i
                 struct CUstream_st *stream);
 
 /*
+ * Draft-source controller (Strata engine article, gtnt.cn/news/124732, section
+ * 五): per request and step, choose 2 = the lookup draft, 1 = the draft model's
+ * draft, or 0 = plain decoding, by expected committed tokens per unit of verify
+ * time.  This is the Strata engine's online cost-benefit rule.  A caller that
+ * uses it with lookup_fuse passes lookup_mlen = 0 where the choice is not 2.
+ *
+ * lookup_mlen  int32 [B]: this step's lookup match length (0 = no match)
+ * accepted     int32 [B]: tokens accepted at the previous step from the draft of
+ *              the source chosen then (clamped to [0, the tokens it drafted])
+ * acc          float [B][5] in/out: EMA acceptance rate of the lookup draft per
+ *              match-length bucket (0..3), then of the model's draft; the caller
+ *              sets the priors
+ * prev         int32 [B][3] in/out: last choice, its bucket, tokens it drafted;
+ *              all zero initially
+ * out_choice   int32 [B]: 0, 1 or 2
+ * n_lookup, n_model     tokens each source drafts per step (>= 0)
+ * t_lookup, t_model     measured verify round time with each source's block (> 0)
+ * t_plain               measured plain decoding step time (> 0)
+ * alpha                 EMA weight of the newest rate, in [0, 1]
+ * margin                lookup needs more than (1 + margin) x the model's benefit (0.05)
+ * edge1 <= edge2 <= edge3   bucket of m = how many edges m reaches (6, 8, 12)
+ *
+ * Per request, in float32 with each operation rounded as written:
+ *   if prev choice c is 1 or 2 and it drafted n > 0 tokens:
+ *     rate = min(max(accepted, 0), n) / n;
+ *     slot = c == 2 ? prev bucket : 4;  acc[slot] = (1 - alpha) * acc[slot] + alpha * rate
+ *   E(a, n) = 1 + a + ... + a^n  (accepted run plus the target's own token)
+ *   model  = E(acc[4], n_model) / t_model
+ *   lookup = E(acc[bucket(m)], n_lookup) / t_lookup, only when m > 0
+ *   choice = 2 if lookup > (1 + margin) * model, else 1;
+ *            0 if the chosen source's value is not above 1 / t_plain
+ *   prev = {choice, its bucket (lookup) or 0, the tokens it drafts}
+ * Errors: LOOKUP_DRAFT_EINVAL for B < 0, negative n, non-positive times, alpha
+ * outside [0, 1], a negative margin, decreasing edges, or a null pointer with B > 0.
+ */
+int lookup_policy(const int32_t *lookup_mlen, const int32_t *accepted, int32_t B, int32_t n_lookup,
+                  int32_t n_model, float t_lookup, float t_model, float t_plain, float alpha, float margin,
+                  int32_t edge1, int32_t edge2, int32_t edge3, float *acc, int32_t *prev, int32_t *out_choice,
+                  struct CUstream_st *stream);
+
+/*
  * A draft step followed by lookup_plan, in two launches instead of four
  * (HyperQwen lookup-drafting article, sections "第1步", "第3步", "第2步").  The
  * scan is lookup_draft's; the second kernel reduces each request's scan results

@@ -28,7 +28,7 @@ __all__ = [
     "LookupDraftError", "load_library", "lookup_draft", "lookup_draft_ex", "lookup_draft_host",
     "lookup_draft_scan", "lookup_draft_fill", "lookup_draft_noalloc", "workspace_bytes",
     "set_wait_limit_ns", "lookup_fuse", "lookup_schedule", "lookup_plan", "lookup_draft_plan", "lookup_verify",
-    "lookup_append",
+    "lookup_append", "lookup_policy",
     "NgramIndex", "index_slots_for", "index_bytes", "lookup_index_build", "lookup_index_append",
     "lookup_index_draft", "ContextCache", "load_checked_library", "check_word",
     "MAX_M", "MAX_K", "LEN_FAILED", "CHECK_BITS",
@@ -153,6 +153,9 @@ def _declare_loop(lib: ctypes.CDLL) -> None:
     lib.lookup_draft_plan.argtypes = [vp, vp, i32, i32, i32, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                       vp, vp, vp, vp, vp, vp, vp, vp]
     lib.lookup_draft_plan.restype = ctypes.c_int
+    f32 = ctypes.c_float
+    lib.lookup_policy.argtypes = [vp, vp, i32, i32, i32, f32, f32, f32, f32, f32, i32, i32, i32, vp, vp, vp, vp]
+    lib.lookup_policy.restype = ctypes.c_int
     lib.lookup_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp]
     lib.lookup_verify.restype = ctypes.c_int
     lib.lookup_append.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp]
@@ -491,6 +494,29 @@ def lookup_draft_plan(tokens, offsets, model_draft, committed, state, min_m: int
                                    agree_n, tail_min, slack, enter_steps, sticky, sp, *optr, _stream_handle(stream))
     _check(rc, lib)
     return lng, block, ln, pm, ml, dl
+
+
+def lookup_policy(lookup_mlen, accepted, acc, prev, n_lookup: int, n_model: int, t_lookup: float, t_model: float,
+                  t_plain: float, alpha: float = 0.125, margin: float = 0.05, edges=(6, 8, 12), out=None,
+                  stream=None):
+    """Draft-source controller (Strata engine article, section 五): 0 plain decoding,
+    1 the draft model, 2 the lookup draft, per request.  ``acc`` (float32 [B, 5])
+    and ``prev`` (int32 [B, 3]) are updated in place.  Returns the choices [B]."""
+    import torch
+    lib = load_library()
+    dev = lookup_mlen.device
+    B = lookup_mlen.shape[0]
+    args = (_dev(lookup_mlen, torch.int32, (B,), dev, "lookup_mlen"), _dev(accepted, torch.int32, (B,), dev, "accepted"))
+    ap = _dev(acc, torch.float32, (B, 5), dev, "acc")
+    pp = _dev(prev, torch.int32, (B, 3), dev, "prev")
+    if out is None:
+        out = torch.empty(B, dtype=torch.int32, device=dev)
+    op = _dev(out, torch.int32, (B,), dev, "choice")
+    with torch.cuda.device(dev):
+        rc = lib.lookup_policy(*args, B, n_lookup, n_model, t_lookup, t_model, t_plain, alpha, margin,
+                               int(edges[0]), int(edges[1]), int(edges[2]), ap, pp, op, _stream_handle(stream))
+    _check(rc, lib)
+    return out
 
 
 def lookup_verify(block, length, target, probs=None, qprobs=None, point_mass=None, u=None,

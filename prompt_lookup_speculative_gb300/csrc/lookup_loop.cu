@@ -153,6 +153,74 @@ __global__ void plan_kernel(ScheduleParams sp, FuseParams fp) {
     if (lane == 0) fp.out_len[r] = tail ? W : fp.H;
 }
 
+// ---------------------------------------------------- draft-source controller ----
+// Strata engine article, gtnt.cn/news/124732, section 五: per request and step,
+// expected committed tokens per unit of verify time for the draft model's draft
+// and for the lookup draft; acceptance estimated online by an EMA, per
+// match-length bucket for the lookup draft; lookup only when it beats the model
+// by more than the margin; plain decoding when neither beats one token per
+// t_plain.  float32, each operation rounded as written (the intrinsics keep the
+// compiler from fusing them), so every choice is reproducible bit for bit.
+struct PolicyParams {
+    const int32_t *lookup_mlen;
+    const int32_t *accepted;
+    float *acc;                  // [B][5]: lookup acceptance per bucket, then the model's
+    int32_t *prev;               // [B][3]: last choice, its bucket, tokens it drafted
+    int32_t *out_choice;
+    int32_t B, n_lookup, n_model, edge1, edge2, edge3;
+    float t_lookup, t_model, t_plain, alpha, margin;
+};
+
+// 1 + a + a^2 + ... + a^n
+__device__ inline float expected_committed(float a, int32_t n) {
+    float sum = 1.0f, term = 1.0f;
+    for (int32_t i = 1; i <= n; ++i) {
+        term = __fmul_rn(term, a);
+        sum = __fadd_rn(sum, term);
+    }
+    return sum;
+}
+
+// One thread per request.
+__global__ void policy_kernel(PolicyParams p) {
+    wait_for_prerequisite_grid();
+    allow_dependent_launch();
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= p.B) return;
+    float *acc = p.acc + 5 * int64_t(r);
+    int32_t *prev = p.prev + 3 * int64_t(r);
+    // 1. the previous step's outcome updates the estimate of the source that drafted it
+    const int32_t last = prev[0], n = prev[2];
+    if ((last == 1 || last == 2) && n > 0) {
+        int32_t a = p.accepted[r];
+        a = a < 0 ? 0 : (a > n ? n : a);
+        const float rate = __fdiv_rn(__int2float_rn(a), __int2float_rn(n));
+        const int32_t slot = last == 2 ? prev[1] : 4;
+        const float kept = __fmul_rn(__fsub_rn(1.0f, p.alpha), acc[slot]);
+        const float added = __fmul_rn(p.alpha, rate);
+        acc[slot] = __fadd_rn(kept, added);
+    }
+    // 2. expected committed tokens per unit of verify time, per source
+    const int32_t m = p.lookup_mlen[r];
+    const int32_t b = int32_t(m >= p.edge1) + int32_t(m >= p.edge2) + int32_t(m >= p.edge3);
+    const bool avail = m > 0;
+    const float b_model = __fdiv_rn(expected_committed(acc[4], p.n_model), p.t_model);
+    const float b_lookup = avail ? __fdiv_rn(expected_committed(acc[b], p.n_lookup), p.t_lookup) : 0.0f;
+    const float b_plain = __fdiv_rn(1.0f, p.t_plain);
+    // 3. lookup only when it beats the model by more than the margin; 4. else plain
+    int32_t choice = 1;
+    float best = b_model;
+    if (avail && b_lookup > __fmul_rn(__fadd_rn(1.0f, p.margin), b_model)) {
+        choice = 2;
+        best = b_lookup;
+    }
+    if (!(best > b_plain)) choice = 0;
+    prev[0] = choice;
+    prev[1] = choice == 2 ? b : 0;
+    prev[2] = choice == 2 ? p.n_lookup : (choice == 1 ? p.n_model : 0);
+    p.out_choice[r] = choice;
+}
+
 // ------------------------------------------------------------ verification ----
 struct VerifyParams {
     const int32_t *block;
@@ -581,6 +649,21 @@ int lookup_plan(const int32_t *lookup_draft, const int32_t *lookup_mlen, const i
     FuseParams fp{lookup_draft, lookup_mlen, model_draft, out_long, out_block, out_len, out_point_mass,
                   B, K, H, T, replace_min, agree_min, agree_n, tail_min};
     return lkd::launch_pdl2(plan_kernel, blocks_for(B, kPlanWarps), unsigned(kPlanWarps * 32), stream, sp, fp);
+}
+
+int lookup_policy(const int32_t *lookup_mlen, const int32_t *accepted, int32_t B, int32_t n_lookup, int32_t n_model,
+                  float t_lookup, float t_model, float t_plain, float alpha, float margin, int32_t edge1,
+                  int32_t edge2, int32_t edge3, float *acc, int32_t *prev, int32_t *out_choice,
+                  struct CUstream_st *stream) {
+    lkd::TraceRange trace_("lookup_policy");
+    if (B < 0 || n_lookup < 0 || n_model < 0 || !(t_lookup > 0.0f) || !(t_model > 0.0f) || !(t_plain > 0.0f) ||
+        !(alpha >= 0.0f && alpha <= 1.0f) || !(margin >= 0.0f) || edge1 > edge2 || edge2 > edge3)
+        return LOOKUP_DRAFT_EINVAL;
+    if (B == 0) return LOOKUP_DRAFT_OK;
+    if (!lookup_mlen || !accepted || !acc || !prev || !out_choice) return LOOKUP_DRAFT_EINVAL;
+    PolicyParams p{lookup_mlen, accepted, acc, prev, out_choice, B, n_lookup, n_model, edge1, edge2, edge3,
+                   t_lookup, t_model, t_plain, alpha, margin};
+    return launch_pdl(policy_kernel, blocks_for(B, 256), 256u, stream, p);
 }
 
 int lookup_verify(const int32_t *block, const int32_t *len, const int32_t *target, const float *probs,

@@ -440,3 +440,34 @@ def test_draft_plan_block_shapes(H, T, agree_n):
     for nm, g, e in (("long", lg, lg_o), ("state", st_g, st_o), ("block", blk, blk_o), ("len", ln, len_o),
                      ("point mass", pm, pm_o), ("mlen", ml, m_o), ("draft len", dl, l_o)):
         np.testing.assert_array_equal(host(g), e, err_msg=nm)
+
+
+# ------------------------------------------------------ draft-source controller ----
+@pytest.mark.parametrize("B", [1, 7, 4096])
+@pytest.mark.parametrize("params", [
+    dict(n_lookup=7, n_model=3, t_lookup=1.3, t_model=1.1, t_plain=0.77, alpha=0.125, margin=0.05),
+    dict(n_lookup=15, n_model=3, t_lookup=2.9, t_model=1.0, t_plain=0.9, alpha=0.3, margin=0.0, edges=(5, 7, 9)),
+    dict(n_lookup=4, n_model=0, t_lookup=1.0, t_model=0.5, t_plain=0.4, alpha=1.0, margin=0.25, edges=(4, 4, 12)),
+])
+def test_policy_matches_oracle_bit_for_bit(B, params):
+    """lookup_policy over a 40-step trace with random match lengths, accepted counts
+    (some outside [0, drafted]) and priors: the choices, the integer state and
+    every float of the acceptance estimates equal the oracle's exactly."""
+    steps = 40
+    rng = gen.rng_for(B * 31 + len(params), 90)
+    acc_o = rng.uniform(0.0, 1.0, size=(B, 5)).astype(np.float32)
+    prev_o = np.zeros((B, 3), np.int32)
+    acc_g, prev_g = dev(acc_o.copy()), dev(prev_o.copy())
+    seen = set()
+    for s in range(steps):
+        m = np.where(rng.random(B) < 0.3, 0, rng.integers(3, 15, size=B)).astype(np.int32)
+        accepted = rng.integers(-1, 18, size=B).astype(np.int32)
+        want = oracle.policy(m, accepted, acc_o, prev_o, **params)
+        got = pkg.lookup_policy(dev(m), dev(accepted), acc_g, prev_g, **params)
+        np.testing.assert_array_equal(host(got), want, err_msg=f"choice, step {s}")
+        np.testing.assert_array_equal(host(prev_g), prev_o, err_msg=f"prev, step {s}")
+        a = host(acc_g)
+        assert np.array_equal(a.view(np.uint32), acc_o.view(np.uint32)), f"acceptance bits, step {s}"
+        seen.update(int(c) for c in want)
+    if B > 1:
+        assert len(seen) >= 2                        # the trace switches between choices

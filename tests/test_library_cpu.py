@@ -318,3 +318,24 @@ def test_cuda_failure_is_reported_without_a_gpu(lib):
     assert msg and "cuda" in msg.lower()
     assert lib.lookup_draft_strerror(rc) == b"CUDA error"
     assert lib.lookup_draft_noalloc(FAKE, FAKE, 4, 4, 12, 15, FAKE, FAKE, FAKE, None) == -2
+
+
+def test_policy_rejects_bad_parameters(lib):
+    F = FAKE
+    ok = [F, F, 4, 7, 3, 1.0, 1.0, 1.0, 0.125, 0.05, 6, 8, 12, F, F, F, None]
+
+    def call(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return lib.lookup_policy(*a)
+
+    assert call(a2=-1) == -1                # B < 0
+    assert call(a3=-1) == -1                # n_lookup < 0
+    assert call(a6=0.0) == -1               # t_model not positive
+    assert call(a7=-1.0) == -1              # t_plain negative
+    assert call(a8=1.5) == -1               # alpha above 1
+    assert call(a9=-0.1) == -1              # negative margin
+    assert call(a10=9) == -1                # edges decreasing
+    assert call(a13=None) == -1             # no acceptance state
+    assert lib.lookup_policy(None, None, 0, 7, 3, 1.0, 1.0, 1.0, 0.125, 0.05, 6, 8, 12, None, None, None, None) == 0
