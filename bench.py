@@ -650,7 +650,7 @@ def measure_loop(lib, pkg, w, dev, stream, toks, offs, reps: int) -> dict:
     choice = torch.empty(B, dtype=i32, device=dev)
 
     def policy(j, hs):                                   # the draft-source controller
-        check(lib.lookup_policy(mp, blen.data_ptr(), B, H, 3, 1.3, 1.1, 0.8, 0.125, 0.05, 6, 8, 12, acc.data_ptr(),
+        check(lib.lookup_policy(mp, accepted.data_ptr(), B, H, 3, 1.3, 1.1, 0.8, 0.125, 0.05, 6, 8, 12, acc.data_ptr(),
                                 prev.data_ptr(), choice.data_ptr(), hs))
 
     def verify_greedy(j, hs):
