@@ -181,7 +181,9 @@ __device__ inline float expected_committed(float a, int32_t n) {
     return sum;
 }
 
-// One thread per request.
+// One thread per request.  Its inputs, the five estimates included, are loaded in
+// one round; the update and the choice work on registers (unrolled selects, no
+// indexed local array), and the updated estimate is stored once.
 __global__ void policy_kernel(PolicyParams p) {
     wait_for_prerequisite_grid();
     allow_dependent_launch();
@@ -189,23 +191,38 @@ __global__ void policy_kernel(PolicyParams p) {
     if (r >= p.B) return;
     float *acc = p.acc + 5 * int64_t(r);
     int32_t *prev = p.prev + 3 * int64_t(r);
+    float e[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) e[i] = acc[i];
+    const int32_t last = prev[0], last_bucket = prev[1], n = prev[2];
+    const int32_t m = p.lookup_mlen[r];
+    int32_t a = p.accepted[r];
     // 1. the previous step's outcome updates the estimate of the source that drafted it
-    const int32_t last = prev[0], n = prev[2];
     if ((last == 1 || last == 2) && n > 0) {
-        int32_t a = p.accepted[r];
         a = a < 0 ? 0 : (a > n ? n : a);
         const float rate = __fdiv_rn(__int2float_rn(a), __int2float_rn(n));
-        const int32_t slot = last == 2 ? prev[1] : 4;
-        const float kept = __fmul_rn(__fsub_rn(1.0f, p.alpha), acc[slot]);
+        const int32_t slot = last == 2 ? last_bucket : 4;
+        float old = e[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (slot == i) old = e[i];
+        const float kept = __fmul_rn(__fsub_rn(1.0f, p.alpha), old);
         const float added = __fmul_rn(p.alpha, rate);
-        acc[slot] = __fadd_rn(kept, added);
+        const float upd = __fadd_rn(kept, added);
+#pragma unroll
+        for (int i = 0; i < 5; ++i)
+            if (slot == i) e[i] = upd;
+        acc[slot] = upd;
     }
     // 2. expected committed tokens per unit of verify time, per source
-    const int32_t m = p.lookup_mlen[r];
     const int32_t b = int32_t(m >= p.edge1) + int32_t(m >= p.edge2) + int32_t(m >= p.edge3);
+    float eb = e[0];
+#pragma unroll
+    for (int i = 1; i < 4; ++i)
+        if (b == i) eb = e[i];
     const bool avail = m > 0;
-    const float b_model = __fdiv_rn(expected_committed(acc[4], p.n_model), p.t_model);
-    const float b_lookup = avail ? __fdiv_rn(expected_committed(acc[b], p.n_lookup), p.t_lookup) : 0.0f;
+    const float b_model = __fdiv_rn(expected_committed(e[4], p.n_model), p.t_model);
+    const float b_lookup = avail ? __fdiv_rn(expected_committed(eb, p.n_lookup), p.t_lookup) : 0.0f;
     const float b_plain = __fdiv_rn(1.0f, p.t_plain);
     // 3. lookup only when it beats the model by more than the margin; 4. else plain
     int32_t choice = 1;
