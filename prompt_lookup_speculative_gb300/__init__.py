@@ -91,8 +91,22 @@ def load_checked_library() -> ctypes.CDLL:
                 raise RuntimeError(f"the checked CUDA library {path} is missing; run build() first")
             lib = ctypes.CDLL(path)
             _declare_draft(lib)
-            _checked_lib = lib
+            _checked_lib = _Declared(lib)
         return _checked_lib
+
+
+class _Declared:
+    """A library whose entry points can only be called once their argument types
+    are declared: ctypes would otherwise pass 64-bit pointers as 32-bit ints."""
+
+    def __init__(self, lib: ctypes.CDLL):
+        self._lib = lib
+
+    def __getattr__(self, name):
+        fn = getattr(self._lib, name)
+        if name.startswith("lookup_") and fn.argtypes is None:
+            raise AttributeError(f"{name}: no argument types declared for this library")
+        return fn
 
 
 def check_word(lib: ctypes.CDLL, clear: bool = False) -> int:
@@ -137,6 +151,10 @@ def _declare_draft(lib: ctypes.CDLL) -> None:
     lib.lookup_draft_checked_build.restype = ctypes.c_int
     lib.lookup_draft_check_word.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     lib.lookup_draft_check_word.restype = ctypes.c_int
+    # declared in lookup_loop.h, defined beside the draft step (so both builds export it)
+    lib.lookup_draft_plan.argtypes = [vp, vp, i32, i32, i32, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                      vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.lookup_draft_plan.restype = ctypes.c_int
 
 
 def _declare_loop(lib: ctypes.CDLL) -> None:
@@ -150,9 +168,6 @@ def _declare_loop(lib: ctypes.CDLL) -> None:
     lib.lookup_plan.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp,
                                 vp, vp, vp]
     lib.lookup_plan.restype = ctypes.c_int
-    lib.lookup_draft_plan.argtypes = [vp, vp, i32, i32, i32, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
-                                      vp, vp, vp, vp, vp, vp, vp, vp]
-    lib.lookup_draft_plan.restype = ctypes.c_int
     f32 = ctypes.c_float
     lib.lookup_policy.argtypes = [vp, vp, i32, i32, i32, f32, f32, f32, f32, f32, i32, i32, i32, vp, vp, vp, vp]
     lib.lookup_policy.restype = ctypes.c_int

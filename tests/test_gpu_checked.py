@@ -269,3 +269,42 @@ def test_check_word_reads_and_clears(lib):
     regular = pkg.load_library()
     assert regular.lookup_draft_checked_build() == 0
     assert regular.lookup_draft_check_word(ctypes.byref(out), 0) == 0 and out.value == 0
+
+
+def _draft_plan(lib, t, o, B, md, committed, H, T, min_m=4, max_m=12):
+    W = H + T
+    out = [torch.full(s, 7, dtype=torch.int32, device=DEV) for s in ((B,), (B, W), (B,), (B, W), (B,), (B,))]
+    state = torch.zeros((B, 3), dtype=torch.int32, device=DEV)
+    rc = lib.lookup_draft_plan(t.data_ptr(), o.data_ptr(), B, min_m, max_m, md.data_ptr(), committed.data_ptr(), H, T,
+                               8, 6, 2, 4, 1, 2, 3, state.data_ptr(), *(x.data_ptr() for x in out), _stream())
+    assert rc == 0, lib.lookup_draft_strerror(rc)
+    torch.cuda.synchronize()
+    return [x.cpu().numpy() for x in out] + [state.cpu().numpy()]
+
+
+@pytest.mark.parametrize("name", ["recitation25k", "chats"])
+def test_draft_plan_matches_the_regular_build_without_alarms(lib, name):
+    regular = pkg.load_library()
+    w = gen.make_workload(name, 24)
+    t, o = torch.from_numpy(w.tokens).to(DEV), torch.from_numpy(w.offsets).to(DEV)
+    H, T = 7, 8
+    rng = np.random.default_rng(5)
+    md = torch.from_numpy(rng.integers(0, 50, size=(w.B, H)).astype(np.int32)).to(DEV)
+    committed = torch.from_numpy(rng.integers(1, H + T + 2, size=w.B).astype(np.int32)).to(DEV)
+    got = _draft_plan(lib, t, o, w.B, md, committed, H, T)
+    want = _draft_plan(regular, t, o, w.B, md, committed, H, T)
+    for g, e in zip(got, want):
+        np.testing.assert_array_equal(g, e)
+    assert pkg.check_word(lib) == 0
+
+
+def test_draft_plan_with_decreasing_offsets_plans_every_request_as_failed(lib):
+    tokens, offsets = _decreasing_pair(1100, 77)
+    B, H, T = offsets.size - 1, 3, 2
+    t, o = torch.from_numpy(tokens).to(DEV), torch.from_numpy(offsets).to(DEV)
+    md = torch.full((B, H), 5, dtype=torch.int32, device=DEV)
+    committed = torch.ones(B, dtype=torch.int32, device=DEV)
+    lng, blk, ln, pm, ml, dl, st = _draft_plan(lib, t, o, B, md, committed, H, T)
+    assert np.all(dl == pkg.LEN_FAILED) and np.all(ml == 0)
+    assert np.all(blk[:, :H] == 5) and np.all(blk[:, H:] == -1) and np.all(ln == H) and np.all(pm == 0)
+    assert pkg.check_word(lib, clear=True) == OFFSETS_BIT

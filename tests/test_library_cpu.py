@@ -339,3 +339,15 @@ def test_policy_rejects_bad_parameters(lib):
     assert call(a10=9) == -1                # edges decreasing
     assert call(a13=None) == -1             # no acceptance state
     assert lib.lookup_policy(None, None, 0, 7, 3, 1.0, 1.0, 1.0, 0.125, 0.05, 6, 8, 12, None, None, None, None) == 0
+
+
+def test_binding_declares_argument_types_of_every_entry_point(lib, checked_lib):
+    """ctypes passes undeclared integer arguments as C ints: a 64-bit device
+    pointer would be cut to 32 bits.  Every function the headers declare has its
+    argument types set in the binding, for both builds."""
+    for name in sorted(declared_functions()):
+        assert getattr(lib, name).argtypes is not None, f"{name}: argument types not declared"
+    for name in sorted(declared_in("lookup_draft.h") | {"lookup_draft_plan"}):
+        assert getattr(checked_lib, name).argtypes is not None, f"checked {name}: argument types not declared"
+    with pytest.raises(AttributeError):
+        checked_lib.lookup_policy                       # not in the checked build at all
