@@ -7,7 +7,7 @@
 // extended by its own draft (e[L+j] = e[p+m+j]).  The exact contract is in
 // include/lookup_draft.h.
 //
-// Two kernels, both on the caller's stream:
+// A draft step is two kernels, both on the caller's stream:
 //
 //  scan_kernel -- the split-history scan, HBM bound (4 bytes per history token,
 //    read once).  The whole batch is one array of 16-byte quads; the grid (one CTA
@@ -31,18 +31,24 @@
 //    lanes' best keys across tiles and writes the warp's maximum into the
 //    (request, virtual chunk) slot when it moves on.
 //
-//  fill_kernel -- one warp per request: max over the request's slots, then the
-//    draft tokens t[p + m + (j mod d)], d = L - p - m, and the length/position.
+//  fill_kernel -- one warp per request (fill_lanes_kernel: one request per lane,
+//    for batches of 1,024 requests or more): max over the request's slots, then
+//    the draft tokens t[p + m + (j mod d)], d = L - p - m, and the length/position.
 //
-// Both kernels use programmatic dependent launch: each lets the next kernel on
+// fill_plan_kernel is the fill's warp going on with the decode loop's next two
+// steps, long-block scheduling and fusion (lookup_draft_plan).
+//
+// The kernels use programmatic dependent launch: each lets the next kernel on
 // the stream start its prologue early and waits for its predecessor's results
-// before reading them.
+// before reading them.  Compiled with LOOKUP_DRAFT_CHECKED=1, they also check
+// every index they compute (the checked build, below).
 //
 // Partial-result slots.  Virtual chunk v owns slot (r + v) for every non-empty
 // request r that has a token in its range.  Virtual chunks and requests are both
 // ordered and disjoint, so the (v, r) pairs form a monotone staircase and r + v
-// never repeats: every slot has one writer (one warp), needs no atomics, and no
-// clearing before a call (its warp zeroes it before use).
+// never repeats: every slot belongs to one warp, whose lanes fold their keys into
+// it with atomicMax (no other warp contends on it), and it needs no clearing
+// before a call (its warp zeroes it before use).
 //
 // No spin-wait is unbounded: every mbarrier wait gives up at a deadline.  A warp
 // that gives up lets its own copies land (bounded), marks its requests as failed
