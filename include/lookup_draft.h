@@ -88,7 +88,9 @@ struct CUstream_st;                     /* same type as cudaStream_t */
  * stream before destroying it if calls on it may still run, since a stream
  * created later may receive the same handle, and with it the same buffer.
  * Set-up: the first call on a device sets up per-device state.  Make it outside
- * stream capture.
+ * stream capture.  The first call on each stream (and one with a larger batch)
+ * allocates: while another thread captures a stream in global capture mode, an
+ * allocation may invalidate that capture, so make those calls first.
  * Errors: LOOKUP_DRAFT_EINVAL for null pointers (with B > 0), bad m range, K out of
  * range, or misaligned tokens/offsets; LOOKUP_DRAFT_ECUDA when an allocation or
  * launch fails.
