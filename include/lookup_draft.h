@@ -84,7 +84,8 @@ struct CUstream_st;                     /* same type as cudaStream_t */
  * pool instead (memory nodes in the graph).
  * A graph captured from calls on a stream uses that stream's buffer, as it uses
  * its fixed output buffers: replays of it must not overlap in time with other
- * calls on that stream.  Buffers are keyed by the stream handle: synchronise a
+ * calls on that stream.  Buffers are keyed by the stream handle (the per-thread
+ * default stream, cudaStreamPerThread, by the calling thread): synchronise a
  * stream before destroying it if calls on it may still run, since a stream
  * created later may receive the same handle, and with it the same buffer.
  * Set-up: the first call on a device sets up per-device state.  Make it outside

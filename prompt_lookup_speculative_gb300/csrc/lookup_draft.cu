@@ -1465,7 +1465,10 @@ thread_local LastScratch t_last;
 // The scratch of `stream` on device `dev`, holding at least `need` bytes; nullptr
 // (no error) when it has none and cannot make one now: the stream is capturing.
 int stream_scratch(int dev, cudaStream_t stream, size_t need, unsigned long long **out) {
-    const uintptr_t key = reinterpret_cast<uintptr_t>(stream);
+    // cudaStreamPerThread is one handle for a different stream in every thread:
+    // keyed by the calling thread instead (an address of its own, never a handle).
+    const uintptr_t key = stream == cudaStreamPerThread ? reinterpret_cast<uintptr_t>(&t_last) | 1u
+                                                        : reinterpret_cast<uintptr_t>(stream);
     if (t_last.dev == dev && t_last.stream == key && t_last.sc.bytes >= need) {
         *out = t_last.sc.slots;
         return LOOKUP_DRAFT_OK;

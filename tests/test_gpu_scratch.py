@@ -192,3 +192,38 @@ def test_threads_calling_on_their_own_and_shared_streams():
     for i, calls in enumerate(work):
         for j, (b, out) in enumerate(calls):
             b.check(out, f"thread {i}, call {j}")
+
+
+def test_per_thread_default_streams_get_their_own_scratch():
+    """cudaStreamPerThread names a different stream in each thread: two threads
+    passing that handle run concurrently and must not share one scratch buffer."""
+    import threading
+
+    lib = pkg.load_library()
+    per_thread = 2                                      # the cudaStreamPerThread handle
+    b1, b2 = Batch("recitation25k", 64), Batch("chats", 65)
+    work = [[(b1, b1.outputs()) for _ in range(8)], [(b2, b2.outputs()) for _ in range(8)]]
+    torch.cuda.synchronize()
+    errors = []
+
+    def run(calls):
+        try:
+            for b, (d, ln, p) in calls:
+                w = b.w
+                rc = lib.lookup_draft(b.t.data_ptr(), b.o.data_ptr(), w.B, w.min_m, w.max_m, w.K, d.data_ptr(),
+                                      ln.data_ptr(), p.data_ptr(), per_thread)
+                assert rc == 0, lib.lookup_draft_last_cuda_error()
+            torch.cuda.synchronize()
+        except Exception as exc:  # surfaced below
+            errors.append(exc)
+
+    threads = [threading.Thread(target=run, args=(calls,)) for calls in work]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for i, calls in enumerate(work):
+        for j, (b, out) in enumerate(calls):
+            b.check(out, f"thread {i}, call {j}")
