@@ -1,0 +1,124 @@
+"""Randomised parity sweeps of the drafting step against the oracle.
+
+Every case is drawn from a seeded generator, so a failure names a reproducible
+case.  A case mixes what the fixed tests take one at a time:
+- batch sizes from 1 to 6,000 requests (both fills, offsets in shared and in
+  global memory);
+- history lengths from empty through short (under min_m) to 60,000 tokens;
+- alphabets from 2 letters (dense matches, periodic text) to a Zipf vocabulary,
+  with some tokens replaced by INT32_MIN, INT32_MAX and negative values;
+- m ranges anywhere in [1, 32], K in [0, 64], every 4-byte phase of the tokens
+  pointer, and tokens before offsets[0] that belong to no request.
+Each case is compared element by element with the oracle: the draft, its
+length, the position and m.  The two-launch loop path (draft, then scheduling
+and fusion) is swept the same way against the oracle's draft, schedule and fuse.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import gen
+import oracle
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU machines too
+    pytestmark = [pytest.mark.gpu, pytest.mark.skip(reason="needs a CUDA GPU")]
+
+import prompt_lookup_speculative_gb300 as pkg  # noqa: E402
+
+DEV = "cuda:0"
+EXTREMES = np.array([np.iinfo(np.int32).min, np.iinfo(np.int32).max, -1, -7, 1 << 20], np.int32)
+
+
+def random_batch(rng: np.random.Generator):
+    """A seeded random batch: (tokens, offsets, min_m, max_m, K, pad)."""
+    B = int(np.exp(rng.uniform(0, np.log(6000))))
+    kind = rng.integers(0, 4)
+    if kind == 0:                                        # many short requests, some empty
+        lengths = rng.integers(0, 40, size=B)
+    elif kind == 1:                                      # log-uniform up to 60k
+        lengths = np.exp(rng.uniform(0, np.log(60000), size=B)).astype(np.int64)
+    elif kind == 2:                                      # a mixture with empties and near-min_m ones
+        lengths = rng.choice([0, 1, 2, 3, 4, 5, 13, 200, 3000], size=B)
+    else:                                                # equal lengths
+        lengths = np.full(B, int(rng.integers(1, 5000)))
+    budget = 3_000_000                                   # keep the oracle's work bounded
+    if lengths.sum() > budget:
+        lengths = (lengths * (budget / lengths.sum())).astype(np.int64)
+    n = int(lengths.sum())
+    alpha = int(rng.choice([2, 3, 5, 50, 32000]))
+    if alpha == 32000:
+        tokens = gen.zipf_tokens(rng, n, 32000, 1.1, rng.permutation(32000).astype(np.int32))
+    else:
+        tokens = rng.integers(0, alpha, size=n).astype(np.int32)
+    if n and rng.random() < 0.3:                         # extreme values sprinkled in
+        at = rng.integers(0, n, size=max(1, n // 50))
+        tokens[at] = EXTREMES[rng.integers(0, EXTREMES.size, size=at.size)]
+    lead = int(rng.integers(0, 10))
+    tokens = np.concatenate([rng.integers(0, 3, lead).astype(np.int32), tokens])
+    offsets = gen.offsets_from_lengths(lengths) + lead
+    min_m = int(rng.integers(1, 9))
+    max_m = int(rng.integers(min_m, 33))
+    K = int(rng.integers(0, 65))
+    pad = int(rng.integers(0, 4))
+    return tokens.astype(np.int32), offsets.astype(np.int64), min_m, max_m, K, pad
+
+
+def device_batch(tokens, offsets, pad):
+    buf = torch.zeros(tokens.size + pad + 4, dtype=torch.int32, device=DEV)
+    buf[pad:pad + tokens.size] = torch.from_numpy(tokens).to(DEV)
+    return buf[pad:pad + tokens.size], torch.from_numpy(offsets).to(DEV)
+
+
+@pytest.mark.parametrize("block", range(16))
+def test_draft_matches_oracle_on_random_batches(block):
+    """Sixteen blocks of 25 random cases each."""
+    rng = np.random.default_rng(20260 + block)
+    for case in range(25):
+        tokens, offsets, min_m, max_m, K, pad = random_batch(rng)
+        t, o = device_batch(tokens, offsets, pad)
+        d, ln, p, m = pkg.lookup_draft_ex(t, o, min_m, max_m, K)
+        torch.cuda.synchronize()
+        want = oracle.lookup_draft(tokens, offsets, min_m, max_m, K, threads=16)
+        label = (f"block {block} case {case}: B={offsets.size - 1} tokens={tokens.size} "
+                 f"m=[{min_m},{max_m}] K={K} pad={pad}")
+        for name, g, w in zip(("draft", "len", "pos", "mlen"), (d, ln, p, m), want):
+            np.testing.assert_array_equal(g.cpu().numpy(), w, err_msg=f"{label}: {name}")
+
+
+@pytest.mark.parametrize("block", range(6))
+def test_draft_plan_matches_oracle_on_random_batches(block):
+    """lookup_draft_plan on random batches, block shapes and thresholds, against
+    the oracle's draft (K = H + T), schedule and fuse."""
+    rng = np.random.default_rng(30260 + block)
+    for case in range(25):
+        tokens, offsets, min_m, max_m, _, pad = random_batch(rng)
+        B = offsets.size - 1
+        H = int(rng.integers(1, 33))
+        T = int(rng.integers(0, 65 - H))
+        agree_n = int(rng.integers(0, H + 1))
+        kw = dict(replace_min=int(rng.integers(1, 13)), agree_min=int(rng.integers(1, 13)), agree_n=agree_n,
+                  tail_min=int(rng.integers(1, 13)), slack=int(rng.integers(0, 4)),
+                  enter_steps=int(rng.integers(1, 4)), sticky=int(rng.integers(0, 5)))
+        d_o, l_o, p_o, m_o = oracle.lookup_draft(tokens, offsets, min_m, max_m, H + T, threads=16)
+        md = rng.integers(-2, 4, size=(B, H)).astype(np.int32)
+        take = rng.random(B) < 0.5
+        md[take] = d_o[take, :H]
+        committed = rng.integers(1, H + T + 2, size=B).astype(np.int32)
+        state = np.stack([rng.integers(0, 2, B), rng.integers(0, 3, B), rng.integers(0, 4, B)], 1).astype(np.int32)
+        st_o = state.copy()
+        lg_o = oracle.schedule(m_o, committed, st_o, H, T, tail_min=kw["tail_min"], slack=kw["slack"],
+                               enter_steps=kw["enter_steps"], sticky=kw["sticky"])
+        blk_o, len_o, pm_o = oracle.fuse(d_o, m_o, md, lg_o, H, T, replace_min=kw["replace_min"],
+                                         agree_min=kw["agree_min"], agree_n=agree_n, tail_min=kw["tail_min"])
+        t, o = device_batch(tokens, offsets, pad)
+        st_g = torch.from_numpy(state.copy()).to(DEV)
+        got = pkg.lookup_draft_plan(t, o, torch.from_numpy(md).to(DEV), torch.from_numpy(committed).to(DEV), st_g,
+                                    min_m, max_m, H, T, **kw)
+        torch.cuda.synchronize()
+        label = f"block {block} case {case}: B={B} m=[{min_m},{max_m}] H={H} T={T} {kw}"
+        for name, g, w in zip(("long", "block", "len", "point mass", "mlen", "draft len", "state"),
+                              (*got, st_g), (lg_o, blk_o, len_o, pm_o, m_o, l_o, st_o)):
+            np.testing.assert_array_equal(g.cpu().numpy(), w, err_msg=f"{label}: {name}")
