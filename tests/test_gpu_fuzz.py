@@ -11,7 +11,9 @@ case.  A case mixes what the fixed tests take one at a time:
   pointer, and tokens before offsets[0] that belong to no request.
 Each case is compared element by element with the oracle: the draft, its
 length, the position and m.  The two-launch loop path (draft, then scheduling
-and fusion) is swept the same way against the oracle's draft, schedule and fuse.
+and fusion) is swept the same way against the oracle's draft, schedule and fuse,
+and the incremental index and the context cache over random 3-step decode loops
+(draft, commit, append in place).
 """
 from __future__ import annotations
 
@@ -122,3 +124,93 @@ def test_draft_plan_matches_oracle_on_random_batches(block):
         for name, g, w in zip(("long", "block", "len", "point mass", "mlen", "draft len", "state"),
                               (*got, st_g), (lg_o, blk_o, len_o, pm_o, m_o, l_o, st_o)):
             np.testing.assert_array_equal(g.cpu().numpy(), w, err_msg=f"{label}: {name}")
+
+
+def small_random_batch(rng: np.random.Generator):
+    """A random batch kept small enough for the slab structures' memory: up to
+    400 requests of up to 20,000 tokens, about 400k tokens at most."""
+    B = int(np.exp(rng.uniform(0, np.log(400))))
+    lengths = np.where(rng.random(B) < 0.2, rng.integers(0, 6, size=B),
+                       np.exp(rng.uniform(0, np.log(20000), size=B)).astype(np.int64))
+    if lengths.sum() > 400_000:
+        lengths = (lengths * (400_000 / lengths.sum())).astype(np.int64)
+    n = int(lengths.sum())
+    alpha = int(rng.choice([2, 3, 7, 50, 32000]))
+    tokens = rng.integers(0, alpha, size=n).astype(np.int32)
+    if n and rng.random() < 0.3:
+        at = rng.integers(0, n, size=max(1, n // 50))
+        tokens[at] = EXTREMES[rng.integers(0, EXTREMES.size, size=at.size)]
+    return tokens, gen.offsets_from_lengths(lengths).astype(np.int64)
+
+
+def _commit(rng, draft, length, B, W, K):
+    """A synthetic continuation: an accepted prefix of the draft, then one more token."""
+    acc = np.minimum(rng.integers(0, W, size=B), np.where(length > 0, K, 0))
+    commit = rng.integers(-3, 50, size=(B, W)).astype(np.int32)
+    for r in range(B):
+        commit[r, :acc[r]] = draft[r, :acc[r]]
+    return commit, (acc + 1).astype(np.int32)
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_index_matches_oracle_on_random_decode_loops(case):
+    rng = np.random.default_rng(40260 + case)
+    tokens, offsets = small_random_batch(rng)
+    B = offsets.size - 1
+    min_m = int(rng.integers(1, 7))
+    max_m = int(rng.integers(min_m, 33))
+    K = int(rng.integers(0, 65))
+    W = 16
+    st, base, length, cap = gen.slabs_from_batch(tokens, offsets, 4 * W, seed=case)
+    t, b, n = (torch.from_numpy(np.ascontiguousarray(a)).to(DEV) for a in (st, base, length))
+    capd = torch.from_numpy(cap).to(DEV)
+    idx = pkg.NgramIndex(st.shape[0], min_m, max_m)
+    idx.build(t, b, n)
+    cur_t, cur_o = tokens, offsets
+    for step in range(3):
+        d, ln, p, m = idx.draft(t, b, n, K)[:4]
+        want = oracle.lookup_draft(cur_t, cur_o, min_m, max_m, K, threads=16)
+        label = f"case {case} step {step}: B={B} m=[{min_m},{max_m}] K={K}"
+        for name, g, w in zip(("draft", "len", "pos", "mlen"), (d, ln, p, m), want):
+            np.testing.assert_array_equal(g.cpu().numpy(), w, err_msg=f"{label}: {name}")
+        commit, ncommit = _commit(rng, want[0], want[1], B, W, K)
+        status = idx.append(t, b, n, capd, torch.from_numpy(commit).to(DEV), torch.from_numpy(ncommit).to(DEV))
+        assert (status.cpu().numpy() == 0).all(), label
+        cur_t, cur_o = oracle.append(cur_t, cur_o, commit, ncommit)
+        got_t, got_o = gen.csr_of_slabs(t.cpu().numpy(), base, n.cpu().numpy())
+        np.testing.assert_array_equal(got_o, cur_o, err_msg=label)
+        np.testing.assert_array_equal(got_t, cur_t, err_msg=label)
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_context_cache_matches_oracle_on_random_decode_loops(case):
+    rng = np.random.default_rng(50260 + case)
+    tokens, offsets = small_random_batch(rng)
+    B = offsets.size - 1
+    n_min = int(rng.integers(1, 5))
+    n_max = int(rng.integers(n_min, 5))
+    min_count = tuple(int(x) for x in rng.integers(1, 4, size=4))
+    share = tuple((int(a), int(a) + int(c)) for a, c in zip(rng.integers(1, 3, size=4), rng.integers(0, 4, size=4)))
+    K = int(rng.integers(1, 13))
+    W = 9
+    st, base, length, cap = gen.slabs_from_batch(tokens, offsets, 4 * W, seed=case)
+    t, b, n = (torch.from_numpy(np.ascontiguousarray(a)).to(DEV) for a in (st, base, length))
+    capd = torch.from_numpy(cap).to(DEV)
+    cc = pkg.ContextCache(st.shape[0], n_min, n_max, min_count=min_count, share=share)
+    cc.build(t, b, n)
+    cur_t, cur_o = tokens, offsets
+    for step in range(3):
+        d, ln = cc.draft(t, b, n, K)
+        wd, wl = oracle.ctx_draft(cur_t, cur_o, K, n_min=n_min, n_max=n_max, min_count=min_count, share=share,
+                                  threads=16)
+        label = f"case {case} step {step}: B={B} n=[{n_min},{n_max}] K={K} {min_count} {share}"
+        np.testing.assert_array_equal(ln.cpu().numpy(), wl, err_msg=f"{label}: len")
+        np.testing.assert_array_equal(d.cpu().numpy(), wd, err_msg=f"{label}: draft")
+        acc = np.minimum(np.minimum(rng.integers(0, K + 1, size=B), wl), W - 1)   # the row holds W tokens
+        commit = rng.integers(-3, 50, size=(B, W)).astype(np.int32)
+        for r in range(B):
+            commit[r, :acc[r]] = wd[r, :acc[r]]
+        ncommit = (acc + 1).astype(np.int32)
+        status = cc.append(t, b, n, capd, torch.from_numpy(commit).to(DEV), torch.from_numpy(ncommit).to(DEV))
+        assert (status.cpu().numpy() == 0).all(), label
+        cur_t, cur_o = oracle.append(cur_t, cur_o, commit, ncommit)
