@@ -320,8 +320,13 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                 step(i, hc)
         return g
 
+    # the library counts the launches it enqueues; a capture enqueues each once
+    n0 = lib.lookup_draft_launch_count()
     g_full = capture(ncopy)
+    n1 = lib.lookup_draft_launch_count()
     g_tail = capture(tail) if tail else None
+    n2 = lib.lookup_draft_launch_count()
+    timed_launches = int((n1 - n0) * full_reps + (n2 - n1))
     clock_hz = float(getattr(torch.cuda.get_device_properties(dev), "clock_rate", 2_000_000)) * 1000.0
     with torch.cuda.stream(stream):
         for _ in range(3):                           # first launches upload the graphs
@@ -556,7 +561,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         "index": index,
         "context_cache": ctx,
         "workloads": workloads,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": timed_launches,
         "parity_with_oracle": bool(parity),
         "clocks": clocks.summary(),
         "gpu": torch.cuda.get_device_name(dev),
@@ -694,16 +699,20 @@ def measure_loop(lib, pkg, w, dev, stream, toks, offs, reps: int) -> dict:
         append(j, hs)
 
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = {}                                        # kernels per call, counted by the library at capture
 
     def timed(fn) -> float:
         with torch.cuda.stream(stream):
             for j in range(ncopy):                      # eager warm-up
                 fn(j, int(stream.cuda_stream))
         g = torch.cuda.CUDAGraph()
+        c0 = lib.lookup_draft_launch_count()
         with torch.cuda.graph(g, stream=stream):
             hc = int(torch.cuda.current_stream().cuda_stream)
             for j in range(ncopy):
                 fn(j, hc)
+        n = lib.lookup_draft_launch_count() - c0
+        launches[fn.__name__] = n // ncopy if n % ncopy == 0 else n / ncopy
         with torch.cuda.stream(stream):
             for _ in range(3):
                 g.replay()
@@ -736,9 +745,8 @@ def measure_loop(lib, pkg, w, dev, stream, toks, offs, reps: int) -> dict:
     res = {k: (round(v, 3) if isinstance(v, float) else v) for k, v in res.items()}
     res["append_algorithmic_bytes"] = append_bytes
     res["append_gbs"] = round(append_bytes / (res["append_us"] * 1e-6) / 1e9, 1)
-    res["loop_step_launches"] = 2 + 1 + 1 + 1 + 2
-    res["loop_step_plan_launches"] = 2 + 1 + 1 + 2
-    res["loop_step_draft_plan_launches"] = 2 + 1 + 2
+    for name in ("loop_step", "loop_step_plan", "loop_step_draft_plan", "draft_plan", "append"):
+        res[f"{name}_launches"] = launches[name]
     res["method"] = (f"each call captured {ncopy}x back to back in a CUDA graph over rotating input copies, "
                      f"{reps} replays, CUDA events on the launching stream")
     return res
@@ -806,12 +814,17 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
         check(lib.lookup_index_draft(tp, bp, lp, B, w.min_m, w.max_m, k, mem, idx.slots, 64, draft.data_ptr(),
                                      dl.data_ptr(), dp.data_ptr(), dm.data_ptr(), None, h))
 
+    launches = {}                                        # kernels per call, counted by the library at capture
+
     def timed(fn, per_graph: int, reps: int) -> float:
         g = torch.cuda.CUDAGraph()
+        c0 = lib.lookup_draft_launch_count()
         with torch.cuda.graph(g, stream=stream):
             hc = int(torch.cuda.current_stream().cuda_stream)
             for _ in range(per_graph):
                 fn(hc)
+        n = lib.lookup_draft_launch_count() - c0
+        launches[fn.__name__] = n // per_graph if n % per_graph == 0 else n / per_graph
         with torch.cuda.stream(stream):
             g.replay()
             ev0.record(stream)
@@ -863,6 +876,31 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
     loop_us = timed(loop_call, 16, 4)                     # 80 steps: at most 1280 tokens of room
     torch.cuda.synchronize(dev)
     room_ok = bool((status == 0).all().item())
+
+    # the same step with the draft, scheduling and fusion in one launch
+    # (lookup_index_draft_plan), from the original histories: lengths restored and
+    # the index rebuilt (untimed), so the appends have the same room again
+    length.copy_(torch.from_numpy(len_h))
+    state.zero_()
+    with torch.cuda.stream(stream):
+        idx.build(tokens, base, length, stream=stream)
+    torch.cuda.synchronize(dev)
+    dlen = torch.empty(B, dtype=i32, device=dev)
+    fb = torch.empty(B, dtype=i32, device=dev)
+
+    def loop_plan_call(h):
+        check(lib.lookup_index_draft_plan(tp, bp, lp, B, w.min_m, w.max_m, mem, idx.slots, 64,
+                                          model_draft.data_ptr(), committed.data_ptr(), H, T, 8, 6, 2, 4, 1, 2, 3,
+                                          state.data_ptr(), long_block.data_ptr(), block.data_ptr(), blen.data_ptr(),
+                                          pm.data_ptr(), dm.data_ptr(), dlen.data_ptr(), fb.data_ptr(), h))
+        check(lib.lookup_verify(block.data_ptr(), blen.data_ptr(), target.data_ptr(), None, None, None, None, B, P,
+                                accepted.data_ptr(), commit.data_ptr(), ncommit.data_ptr(), h))
+        check(lib.lookup_index_append(tp, bp, lp, cp, commit.data_ptr(), ncommit.data_ptr(), B, P + 1, w.min_m,
+                                      w.max_m, mem, idx.slots, 64, status.data_ptr(), h))
+
+    loop_plan_us = timed(loop_plan_call, 16, 4)           # 80 steps again
+    torch.cuda.synchronize(dev)
+    room_ok = room_ok and bool((status == 0).all().item())
     total_tokens = int(st.shape[0])
     res = {
         "layout": f"slabs with {INDEX_SPARE} tokens of room per request",
@@ -873,7 +911,11 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
         "draft_us": round(draft_us, 3),
         "append8_us": round(append_us, 3),
         "loop_step_us": round(loop_us, 3),
-        "loop_step_launches": 6,
+        "loop_step_launches": launches["loop_call"],
+        "loop_step_plan_us": round(loop_plan_us, 3),
+        "loop_step_plan_launches": launches["loop_plan_call"],
+        "draft_launches": launches["draft_call"],
+        "append8_launches": launches["append_call"],
         "parity_with_oracle": bool(parity),
         "fallback_requests": fallbacks,
         "appends_fit": room_ok,

@@ -203,6 +203,14 @@ const char *lookup_draft_strerror(int code);
  * ("" if none).  Valid until that thread's next call into the library. */
 const char *lookup_draft_last_cuda_error(void);
 
+/* Number of kernel launches this library has enqueued since it was loaded, on
+ * every thread and stream (successful launches only; a failed call may have
+ * enqueued some of its launches before the failure).  Inside a stream capture a
+ * launch becomes a graph node and counts once, when it is captured: replays of
+ * the graph are not counted.  The difference across a capture is the number of
+ * kernels each replay runs.  Never fails; needs no GPU. */
+uint64_t lookup_draft_launch_count(void);
+
 /*
  * Diagnostics: the time limit, in nanoseconds, on the scan kernel's bounded waits
  * (default 1e9), counted from each scan CTA's start.  A CTA whose wait for the

@@ -101,6 +101,31 @@ int lookup_index_draft(const int32_t *tokens, const int64_t *base, const int32_t
                        int32_t hash_bits, int32_t *out_draft, int32_t *out_len, int32_t *out_pos,
                        int32_t *out_mlen, int32_t *out_fallback, struct CUstream_st *stream);
 
+/*
+ * lookup_index_draft followed by lookup_plan (include/lookup_loop.h), in one
+ * launch: each request's warp answers the index query (K = H + T), keeps the
+ * draft tokens in registers and applies the scheduling and fusion rules of
+ * HyperQwen lookup-drafting article sections "第3步" and "第2步" to them.  The
+ * draft itself is not written.
+ *
+ * tokens, base, len, B, min_m, max_m, index, slots, hash_bits   as for lookup_index_draft
+ * model_draft, committed, H, T, replace_min, agree_min, agree_n, tail_min,
+ * slack, enter_steps, sticky, state, out_long, out_block, out_len,
+ * out_point_mass     as for lookup_plan; H + T <= LOOKUP_DRAFT_MAX_K
+ * out_mlen, out_draft_len, out_fallback   int32 [B] or NULL: m, the length
+ *                    lookup_index_draft would report, and its fallback flag
+ * Every output equals lookup_index_draft (K = H + T) followed by lookup_plan.
+ * Errors: those of the two calls.
+ */
+int lookup_index_draft_plan(const int32_t *tokens, const int64_t *base, const int32_t *len, int32_t B,
+                            int32_t min_m, int32_t max_m, const void *index, int64_t slots, int32_t hash_bits,
+                            const int32_t *model_draft, const int32_t *committed, int32_t H, int32_t T,
+                            int32_t replace_min, int32_t agree_min, int32_t agree_n, int32_t tail_min,
+                            int32_t slack, int32_t enter_steps, int32_t sticky, int32_t *state,
+                            int32_t *out_long, int32_t *out_block, int32_t *out_len, int32_t *out_point_mass,
+                            int32_t *out_mlen, int32_t *out_draft_len, int32_t *out_fallback,
+                            struct CUstream_st *stream);
+
 #ifdef __cplusplus
 }
 #endif

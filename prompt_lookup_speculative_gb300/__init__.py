@@ -30,7 +30,8 @@ __all__ = [
     "set_wait_limit_ns", "lookup_fuse", "lookup_schedule", "lookup_plan", "lookup_draft_plan", "lookup_verify",
     "lookup_append", "lookup_policy",
     "NgramIndex", "index_slots_for", "index_bytes", "lookup_index_build", "lookup_index_append",
-    "lookup_index_draft", "ContextCache", "load_checked_library", "check_word",
+    "lookup_index_draft", "lookup_index_draft_plan", "ContextCache", "load_checked_library", "check_word",
+    "launch_count",
     "MAX_M", "MAX_K", "LEN_FAILED", "CHECK_BITS",
 ]
 
@@ -117,6 +118,12 @@ def check_word(lib: ctypes.CDLL, clear: bool = False) -> int:
     return int(out.value)
 
 
+def launch_count(lib: ctypes.CDLL | None = None) -> int:
+    """Kernel launches the library has enqueued since it was loaded (a capture
+    counts each captured launch once; replays are not counted)."""
+    return int((lib or load_library()).lookup_draft_launch_count())
+
+
 def _declare(lib: ctypes.CDLL) -> None:
     _declare_draft(lib)
     _declare_loop(lib)
@@ -143,6 +150,8 @@ def _declare_draft(lib: ctypes.CDLL) -> None:
     lib.lookup_draft_strerror.restype = ctypes.c_char_p
     lib.lookup_draft_last_cuda_error.argtypes = []
     lib.lookup_draft_last_cuda_error.restype = ctypes.c_char_p
+    lib.lookup_draft_launch_count.argtypes = []
+    lib.lookup_draft_launch_count.restype = ctypes.c_uint64
     lib.lookup_draft_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.lookup_draft_set_wait_limit_ns.restype = None
     lib.lookup_draft_read_floor.argtypes = [vp, sz, i32, i32, vp, vp]
@@ -186,6 +195,9 @@ def _declare_loop(lib: ctypes.CDLL) -> None:
     lib.lookup_index_append.restype = ctypes.c_int
     lib.lookup_index_draft.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, i64, i32, vp, vp, vp, vp, vp, vp]
     lib.lookup_index_draft.restype = ctypes.c_int
+    lib.lookup_index_draft_plan.argtypes = [vp, vp, vp, i32, i32, i32, vp, i64, i32, vp, vp, i32, i32, i32, i32, i32,
+                                            i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.lookup_index_draft_plan.restype = ctypes.c_int
     lib.lookup_ctx_slots_for.argtypes = [i64, i32, i32]
     lib.lookup_ctx_slots_for.restype = i64
     lib.lookup_ctx_bytes.argtypes = [i64]
@@ -676,6 +688,33 @@ def lookup_index_draft(tokens, base, length, min_m: int, max_m: int, K: int, ind
     return (draft, ln, pos, mlen, fb) if with_fallback else (draft, ln, pos, mlen)
 
 
+def lookup_index_draft_plan(tokens, base, length, min_m: int, max_m: int, index, slots: int, model_draft, committed,
+                            state, H: int = 7, T: int = 8, replace_min: int = 8, agree_min: int = 6, agree_n: int = 2,
+                            tail_min: int = 4, slack: int = 1, enter_steps: int = 2, sticky: int = 3,
+                            hash_bits: int = 64, out=None, stream=None):
+    """lookup_index_draft (K = H + T) followed by lookup_plan, in one launch;
+    ``state`` (int32 [B, 3]) is updated in place.  Returns (long, block, len,
+    point_mass, mlen, draft_len, fallback)."""
+    import torch
+    lib = load_library()
+    dev, B, (bp, lp) = _slab_args(tokens, base, length)
+    W = H + T
+    args = (_dev(model_draft, torch.int32, (B, H), dev, "model_draft"),
+            _dev(committed, torch.int32, (B,), dev, "committed"))
+    sp = _dev(state, torch.int32, (B, 3), dev, "state")
+    shapes = ((B,), (B, W), (B,), (B, W), (B,), (B,), (B,))
+    if out is None:
+        out = tuple(torch.empty(sh, dtype=torch.int32, device=dev) for sh in shapes)
+    names = ("long", "block", "len", "point_mass", "mlen", "draft_len", "fallback")
+    optr = tuple(_dev(t, torch.int32, sh, dev, nm) for t, sh, nm in zip(out, shapes, names))
+    with torch.cuda.device(dev):
+        rc = lib.lookup_index_draft_plan(tokens.data_ptr(), bp, lp, B, min_m, max_m, index.data_ptr(), int(slots),
+                                         hash_bits, *args, H, T, replace_min, agree_min, agree_n, tail_min, slack,
+                                         enter_steps, sticky, sp, *optr, _stream_handle(stream))
+    _check(rc, lib)
+    return out
+
+
 class NgramIndex:
     """A device-resident n-gram index over slab histories (include/lookup_index.h).
 
@@ -698,6 +737,14 @@ class NgramIndex:
     def append(self, tokens, base, length, cap, commit, ncommit, status=None, stream=None):
         return lookup_index_append(tokens, base, length, cap, commit, ncommit, self.min_m, self.max_m,
                                    self.memory, self.slots, self.hash_bits, status, stream)
+
+    def draft_plan(self, tokens, base, length, model_draft, committed, state, H: int = 7, T: int = 8, stream=None,
+                   **rules):
+        """The draft from the index, then scheduling and fusion, in one launch
+        (lookup_index_draft_plan)."""
+        return lookup_index_draft_plan(tokens, base, length, self.min_m, self.max_m, self.memory, self.slots,
+                                       model_draft, committed, state, H, T, hash_bits=self.hash_bits, stream=stream,
+                                       **rules)
 
     def draft(self, tokens, base, length, K: int = 15, out=None, with_fallback: bool = False, stream=None):
         return lookup_index_draft(tokens, base, length, self.min_m, self.max_m, K, self.memory, self.slots,

@@ -13,6 +13,8 @@
 // Records a CUDA failure for lookup_draft_last_cuda_error (lookup_draft.cu);
 // returns LOOKUP_DRAFT_ECUDA.
 int lookup_record_cuda_error(cudaError_t e, const char *what);
+// Counts one enqueued kernel launch (lookup_draft_launch_count, lookup_draft.cu).
+void lookup_note_launch();
 
 namespace lkd {
 
@@ -61,6 +63,60 @@ __device__ inline void fuse_choice(int32_t i, int32_t H, bool head_lookup, bool 
     }
 }
 
+// The decode loop's scheduling and fusion for one request, in the warp that holds
+// its lookup draft: lanes hold draft tokens j = lane and lane + 32 (-1 without a
+// match), m is the match length (0 without one), W = H + T <= 64.  Every lane
+// reads the old state and applies the rule, the warp synchronises, lane 0 writes
+// the new state, the long flag and the block length, and the lanes write the
+// block's positions: lookup_schedule then lookup_fuse, for that request.
+struct PlanIO {
+    const int32_t *model_draft;   // [B][H]
+    const int32_t *committed;     // [B]
+    int32_t *state;               // [B][3] in/out
+    int32_t *out_long;
+    int32_t *out_block;           // [B][H + T]
+    int32_t *out_len;
+    int32_t *out_pm;              // [B][H + T]
+    int32_t H, T, replace_min, agree_min, agree_n, tail_min, slack, enter_steps, sticky;
+};
+
+__device__ inline void plan_warp(const PlanIO &pa, int r, int lane, int32_t m, int32_t tok0, int32_t tok1) {
+    const int W = pa.H + pa.T;
+    const int j1 = lane + 32;
+    // head rule: the model agrees with the draft's first agree_n tokens
+    const int32_t *md = pa.model_draft + int64_t(r) * pa.H;
+    const int32_t md0 = lane < pa.H ? md[lane] : -1, md1 = j1 < pa.H ? md[j1] : -1;
+    const bool ne = (lane < pa.agree_n && tok0 != md0) || (j1 < pa.agree_n && tok1 != md1);
+    const bool agree = __all_sync(0xffffffffu, !ne);
+    const bool head = m >= pa.replace_min || (m >= pa.agree_min && agree);
+    // scheduling: every lane reads the old state, then lane 0 writes the new one
+    int32_t *st = pa.state + 3 * int64_t(r);
+    int32_t lng = st[0], streak = st[1], hold = st[2];
+    schedule_update(m, pa.committed[r], pa.H, pa.T, pa.tail_min, pa.slack, pa.enter_steps, pa.sticky, lng, streak,
+                    hold);
+    __syncwarp();
+    const bool tail = lng != 0 && m >= pa.tail_min;
+    if (lane == 0) {
+        st[0] = lng;
+        st[1] = streak;
+        st[2] = hold;
+        pa.out_long[r] = lng;
+        pa.out_len[r] = tail ? W : pa.H;
+    }
+    // fusion of the block's positions
+    int32_t v, pm;
+    if (lane < W) {
+        fuse_choice(lane, pa.H, head, tail, tok0, md0, v, pm);
+        pa.out_block[int64_t(r) * W + lane] = v;
+        pa.out_pm[int64_t(r) * W + lane] = pm;
+    }
+    if (j1 < W) {
+        fuse_choice(j1, pa.H, head, tail, tok1, md1, v, pm);
+        pa.out_block[int64_t(r) * W + j1] = v;
+        pa.out_pm[int64_t(r) * W + j1] = pm;
+    }
+}
+
 // splitmix64's output mix (Steele, Lea and Flood, "Fast splittable pseudorandom
 // number generators", OOPSLA 2014).
 __device__ inline uint64_t mix64(uint64_t x) {
@@ -104,7 +160,9 @@ inline int launch_pdl(void (*kernel)(Params), unsigned grid, unsigned block, cud
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
-    return e == cudaSuccess ? LOOKUP_DRAFT_OK : lookup_record_cuda_error(e, "kernel launch");
+    if (e != cudaSuccess) return lookup_record_cuda_error(e, "kernel launch");
+    lookup_note_launch();
+    return LOOKUP_DRAFT_OK;
 }
 
 // The same for a kernel of two parameter structs.
@@ -122,7 +180,9 @@ inline int launch_pdl2(void (*kernel)(P1, P2), unsigned grid, unsigned block, cu
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, b);
-    return e == cudaSuccess ? LOOKUP_DRAFT_OK : lookup_record_cuda_error(e, "kernel launch");
+    if (e != cudaSuccess) return lookup_record_cuda_error(e, "kernel launch");
+    lookup_note_launch();
+    return LOOKUP_DRAFT_OK;
 }
 
 inline int sm_count(int *out) {

@@ -1044,16 +1044,9 @@ __global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_kernel(F
 // lookup-drafting article, sections "第3步" and "第2步"), the rules lookup_plan
 // applies, on the draft lookup_draft_ex would write (K = H + T <= 64).
 struct PlanArgs {
-    const int32_t *model_draft;   // [B][H]
-    const int32_t *committed;     // [B]
-    int32_t *state;               // [B][3] in/out
-    int32_t *out_long;
-    int32_t *out_block;           // [B][H + T]
-    int32_t *out_len;
-    int32_t *out_pm;              // [B][H + T]
+    lkd::PlanIO io;
     int32_t *out_mlen;            // may be null
     int32_t *out_draft_len;       // may be null
-    int32_t H, T, replace_min, agree_min, agree_n, tail_min, slack, enter_steps, sticky;
 };
 
 __global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_plan_kernel(FillParams prm, PlanArgs pa) {
@@ -1064,7 +1057,7 @@ __global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_plan_ker
         const int32_t m = found ? int32_t(km) : 0;
         const int64_t p = found ? kp : 0;
         const int d = found ? int(L - p - m) : 1;
-        const int W = pa.H + pa.T;
+        const int W = pa.io.H + pa.io.T;
         // Draft tokens lane and lane + 32 (-1 without a match), as write_draft forms them.
         const int32_t *src = prm.tokens + o0 + p + m;
         const int j1 = lane + 32;
@@ -1075,39 +1068,10 @@ __global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_plan_ker
         const int32_t tok1 = (found && j1 < W && LKD_OK(p + m + (j1 < d ? j1 : j1 % d) < L, LOOKUP_DRAFT_CHECK_TOKENS))
                                  ? __ldg(src + (j1 < d ? j1 : j1 % d))
                                  : -1;
-        // Head rule: the model agrees with the draft's first agree_n tokens.
-        const int32_t *md = pa.model_draft + int64_t(r) * pa.H;
-        const int32_t md0 = lane < pa.H ? md[lane] : -1, md1 = j1 < pa.H ? md[j1] : -1;
-        const bool ne = (lane < pa.agree_n && tok0 != md0) || (j1 < pa.agree_n && tok1 != md1);
-        const bool agree = __all_sync(0xffffffffu, !ne);
-        const bool head = m >= pa.replace_min || (m >= pa.agree_min && agree);
-        // Scheduling: every lane reads the old state, then lane 0 writes the new one.
-        int32_t *st = pa.state + 3 * int64_t(r);
-        int32_t lng = st[0], streak = st[1], hold = st[2];
-        lkd::schedule_update(m, pa.committed[r], pa.H, pa.T, pa.tail_min, pa.slack, pa.enter_steps, pa.sticky,
-                             lng, streak, hold);
-        __syncwarp();
-        const bool tail = lng != 0 && m >= pa.tail_min;
+        lkd::plan_warp(pa.io, r, lane, m, tok0, tok1);
         if (lane == 0) {
-            st[0] = lng;
-            st[1] = streak;
-            st[2] = hold;
-            pa.out_long[r] = lng;
-            pa.out_len[r] = tail ? W : pa.H;
             if (pa.out_mlen) pa.out_mlen[r] = m;
             if (pa.out_draft_len) pa.out_draft_len[r] = found ? W : (failed ? LOOKUP_DRAFT_LEN_FAILED : 0);
-        }
-        // Fusion of the block's positions.
-        int32_t v, pm;
-        if (lane < W) {
-            lkd::fuse_choice(lane, pa.H, head, tail, tok0, md0, v, pm);
-            pa.out_block[int64_t(r) * W + lane] = v;
-            pa.out_pm[int64_t(r) * W + lane] = pm;
-        }
-        if (j1 < W) {
-            lkd::fuse_choice(j1, pa.H, head, tail, tok1, md1, v, pm);
-            pa.out_block[int64_t(r) * W + j1] = v;
-            pa.out_pm[int64_t(r) * W + j1] = pm;
         }
     });
 }
@@ -1552,7 +1516,7 @@ int run_plan(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t m
     fp.offsets = offsets;
     fp.slots = slots;
     fp.B = B;
-    fp.K = pa.H + pa.T;
+    fp.K = pa.io.H + pa.io.T;
     fp.grid = grid_for(*st);
 #if LOOKUP_DRAFT_CHECKED
     fp.nslots = int64_t(B) + int64_t(fp.grid) * kWarps;
@@ -1591,6 +1555,11 @@ std::mutex g_static_mu;
 __attribute__((visibility("hidden"))) int lookup_record_cuda_error(cudaError_t e, const char *what) {
     return cuda_fail(e, what);
 }
+
+// Kernel launches the library has enqueued, process-wide (lookup_draft_launch_count).
+static std::atomic<uint64_t> g_launches{0};
+
+__attribute__((visibility("hidden"))) void lookup_note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 // Fixed scratch of lookup_draft_noalloc (file scope; every GPU that loads the
 // library holds it until the process exits).
@@ -1813,6 +1782,8 @@ const char *lookup_draft_strerror(int code) {
 
 const char *lookup_draft_last_cuda_error(void) { return g_cuda_msg; }
 
+uint64_t lookup_draft_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
 void lookup_draft_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns ? ns : kDefaultWaitNs); }
 
 int lookup_draft_plan(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t min_m, int32_t max_m,
@@ -1834,8 +1805,9 @@ int lookup_draft_plan(const int32_t *tokens, const int64_t *offsets, int32_t B, 
                              out_draft_len};
     for (const int32_t *q : ptrs)
         if (q && !aligned(q, 4)) return LOOKUP_DRAFT_EINVAL;
-    PlanArgs pa{model_draft, committed, state, out_long, out_block, out_len, out_point_mass, out_mlen,
-                out_draft_len, H, T, replace_min, agree_min, agree_n, tail_min, slack, enter_steps, sticky};
+    PlanArgs pa{{model_draft, committed, state, out_long, out_block, out_len, out_point_mass, H, T, replace_min,
+                 agree_min, agree_n, tail_min, slack, enter_steps, sticky},
+                out_mlen, out_draft_len};
     return run_plan(tokens, offsets, B, min_m, max_m, pa, stream);
 }
 

@@ -425,7 +425,11 @@ __device__ unsigned long long brute_force(const int32_t *t, int L, int tok, int 
     return best;
 }
 
-__global__ void __launch_bounds__(kWarpThreads) index_draft_kernel(DraftParams p) {
+// PLAN: the draft tokens stay in the warp's registers and the decode loop's
+// scheduling and fusion follow (lkd::plan_warp); out_len then receives the length
+// lookup_index_draft would report, and no draft row is written.
+template <bool PLAN>
+__global__ void __launch_bounds__(kWarpThreads) index_draft_kernel(DraftParams p, lkd::PlanIO pio) {
     wait_for_prerequisite_grid();
     allow_dependent_launch();
     const int lane = threadIdx.x & 31;
@@ -440,9 +444,10 @@ __global__ void __launch_bounds__(kWarpThreads) index_draft_kernel(DraftParams p
         const int32_t *t = p.tokens + base;
         // suffix token i (counted from the end) in lane i
         const int tok = (lane < p.max_m && lane < L) ? t[L - 1 - lane] : 0;
-        int32_t *row = p.out_draft + int64_t(r) * p.K;
+        int32_t *row = PLAN ? nullptr : p.out_draft + int64_t(r) * p.K;
         unsigned long long best = 0ull;
         bool fallback = overflow, drafted = false;
+        int32_t tok0 = -1, tok1 = -1;                    // PLAN: draft tokens lane and lane + 32
         if (hd_ok && !overflow && L >= p.min_m + 1) {
             // keys: lane j hashes the n-gram of length n = min_m + j
             const int n = p.min_m + lane;
@@ -483,8 +488,13 @@ __global__ void __launch_bounds__(kWarpThreads) index_draft_kernel(DraftParams p
                     fallback = true;                             // the slot was shared with another key
                 } else {
                     best = (uint64_t(uint32_t(m)) << 32) | uint32_t(c - m + 1);
-                    if (lane < p.K) row[lane] = d0;
-                    if (lane + 32 < p.K) row[lane + 32] = d1;
+                    if (PLAN) {
+                        tok0 = lane < p.K ? d0 : -1;
+                        tok1 = lane + 32 < p.K ? d1 : -1;
+                    } else {
+                        if (lane < p.K) row[lane] = d0;
+                        if (lane + 32 < p.K) row[lane + 32] = d1;
+                    }
                     drafted = true;
                 }
             }
@@ -495,11 +505,18 @@ __global__ void __launch_bounds__(kWarpThreads) index_draft_kernel(DraftParams p
         const bool found = hd_ok && m > 0;
         if (!drafted) {                                         // the draft from the self-extended history
             const int d = L - pos - m;
-            for (int j = lane; j < p.K; j += 32) row[j] = found ? t[pos + m + (j % d)] : -1;
+            if (PLAN) {
+                tok0 = (found && lane < p.K) ? t[pos + m + (lane % d)] : -1;
+                tok1 = (found && lane + 32 < p.K) ? t[pos + m + ((lane + 32) % d)] : -1;
+            } else {
+                for (int j = lane; j < p.K; j += 32) row[j] = found ? t[pos + m + (j % d)] : -1;
+            }
         }
+        if (PLAN) lkd::plan_warp(pio, r, lane, found ? m : 0, tok0, tok1);
         if (lane == 0) {
-            p.out_len[r] = !hd_ok ? LOOKUP_DRAFT_LEN_FAILED : (found ? p.K : 0);
-            p.out_pos[r] = found ? pos : -1;
+            // PLAN: out_len (the draft length) is optional and no position is written
+            if (!PLAN || p.out_len) p.out_len[r] = !hd_ok ? LOOKUP_DRAFT_LEN_FAILED : (found ? p.K : 0);
+            if (!PLAN) p.out_pos[r] = found ? pos : -1;
             if (p.out_mlen) p.out_mlen[r] = found ? m : 0;
             if (p.out_fallback) p.out_fallback[r] = fallback ? 1 : 0;
         }
@@ -656,7 +673,49 @@ int lookup_index_draft(const int32_t *tokens, const int64_t *base, const int32_t
     p.max_m = max_m;
     p.K = K;
     p.hash_bits = hash_bits;
-    return launch_pdl(index_draft_kernel, warp_grid(B, sms), unsigned(kWarpThreads), stream, p);
+    return lkd::launch_pdl2(index_draft_kernel<false>, warp_grid(B, sms), unsigned(kWarpThreads), stream, p,
+                            lkd::PlanIO{});
+}
+
+int lookup_index_draft_plan(const int32_t *tokens, const int64_t *base, const int32_t *len, int32_t B, int32_t min_m,
+                            int32_t max_m, const void *index, int64_t slots, int32_t hash_bits,
+                            const int32_t *model_draft, const int32_t *committed, int32_t H, int32_t T,
+                            int32_t replace_min, int32_t agree_min, int32_t agree_n, int32_t tail_min, int32_t slack,
+                            int32_t enter_steps, int32_t sticky, int32_t *state, int32_t *out_long,
+                            int32_t *out_block, int32_t *out_len, int32_t *out_point_mass, int32_t *out_mlen,
+                            int32_t *out_draft_len, int32_t *out_fallback, struct CUstream_st *stream) {
+    lkd::TraceRange trace_("lookup_index_draft_plan");
+    if (B < 0 || !params_ok(min_m, max_m, hash_bits, slots) || H < 1 || T < 0 ||
+        int64_t(H) + T > LOOKUP_DRAFT_MAX_K || agree_n < 0 || agree_n > H || enter_steps < 1 || sticky < 0 ||
+        slack < 0)
+        return LOOKUP_DRAFT_EINVAL;
+    if (B == 0) return LOOKUP_DRAFT_OK;
+    if (!tokens || !base || !len || !index || !aligned16(index) || !model_draft || !committed || !state ||
+        !out_long || !out_block || !out_len || !out_point_mass)
+        return LOOKUP_DRAFT_EINVAL;
+    int sms = 0;
+    int rc = sm_count(&sms);
+    if (rc != LOOKUP_DRAFT_OK) return rc;
+    DraftParams p{};
+    p.tokens = tokens;
+    p.base = base;
+    p.len = len;
+    p.hd = static_cast<const Header *>(index);
+    p.tab = reinterpret_cast<const Slot *>(static_cast<const char *>(index) + sizeof(Header));
+    p.out_draft = nullptr;                               // the draft stays in registers
+    p.out_len = out_draft_len;
+    p.out_pos = nullptr;
+    p.out_mlen = out_mlen;
+    p.out_fallback = out_fallback;
+    p.slots = slots;
+    p.B = B;
+    p.min_m = min_m;
+    p.max_m = max_m;
+    p.K = H + T;
+    p.hash_bits = hash_bits;
+    const lkd::PlanIO pio{model_draft, committed, state, out_long, out_block, out_len, out_point_mass, H, T,
+                          replace_min, agree_min, agree_n, tail_min, slack, enter_steps, sticky};
+    return lkd::launch_pdl2(index_draft_kernel<true>, warp_grid(B, sms), unsigned(kWarpThreads), stream, p, pio);
 }
 
 }  // extern "C"

@@ -206,3 +206,76 @@ def test_append_repeated_ngrams_in_one_call(period):
         got = idx.draft(t, b, n, 15, with_fallback=True)
         check_draft(got, oracle.lookup_draft(cur_t, cur_o, 4, 12, 15))
         assert host(got[4]).sum() == 0
+
+
+# ---------------------------------------------------- index draft, then plan ----
+def _plan_inputs(B, H, T, d_o, seed):
+    rng = gen.rng_for(seed, 43)
+    md = rng.integers(0, 50, size=(B, H)).astype(np.int32)
+    take = rng.random(B) < 0.4
+    md[take] = d_o[take, :H]
+    committed = rng.integers(1, H + T + 2, size=B).astype(np.int32)
+    state = np.stack([rng.integers(0, 2, B), rng.integers(0, 3, B), rng.integers(0, 4, B)], 1).astype(np.int32)
+    return md, committed, state
+
+
+def _oracle_plan(d_o, m_o, md, committed, state, H, T):
+    st = state.copy()
+    lg = oracle.schedule(m_o, committed, st, H, T)
+    blk, ln, pm = oracle.fuse(d_o, m_o, md, lg, H, T)
+    return lg, blk, ln, pm, st
+
+
+@pytest.mark.parametrize("hash_bits", [64, 3])
+@pytest.mark.parametrize("name", gen.WORKLOADS)
+def test_index_draft_plan_is_index_draft_then_plan(name, hash_bits):
+    """hash_bits = 3: nearly all keys share slots, so most requests take the
+    brute-force path, and the plan must follow its draft as well."""
+    w = gen.make_workload(name)
+    H, T = 7, 8
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, 32, seed=w.seed)
+    idx, t, b, n = built(st, base, length, w.min_m, w.max_m, hash_bits=hash_bits)
+    d_o, l_o, p_o, m_o = oracle_draft(st, base, length, w.min_m, w.max_m, H + T)
+    md, committed, state = _plan_inputs(w.B, H, T, d_o, w.seed)
+    lg_o, blk_o, len_o, pm_o, st_o = _oracle_plan(d_o, m_o, md, committed, state, H, T)
+    st_g = dev(state)
+    lg, blk, ln, pm, ml, dl, fb = idx.draft_plan(t, b, n, dev(md), dev(committed), st_g, H, T)
+    for nm, g, e in (("long", lg, lg_o), ("block", blk, blk_o), ("len", ln, len_o), ("point mass", pm, pm_o),
+                     ("mlen", ml, m_o), ("draft len", dl, l_o), ("state", st_g, st_o)):
+        np.testing.assert_array_equal(host(g), e, err_msg=nm)
+    if hash_bits == 64:
+        assert host(fb).sum() == 0
+
+
+@pytest.mark.parametrize("name", ["recitation25k", "chats"])
+def test_index_decode_loop_with_plan(name):
+    """Index draft + plan -> greedy verify -> index append, four steps, against the
+    oracle's draft -> schedule -> fuse -> verify -> append."""
+    w = gen.make_workload(name)
+    H, T = 7, 8
+    W = H + T + 1
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, 5 * W, seed=w.seed)
+    idx, t, b, n = built(st, base, length, w.min_m, w.max_m)
+    capd = dev(cap)
+    B = w.B
+    cur_t, cur_o = w.tokens, w.offsets
+    st_o = np.zeros((B, 3), np.int32)
+    st_g = dev(st_o)
+    committed = np.full(B, H + 1, np.int32)
+    for step in range(4):
+        d_o, l_o, p_o, m_o = oracle.lookup_draft(cur_t, cur_o, w.min_m, w.max_m, H + T, threads=16)
+        md, _, _ = _plan_inputs(B, H, T, d_o, step)
+        lg_o = oracle.schedule(m_o, committed, st_o, H, T)
+        blk_o, len_o, pm_o = oracle.fuse(d_o, m_o, md, lg_o, H, T)
+        lg, blk, ln, pm, ml, dl, fb = idx.draft_plan(t, b, n, dev(md), dev(committed), st_g, H, T)
+        for nm, g, e in (("long", lg, lg_o), ("block", blk, blk_o), ("len", ln, len_o), ("state", st_g, st_o)):
+            np.testing.assert_array_equal(host(g), e, err_msg=f"{nm}, step {step}")
+        rng = gen.rng_for(step, 44)
+        target = rng.integers(0, 50, size=(B, H + T + 1)).astype(np.int32)
+        f = rng.integers(0, H + T + 1, size=B)
+        for r in range(B):
+            target[r, :f[r]] = blk_o[r, :f[r]]
+        acc_o, com_o, nc_o = oracle.verify(blk_o, len_o, target)
+        assert (host(idx.append(t, b, n, capd, dev(com_o), dev(nc_o))) == 0).all()
+        cur_t, cur_o = oracle.append(cur_t, cur_o, com_o, nc_o)
+        committed = nc_o

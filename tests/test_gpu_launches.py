@@ -1,0 +1,118 @@
+"""The library's own count of the kernels it enqueues (lookup_draft_launch_count).
+
+Each entry point enqueues a fixed number of kernels: the drafting step two (scan,
+fill), each decode-loop step one, the flat append one for batches up to 1024 and
+two above, the index and context-cache appends one while every request gets a CTA
+in one wave, and two above it, the builds three.  The count is what the benchmark
+reports as the kernels of its timed region.  Inside a capture every launch counts
+once, and replays add nothing.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import gen
+
+torch = pytest.importorskip("torch")
+pkg = pytest.importorskip("prompt_lookup_speculative_gb300")
+
+pytestmark = pytest.mark.gpu
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def launches(fn):
+    """Kernels the library enqueued during fn() (which must not fail)."""
+    n0 = pkg.launch_count()
+    fn()
+    torch.cuda.synchronize()
+    return pkg.launch_count() - n0
+
+
+@pytest.fixture(scope="module")
+def batches():
+    out = {}
+    for name in ("recitation25k", "chats"):
+        w = gen.make_workload(name)
+        out[name] = (w, dev(w.tokens), dev(w.offsets))
+    return out
+
+
+@pytest.mark.parametrize("name", ["recitation25k", "chats"])
+def test_drafting_step_is_two_launches(batches, name):
+    w, t, o = batches[name]
+    assert launches(lambda: pkg.lookup_draft(t, o, w.min_m, w.max_m, w.K)) == 2
+    assert launches(lambda: pkg.lookup_draft_ex(t, o, w.min_m, w.max_m, w.K)) == 2
+    assert launches(lambda: pkg.lookup_draft_noalloc(t, o, w.min_m, w.max_m, w.K)) == 2
+
+
+def test_host_entry_point_adds_at_most_a_copy_kernel(batches):
+    w, _, _ = batches["recitation25k"]
+    n = launches(lambda: pkg.lookup_draft_host(w.tokens, w.offsets, w.min_m, w.max_m, w.K))
+    assert n in (2, 3)
+
+
+@pytest.mark.parametrize("name", ["recitation25k", "chats"])
+def test_decode_loop_steps_are_one_launch_each(batches, name):
+    w, t, o = batches[name]
+    B, H, T = w.B, 7, 8
+    d, ln, pos, m = pkg.lookup_draft_ex(t, o, w.min_m, w.max_m, H + T)
+    md = dev(np.zeros((B, H), np.int32))
+    committed = dev(np.full(B, H + 1, np.int32))
+    state = dev(np.zeros((B, 3), np.int32))
+    lg = dev(np.zeros(B, np.int32))
+    assert launches(lambda: pkg.lookup_schedule(m, committed, state, H, T)) == 1
+    assert launches(lambda: pkg.lookup_fuse(d, m, md, lg, H, T)) == 1
+    assert launches(lambda: pkg.lookup_plan(d, m, md, committed, state, H, T)) == 1
+    assert launches(lambda: pkg.lookup_draft_plan(t, o, md, committed, state, w.min_m, w.max_m, H, T)) == 2
+    blk, blen, _ = pkg.lookup_fuse(d, m, md, lg, H, T)
+    target = dev(np.zeros((B, H + T + 1), np.int32))
+    res = []
+    assert launches(lambda: res.append(pkg.lookup_verify(blk, blen, target))) == 1
+    _, commit, ncommit = res[0]
+    assert launches(lambda: pkg.lookup_append(t, o, commit, ncommit)) == (1 if B <= 1024 else 2)
+    acc = dev(np.full((B, 5), 0.5, np.float32))
+    prev = dev(np.zeros((B, 3), np.int32))
+    assert launches(lambda: pkg.lookup_policy(m, ncommit, acc, prev, H, 3, 1.3, 1.1, 0.8)) == 1
+
+
+def test_index_entry_points(batches):
+    w, _, _ = batches["recitation25k"]
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, 64, seed=w.seed)
+    t, b, n, c = dev(st), dev(base), dev(length), dev(cap)
+    idx = pkg.NgramIndex(st.shape[0], w.min_m, w.max_m)
+    assert launches(lambda: idx.build(t, b, n)) == 3
+    assert launches(lambda: idx.draft(t, b, n, 15)) == 1
+    B, H, T = w.B, 7, 8
+    md = dev(np.zeros((B, H), np.int32))
+    committed = dev(np.full(B, H + 1, np.int32))
+    state = dev(np.zeros((B, 3), np.int32))
+    assert launches(lambda: idx.draft_plan(t, b, n, md, committed, state, H, T)) == 1
+    commit = dev(np.ones((B, 8), np.int32))
+    ncommit = dev(np.full(B, 8, np.int32))
+    assert launches(lambda: idx.append(t, b, n, c, commit, ncommit)) == 1     # B = 64: one wave
+
+
+def test_capture_counts_once_and_replays_add_nothing(batches):
+    w, t, o = batches["recitation25k"]
+    out = pkg.lookup_draft(t, o, w.min_m, w.max_m, w.K)        # eager first: the stream's scratch
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pkg.lookup_draft(t, o, w.min_m, w.max_m, w.K, out=out, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    n0 = pkg.launch_count()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            pkg.lookup_draft(t, o, w.min_m, w.max_m, w.K, out=out, stream=torch.cuda.current_stream())
+    n1 = pkg.launch_count()
+    assert n1 - n0 == 6
+    for _ in range(4):
+        g.replay()
+    torch.cuda.synchronize()
+    assert pkg.launch_count() == n1

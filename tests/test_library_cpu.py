@@ -320,6 +320,18 @@ def test_cuda_failure_is_reported_without_a_gpu(lib):
     assert lib.lookup_draft_noalloc(FAKE, FAKE, 4, 4, 12, 15, FAKE, FAKE, FAKE, None) == -2
 
 
+def test_launch_counter_needs_no_gpu_and_counts_no_failed_call(lib):
+    """lookup_draft_launch_count answers without a device; calls refused on their
+    arguments or failing on CUDA enqueue nothing and leave it unchanged."""
+    n0 = lib.lookup_draft_launch_count()
+    assert lib.lookup_draft(FAKE, FAKE, 4, 4, 12, 15, FAKE, FAKE, FAKE, None) == -2
+    assert lib.lookup_draft(FAKE, FAKE, 4, 4, 3, 15, FAKE, FAKE, FAKE, None) == -1
+    assert lib.lookup_draft_plan(FAKE, FAKE, 4, 4, 12, FAKE, FAKE, 7, 8, 8, 6, 2, 4, 1, 2, 3, FAKE, FAKE, FAKE, FAKE,
+                                 FAKE, FAKE, None, None) != 0
+    assert lib.lookup_draft_launch_count() == n0
+    assert pkg.launch_count(lib) == n0
+
+
 def test_policy_rejects_bad_parameters(lib):
     F = FAKE
     ok = [F, F, 4, 7, 3, 1.0, 1.0, 1.0, 0.125, 0.05, 6, 8, 12, F, F, F, None]
@@ -351,3 +363,25 @@ def test_binding_declares_argument_types_of_every_entry_point(lib, checked_lib):
         assert getattr(checked_lib, name).argtypes is not None, f"checked {name}: argument types not declared"
     with pytest.raises(AttributeError):
         checked_lib.lookup_policy                       # not in the checked build at all
+
+
+def test_index_draft_plan_rejects_bad_parameters(lib):
+    F = FAKE
+    ok = [F, F, F, 4, 4, 12, F, 1024, 64, F, F, 7, 8, 8, 6, 2, 4, 1, 2, 3, F, F, F, F, F, None, None, None, None]
+    assert len(ok) == 29
+
+    def call(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return lib.lookup_index_draft_plan(*a)
+
+    assert call(a11=0) == -1                # H < 1
+    assert call(a11=40, a12=25) == -1       # H + T above LOOKUP_DRAFT_MAX_K
+    assert call(a15=8) == -1                # agree_n > H
+    assert call(a18=0) == -1                # enter_steps < 1
+    assert call(a7=1000) == -1              # slots not a power of two
+    assert call(a20=None) == -1             # no state
+    assert call(a6=F + 8) == -1             # misaligned index
+    assert lib.lookup_index_draft_plan(None, None, None, 0, 4, 12, None, 1024, 64, None, None, 7, 8, 8, 6, 2, 4, 1, 2,
+                                       3, None, None, None, None, None, None, None, None, None) == 0
