@@ -29,7 +29,11 @@
  * Execution: every call enqueues its work on `stream` (NULL = the legacy
  * default stream) and returns without synchronising, except lookup_draft_host.
  * Device pointers must be valid on the current device.  The library keeps no
- * pointer to caller memory after a call returns.  Calls are thread-safe.
+ * pointer to caller memory after a call returns.  Calls are thread-safe.  Calls
+ * from several threads on one stream that use the stream's scratch (lookup_draft,
+ * lookup_draft_ex, lookup_draft_plan, lookup_draft_host) hold the stream's lock
+ * while they enqueue their kernels (lookup_draft_host: until it has synchronised),
+ * so their kernels never interleave; they run in the order the threads take it.
  *
  * Return codes: LOOKUP_DRAFT_OK, or a negative LOOKUP_DRAFT_E* code.  A call that
  * returns an error may have enqueued nothing or part of its work; its outputs
@@ -148,8 +152,10 @@ int lookup_draft_fill(const int32_t *tokens, const int64_t *offsets, int32_t B,
 
 /*
  * lookup_draft on HOST buffers: copies tokens[offsets[0] .. offsets[B]) and the
- * offsets to the current device (stream-ordered scratch from the library pool),
- * runs the step on `stream`, delivers the outputs into the host arrays and
+ * offsets to the current device, into the stream's scratch (the buffer
+ * lookup_draft keeps per stream, grown to hold the copy, the outputs and the
+ * scan's slots; the pool's stream-ordered memory inside stream capture, where
+ * the final synchronisation fails), runs the step on `stream`, delivers the outputs into the host arrays and
  * synchronises the stream before returning.  Page-locked output arrays that the
  * device can address (cudaHostAlloc / cudaHostRegister memory) are written by
  * the draft-fill kernel directly; other host memory receives the outputs by

@@ -1411,6 +1411,11 @@ int launch_host_copy(const DeviceState &st, const CopyParams &cp, cudaStream_t s
 struct StreamScratch {
     unsigned long long *slots = nullptr;
     size_t bytes = 0;
+    // Held by a call while it enqueues the kernels that use the buffer (the host
+    // entry point: until its stream synchronisation), so that calls from several
+    // threads on one stream never interleave their kernels on it.  One per stream
+    // key, kept across growth; never freed.
+    std::mutex *mu = nullptr;
 };
 std::mutex g_scratch_mu;
 std::unordered_map<uintptr_t, StreamScratch> g_scratch[kMaxDevices];
@@ -1426,22 +1431,26 @@ struct LastScratch {
 };
 thread_local LastScratch t_last;
 
-// The scratch of `stream` on device `dev`, holding at least `need` bytes; nullptr
-// (no error) when it has none and cannot make one now: the stream is capturing.
-int stream_scratch(int dev, cudaStream_t stream, size_t need, unsigned long long **out) {
+// The scratch of `stream` on device `dev`, holding at least `need` bytes, and the
+// stream's lock (*mu) to hold while enqueuing work on it; nullptr for both (no
+// error) when it has none and cannot make one now: the stream is capturing.
+int stream_scratch(int dev, cudaStream_t stream, size_t need, unsigned long long **out, std::mutex **mu) {
     // cudaStreamPerThread is one handle for a different stream in every thread:
     // keyed by the calling thread instead (an address of its own, never a handle).
     const uintptr_t key = stream == cudaStreamPerThread ? reinterpret_cast<uintptr_t>(&t_last) | 1u
                                                         : reinterpret_cast<uintptr_t>(stream);
     if (t_last.dev == dev && t_last.stream == key && t_last.sc.bytes >= need) {
         *out = t_last.sc.slots;
+        *mu = t_last.sc.mu;
         return LOOKUP_DRAFT_OK;
     }
     *out = nullptr;
+    *mu = nullptr;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
     StreamScratch &sc = g_scratch[dev][key];
     if (sc.bytes >= need) {
         *out = sc.slots;
+        *mu = sc.mu;
         t_last.dev = dev;
         t_last.stream = key;
         t_last.sc = sc;
@@ -1452,11 +1461,13 @@ int stream_scratch(int dev, cudaStream_t stream, size_t need, unsigned long long
     if (cs != cudaStreamCaptureStatusNone) return LOOKUP_DRAFT_OK;
     size_t bytes = sc.bytes * 2 > need ? sc.bytes * 2 : need;
     bytes = (bytes + 65535) & ~size_t(65535);
+    if (!sc.mu) sc.mu = new std::mutex;
     void *p = nullptr;
     LD_CUDA(cudaMalloc(&p, bytes));                     // valid on every stream at once
     sc.slots = static_cast<unsigned long long *>(p);    // the old buffer, if any, stays allocated
     sc.bytes = bytes;
     *out = sc.slots;
+    *mu = sc.mu;
     t_last.dev = dev;
     t_last.stream = key;
     t_last.sc = sc;
@@ -1472,9 +1483,11 @@ int run_step(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t m
     LD_CUDA(cudaGetDevice(&dev));
     const size_t need = workspace_bytes_for(B, grid_for(*st));
     unsigned long long *slots = nullptr;
-    rc = stream_scratch(dev, stream, need, &slots);
+    std::mutex *mu = nullptr;
+    rc = stream_scratch(dev, stream, need, &slots, &mu);
     if (rc != LOOKUP_DRAFT_OK) return rc;
     if (slots) {
+        std::lock_guard<std::mutex> hold(*mu);
         rc = launch_scan(*st, tokens, offsets, B, min_m, max_m, slots, stream);
         if (rc == LOOKUP_DRAFT_OK)
             rc = launch_fill(*st, tokens, offsets, B, K, slots, out_draft, out_len, out_pos, out_mlen, stream);
@@ -1504,8 +1517,11 @@ int run_plan(const int32_t *tokens, const int64_t *offsets, int32_t B, int32_t m
     LD_CUDA(cudaGetDevice(&dev));
     const size_t need = workspace_bytes_for(B, grid_for(*st));
     unsigned long long *slots = nullptr;
-    rc = stream_scratch(dev, stream, need, &slots);
+    std::mutex *mu = nullptr;
+    rc = stream_scratch(dev, stream, need, &slots, &mu);
     if (rc != LOOKUP_DRAFT_OK) return rc;
+    std::unique_lock<std::mutex> hold;
+    if (mu) hold = std::unique_lock<std::mutex>(*mu);
     void *ws = nullptr;
     if (!slots) {
         LD_CUDA(cudaMallocFromPoolAsync(&ws, need, st->pool, stream));
@@ -1691,8 +1707,20 @@ int lookup_draft_host(const int32_t *h_tokens, const int64_t *h_offsets, int32_t
     const size_t out_words = size_t(B) * size_t(K) + 2 * size_t(B);
     const size_t ws_bytes = workspace_bytes_for(B, grid_for(*st));
     const size_t total = tok_bytes + ((off_bytes + 15) & ~size_t(15)) + ((out_words * 4 + 15) & ~size_t(15)) + ws_bytes;
-    void *buf = nullptr;
-    LD_CUDA(cudaMallocFromPoolAsync(&buf, total, st->pool, stream));
+    // The stream's scratch holds the staging buffer: calls on one stream are
+    // ordered and this one synchronises before it returns, so the buffer is idle
+    // between calls.  Without one (a capturing stream, where the synchronisation
+    // below fails anyway) the buffer comes from the pool for this call.
+    int dev = 0;
+    LD_CUDA(cudaGetDevice(&dev));
+    unsigned long long *staging = nullptr;
+    std::mutex *mu = nullptr;
+    rc = stream_scratch(dev, stream, total, &staging, &mu);
+    if (rc != LOOKUP_DRAFT_OK) return rc;
+    std::unique_lock<std::mutex> hold;                  // until the synchronisation below
+    if (mu) hold = std::unique_lock<std::mutex>(*mu);
+    void *buf = staging;
+    if (!buf) LD_CUDA(cudaMallocFromPoolAsync(&buf, total, st->pool, stream));
     unsigned char *base = static_cast<unsigned char *>(buf);
     int32_t *d_tok = reinterpret_cast<int32_t *>(base + phase);
     int64_t *d_off = reinterpret_cast<int64_t *>(base + tok_bytes);
@@ -1743,7 +1771,7 @@ int lookup_draft_host(const int32_t *h_tokens, const int64_t *h_offsets, int32_t
     if (rc == LOOKUP_DRAFT_OK && !direct && e == cudaSuccess)
         e = cudaMemcpyAsync(h_out_pos, d_pos, size_t(B) * 4, cudaMemcpyDeviceToHost, stream);
     if (rc == LOOKUP_DRAFT_OK && e != cudaSuccess) rc = cuda_fail(e, "cudaMemcpyAsync (device to host)");
-    cudaError_t fe = cudaFreeAsync(buf, stream);
+    cudaError_t fe = staging ? cudaSuccess : cudaFreeAsync(buf, stream);
     cudaError_t se = cudaStreamSynchronize(stream);
     if (rc == LOOKUP_DRAFT_OK && fe != cudaSuccess) rc = cuda_fail(fe, "cudaFreeAsync");
     if (rc == LOOKUP_DRAFT_OK && se != cudaSuccess) rc = cuda_fail(se, "cudaStreamSynchronize");

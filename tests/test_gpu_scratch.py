@@ -11,7 +11,12 @@ Checked here:
 - a graph captured on a fresh stream (the pool path), and one captured after an
   eager call (the stream's buffer), each replayed several times;
 - a graph replayed after a later, larger call replaced its stream's buffer (the
-  old buffer stays allocated).
+  old buffer stays allocated);
+- lookup_draft_host, which stages its copy of the inputs, its outputs and the
+  slots in the same per-stream buffer: interleaved with device calls on one
+  stream (growing it), before and after graph capture, and from several threads
+  on one shared stream, where each call holds the stream's lock while it enqueues
+  its kernels.
 """
 from __future__ import annotations
 
@@ -227,3 +232,130 @@ def test_per_thread_default_streams_get_their_own_scratch():
     for i, calls in enumerate(work):
         for j, (b, out) in enumerate(calls):
             b.check(out, f"thread {i}, call {j}")
+
+
+class HostBatch:
+    """A batch on host memory for lookup_draft_host: page-locked (read by the
+    device's copy kernel, outputs written in place) or pageable (copy-engine
+    transfers both ways)."""
+
+    def __init__(self, name: str, seed: int, pinned: bool = True):
+        self.w = many_requests(12000, seed) if name == "many" else gen.make_workload(name, seed)
+        self.pinned = pinned
+        self.t = self._host(torch.from_numpy(self.w.tokens))
+        self.o = self._host(torch.from_numpy(self.w.offsets))
+        self.want = oracle.lookup_draft(self.w.tokens, self.w.offsets, self.w.min_m, self.w.max_m, self.w.K,
+                                        threads=8)
+
+    def _host(self, x):
+        return x.pin_memory() if self.pinned else x.clone()
+
+    def outputs(self):
+        w = self.w
+        return tuple(self._host(torch.full(sh, 7, dtype=torch.int32)) for sh in ((w.B, w.K), (w.B,), (w.B,)))
+
+    def call(self, lib, out, stream):
+        w = self.w
+        d, ln, p = out
+        rc = lib.lookup_draft_host(self.t.data_ptr(), self.o.data_ptr(), w.B, w.min_m, w.max_m, w.K, d.data_ptr(),
+                                   ln.data_ptr(), p.data_ptr(), stream.cuda_stream)
+        assert rc == 0, (lib.lookup_draft_strerror(rc), lib.lookup_draft_last_cuda_error())
+
+    def check(self, out, what: str):
+        for name, g, e in zip(("draft", "len", "pos"), out, self.want[:3]):
+            np.testing.assert_array_equal(g.numpy(), e, err_msg=f"{what}: {name}")
+
+
+def test_host_and_device_calls_share_one_streams_buffer():
+    """The host entry point copies its inputs into the stream's buffer, which the
+    device calls before and after it on the same stream also use; each host call
+    that needs more than the buffer holds grows it."""
+    lib = pkg.load_library()
+    s = torch.cuda.Stream()
+    dev_calls = [Batch("tiny", 70), Batch("chats", 71), Batch("many", 72), Batch("tiny", 73)]
+    host_calls = [HostBatch("recitation25k", 74), HostBatch("tiny", 75), HostBatch("ragged262k", 76),
+                  HostBatch("chats", 77, pinned=False), HostBatch("periodic", 78)]
+    dev_out = [b.outputs() for b in dev_calls]
+    torch.cuda.synchronize()
+    order = [("d", 0), ("h", 0), ("d", 1), ("h", 1), ("h", 2), ("d", 2), ("h", 3), ("d", 3), ("h", 4)]
+    for kind, i in order:
+        with torch.cuda.stream(s):
+            if kind == "d":
+                dev_calls[i].call(lib, dev_out[i], s)
+            else:
+                out = host_calls[i].outputs()
+                host_calls[i].call(lib, out, s)              # synchronous: checked at once
+                host_calls[i].check(out, f"host call {i}")
+    torch.cuda.synchronize()
+    for i, (b, out) in enumerate(zip(dev_calls, dev_out)):
+        b.check(out, f"device call {i}")
+
+
+@pytest.mark.parametrize("host_batch", ["tiny", "ragged262k"])
+def test_graph_replayed_after_a_host_call_on_its_stream(host_batch):
+    """A graph captured after an eager call uses the stream's buffer; a host call
+    on that stream then reuses the buffer (tiny) or replaces it with a larger one
+    (ragged262k). Replays that do not overlap the host call stay exact."""
+    lib = pkg.load_library()
+    s = torch.cuda.Stream()
+    b = Batch("recitation25k", 80)
+    h = HostBatch(host_batch, 81)
+    o = b.outputs()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        b.call(lib, o, s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        b.call(lib, o, torch.cuda.current_stream())
+    ho = h.outputs()
+    with torch.cuda.stream(s):
+        h.call(lib, ho, s)
+    h.check(ho, "host call")
+    for rep in range(3):
+        for x in o:
+            x.fill_(7)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            g.replay()
+        torch.cuda.synchronize()
+        b.check(o, f"replay {rep}")
+
+
+def test_threads_mixing_host_and_device_calls_on_one_stream():
+    """Four threads on ONE stream, each alternating device calls and host calls.
+    Without the stream's lock, one thread's scan could land between another
+    call's scan and fill (or its copy) on the shared stream and read that call's
+    slots or staged tokens; with it every result is exact."""
+    import threading
+
+    lib = pkg.load_library()
+    shared = torch.cuda.Stream()
+    dev_b = [Batch("tiny", 90), Batch("recitation25k", 91), Batch("chats", 92), Batch("many", 93)]
+    host_b = [HostBatch("periodic", 94), HostBatch("tiny", 95), HostBatch("recitation25k", 96),
+              HostBatch("tiny", 97, pinned=False)]
+    rounds = 8
+    work = [[(dev_b[(i + k) % 4], dev_b[(i + k) % 4].outputs(), host_b[(i + 2 * k) % 4],
+              host_b[(i + 2 * k) % 4].outputs()) for k in range(rounds)] for i in range(4)]
+    torch.cuda.synchronize()
+    errors = []
+
+    def run(calls):
+        try:
+            for db, dout, hb, hout in calls:
+                db.call(lib, dout, shared)
+                hb.call(lib, hout, shared)
+                hb.check(hout, "host call in a thread")
+        except Exception as exc:  # surfaced below
+            errors.append(exc)
+
+    threads = [threading.Thread(target=run, args=(calls,)) for calls in work]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for i, calls in enumerate(work):
+        for k, (db, dout, _, _) in enumerate(calls):
+            db.check(dout, f"thread {i}, round {k}")
