@@ -761,7 +761,10 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
     slabs with INDEX_SPARE tokens of room each): build time, index size, the
     draft from the index (which must equal the oracle's `want`), the in-place
     append of 8 committed tokens per request, and one whole decode-loop step on
-    the index (draft, schedule, fuse, greedy verify, append).  Each call is
+    the index (draft, schedule, fuse, greedy verify, append) three ways: five
+    entry points (``loop_step_us``), the draft with scheduling and fusion in one
+    (``loop_step_plan_us``), and that plus verification with the append in one
+    (``loop_step_two_call_us``), each from the same starting histories.  Each call is
     captured back to back in a CUDA graph and timed with CUDA events on its
     stream; the index is larger than L2 and its accesses are scattered."""
     import numpy as np
@@ -877,14 +880,18 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
     torch.cuda.synchronize(dev)
     room_ok = bool((status == 0).all().item())
 
+    def restart():
+        """The original histories again (lengths restored, the index rebuilt,
+        untimed), so the next loop's appends have the same room."""
+        length.copy_(torch.from_numpy(len_h))
+        state.zero_()
+        with torch.cuda.stream(stream):
+            idx.build(tokens, base, length, stream=stream)
+        torch.cuda.synchronize(dev)
+
     # the same step with the draft, scheduling and fusion in one launch
-    # (lookup_index_draft_plan), from the original histories: lengths restored and
-    # the index rebuilt (untimed), so the appends have the same room again
-    length.copy_(torch.from_numpy(len_h))
-    state.zero_()
-    with torch.cuda.stream(stream):
-        idx.build(tokens, base, length, stream=stream)
-    torch.cuda.synchronize(dev)
+    # (lookup_index_draft_plan), from the original histories
+    restart()
     dlen = torch.empty(B, dtype=i32, device=dev)
     fb = torch.empty(B, dtype=i32, device=dev)
 
@@ -901,6 +908,23 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
     loop_plan_us = timed(loop_plan_call, 16, 4)           # 80 steps again
     torch.cuda.synchronize(dev)
     room_ok = room_ok and bool((status == 0).all().item())
+
+    # and with verification and the append in one launch too (lookup_index_verify_append)
+    restart()
+
+    def loop_two_call(h):
+        check(lib.lookup_index_draft_plan(tp, bp, lp, B, w.min_m, w.max_m, mem, idx.slots, 64,
+                                          model_draft.data_ptr(), committed.data_ptr(), H, T, 8, 6, 2, 4, 1, 2, 3,
+                                          state.data_ptr(), long_block.data_ptr(), block.data_ptr(), blen.data_ptr(),
+                                          pm.data_ptr(), dm.data_ptr(), dlen.data_ptr(), fb.data_ptr(), h))
+        check(lib.lookup_index_verify_append(block.data_ptr(), blen.data_ptr(), target.data_ptr(), None, None, None,
+                                             None, B, P, tp, bp, lp, cp, w.min_m, w.max_m, mem, idx.slots, 64,
+                                             accepted.data_ptr(), commit.data_ptr(), ncommit.data_ptr(),
+                                             status.data_ptr(), h))
+
+    loop_two_us = timed(loop_two_call, 16, 4)             # 80 steps again
+    torch.cuda.synchronize(dev)
+    room_ok = room_ok and bool((status == 0).all().item())
     total_tokens = int(st.shape[0])
     res = {
         "layout": f"slabs with {INDEX_SPARE} tokens of room per request",
@@ -914,6 +938,8 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
         "loop_step_launches": launches["loop_call"],
         "loop_step_plan_us": round(loop_plan_us, 3),
         "loop_step_plan_launches": launches["loop_plan_call"],
+        "loop_step_two_call_us": round(loop_two_us, 3),
+        "loop_step_two_call_launches": launches["loop_two_call"],
         "draft_launches": launches["draft_call"],
         "append8_launches": launches["append_call"],
         "parity_with_oracle": bool(parity),

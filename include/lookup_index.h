@@ -126,6 +126,30 @@ int lookup_index_draft_plan(const int32_t *tokens, const int64_t *base, const in
                             int32_t *out_mlen, int32_t *out_draft_len, int32_t *out_fallback,
                             struct CUstream_st *stream);
 
+/*
+ * lookup_verify (include/lookup_loop.h) followed by lookup_index_append with its
+ * commit rows (W = P + 1): the verification of HyperQwen lookup-drafting article
+ * section "第3步", then the in-place append of the committed tokens to the
+ * histories and the index.  When every request gets a CTA in one wave (as for
+ * lookup_index_append), one launch: each request's CTA verifies its block in one
+ * warp and appends what it committed.  Otherwise the two calls, in order.
+ *
+ * block, block_len, target, probs, qprobs, point_mass, u, B, P, out_accepted,
+ * out_commit, out_ncommit    as for lookup_verify (out_commit and out_ncommit
+ *                            are written, then read by the append)
+ * tokens, base, len, cap, min_m, max_m, index, slots, hash_bits, out_status
+ *                            as for lookup_index_append
+ * Every output equals lookup_verify followed by lookup_index_append(..., commit =
+ * out_commit, ncommit = out_ncommit, W = P + 1, ...).
+ * Errors: those of the two calls.
+ */
+int lookup_index_verify_append(const int32_t *block, const int32_t *block_len, const int32_t *target,
+                               const float *probs, const float *qprobs, const int32_t *point_mass,
+                               const float *u, int32_t B, int32_t P, int32_t *tokens, const int64_t *base,
+                               int32_t *len, const int32_t *cap, int32_t min_m, int32_t max_m, void *index,
+                               int64_t slots, int32_t hash_bits, int32_t *out_accepted, int32_t *out_commit,
+                               int32_t *out_ncommit, int32_t *out_status, struct CUstream_st *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,7 +30,8 @@ __all__ = [
     "set_wait_limit_ns", "lookup_fuse", "lookup_schedule", "lookup_plan", "lookup_draft_plan", "lookup_verify",
     "lookup_append", "lookup_policy",
     "NgramIndex", "index_slots_for", "index_bytes", "lookup_index_build", "lookup_index_append",
-    "lookup_index_draft", "lookup_index_draft_plan", "ContextCache", "load_checked_library", "check_word",
+    "lookup_index_draft", "lookup_index_draft_plan", "lookup_index_verify_append", "ContextCache",
+    "load_checked_library", "check_word",
     "launch_count",
     "MAX_M", "MAX_K", "LEN_FAILED", "CHECK_BITS",
 ]
@@ -193,6 +194,9 @@ def _declare_loop(lib: ctypes.CDLL) -> None:
     lib.lookup_index_build.restype = ctypes.c_int
     lib.lookup_index_append.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, i64, i32, vp, vp]
     lib.lookup_index_append.restype = ctypes.c_int
+    lib.lookup_index_verify_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, i32, i32, vp,
+                                               i64, i32, vp, vp, vp, vp, vp]
+    lib.lookup_index_verify_append.restype = ctypes.c_int
     lib.lookup_index_draft.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, i64, i32, vp, vp, vp, vp, vp, vp]
     lib.lookup_index_draft.restype = ctypes.c_int
     lib.lookup_index_draft_plan.argtypes = [vp, vp, vp, i32, i32, i32, vp, i64, i32, vp, vp, i32, i32, i32, i32, i32,
@@ -665,6 +669,41 @@ def lookup_index_append(tokens, base, length, cap, commit, ncommit, min_m: int, 
     return status
 
 
+def lookup_index_verify_append(block, length, target, tokens, base, slab_len, cap, min_m: int, max_m: int, index,
+                               slots: int, probs=None, qprobs=None, point_mass=None, u=None, hash_bits: int = 64,
+                               out=None, status=None, stream=None):
+    """lookup_verify followed by lookup_index_append of its commit rows, in one
+    launch when the batch fits one wave of per-request CTAs.  ``length`` is the
+    blocks' lengths, ``slab_len`` the histories' (grown in place).  Returns
+    (accepted [B], commit [B, P+1], ncommit [B], status [B])."""
+    import torch
+    lib = load_library()
+    dev, B, (bp, lp, cp) = _slab_args(tokens, base, slab_len, cap)
+    P = block.shape[1]
+    f32 = torch.float32
+    args = (_dev(block, torch.int32, (B, P), dev, "block"), _dev(length, torch.int32, (B,), dev, "len"),
+            _dev(target, torch.int32, (B, P + 1), dev, "target"),
+            _dev(probs, f32, (B, P), dev, "probs", optional=True),
+            _dev(qprobs, f32, (B, P), dev, "qprobs", optional=True),
+            _dev(point_mass, torch.int32, (B, P), dev, "point_mass", optional=True),
+            _dev(u, f32, (B, P), dev, "u", optional=probs is None))
+    if out is None:
+        out = (torch.empty(B, dtype=torch.int32, device=dev), torch.empty((B, P + 1), dtype=torch.int32, device=dev),
+               torch.empty(B, dtype=torch.int32, device=dev))
+    acc, commit, nc = out
+    optr = (_dev(acc, torch.int32, (B,), dev, "accepted"), _dev(commit, torch.int32, (B, P + 1), dev, "commit"),
+            _dev(nc, torch.int32, (B,), dev, "ncommit"))
+    if status is None:
+        status = torch.empty(B, dtype=torch.int32, device=dev)
+    sp = _dev(status, torch.int32, (B,), dev, "status")
+    with torch.cuda.device(dev):
+        rc = lib.lookup_index_verify_append(*args, B, P, tokens.data_ptr(), bp, lp, cp, min_m, max_m,
+                                            index.data_ptr(), int(slots), hash_bits, *optr, sp,
+                                            _stream_handle(stream))
+    _check(rc, lib)
+    return acc, commit, nc, status
+
+
 def lookup_index_draft(tokens, base, length, min_m: int, max_m: int, K: int, index, slots: int,
                        hash_bits: int = 64, out=None, with_fallback: bool = False, stream=None):
     """The draft step from the index; exactly lookup_draft_ex's results for the slab
@@ -737,6 +776,13 @@ class NgramIndex:
     def append(self, tokens, base, length, cap, commit, ncommit, status=None, stream=None):
         return lookup_index_append(tokens, base, length, cap, commit, ncommit, self.min_m, self.max_m,
                                    self.memory, self.slots, self.hash_bits, status, stream)
+
+    def verify_append(self, block, block_len, target, tokens, base, length, cap, stream=None, **sampled):
+        """Verify the blocks, then append what they commit (lookup_index_verify_append);
+        ``sampled`` takes probs, qprobs, point_mass and u for sampled verification."""
+        return lookup_index_verify_append(block, block_len, target, tokens, base, length, cap, self.min_m,
+                                          self.max_m, self.memory, self.slots, hash_bits=self.hash_bits,
+                                          stream=stream, **sampled)
 
     def draft_plan(self, tokens, base, length, model_draft, committed, state, H: int = 7, T: int = 8, stream=None,
                    **rules):

@@ -117,6 +117,62 @@ __device__ inline void plan_warp(const PlanIO &pa, int r, int lane, int32_t m, i
     }
 }
 
+// Verification of request r's proposal block by one warp (HyperQwen lookup-drafting
+// article, "第3步"): the accepted length a is the first position that fails, greedy
+// (the target's token differs) or sampled (u * q >= p in float32, q = 1 at a
+// point mass); the commit row holds the accepted tokens, then the target's token
+// at a, then -1.  A block length outside [0, P] gives an error row (accepted -1,
+// no committed token).  Blocks are [B, P], the target rows [B, P + 1].
+constexpr int kMaxBlock = 1 << 16;        // positions of a verify block (H + T) at most
+
+struct VerifyIO {
+    const int32_t *block, *len, *target;
+    const float *probs, *qprobs;
+    const int32_t *point_mass;
+    const float *u;
+    int32_t *out_accepted, *out_commit, *out_ncommit;
+    int32_t P;
+};
+
+__device__ inline void verify_warp(const VerifyIO &v, int r, int lane) {
+    const int64_t o = int64_t(r) * v.P;
+    const int32_t len = v.len[r];
+    int32_t *commit = v.out_commit + int64_t(r) * (v.P + 1);
+    if (len < 0 || len > v.P) {                          // no valid block: an error row
+        for (int i = lane; i <= v.P; i += 32) commit[i] = -1;
+        if (lane == 0) {
+            v.out_accepted[r] = -1;
+            v.out_ncommit[r] = 0;
+        }
+        return;
+    }
+    int32_t a = len;
+    for (int base = 0; base < len; base += 32) {
+        const int i = base + lane;
+        bool ok = true;
+        if (i < len) {
+            if (v.probs == nullptr) {
+                ok = v.block[o + i] == v.target[int64_t(r) * (v.P + 1) + i];
+            } else {
+                float q = v.qprobs ? v.qprobs[o + i] : 1.0f;
+                if (v.point_mass && v.point_mass[o + i]) q = 1.0f;   // the point-mass rewrite
+                ok = __fmul_rn(v.u[o + i], q) < v.probs[o + i];
+            }
+        }
+        const unsigned bad = __ballot_sync(0xffffffffu, !ok);
+        if (bad) {
+            a = base + __ffs(bad) - 1;
+            break;
+        }
+    }
+    for (int i = lane; i <= v.P; i += 32)
+        commit[i] = i < a ? v.block[o + i] : (i == a ? v.target[int64_t(r) * (v.P + 1) + a] : -1);
+    if (lane == 0) {
+        v.out_accepted[r] = a;
+        v.out_ncommit[r] = a + 1;
+    }
+}
+
 // splitmix64's output mix (Steele, Lea and Flood, "Fast splittable pseudorandom
 // number generators", OOPSLA 2014).
 __device__ inline uint64_t mix64(uint64_t x) {

@@ -25,6 +25,7 @@
 // hash.
 
 #include "lookup_index.h"
+#include "lookup_loop.h"
 
 #include "common.cuh"
 
@@ -284,9 +285,11 @@ __device__ inline int append_status(const AppendParams &p, bool ok, int r, int &
 // history or straight from `commit`, so no insertion waits for a write.  Every
 // thread reads the request's old length first; after a barrier (no thread reads
 // it any more) one thread writes the new length and the status, so the append
-// is one launch.
-template <int kMaxLen>
-__global__ void __launch_bounds__(kAppendThreads) index_append_request_kernel(AppendParams p) {
+// is one launch.  VERIFY: warp 0 first verifies the request's block into v's
+// outputs (lookup_verify's rule, for that request), which p.commit and p.ncommit
+// point at; after a barrier the CTA appends what it committed.
+template <int kMaxLen, bool VERIFY>
+__global__ void __launch_bounds__(kAppendThreads) index_append_request_kernel(AppendParams p, lkd::VerifyIO v) {
     wait_for_prerequisite_grid();
     allow_dependent_launch();
     const bool ok = header_ok(p.hd, p.min_m, p.max_m, p.hash_bits, p.slots);
@@ -294,6 +297,10 @@ __global__ void __launch_bounds__(kAppendThreads) index_append_request_kernel(Ap
     const int nl = p.max_m - p.min_m + 1;
     const int64_t per_r = int64_t(p.W) * nl;
     for (int r = blockIdx.x; r < p.B; r += gridDim.x) {
+        if (VERIFY) {
+            if (threadIdx.x < 32) lkd::verify_warp(v, r, threadIdx.x);
+            __syncthreads();                                 // the commit row and count are written
+        }
         int L, n;
         int64_t base;
         const int st = append_status(p, ok, r, L, n, base);
@@ -593,6 +600,18 @@ int lookup_index_build(const int32_t *tokens, const int64_t *base, const int32_t
     return rc;
 }
 
+// A CTA per request, sized to its tasks (a warp at least, kAppendThreads at most),
+// when every request gets one in a single wave: the append is one launch.  Larger
+// batches spread the tasks densely over the threads and set the lengths in a
+// second launch (one CTA per request would take several waves).
+bool one_wave_append(int32_t B, int32_t W, int32_t min_m, int32_t max_m, int sms, unsigned &block) {
+    const int64_t per_r = int64_t(W) * (max_m - min_m + 1);
+    const int64_t b = per_r < 32 ? 32 : (per_r >= kAppendThreads ? kAppendThreads : (per_r + 31) / 32 * 32);
+    const int64_t wave = int64_t(sms) * (2048 / b < 32 ? 2048 / b : 32);   // resident CTAs
+    block = unsigned(b);
+    return B <= wave;
+}
+
 int lookup_index_append(int32_t *tokens, const int64_t *base, int32_t *len, const int32_t *cap, const int32_t *commit,
                         const int32_t *ncommit, int32_t B, int32_t W, int32_t min_m, int32_t max_m, void *index,
                         int64_t slots, int32_t hash_bits, int32_t *out_status, struct CUstream_st *stream) {
@@ -620,18 +639,13 @@ int lookup_index_append(int32_t *tokens, const int64_t *base, int32_t *len, cons
     p.min_m = min_m;
     p.max_m = max_m;
     p.hash_bits = hash_bits;
-    // A CTA per request, sized to its tasks (a warp at least, kAppendThreads at
-    // most), when every request gets one in a single wave: one launch.  Larger
-    // batches spread the tasks densely over the threads and set the lengths in a
-    // second launch (one CTA per request would take several waves).
-    const int64_t per_r = int64_t(W) * (max_m - min_m + 1);
-    const int64_t block = per_r < 32 ? 32 : (per_r >= kAppendThreads ? kAppendThreads : (per_r + 31) / 32 * 32);
-    const int64_t wave = int64_t(sms) * (2048 / block < 32 ? 2048 / block : 32);   // resident CTAs
+    unsigned block = 0;
     // the token window in registers: 16 entries when max_m allows, else 32
-    if (B <= wave)
-        return launch_pdl(max_m <= 16 ? index_append_request_kernel<16>
-                                      : index_append_request_kernel<LOOKUP_DRAFT_MAX_M>,
-                          unsigned(B), unsigned(block), stream, p);
+    if (one_wave_append(B, W, min_m, max_m, sms, block))
+        return lkd::launch_pdl2(max_m <= 16 ? index_append_request_kernel<16, false>
+                                            : index_append_request_kernel<LOOKUP_DRAFT_MAX_M, false>,
+                                unsigned(B), block, stream, p, lkd::VerifyIO{});
+    const int64_t per_r = int64_t(W) * (max_m - min_m + 1);
     const int64_t tasks = int64_t(B) * per_r;
     const int64_t want = (tasks + kAppendThreads - 1) / kAppendThreads;
     const unsigned grid = unsigned(want < int64_t(sms) * 8 ? (want > 0 ? want : 1) : int64_t(sms) * 8);
@@ -641,6 +655,55 @@ int lookup_index_append(int32_t *tokens, const int64_t *base, int32_t *len, cons
     const unsigned grid2 = unsigned((int64_t(B) + kAppendThreads - 1) / kAppendThreads);
     return launch_pdl(append_len_kernel, grid2 < unsigned(sms * 4) ? grid2 : unsigned(sms * 4), unsigned(kAppendThreads),
                       stream, p);
+}
+
+int lookup_index_verify_append(const int32_t *block, const int32_t *block_len, const int32_t *target,
+                               const float *probs, const float *qprobs, const int32_t *point_mass, const float *u,
+                               int32_t B, int32_t P, int32_t *tokens, const int64_t *base, int32_t *len,
+                               const int32_t *cap, int32_t min_m, int32_t max_m, void *index, int64_t slots,
+                               int32_t hash_bits, int32_t *out_accepted, int32_t *out_commit, int32_t *out_ncommit,
+                               int32_t *out_status, struct CUstream_st *stream) {
+    lkd::TraceRange trace_("lookup_index_verify_append");
+    if (B < 0 || P < 0 || P > lkd::kMaxBlock || !params_ok(min_m, max_m, hash_bits, slots)) return LOOKUP_DRAFT_EINVAL;
+    if (B == 0) return LOOKUP_DRAFT_OK;
+    if ((P > 0 && !block) || !block_len || !target || (probs && !u) || !out_accepted || !out_commit || !out_ncommit)
+        return LOOKUP_DRAFT_EINVAL;
+    if (!tokens || !base || !len || !cap || !index || !aligned16(index)) return LOOKUP_DRAFT_EINVAL;
+    int sms = 0;
+    int rc = sm_count(&sms);
+    if (rc != LOOKUP_DRAFT_OK) return rc;
+    const int32_t W = P + 1;
+    unsigned threads = 0;
+    if (!one_wave_append(B, W, min_m, max_m, sms, threads)) {
+        // several waves: the two steps as two calls (the dense append reads every
+        // request's commit row, so all of them are verified first)
+        rc = lookup_verify(block, block_len, target, probs, qprobs, point_mass, u, B, P, out_accepted, out_commit,
+                           out_ncommit, stream);
+        if (rc != LOOKUP_DRAFT_OK) return rc;
+        return lookup_index_append(tokens, base, len, cap, out_commit, out_ncommit, B, W, min_m, max_m, index, slots,
+                                   hash_bits, out_status, stream);
+    }
+    AppendParams p{};
+    p.tokens = tokens;
+    p.base = base;
+    p.len = len;
+    p.cap = cap;
+    p.commit = out_commit;
+    p.ncommit = out_ncommit;
+    p.hd = static_cast<Header *>(index);
+    p.tab = reinterpret_cast<Slot *>(static_cast<char *>(index) + sizeof(Header));
+    p.status = out_status;
+    p.slots = slots;
+    p.B = B;
+    p.W = W;
+    p.min_m = min_m;
+    p.max_m = max_m;
+    p.hash_bits = hash_bits;
+    const lkd::VerifyIO v{block, block_len, target, probs, qprobs, point_mass, u, out_accepted, out_commit,
+                          out_ncommit, P};
+    return lkd::launch_pdl2(max_m <= 16 ? index_append_request_kernel<16, true>
+                                        : index_append_request_kernel<LOOKUP_DRAFT_MAX_M, true>,
+                            unsigned(B), threads, stream, p, v);
 }
 
 int lookup_index_draft(const int32_t *tokens, const int64_t *base, const int32_t *len, int32_t B, int32_t min_m,

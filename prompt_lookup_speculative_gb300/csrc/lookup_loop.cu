@@ -32,7 +32,7 @@ using lkd::allow_dependent_launch;
 using lkd::launch_pdl;
 using lkd::wait_for_prerequisite_grid;
 
-constexpr int kMaxBlock = 1 << 16;        // H + T (a verify block) at most
+using lkd::kMaxBlock;                      // H + T (a verify block) at most
 constexpr int kScanThreads = 1024;       // offsets_kernel
 constexpr int kCopyThreads = 256;        // append_kernel
 constexpr int kCopyCtasPerSm = 3;
@@ -240,17 +240,8 @@ __global__ void policy_kernel(PolicyParams p) {
 
 // ------------------------------------------------------------ verification ----
 struct VerifyParams {
-    const int32_t *block;
-    const int32_t *len;
-    const int32_t *target;
-    const float *probs;
-    const float *qprobs;
-    const int32_t *point_mass;
-    const float *u;
-    int32_t *out_accepted;
-    int32_t *out_commit;
-    int32_t *out_ncommit;
-    int32_t B, P;
+    lkd::VerifyIO io;
+    int32_t B;
 };
 
 constexpr int kVerifyWarps = 4;
@@ -260,45 +251,9 @@ constexpr int kVerifyWarps = 4;
 __global__ void verify_kernel(VerifyParams p) {
     wait_for_prerequisite_grid();
     allow_dependent_launch();
-    const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * kVerifyWarps + (threadIdx.x >> 5);
     if (r >= p.B) return;
-    const int64_t o = int64_t(r) * p.P;
-    const int32_t len = p.len[r];
-    int32_t *commit = p.out_commit + int64_t(r) * (p.P + 1);
-    if (len < 0 || len > p.P) {                          // no valid block: an error row
-        for (int i = lane; i <= p.P; i += 32) commit[i] = -1;
-        if (lane == 0) {
-            p.out_accepted[r] = -1;
-            p.out_ncommit[r] = 0;
-        }
-        return;
-    }
-    int32_t a = len;
-    for (int base = 0; base < len; base += 32) {
-        const int i = base + lane;
-        bool ok = true;
-        if (i < len) {
-            if (p.probs == nullptr) {
-                ok = p.block[o + i] == p.target[int64_t(r) * (p.P + 1) + i];
-            } else {
-                float q = p.qprobs ? p.qprobs[o + i] : 1.0f;
-                if (p.point_mass && p.point_mass[o + i]) q = 1.0f;   // the point-mass rewrite
-                ok = __fmul_rn(p.u[o + i], q) < p.probs[o + i];
-            }
-        }
-        const unsigned bad = __ballot_sync(0xffffffffu, !ok);
-        if (bad) {
-            a = base + __ffs(bad) - 1;
-            break;
-        }
-    }
-    for (int i = lane; i <= p.P; i += 32)
-        commit[i] = i < a ? p.block[o + i] : (i == a ? p.target[int64_t(r) * (p.P + 1) + a] : -1);
-    if (lane == 0) {
-        p.out_accepted[r] = a;
-        p.out_ncommit[r] = a + 1;
-    }
+    lkd::verify_warp(p.io, r, threadIdx.x & 31);
 }
 
 // ------------------------------------------------------------------ append ----
@@ -691,7 +646,7 @@ int lookup_verify(const int32_t *block, const int32_t *len, const int32_t *targe
     if (B == 0) return LOOKUP_DRAFT_OK;
     if ((P > 0 && !block) || !len || !target || (probs && !u) || !out_accepted || !out_commit || !out_ncommit)
         return LOOKUP_DRAFT_EINVAL;
-    VerifyParams p{block, len, target, probs, qprobs, point_mass, u, out_accepted, out_commit, out_ncommit, B, P};
+    VerifyParams p{{block, len, target, probs, qprobs, point_mass, u, out_accepted, out_commit, out_ncommit, P}, B};
     return launch_pdl(verify_kernel, blocks_for(B, kVerifyWarps), unsigned(kVerifyWarps * 32), stream, p);
 }
 

@@ -279,3 +279,115 @@ def test_index_decode_loop_with_plan(name):
         assert (host(idx.append(t, b, n, capd, dev(com_o), dev(nc_o))) == 0).all()
         cur_t, cur_o = oracle.append(cur_t, cur_o, com_o, nc_o)
         committed = nc_o
+
+
+# --------------------------------------------------- verify, then append ----
+def _verify_inputs(B, P, seed, mode):
+    blk, ln, tg, pr, qp, pm, u = gen.loop_verify_inputs(B, P, seed)
+    if mode == "greedy":
+        return (blk, ln, tg), {}
+    return (blk, ln, tg), dict(probs=pr, qprobs=qp, point_mass=pm, u=u)
+
+
+@pytest.mark.parametrize("mode", ["greedy", "sampled"])
+@pytest.mark.parametrize("name", ["tiny", "recitation25k", "chats"])
+def test_index_verify_append_is_verify_then_append(name, mode):
+    """recitation25k and tiny: one launch (a CTA per request verifies, then
+    appends); chats (4,096 requests, more than one wave): the two calls."""
+    w = gen.make_workload(name)
+    P = 15
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, 3 * (P + 1), seed=w.seed)
+    idx, t, b, n = built(st, base, length, w.min_m, w.max_m)
+    (blk, ln, tg), smp = _verify_inputs(w.B, P, w.seed, mode)
+    acc_o, com_o, nc_o = oracle.verify(blk, ln, tg, **smp)
+    acc, com, nc, status = idx.verify_append(dev(blk), dev(ln), dev(tg), t, b, n, dev(cap),
+                                             **{k: dev(v) for k, v in smp.items()})
+    for nm, g, e in (("accepted", acc, acc_o), ("commit", com, com_o), ("ncommit", nc, nc_o)):
+        np.testing.assert_array_equal(host(g), e, err_msg=nm)
+    assert (host(status) == 0).all()
+    cur_t, cur_o = oracle.append(w.tokens, w.offsets, com_o, nc_o)
+    got_t, got_o = gen.csr_of_slabs(host(t), base, host(n))
+    np.testing.assert_array_equal(got_o, cur_o)
+    np.testing.assert_array_equal(got_t, cur_t)
+    check_draft(idx.draft(t, b, n, w.K), oracle.lookup_draft(cur_t, cur_o, w.min_m, w.max_m, w.K, threads=16))
+
+
+def test_index_verify_append_error_rows_and_full_slabs():
+    """A block length outside [0, P] gives the header's error row (accepted -1, no
+    committed token, commit row -1) and appends nothing; a request whose slab
+    cannot hold its committed tokens gets status 1 and keeps its history, while
+    its verification outputs are still written."""
+    w = gen.make_workload("recitation25k")
+    P = 15
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, P + 1, seed=w.seed)
+    cap = cap.copy()
+    (blk, ln, tg), _ = _verify_inputs(w.B, P, 7, "greedy")
+    bad = np.zeros(w.B, bool)
+    bad[[3, 17]] = True
+    ln_bad = ln.copy()
+    ln_bad[3], ln_bad[17] = -1, P + 4
+    full = np.zeros(w.B, bool)
+    full[[5, 40]] = True
+    cap[full] = length[full]                              # no room at all: any commit overflows
+    idx, t, b, n = built(st, base, length, w.min_m, w.max_m)
+    ok = ~bad
+    acc_o, com_o, nc_o = oracle.verify(blk[ok], ln[ok], tg[ok])
+    acc, com, nc, status = idx.verify_append(dev(blk), dev(ln_bad), dev(tg), t, b, n, dev(cap))
+    acc, com, nc, status = host(acc), host(com), host(nc), host(status)
+    np.testing.assert_array_equal(acc[ok], acc_o)
+    np.testing.assert_array_equal(com[ok], com_o)
+    np.testing.assert_array_equal(nc[ok], nc_o)
+    assert (acc[bad] == -1).all() and (nc[bad] == 0).all() and (com[bad] == -1).all()
+    want_status = np.where(full & ok, 1, 0)
+    np.testing.assert_array_equal(status, want_status)
+    nc_eff = np.zeros(w.B, np.int32)
+    nc_eff[ok] = nc_o
+    nc_eff[full] = 0
+    com_eff = np.full((w.B, P + 1), -1, np.int32)
+    com_eff[ok] = com_o
+    cur_t, cur_o = oracle.append(w.tokens, w.offsets, com_eff, nc_eff)
+    got_t, got_o = gen.csr_of_slabs(host(t), base, host(n))
+    np.testing.assert_array_equal(got_o, cur_o)
+    np.testing.assert_array_equal(got_t, cur_t)
+    check_draft(idx.draft(t, b, n, w.K), oracle.lookup_draft(cur_t, cur_o, w.min_m, w.max_m, w.K, threads=16))
+
+
+@pytest.mark.parametrize("name", ["recitation25k", "periodic"])
+def test_index_decode_loop_in_two_launches(name):
+    """The decode loop on the index with lookup_index_draft_plan and
+    lookup_index_verify_append (two launches a step), four steps, against the
+    oracle's draft -> schedule -> fuse -> verify -> append."""
+    w = gen.make_workload(name)
+    H, T = 7, 8
+    P = H + T
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, 5 * (P + 1), seed=w.seed)
+    idx, t, b, n = built(st, base, length, w.min_m, w.max_m)
+    capd = dev(cap)
+    B = w.B
+    cur_t, cur_o = w.tokens, w.offsets
+    st_o = np.zeros((B, 3), np.int32)
+    st_g = dev(st_o)
+    committed = np.full(B, H + 1, np.int32)
+    for step in range(4):
+        d_o, l_o, p_o, m_o = oracle.lookup_draft(cur_t, cur_o, w.min_m, w.max_m, P, threads=16)
+        md, _, _ = _plan_inputs(B, H, T, d_o, step)
+        lg_o = oracle.schedule(m_o, committed, st_o, H, T)
+        blk_o, len_o, pm_o = oracle.fuse(d_o, m_o, md, lg_o, H, T)
+        lg, blk, ln, pm, ml, dl, fb = idx.draft_plan(t, b, n, dev(md), dev(committed), st_g, H, T)
+        np.testing.assert_array_equal(host(blk), blk_o, err_msg=f"block, step {step}")
+        np.testing.assert_array_equal(host(ln), len_o, err_msg=f"len, step {step}")
+        rng = gen.rng_for(step, 45)
+        target = rng.integers(0, 50, size=(B, P + 1)).astype(np.int32)
+        f = rng.integers(0, P + 1, size=B)
+        for r in range(B):
+            target[r, :f[r]] = blk_o[r, :f[r]]
+        acc_o, com_o, nc_o = oracle.verify(blk_o, len_o, target)
+        acc, com, nc, status = idx.verify_append(blk, ln, dev(target), t, b, n, capd)
+        np.testing.assert_array_equal(host(nc), nc_o, err_msg=f"ncommit, step {step}")
+        np.testing.assert_array_equal(host(com), com_o, err_msg=f"commit, step {step}")
+        assert (host(status) == 0).all()
+        cur_t, cur_o = oracle.append(cur_t, cur_o, com_o, nc_o)
+        committed = nc_o
+    got_t, got_o = gen.csr_of_slabs(host(t), base, host(n))
+    np.testing.assert_array_equal(got_t, cur_t)
+    np.testing.assert_array_equal(got_o, cur_o)

@@ -385,3 +385,29 @@ def test_index_draft_plan_rejects_bad_parameters(lib):
     assert call(a6=F + 8) == -1             # misaligned index
     assert lib.lookup_index_draft_plan(None, None, None, 0, 4, 12, None, 1024, 64, None, None, 7, 8, 8, 6, 2, 4, 1, 2,
                                        3, None, None, None, None, None, None, None, None, None) == 0
+
+
+def test_index_verify_append_rejects_bad_parameters(lib):
+    F = FAKE
+    # block, block_len, target, probs, qprobs, point_mass, u, B, P, tokens, base, len, cap, min_m, max_m, index,
+    # slots, hash_bits, out_accepted, out_commit, out_ncommit, out_status, stream
+    ok = [F, F, F, None, None, None, None, 4, 15, F, F, F, F, 4, 12, F, 1024, 64, F, F, F, None, None]
+    assert len(ok) == 23
+
+    def call(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return lib.lookup_index_verify_append(*a)
+
+    assert call(a8=-1) == -1                # P < 0
+    assert call(a8=(1 << 16) + 1) == -1     # P above the verify block limit
+    assert call(a3=F) == -1                 # probs without u
+    assert call(a0=None) == -1              # no block with P > 0
+    assert call(a19=None) == -1             # no commit output
+    assert call(a12=None) == -1             # no cap
+    assert call(a16=1000) == -1             # slots not a power of two
+    assert call(a14=3) == -1                # max_m < min_m
+    assert call(a15=F + 8) == -1            # misaligned index
+    assert call(a7=-1) == -1                # B < 0
+    assert call(a7=0, a0=None, a1=None, a2=None, a9=None, a15=None) == 0   # B == 0: nothing to do
