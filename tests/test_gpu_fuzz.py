@@ -13,7 +13,8 @@ Each case is compared element by element with the oracle: the draft, its
 length, the position and m.  The two-launch loop path (draft, then scheduling
 and fusion) is swept the same way against the oracle's draft, schedule and fuse,
 and the incremental index and the context cache over random 3-step decode loops
-(draft, commit, append in place).
+(draft, commit, append in place), the index also in its two-launch form (draft
+with scheduling and fusion, then verification with the append).
 """
 from __future__ import annotations
 
@@ -214,3 +215,72 @@ def test_context_cache_matches_oracle_on_random_decode_loops(case):
         status = cc.append(t, b, n, capd, torch.from_numpy(commit).to(DEV), torch.from_numpy(ncommit).to(DEV))
         assert (status.cpu().numpy() == 0).all(), label
         cur_t, cur_o = oracle.append(cur_t, cur_o, commit, ncommit)
+
+
+@pytest.mark.parametrize("case", range(10))
+def test_index_two_launch_loop_matches_oracle_on_random_decode_loops(case):
+    """The decode loop on the index in two launches a step (lookup_index_draft_plan,
+    then lookup_index_verify_append) on random batches, block shapes, thresholds,
+    key widths (3 bits: most requests on the fallback) and greedy or sampled
+    verification with the block's point masses, against the oracle's draft,
+    schedule, fuse, verify and append over three steps."""
+    rng = np.random.default_rng(50260 + case)
+    tokens, offsets = small_random_batch(rng)
+    B = offsets.size - 1
+    min_m = int(rng.integers(1, 7))
+    max_m = int(rng.integers(min_m, 33))
+    H = int(rng.integers(1, 33))
+    T = int(rng.integers(0, 65 - H))
+    P = H + T
+    agree_n = int(rng.integers(0, H + 1))
+    kw = dict(replace_min=int(rng.integers(1, 13)), agree_min=int(rng.integers(1, 13)), agree_n=agree_n,
+              tail_min=int(rng.integers(1, 13)), slack=int(rng.integers(0, 4)),
+              enter_steps=int(rng.integers(1, 4)), sticky=int(rng.integers(0, 5)))
+    hash_bits = int(rng.choice([64, 64, 3]))
+    sampled = bool(rng.random() < 0.5)
+    st, base, length, cap = gen.slabs_from_batch(tokens, offsets, 4 * (P + 1), seed=case)
+    t, b, n = (torch.from_numpy(np.ascontiguousarray(a)).to(DEV) for a in (st, base, length))
+    capd = torch.from_numpy(cap).to(DEV)
+    idx = pkg.NgramIndex(st.shape[0], min_m, max_m, hash_bits=hash_bits)
+    idx.build(t, b, n)
+    cur_t, cur_o = tokens, offsets
+    st_o = np.zeros((B, 3), np.int32)
+    st_g = torch.from_numpy(st_o.copy()).to(DEV)
+    committed = np.full(B, H + 1, np.int32)
+    label = f"case {case}: B={B} m=[{min_m},{max_m}] H={H} T={T} bits={hash_bits} sampled={sampled} {kw}"
+    for step in range(3):
+        d_o, l_o, p_o, m_o = oracle.lookup_draft(cur_t, cur_o, min_m, max_m, P, threads=16)
+        md = rng.integers(-2, 4, size=(B, H)).astype(np.int32)
+        take = rng.random(B) < 0.5
+        md[take] = d_o[take, :H]
+        lg_o = oracle.schedule(m_o, committed, st_o, H, T, tail_min=kw["tail_min"], slack=kw["slack"],
+                               enter_steps=kw["enter_steps"], sticky=kw["sticky"])
+        blk_o, len_o, pm_o = oracle.fuse(d_o, m_o, md, lg_o, H, T, replace_min=kw["replace_min"],
+                                         agree_min=kw["agree_min"], agree_n=agree_n, tail_min=kw["tail_min"])
+        lg, blk, ln, pm, ml, dl, fb = idx.draft_plan(t, b, n, torch.from_numpy(md).to(DEV),
+                                                     torch.from_numpy(committed).to(DEV), st_g, H, T, **kw)
+        at = f"{label} step {step}"
+        for name, g, w in (("long", lg, lg_o), ("block", blk, blk_o), ("len", ln, len_o), ("point mass", pm, pm_o),
+                           ("mlen", ml, m_o), ("draft len", dl, l_o), ("state", st_g, st_o)):
+            np.testing.assert_array_equal(g.cpu().numpy(), w, err_msg=f"{at}: {name}")
+        target = rng.integers(-3, 50, size=(B, P + 1)).astype(np.int32)
+        f = rng.integers(0, P + 1, size=B)
+        for r in range(B):
+            target[r, :f[r]] = blk_o[r, :f[r]]
+        smp = {}
+        if sampled:
+            smp = dict(probs=rng.random((B, P), dtype=np.float32),
+                       qprobs=(1.0 - rng.random((B, P), dtype=np.float32)).astype(np.float32),
+                       u=rng.random((B, P), dtype=np.float32))
+        acc_o, com_o, nc_o = oracle.verify(blk_o, len_o, target, point_mass=pm_o if sampled else None, **smp)
+        acc, com, nc, status = idx.verify_append(blk, ln, torch.from_numpy(target).to(DEV), t, b, n, capd,
+                                                 **({k: torch.from_numpy(v).to(DEV) for k, v in smp.items()}
+                                                    | ({"point_mass": pm} if sampled else {})))
+        for name, g, w in (("accepted", acc, acc_o), ("commit", com, com_o), ("ncommit", nc, nc_o)):
+            np.testing.assert_array_equal(g.cpu().numpy(), w, err_msg=f"{at}: {name}")
+        assert (status.cpu().numpy() == 0).all(), at
+        cur_t, cur_o = oracle.append(cur_t, cur_o, com_o, nc_o)
+        got_t, got_o = gen.csr_of_slabs(t.cpu().numpy(), base, n.cpu().numpy())
+        np.testing.assert_array_equal(got_o, cur_o, err_msg=at)
+        np.testing.assert_array_equal(got_t, cur_t, err_msg=at)
+        committed = nc_o
