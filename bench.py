@@ -741,6 +741,7 @@ def measure_loop(lib, pkg, w, dev, stream, toks, offs, reps: int) -> dict:
     # the append's algorithmic bytes: every history token read and written once,
     # the committed tokens read and written, the counts and both offset arrays
     committed_tokens = int(ncommit.sum().item())
+    res["loop_step_committed_per_request"] = round(committed_tokens / max(B, 1), 2)
     append_bytes = 8 * w.total_tokens + 8 * committed_tokens + 4 * B + 16 * (B + 1)
     res = {k: (round(v, 3) if isinstance(v, float) else v) for k, v in res.items()}
     res["append_algorithmic_bytes"] = append_bytes
@@ -856,11 +857,19 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
     model_draft = torch.from_numpy(rng.integers(0, 50, size=(B, H)).astype(np.int32)).to(dev)
     state = torch.zeros((B, 3), dtype=i32, device=dev)
     long_block = torch.zeros(B, dtype=i32, device=dev)
-    committed = torch.full((B,), H + 1, dtype=i32, device=dev)
+    committed = torch.full((B,), H + T + 1, dtype=i32, device=dev)   # as in the scan's loop step
     block = torch.empty((B, P), dtype=i32, device=dev)
     blen = torch.empty(B, dtype=i32, device=dev)
     pm = torch.empty((B, P), dtype=i32, device=dev)
     target = torch.from_numpy(rng.integers(0, 50, size=(B, P + 1)).astype(np.int32)).to(dev)
+    # Verification by the sampled rule (u * 1 < p) with draws that accept exactly the
+    # first f[r] positions, f uniform in [0, P] as the scan's loop step's target
+    # agreement: the same commits per step whatever tokens the growing histories
+    # put in the block (a fixed greedy target would agree with almost none).
+    f = rng.integers(0, P + 1, size=B)
+    probs = torch.full((B, P), 0.5, dtype=torch.float32, device=dev)
+    u = torch.from_numpy(np.where(np.arange(P)[None, :] < f[:, None], 0.0, 0.75).astype(np.float32)).to(dev)
+    pp, up = probs.data_ptr(), u.data_ptr()
     accepted = torch.empty(B, dtype=i32, device=dev)
     commit = torch.empty((B, P + 1), dtype=i32, device=dev)
     ncommit = torch.empty(B, dtype=i32, device=dev)
@@ -871,7 +880,7 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
                                   long_block.data_ptr(), h))
         check(lib.lookup_fuse(draft.data_ptr(), dm.data_ptr(), model_draft.data_ptr(), long_block.data_ptr(), B,
                               P, H, T, 8, 6, 2, 4, block.data_ptr(), blen.data_ptr(), pm.data_ptr(), h))
-        check(lib.lookup_verify(block.data_ptr(), blen.data_ptr(), target.data_ptr(), None, None, None, None, B, P,
+        check(lib.lookup_verify(block.data_ptr(), blen.data_ptr(), target.data_ptr(), pp, None, None, up, B, P,
                                 accepted.data_ptr(), commit.data_ptr(), ncommit.data_ptr(), h))
         check(lib.lookup_index_append(tp, bp, lp, cp, commit.data_ptr(), ncommit.data_ptr(), B, P + 1, w.min_m,
                                       w.max_m, mem, idx.slots, 64, status.data_ptr(), h))
@@ -900,7 +909,7 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
                                           model_draft.data_ptr(), committed.data_ptr(), H, T, 8, 6, 2, 4, 1, 2, 3,
                                           state.data_ptr(), long_block.data_ptr(), block.data_ptr(), blen.data_ptr(),
                                           pm.data_ptr(), dm.data_ptr(), dlen.data_ptr(), fb.data_ptr(), h))
-        check(lib.lookup_verify(block.data_ptr(), blen.data_ptr(), target.data_ptr(), None, None, None, None, B, P,
+        check(lib.lookup_verify(block.data_ptr(), blen.data_ptr(), target.data_ptr(), pp, None, None, up, B, P,
                                 accepted.data_ptr(), commit.data_ptr(), ncommit.data_ptr(), h))
         check(lib.lookup_index_append(tp, bp, lp, cp, commit.data_ptr(), ncommit.data_ptr(), B, P + 1, w.min_m,
                                       w.max_m, mem, idx.slots, 64, status.data_ptr(), h))
@@ -917,14 +926,15 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
                                           model_draft.data_ptr(), committed.data_ptr(), H, T, 8, 6, 2, 4, 1, 2, 3,
                                           state.data_ptr(), long_block.data_ptr(), block.data_ptr(), blen.data_ptr(),
                                           pm.data_ptr(), dm.data_ptr(), dlen.data_ptr(), fb.data_ptr(), h))
-        check(lib.lookup_index_verify_append(block.data_ptr(), blen.data_ptr(), target.data_ptr(), None, None, None,
-                                             None, B, P, tp, bp, lp, cp, w.min_m, w.max_m, mem, idx.slots, 64,
+        check(lib.lookup_index_verify_append(block.data_ptr(), blen.data_ptr(), target.data_ptr(), pp, None, None,
+                                             up, B, P, tp, bp, lp, cp, w.min_m, w.max_m, mem, idx.slots, 64,
                                              accepted.data_ptr(), commit.data_ptr(), ncommit.data_ptr(),
                                              status.data_ptr(), h))
 
     loop_two_us = timed(loop_two_call, 16, 4)             # 80 steps again
     torch.cuda.synchronize(dev)
     room_ok = room_ok and bool((status == 0).all().item())
+    committed_mean = float(ncommit.float().mean().item())  # the last step's, per request
     total_tokens = int(st.shape[0])
     res = {
         "layout": f"slabs with {INDEX_SPARE} tokens of room per request",
@@ -940,6 +950,8 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
         "loop_step_plan_launches": launches["loop_plan_call"],
         "loop_step_two_call_us": round(loop_two_us, 3),
         "loop_step_two_call_launches": launches["loop_two_call"],
+        "loop_step_committed_per_request": round(committed_mean, 2),
+        "loop_step_verify": "sampled rule, draws accepting the first f positions, f uniform in [0, P]",
         "draft_launches": launches["draft_call"],
         "append8_launches": launches["append_call"],
         "parity_with_oracle": bool(parity),
