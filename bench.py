@@ -98,6 +98,9 @@ def parse_args(argv=None):
                     help="skip the step and scan timings of every workload")
     ap.add_argument("--loop-only", action="store_true",
                     help="time only the decode-loop steps (replays = steps / copies of the batch)")
+    ap.add_argument("--size-sweep", action="store_true",
+                    help="time the step, the scan and the read floor on the recitation recipe at history "
+                         "lengths 4,096 to 400,000 tokens (B = 64) and fit a fixed cost plus a rate to each")
     return ap.parse_args(argv)
 
 
@@ -248,6 +251,13 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     torch.cuda.set_device(dev)
     dist = dist_init(world, "nccl")
     lib = pkg.load_library()
+
+    if args.size_sweep:
+        if rank == 0:
+            print(json.dumps(size_sweep(lib, pkg, dev, max(10, min(200, args.steps)))), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
 
     seed = rank_seed(gen.DEFAULT_SEED[args.workload] if args.seed is None else args.seed, rank)
     w = gen.make_workload(args.workload, seed)
@@ -1153,6 +1163,49 @@ def time_workload(lib, pkg, w, dev, stream, l2: int, reps_cap: int, with_floor: 
     del toks, offs, ws
     torch.cuda.synchronize(dev)
     return res
+
+
+SWEEP_LENGTHS = (4096, 8192, 16384, 25000, 50000, 100000, 200000, 400000)
+
+
+def size_sweep(lib, pkg, dev, reps_cap: int) -> dict:
+    """The step, the scan and the plain-read floor against history size: the
+    recitation recipe (B = 64, gen.make_workload(..., length=L)) at each length of
+    SWEEP_LENGTHS, timed by time_workload like the main line, each checked
+    against the oracle.  A least-squares line time = fixed + bytes / rate is fitted
+    to the scan's and to the floor's times; from it, the history size at which
+    each would reach 60% of the measured copy bandwidth."""
+    import numpy as np
+    import torch
+
+    import gen
+
+    peak, _ = measured_hbm_peak()
+    stream = torch.cuda.Stream(dev)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2**20))
+    points = []
+    for L in SWEEP_LENGTHS:
+        w = gen.make_workload("recitation25k", length=L)
+        r = time_workload(lib, pkg, w, dev, stream, l2, reps_cap, True)
+        r["L"] = L
+        points.append(r)
+    mb = np.array([p["history_bytes"] for p in points], dtype=np.float64)
+    fit = {}
+    for name, key in (("scan", "scan_us"), ("read_floor", "read_floor_us")):
+        t = np.array([p[key] for p in points], dtype=np.float64)
+        slope, fixed = np.polyfit(mb, t, 1)                  # us per byte, us
+        rate = 1e-3 / slope                                  # GB/s (bytes / us / 1e3)
+        # bytes b with b / (fixed + b / rate) = 0.6 * peak, if the rate allows it
+        want = 0.6 * peak
+        b60 = (want * fixed * 1e3 / (1.0 - want / rate)) if rate > want else None
+        fit[name] = {"fixed_us": round(float(fixed), 3), "rate_gbs": round(float(rate), 1),
+                     "rate_frac_of_peak": round(float(rate) / peak, 4),
+                     "bytes_for_60pct": None if b60 is None else int(b60)}
+    return {"metric": "µs per draft step, scan and plain read against history size", "unit": "us",
+            "data": "synthetic", "peak_gbs": peak,
+            "config": {"workload": "recitation recipe, B = 64, L in " + ", ".join(map(str, SWEEP_LENGTHS)),
+                       "l2": "each size over rotating device copies (> 2x L2)"},
+            "size_sweep": points, "fit": fit}
 
 
 def measure_workloads(lib, pkg, dev, stream, names, seed_offset: int, reps_cap: int) -> dict:

@@ -109,9 +109,14 @@ def _choose(rng: np.random.Generator, B: int, frac: float) -> np.ndarray:
     return np.sort(rng.permutation(B)[:n])
 
 
-def make_workload(name: str, seed: int | None = None) -> Workload:
+def make_workload(name: str, seed: int | None = None, length: int | None = None) -> Workload:
+    """The named workload's batch.  ``length`` (recitation25k only, >= 4001)
+    replaces the 25,000-token history length, with every other draw of the
+    recipe unchanged; the workload is then named recitation_L<length>."""
     if name not in WORKLOADS:
         raise KeyError(f"unknown workload {name!r}; known: {WORKLOADS}")
+    if length is not None and (name != "recitation25k" or int(length) < 4001):
+        raise ValueError("length applies to recitation25k only, and must be at least 4001")
     seed = DEFAULT_SEED[name] if seed is None else int(seed)
     rng = rng_for(seed, WORKLOADS.index(name))
     planted: dict = {}
@@ -148,8 +153,10 @@ def make_workload(name: str, seed: int | None = None) -> Workload:
     perm = rng.permutation(VOCAB_QWEN).astype(np.int64)
     if name == "recitation25k":
         B, s, frac = 64, 1.1, 0.3
-        lengths = np.full(B, 25000, dtype=np.int64)
+        lengths = np.full(B, 25000 if length is None else int(length), dtype=np.int64)
         K = 15
+        if length is not None:
+            name = f"recitation_L{int(length)}"
     elif name == "ragged262k":
         B, s, frac = 256, 1.1, 0.2
         lengths = np.floor(np.exp(rng.uniform(np.log(512), np.log(262144), size=B))).astype(np.int64)
@@ -163,7 +170,7 @@ def make_workload(name: str, seed: int | None = None) -> Workload:
     for r in _choose(rng, B, frac):
         r = int(r)
         L = int(lengths[r])
-        if name == "recitation25k":
+        if name.startswith("recitation"):
             span = 2000
             c = int(rng.integers(1, 2001))
             s0 = int(rng.integers(0, L - c - span + 1))
