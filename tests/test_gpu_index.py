@@ -391,3 +391,34 @@ def test_index_decode_loop_in_two_launches(name):
     got_t, got_o = gen.csr_of_slabs(host(t), base, host(n))
     np.testing.assert_array_equal(got_t, cur_t)
     np.testing.assert_array_equal(got_o, cur_o)
+
+
+def test_index_verify_append_with_empty_blocks():
+    """P = 0: no proposals (the block pointer may be NULL); every request commits
+    the target's one token, which the append writes and indexes."""
+    w = gen.make_workload("periodic")
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, 8, seed=w.seed)
+    idx, t, b, n = built(st, base, length, w.min_m, w.max_m)
+    blk = np.zeros((w.B, 0), np.int32)
+    ln = np.zeros(w.B, np.int32)
+    tg = gen.rng_for(5, 46).integers(0, 50, size=(w.B, 1)).astype(np.int32)
+    acc_o, com_o, nc_o = oracle.verify(blk, ln, tg)
+    lib = pkg.load_library()
+    acc = torch.empty(w.B, dtype=torch.int32, device="cuda")
+    com = torch.empty((w.B, 1), dtype=torch.int32, device="cuda")
+    nc = torch.empty(w.B, dtype=torch.int32, device="cuda")
+    status = torch.empty(w.B, dtype=torch.int32, device="cuda")
+    lnd, tgd, capd = dev(ln), dev(tg), dev(cap)
+    rc = lib.lookup_index_verify_append(None, lnd.data_ptr(), tgd.data_ptr(), None, None, None, None, w.B, 0,
+                                        t.data_ptr(), b.data_ptr(), n.data_ptr(), capd.data_ptr(), w.min_m, w.max_m,
+                                        idx.memory.data_ptr(), idx.slots, 64, acc.data_ptr(), com.data_ptr(),
+                                        nc.data_ptr(), status.data_ptr(), None)
+    assert rc == 0
+    np.testing.assert_array_equal(host(acc), acc_o)
+    np.testing.assert_array_equal(host(com), com_o)
+    np.testing.assert_array_equal(host(nc), nc_o)
+    assert (host(status) == 0).all()
+    cur_t, cur_o = oracle.append(w.tokens, w.offsets, com_o, nc_o)
+    got_t, got_o = gen.csr_of_slabs(host(t), base, host(n))
+    np.testing.assert_array_equal(got_t, cur_t)
+    check_draft(idx.draft(t, b, n, w.K), oracle.lookup_draft(cur_t, cur_o, w.min_m, w.max_m, w.K, threads=16))

@@ -116,3 +116,17 @@ def test_capture_counts_once_and_replays_add_nothing(batches):
         g.replay()
     torch.cuda.synchronize()
     assert pkg.launch_count() == n1
+
+
+@pytest.mark.parametrize("name,want", [("recitation25k", 1), ("chats", 3)])
+def test_index_verify_append_launches(batches, name, want):
+    """One launch while every request gets an append CTA in one wave (B = 64);
+    verify, then the dense append and its length pass, above it (B = 4,096)."""
+    w, _, _ = batches[name]
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, 64, seed=w.seed)
+    t, b, n, c = dev(st), dev(base), dev(length), dev(cap)
+    idx = pkg.NgramIndex(st.shape[0], w.min_m, w.max_m)
+    idx.build(t, b, n)
+    P = 15
+    blk, ln, tg, *_ = gen.loop_verify_inputs(w.B, P, 3)
+    assert launches(lambda: idx.verify_append(dev(blk), dev(ln), dev(tg), t, b, n, c)) == want
