@@ -253,6 +253,18 @@ int lookup_draft_read_floor(const void *data, size_t bytes, int32_t ctas_per_sm,
                             uint32_t *out_word, struct CUstream_st *stream);
 
 /*
+ * The same measurement aid with 1-D bulk copies (TMA) into shared memory, the
+ * way the scan reads its history: one CTA of 16 warps per SM, each warp
+ * streaming a contiguous range of the buffer through a ring of three tiles of
+ * up to 3 KB, each waited for on its mbarrier and folded from shared memory.
+ * data/bytes/out_word as for lookup_draft_read_floor.  Its waits are bounded by
+ * the limit lookup_draft_set_wait_limit_ns sets (1 s by default); a warp whose
+ * wait runs out stores 0xFFFFFFFF in *out_word, waits (bounded again) for its
+ * copies in flight and stops, leaving the context usable.
+ */
+int lookup_draft_read_floor_bulk(const void *data, size_t bytes, uint32_t *out_word, struct CUstream_st *stream);
+
+/*
  * Checked build (a debugging aid; the source article has no counterpart).  The
  * drafting step's source also compiles with LOOKUP_DRAFT_CHECKED=1 into a second
  * library with the same entry points.  There, the scan and fill kernels check

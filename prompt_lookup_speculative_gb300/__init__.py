@@ -157,6 +157,8 @@ def _declare_draft(lib: ctypes.CDLL) -> None:
     lib.lookup_draft_set_wait_limit_ns.restype = None
     lib.lookup_draft_read_floor.argtypes = [vp, sz, i32, i32, vp, vp]
     lib.lookup_draft_read_floor.restype = ctypes.c_int
+    lib.lookup_draft_read_floor_bulk.argtypes = [vp, sz, vp, vp]
+    lib.lookup_draft_read_floor_bulk.restype = ctypes.c_int
     lib.lookup_draft_checked_build.argtypes = []
     lib.lookup_draft_checked_build.restype = ctypes.c_int
     lib.lookup_draft_check_word.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
@@ -390,9 +392,11 @@ def _host_ptr(a) -> int:
 
 def read_floor(data, ctas_per_sm: int = 4, threads: int = 256, out=None, stream=None) -> None:
     """Measurement aid: one launch that only streams ``data`` (a CUDA tensor whose
-    byte size is a multiple of 16, 16-byte aligned) on the stream.  ``out`` is a
+    byte size is a multiple of 16, 16-byte aligned) on the stream, with 16-byte
+    loads (``ctas_per_sm`` x ``threads``) or, with ``ctas_per_sm`` = 0, with bulk
+    copies into shared memory (lookup_draft_read_floor_bulk).  ``out`` is a
     one-element int32 CUDA tensor the kernel may write (a fold of the data, in the
-    rare case it equals a fixed pattern)."""
+    rare case it equals a fixed pattern; -1 from the bulk read whose wait ran out)."""
     import torch
     lib = load_library()
     if not (isinstance(data, torch.Tensor) and data.is_cuda and data.is_contiguous()):
@@ -400,12 +404,17 @@ def read_floor(data, ctas_per_sm: int = 4, threads: int = 256, out=None, stream=
     if out is None:
         out = torch.zeros(1, dtype=torch.int32, device=data.device)
     nbytes = data.numel() * data.element_size()
+    if ctas_per_sm == 0:                 # the bulk-copy (TMA) read: one CTA per SM, threads ignored
+        _check(lib.lookup_draft_read_floor_bulk(data.data_ptr(), nbytes, out.data_ptr(), _stream_handle(stream)),
+               lib)
+        return
     _check(lib.lookup_draft_read_floor(data.data_ptr(), nbytes, ctas_per_sm, threads, out.data_ptr(),
                                        _stream_handle(stream)), lib)
 
 
 def set_wait_limit_ns(ns: int) -> None:
-    """Diagnostics: limit on each bounded wait inside the scan kernel (0 = default 1 s)."""
+    """Diagnostics: limit on each bounded wait inside the scan and the bulk read
+    floor (0 = default 1 s)."""
     load_library().lookup_draft_set_wait_limit_ns(int(ns))
 
 

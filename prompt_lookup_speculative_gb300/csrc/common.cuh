@@ -15,6 +15,8 @@
 int lookup_record_cuda_error(cudaError_t e, const char *what);
 // Counts one enqueued kernel launch (lookup_draft_launch_count, lookup_draft.cu).
 void lookup_note_launch();
+// The limit on a kernel's bounded waits, in ns (lookup_draft_set_wait_limit_ns).
+uint64_t lookup_wait_limit_ns();
 
 namespace lkd {
 
@@ -170,6 +172,81 @@ __device__ inline void verify_warp(const VerifyIO &v, int r, int lane) {
     if (lane == 0) {
         v.out_accepted[r] = a;
         v.out_ncommit[r] = a + 1;
+    }
+}
+
+// Shared memory addresses, mbarriers, 1-D bulk copies (TMA) and the global timer.
+__device__ inline uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ inline void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ inline void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ inline void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ inline void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.  Both
+// addresses and the size are multiples of 16 bytes.
+__device__ inline void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// The same copy with an L2 evict-first policy, for history tiles: each is read
+// once, so the lines that are used again across launches (the kernels' code, the
+// slots, the offsets) are the ones kept in L2.
+__device__ inline void bulk_copy_g2s_stream(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ inline void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+__device__ inline bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ inline uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of `bar` to complete; false once the global timer has
+// passed `deadline_ns` (checked before every try, so a past deadline fails at once).
+__device__ inline bool mbar_wait_until(uint32_t bar, uint32_t parity, uint64_t deadline_ns) {
+    for (;;) {
+        if (global_ns() > deadline_ns) return false;
+        if (mbar_try_wait(bar, parity)) return true;
     }
 }
 

@@ -212,79 +212,18 @@ __device__ inline int64_t vchunk_of_quad(const Partition &P, int64_t x) {
 }
 
 // ----------------------------------------------------------- PTX wrappers ----
-__device__ inline uint32_t smem_addr(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ inline void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ inline void fence_barrier_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ inline void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ inline void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.  Both
-// addresses and the size are multiples of 16 bytes.
-__device__ inline void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-// The same copy with an L2 evict-first policy, for history tiles: each is read
-// once, so the lines that are used again across launches (the kernels' code, the
-// slots, the offsets) are the ones kept in L2.
-__device__ inline void bulk_copy_g2s_stream(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    uint64_t policy;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
-            "r"(dst),
-        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-        : "memory");
-}
-
-__device__ inline void prefetch_l2(const void *p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
-__device__ inline bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ inline uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wait for phase `parity` of `bar` to complete; false once the global timer has
-// passed `deadline_ns` (checked before every try, so a past deadline fails at once).
-__device__ inline bool mbar_wait_until(uint32_t bar, uint32_t parity, uint64_t deadline_ns) {
-    for (;;) {
-        if (global_ns() > deadline_ns) return false;
-        if (mbar_try_wait(bar, parity)) return true;
-    }
-}
+// (common.cuh: shared memory addresses, mbarriers, 1-D bulk copies, the global timer)
+using lkd::bulk_copy_g2s;
+using lkd::bulk_copy_g2s_stream;
+using lkd::fence_barrier_init;
+using lkd::fence_proxy_async_smem;
+using lkd::global_ns;
+using lkd::mbar_expect_tx;
+using lkd::mbar_init;
+using lkd::mbar_try_wait;
+using lkd::mbar_wait_until;
+using lkd::prefetch_l2;
+using lkd::smem_addr;
 
 // ------------------------------------------------------------ scan kernel ----
 // Dynamic shared memory: the warps' tile rings, their mbarriers (plus one for the
@@ -1576,6 +1515,10 @@ __attribute__((visibility("hidden"))) int lookup_record_cuda_error(cudaError_t e
 static std::atomic<uint64_t> g_launches{0};
 
 __attribute__((visibility("hidden"))) void lookup_note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+__attribute__((visibility("hidden"))) uint64_t lookup_wait_limit_ns() {
+    return g_wait_ns.load(std::memory_order_relaxed);
+}
 
 // Fixed scratch of lookup_draft_noalloc (file scope; every GPU that loads the
 // library holds it until the process exits).

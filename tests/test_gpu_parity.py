@@ -360,7 +360,7 @@ def test_host_entry_point_pinned_empty_histories():
     np.testing.assert_array_equal(d, np.full((2, 3), -1, np.int32))
 
 
-@pytest.mark.parametrize("shape", [(1, 32), (2, 512), (4, 256), (8, 256)])
+@pytest.mark.parametrize("shape", [(1, 32), (2, 512), (4, 256), (8, 256), (0, 0)])
 def test_read_floor_streams_without_writing(shape):
     """The measurement aid reads its bytes and leaves the output word alone unless
     their fold hits its fixed pattern (the XOR of 0 .. 2^20 - 1 is 0)."""
@@ -370,6 +370,27 @@ def test_read_floor_streams_without_writing(shape):
     pkg.read_floor(x[:4], *shape, out=out)                   # fewer 16-byte units than threads
     torch.cuda.synchronize()
     assert out.item() == 123
+
+
+def test_bulk_read_floor_wait_runs_out_cleanly():
+    """With a 1 ns wait limit the bulk read's warps give up at their first tile,
+    store -1, let their copies land (bounded by 1 s, not by the limit) and stop;
+    the context stays usable and the next read with the default limit is clean."""
+    x = torch.arange(1 << 24, dtype=torch.int32, device=DEV)      # 64 MB
+    out = torch.full((1,), 123, dtype=torch.int32, device=DEV)
+    try:
+        pkg.set_wait_limit_ns(1)
+        pkg.read_floor(x, 0, 0, out=out)
+        torch.cuda.synchronize()
+    finally:
+        pkg.set_wait_limit_ns(0)
+    assert out.item() == -1
+    out.fill_(123)
+    pkg.read_floor(x, 0, 0, out=out)
+    torch.cuda.synchronize()
+    assert out.item() == 123
+    w = gen.make_workload("tiny", 19)
+    assert_parity(w.tokens, w.offsets, w.min_m, w.max_m, w.K)
 
 
 def test_repeated_calls_and_streams():

@@ -44,7 +44,7 @@ def test_header_declares_the_entry_points():
                  "lookup_fuse", "lookup_schedule", "lookup_verify", "lookup_append", "lookup_index_slots_for",
                  "lookup_index_bytes", "lookup_index_build", "lookup_index_append", "lookup_index_draft",
                  "lookup_ctx_slots_for", "lookup_ctx_bytes", "lookup_ctx_build", "lookup_ctx_append",
-                 "lookup_ctx_draft", "lookup_draft_read_floor"):
+                 "lookup_ctx_draft", "lookup_draft_read_floor", "lookup_draft_read_floor_bulk"):
         assert must in names
 
 
@@ -100,6 +100,15 @@ def test_rejects_null_and_misaligned_pointers(lib):
     assert lib.lookup_draft_scan(FAKE, FAKE, 4, 4, 12, None, 1 << 20, None) == -1
     assert lib.lookup_draft_scan(FAKE, FAKE, 4, 4, 12, FAKE + 4, 1 << 20, None) == -1
     assert lib.lookup_draft_fill(FAKE, FAKE, 4, 4, 12, 15, None, 1 << 20, FAKE, FAKE, FAKE, None, None) == -1
+
+
+def test_bulk_read_floor_checks_its_arguments(lib):
+    assert lib.lookup_draft_read_floor_bulk(FAKE, 1 << 20, None, None) == -1          # no output word
+    assert lib.lookup_draft_read_floor_bulk(FAKE, 1 << 20, FAKE + 2, None) == -1      # misaligned word
+    assert lib.lookup_draft_read_floor_bulk(None, 1 << 20, FAKE, None) == -1          # no data
+    assert lib.lookup_draft_read_floor_bulk(FAKE + 4, 1 << 20, FAKE, None) == -1      # data not 16-byte aligned
+    assert lib.lookup_draft_read_floor_bulk(FAKE, (1 << 20) + 4, FAKE, None) == -1    # size not a multiple of 16
+    assert lib.lookup_draft_read_floor_bulk(None, 0, FAKE, None) == 0                 # nothing to read
 
 
 def test_read_floor_checks_its_arguments(lib):
