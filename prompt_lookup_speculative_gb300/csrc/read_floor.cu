@@ -167,12 +167,18 @@ extern "C" int lookup_draft_read_floor_bulk(const void *data, size_t bytes, uint
     int sms = 0;
     int rc = sm_count(&sms);
     if (rc != LOOKUP_DRAFT_OK) return rc;
-    static std::atomic<bool> attr_set{false};
-    if (!attr_set.load(std::memory_order_acquire)) {
+    // the shared-memory opt-in is a per-device attribute: set once on each device
+    constexpr int kMaxDevices = 64;
+    static std::atomic<bool> attr_set[kMaxDevices];
+    int dev = 0;
+    const cudaError_t ge = cudaGetDevice(&dev);
+    if (ge != cudaSuccess) return lookup_record_cuda_error(ge, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return lookup_record_cuda_error(cudaErrorInvalidDevice, "device index");
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
         const cudaError_t e =
             cudaFuncSetAttribute(read_floor_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kBulkSmem));
         if (e != cudaSuccess) return lookup_record_cuda_error(e, "cudaFuncSetAttribute");
-        attr_set.store(true, std::memory_order_release);
+        attr_set[dev].store(true, std::memory_order_release);
     }
     BulkParams prm;
     prm.p = static_cast<const int4 *>(data);
