@@ -947,6 +947,47 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
     torch.cuda.synchronize(dev)
     room_ok = room_ok and bool((status == 0).all().item())
     committed_mean = float(ncommit.float().mean().item())  # the last step's, per request
+
+    # prompt-lookup decoding without a draft model: the block is the previous
+    # step's lookup draft (P tokens), in two alternating buffers; one step is
+    # verification, the append and the next draft
+    drafts = [torch.full((B, P), -1, dtype=i32, device=dev) for _ in range(2)]
+    dlens = [torch.zeros(B, dtype=i32, device=dev) for _ in range(2)]
+    dpos, dml = torch.empty(B, dtype=i32, device=dev), torch.empty(B, dtype=i32, device=dev)
+    turn = [0]
+
+    def plain_one_call(h):
+        a, b2 = turn[0] % 2, (turn[0] + 1) % 2
+        turn[0] += 1
+        check(lib.lookup_index_verify_append_draft(drafts[a].data_ptr(), dlens[a].data_ptr(), target.data_ptr(), pp,
+                                                   None, None, up, B, P, tp, bp, lp, cp, w.min_m, w.max_m, mem,
+                                                   idx.slots, 64, P, accepted.data_ptr(), commit.data_ptr(),
+                                                   ncommit.data_ptr(), status.data_ptr(), drafts[b2].data_ptr(),
+                                                   dlens[b2].data_ptr(), dpos.data_ptr(), dml.data_ptr(), None, h))
+
+    def plain_two_calls(h):
+        a, b2 = turn[0] % 2, (turn[0] + 1) % 2
+        turn[0] += 1
+        check(lib.lookup_index_verify_append(drafts[a].data_ptr(), dlens[a].data_ptr(), target.data_ptr(), pp, None,
+                                             None, up, B, P, tp, bp, lp, cp, w.min_m, w.max_m, mem, idx.slots, 64,
+                                             accepted.data_ptr(), commit.data_ptr(), ncommit.data_ptr(),
+                                             status.data_ptr(), h))
+        check(lib.lookup_index_draft(tp, bp, lp, B, w.min_m, w.max_m, P, mem, idx.slots, 64, drafts[b2].data_ptr(),
+                                     dlens[b2].data_ptr(), dpos.data_ptr(), dml.data_ptr(), None, h))
+
+    restart()
+    plain_two_us = timed(plain_two_calls, 16, 4)          # 80 steps from the original histories
+    torch.cuda.synchronize(dev)
+    room_ok = room_ok and bool((status == 0).all().item())
+    restart()
+    for x in drafts:
+        x.fill_(-1)
+    for x in dlens:
+        x.zero_()
+    plain_one_us = timed(plain_one_call, 16, 4)
+    torch.cuda.synchronize(dev)
+    room_ok = room_ok and bool((status == 0).all().item())
+    plain_committed = float(ncommit.float().mean().item())
     total_tokens = int(st.shape[0])
     res = {
         "layout": f"slabs with {INDEX_SPARE} tokens of room per request",
@@ -964,6 +1005,13 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
         "loop_step_two_call_launches": launches["loop_two_call"],
         "loop_step_committed_per_request": round(committed_mean, 2),
         "loop_step_verify": "sampled rule, draws accepting the first f positions, f uniform in [0, P]",
+        "plain_lookup_step_us": round(plain_one_us, 3),
+        "plain_lookup_step_launches": launches["plain_one_call"],
+        "plain_lookup_step_two_call_us": round(plain_two_us, 3),
+        "plain_lookup_step_two_call_launches": launches["plain_two_calls"],
+        "plain_lookup_committed_per_request": round(plain_committed, 2),
+        "plain_lookup": "no draft model: the block is the previous step's lookup draft (P tokens); a step is "
+                        "verification, the append and the next draft (lookup_index_verify_append_draft)",
         "draft_launches": launches["draft_call"],
         "append8_launches": launches["append_call"],
         "parity_with_oracle": bool(parity),

@@ -150,6 +150,33 @@ int lookup_index_verify_append(const int32_t *block, const int32_t *block_len, c
                                int64_t slots, int32_t hash_bits, int32_t *out_accepted, int32_t *out_commit,
                                int32_t *out_ncommit, int32_t *out_status, struct CUstream_st *stream);
 
+/*
+ * lookup_index_verify_append followed by lookup_index_draft (K tokens) on the
+ * grown histories: the whole step after the target model in prompt-lookup
+ * decoding without a draft model, where the next block is the lookup draft.
+ * When every request gets a CTA in one wave, one launch: each request's CTA
+ * verifies its block, appends what it committed, and drafts from its grown
+ * history and the index.  The CTAs of other requests insert only their own
+ * requests' keys, which never move or empty a slot, and an overflow anywhere
+ * sends the query to the exact scan, so the draft is exact whatever the order.
+ * Otherwise the two calls, in order.
+ *
+ * block ... out_status       as for lookup_index_verify_append
+ * K, out_draft, out_draft_len, out_pos, out_mlen, out_fallback
+ *                            as for lookup_index_draft (K, out_draft, out_len,
+ *                            out_pos, out_mlen, out_fallback)
+ * Every output equals lookup_index_verify_append followed by lookup_index_draft.
+ * Errors: those of the two calls.
+ */
+int lookup_index_verify_append_draft(const int32_t *block, const int32_t *block_len, const int32_t *target,
+                                     const float *probs, const float *qprobs, const int32_t *point_mass,
+                                     const float *u, int32_t B, int32_t P, int32_t *tokens, const int64_t *base,
+                                     int32_t *len, const int32_t *cap, int32_t min_m, int32_t max_m, void *index,
+                                     int64_t slots, int32_t hash_bits, int32_t K, int32_t *out_accepted,
+                                     int32_t *out_commit, int32_t *out_ncommit, int32_t *out_status,
+                                     int32_t *out_draft, int32_t *out_draft_len, int32_t *out_pos, int32_t *out_mlen,
+                                     int32_t *out_fallback, struct CUstream_st *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,7 +30,8 @@ __all__ = [
     "set_wait_limit_ns", "lookup_fuse", "lookup_schedule", "lookup_plan", "lookup_draft_plan", "lookup_verify",
     "lookup_append", "lookup_policy",
     "NgramIndex", "index_slots_for", "index_bytes", "lookup_index_build", "lookup_index_append",
-    "lookup_index_draft", "lookup_index_draft_plan", "lookup_index_verify_append", "ContextCache",
+    "lookup_index_draft", "lookup_index_draft_plan", "lookup_index_verify_append",
+    "lookup_index_verify_append_draft", "ContextCache",
     "load_checked_library", "check_word",
     "launch_count",
     "MAX_M", "MAX_K", "LEN_FAILED", "CHECK_BITS",
@@ -199,6 +200,9 @@ def _declare_loop(lib: ctypes.CDLL) -> None:
     lib.lookup_index_verify_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, i32, i32, vp,
                                                i64, i32, vp, vp, vp, vp, vp]
     lib.lookup_index_verify_append.restype = ctypes.c_int
+    lib.lookup_index_verify_append_draft.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, i32, i32,
+                                                     vp, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.lookup_index_verify_append_draft.restype = ctypes.c_int
     lib.lookup_index_draft.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, i64, i32, vp, vp, vp, vp, vp, vp]
     lib.lookup_index_draft.restype = ctypes.c_int
     lib.lookup_index_draft_plan.argtypes = [vp, vp, vp, i32, i32, i32, vp, i64, i32, vp, vp, i32, i32, i32, i32, i32,
@@ -713,6 +717,37 @@ def lookup_index_verify_append(block, length, target, tokens, base, slab_len, ca
     return acc, commit, nc, status
 
 
+def lookup_index_verify_append_draft(block, length, target, tokens, base, slab_len, cap, min_m: int, max_m: int,
+                                     index, slots: int, K: int, probs=None, qprobs=None, point_mass=None, u=None,
+                                     hash_bits: int = 64, out=None, stream=None):
+    """lookup_index_verify_append, then lookup_index_draft (K tokens) on the grown
+    histories: one launch when the batch fits one wave of per-request CTAs.
+    Returns (accepted, commit [B, P+1], ncommit, status, draft [B, K], draft_len,
+    pos, mlen, fallback)."""
+    import torch
+    lib = load_library()
+    dev, B, (bp, lp, cp) = _slab_args(tokens, base, slab_len, cap)
+    P = block.shape[1]
+    f32 = torch.float32
+    args = (_dev(block, torch.int32, (B, P), dev, "block"), _dev(length, torch.int32, (B,), dev, "len"),
+            _dev(target, torch.int32, (B, P + 1), dev, "target"),
+            _dev(probs, f32, (B, P), dev, "probs", optional=True),
+            _dev(qprobs, f32, (B, P), dev, "qprobs", optional=True),
+            _dev(point_mass, torch.int32, (B, P), dev, "point_mass", optional=True),
+            _dev(u, f32, (B, P), dev, "u", optional=probs is None))
+    shapes = ((B,), (B, P + 1), (B,), (B,), (B, K), (B,), (B,), (B,), (B,))
+    names = ("accepted", "commit", "ncommit", "status", "draft", "draft_len", "pos", "mlen", "fallback")
+    if out is None:
+        out = tuple(torch.empty(sh, dtype=torch.int32, device=dev) for sh in shapes)
+    optr = tuple(_dev(t, torch.int32, sh, dev, nm) for t, sh, nm in zip(out, shapes, names))
+    with torch.cuda.device(dev):
+        rc = lib.lookup_index_verify_append_draft(*args, B, P, tokens.data_ptr(), bp, lp, cp, min_m, max_m,
+                                                  index.data_ptr(), int(slots), hash_bits, K, *optr[:4], *optr[4:],
+                                                  _stream_handle(stream))
+    _check(rc, lib)
+    return out
+
+
 def lookup_index_draft(tokens, base, length, min_m: int, max_m: int, K: int, index, slots: int,
                        hash_bits: int = 64, out=None, with_fallback: bool = False, stream=None):
     """The draft step from the index; exactly lookup_draft_ex's results for the slab
@@ -792,6 +827,14 @@ class NgramIndex:
         return lookup_index_verify_append(block, block_len, target, tokens, base, length, cap, self.min_m,
                                           self.max_m, self.memory, self.slots, hash_bits=self.hash_bits,
                                           stream=stream, **sampled)
+
+    def verify_append_draft(self, block, block_len, target, tokens, base, length, cap, K: int = 15, stream=None,
+                            **sampled):
+        """Verify the blocks, append what they commit, and draft K tokens from the
+        grown histories (lookup_index_verify_append_draft)."""
+        return lookup_index_verify_append_draft(block, block_len, target, tokens, base, length, cap, self.min_m,
+                                                self.max_m, self.memory, self.slots, K, hash_bits=self.hash_bits,
+                                                stream=stream, **sampled)
 
     def draft_plan(self, tokens, base, length, model_draft, committed, state, H: int = 7, T: int = 8, stream=None,
                    **rules):

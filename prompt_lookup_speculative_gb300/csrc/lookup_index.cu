@@ -277,61 +277,6 @@ __device__ inline int append_status(const AppendParams &p, bool ok, int r, int &
     return !ok ? 2 : (int64_t(L) + n > int64_t(p.cap[r]) ? 1 : 0);
 }
 
-// Batches that fit in one wave: one CTA per request at a time (grid-stride over
-// requests), the CTA's threads take the request's (new token j, length) tasks:
-// write token j at position L + j and insert the n-gram that ends one position
-// earlier, at L - 1 + j (the old last position first; the new last position is
-// indexed by the next append).  The tokens of an n-gram come from the old
-// history or straight from `commit`, so no insertion waits for a write.  Every
-// thread reads the request's old length first; after a barrier (no thread reads
-// it any more) one thread writes the new length and the status, so the append
-// is one launch.  VERIFY: warp 0 first verifies the request's block into v's
-// outputs (lookup_verify's rule, for that request), which p.commit and p.ncommit
-// point at; after a barrier the CTA appends what it committed.
-template <int kMaxLen, bool VERIFY>
-__global__ void __launch_bounds__(kAppendThreads) index_append_request_kernel(AppendParams p, lkd::VerifyIO v) {
-    wait_for_prerequisite_grid();
-    allow_dependent_launch();
-    const bool ok = header_ok(p.hd, p.min_m, p.max_m, p.hash_bits, p.slots);
-    const int64_t mask = (p.slots / kBucket) - 1;       // bucket mask
-    const int nl = p.max_m - p.min_m + 1;
-    const int64_t per_r = int64_t(p.W) * nl;
-    for (int r = blockIdx.x; r < p.B; r += gridDim.x) {
-        if (VERIFY) {
-            if (threadIdx.x < 32) lkd::verify_warp(v, r, threadIdx.x);
-            __syncthreads();                                 // the commit row and count are written
-        }
-        int L, n;
-        int64_t base;
-        const int st = append_status(p, ok, r, L, n, base);
-        const int32_t *crow = p.commit + int64_t(r) * p.W;
-        for (int64_t t = threadIdx.x; st == 0 && t < per_r; t += blockDim.x) {
-            const int j = int(t / nl), len_n = p.min_m + int(t % nl);   // new token j, length len_n
-            if (j >= n) break;                                   // tasks are ordered by j
-            if (len_n == p.min_m) p.tokens[base + L + j] = crow[j];  // one writer per new token
-            const int i = L - 1 + j;                             // the n-gram's end: one before the new token
-            if (i + 1 < len_n) continue;                         // no n-gram of that length ends here
-            // the len_n tokens ending at i, from the old history or from commit, loaded at once
-            int32_t v[kMaxLen];
-#pragma unroll
-            for (int k = 0; k < kMaxLen; ++k) {
-                const int src = i - k;
-                v[k] = k >= len_n ? 0 : (src >= L ? crow[src - L] : p.tokens[base + src]);
-            }
-            uint64_t h = seed_of(r);
-#pragma unroll
-            for (int k = 0; k < kMaxLen; ++k)
-                if (k < len_n) h = step_hash(h, v[k]);
-            insert(p.tab, mask, key_of(h, len_n, p.hash_bits), int(base + i), p.hd);
-        }
-        __syncthreads();                                     // every reader of len[r] is done
-        if (threadIdx.x == 0) {
-            if (st == 0) p.len[r] = L + n;
-            if (p.status) p.status[r] = st;
-        }
-    }
-}
-
 // Large batches (more requests than one wave of per-request CTAs): the writes
 // and insertions with one thread per (request, new token, length) task,
 // grid-stride over B * W * (max_m - min_m + 1) tasks, then the lengths in a
@@ -432,6 +377,96 @@ __device__ unsigned long long brute_force(const int32_t *t, int L, int tok, int 
     return best;
 }
 
+// One request's index query in the calling warp (all 32 lanes): the longest
+// suffix n-gram with a stored earlier end, checked against the history, else
+// the brute-force scan; the draft row, length, position, m and fallback flag,
+// or with PLAN the decode loop's scheduling and fusion on the draft tokens.
+template <bool PLAN>
+__device__ __forceinline__ void index_draft_request(const DraftParams &p, const lkd::PlanIO &pio, int r, int lane,
+                                                    bool hd_ok, bool overflow, int64_t mask, int nl) {
+    const int L = max(p.len[r], 0);
+    const int64_t base = p.base[r];
+    const int32_t *t = p.tokens + base;
+    // suffix token i (counted from the end) in lane i
+    const int tok = (lane < p.max_m && lane < L) ? t[L - 1 - lane] : 0;
+    int32_t *row = PLAN ? nullptr : p.out_draft + int64_t(r) * p.K;
+    unsigned long long best = 0ull;
+    bool fallback = overflow, drafted = false;
+    int32_t tok0 = -1, tok1 = -1;                    // PLAN: draft tokens lane and lane + 32
+    if (hd_ok && !overflow && L >= p.min_m + 1) {
+        // keys: lane j hashes the n-gram of length n = min_m + j
+        const int n = p.min_m + lane;
+        unsigned long long key = 0ull;
+        uint64_t h = seed_of(r);
+        const int top = min(p.max_m, L);
+        for (int k = 0; k < top; ++k) {
+            h = step_hash(h, __shfl_sync(0xffffffffu, tok, k));
+            if (k + 1 == n) key = key_of(h, n, p.hash_bits);
+        }
+        // 0 none, 1 candidate, 2 inconsistent (a position outside the request:
+        // the slot is shared with another key)
+        int state = 0, cand = -1;
+        if (lane < nl && n <= L - 1) {
+            int pos = -1;
+            if (find(p.tab, mask, key, pos)) {
+                const int64_t c = int64_t(pos) - base;       // relative end position
+                if (c < n - 1 || c > L - 2) state = 2;
+                else { state = 1; cand = int(c); }
+            }
+        }
+        const unsigned cmask = __ballot_sync(0xffffffffu, state == 1);
+        const unsigned incons = __ballot_sync(0xffffffffu, state == 2);
+        const int jbest = cmask ? 31 - __clz(cmask) : -1;
+        // a longer length whose slot is inconsistent may hide the true match
+        const unsigned above = jbest >= 0 ? (jbest < 31 ? ~((2u << jbest) - 1) : 0u) : 0xffffffffu;
+        if (incons & above) {
+            fallback = true;
+        } else if (jbest >= 0) {
+            // check the candidate and gather its draft in the same round of loads
+            const int m = p.min_m + jbest;
+            const int c = __shfl_sync(0xffffffffu, cand, jbest);
+            const int d = L - 1 - c;                         // L - pos - m
+            const bool bad = lane < m && t[c - lane] != tok;
+            const int32_t d0 = lane < p.K ? t[c + 1 + lane % d] : 0;
+            const int32_t d1 = lane + 32 < p.K ? t[c + 1 + (lane + 32) % d] : 0;
+            if (__ballot_sync(0xffffffffu, bad)) {
+                fallback = true;                             // the slot was shared with another key
+            } else {
+                best = (uint64_t(uint32_t(m)) << 32) | uint32_t(c - m + 1);
+                if (PLAN) {
+                    tok0 = lane < p.K ? d0 : -1;
+                    tok1 = lane + 32 < p.K ? d1 : -1;
+                } else {
+                    if (lane < p.K) row[lane] = d0;
+                    if (lane + 32 < p.K) row[lane + 32] = d1;
+                }
+                drafted = true;
+            }
+        }
+    }
+    if (fallback && hd_ok) best = brute_force(t, L, tok, p.min_m, p.max_m, lane);
+    const int m = int(best >> 32);
+    const int pos = int(uint32_t(best));
+    const bool found = hd_ok && m > 0;
+    if (!drafted) {                                         // the draft from the self-extended history
+        const int d = L - pos - m;
+        if (PLAN) {
+            tok0 = (found && lane < p.K) ? t[pos + m + (lane % d)] : -1;
+            tok1 = (found && lane + 32 < p.K) ? t[pos + m + ((lane + 32) % d)] : -1;
+        } else {
+            for (int j = lane; j < p.K; j += 32) row[j] = found ? t[pos + m + (j % d)] : -1;
+        }
+    }
+    if (PLAN) lkd::plan_warp(pio, r, lane, found ? m : 0, tok0, tok1);
+    if (lane == 0) {
+        // PLAN: out_len (the draft length) is optional and no position is written
+        if (!PLAN || p.out_len) p.out_len[r] = !hd_ok ? LOOKUP_DRAFT_LEN_FAILED : (found ? p.K : 0);
+        if (!PLAN) p.out_pos[r] = found ? pos : -1;
+        if (p.out_mlen) p.out_mlen[r] = found ? m : 0;
+        if (p.out_fallback) p.out_fallback[r] = fallback ? 1 : 0;
+    }
+}
+
 // PLAN: the draft tokens stay in the warp's registers and the decode loop's
 // scheduling and fusion follow (lkd::plan_warp); out_len then receives the length
 // lookup_index_draft would report, and no draft row is written.
@@ -445,90 +480,87 @@ __global__ void __launch_bounds__(kWarpThreads) index_draft_kernel(DraftParams p
     const bool overflow = hd_ok && p.hd->overflow != 0u;
     const int64_t mask = (p.slots / kBucket) - 1;       // bucket mask
     const int nl = p.max_m - p.min_m + 1;
-    for (int r = (blockIdx.x * kWarpThreads + threadIdx.x) >> 5; r < p.B; r += nwarps) {
-        const int L = max(p.len[r], 0);
-        const int64_t base = p.base[r];
-        const int32_t *t = p.tokens + base;
-        // suffix token i (counted from the end) in lane i
-        const int tok = (lane < p.max_m && lane < L) ? t[L - 1 - lane] : 0;
-        int32_t *row = PLAN ? nullptr : p.out_draft + int64_t(r) * p.K;
-        unsigned long long best = 0ull;
-        bool fallback = overflow, drafted = false;
-        int32_t tok0 = -1, tok1 = -1;                    // PLAN: draft tokens lane and lane + 32
-        if (hd_ok && !overflow && L >= p.min_m + 1) {
-            // keys: lane j hashes the n-gram of length n = min_m + j
-            const int n = p.min_m + lane;
-            unsigned long long key = 0ull;
+    for (int r = (blockIdx.x * kWarpThreads + threadIdx.x) >> 5; r < p.B; r += nwarps)
+        index_draft_request<PLAN>(p, pio, r, lane, hd_ok, overflow, mask, nl);
+}
+
+// ------------------------------------------------------- append, per request ----
+struct AppendExtra {
+    lkd::VerifyIO v;                                     // VERIFY
+    DraftParams d;                                       // DRAFT
+};
+
+// Batches that fit in one wave: one CTA per request at a time (grid-stride over
+// requests), the CTA's threads take the request's (new token j, length) tasks:
+// write token j at position L + j and insert the n-gram that ends one position
+// earlier, at L - 1 + j (the old last position first; the new last position is
+// indexed by the next append).  The tokens of an n-gram come from the old
+// history or straight from `commit`, so no insertion waits for a write.  Every
+// thread reads the request's old length first; after a barrier (no thread reads
+// it any more) one thread writes the new length and the status, so the append
+// is one launch.  VERIFY: warp 0 first verifies the request's block into x.v's
+// outputs (lookup_verify's rule, for that request), which p.commit and p.ncommit
+// point at; after a barrier the CTA appends what it committed.  DRAFT: after the
+// new length is written, warp 0 drafts the request from the grown history and
+// the index (lookup_index_draft's answer, into x.d's outputs).
+template <int kMaxLen, bool VERIFY, bool DRAFT>
+__global__ void __launch_bounds__(kAppendThreads) index_append_request_kernel(AppendParams p, AppendExtra x) {
+    wait_for_prerequisite_grid();
+    allow_dependent_launch();
+    const bool ok = header_ok(p.hd, p.min_m, p.max_m, p.hash_bits, p.slots);
+    const int64_t mask = (p.slots / kBucket) - 1;       // bucket mask
+    const int nl = p.max_m - p.min_m + 1;
+    const int64_t per_r = int64_t(p.W) * nl;
+    for (int r = blockIdx.x; r < p.B; r += gridDim.x) {
+        if (VERIFY) {
+            if (threadIdx.x < 32) lkd::verify_warp(x.v, r, threadIdx.x);
+            __syncthreads();                                 // the commit row and count are written
+        }
+        int L, n;
+        int64_t base;
+        const int st = append_status(p, ok, r, L, n, base);
+        const int32_t *crow = p.commit + int64_t(r) * p.W;
+        for (int64_t t = threadIdx.x; st == 0 && t < per_r; t += blockDim.x) {
+            const int j = int(t / nl), len_n = p.min_m + int(t % nl);   // new token j, length len_n
+            if (j >= n) break;                                   // tasks are ordered by j
+            if (len_n == p.min_m) p.tokens[base + L + j] = crow[j];  // one writer per new token
+            const int i = L - 1 + j;                             // the n-gram's end: one before the new token
+            if (i + 1 < len_n) continue;                         // no n-gram of that length ends here
+            // the len_n tokens ending at i, from the old history or from commit, loaded at once
+            int32_t v[kMaxLen];
+#pragma unroll
+            for (int k = 0; k < kMaxLen; ++k) {
+                const int src = i - k;
+                v[k] = k >= len_n ? 0 : (src >= L ? crow[src - L] : p.tokens[base + src]);
+            }
             uint64_t h = seed_of(r);
-            const int top = min(p.max_m, L);
-            for (int k = 0; k < top; ++k) {
-                h = step_hash(h, __shfl_sync(0xffffffffu, tok, k));
-                if (k + 1 == n) key = key_of(h, n, p.hash_bits);
-            }
-            // 0 none, 1 candidate, 2 inconsistent (a position outside the request:
-            // the slot is shared with another key)
-            int state = 0, cand = -1;
-            if (lane < nl && n <= L - 1) {
-                int pos = -1;
-                if (find(p.tab, mask, key, pos)) {
-                    const int64_t c = int64_t(pos) - base;       // relative end position
-                    if (c < n - 1 || c > L - 2) state = 2;
-                    else { state = 1; cand = int(c); }
-                }
-            }
-            const unsigned cmask = __ballot_sync(0xffffffffu, state == 1);
-            const unsigned incons = __ballot_sync(0xffffffffu, state == 2);
-            const int jbest = cmask ? 31 - __clz(cmask) : -1;
-            // a longer length whose slot is inconsistent may hide the true match
-            const unsigned above = jbest >= 0 ? (jbest < 31 ? ~((2u << jbest) - 1) : 0u) : 0xffffffffu;
-            if (incons & above) {
-                fallback = true;
-            } else if (jbest >= 0) {
-                // check the candidate and gather its draft in the same round of loads
-                const int m = p.min_m + jbest;
-                const int c = __shfl_sync(0xffffffffu, cand, jbest);
-                const int d = L - 1 - c;                         // L - pos - m
-                const bool bad = lane < m && t[c - lane] != tok;
-                const int32_t d0 = lane < p.K ? t[c + 1 + lane % d] : 0;
-                const int32_t d1 = lane + 32 < p.K ? t[c + 1 + (lane + 32) % d] : 0;
-                if (__ballot_sync(0xffffffffu, bad)) {
-                    fallback = true;                             // the slot was shared with another key
-                } else {
-                    best = (uint64_t(uint32_t(m)) << 32) | uint32_t(c - m + 1);
-                    if (PLAN) {
-                        tok0 = lane < p.K ? d0 : -1;
-                        tok1 = lane + 32 < p.K ? d1 : -1;
-                    } else {
-                        if (lane < p.K) row[lane] = d0;
-                        if (lane + 32 < p.K) row[lane + 32] = d1;
-                    }
-                    drafted = true;
-                }
-            }
+#pragma unroll
+            for (int k = 0; k < kMaxLen; ++k)
+                if (k < len_n) h = step_hash(h, v[k]);
+            insert(p.tab, mask, key_of(h, len_n, p.hash_bits), int(base + i), p.hd);
         }
-        if (fallback && hd_ok) best = brute_force(t, L, tok, p.min_m, p.max_m, lane);
-        const int m = int(best >> 32);
-        const int pos = int(uint32_t(best));
-        const bool found = hd_ok && m > 0;
-        if (!drafted) {                                         // the draft from the self-extended history
-            const int d = L - pos - m;
-            if (PLAN) {
-                tok0 = (found && lane < p.K) ? t[pos + m + (lane % d)] : -1;
-                tok1 = (found && lane + 32 < p.K) ? t[pos + m + ((lane + 32) % d)] : -1;
-            } else {
-                for (int j = lane; j < p.K; j += 32) row[j] = found ? t[pos + m + (j % d)] : -1;
-            }
+        __syncthreads();                                     // every reader of len[r] is done
+        if (threadIdx.x == 0) {
+            if (st == 0) p.len[r] = L + n;
+            if (p.status) p.status[r] = st;
         }
-        if (PLAN) lkd::plan_warp(pio, r, lane, found ? m : 0, tok0, tok1);
-        if (lane == 0) {
-            // PLAN: out_len (the draft length) is optional and no position is written
-            if (!PLAN || p.out_len) p.out_len[r] = !hd_ok ? LOOKUP_DRAFT_LEN_FAILED : (found ? p.K : 0);
-            if (!PLAN) p.out_pos[r] = found ? pos : -1;
-            if (p.out_mlen) p.out_mlen[r] = found ? m : 0;
-            if (p.out_fallback) p.out_fallback[r] = fallback ? 1 : 0;
+        if (DRAFT) {
+            // The new tokens, the request's insertions and its length are written;
+            // the table is read through L2, where the insertions' atomics land.
+            // Other CTAs insert only other requests' keys, which never move or
+            // empty a slot, and an overflow anywhere sends the query to the exact
+            // scan.
+            __syncthreads();
+            if (threadIdx.x < 32) {
+                const bool overflow = ok && __ldcg(&p.hd->overflow) != 0u;
+                index_draft_request<false>(x.d, lkd::PlanIO{}, r, threadIdx.x, ok, overflow, mask, nl);
+            }
+            __syncthreads();                                 // before the next request reuses the CTA
         }
     }
 }
+
+
 
 // ------------------------------------------------------------------- host ----
 bool pow2(int64_t x) { return x >= 16 && (x & (x - 1)) == 0; }
@@ -642,9 +674,9 @@ int lookup_index_append(int32_t *tokens, const int64_t *base, int32_t *len, cons
     unsigned block = 0;
     // the token window in registers: 16 entries when max_m allows, else 32
     if (one_wave_append(B, W, min_m, max_m, sms, block))
-        return lkd::launch_pdl2(max_m <= 16 ? index_append_request_kernel<16, false>
-                                            : index_append_request_kernel<LOOKUP_DRAFT_MAX_M, false>,
-                                unsigned(B), block, stream, p, lkd::VerifyIO{});
+        return lkd::launch_pdl2(max_m <= 16 ? index_append_request_kernel<16, false, false>
+                                            : index_append_request_kernel<LOOKUP_DRAFT_MAX_M, false, false>,
+                                unsigned(B), block, stream, p, AppendExtra{});
     const int64_t per_r = int64_t(W) * (max_m - min_m + 1);
     const int64_t tasks = int64_t(B) * per_r;
     const int64_t want = (tasks + kAppendThreads - 1) / kAppendThreads;
@@ -699,11 +731,84 @@ int lookup_index_verify_append(const int32_t *block, const int32_t *block_len, c
     p.min_m = min_m;
     p.max_m = max_m;
     p.hash_bits = hash_bits;
-    const lkd::VerifyIO v{block, block_len, target, probs, qprobs, point_mass, u, out_accepted, out_commit,
-                          out_ncommit, P};
-    return lkd::launch_pdl2(max_m <= 16 ? index_append_request_kernel<16, true>
-                                        : index_append_request_kernel<LOOKUP_DRAFT_MAX_M, true>,
-                            unsigned(B), threads, stream, p, v);
+    AppendExtra x{};
+    x.v = lkd::VerifyIO{block, block_len, target, probs, qprobs, point_mass, u, out_accepted, out_commit,
+                        out_ncommit, P};
+    return lkd::launch_pdl2(max_m <= 16 ? index_append_request_kernel<16, true, false>
+                                        : index_append_request_kernel<LOOKUP_DRAFT_MAX_M, true, false>,
+                            unsigned(B), threads, stream, p, x);
+}
+
+int lookup_index_verify_append_draft(const int32_t *block, const int32_t *block_len, const int32_t *target,
+                                     const float *probs, const float *qprobs, const int32_t *point_mass,
+                                     const float *u, int32_t B, int32_t P, int32_t *tokens, const int64_t *base,
+                                     int32_t *len, const int32_t *cap, int32_t min_m, int32_t max_m, void *index,
+                                     int64_t slots, int32_t hash_bits, int32_t K, int32_t *out_accepted,
+                                     int32_t *out_commit, int32_t *out_ncommit, int32_t *out_status,
+                                     int32_t *out_draft, int32_t *out_draft_len, int32_t *out_pos, int32_t *out_mlen,
+                                     int32_t *out_fallback, struct CUstream_st *stream) {
+    lkd::TraceRange trace_("lookup_index_verify_append_draft");
+    if (B < 0 || P < 0 || P > lkd::kMaxBlock || K < 0 || K > LOOKUP_DRAFT_MAX_K ||
+        !params_ok(min_m, max_m, hash_bits, slots))
+        return LOOKUP_DRAFT_EINVAL;
+    if (B == 0) return LOOKUP_DRAFT_OK;
+    if ((P > 0 && !block) || !block_len || !target || (probs && !u) || !out_accepted || !out_commit || !out_ncommit)
+        return LOOKUP_DRAFT_EINVAL;
+    if (!tokens || !base || !len || !cap || !index || !aligned16(index) || (K > 0 && !out_draft) ||
+        !out_draft_len || !out_pos)
+        return LOOKUP_DRAFT_EINVAL;
+    int sms = 0;
+    int rc = sm_count(&sms);
+    if (rc != LOOKUP_DRAFT_OK) return rc;
+    const int32_t W = P + 1;
+    unsigned threads = 0;
+    if (!one_wave_append(B, W, min_m, max_m, sms, threads)) {
+        // several waves: verification and the append, then the draft, as calls
+        rc = lookup_index_verify_append(block, block_len, target, probs, qprobs, point_mass, u, B, P, tokens, base,
+                                        len, cap, min_m, max_m, index, slots, hash_bits, out_accepted, out_commit,
+                                        out_ncommit, out_status, stream);
+        if (rc != LOOKUP_DRAFT_OK) return rc;
+        return lookup_index_draft(tokens, base, len, B, min_m, max_m, K, index, slots, hash_bits, out_draft,
+                                  out_draft_len, out_pos, out_mlen, out_fallback, stream);
+    }
+    AppendParams p{};
+    p.tokens = tokens;
+    p.base = base;
+    p.len = len;
+    p.cap = cap;
+    p.commit = out_commit;
+    p.ncommit = out_ncommit;
+    p.hd = static_cast<Header *>(index);
+    p.tab = reinterpret_cast<Slot *>(static_cast<char *>(index) + sizeof(Header));
+    p.status = out_status;
+    p.slots = slots;
+    p.B = B;
+    p.W = W;
+    p.min_m = min_m;
+    p.max_m = max_m;
+    p.hash_bits = hash_bits;
+    AppendExtra x{};
+    x.v = lkd::VerifyIO{block, block_len, target, probs, qprobs, point_mass, u, out_accepted, out_commit,
+                        out_ncommit, P};
+    x.d.tokens = tokens;
+    x.d.base = base;
+    x.d.len = len;
+    x.d.hd = p.hd;
+    x.d.tab = p.tab;
+    x.d.out_draft = out_draft;
+    x.d.out_len = out_draft_len;
+    x.d.out_pos = out_pos;
+    x.d.out_mlen = out_mlen;
+    x.d.out_fallback = out_fallback;
+    x.d.slots = slots;
+    x.d.B = B;
+    x.d.min_m = min_m;
+    x.d.max_m = max_m;
+    x.d.K = K;
+    x.d.hash_bits = hash_bits;
+    return lkd::launch_pdl2(max_m <= 16 ? index_append_request_kernel<16, true, true>
+                                        : index_append_request_kernel<LOOKUP_DRAFT_MAX_M, true, true>,
+                            unsigned(B), threads, stream, p, x);
 }
 
 int lookup_index_draft(const int32_t *tokens, const int64_t *base, const int32_t *len, int32_t B, int32_t min_m,

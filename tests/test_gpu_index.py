@@ -422,3 +422,66 @@ def test_index_verify_append_with_empty_blocks():
     got_t, got_o = gen.csr_of_slabs(host(t), base, host(n))
     np.testing.assert_array_equal(got_t, cur_t)
     check_draft(idx.draft(t, b, n, w.K), oracle.lookup_draft(cur_t, cur_o, w.min_m, w.max_m, w.K, threads=16))
+
+
+# ------------------------------------------- verify, append, then draft ----
+@pytest.mark.parametrize("mode", ["greedy", "sampled"])
+@pytest.mark.parametrize("name,hash_bits", [("tiny", 64), ("recitation25k", 64), ("recitation25k", 3), ("chats", 64)])
+def test_index_verify_append_draft_is_the_composition(name, hash_bits, mode):
+    """One launch on one-wave batches (a CTA per request verifies, appends and
+    drafts), the calls on chats; with 3-bit keys most requests draft through the
+    exact scan.  Against the oracle's verify, append and draft."""
+    w = gen.make_workload(name)
+    P = 15
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, 3 * (P + 1), seed=w.seed)
+    idx, t, b, n = built(st, base, length, w.min_m, w.max_m, hash_bits=hash_bits)
+    (blk, ln, tg), smp = _verify_inputs(w.B, P, w.seed + 1, mode)
+    acc_o, com_o, nc_o = oracle.verify(blk, ln, tg, **smp)
+    cur_t, cur_o = oracle.append(w.tokens, w.offsets, com_o, nc_o)
+    want = oracle.lookup_draft(cur_t, cur_o, w.min_m, w.max_m, w.K, threads=16)
+    got = idx.verify_append_draft(dev(blk), dev(ln), dev(tg), t, b, n, dev(cap), w.K,
+                                  **{k: dev(v) for k, v in smp.items()})
+    acc, com, nc, status, d, dl, pos, m, fb = got
+    for nm, g, e in (("accepted", acc, acc_o), ("commit", com, com_o), ("ncommit", nc, nc_o)):
+        np.testing.assert_array_equal(host(g), e, err_msg=nm)
+    assert (host(status) == 0).all()
+    got_t, got_o = gen.csr_of_slabs(host(t), base, host(n))
+    np.testing.assert_array_equal(got_t, cur_t)
+    check_draft((d, dl, pos, m), want)
+    if hash_bits == 64:
+        assert host(fb).sum() == 0
+
+
+@pytest.mark.parametrize("name", ["recitation25k", "periodic", "tiny"])
+def test_index_plain_lookup_decode_loop_in_one_launch(name):
+    """Prompt-lookup decoding without a draft model: the block is the previous
+    step's lookup draft (K = P proposals, or none without a match), the target
+    agrees with it on a random prefix, and each step is one call of
+    lookup_index_verify_append_draft.  Five steps against the oracle."""
+    w = gen.make_workload(name)
+    P = 15
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, 6 * (P + 1), seed=w.seed)
+    idx, t, b, n = built(st, base, length, w.min_m, w.max_m)
+    capd = dev(cap)
+    cur_t, cur_o = w.tokens, w.offsets
+    want = oracle.lookup_draft(cur_t, cur_o, w.min_m, w.max_m, P, threads=16)
+    blk_o, len_o = want[0], want[1]
+    blk_g, len_g = dev(blk_o), dev(len_o)
+    for step in range(5):
+        rng = gen.rng_for(step, 47)
+        target = rng.integers(0, 50, size=(w.B, P + 1)).astype(np.int32)
+        f = rng.integers(0, P + 1, size=w.B)
+        for r in range(w.B):
+            target[r, :f[r]] = blk_o[r, :f[r]]
+        acc_o, com_o, nc_o = oracle.verify(blk_o, len_o, target)
+        cur_t, cur_o = oracle.append(cur_t, cur_o, com_o, nc_o)
+        want = oracle.lookup_draft(cur_t, cur_o, w.min_m, w.max_m, P, threads=16)
+        acc, com, nc, status, d, dl, pos, m, fb = idx.verify_append_draft(blk_g, len_g, dev(target), t, b, n, capd, P)
+        np.testing.assert_array_equal(host(nc), nc_o, err_msg=f"ncommit, step {step}")
+        np.testing.assert_array_equal(host(com), com_o, err_msg=f"commit, step {step}")
+        assert (host(status) == 0).all()
+        check_draft((d, dl, pos, m), want)
+        blk_o, len_o = want[0], want[1]
+        blk_g, len_g = d, dl
+    got_t, got_o = gen.csr_of_slabs(host(t), base, host(n))
+    np.testing.assert_array_equal(got_t, cur_t)

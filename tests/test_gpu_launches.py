@@ -130,3 +130,17 @@ def test_index_verify_append_launches(batches, name, want):
     P = 15
     blk, ln, tg, *_ = gen.loop_verify_inputs(w.B, P, 3)
     assert launches(lambda: idx.verify_append(dev(blk), dev(ln), dev(tg), t, b, n, c)) == want
+
+
+@pytest.mark.parametrize("name,want", [("recitation25k", 1), ("chats", 4)])
+def test_index_verify_append_draft_launches(batches, name, want):
+    """One launch on a one-wave batch; verify, the dense append and its length
+    pass, then the draft on chats."""
+    w, _, _ = batches[name]
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, 64, seed=w.seed)
+    t, b, n, c = dev(st), dev(base), dev(length), dev(cap)
+    idx = pkg.NgramIndex(st.shape[0], w.min_m, w.max_m)
+    idx.build(t, b, n)
+    P = 15
+    blk, ln, tg, *_ = gen.loop_verify_inputs(w.B, P, 4)
+    assert launches(lambda: idx.verify_append_draft(dev(blk), dev(ln), dev(tg), t, b, n, c, 15)) == want

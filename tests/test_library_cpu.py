@@ -420,3 +420,30 @@ def test_index_verify_append_rejects_bad_parameters(lib):
     assert call(a15=F + 8) == -1            # misaligned index
     assert call(a7=-1) == -1                # B < 0
     assert call(a7=0, a0=None, a1=None, a2=None, a9=None, a15=None) == 0   # B == 0: nothing to do
+
+
+def test_index_verify_append_draft_rejects_bad_parameters(lib):
+    F = FAKE
+    # block, block_len, target, probs, qprobs, point_mass, u, B, P, tokens, base, len, cap, min_m, max_m, index,
+    # slots, hash_bits, K, out_accepted, out_commit, out_ncommit, out_status, out_draft, out_draft_len, out_pos,
+    # out_mlen, out_fallback, stream
+    ok = [F, F, F, None, None, None, None, 4, 15, F, F, F, F, 4, 12, F, 1024, 64, 15, F, F, F, None, F, F, F, None,
+          None, None]
+    assert len(ok) == 29
+
+    def call(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return lib.lookup_index_verify_append_draft(*a)
+
+    assert call(a18=-1) == -1               # K < 0
+    assert call(a18=65) == -1               # K above LOOKUP_DRAFT_MAX_K
+    assert call(a23=None) == -1             # no draft rows with K > 0
+    assert call(a24=None) == -1             # no draft lengths
+    assert call(a25=None) == -1             # no positions
+    assert call(a8=-1) == -1                # P < 0
+    assert call(a3=F) == -1                 # probs without u
+    assert call(a16=1000) == -1             # slots not a power of two
+    assert call(a15=F + 8) == -1            # misaligned index
+    assert call(a7=0, a0=None, a9=None) == 0   # B == 0: nothing to do
