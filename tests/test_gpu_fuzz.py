@@ -14,7 +14,8 @@ length, the position and m.  The two-launch loop path (draft, then scheduling
 and fusion) is swept the same way against the oracle's draft, schedule and fuse,
 and the incremental index and the context cache over random 3-step decode loops
 (draft, commit, append in place), the index also in its two-launch form (draft
-with scheduling and fusion, then verification with the append).
+with scheduling and fusion, then verification with the append) and in plain
+prompt-lookup decoding (verification, append and the next draft in one launch).
 """
 from __future__ import annotations
 
@@ -284,3 +285,64 @@ def test_index_two_launch_loop_matches_oracle_on_random_decode_loops(case):
         np.testing.assert_array_equal(got_o, cur_o, err_msg=at)
         np.testing.assert_array_equal(got_t, cur_t, err_msg=at)
         committed = nc_o
+
+
+@pytest.mark.parametrize("case", range(10))
+def test_index_plain_lookup_loop_matches_oracle_on_random_batches(case):
+    """Prompt-lookup decoding without a draft model through
+    lookup_index_verify_append_draft: the block is the previous step's lookup
+    draft, verified greedily (against a target that agrees on a random prefix)
+    or by the sampled rule, then appended and drafted again, three steps, against
+    the oracle's verify, append and draft.  Random batches, m ranges, K, key
+    widths (3 bits: the exact scan), and one batch of more requests than a wave
+    of append CTAs holds (the calls in order)."""
+    rng = np.random.default_rng(60260 + case)
+    if case == 9:                                        # more than one wave: many short requests
+        lengths = rng.integers(0, 300, size=5000)
+        tokens = rng.integers(0, 5, size=int(lengths.sum())).astype(np.int32)
+        offsets = gen.offsets_from_lengths(lengths).astype(np.int64)
+    else:
+        tokens, offsets = small_random_batch(rng)
+    B = offsets.size - 1
+    min_m = int(rng.integers(1, 7))
+    max_m = int(rng.integers(min_m, 33))
+    K = int(rng.integers(1, 33))
+    hash_bits = int(rng.choice([64, 64, 3]))
+    sampled = bool(rng.random() < 0.5)
+    st, base, length, cap = gen.slabs_from_batch(tokens, offsets, 4 * (K + 1), seed=case)
+    t, b, n = (torch.from_numpy(np.ascontiguousarray(a)).to(DEV) for a in (st, base, length))
+    capd = torch.from_numpy(cap).to(DEV)
+    idx = pkg.NgramIndex(st.shape[0], min_m, max_m, hash_bits=hash_bits)
+    idx.build(t, b, n)
+    cur_t, cur_o = tokens, offsets
+    want = oracle.lookup_draft(cur_t, cur_o, min_m, max_m, K, threads=16)
+    blk_o, len_o = want[0], want[1]
+    blk_g, len_g = torch.from_numpy(blk_o).to(DEV), torch.from_numpy(len_o).to(DEV)
+    label = f"case {case}: B={B} m=[{min_m},{max_m}] K={K} bits={hash_bits} sampled={sampled}"
+    for step in range(3):
+        target = rng.integers(-3, 50, size=(B, K + 1)).astype(np.int32)
+        f = rng.integers(0, K + 1, size=B)
+        for r in range(B):
+            target[r, :f[r]] = blk_o[r, :f[r]]
+        smp = {}
+        if sampled:
+            smp = dict(probs=rng.random((B, K), dtype=np.float32),
+                       qprobs=(1.0 - rng.random((B, K), dtype=np.float32)).astype(np.float32),
+                       u=rng.random((B, K), dtype=np.float32))
+        acc_o, com_o, nc_o = oracle.verify(blk_o, len_o, target, **smp)
+        cur_t, cur_o = oracle.append(cur_t, cur_o, com_o, nc_o)
+        want = oracle.lookup_draft(cur_t, cur_o, min_m, max_m, K, threads=16)
+        got = idx.verify_append_draft(blk_g, len_g, torch.from_numpy(target).to(DEV), t, b, n, capd, K,
+                                      **{k: torch.from_numpy(v).to(DEV) for k, v in smp.items()})
+        acc, com, nc, status, d, dl, pos, m, fb = got
+        at = f"{label} step {step}"
+        for name, g, w in (("accepted", acc, acc_o), ("commit", com, com_o), ("ncommit", nc, nc_o),
+                           ("draft", d, want[0]), ("draft len", dl, want[1]), ("pos", pos, want[2]),
+                           ("mlen", m, want[3])):
+            np.testing.assert_array_equal(g.cpu().numpy(), w, err_msg=f"{at}: {name}")
+        assert (status.cpu().numpy() == 0).all(), at
+        blk_o, len_o = want[0], want[1]
+        blk_g, len_g = d, dl
+    got_t, got_o = gen.csr_of_slabs(t.cpu().numpy(), base, n.cpu().numpy())
+    np.testing.assert_array_equal(got_o, cur_o, err_msg=label)
+    np.testing.assert_array_equal(got_t, cur_t, err_msg=label)
