@@ -166,6 +166,9 @@ int lookup_index_verify_append(const int32_t *block, const int32_t *block_len, c
  *                            as for lookup_index_draft (K, out_draft, out_len,
  *                            out_pos, out_mlen, out_fallback)
  * Every output equals lookup_index_verify_append followed by lookup_index_draft.
+ * With K == P, out_draft may be the block array and out_draft_len the block
+ * lengths (the next step's block, written in place): each request's block is
+ * read before its draft is written.
  * Errors: those of the two calls.
  */
 int lookup_index_verify_append_draft(const int32_t *block, const int32_t *block_len, const int32_t *target,

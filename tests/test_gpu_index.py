@@ -452,12 +452,14 @@ def test_index_verify_append_draft_is_the_composition(name, hash_bits, mode):
         assert host(fb).sum() == 0
 
 
+@pytest.mark.parametrize("in_place", [False, True])
 @pytest.mark.parametrize("name", ["recitation25k", "periodic", "tiny"])
-def test_index_plain_lookup_decode_loop_in_one_launch(name):
+def test_index_plain_lookup_decode_loop_in_one_launch(name, in_place):
     """Prompt-lookup decoding without a draft model: the block is the previous
     step's lookup draft (K = P proposals, or none without a match), the target
     agrees with it on a random prefix, and each step is one call of
-    lookup_index_verify_append_draft.  Five steps against the oracle."""
+    lookup_index_verify_append_draft; in_place: the draft overwrites the block
+    and its lengths.  Five steps against the oracle."""
     w = gen.make_workload(name)
     P = 15
     st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, 6 * (P + 1), seed=w.seed)
@@ -476,7 +478,19 @@ def test_index_plain_lookup_decode_loop_in_one_launch(name):
         acc_o, com_o, nc_o = oracle.verify(blk_o, len_o, target)
         cur_t, cur_o = oracle.append(cur_t, cur_o, com_o, nc_o)
         want = oracle.lookup_draft(cur_t, cur_o, w.min_m, w.max_m, P, threads=16)
-        acc, com, nc, status, d, dl, pos, m, fb = idx.verify_append_draft(blk_g, len_g, dev(target), t, b, n, capd, P)
+        if in_place:
+            outs = (torch.empty(w.B, dtype=torch.int32, device="cuda"),
+                    torch.empty((w.B, P + 1), dtype=torch.int32, device="cuda"),
+                    torch.empty(w.B, dtype=torch.int32, device="cuda"),
+                    torch.empty(w.B, dtype=torch.int32, device="cuda"), blk_g, len_g,
+                    torch.empty(w.B, dtype=torch.int32, device="cuda"),
+                    torch.empty(w.B, dtype=torch.int32, device="cuda"),
+                    torch.empty(w.B, dtype=torch.int32, device="cuda"))
+            got = pkg.lookup_index_verify_append_draft(blk_g, len_g, dev(target), t, b, n, capd, w.min_m, w.max_m,
+                                                       idx.memory, idx.slots, P, out=outs)
+        else:
+            got = idx.verify_append_draft(blk_g, len_g, dev(target), t, b, n, capd, P)
+        acc, com, nc, status, d, dl, pos, m, fb = got
         np.testing.assert_array_equal(host(nc), nc_o, err_msg=f"ncommit, step {step}")
         np.testing.assert_array_equal(host(com), com_o, err_msg=f"commit, step {step}")
         assert (host(status) == 0).all()
