@@ -988,6 +988,13 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
     torch.cuda.synchronize(dev)
     room_ok = room_ok and bool((status == 0).all().item())
     plain_committed = float(ncommit.float().mean().item())
+    # the replays' last step wrote buffer 0 (16 steps per graph): the draft of the
+    # grown histories, which must be the oracle's
+    import oracle
+    grown_t, grown_o = gen.csr_of_slabs(tokens.cpu().numpy(), base_h, length.cpu().numpy())
+    want_grown = oracle.lookup_draft(grown_t, grown_o, w.min_m, w.max_m, P, threads=os.cpu_count() or 1)
+    plain_parity = (np.array_equal(drafts[0].cpu().numpy(), want_grown[0])
+                    and np.array_equal(dlens[0].cpu().numpy(), want_grown[1]))
     total_tokens = int(st.shape[0])
     res = {
         "layout": f"slabs with {INDEX_SPARE} tokens of room per request",
@@ -1010,6 +1017,7 @@ def measure_index(lib, pkg, w, dev, stream, want) -> dict:
         "plain_lookup_step_two_call_us": round(plain_two_us, 3),
         "plain_lookup_step_two_call_launches": launches["plain_two_calls"],
         "plain_lookup_committed_per_request": round(plain_committed, 2),
+        "plain_lookup_parity_with_oracle": bool(plain_parity),
         "plain_lookup": "no draft model: the block is the previous step's lookup draft (P tokens); a step is "
                         "verification, the append and the next draft (lookup_index_verify_append_draft)",
         "draft_launches": launches["draft_call"],
