@@ -499,3 +499,39 @@ def test_index_plain_lookup_decode_loop_in_one_launch(name, in_place):
         blk_g, len_g = d, dl
     got_t, got_o = gen.csr_of_slabs(host(t), base, host(n))
     np.testing.assert_array_equal(got_t, cur_t)
+
+
+def test_index_verify_append_draft_error_rows_and_full_slabs():
+    """As for verify-and-append: an out-of-range block length gives the error row
+    and appends nothing, a full slab gets status 1 and keeps its history; every
+    request is then drafted from its history as it stands."""
+    w = gen.make_workload("recitation25k")
+    P = 15
+    st, base, length, cap = gen.slabs_from_batch(w.tokens, w.offsets, P + 1, seed=w.seed)
+    cap = cap.copy()
+    (blk, ln, tg), _ = _verify_inputs(w.B, P, 9, "greedy")
+    bad = np.zeros(w.B, bool)
+    bad[[2, 30]] = True
+    ln_bad = ln.copy()
+    ln_bad[2], ln_bad[30] = -3, P + 1
+    full = np.zeros(w.B, bool)
+    full[[7, 41]] = True
+    cap[full] = length[full]
+    idx, t, b, n = built(st, base, length, w.min_m, w.max_m)
+    ok = ~bad
+    acc_o, com_o, nc_o = oracle.verify(blk[ok], ln[ok], tg[ok])
+    got = idx.verify_append_draft(dev(blk), dev(ln_bad), dev(tg), t, b, n, dev(cap), w.K)
+    acc, com, nc, status, d, dl, pos, m, fb = (host(x) for x in got)
+    np.testing.assert_array_equal(acc[ok], acc_o)
+    np.testing.assert_array_equal(nc[ok], nc_o)
+    assert (acc[bad] == -1).all() and (nc[bad] == 0).all()
+    np.testing.assert_array_equal(status, np.where(full & ok, 1, 0))
+    nc_eff = np.zeros(w.B, np.int32)
+    nc_eff[ok] = nc_o
+    nc_eff[full] = 0
+    com_eff = np.full((w.B, P + 1), -1, np.int32)
+    com_eff[ok] = com_o
+    cur_t, cur_o = oracle.append(w.tokens, w.offsets, com_eff, nc_eff)
+    want = oracle.lookup_draft(cur_t, cur_o, w.min_m, w.max_m, w.K, threads=16)
+    for nm, g, e in (("draft", d, want[0]), ("draft len", dl, want[1]), ("pos", pos, want[2]), ("mlen", m, want[3])):
+        np.testing.assert_array_equal(g, e, err_msg=nm)
