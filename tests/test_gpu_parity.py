@@ -372,6 +372,19 @@ def test_read_floor_streams_without_writing(shape):
     assert out.item() == 123
 
 
+@pytest.mark.parametrize("n16", [3, 193, (3 << 16) + 3, (41 << 16) + 1])
+def test_bulk_read_floor_odd_sizes(n16):
+    """The bulk read over sizes whose warp ranges and tiles end unevenly (48 bytes,
+    one tile and a quad, 3 MB + 48 bytes, 41 MB + 16 bytes): it completes and
+    leaves the output word alone."""
+    x = torch.zeros(4 * n16, dtype=torch.int32, device=DEV)
+    x[::7] = 1
+    out = torch.full((1,), 123, dtype=torch.int32, device=DEV)
+    pkg.read_floor(x, 0, 0, out=out)
+    torch.cuda.synchronize()
+    assert out.item() == 123
+
+
 def test_bulk_read_floor_wait_runs_out_cleanly():
     """With a 1 ns wait limit the bulk read's warps give up at their first tile,
     store -1, let their copies land (bounded by 1 s, not by the limit) and stop;
