@@ -23,6 +23,14 @@
 // candidate that does not check out (or a table that overflowed) sends the
 // request to a warp brute-force scan instead: the result never depends on the
 // hash.
+//
+// Decode loop: the append writes the committed tokens in place and inserts
+// their n-grams, one CTA per request when the batch fits one wave of them.  The
+// same kernel can first verify the request's block (lookup_index_verify_append)
+// and, after the new length is written, draft its next block from the grown
+// history (lookup_index_verify_append_draft); the query is the one device
+// function the draft kernels use, so every fused form returns what the separate
+// calls would.
 
 #include "lookup_index.h"
 #include "lookup_loop.h"
