@@ -82,19 +82,31 @@ struct PlanIO {
     int32_t H, T, replace_min, agree_min, agree_n, tail_min, slack, enter_steps, sticky;
 };
 
-__device__ inline void plan_warp(const PlanIO &pa, int r, int lane, int32_t m, int32_t tok0, int32_t tok1) {
+// A request's inputs to the rules, read by each lane: the model's proposals j =
+// lane and lane + 32, the commit count and the old state.
+struct PlanIn {
+    int32_t md0, md1, committed, lng, streak, hold;
+};
+
+__device__ inline PlanIn plan_load(const PlanIO &pa, int r, int lane) {
+    const int32_t *md = pa.model_draft + int64_t(r) * pa.H;
+    const int32_t *st = pa.state + 3 * int64_t(r);
+    const int j1 = lane + 32;
+    return PlanIn{lane < pa.H ? md[lane] : -1, j1 < pa.H ? md[j1] : -1, pa.committed[r], st[0], st[1], st[2]};
+}
+
+__device__ inline void plan_apply(const PlanIO &pa, int r, int lane, int32_t m, int32_t tok0, int32_t tok1,
+                                  const PlanIn &in) {
     const int W = pa.H + pa.T;
     const int j1 = lane + 32;
     // head rule: the model agrees with the draft's first agree_n tokens
-    const int32_t *md = pa.model_draft + int64_t(r) * pa.H;
-    const int32_t md0 = lane < pa.H ? md[lane] : -1, md1 = j1 < pa.H ? md[j1] : -1;
-    const bool ne = (lane < pa.agree_n && tok0 != md0) || (j1 < pa.agree_n && tok1 != md1);
+    const bool ne = (lane < pa.agree_n && tok0 != in.md0) || (j1 < pa.agree_n && tok1 != in.md1);
     const bool agree = __all_sync(0xffffffffu, !ne);
     const bool head = m >= pa.replace_min || (m >= pa.agree_min && agree);
-    // scheduling: every lane reads the old state, then lane 0 writes the new one
+    // scheduling: every lane holds the old state, then lane 0 writes the new one
     int32_t *st = pa.state + 3 * int64_t(r);
-    int32_t lng = st[0], streak = st[1], hold = st[2];
-    schedule_update(m, pa.committed[r], pa.H, pa.T, pa.tail_min, pa.slack, pa.enter_steps, pa.sticky, lng, streak,
+    int32_t lng = in.lng, streak = in.streak, hold = in.hold;
+    schedule_update(m, in.committed, pa.H, pa.T, pa.tail_min, pa.slack, pa.enter_steps, pa.sticky, lng, streak,
                     hold);
     __syncwarp();
     const bool tail = lng != 0 && m >= pa.tail_min;
@@ -108,15 +120,19 @@ __device__ inline void plan_warp(const PlanIO &pa, int r, int lane, int32_t m, i
     // fusion of the block's positions
     int32_t v, pm;
     if (lane < W) {
-        fuse_choice(lane, pa.H, head, tail, tok0, md0, v, pm);
+        fuse_choice(lane, pa.H, head, tail, tok0, in.md0, v, pm);
         pa.out_block[int64_t(r) * W + lane] = v;
         pa.out_pm[int64_t(r) * W + lane] = pm;
     }
     if (j1 < W) {
-        fuse_choice(j1, pa.H, head, tail, tok1, md1, v, pm);
+        fuse_choice(j1, pa.H, head, tail, tok1, in.md1, v, pm);
         pa.out_block[int64_t(r) * W + j1] = v;
         pa.out_pm[int64_t(r) * W + j1] = pm;
     }
+}
+
+__device__ inline void plan_warp(const PlanIO &pa, int r, int lane, int32_t m, int32_t tok0, int32_t tok1) {
+    plan_apply(pa, r, lane, m, tok0, tok1, plan_load(pa, r, lane));
 }
 
 // Verification of request r's proposal block by one warp (HyperQwen lookup-drafting

@@ -989,6 +989,13 @@ struct PlanArgs {
 };
 
 __global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_plan_kernel(FillParams prm, PlanArgs pa) {
+    // The rules' own inputs (the model's proposals, the commit count, the state)
+    // are not written by the scan, this kernel's only predecessor in the call, and
+    // everything before the scan had completed when it let this kernel launch: read
+    // them now, before the wait inside fold_request.
+    const int rq = blockIdx.x * kFillWarps + (threadIdx.x >> 5);
+    lkd::PlanIn in{};
+    if (rq < prm.B) in = lkd::plan_load(pa.io, rq, threadIdx.x & 31);
     fold_request(prm, [&](int r, int lane, int64_t o0, int64_t L, unsigned long long key) {
         const int64_t km = int64_t(key >> 32), kp = int64_t(uint32_t(key));
         const bool failed = key != 0ull && (key == kKeyFailed || km < 1 || kp + km > L - 1);
@@ -1007,7 +1014,7 @@ __global__ void __launch_bounds__(kFillWarps * 32, kFillMinBlocks) fill_plan_ker
         const int32_t tok1 = (found && j1 < W && LKD_OK(p + m + (j1 < d ? j1 : j1 % d) < L, LOOKUP_DRAFT_CHECK_TOKENS))
                                  ? __ldg(src + (j1 < d ? j1 : j1 % d))
                                  : -1;
-        lkd::plan_warp(pa.io, r, lane, m, tok0, tok1);
+        lkd::plan_apply(pa.io, r, lane, m, tok0, tok1, in);
         if (lane == 0) {
             if (pa.out_mlen) pa.out_mlen[r] = m;
             if (pa.out_draft_len) pa.out_draft_len[r] = found ? W : (failed ? LOOKUP_DRAFT_LEN_FAILED : 0);
